@@ -1,0 +1,273 @@
+/*
+ * fa_oracle.c -- plain fp64 CPU oracle for the attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline use it.  It shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * What it computes is the plain definition of masked softmax attention with a
+ * per-row log-sum-exp, one (query token, query head) row at a time:
+ *
+ *   s_j   = scale * <q_i, k_j>                     (all keys j of the sequence)
+ *   s_j   = cap * tanh(s_j / cap)                  (soft-cap score mod)
+ *   s_j   = s_j - slope * |i' - j|                 (ALiBi score mod)
+ *   A_i   = { j : causal, window, block mask and j < Sk allow (i, j) }
+ *   m     = max_{j in A_i} s_j
+ *   l     = sum_{j in A_i} exp(s_j - m)
+ *   out_i = sum_{j in A_i} exp(s_j - m) v_j / l
+ *   LSE_i = m + ln(l)
+ *
+ * with out_i = 0 and LSE_i = -inf when A_i is empty.  Sources:
+ *  - online softmax and LSE = M + log(L): RL-Kernel PR #237 "SM90 TMA +
+ *    mma.sync FlashAttention", first commit (attention-domain LSE) and the
+ *    summary (independent per-sequence masked-softmax + logsumexp reference);
+ *  - LSE stored on fully masked tiles: FlyDSL PR #844 "Add forward LSE output",
+ *    Changes list;
+ *  - packed varlen cu_seqlens tensors [total_tokens, H, D]: RL-Kernel PR #237,
+ *    first commit;
+ *  - paged KV through block_table, FP8 e4m3 KV with per-token scales, Q/K 192
+ *    and V/O 128: FlyDSL PR #1066 overview and PR description; fkl_python PR #7,
+ *    fp8 KV commit (scale = max|row|/448);
+ *  - bottom-right causal alignment: FlyDSL PR #1066 review (COMMENT, "What I
+ *    verified": bottom-right causal mask, cross_seqlen=True);
+ *  - ALiBi, SoftCap, SlidingWindow and 128x128 block masks: fkl_python PR #7,
+ *    flex attention commit.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ * i' = i + Sk - Sq; window W>0 keeps 0 <= i'-j < W when causal, |i'-j| < W
+ * otherwise; ALiBi bias -slope*|i'-j| for every head; soft-cap acts on the
+ * scaled score before ALiBi; block-mask index (b*Hq + h, i/128, j/128) with
+ * sequence-local i, j; GQA head hk = h / (Hq/Hkv); per-token scales are one
+ * fp32 per (page, slot, kv head).
+ *
+ * All arithmetic is double precision; bf16 and e4m3 inputs are widened exactly.
+ * Threads (pthreads) only split the independent rows between cores.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { KV_BF16 = 0, KV_E4M3 = 1, KV_F64 = 2 };
+enum { MOD_NONE = 0, MOD_ALIBI = 1, MOD_SOFTCAP = 2 };
+
+typedef struct {
+    const uint16_t *q;            /* bf16 bits [T_q][Hq][Dk] */
+    const void *k, *v;            /* packed [T_k][Hkv][D] or paged [N_pg][P_s][Hkv][D] */
+    int32_t kv_dtype;             /* KV_BF16 | KV_E4M3 | KV_F64 */
+    const int32_t *block_table;   /* [B][bt_stride] or NULL (packed K/V) */
+    int64_t bt_stride;
+    const int32_t *cu_q, *cu_k;   /* [B+1] */
+    int32_t num_seqs;
+    const float *k_scale, *v_scale; /* per token and kv head; NULL unless e4m3 */
+    int32_t hq, hkv, dk, dv, page_size;
+    double softmax_scale;
+    int32_t causal, window, mod_kind;
+    double alibi_slope, softcap;
+    const uint8_t *block_mask;    /* [B*Hq][n_qblk][n_kblk] or NULL */
+    int32_t n_qblk, n_kblk, blk_q, blk_k;
+    int64_t kv_lo, kv_hi;         /* restrict keys to [kv_lo, kv_hi) when kv_hi >= 0 */
+} fa_oracle_problem;
+
+/* bf16 -> double: the bf16 bits are the upper half of an IEEE binary32. */
+double fa_oracle_bf16_decode(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP FP8 E4M3 (the "OCP E4M3" of FlyDSL PR #1066): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN. */
+double fa_oracle_e4m3_decode(uint8_t x) {
+    int s = (x >> 7) & 1, e = (x >> 3) & 0xF, m = x & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp((double)m / 8.0, -6);          /* subnormal */
+    else mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Row j of the sequence's keys (or values) for kv head hk, widened to double. */
+static void fetch_row(const fa_oracle_problem *p, const void *base, const float *scale,
+                      int b, int64_t j, int hk, int d, double *dst) {
+    int64_t tok;       /* flat token index in the [*, Hkv] view of the pool */
+    if (p->block_table) {
+        int64_t page = p->block_table[(int64_t)b * p->bt_stride + j / p->page_size];
+        tok = page * p->page_size + j % p->page_size;
+    } else {
+        tok = (int64_t)p->cu_k[b] + j;
+    }
+    int64_t off = (tok * p->hkv + hk) * (int64_t)d;
+    double sc = 1.0;
+    if (p->kv_dtype == KV_E4M3) sc = (double)scale[tok * p->hkv + hk];
+    for (int x = 0; x < d; x++) {
+        double val;
+        if (p->kv_dtype == KV_BF16) val = fa_oracle_bf16_decode(((const uint16_t *)base)[off + x]);
+        else if (p->kv_dtype == KV_E4M3) val = fa_oracle_e4m3_decode(((const uint8_t *)base)[off + x]);
+        else val = ((const double *)base)[off + x];
+        dst[x] = val * sc;
+    }
+}
+
+/* Is key j visible from query row i of sequence b, head h? */
+static int allowed(const fa_oracle_problem *p, int b, int h, int64_t i, int64_t j,
+                   int64_t sq, int64_t sk) {
+    int64_t ip = i + sk - sq;                      /* bottom-right aligned query position */
+    if (j < 0 || j >= sk) return 0;
+    if (p->kv_hi >= 0 && (j < p->kv_lo || j >= p->kv_hi)) return 0;
+    if (p->causal && j > ip) return 0;
+    if (p->window > 0) {
+        if (p->causal) {
+            if (ip - j >= p->window) return 0;
+        } else {
+            int64_t dist = ip > j ? ip - j : j - ip;
+            if (dist >= p->window) return 0;
+        }
+    }
+    if (p->block_mask) {
+        int64_t qb = i / p->blk_q, kb = j / p->blk_k;
+        if (qb >= p->n_qblk || kb >= p->n_kblk) return 0;
+        int64_t idx = (((int64_t)b * p->hq + h) * p->n_qblk + qb) * p->n_kblk + kb;
+        if (!p->block_mask[idx]) return 0;
+    }
+    return 1;
+}
+
+/* One row: query token t (global), head h.  Writes out[dv] and *lse. */
+static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, double *lse,
+                    double *qrow, double *krow, double *vrow, double *s, unsigned char *ok) {
+    int b = 0;
+    while (b < p->num_seqs && !(t >= p->cu_q[b] && t < p->cu_q[b + 1])) b++;
+    int64_t sq = p->cu_q[b + 1] - p->cu_q[b];
+    int64_t sk = p->cu_k[b + 1] - p->cu_k[b];
+    int64_t i = t - p->cu_q[b];
+    int64_t ip = i + sk - sq;
+    int hk = h / (p->hq / p->hkv);
+
+    for (int x = 0; x < p->dk; x++)
+        qrow[x] = fa_oracle_bf16_decode(p->q[(t * p->hq + h) * (int64_t)p->dk + x]);
+
+    int any = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < sk; j++) {
+        ok[j] = (unsigned char)allowed(p, b, h, i, j, sq, sk);
+        if (!ok[j]) continue;
+        fetch_row(p, p->k, p->k_scale, b, j, hk, p->dk, krow);
+        double dot = 0.0;
+        for (int x = 0; x < p->dk; x++) dot += qrow[x] * krow[x];
+        double sj = p->softmax_scale * dot;
+        if (p->mod_kind == MOD_SOFTCAP) sj = p->softcap * tanh(sj / p->softcap);
+        if (p->mod_kind == MOD_ALIBI) sj -= p->alibi_slope * (double)(ip > j ? ip - j : j - ip);
+        s[j] = sj;
+        if (sj > m) m = sj;
+        any = 1;
+    }
+    for (int x = 0; x < p->dv; x++) out[x] = 0.0;
+    if (!any) {
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < sk; j++) {
+        if (!ok[j]) continue;
+        double w = exp(s[j] - m);
+        l += w;
+        fetch_row(p, p->v, p->v_scale, b, j, hk, p->dv, vrow);
+        for (int x = 0; x < p->dv; x++) out[x] += w * vrow[x];
+    }
+    for (int x = 0; x < p->dv; x++) out[x] /= l;
+    *lse = m + log(l);
+}
+
+typedef struct {
+    const fa_oracle_problem *p;
+    const int64_t *units;     /* pairs (t, h), or NULL for all rows */
+    int64_t n_units;
+    double *out, *lse;
+    int tid, nthreads;
+    int64_t max_sk;
+} worker_arg;
+
+static void *worker(void *argp) {
+    worker_arg *a = (worker_arg *)argp;
+    const fa_oracle_problem *p = a->p;
+    int64_t cap_k = a->max_sk > 0 ? a->max_sk : 1;
+    double *qrow = (double *)malloc(sizeof(double) * p->dk);
+    double *krow = (double *)malloc(sizeof(double) * p->dk);
+    double *vrow = (double *)malloc(sizeof(double) * p->dv);
+    double *s = (double *)malloc(sizeof(double) * cap_k);
+    unsigned char *ok = (unsigned char *)malloc(cap_k);
+    for (int64_t u = a->tid; u < a->n_units; u += a->nthreads) {
+        int64_t t, h;
+        if (a->units) { t = a->units[2 * u]; h = a->units[2 * u + 1]; }
+        else { t = u / p->hq; h = u % p->hq; }
+        one_row(p, t, (int)h, a->out + u * p->dv, a->lse + u, qrow, krow, vrow, s, ok);
+    }
+    free(qrow); free(krow); free(vrow); free(s); free(ok);
+    return NULL;
+}
+
+/*
+ * Compute rows of the forward pass.
+ *   units   : NULL for every (t, h) in t-major order, else n_units pairs (t, h)
+ *   out     : [n_units][Dv] doubles;  lse: [n_units] doubles
+ * Returns 0, or -1 on a malformed problem.
+ */
+int fa_oracle_fwd(const fa_oracle_problem *p, const int64_t *units, int64_t n_units,
+                  double *out, double *lse, int nthreads) {
+    if (!p || p->hq <= 0 || p->hkv <= 0 || p->hq % p->hkv || p->num_seqs < 0) return -1;
+    if (p->block_table && p->page_size <= 0) return -1;
+    if (!units) n_units = (int64_t)p->cu_q[p->num_seqs] * p->hq;
+    int64_t max_sk = 0;
+    for (int b = 0; b < p->num_seqs; b++) {
+        int64_t sk = p->cu_k[b + 1] - p->cu_k[b];
+        if (sk > max_sk) max_sk = sk;
+    }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    pthread_t th[1024];
+    worker_arg args[1024];
+    for (int i = 0; i < nthreads; i++) {
+        args[i] = (worker_arg){p, units, n_units, out, lse, i, nthreads, max_sk};
+        if (nthreads > 1) pthread_create(&th[i], NULL, worker, &args[i]);
+    }
+    if (nthreads == 1) worker(&args[0]);
+    else for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
+    return 0;
+}
+
+/*
+ * Merge of partial results over disjoint key sets (split-KV combine).
+ * Softmax over a union of disjoint key sets S_1..S_n: with L_s the LSE and
+ * O_s the normalised output over S_s,
+ *   LSE = ln sum_s exp(L_s),   out = sum_s exp(L_s - LSE) * O_s.
+ * Sets with L_s = -inf contribute nothing; all -inf gives out 0, LSE -inf.
+ * The pages' split-K combine finalises m_max*ln2 + ln(den) from per-split
+ * (m, l) (FlyDSL PR #844, Changes list); this is the same merge in the
+ * natural-log domain.
+ *   o_part: [n_split][n][Dv], lse_part: [n_split][n]
+ */
+void fa_oracle_combine(const double *o_part, const double *lse_part, int n_split, int64_t n,
+                       int dv, double *out, double *lse) {
+    for (int64_t r = 0; r < n; r++) {
+        double mx = -INFINITY;
+        for (int s = 0; s < n_split; s++) {
+            double v = lse_part[(int64_t)s * n + r];
+            if (v > mx) mx = v;
+        }
+        for (int x = 0; x < dv; x++) out[r * dv + x] = 0.0;
+        if (mx == -INFINITY) { lse[r] = -INFINITY; continue; }
+        double den = 0.0;
+        for (int s = 0; s < n_split; s++) den += exp(lse_part[(int64_t)s * n + r] - mx);
+        double L = mx + log(den);
+        lse[r] = L;
+        for (int s = 0; s < n_split; s++) {
+            double w = exp(lse_part[(int64_t)s * n + r] - L);
+            if (w == 0.0) continue;
+            for (int x = 0; x < dv; x++) out[r * dv + x] += w * o_part[((int64_t)s * n + r) * dv + x];
+        }
+    }
+}
