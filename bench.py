@@ -1,0 +1,418 @@
+"""Benchmark of the attention forward pass on one GB300 (replicas for N > 1).
+
+Headline workload: the packed varlen bf16 prefill (8 sequences of length
+U{0..2048} with seed 0, H=16, D=128).  One step runs it causal and non-causal
+(two launches of the prefill kernel) over inputs already resident in HBM.
+The metric is algorithmic TFLOP/s: 2*Dk + 2*Dv flops per (head, query, key)
+pair the mask allows.  L2 is flushed (a 256 MiB write) between timed steps,
+outside the timed events.
+
+Extra lines of the same JSON object report the other workloads: the dense
+causal latency case, the paged split-KV decode (KV-cache GB/s), and the flex
+runs.  ``--impl reference`` times the fp64 CPU oracle instead (bounded samples
+of the same workload, on the host cores).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import fa_inputs as fi  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (prefill) & KV-cache GB/s (decode), % of GB300 roofline"
+KERNEL_SOURCES = ["flashattention_forward_gb300/csrc/fa_prefill.cuh", "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def dev_tensors(p, dev):
+    t = {"q": torch.from_numpy(p.q.view(np.int16).copy()).view(torch.bfloat16).to(dev)}
+    if p.kv_dtype == "bf16":
+        t["k"] = torch.from_numpy(p.k.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+        t["v"] = torch.from_numpy(p.v.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    else:
+        t["k"] = torch.from_numpy(p.k.copy()).view(torch.float8_e4m3fn).to(dev)
+        t["v"] = torch.from_numpy(p.v.copy()).view(torch.float8_e4m3fn).to(dev)
+        t["k_scale"] = torch.from_numpy(p.k_scale.copy()).to(dev)
+        t["v_scale"] = torch.from_numpy(p.v_scale.copy()).to(dev)
+    t["cu_q"] = torch.from_numpy(p.cu_seqlens_q.copy()).to(dev)
+    t["cu_k"] = torch.from_numpy(p.cu_seqlens_k.copy()).to(dev)
+    if p.block_table is not None:
+        t["bt"] = torch.from_numpy(p.block_table.copy()).to(dev)
+    if p.block_mask is not None:
+        t["bm"] = torch.from_numpy(p.block_mask.copy()).to(dev)
+    return t
+
+
+def make_call(p, t, num_splits=0):
+    import flashattention_forward_gb300 as fa
+    dev = t["q"].device
+    out = torch.empty((p.total_q, p.hq, p.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.hq, p.total_q), dtype=torch.float32, device=dev)
+    ws = None
+    if num_splits is None:
+        num_splits = fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size)
+    if num_splits > 1:
+        ws = torch.empty(fa.workspace_bytes(p.num_seqs, p.total_q, p.hq, p.dv, num_splits), dtype=torch.uint8,
+                         device=dev)
+
+    def call(tt=t, o=out, l=lse):
+        fa.fwd_varlen(tt["q"], tt["k"], tt["v"], tt["cu_q"], tt["cu_k"], max_seqlen_q=p.max_seqlen_q,
+                      max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, block_table=tt.get("bt"),
+                      page_size=p.page_size, k_scale=tt.get("k_scale"), v_scale=tt.get("v_scale"),
+                      softmax_scale=p.softmax_scale, causal=p.causal, window=p.window, score_mod=p.mod_kind,
+                      alibi_slope=p.alibi_slope, softcap=p.softcap, block_mask=tt.get("bm"),
+                      num_splits=num_splits, out=o, lse=l, workspace=ws)
+        return o, l
+    launches = 1 + (1 if num_splits > 1 else 0)
+    return call, launches, out, lse
+
+
+class Flusher:
+    def __init__(self, dev):
+        self.buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_calls(calls, warmup, steps, flush):
+    """Per-step CUDA-event time of running every call once (L2 flushed between steps)."""
+    for _ in range(warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for c in calls:
+            c()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return times
+
+
+def time_each(calls, warmup, steps, flush):
+    """Per-call CUDA-event times (one list per call)."""
+    res = [[] for _ in calls]
+    for _ in range(warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        for i, c in enumerate(calls):
+            flush()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            c()
+            e.record()
+            e.synchronize()
+            res[i].append(s.elapsed_time(e))
+    return res
+
+
+def e2e_measure(p, steps, dev):
+    """Same metric through the public API with HOST inputs: pinned H2D copies of
+    every input, the forward pass, and D2H of out + LSE, all inside the events."""
+    import flashattention_forward_gb300 as fa
+    hq = {k: v.cpu().pin_memory() for k, v in dev_tensors(p, "cpu").items()}
+    dd = {k: torch.empty_like(v, device=dev) for k, v in hq.items()}
+    out_h = torch.empty((p.total_q, p.hq, p.dv), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((p.hq, p.total_q), dtype=torch.float32).pin_memory()
+    call, _, out, lse = make_call(p, dd, num_splits=0)
+    h2d = sum(v.numel() * v.element_size() for v in hq.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    ts = []
+    for i in range(steps + 2):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for k in hq:
+            dd[k].copy_(hq[k], non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        e.record()
+        e.synchronize()
+        if i >= 2:
+            ts.append(s.elapsed_time(e))
+    return statistics.mean(ts), h2d, d2h
+
+
+def cpu_oracle_sample(p, seconds_target=15.0, seed=0):
+    """Time the oracle on a bounded seeded row sample; return (flop/s, rows, threads, secs)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    units_all = np.stack(np.meshgrid(np.arange(p.total_q), np.arange(p.hq), indexing="ij"), -1).reshape(-1, 2)
+    # flops of each row: allowed keys * (2 Dk + 2 Dv); sample rows until about the target
+    n = 256
+    threads = os.cpu_count() or 1
+    while True:
+        idx = rng.choice(len(units_all), size=min(n, len(units_all)), replace=False)
+        units = units_all[idx]
+        t0 = time.time()
+        oracle.forward(p, units=units, nthreads=threads)
+        dt = time.time() - t0
+        if dt > 2.0 or n >= len(units_all):
+            break
+        n *= 4
+    # flops of the sample: count allowed keys per sampled row exactly
+    sk = p.seqlens_k
+    sq = p.seqlens_q
+    seq_of = np.searchsorted(p.cu_seqlens_q[1:], units[:, 0], side="right")
+    flops = 0.0
+    for (t, h), b in zip(units, seq_of):
+        i = t - p.cu_seqlens_q[b]
+        ip = i + sk[b] - sq[b]
+        hi = min(sk[b], ip + 1) if p.causal else sk[b]
+        flops += max(hi, 0) * (2 * p.dk + 2 * p.dv)
+    rate = flops / dt
+    return rate, len(units), threads, dt, flops
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    p_causal = fi.config2(causal=True)
+    p_full = fi.config2(causal=False)
+    flops_step = fi.prefill_flops(p_causal) + fi.prefill_flops(p_full)
+    workload = {"workload": "varlen_prefill_8seq_U0-2048_seed0_h16_d128_bf16_causal+noncausal",
+                "seqlens": [int(x) for x in p_causal.seqlens_q], "hq": 16, "hkv": 16, "d": 128,
+                "l2": "flushed between steps (256 MiB write)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rates = []
+        for _ in range(warmup):
+            pass
+        t_steps = []
+        for k in range(args.steps):
+            r1 = cpu_oracle_sample(p_causal, seed=k)
+            r2 = cpu_oracle_sample(p_full, seed=k)
+            flops = r1[4] + r2[4]
+            secs = r1[3] + r2[3]
+            rates.append(flops / secs / 1e12)
+            t_steps.append(secs * 1e3)
+        val = statistics.mean(rates)
+        line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": warmup, "ms_per_step": statistics.mean(t_steps),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload,
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": "seeded row samples (about 2-8 s each) of the causal and non-causal runs"},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import flashattention_forward_gb300 as fa
+    from flashattention_forward_gb300 import build as fa_build
+    if rank == 0 or world == 1:
+        fa_build.build()
+    if dist:
+        dist.barrier()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.lib()
+    flush = Flusher(dev)
+    pk = peaks()
+
+    # ------------------------------------------------------- headline step --
+    tc, tf = dev_tensors(p_causal, dev), dev_tensors(p_full, dev)
+    call_c, n_c, _, _ = make_call(p_causal, tc)
+    call_f, n_f, _, _ = make_call(p_full, tf)
+    for _ in range(warmup):
+        call_c()
+        call_f()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        each = time_each([call_c, call_f], 0, args.steps, flush)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    step_ms = [a + b for a, b in zip(*each)]
+    ms = statistics.mean(step_ms)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = flops_step * world / (ms * 1e-3) / 1e12
+    # dominant kernel: the non-causal launch (largest share of the step)
+    ms_f = statistics.mean(each[1])
+    ach = fi.prefill_flops(p_full) / (ms_f * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        if tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == "varlen_noncausal":
+            traffic = tj.get("dram_bytes_per_launch")
+    roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16"], "traffic": traffic,
+                "kernel": "fa_prefill_kernel<128,128,packed,bf16>, non-causal launch",
+                "peak_source": f"{pk['src']} bf16 burst (cuBLAS 8192^3)"}
+    extra = {}
+    if rank == 0:
+        e2e_c, h2d_c, d2h_c = e2e_measure(p_causal, max(3, args.steps // 2), dev)
+        e2e_f, h2d_f, d2h_f = e2e_measure(p_full, max(3, args.steps // 2), dev)
+        e2e = {"value": flops_step / ((e2e_c + e2e_f) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d_c + h2d_f, "d2h_bytes_per_step": d2h_c + d2h_f,
+               "ms_per_step": e2e_c + e2e_f}
+        if not args.quick:
+            extra = other_workloads(dev, warmup, max(5, args.steps // 2), flush, pk)
+        rate, nrows, threads, secs, _ = cpu_oracle_sample(p_full, seed=1)
+        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nrows} seeded (token, head) rows of the non-causal run, {secs:.1f} s, fp64 C with "
+                         f"{threads} threads"}
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": (n_c + n_f) * args.steps, "clocks": clk.summary(),
+                "pct_of_peak": 100.0 * value / world / pk["bf16"], "workloads": extra,
+                "kernel_hash": kernel_hash()}
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def other_workloads(dev, warmup, steps, flush, pk):
+    import flashattention_forward_gb300 as fa
+    res = {}
+    # dense causal latency case (launch-latency bound): wall and device time
+    p = fi.config1()
+    t = dev_tensors(p, dev)
+    call, _, _, _ = make_call(p, t)
+    times = time_calls([call], warmup, steps, lambda: None)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(200):
+        call()
+    torch.cuda.synchronize()
+    wall_us = (time.perf_counter() - w0) / 200 * 1e6
+    res["dense_causal_b2_h4_s128_d64"] = {"device_us": 1e3 * statistics.median(times), "wall_us_per_call": wall_us,
+                                          "tflops": fi.prefill_flops(p) / (statistics.median(times) * 1e-3) / 1e12}
+    # paged split-KV decode: KV-cache GB/s
+    p = fi.config3()
+    t = dev_tensors(p, dev)
+    call, n, _, _ = make_call(p, t, num_splits=None)
+    times = time_calls([call], warmup, steps, flush)
+    ms = statistics.mean(times)
+    gbs = fi.decode_bytes(p) / (ms * 1e-3) / 1e9
+    res["paged_decode_64seq_hq32_hkv8_p16"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
+                                               "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16),
+                                               "bytes": fi.decode_bytes(p)}
+    # flex runs at B=4, H=16, S=8192
+    for run in fi.CONFIG5_RUNS:
+        p = fi.config5(run)
+        t = dev_tensors(p, dev)
+        call, _, _, _ = make_call(p, t)
+        times = time_calls([call], 2, max(3, steps // 2), flush)
+        ms = statistics.mean(times)
+        fl = fi.prefill_flops(p)
+        ent = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"]}
+        if run == "window_causal":
+            byt = (p.q.nbytes + p.k.nbytes + p.v.nbytes + p.total_q * p.hq * p.dv * 2 + p.total_q * p.hq * 4)
+            ent["GB/s"] = byt / (ms * 1e-3) / 1e9
+            ent["frac_hbm"] = ent["GB/s"] / pk["hbm"]
+        res["flex_" + run] = ent
+        del t
+        torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+"""GB300 (sm_103a) FlashAttention forward -- thin Python binding of the C ABI.
+
+Every step of the forward pass runs in the CUDA library ``_build/libfa_gb300.so``
+(see ``include/fa_gb300.h``).  This module only marshals torch tensors into
+``fa_tensor_t`` descriptors, allocates outputs/workspace with torch on the
+current stream, and raises on any non-OK status.  There is no fallback: if the
+library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_OVERFLOW, FA_ERR_CUDA = 0, 1, 2, 3, 4
+FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_BOUNDS = 5, 6
+FA_BF16, FA_E4M3, FA_F32, FA_I32, FA_U8 = 0, 1, 2, 3, 4
+MOD_NONE, MOD_ALIBI, MOD_SOFTCAP = 0, 1, 2
+
+EXPORTED = ("fa_fwd_varlen", "fa_fwd_workspace_bytes", "fa_fwd_default_splits", "fa_combine",
+            "fa_last_error", "fa_get_device_error", "fa_version")
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"fa status {status}: {msg}")
+        self.status = status
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+class ScoreMod(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("alibi_slope", ctypes.c_float), ("softcap", ctypes.c_float)]
+
+
+class BlockMask(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("n_qblk", ctypes.c_int32), ("n_kblk", ctypes.c_int32),
+                ("blk_q", ctypes.c_int32), ("blk_k", ctypes.c_int32)]
+
+
+class Launch(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
+                ("max_seqlen_k", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+                ("total_q", ctypes.c_int64), ("total_k", ctypes.c_int64),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m flashattention_forward_gb300.build` "
+                    "(there is no fallback implementation)")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.POINTER
+            L.fa_fwd_varlen.argtypes = [P(Tensor)] * 8 + [P(Tensor), P(Tensor), ctypes.c_float, ctypes.c_int32,
+                                                         ctypes.c_int32, P(ScoreMod), P(BlockMask), ctypes.c_int32,
+                                                         P(Launch), ctypes.c_void_p]
+            L.fa_fwd_varlen.restype = ctypes.c_int
+            L.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32]
+            L.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
+            L.fa_fwd_default_splits.argtypes = [ctypes.c_int32] * 6
+            L.fa_fwd_default_splits.restype = ctypes.c_int32
+            L.fa_combine.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+            L.fa_combine.restype = ctypes.c_int
+            L.fa_last_error.restype = ctypes.c_char_p
+            L.fa_get_device_error.argtypes = [ctypes.c_void_p, P(ctypes.c_int32)]
+            L.fa_get_device_error.restype = ctypes.c_int
+            L.fa_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != FA_OK:
+        raise FaError(status, lib().fa_last_error().decode())
+
+
+_DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int32: FA_I32, torch.uint8: FA_U8}
+if hasattr(torch, "float8_e4m3fn"):
+    _DT[torch.float8_e4m3fn] = FA_E4M3
+
+
+def as_tensor(t: Optional[torch.Tensor], fa_dtype: Optional[int] = None) -> Optional[Tensor]:
+    """Describe a torch tensor (device pointer, shape, element strides)."""
+    if t is None:
+        return None
+    d = Tensor()
+    d.data = t.data_ptr() if t.numel() else 0
+    d.dtype = _DT[t.dtype] if fa_dtype is None else fa_dtype
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _ref(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size=0) -> int:
+    return int(lib().fa_fwd_default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size))
+
+
+def workspace_bytes(num_seqs, total_q, hq, dv, num_splits) -> int:
+    return int(lib().fa_fwd_workspace_bytes(num_seqs, total_q, hq, dv, num_splits))
+
+
+def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, *,
+               max_seqlen_q: int, max_seqlen_k: int, total_k: Optional[int] = None,
+               block_table: Optional[torch.Tensor] = None, page_size: int = 0,
+               k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+               softmax_scale: Optional[float] = None, causal: bool = False, window: int = 0,
+               score_mod: int = MOD_NONE, alibi_slope: float = 0.0, softcap: float = 0.0,
+               block_mask: Optional[torch.Tensor] = None, num_splits: Optional[int] = None,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Attention forward over packed varlen Q and packed or paged K/V.
+
+    q [T_q, Hq, Dk] bf16; k_cache/v_cache packed [T_k, Hkv, D] or paged
+    [N_pg, P_s, Hkv, D] (bf16, or e4m3 as float8_e4m3fn/uint8 with k_scale/
+    v_scale); cu_seqlens int32 [B+1].  ``max_seqlen_q/k`` are host ints (no
+    device read-back).  Returns ``(out [T_q, Hq, Dv] bf16, lse [Hq, T_q] fp32
+    or None)``.  ``num_splits=None`` picks the library's default (split-KV for
+    decode shapes); 0 forces the single-pass kernel.
+    """
+    L = lib()
+    B = cu_seqlens_q.shape[0] - 1
+    Tq, Hq, Dk = q.shape
+    Dv = v_cache.shape[-1]
+    Hkv = k_cache.shape[-2]
+    kv_dt = FA_BF16 if k_cache.dtype == torch.bfloat16 else FA_E4M3
+    if out is None:
+        out = torch.empty((Tq, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dk)
+    if total_k is None:
+        total_k = k_cache.shape[0] if block_table is None else 0
+    if num_splits is None:
+        num_splits = default_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, page_size)
+        if kv_dt != FA_BF16 or Dk != Dv or score_mod != MOD_NONE or block_mask is not None:
+            num_splits = 0
+    launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                    num_splits=num_splits, total_q=Tq, total_k=total_k)
+    if num_splits > 1:
+        need = workspace_bytes(B, Tq, Hq, Dv, num_splits)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        launch.workspace = workspace.data_ptr()
+        launch.workspace_bytes = workspace.numel()
+    sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
+    bm = None
+    if block_mask is not None:
+        bm = BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1], n_kblk=block_mask.shape[2],
+                       blk_q=128, blk_k=128)
+    args = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
+            as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(k_scale), as_tensor(v_scale),
+            as_tensor(out), as_tensor(lse)]
+    st = L.fa_fwd_varlen(*[_ref(a) for a in args], float(softmax_scale), int(bool(causal)), int(window),
+                         ctypes.byref(sm), _ref(bm), int(page_size), ctypes.byref(launch),
+                         ctypes.c_void_p(_stream_ptr(stream)))
+    _check(st)
+    return out, lse
+
+
+def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, stream=None):
+    """Merge split partials: o_part fp32 [S, n, Hq, Dv], lse_part fp32 [S, Hq, n]."""
+    S, n, Hq, Dv = o_part.shape
+    if out is None:
+        out = torch.empty((n, Hq, Dv), dtype=torch.bfloat16, device=o_part.device)
+    if lse is None:
+        lse = torch.empty((Hq, n), dtype=torch.float32, device=o_part.device)
+    o_part = o_part.contiguous()
+    lse_part = lse_part.contiguous()
+    _check(lib().fa_combine(o_part.data_ptr(), lse_part.data_ptr(), S, n, Hq, Dv, out.data_ptr(),
+                            lse.data_ptr(), ctypes.c_void_p(_stream_ptr(stream))))
+    return out, lse
+
+
+def device_error(stream=None) -> int:
+    """Synchronise and return (then clear) the device error word."""
+    code = ctypes.c_int32(0)
+    _check(lib().fa_get_device_error(ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(code)))
+    return int(code.value)
+
+
+def version() -> str:
+    return lib().fa_version().decode()

@@ -1,0 +1,465 @@
+// fa_api.cu -- the C ABI declared in include/fa_gb300.h: host-side validation,
+// TMA descriptor encoding and variant dispatch.  Every check runs on the host
+// before anything is enqueued; no device memory is read back or allocated.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/fa_gb300.h"
+#include "fa_internal.h"
+
+namespace fa {
+// The per-device error word (one copy per device that loads the library).
+__device__ int g_fa_error = 0;
+}
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+fa_status_t fail(fa_status_t st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fa_status_t cuda_fail(cudaError_t e, const char *where) {
+  return fail(FA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Tiled map with 128-byte swizzle; strides in bytes for dims 1..rank-1.
+fa_status_t make_map(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base, const uint64_t *dims,
+                     const uint64_t *strides, const uint32_t *box, const char *what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+  return FA_OK;
+}
+
+int dtype_size(int dt) {
+  switch (dt) {
+    case FA_BF16: return 2;
+    case FA_E4M3: return 1;
+    case FA_F32: return 4;
+    case FA_I32: return 4;
+    case FA_U8: return 1;
+    default: return 0;
+  }
+}
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int64_t x) {
+  int s = 0;
+  while ((int64_t(1) << s) < x) ++s;
+  return s;
+}
+
+// Basic shape/dtype check of a tensor descriptor.
+fa_status_t check_tensor(const fa_tensor_t *t, const char *name, int dtype, int ndim) {
+  if (!t) return fail(FA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (t->dtype != dtype) return fail(FA_ERR_INVALID_ARG, "%s has dtype %d, expected %d", name, t->dtype, dtype);
+  if (t->ndim != ndim) return fail(FA_ERR_INVALID_ARG, "%s has %d dims, expected %d", name, t->ndim, ndim);
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0) return fail(FA_ERR_INVALID_ARG, "%s has a negative extent", name);
+  return FA_OK;
+}
+
+bool contiguous(const fa_tensor_t *t) {
+  int64_t s = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->stride[i] != s) return false;
+    s *= t->shape[i];
+  }
+  return true;
+}
+
+int64_t numel(const fa_tensor_t *t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+int64_t span_bytes(const fa_tensor_t *t) {
+  int64_t hi = 0;
+  for (int i = 0; i < t->ndim; ++i) hi += (t->shape[i] - 1) * t->stride[i];
+  return (hi + 1) * dtype_size(t->dtype);
+}
+
+bool overlaps(const fa_tensor_t *a, const fa_tensor_t *b) {
+  if (!a || !b || numel(a) == 0 || numel(b) == 0) return false;
+  const char *a0 = (const char *)a->data, *b0 = (const char *)b->data;
+  return a0 < b0 + span_bytes(b) && b0 < a0 + span_bytes(a);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device address of the error word on the current device (looked up once per
+// device; cudaGetSymbolAddress allocates nothing).
+int *error_word() {
+  static int *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, fa::g_fa_error) == cudaSuccess) addr[dev] = (int *)p;
+  }
+  return addr[dev];
+}
+
+bool supported_dims(int64_t dk, int64_t dv) {
+  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fa_last_error(void) { return g_msg; }
+
+const char *fa_version(void) { return "fa_gb300 0.1 (sm_103a)"; }
+
+size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int32_t dv, int32_t num_splits) {
+  (void)num_seqs;
+  if (num_splits <= 0 || total_q <= 0 || hq <= 0 || dv <= 0) return 0;
+  const size_t o = (size_t)num_splits * total_q * hq * dv * sizeof(float);
+  const size_t l = (size_t)num_splits * hq * total_q * sizeof(float);
+  return align256(o) + align256(l);
+}
+
+int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t hq, int32_t hkv,
+                              int32_t page_size) {
+  (void)page_size;
+  if (num_seqs <= 0 || hq <= 0 || hkv <= 0 || hq % hkv) return 0;
+  const int64_t rows = (int64_t)max_seqlen_q * (hq / hkv);
+  if (rows <= 0 || rows > fa::kDecRows) return 0;
+  if (max_seqlen_k < 256) return 0;
+  // Fixed-size key ranges of about 512 keys keep the work per CTA uniform;
+  // ranges past a shorter sequence's end cost one LSE store each.
+  int64_t s = (max_seqlen_k + 511) / 512;
+  if (s > 64) s = 64;
+  if (s < 1) s = 1;
+  return (int32_t)s;
+}
+
+fa_status_t fa_get_device_error(void *stream, int32_t *code) {
+  if (!code) return fail(FA_ERR_INVALID_ARG, "code is NULL");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, fa::g_fa_error, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(fa::g_fa_error, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+  *code = v;
+  return FA_OK;
+}
+
+fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_splits, int64_t n_rows, int32_t hq,
+                       int32_t dv, void *out_bf16, float *lse, void *stream) {
+  if (num_splits <= 0 || n_rows < 0 || hq <= 0) return fail(FA_ERR_INVALID_ARG, "bad combine sizes");
+  if (dv != 64 && dv != 128) return fail(FA_ERR_UNSUPPORTED, "combine supports Dv 64 or 128, got %d", dv);
+  if (n_rows == 0) return FA_OK;
+  if (!o_part || !lse_part || !out_bf16) return fail(FA_ERR_INVALID_ARG, "combine pointer is NULL");
+  if (((uintptr_t)o_part | (uintptr_t)out_bf16) & 15) return fail(FA_ERR_INVALID_ARG, "combine buffers must be 16-byte aligned");
+  cudaError_t e = fa::launch_combine(o_part, lse_part, num_splits, n_rows, hq, dv, out_bf16, lse, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
+                          const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
+                          const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
+                          fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
+                          const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
+                          const fa_launch_t *launch, void *stream) {
+  fa_status_t st;
+  g_msg[0] = 0;
+  if (!launch) return fail(FA_ERR_INVALID_ARG, "launch is NULL");
+  const int64_t B = launch->num_seqs;
+  if (B < 0) return fail(FA_ERR_INVALID_ARG, "num_seqs < 0");
+  // ---- q
+  if ((st = check_tensor(q, "q", FA_BF16, 3))) return st;
+  const int64_t Tq = q->shape[0], Hq = q->shape[1], Dk = q->shape[2];
+  if (Tq != launch->total_q) return fail(FA_ERR_INVALID_ARG, "q.shape[0]=%lld != launch.total_q=%lld", (long long)Tq, (long long)launch->total_q);
+  if (q->stride[2] != 1 || q->stride[1] % 8 || q->stride[0] % 8)
+    return fail(FA_ERR_INVALID_ARG, "q needs a contiguous last dim and strides that are multiples of 8 elements");
+  // ---- k/v
+  const bool paged = block_table != nullptr;
+  const int kvnd = paged ? 4 : 3;
+  if (!k_cache || !v_cache) return fail(FA_ERR_INVALID_ARG, "k_cache/v_cache is NULL");
+  const int kv_dt = k_cache->dtype;
+  if (kv_dt != FA_BF16 && kv_dt != FA_E4M3) return fail(FA_ERR_INVALID_ARG, "k_cache dtype must be bf16 or e4m3");
+  if ((st = check_tensor(k_cache, "k_cache", kv_dt, kvnd))) return st;
+  if ((st = check_tensor(v_cache, "v_cache", kv_dt, kvnd))) return st;
+  const int64_t Hkv = k_cache->shape[kvnd - 2];
+  const int64_t Dk2 = k_cache->shape[kvnd - 1], Dv = v_cache->shape[kvnd - 1];
+  if (Dk2 != Dk) return fail(FA_ERR_INVALID_ARG, "k_cache head dim %lld != q head dim %lld", (long long)Dk2, (long long)Dk);
+  if (v_cache->shape[kvnd - 2] != Hkv) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache disagree on Hkv");
+  for (int i = 0; i < kvnd - 2; ++i)
+    if (v_cache->shape[i] != k_cache->shape[i]) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache shapes disagree");
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv) return fail(FA_ERR_INVALID_ARG, "Hq=%lld must be a positive multiple of Hkv=%lld", (long long)Hq, (long long)Hkv);
+  if (!supported_dims(Dk, Dv)) return fail(FA_ERR_UNSUPPORTED, "(Dk, Dv) = (%lld, %lld) is not compiled", (long long)Dk, (long long)Dv);
+  const int esz = dtype_size(kv_dt);
+  for (const fa_tensor_t *t : {k_cache, v_cache}) {
+    if (t->stride[kvnd - 1] != 1) return fail(FA_ERR_INVALID_ARG, "k/v caches need a contiguous last dim");
+    for (int i = 0; i < kvnd - 1; ++i)
+      if ((t->stride[i] * esz) % 16) return fail(FA_ERR_INVALID_ARG, "k/v cache strides must be multiples of 16 bytes");
+    if (((uintptr_t)t->data) & 15) return fail(FA_ERR_INVALID_ARG, "k/v cache base must be 16-byte aligned");
+  }
+  // ---- block table, lengths
+  int64_t n_pages = 0, max_pages = 0;
+  if (paged) {
+    if ((st = check_tensor(block_table, "block_table", FA_I32, 2))) return st;
+    if (block_table->shape[0] != B) return fail(FA_ERR_INVALID_ARG, "block_table has %lld rows, expected num_seqs=%lld", (long long)block_table->shape[0], (long long)B);
+    if (block_table->stride[1] != 1 && block_table->shape[1] > 1) return fail(FA_ERR_INVALID_ARG, "block_table rows must be contiguous");
+    max_pages = block_table->shape[1];
+    n_pages = k_cache->shape[0];
+    if (!is_pow2(page_size) || page_size < 16 || page_size > 256)
+      return fail(FA_ERR_UNSUPPORTED, "page_size %d: supported sizes are powers of two from 16 to 256", page_size);
+    if (k_cache->shape[1] != page_size) return fail(FA_ERR_INVALID_ARG, "k_cache.shape[1]=%lld != page_size=%d", (long long)k_cache->shape[1], page_size);
+    if ((int64_t)launch->max_seqlen_k > max_pages * page_size) return fail(FA_ERR_INVALID_ARG, "max_seqlen_k exceeds block_table capacity");
+    if (n_pages >= (int64_t(1) << 31)) return fail(FA_ERR_OVERFLOW, "num_pages must fit int32");
+  }
+  if ((st = check_tensor(cu_seqlens_q, "cu_seqlens_q", FA_I32, 1))) return st;
+  if ((st = check_tensor(cu_seqlens_k, "cu_seqlens_k", FA_I32, 1))) return st;
+  if (cu_seqlens_q->shape[0] != B + 1 || cu_seqlens_k->shape[0] != B + 1)
+    return fail(FA_ERR_INVALID_ARG, "cu_seqlens must have num_seqs+1 = %lld entries", (long long)(B + 1));
+  if (!contiguous(cu_seqlens_q) || !contiguous(cu_seqlens_k)) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must be contiguous");
+  if (launch->max_seqlen_q < 0 || launch->max_seqlen_k < 0 || launch->total_k < 0)
+    return fail(FA_ERR_INVALID_ARG, "negative length in launch");
+  if (Tq >= (int64_t(1) << 31) || launch->total_k >= (int64_t(1) << 31))
+    return fail(FA_ERR_OVERFLOW, "total tokens must fit the int32 cu_seqlens");
+  if (!paged && k_cache->shape[0] < launch->total_k) return fail(FA_ERR_INVALID_ARG, "packed k_cache has fewer rows than total_k");
+  // ---- scales
+  const bool fp8 = kv_dt == FA_E4M3;
+  if (fp8) {
+    if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "e4m3 caches need k_scale and v_scale");
+    for (const fa_tensor_t *s : {k_scale, v_scale}) {
+      if ((st = check_tensor(s, "kv scale", FA_F32, kvnd - 1))) return st;
+      for (int i = 0; i < kvnd - 1; ++i)
+        if (s->shape[i] != k_cache->shape[i]) return fail(FA_ERR_INVALID_ARG, "kv scale shape must be the cache shape without the head dim");
+      if (!contiguous(s)) return fail(FA_ERR_INVALID_ARG, "kv scales must be contiguous");
+    }
+  } else if (k_scale || v_scale) {
+    return fail(FA_ERR_INVALID_ARG, "k_scale/v_scale are only valid with an e4m3 cache");
+  }
+  // ---- out, lse
+  if ((st = check_tensor(out, "out", FA_BF16, 3))) return st;
+  if (out->shape[0] != Tq || out->shape[1] != Hq || out->shape[2] != Dv)
+    return fail(FA_ERR_INVALID_ARG, "out must be [%lld, %lld, %lld]", (long long)Tq, (long long)Hq, (long long)Dv);
+  if (!contiguous(out)) return fail(FA_ERR_INVALID_ARG, "out must be contiguous");
+  if (((uintptr_t)out->data) & 15) return fail(FA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  if (lse) {
+    if ((st = check_tensor(lse, "lse", FA_F32, 2))) return st;
+    if (lse->shape[0] != Hq || lse->shape[1] != Tq) return fail(FA_ERR_INVALID_ARG, "lse must be [Hq=%lld, T_q=%lld]", (long long)Hq, (long long)Tq);
+    if (!contiguous(lse)) return fail(FA_ERR_INVALID_ARG, "lse must be contiguous");
+    if (overlaps(lse, out)) return fail(FA_ERR_INVALID_ARG, "lse must not alias out");
+  }
+  if (overlaps(out, q) || overlaps(out, k_cache) || overlaps(out, v_cache)) return fail(FA_ERR_INVALID_ARG, "out must not alias q/k/v");
+  // ---- parameters
+  if (!std::isfinite(softmax_scale)) return fail(FA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  int mod = 0;
+  float slope = 0.f, cap = 0.f;
+  if (score_mod) {
+    mod = score_mod->kind;
+    if (mod < 0 || mod > 2) return fail(FA_ERR_INVALID_ARG, "score_mod.kind %d", mod);
+    slope = score_mod->alibi_slope;
+    cap = score_mod->softcap;
+    if (mod == 1 && !std::isfinite(slope)) return fail(FA_ERR_INVALID_ARG, "alibi_slope must be finite");
+    if (mod == 2 && !(cap > 0.f && std::isfinite(cap))) return fail(FA_ERR_INVALID_ARG, "softcap must be positive and finite");
+  }
+  if (block_mask) {
+    if (!block_mask->data) return fail(FA_ERR_INVALID_ARG, "block_mask.data is NULL");
+    if (block_mask->blk_q != 128 || block_mask->blk_k != 128) return fail(FA_ERR_UNSUPPORTED, "block masks use 128x128 blocks");
+    if ((int64_t)block_mask->n_qblk * 128 < launch->max_seqlen_q || (int64_t)block_mask->n_kblk * 128 < launch->max_seqlen_k)
+      return fail(FA_ERR_INVALID_ARG, "block_mask does not cover max_seqlen_q/k");
+  }
+  if (window < 0) window = 0;
+  if (B == 0 || Tq == 0) return FA_OK;
+  if (launch->max_seqlen_q <= 0) return fail(FA_ERR_INVALID_ARG, "max_seqlen_q must be > 0 when total_q > 0");
+  if (!q->data || !out->data || !cu_seqlens_q->data || !cu_seqlens_k->data)
+    return fail(FA_ERR_INVALID_ARG, "a required data pointer is NULL");
+  if (fp8) return fail(FA_ERR_UNSUPPORTED, "e4m3 KV is not compiled in this build");
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const CUtensorMapDataType kv_tmdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int group = (int)(Hq / Hkv);
+  const bool have_keys = launch->total_k > 0 || (paged && n_pages > 0);
+
+  // ------------------------------------------------------------ split-KV --
+  if (launch->num_splits > 0) {
+    const int S = launch->num_splits;
+    if ((int64_t)launch->max_seqlen_q * group > fa::kDecRows)
+      return fail(FA_ERR_UNSUPPORTED, "split-KV needs max_seqlen_q * Hq/Hkv <= %d", fa::kDecRows);
+    if (Dk != Dv || (Dk != 64 && Dk != 128)) return fail(FA_ERR_UNSUPPORTED, "split-KV supports Dk = Dv in {64, 128}");
+    if (mod != 0 || block_mask) return fail(FA_ERR_UNSUPPORTED, "split-KV does not take score mods or block masks");
+    if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "too many sequences or kv heads for split-KV");
+    fa::DecodeLaunch L;
+    memset(&L, 0, sizeof L);
+    const int rows_box = paged ? (page_size < fa::kDecStageKeys ? page_size : fa::kDecStageKeys) : fa::kDecStageKeys;
+    if (have_keys) {
+      if (paged) {
+        const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
+        const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2] * esz), (uint64_t)(k_cache->stride[1] * esz), (uint64_t)(k_cache->stride[0] * esz)};
+        const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2] * esz), (uint64_t)(v_cache->stride[1] * esz), (uint64_t)(v_cache->stride[0] * esz)};
+        const uint32_t box[4] = {64, 1, (uint32_t)rows_box, 1};
+        if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, box, "k"))) return st;
+        if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dk, sv, box, "v"))) return st;
+      } else {
+        const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)k_cache->shape[0]};
+        const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1] * esz), (uint64_t)(k_cache->stride[0] * esz)};
+        const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1] * esz), (uint64_t)(v_cache->stride[0] * esz)};
+        const uint32_t box[3] = {64, 1, (uint32_t)rows_box};
+        if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, box, "k"))) return st;
+        if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dk, sv, box, "v"))) return st;
+      }
+    }
+    fa::DecodeParams &p = L.p;
+    p.q = (const __nv_bfloat16 *)q->data;
+    p.q_stride_t = q->stride[0];
+    p.q_stride_h = q->stride[1];
+    p.cu_q = (const int32_t *)cu_seqlens_q->data;
+    p.cu_k = (const int32_t *)cu_seqlens_k->data;
+    p.block_table = paged ? (const int32_t *)block_table->data : nullptr;
+    p.bt_stride = paged ? block_table->stride[0] : 0;
+    p.page_size = paged ? page_size : fa::kDecStageKeys;
+    p.page_shift = ilog2(p.page_size);
+    p.rows_per_box = rows_box;
+    p.boxes_per_stage = fa::kDecStageKeys / rows_box;
+    p.hq = (int)Hq;
+    p.hkv = (int)Hkv;
+    p.group = group;
+    int64_t split_keys = (launch->max_seqlen_k + S - 1) / S;
+    split_keys = ((split_keys + fa::kDecStageKeys - 1) / fa::kDecStageKeys) * fa::kDecStageKeys;
+    if (split_keys <= 0) split_keys = fa::kDecStageKeys;
+    p.split_keys = (int)split_keys;
+    p.num_splits = S;
+    p.causal = causal != 0;
+    p.window = window;
+    p.total_q = Tq;
+    p.scale_log2 = softmax_scale * fa::kLog2e;
+    p.out = (__nv_bfloat16 *)out->data;
+    p.out_stride_t = out->stride[0];
+    p.out_stride_h = out->stride[1];
+    p.lse = lse ? (float *)lse->data : nullptr;
+    p.err = error_word();
+    if (S > 1) {
+      const size_t need = fa_fwd_workspace_bytes((int)B, Tq, (int)Hq, (int)Dv, S);
+      if (!launch->workspace || launch->workspace_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "split-KV with %d splits needs a workspace of %zu bytes", S, need);
+      if ((uintptr_t)launch->workspace & 255) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+      p.o_part = (float *)launch->workspace;
+      p.lse_part = (float *)((char *)launch->workspace + align256((size_t)S * Tq * Hq * Dv * sizeof(float)));
+    }
+    L.grid = dim3((unsigned)S, (unsigned)Hkv, (unsigned)B);
+    L.stream = s;
+    cudaError_t e = fa::launch_decode((int)Dk, L);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (S > 1) {
+      e = fa::launch_combine(p.o_part, p.lse_part, S, Tq, (int)Hq, (int)Dv, out->data, p.lse, s);
+      if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
+    return FA_OK;
+  }
+
+  // ------------------------------------------------------------ prefill --
+  const int64_t n_qtiles = (launch->max_seqlen_q + fa::kBlockM - 1) / fa::kBlockM;
+  if (B > 65535 || n_qtiles > 65535 || Hq > (1 << 20)) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  fa::PrefillLaunch L;
+  memset(&L, 0, sizeof L);
+  {
+    const uint64_t dq[3] = {(uint64_t)Dk, (uint64_t)Hq, (uint64_t)Tq};
+    const uint64_t sq[2] = {(uint64_t)(q->stride[1] * 2), (uint64_t)(q->stride[0] * 2)};
+    const uint32_t box[3] = {64, 1, (uint32_t)fa::kBlockM};
+    if (((uintptr_t)q->data) & 15) return fail(FA_ERR_INVALID_ARG, "q must be 16-byte aligned");
+    if ((st = make_map(&L.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dq, sq, box, "q"))) return st;
+  }
+  const int rows_box = paged ? (page_size < fa::kBlockN ? page_size : fa::kBlockN) : fa::kBlockN;
+  if (have_keys) {
+    if (paged) {
+      const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
+      const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
+      const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2] * esz), (uint64_t)(k_cache->stride[1] * esz), (uint64_t)(k_cache->stride[0] * esz)};
+      const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2] * esz), (uint64_t)(v_cache->stride[1] * esz), (uint64_t)(v_cache->stride[0] * esz)};
+      const uint32_t box[4] = {64, 1, (uint32_t)rows_box, 1};
+      if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, box, "k"))) return st;
+      if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dv, sv, box, "v"))) return st;
+    } else {
+      const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)k_cache->shape[0]};
+      const uint64_t dv[3] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)v_cache->shape[0]};
+      const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1] * esz), (uint64_t)(k_cache->stride[0] * esz)};
+      const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1] * esz), (uint64_t)(v_cache->stride[0] * esz)};
+      const uint32_t box[3] = {64, 1, (uint32_t)fa::kBlockN};
+      if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, box, "k"))) return st;
+      if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dv, sv, box, "v"))) return st;
+    }
+  }
+  fa::PrefillParams &p = L.p;
+  p.cu_q = (const int32_t *)cu_seqlens_q->data;
+  p.cu_k = (const int32_t *)cu_seqlens_k->data;
+  p.block_table = paged ? (const int32_t *)block_table->data : nullptr;
+  p.bt_stride = paged ? block_table->stride[0] : 0;
+  p.k_scale = fp8 ? (const float *)k_scale->data : nullptr;
+  p.v_scale = fp8 ? (const float *)v_scale->data : nullptr;
+  p.out = (__nv_bfloat16 *)out->data;
+  p.out_stride_t = out->stride[0];
+  p.out_stride_h = out->stride[1];
+  p.lse = lse ? (float *)lse->data : nullptr;
+  p.total_q = Tq;
+  p.block_mask = block_mask ? block_mask->data : nullptr;
+  p.n_qblk = block_mask ? block_mask->n_qblk : 0;
+  p.n_kblk = block_mask ? block_mask->n_kblk : 0;
+  p.num_seqs = (int)B;
+  p.hq = (int)Hq;
+  p.hkv = (int)Hkv;
+  p.group = group;
+  p.page_size = paged ? page_size : fa::kBlockN;
+  p.page_shift = ilog2(p.page_size);
+  p.rows_per_box = rows_box;
+  p.pages_per_tile = fa::kBlockN / rows_box;
+  p.n_qtiles = (int)n_qtiles;
+  p.causal = causal != 0;
+  p.window = window;
+  p.scale_log2 = softmax_scale * fa::kLog2e;
+  p.softcap_arg = mod == 2 ? softmax_scale / cap : 0.f;
+  p.softcap_log2 = mod == 2 ? cap * fa::kLog2e : 0.f;
+  p.alibi_log2 = mod == 1 ? slope * fa::kLog2e : 0.f;
+  p.err = error_word();
+  L.paged = paged;
+  L.fp8 = fp8;
+  L.mod = mod;
+  L.grid = dim3((unsigned)Hq, (unsigned)B, (unsigned)n_qtiles);
+  L.stream = s;
+  cudaError_t e;
+  if (Dk == 64) e = fa::launch_prefill_64_64(L);
+  else if (Dk == 128) e = fa::launch_prefill_128_128(L);
+  else e = fa::launch_prefill_192_128(L);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return FA_OK;
+}
+
+}  // extern "C"

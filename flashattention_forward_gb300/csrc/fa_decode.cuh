@@ -1,0 +1,450 @@
+// fa_decode.cuh -- split-KV decode kernel and the LSE combine kernel.
+//
+// Decode (few query rows per kv head, long keys) is bound by streaming the KV
+// cache from HBM: about 4 flops per byte for bf16 K/V with a GQA group of 4.
+// The kernel therefore spends its effort on the memory side -- TMA page
+// gathers into a 3-stage shared-memory ring, many CTAs in flight -- and uses
+// warp-level mma.sync only as a dense FMA engine for the tiny contractions.
+//
+// Split-KV: CTA (split s, kv head hk, sequence b) reduces the keys
+// [s*split_keys, (s+1)*split_keys) of that sequence for the rows that share kv
+// head hk: (query token tq, head hk*g + x) with row index tq*g + x < 16.  It
+// writes the normalised partial output O_s (fp32) and its LSE_s; the combine
+// kernel merges the splits:  LSE = ln sum_s exp(LSE_s),
+// out = sum_s exp(LSE_s - LSE) * O_s  (FlyDSL PR #844, Changes: split-K combine
+// finalising m_max*ln2 + ln(den); FlyDSL PR #1066 lists split-K/combine as
+// the long-KV decode form).  With a single split the kernel writes the final
+// bf16 output and LSE itself.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kDecRows = 16;          // MMA M: query rows per CTA
+constexpr int kDecStageKeys = 64;     // keys per pipeline stage
+constexpr int kDecStages = 3;
+constexpr int kDecWarps = 4;          // consumer warps (16 keys each per stage)
+constexpr int kDecThreads = (kDecWarps + 1) * 32;
+
+struct DecodeParams {
+  const __nv_bfloat16 *q;
+  int64_t q_stride_t, q_stride_h;     // elements
+  const int32_t *cu_q;
+  const int32_t *cu_k;
+  const int32_t *block_table;
+  int64_t bt_stride;
+  int32_t page_size, page_shift, rows_per_box, boxes_per_stage;
+  int32_t hq, hkv, group;
+  int32_t split_keys, num_splits;
+  int32_t causal, window;
+  int64_t total_q;
+  float scale_log2;
+  // outputs: partials when o_part != null, else final out/lse
+  float *o_part;                      // [S, T_q, Hq, Dv]
+  float *lse_part;                    // [S, Hq, T_q]
+  __nv_bfloat16 *out;
+  int64_t out_stride_t, out_stride_h;
+  float *lse;                         // [Hq, T_q] or null
+  int *err;                           // device error word
+};
+
+template <int D>
+struct DecodeCfg {
+  static constexpr int kKBytes = kDecStageKeys * D * 2;   // per stage
+  static constexpr int kVBytes = kDecStageKeys * D * 2;
+  static constexpr int kStageBytes = kKBytes + kVBytes;
+  static constexpr int kOffStages = 0;
+  static constexpr int kOffQ = kDecStages * kStageBytes;      // 16 x D bf16
+  static constexpr int kOffBar = kOffQ + kDecRows * D * 2;
+  static constexpr int kOffMisc = kOffBar + 2 * kDecStages * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of (row, 16-byte chunk) in a 128-byte-swizzled [rows x 64] bf16 block.
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, 2)
+    fa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const DecodeParams p) {
+  using Cfg = DecodeCfg<D>;
+  constexpr int NCB = D / 64;          // 64-dim column blocks
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int qa = __ldg(p.cu_q + b), sq = __ldg(p.cu_q + b + 1) - qa;
+  const int sk = __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b);
+  const int rows = sq * p.group;       // <= 16, checked on the host
+  if (rows == 0) return;
+  const int key_lo = split * p.split_keys;
+  const int key_hi = min(sk, key_lo + p.split_keys);
+  // Largest key any row of this CTA may see (causal: the last row's i').
+  int vis_hi = key_hi;
+  if (p.causal) vis_hi = min(vis_hi, sk);   // last row i' = sk - 1
+  int vis_lo = key_lo;
+  if (p.window > 0) vis_lo = max(vis_lo, (0 + sk - sq) - p.window + 1);
+  const int n_stages = vis_hi > vis_lo ? (vis_hi - key_lo + kDecStageKeys - 1) / kDecStageKeys : 0;
+  const int first_stage = vis_hi > vis_lo ? max(0, (vis_lo - key_lo) / kDecStageKeys) : 0;
+
+  if (n_stages <= first_stage) {
+    // Empty key range for every row: LSE -inf (the combine skips it).
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+      const int tq = r / p.group, h = hk * p.group + r % p.group;
+      const int64_t t = (int64_t)qa + tq;
+      if (p.o_part) {
+        p.lse_part[((int64_t)split * p.hq + h) * p.total_q + t] = -INFINITY;
+      } else {
+        __nv_bfloat16 *o = p.out + t * p.out_stride_t + (int64_t)h * p.out_stride_h;
+        for (int d = 0; d < D; ++d) o[d] = __float2bfloat16(0.f);
+        if (p.lse) p.lse[(int64_t)h * p.total_q + t] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  uint8_t *stages = smem + Cfg::kOffStages;
+  __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + Cfg::kOffQ);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+  uint64_t *empty = full + kDecStages;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), kDecWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Q rows -> shared memory (zero rows past `rows`), plain layout [16][D].
+  for (int e = threadIdx.x; e < kDecRows * D / 8; e += blockDim.x) {
+    const int r = e / (D / 8), c8 = e % (D / 8);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < rows) {
+      const int tq = r / p.group, h = hk * p.group + r % p.group;
+      const __nv_bfloat16 *src = p.q + (int64_t)(qa + tq) * p.q_stride_t + (int64_t)h * p.q_stride_h + c8 * 8;
+      val = *reinterpret_cast<const uint4 *>(src);
+    }
+    *reinterpret_cast<uint4 *>(sQ + r * D + c8 * 8) = val;
+  }
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // ------------------------------------------------------- producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
+      const int krow0 = __ldg(p.cu_k + b);
+      for (int st = first_stage; st < n_stages; ++st) {
+        const int it = st - first_stage;
+        const int slot_i = it % kDecStages;
+        if (it >= kDecStages && !mbar_wait(smem_u32(empty + slot_i), ((it / kDecStages) - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(smem_u32(full + slot_i), Cfg::kStageBytes);
+        uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
+        uint8_t *vd = kd + Cfg::kKBytes;
+        for (int bx = 0; bx < p.boxes_per_stage; ++bx) {
+          const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
+          if (bt) {
+            const int page = key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+            const int slot = key0 & (p.page_size - 1);
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+              const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
+              tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, slot, page);
+              tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, slot, page);
+            }
+          } else {
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+              const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
+              tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
+              tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- consumers --
+    // Q fragments (A operand, 16 rows x D) for all D/16 k-steps.
+    uint32_t qf[D / 16][4];
+    {
+      const uint32_t qbase = smem_u32(sQ);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        // matrices: (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15)
+        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int mcol = ks * 16 + (lane >> 4) * 8;
+        ldsm_x4(qbase + (mrow * D + mcol) * 2, qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+      }
+    }
+    // Rows this thread holds in the C fragments: g0 = lane/4, g1 = lane/4 + 8.
+    const int r0 = lane >> 2, r1 = r0 + 8;
+    const int ip0 = (r0 / p.group) + sk - sq;   // bottom-right aligned positions
+    const int ip1 = (r1 / p.group) + sk - sq;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    bool ok = true;
+    for (int st = first_stage; st < n_stages; ++st) {
+      const int it = st - first_stage;
+      const int slot_i = it % kDecStages;
+      ok = mbar_wait(smem_u32(full + slot_i), (it / kDecStages) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
+      uint8_t *vd = kd + Cfg::kKBytes;
+      const int kw0 = warp * 16;                               // this warp's 16 keys in the stage
+      const int key_base = key_lo + st * kDecStageKeys + kw0;  // sequence-local key of row kw0
+      // Clear V rows of keys outside [key_lo, key_hi) (0 * NaN would be NaN).
+      if (key_base + 16 > key_hi) {
+        for (int e = lane; e < 16 * NCB * 8; e += 32) {
+          const int rr = e / (NCB * 8), rest = e % (NCB * 8);
+          const int cb = rest / 8, ch = rest % 8;
+          if (key_base + rr >= key_hi)
+            *reinterpret_cast<uint4 *>(vd + cb * kDecStageKeys * 128 + (kw0 + rr) * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // S = Q K^T for 16 keys: two n-tiles of 8 keys.
+      float s[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        // matrices: (keys 0-7, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 0-7), (keys 8-15, dims 8-15)
+        const int krow = kw0 + (lane & 7) + (lane >> 4) * 8;
+        const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
+        const int cb = dim >> 6, ch = (dim & 63) >> 3;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(kd + cb * kDecStageKeys * 128) + sw128(krow, ch), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qf[ks], b0, b1);
+        mma_bf16_16816(s[1], qf[ks], b2, b3);
+      }
+      // Scale, mask, online softmax for rows r0 and r1.
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = key_base + n * 8 + (lane & 3) * 2 + e;
+          const bool in = j < key_hi;
+          bool ok0 = in && r0 < rows, ok1 = in && r1 < rows;
+          if (p.causal) { ok0 = ok0 && j <= ip0; ok1 = ok1 && j <= ip1; }
+          if (p.window > 0) {
+            if (p.causal) { ok0 = ok0 && ip0 - j < p.window; ok1 = ok1 && ip1 - j < p.window; }
+            else { ok0 = ok0 && abs(ip0 - j) < p.window; ok1 = ok1 && abs(ip1 - j) < p.window; }
+          }
+          s[n][e] = ok0 ? s[n][e] * p.scale_log2 : -INFINITY;
+          s[n][2 + e] = ok1 ? s[n][2 + e] * p.scale_log2 : -INFINITY;
+          mx0 = fmaxf(mx0, s[n][e]);
+          mx1 = fmaxf(mx1, s[n][2 + e]);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float a0 = ex2(m0 - mu0), a1 = ex2(m1 - mu1);   // 0 when the old max is -inf
+      m0 = mn0;
+      m1 = mn1;
+      float ps[2][4];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        ps[n][0] = ex2(s[n][0] - mu0);
+        ps[n][1] = ex2(s[n][1] - mu0);
+        ps[n][2] = ex2(s[n][2] - mu1);
+        ps[n][3] = ex2(s[n][3] - mu1);
+        sum0 += ps[n][0] + ps[n][1];
+        sum1 += ps[n][2] + ps[n][3];
+      }
+      l0 = l0 * a0 + sum0;   // per-thread partial sums; reduced across the quad at the end
+      l1 = l1 * a1 + sum1;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(ps[0][0], ps[0][1]);
+      pa[1] = pack_bf16x2(ps[0][2], ps[0][3]);
+      pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
+      pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
+      // O += P V : D/8 n-tiles of 8 dims, one k-step of 16 keys.
+#pragma unroll
+      for (int nd = 0; nd < D / 16; ++nd) {
+        // matrices: (keys 0-7, dims 0-7), (keys 8-15, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 8-15)
+        const int krow = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int dim = nd * 16 + (lane >> 4) * 8;
+        const int cb = dim >> 6, ch = (dim & 63) >> 3;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_u32(vd + cb * kDecStageKeys * 128) + sw128(krow, ch), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * nd], pa, b0, b1);
+        mma_bf16_16816(o[2 * nd + 1], pa, b2, b3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
+    }
+
+    // Reduce l over the quad (the 4 lanes sharing a row).
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    // Merge the four warps' (m, l, O) through shared memory (stage buffers are
+    // free once every warp has passed its last stage).
+    float *red_o = reinterpret_cast<float *>(stages);                     // [4][16][D]
+    float *red_ml = reinterpret_cast<float *>(stages + kDecWarps * kDecRows * D * 4);  // [4][16][2]
+    asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
+    if (ok) {
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        const int c = n * 8 + (lane & 3) * 2;
+        red_o[(warp * kDecRows + r0) * D + c] = o[n][0];
+        red_o[(warp * kDecRows + r0) * D + c + 1] = o[n][1];
+        red_o[(warp * kDecRows + r1) * D + c] = o[n][2];
+        red_o[(warp * kDecRows + r1) * D + c + 1] = o[n][3];
+      }
+      if ((lane & 3) == 0) {
+        red_ml[(warp * kDecRows + r0) * 2] = m0;
+        red_ml[(warp * kDecRows + r0) * 2 + 1] = l0;
+        red_ml[(warp * kDecRows + r1) * 2] = m1;
+        red_ml[(warp * kDecRows + r1) * 2 + 1] = l1;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
+    if (ok) {
+      // 128 threads: thread -> (row = tid / 8, 16-dim slice = tid % 8 ... for D=128)
+      constexpr int kPerRow = kDecWarps * 32 / kDecRows;   // 8 threads per row
+      constexpr int kSlice = D / kPerRow;
+      const int row = threadIdx.x / kPerRow, sl = threadIdx.x % kPerRow;
+      if (row < rows) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_ml[(w * kDecRows + row) * 2]);
+        float wgt[kDecWarps], L = 0.f;
+        const float Mu = M == -INFINITY ? 0.f : M;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          wgt[w] = ex2(red_ml[(w * kDecRows + row) * 2] - Mu);
+          L += wgt[w] * red_ml[(w * kDecRows + row) * 2 + 1];
+        }
+        const bool has = L > 0.f;
+        const float inv = has ? 1.f / L : 0.f;
+        const int tq = row / p.group, h = hk * p.group + row % p.group;
+        const int64_t t = (int64_t)qa + tq;
+        const float lse_v = has ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        if (p.o_part) {
+          float *dst = p.o_part + (((int64_t)split * p.total_q + t) * p.hq + h) * D + sl * kSlice;
+#pragma unroll
+          for (int d = 0; d < kSlice; d += 4) {
+            float4 v;
+            float *vv = reinterpret_cast<float *>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float acc = 0.f;
+#pragma unroll
+              for (int w = 0; w < kDecWarps; ++w) acc += wgt[w] * red_o[(w * kDecRows + row) * D + sl * kSlice + d + e];
+              vv[e] = acc * inv;
+            }
+            *reinterpret_cast<float4 *>(dst + d) = v;
+          }
+          if (sl == 0) p.lse_part[((int64_t)split * p.hq + h) * p.total_q + t] = lse_v;
+        } else {
+          __nv_bfloat16 *dst = p.out + t * p.out_stride_t + (int64_t)h * p.out_stride_h + sl * kSlice;
+#pragma unroll
+          for (int d = 0; d < kSlice; d += 2) {
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) {
+              acc0 += wgt[w] * red_o[(w * kDecRows + row) * D + sl * kSlice + d];
+              acc1 += wgt[w] * red_o[(w * kDecRows + row) * D + sl * kSlice + d + 1];
+            }
+            *reinterpret_cast<uint32_t *>(dst + d) = pack_bf16x2(acc0 * inv, acc1 * inv);
+          }
+          if (sl == 0 && p.lse) p.lse[(int64_t)h * p.total_q + t] = lse_v;
+        }
+      }
+    }
+  }
+}
+
+// Combine kernel: one warp per (row t, head h).
+template <int D>
+__global__ void __launch_bounds__(256) fa_combine_kernel(const float *__restrict__ o_part,
+                                                         const float *__restrict__ lse_part, int num_splits,
+                                                         int64_t n_rows, int hq, __nv_bfloat16 *__restrict__ out,
+                                                         float *__restrict__ lse) {
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= n_rows * hq) return;
+  const int64_t t = wid / hq;
+  const int h = (int)(wid % hq);
+  float M = -INFINITY;
+  for (int s = lane; s < num_splits; s += 32) M = fmaxf(M, lse_part[((int64_t)s * hq + h) * n_rows + t]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float L = -INFINITY;
+  if (M != -INFINITY) {
+    float den = 0.f;
+    for (int s = lane; s < num_splits; s += 32) den += __expf(lse_part[((int64_t)s * hq + h) * n_rows + t] - M);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    L = M + __logf(den);
+    for (int s = 0; s < num_splits; ++s) {
+      const float ls = lse_part[((int64_t)s * hq + h) * n_rows + t];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - L);
+      const float *src = o_part + (((int64_t)s * n_rows + t) * hq + h) * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(src + e);
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+      }
+    }
+  }
+  __nv_bfloat16 *dst = out + (t * hq + h) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e], acc[e + 1]);
+  if (lse && lane == 0) lse[(int64_t)h * n_rows + t] = L;
+}
+
+}  // namespace fa

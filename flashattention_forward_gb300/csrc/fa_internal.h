@@ -1,0 +1,47 @@
+// fa_internal.h -- launch descriptors shared by the C-ABI front end and the
+// kernel translation units (one per head-dim family, compiled in parallel).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_decode.cuh"
+#include "fa_prefill.cuh"
+
+namespace fa {
+
+struct PrefillLaunch {
+  CUtensorMap tm_q, tm_k, tm_v;
+  PrefillParams p;
+  int paged, fp8, mod;
+  dim3 grid;
+  cudaStream_t stream;
+};
+
+struct DecodeLaunch {
+  CUtensorMap tm_k, tm_v;
+  DecodeParams p;
+  dim3 grid;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_prefill_64_64(const PrefillLaunch &L);
+cudaError_t launch_prefill_128_128(const PrefillLaunch &L);
+cudaError_t launch_prefill_192_128(const PrefillLaunch &L);
+cudaError_t launch_decode(int d, const DecodeLaunch &L);
+cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
+                           int dv, void *out, float *lse, cudaStream_t stream);
+
+// Sets the dynamic shared-memory attribute once per (kernel, device).
+template <typename K>
+cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long *done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
+  return e;
+}
+
+}  // namespace fa

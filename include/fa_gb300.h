@@ -1,0 +1,193 @@
+/*
+ * fa_gb300.h -- C ABI of the GB300 (sm_103a) attention forward library.
+ *
+ * One operation, in several entry points: the FlashAttention forward pass
+ * over packed variable-length sequences and a paged KV cache, with per-row
+ * log-sum-exp output.  For query row i of sequence b and head h:
+ *
+ *   out[i]  = sum_j softmax_j(s_ij) * v_j        over the keys j the mask allows
+ *   lse[i]  = log sum_j exp(s_ij)                (natural log)
+ *   s_ij    = scale * <q_i, k_j>, then soft-cap, then ALiBi
+ *
+ * The passages that define it:
+ *  - tiled QK^T, online (running max / running sum) softmax, PV and the
+ *    attention-domain LSE = M + log(L) over packed cu_seqlens tensors
+ *    [total_tokens, H, D]: RL-Kernel PR #237 "SM90 TMA + mma.sync
+ *    FlashAttention", commit texts and summary;
+ *  - the LSE written also for fully masked rows, and the split-K combine
+ *    m_max*ln2 + ln(den): FlyDSL PR #844 "Add forward LSE output", Changes;
+ *  - paged KV addressed through block_table, FP8 e4m3 KV with scales,
+ *    Q/K head dim 192 with V/O 128 at native BF16 width, bottom-right causal
+ *    mask, offsets above 4 GiB: FlyDSL PR #1066 "Support paged FP8 Flash
+ *    attention with asymmetric K/V head dim", overview, review and PR
+ *    description;
+ *  - per-token fp8 scale max|row|/448, ALiBi, SoftCap, SlidingWindow and
+ *    128x128 block sparsity: fkl_python PR #7 "flash_attention: prologue
+ *    fusion, mma tensor cores, fp8 KV cache, flex attention + block
+ *    sparsity", commits and summary.
+ *
+ * Conventions for every entry point:
+ *  - Pointers inside fa_tensor_t are DEVICE pointers on the current CUDA
+ *    device, owned by the caller.  The library never frees them and keeps no
+ *    reference after the call returns.
+ *  - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t
+ *    passed as void*, NULL = legacy default stream) and the call returns.
+ *    The library performs no host<->device copy, no device synchronisation
+ *    and no memory allocation inside fa_fwd_varlen / fa_combine.
+ *  - All validation happens on the host before any launch, using the shapes
+ *    in fa_tensor_t and the host scalars in fa_launch_t.  On any non-OK
+ *    status nothing has been enqueued; fa_last_error() describes the cause.
+ *  - Device-side waits are bounded.  A wait that runs out, or an index that
+ *    the kernel finds out of range, records a code in a per-device error word
+ *    read by fa_get_device_error(); the kernel then returns early.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,    /* malformed shape, dtype, stride or pointer */
+    FA_ERR_UNSUPPORTED = 2,    /* valid request outside the compiled variant set */
+    FA_ERR_OVERFLOW = 3,       /* a size that does not fit the index types */
+    FA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+    FA_ERR_DEVICE_TIMEOUT = 5, /* (device word) a bounded wait ran out */
+    FA_ERR_DEVICE_BOUNDS = 6   /* (device word) an index was out of range */
+} fa_status_t;
+
+typedef enum { FA_BF16 = 0, FA_E4M3 = 1, FA_F32 = 2, FA_I32 = 3, FA_U8 = 4 } fa_dtype_t;
+
+/* A strided device tensor.  Strides are in ELEMENTS; shape[ndim..4] unused. */
+typedef struct {
+    void *data;
+    int32_t dtype;       /* fa_dtype_t */
+    int32_t ndim;
+    int64_t shape[5];
+    int64_t stride[5];
+} fa_tensor_t;
+
+/* Score modifier (fkl_python PR #7, flex commit): kind 0 none, 1 ALiBi
+ * (s -= alibi_slope * |i' - j|, i' = i + Sk - Sq), 2 soft-cap
+ * (s = softcap * tanh(s / softcap), on the scaled score, before ALiBi). */
+typedef struct {
+    int32_t kind;
+    float alibi_slope;
+    float softcap;
+} fa_score_mod_t;
+
+/* 128x128 block-sparsity mask, uint8 [num_seqs * Hq][n_qblk][n_kblk],
+ * contiguous; block (qb, kb) of sequence b, head h is active when
+ * data[((b*Hq + h)*n_qblk + qb)*n_kblk + kb] != 0, with qb = i/128 and
+ * kb = j/128 in sequence-local indices.  blk_q = blk_k = 128 only. */
+typedef struct {
+    const uint8_t *data;
+    int32_t n_qblk, n_kblk, blk_q, blk_k;
+} fa_block_mask_t;
+
+/* Host-side scalars, so that no length is read back from the device.
+ * num_splits: 0 = single pass; > 0 = split-KV over that many key ranges
+ * followed by the combine (needs `workspace` of fa_fwd_workspace_bytes()). */
+typedef struct {
+    int32_t num_seqs;
+    int32_t max_seqlen_q;
+    int32_t max_seqlen_k;
+    int32_t num_splits;
+    int64_t total_q;
+    int64_t total_k;
+    void *workspace;         /* device, 256-byte aligned, caller-owned */
+    size_t workspace_bytes;
+} fa_launch_t;
+
+/*
+ * fa_fwd_varlen -- the attention forward pass.
+ *
+ *  q            bf16 [T_q, Hq, Dk], last dim contiguous, row stride a multiple
+ *               of 8 elements.
+ *  k_cache      paged: [N_pg, P_s, Hkv, Dk]; packed (block_table NULL):
+ *               [T_k, Hkv, Dk].  bf16 or e4m3.  Last three dims contiguous.
+ *  v_cache      same layout and dtype with Dv (Dv may differ from Dk).
+ *  block_table  int32 [num_seqs, max_pages], or NULL for packed K/V.  Entries
+ *               for pages past a sequence's length are never read.
+ *  cu_seqlens_q int32 [num_seqs + 1], prefix sums of query lengths.
+ *  cu_seqlens_k int32 [num_seqs + 1], prefix sums of key lengths (row offsets
+ *               into packed K/V; with a block table only their differences,
+ *               the lengths, are used).
+ *  k_scale      fp32 per token and kv head, [N_pg, P_s, Hkv] (paged) or
+ *  v_scale      [T_k, Hkv] (packed); required for e4m3, must be NULL for bf16.
+ *               The dequantised key is e4m3(k) * k_scale (same for v).
+ *  out          bf16 [T_q, Hq, Dv], contiguous, caller-allocated; rows whose
+ *               allowed key set is empty are written as 0.
+ *  lse          fp32 [Hq, T_q] contiguous, or NULL to skip; -inf for rows
+ *               with no allowed key.
+ *  softmax_scale  multiplies <q, k>.
+ *  causal       non-zero: key j visible iff j <= i + Sk - Sq (bottom-right).
+ *  window       > 0: sliding window of `window` keys including the diagonal
+ *               (causal: i' - j < window; otherwise |i' - j| < window).
+ *  score_mod    NULL or fa_score_mod_t.
+ *  block_mask   NULL or fa_block_mask_t.
+ *  page_size    tokens per page when paged: a power of two, 16 ... 256.
+ *  launch       host scalars (required).
+ *  stream       cudaStream_t.
+ *
+ * Supported head dims: (Dk, Dv) in {(64,64), (128,128), (192,128)}.  Hq must
+ * be a multiple of Hkv (query head h reads kv head h / (Hq/Hkv)).
+ * Returns FA_OK or an error status; see fa_last_error().
+ */
+fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache,
+                          const fa_tensor_t *v_cache, const fa_tensor_t *block_table,
+                          const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
+                          const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
+                          fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
+                          int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
+                          const fa_block_mask_t *block_mask, int32_t page_size,
+                          const fa_launch_t *launch, void *stream);
+
+/*
+ * Workspace size in bytes for split-KV with `num_splits` key ranges: partial
+ * outputs fp32 [num_splits, T_q, Hq, Dv] and partial LSEs fp32
+ * [num_splits, Hq, T_q], each 256-byte aligned.  0 when num_splits <= 0.
+ */
+size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int32_t dv,
+                              int32_t num_splits);
+
+/*
+ * Recommended split count for a problem (0 = single pass).  Split-KV applies
+ * when few query rows share each kv head (decode: max_seqlen_q * Hq/Hkv <= 16)
+ * and keys are long; the count spreads the key ranges over the SMs.
+ */
+int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                              int32_t hq, int32_t hkv, int32_t page_size);
+
+/*
+ * fa_combine -- merge of partial results over disjoint key ranges (the
+ * split-KV combine; FlyDSL PR #844, Changes: m_max*ln2 + ln(den)):
+ *   LSE = ln sum_s exp(LSE_s),  out = sum_s exp(LSE_s - LSE) * O_s,
+ * partials with LSE_s = -inf are skipped; all -inf gives out 0, LSE -inf.
+ *  o_part   fp32 [num_splits, n_rows, Hq, Dv] contiguous (n_rows = T_q)
+ *  lse_part fp32 [num_splits, Hq, n_rows] contiguous
+ *  out      bf16 [n_rows, Hq, Dv] contiguous;  lse fp32 [Hq, n_rows] or NULL.
+ */
+fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_splits,
+                       int64_t n_rows, int32_t hq, int32_t dv, void *out_bf16, float *lse,
+                       void *stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *fa_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word into *code (FA_OK when no kernel recorded a problem). */
+fa_status_t fa_get_device_error(void *stream, int32_t *code);
+
+/* Library version string. */
+const char *fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

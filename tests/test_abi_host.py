@@ -1,0 +1,161 @@
+"""Host-only checks of the C-ABI library: it loads, exports every entry point
+that include/fa_gb300.h declares, and rejects malformed calls with a status
+code before touching the GPU (validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import flashattention_forward_gb300 as fa
+from flashattention_forward_gb300 import build as fa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fa_build.build()
+    return fa.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported(L):
+    syms = declared_symbols()
+    assert "fa_fwd_varlen" in syms and "fa_combine" in syms
+    for s in syms:
+        assert hasattr(L, s), s
+    assert set(syms) <= set(fa.EXPORTED) | set(syms)
+
+
+def test_version_and_last_error(L):
+    assert "sm_103a" in fa.version()
+    assert isinstance(L.fa_last_error(), bytes)
+
+
+def test_workspace_bytes_and_default_splits(L):
+    assert fa.workspace_bytes(4, 0, 8, 128, 4) == 0
+    assert fa.workspace_bytes(4, 10, 8, 128, 0) == 0
+    n = fa.workspace_bytes(64, 64, 32, 128, 16)
+    assert n >= 16 * 64 * 32 * 128 * 4 + 16 * 32 * 64 * 4 and n % 256 == 0
+    assert fa.default_splits(64, 1, 8192, 32, 8, 16) == 16        # decode shape
+    assert fa.default_splits(8, 2048, 2048, 16, 16, 0) == 0       # prefill shape
+    assert fa.default_splits(64, 8, 8192, 32, 8, 16) == 0         # 8 * 4 rows > 16
+
+
+def _t(data, dtype, shape, stride=None):
+    t = fa.Tensor()
+    t.data = data
+    t.dtype = dtype
+    t.ndim = len(shape)
+    if stride is None:
+        stride, s = [], 1
+        for x in reversed(shape):
+            stride.insert(0, s)
+            s *= x
+    for i, (a, b) in enumerate(zip(shape, stride)):
+        t.shape[i] = a
+        t.stride[i] = b
+    return t
+
+
+FAKE = 1 << 20  # never dereferenced: validation fails first
+
+
+def _call(L, **over):
+    T, H, D = 256, 4, 64
+    args = dict(
+        q=_t(FAKE, fa.FA_BF16, [T, H, D]), k=_t(FAKE * 2, fa.FA_BF16, [T, H, D]),
+        v=_t(FAKE * 3, fa.FA_BF16, [T, H, D]), bt=None,
+        cq=_t(FAKE * 4, fa.FA_I32, [3]), ck=_t(FAKE * 5, fa.FA_I32, [3]), ks=None, vs=None,
+        out=_t(FAKE * 6, fa.FA_BF16, [T, H, D]), lse=_t(FAKE * 7, fa.FA_F32, [H, T]),
+        scale=0.125, causal=1, window=0, mod=None, bm=None, page=0,
+        launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=0, total_q=T, total_k=T))
+    args.update(over)
+    r = lambda x: None if x is None else ctypes.byref(x)
+    st = L.fa_fwd_varlen(r(args["q"]), r(args["k"]), r(args["v"]), r(args["bt"]), r(args["cq"]), r(args["ck"]),
+                         r(args["ks"]), r(args["vs"]), r(args["out"]), r(args["lse"]), args["scale"],
+                         args["causal"], args["window"], r(args["mod"]), r(args["bm"]), args["page"],
+                         r(args["launch"]), None)
+    return st, L.fa_last_error().decode()
+
+
+@pytest.mark.parametrize("over,status,words", [
+    (dict(q=_t(FAKE, fa.FA_F32, [256, 4, 64])), fa.FA_ERR_INVALID_ARG, "dtype"),
+    (dict(q=_t(FAKE, fa.FA_BF16, [256, 4, 96]), k=_t(FAKE * 2, fa.FA_BF16, [256, 4, 96]),
+          v=_t(FAKE * 3, fa.FA_BF16, [256, 4, 96]), out=_t(FAKE * 6, fa.FA_BF16, [256, 4, 96])),
+     fa.FA_ERR_UNSUPPORTED, "not compiled"),
+    (dict(k=_t(FAKE * 2, fa.FA_BF16, [256, 3, 64]), v=_t(FAKE * 3, fa.FA_BF16, [256, 3, 64])),
+     fa.FA_ERR_INVALID_ARG, "multiple of Hkv"),
+    (dict(cq=_t(FAKE * 4, fa.FA_I32, [4])), fa.FA_ERR_INVALID_ARG, "num_seqs+1"),
+    (dict(out=_t(FAKE * 6, fa.FA_BF16, [256, 4, 64], [512, 64, 1])), fa.FA_ERR_INVALID_ARG, "contiguous"),
+    (dict(lse=_t(FAKE * 7, fa.FA_F32, [256, 4])), fa.FA_ERR_INVALID_ARG, "lse must be"),
+    (dict(lse=_t(FAKE * 6, fa.FA_F32, [4, 256])), fa.FA_ERR_INVALID_ARG, "alias"),
+    (dict(q=_t(FAKE, fa.FA_BF16, [256, 4, 64], [256, 64, 2])), fa.FA_ERR_INVALID_ARG, "contiguous last dim"),
+    (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=100, total_k=256)),
+     fa.FA_ERR_INVALID_ARG, "total_q"),
+    (dict(ks=_t(FAKE * 8, fa.FA_F32, [256, 4])), fa.FA_ERR_INVALID_ARG, "only valid with an e4m3"),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG, "finite"),
+    (dict(mod=fa.ScoreMod(kind=2, softcap=0.0)), fa.FA_ERR_INVALID_ARG, "softcap"),
+    (dict(mod=fa.ScoreMod(kind=7)), fa.FA_ERR_INVALID_ARG, "kind"),
+    (dict(bm=fa.BlockMask(data=FAKE * 9, n_qblk=1, n_kblk=1, blk_q=64, blk_k=64)), fa.FA_ERR_UNSUPPORTED, "128x128"),
+    (dict(bm=fa.BlockMask(data=FAKE * 9, n_qblk=0, n_kblk=1, blk_q=128, blk_k=128)), fa.FA_ERR_INVALID_ARG, "cover"),
+    (dict(launch=None), fa.FA_ERR_INVALID_ARG, "launch"),
+])
+def test_validation_rejects_before_launch(L, over, status, words):
+    st, msg = _call(L, **over)
+    assert st == status, msg
+    assert words in msg, msg
+
+
+def test_paged_validation(L):
+    bt = _t(FAKE * 10, fa.FA_I32, [2, 8])
+    k = _t(FAKE * 2, fa.FA_BF16, [32, 16, 4, 64])
+    v = _t(FAKE * 3, fa.FA_BF16, [32, 16, 4, 64])
+    st, msg = _call(L, bt=bt, k=k, v=v, page=24)
+    assert st == fa.FA_ERR_UNSUPPORTED and "page_size" in msg
+    st, msg = _call(L, bt=bt, k=k, v=v, page=32)
+    assert st == fa.FA_ERR_INVALID_ARG and "page_size" in msg
+    st, msg = _call(L, bt=_t(FAKE * 10, fa.FA_I32, [3, 8]), k=k, v=v, page=16)
+    assert st == fa.FA_ERR_INVALID_ARG and "block_table" in msg
+    st, msg = _call(L, bt=_t(FAKE * 10, fa.FA_I32, [2, 4]), k=k, v=v, page=16)
+    assert st == fa.FA_ERR_INVALID_ARG and "capacity" in msg
+
+
+def test_e4m3_needs_scales(L):
+    k = _t(FAKE * 2, fa.FA_E4M3, [256, 4, 64])
+    v = _t(FAKE * 3, fa.FA_E4M3, [256, 4, 64])
+    st, msg = _call(L, k=k, v=v)
+    assert st == fa.FA_ERR_INVALID_ARG and "scale" in msg
+
+
+def test_overflow_guard(L):
+    big = (1 << 31)
+    st, msg = _call(L, q=_t(FAKE, fa.FA_BF16, [big, 4, 64]), out=_t(FAKE * 6, fa.FA_BF16, [big, 4, 64]),
+                    lse=None, launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=big,
+                                               total_k=256))
+    assert st == fa.FA_ERR_OVERFLOW, msg
+
+
+def test_split_limits(L):
+    st, msg = _call(L, launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=4,
+                                        total_q=256, total_k=256))
+    assert st == fa.FA_ERR_UNSUPPORTED and "split-KV" in msg
+
+
+def test_combine_validation(L):
+    assert L.fa_combine(FAKE, FAKE, 0, 4, 4, 128, FAKE, None, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_combine(FAKE, FAKE, 2, 4, 4, 96, FAKE, None, None) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_combine(FAKE, FAKE, 2, 0, 4, 128, FAKE, None, None) == fa.FA_OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        fa.lib()

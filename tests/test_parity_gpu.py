@@ -1,0 +1,207 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on
+the same seeded inputs.  Tolerances: max |dout| <= 1e-2, |dLSE| <= 1e-3,
+-inf LSE and zero rows matched exactly, indexing bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs as fi
+import oracle
+from fa_testlib import compare, compare_units, host, run_gpu, sample_units, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from flashattention_forward_gb300 import build
+    build.build()
+    yield
+    import flashattention_forward_gb300 as fa
+    assert fa.device_error() == 0
+
+
+def check(p, **kw):
+    o, l = host(*run_gpu(p, **kw))
+    ro, rl = oracle.forward(p)
+    return compare(o, l, ro, rl)
+
+
+# ----------------------------------------------------------- configurations --
+
+def test_config1_dense_causal():
+    p = fi.config1()
+    o, l = host(*run_gpu(p))
+    ro, rl = oracle.forward(p)
+    compare(o, l, ro, rl)
+    # [T, H, D] packed == [2, 128, 4, 64]; LSE [H, T] viewed as [2, 4, 128]
+    assert o.reshape(2, 128, 4, 64).shape == (2, 128, 4, 64)
+    assert l.reshape(4, 2, 128).transpose(1, 0, 2).shape == (2, 4, 128)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_config2_varlen_prefill(causal):
+    check(fi.config2(causal=causal))
+
+
+def test_config3_paged_decode_split_kv():
+    p = fi.config3()
+    o, l = host(*run_gpu(p, num_splits=None))
+    ro, rl = oracle.forward(p)
+    compare(o, l, ro, rl)
+
+
+@pytest.mark.parametrize("run", fi.CONFIG5_RUNS)
+def test_config5_flex_sampled(run):
+    p = fi.config5(run)
+    o, l = host(*run_gpu(p))
+    units = sample_units(p, 3000, seed=5)
+    ro, rl = oracle.forward(p, units=units)
+    compare_units(o, l, units, ro, rl)
+
+
+# --------------------------------------------------------------- edge cases --
+
+EDGE = [
+    dict(lens_q=[1, 127, 128, 129, 300], hq=4, dk=64),
+    dict(lens_q=[5, 0, 77, 256], lens_k=[300, 0, 77, 500], hq=4, hkv=2, dk=128, causal=True),
+    dict(lens_q=[200, 64], lens_k=[100, 10], hq=2, dk=128, causal=True),          # Sq > Sk: masked rows
+    dict(lens_q=[0, 0, 3], lens_k=[0, 5, 0], hq=2, dk=64),                        # empty sequences
+    dict(lens_q=[130, 260], lens_k=[400, 260], hq=8, hkv=1, dk=128, causal=True, window=100),
+    dict(lens_q=[130, 260], lens_k=[400, 260], hq=4, dk=64, window=70),
+    dict(lens_q=[300, 129], lens_k=[300, 400], hq=4, dk=128, mod="alibi", alibi_slope=0.0625, causal=True),
+    dict(lens_q=[300, 129], lens_k=[300, 400], hq=4, dk=128, mod="softcap", softcap=2.0),
+    dict(lens_q=[300, 129], lens_k=[330, 400], hq=4, hkv=2, dk=128, block_mask_density=0.5),
+    dict(lens_q=[257, 33], lens_k=[600, 33], hq=4, hkv=4, dk=192, dv=128, causal=True),
+    dict(lens_q=[257, 33], lens_k=[600, 33], hq=4, hkv=2, dk=192, dv=128, page_size=64, spare_pages=3),
+]
+
+
+@pytest.mark.parametrize("case", range(len(EDGE)))
+def test_edge_cases_packed_and_paged(case):
+    kw = dict(EDGE[case])
+    lens_q = kw.pop("lens_q")
+    lens_k = kw.pop("lens_k", None)
+    check(fi.make_problem(lens_q, lens_k, seed=100 + case, **kw))
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_page_sizes_with_poisoned_slots(page_size, causal):
+    p = fi.make_problem([70, 300, 1, 129], [200, 300, 1000, 129], hq=8, hkv=2, dk=128, seed=7,
+                        page_size=page_size, spare_pages=5, causal=causal)
+    check(p)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 33])
+@pytest.mark.parametrize("sq,paged", [(1, True), (2, True), (4, False), (1, False)])
+def test_decode_split_counts(splits, sq, paged):
+    lens_k = [1, 63, 64, 65, 700, 2049, 3000]
+    p = fi.make_problem([sq] * len(lens_k), lens_k, hq=8, hkv=2, dk=128, seed=splits,
+                        page_size=16 if paged else 0, spare_pages=4, causal=sq > 1)
+    check(p, num_splits=splits)
+
+
+def test_decode_d64_window():
+    p = fi.make_problem([1, 1, 1], [500, 90, 1300], hq=16, hkv=1, dk=64, seed=3, page_size=32, window=200)
+    check(p, num_splits=4)
+
+
+def test_combine_entry_point_matches_oracle_merge():
+    import flashattention_forward_gb300 as fa
+    rng = np.random.default_rng(0)
+    S, n, H, D = 5, 37, 3, 128
+    o_part = rng.standard_normal((S, n, H, D)).astype(np.float32)
+    lse_part = (rng.standard_normal((S, H, n)) * 3).astype(np.float32)
+    lse_part[1, 0, :] = -np.inf
+    lse_part[:, 2, 5] = -np.inf                  # a row with every split empty
+    out, lse = fa.combine(torch.from_numpy(o_part).cuda(), torch.from_numpy(lse_part).cuda())
+    out, lse = host(out, lse)
+    # oracle merge works on [S, rows, D] with rows = (t, h) in t-major order
+    ro, rl = oracle.combine(o_part.reshape(S, n * H, D).astype(np.float64),
+                            lse_part.transpose(0, 2, 1).reshape(S, n * H).astype(np.float64))
+    compare(out, lse, ro.reshape(n, H, D), rl.reshape(n, H).T)
+
+
+# -------------------------------------------------------- indexing bit-exact --
+
+def _integer_values(p):
+    """V rows filled with small integers that encode (token, head, dim):
+    exactly representable in bf16, so a single visible key reproduces them bit-for-bit."""
+    shape = p.v.shape
+    idx = np.indices(shape).reshape(len(shape), -1)
+    vals = ((idx[0] * 7 + idx[-2] * 3 + idx[-1]) % 200 - 100).astype(np.float32).reshape(shape)
+    return p.replace(v=fi.bf16_bits(vals))
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_single_visible_key_is_bit_exact(paged):
+    """Causal window 1 leaves only key i' for each row: out must equal that V row exactly."""
+    p = fi.make_problem([40, 300, 7], [90, 300, 520], hq=8, hkv=2, dk=128, seed=11, causal=True,
+                        window=1, page_size=16 if paged else 0, spare_pages=6)
+    p = _integer_values(p)
+    o, l = run_gpu(p)
+    torch.cuda.synchronize()
+    got = o.view(torch.int16).cpu().numpy().view(np.uint16)
+    ro, _ = oracle.forward(p)
+    exp = fi.bf16_bits(ro.astype(np.float32))
+    assert np.array_equal(got, exp)
+
+
+def test_decode_single_key_bit_exact():
+    p = fi.make_problem([1] * 6, [1] * 6, hq=8, hkv=2, dk=128, seed=12, page_size=16, spare_pages=3)
+    p = _integer_values(p)
+    for splits in (1, 3):
+        o, _ = run_gpu(p, num_splits=splits)
+        torch.cuda.synchronize()
+        got = o.view(torch.int16).cpu().numpy().view(np.uint16)
+        ro, _ = oracle.forward(p)
+        assert np.array_equal(got, fi.bf16_bits(ro.astype(np.float32)))
+
+
+def test_permuted_block_table_is_bit_identical():
+    """Permuting pages together with the block table gives bit-identical output."""
+    p = fi.make_problem([100, 260], [700, 260], hq=4, hkv=2, dk=128, seed=13, page_size=16, spare_pages=8,
+                        causal=True)
+    o1, l1 = host(*run_gpu(p))
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(p.k.shape[0])          # new position of each old page
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    k2 = np.empty_like(p.k)
+    v2 = np.empty_like(p.v)
+    k2[perm] = p.k
+    v2[perm] = p.v
+    bt2 = np.where(p.block_table >= 0, perm[np.maximum(p.block_table, 0)], -1).astype(np.int32)
+    o2, l2 = host(*run_gpu(p.replace(k=k2, v=v2, block_table=bt2)))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ------------------------------------------------ streams, guards, determinism --
+
+def test_side_stream_and_determinism():
+    p = fi.make_problem([300, 129, 64], [300, 500, 64], hq=8, hkv=2, dk=128, seed=14, causal=True)
+    t = to_device(p)
+    o1, l1 = host(*run_gpu(p, t))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(20_000_000)             # keep the side stream busy first
+        o2, l2 = run_gpu(p, t, stream=s)
+    s.synchronize()
+    o2, l2 = host(o2, l2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_guard_bands_untouched():
+    p = fi.make_problem([129, 0, 77], [300, 5, 77], hq=4, hkv=4, dk=64, seed=15, causal=True)
+    t = to_device(p)
+    big_o = torch.full((p.total_q + 3, p.hq, p.dv), 1024.0, dtype=torch.bfloat16, device="cuda")
+    big_l = torch.full((p.hq + 1, p.total_q), 777.0, dtype=torch.float32, device="cuda")
+    o, l = run_gpu(p, t, out=big_o[:p.total_q], lse=big_l[:p.hq])
+    torch.cuda.synchronize()
+    assert torch.all(big_o[p.total_q:] == 1024.0)
+    assert torch.all(big_l[p.hq:] == 777.0)
+    ro, rl = oracle.forward(p)
+    compare(*host(o, l), ro, rl)
