@@ -252,7 +252,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--profile", default=None,
+                    help="run only `warmup + steps` launches of one workload (for ncu captures): "
+                         "varlen_causal, varlen_noncausal, decode, dense, flex_<run>")
     args = ap.parse_args()
+    if args.profile:
+        return profile_only(args.profile, args.warmup, args.steps)
     warmup = max(3, args.warmup)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -412,6 +417,33 @@ def other_workloads(dev, warmup, steps, flush, pk):
         del t
         torch.cuda.empty_cache()
     return res
+
+
+def profile_only(name, warmup, steps):
+    """Launch one workload warmup + steps times, nothing else (for ncu)."""
+    import flashattention_forward_gb300 as fa
+    from flashattention_forward_gb300 import build as fa_build
+    fa_build.build()
+    dev = torch.device("cuda", 0)
+    if name == "varlen_causal":
+        p, splits = fi.config2(causal=True), 0
+    elif name == "varlen_noncausal":
+        p, splits = fi.config2(causal=False), 0
+    elif name == "decode":
+        p, splits = fi.config3(), None
+    elif name == "dense":
+        p, splits = fi.config1(), 0
+    elif name.startswith("flex_"):
+        p, splits = fi.config5(name[5:]), 0
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    t = dev_tensors(p, dev)
+    call, _, _, _ = make_call(p, t, num_splits=splits)
+    for _ in range(warmup + steps):
+        call()
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    print(f"profile workload {name}: {warmup + steps} calls done")
 
 
 if __name__ == "__main__":
