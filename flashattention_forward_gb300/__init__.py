@@ -25,7 +25,8 @@ FA_BF16, FA_E4M3, FA_F32, FA_I32, FA_U8 = 0, 1, 2, 3, 4
 MOD_NONE, MOD_ALIBI, MOD_SOFTCAP = 0, 1, 2
 
 EXPORTED = ("fa_fwd_varlen", "fa_fwd_workspace_bytes", "fa_fwd_default_splits", "fa_combine",
-            "fa_last_error", "fa_get_device_error", "fa_version")
+            "fa_last_error", "fa_get_device_error", "fa_version", "fa_fwd_varlen_noalloc")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class FaError(RuntimeError):
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
             L.fa_get_device_error.argtypes = [ctypes.c_void_p, P(ctypes.c_int32)]
             L.fa_get_device_error.restype = ctypes.c_int
             L.fa_version.restype = ctypes.c_char_p
+            L.fa_fwd_varlen_noalloc.argtypes = L.fa_fwd_varlen.argtypes
+            L.fa_fwd_varlen_noalloc.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -191,6 +194,34 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                          ctypes.byref(sm), _ref(bm), int(page_size), ctypes.byref(launch),
                          ctypes.c_void_p(_stream_ptr(stream)))
     _check(st)
+    return out, lse
+
+
+def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, out: torch.Tensor,
+                       lse: Optional[torch.Tensor], *, max_seqlen_q: int, max_seqlen_k: int,
+                       total_k: Optional[int] = None, block_table: Optional[torch.Tensor] = None,
+                       page_size: int = 0, softmax_scale: Optional[float] = None, causal: bool = False,
+                       window: int = 0, num_splits: int = 0, stream=None):
+    """Split-KV decode through ``fa_fwd_varlen_noalloc``: for callers that cannot
+    allocate device memory (the partials go to the library's static scratch of
+    NOALLOC_SCRATCH_BYTES).  ``out`` (and ``lse`` if wanted) are caller-provided;
+    this wrapper allocates nothing.  ``num_splits=0`` uses the library default."""
+    L = lib()
+    B = cu_seqlens_q.shape[0] - 1
+    Tq, Hq, Dk = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(Dk)
+    if total_k is None:
+        total_k = k_cache.shape[0] if block_table is None else 0
+    launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                    num_splits=num_splits, total_q=Tq, total_k=total_k)
+    args = [as_tensor(q), as_tensor(k_cache), as_tensor(v_cache), as_tensor(block_table),
+            as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), None, None, as_tensor(out), as_tensor(lse)]
+    sm = ScoreMod(kind=MOD_NONE)
+    _check(L.fa_fwd_varlen_noalloc(*[_ref(a) for a in args], float(softmax_scale), int(bool(causal)),
+                                   int(window), ctypes.byref(sm), None, int(page_size), ctypes.byref(launch),
+                                   ctypes.c_void_p(_stream_ptr(stream))))
     return out, lse
 
 

@@ -135,6 +135,10 @@ bool supported_dims(int64_t dk, int64_t dv) {
 
 }  // namespace
 
+namespace fa {
+fa_status_t set_host_error(fa_status_t st, const char *msg) { return fail(st, "%s", msg); }
+}  // namespace fa
+
 extern "C" {
 
 const char *fa_last_error(void) { return g_msg; }

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/fa_gb300.h"
 #include "fa_decode.cuh"
 #include "fa_prefill.cuh"
 
@@ -30,6 +31,9 @@ cudaError_t launch_prefill_192_128(const PrefillLaunch &L);
 cudaError_t launch_decode(int d, const DecodeLaunch &L);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
                            int dv, void *out, float *lse, cudaStream_t stream);
+
+// Records a host-side error message for fa_last_error() and returns `st`.
+fa_status_t set_host_error(fa_status_t st, const char *msg);
 
 // Sets the dynamic shared-memory attribute once per (kernel, device).
 template <typename K>

@@ -177,6 +177,43 @@ fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_s
                        int64_t n_rows, int32_t hq, int32_t dv, void *out_bf16, float *lse,
                        void *stream);
 
+/*
+ * fa_fwd_varlen_noalloc -- the split-KV decode of fa_fwd_varlen for callers
+ * that cannot allocate device memory.  (The pages have no counterpart: this
+ * entry exists for deployment, not for the method.)
+ *
+ * Who needs it: custom ops and plugins that are handed only their input and
+ * output buffers, serving loops whose device memory is fixed at start-up, and
+ * request paths that must not call cudaMalloc because it may synchronise the
+ * device or fail under memory pressure.  Instead of launch->workspace, the
+ * per-split partials go to a static device array of FA_NOALLOC_SCRATCH_BYTES
+ * owned by the library; every GPU that loads the library holds that array
+ * until the process exits.  Nothing is allocated by this call.
+ *
+ * Arguments and layouts are those of fa_fwd_varlen; launch->workspace and
+ * launch->workspace_bytes are ignored.  launch->num_splits <= 0 picks
+ * fa_fwd_default_splits(); the problem must be a split-KV decode shape with
+ * at least 2 splits, and fa_fwd_workspace_bytes() for it must not exceed
+ * FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_UNSUPPORTED is returned with nothing
+ * enqueued.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the one array and leaves its partials there: calls whose
+ * work overlaps on the GPU (different streams, or the same stream from several
+ * host threads without ordering) race on it.  No part of the array needs to
+ * start at zero.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tensor_t *k_cache,
+                                  const fa_tensor_t *v_cache, const fa_tensor_t *block_table,
+                                  const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
+                                  const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
+                                  fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
+                                  int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
+                                  const fa_block_mask_t *block_mask, int32_t page_size,
+                                  const fa_launch_t *launch, void *stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *fa_last_error(void);
 
