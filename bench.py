@@ -32,7 +32,8 @@ import torch  # noqa: E402
 import fa_inputs as fi  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (prefill) & KV-cache GB/s (decode), % of GB300 roofline"
-KERNEL_SOURCES = ["flashattention_forward_gb300/csrc/fa_prefill.cuh", "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
+KERNEL_SOURCES = ["flashattention_forward_gb300/csrc/fa_prefill.cuh", "flashattention_forward_gb300/csrc/fa_prefill2.cuh",
+                  "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
 
 
 def kernel_hash():
@@ -346,7 +347,7 @@ def main():
             traffic = tj.get("dram_bytes_per_launch")
     roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": ach / pk["bf16"], "traffic": traffic,
-                "kernel": "fa_prefill_kernel<128,128,packed,bf16>, non-causal launch",
+                "kernel": "fa_prefill2_kernel<128,128,packed,none>, non-causal launch",
                 "peak_source": f"{pk['src']} bf16 burst (cuBLAS 8192^3)"}
     extra = {}
     if rank == 0:
@@ -433,6 +434,8 @@ def profile_only(name, warmup, steps):
         p, splits = fi.config3(), None
     elif name == "dense":
         p, splits = fi.config1(), 0
+    elif name == "long_noncausal":
+        p, splits = fi.make_problem([8192] * 4, hq=16, dk=128, name="long_noncausal"), 0
     elif name.startswith("flex_"):
         p, splits = fi.config5(name[5:]), 0
     else:

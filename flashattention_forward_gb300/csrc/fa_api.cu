@@ -391,7 +391,9 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   }
 
   // ------------------------------------------------------------ prefill --
-  const int64_t n_qtiles = (launch->max_seqlen_q + fa::kBlockM - 1) / fa::kBlockM;
+  // Dk <= 128 with bf16 K/V runs the two-query-tile kernel (256 rows per CTA).
+  const int64_t rows_per_cta = (Dk <= 128 && !fp8) ? 2 * fa::kBlockM : fa::kBlockM;
+  const int64_t n_qtiles = (launch->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   if (B > 65535 || n_qtiles > 65535 || Hq > (1 << 20)) return fail(FA_ERR_UNSUPPORTED, "grid too large");
   fa::PrefillLaunch L;
   memset(&L, 0, sizeof L);
