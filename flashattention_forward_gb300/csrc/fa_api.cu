@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/fa_gb300.h"
@@ -394,7 +395,10 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   // Dk <= 128 with bf16 K/V runs the two-query-tile kernel (256 rows per CTA).
   const int64_t rows_per_cta = (Dk <= 128 && !fp8) ? 2 * fa::kBlockM : fa::kBlockM;
   const int64_t n_qtiles = (launch->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
-  if (B > 65535 || n_qtiles > 65535 || Hq > (1 << 20)) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  const int64_t head_group = Hq < 8 ? Hq : 8;
+  const int64_t n_hgroups = (Hq + head_group - 1) / head_group;
+  const int64_t n_blocks = B * n_hgroups * n_qtiles * head_group;
+  if (n_blocks >= (int64_t(1) << 31)) return fail(FA_ERR_UNSUPPORTED, "grid too large");
   fa::PrefillLaunch L;
   memset(&L, 0, sizeof L);
   {
@@ -457,8 +461,22 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   p.err = error_word();
   L.paged = paged;
   L.fp8 = fp8;
-  L.mod = mod;
-  L.grid = dim3((unsigned)Hq, (unsigned)B, (unsigned)n_qtiles);
+  {
+    // Test knob: FA_GB300_PREFILL_VARIANT=1 forces the 10-warp two-pass softmax.
+    const char *v = getenv("FA_GB300_PREFILL_VARIANT");
+    L.variant = (v && v[0] == '1') ? 1 : 0;
+  }
+  // The plain-softmax kernels fold a positive scale into the exponent; any
+  // other scale takes the general score path (ALiBi with slope 0).
+  if (mod == 0 && !(softmax_scale > 0.f)) {
+    L.mod = 1;
+    p.alibi_log2 = 0.f;
+  } else {
+    L.mod = mod;
+  }
+  p.head_group = (int)head_group;
+  p.n_hgroups = (int)n_hgroups;
+  L.grid = dim3((unsigned)n_blocks, 1, 1);
   L.stream = s;
   cudaError_t e;
   if (Dk == 64) e = fa::launch_prefill_64_64(L);

@@ -14,6 +14,7 @@ struct PrefillLaunch {
   CUtensorMap tm_q, tm_k, tm_v;
   PrefillParams p;
   int paged, fp8, mod;
+  int variant;   // 0: fastest available, 1: force the 10-warp two-pass softmax
   dim3 grid;
   cudaStream_t stream;
 };

@@ -61,7 +61,26 @@ struct PrefillParams {
   float softcap_log2;   // cap * log2(e)
   float alibi_log2;     // slope * log2(e)
   int *err;             // device error word
+  int32_t head_group;   // heads interleaved per group in the block order
+  int32_t n_hgroups;    // ceil(hq / head_group)
 };
+
+// Block order: for each sequence, for each group of `head_group` heads, query
+// tiles from the latest (longest under a causal mask) to the first, the heads
+// of the group interleaved.  Concurrent CTAs then share the K/V of a few
+// heads through L2, and long tiles start first.  Returns false for padding.
+__device__ __forceinline__ bool decode_block(const PrefillParams &p, int &b, int &h, int &qt) {
+  unsigned L = blockIdx.x;
+  const int g_in = (int)(L % (unsigned)p.head_group);
+  L /= (unsigned)p.head_group;
+  const int pr = (int)(L % (unsigned)p.n_qtiles);
+  L /= (unsigned)p.n_qtiles;
+  const int hg = (int)(L % (unsigned)p.n_hgroups);
+  b = (int)(L / (unsigned)p.n_hgroups);
+  h = hg * p.head_group + g_in;
+  qt = p.n_qtiles - 1 - pr;
+  return h < p.hq;
+}
 
 template <int DK, int DV, bool PAGED, bool FP8, int MOD>
 struct PrefillCfg {
@@ -132,9 +151,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
 
   // ------------------------------------------------------------ work tile --
   TileInfo ti;
-  ti.h = blockIdx.x;
-  ti.b = blockIdx.y;
-  ti.qt = p.n_qtiles - 1 - (int)blockIdx.z;   // longest (latest) query tiles first
+  if (!decode_block(p, ti.b, ti.h, ti.qt)) return;
   ti.hk = ti.h / p.group;
   {
     const int qa = __ldg(p.cu_q + ti.b), qb = __ldg(p.cu_q + ti.b + 1);

@@ -17,14 +17,15 @@
 // the softmax has read S_X; tcgen05.mma ops issued by one thread run in issue
 // order, so QK_X(j+1) (which rewrites S_X) cannot overtake PV_X(j).
 //
-// Warps (320 threads): 0-3 softmax A, 4-7 softmax B, 8 TMA producer (Q, K, V),
-// 9 TMEM allocation + MMA issue.
+// Warps: 0-3 softmax A, 4-7 softmax B, 8 TMA producer (Q, K, V), 9 TMEM
+// allocation + MMA issue; the 12-warp variant adds two idle warps so that
+// warpgroup 2 can hand its registers to the softmax warpgroups (setmaxnreg).
 #pragma once
 #include "fa_prefill.cuh"
 
 namespace fa {
 
-template <int DK, int DV, bool PAGED, int MOD>
+template <int DK, int DV, bool PAGED, int MOD, bool BIGREG>
 struct Prefill2Cfg {
   static constexpr int NSK = (DK <= 64) ? 4 : 3;
   static constexpr int NSV = (DK <= 64) ? 4 : 2;
@@ -38,7 +39,12 @@ struct Prefill2Cfg {
   static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;
-  static constexpr int kThreads = 10 * 32;
+  // BIGREG: 12 warps; the producer/MMA warpgroup gives registers to the two
+  // softmax warpgroups (setmaxnreg), so a whole S row fits in registers.
+  static constexpr int kThreads = (BIGREG ? 12 : 10) * 32;
+  static constexpr int kRegsSoftmax = 208, kRegsOther = 80;
+  // launch registers per thread needed for that split to fit the CTA's pool
+  static constexpr int kMinLaunchRegs = (8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther + kThreads - 1) / kThreads;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(DV <= 128, "O_A/O_B hold 128 columns each");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -88,11 +94,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 
-template <int DK, int DV, bool PAGED, int MOD>
-__global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
+template <int DK, int DV, bool PAGED, int MOD, bool BIGREG>
+__global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThreads, 1)
     fa_prefill2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using Cfg = Prefill2Cfg<DK, DV, PAGED, MOD>;
+  using Cfg = Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>;
   constexpr int NSK = Cfg::NSK, NSV = Cfg::NSV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -100,9 +106,8 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
 
   // ------------------------------------------------------------ work tile --
   PairInfo pi;
-  pi.h = blockIdx.x;
-  pi.b = blockIdx.y;
-  const int pt = p.n_qtiles - 1 - (int)blockIdx.z;   // longest (latest) pairs first
+  int pt;
+  if (!decode_block(p, pi.b, pi.h, pt)) return;
   pi.hk = pi.h / p.group;
   {
     const int qa = __ldg(p.cu_q + pi.b), qb = __ldg(p.cu_q + pi.b + 1);
@@ -200,6 +205,11 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // BIGREG: warpgroups 0-1 (softmax) take the registers warpgroup 2 releases
+  // (setmaxnreg at the head of each role's branch).  The host launches this
+  // variant only when the kernel's launch register count makes
+  // 8*32*224 + 4*32*56 fit the CTA's register pool.
+  if (BIGREG && warp >= 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsOther));
 
   if (warp == 8) {
     // ------------------------------------------------ producer: Q, K, V --
@@ -271,100 +281,94 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
     int n_pv[2] = {0, 0};
     bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
 
+    // Descriptor words, computed once: a K-major 128-byte-swizzled operand
+    // steps 32 bytes per K=16 slice and jumps to the next 64-column block
+    // (rows * 128 bytes) every fourth slice; V (MN-major) steps 16 rows.
+    const uint64_t dq0 = smem_desc_sw128(sQa, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sKa, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sVa, kBlockN * 128, 1024);
+    const uint32_t q_lo = (uint32_t)dq0, k_lo = (uint32_t)dk0, qk_hi = (uint32_t)(dq0 >> 32);
+    const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
     auto qk = [&](int X, int st) {
       const uint32_t d = tmem + (X ? 128u : 0u);
+      uint32_t a = q_lo + (uint32_t)(X * (Cfg::kQTileBytes >> 4));
+      uint32_t b = k_lo + (uint32_t)(st * (Cfg::kKBytes >> 4));
 #pragma unroll
       for (int ks = 0; ks < DK / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
-        const uint64_t da = smem_desc_sw128(sQa + X * Cfg::kQTileBytes + off, 16, 1024);
-        const uint64_t db = smem_desc_sw128(sKa + st * Cfg::kKBytes + off, 16, 1024);
-        mma_ss(d, da, db, idesc_qk, ks > 0);
+        if (ks == 0) mma_ss_w<0>(d, a, qk_hi, b, qk_hi, idesc_qk);
+        else mma_ss_w<1>(d, a, qk_hi, b, qk_hi, idesc_qk);
+        const uint32_t step = ((ks + 1) & 3) ? 2u : (uint32_t)((kBlockM * 128 - 96) >> 4);
+        a += step;
+        b += step;
       }
       tc_commit(smem_u32(s_full + X));
     };
     auto pv = [&](int X, int sv) {
       const uint32_t a = tmem + (X ? 128u : 0u);                 // P_X aliases S_X
       const uint32_t d = tmem + 256u + (X ? 128u : 0u);
+      uint32_t b = v_lo + (uint32_t)(sv * (Cfg::kVBytes >> 4));
+      const uint32_t acc0 = n_pv[X] > 0 ? 1u : 0u;
 #pragma unroll
       for (int ks = 0; ks < kBlockN / 16; ++ks) {
-        const uint64_t db = smem_desc_sw128(sVa + sv * Cfg::kVBytes + ks * 16 * 128, kBlockN * 128, 1024);
-        mma_ts(d, a + ks * 8, db, idesc_pv, (n_pv[X] > 0 || ks > 0) ? 1u : 0u);
+        mma_ts_w(d, a + ks * 8, b, v_hi, idesc_pv, ks > 0 ? 1u : acc0);
+        b += (16 * 128) >> 4;
       }
       tc_commit(smem_u32(o_done + X));
     };
 
-    // prologue: QK of the first tile for both halves
-    if (ok) {
+    // One lane runs the whole issue loop (no warp-wide steps): the tensor
+    // core is fed only while this thread is free, so the loop keeps its
+    // bookkeeping small -- activity flags of the next tile are carried over.
+    if (lane == 0 && ok) {
+      bool a0 = half_active(p, pi, 0, first_kt), a1 = half_active(p, pi, 1, first_kt);
       ok = mbar_wait(smem_u32(k_full + 0), 0, abort_flag, p.err);
       if (ok) {
         tc_fence_after();
-        if (lane == 0) {
-          if (half_active(p, pi, 0, first_kt)) qk(0, 0);
-          if (half_active(p, pi, 1, first_kt)) qk(1, 0);
-          tc_commit(smem_u32(k_empty + 0));
-        }
-        __syncwarp();
+        if (a0) qk(0, 0);
+        if (a1) qk(1, 0);
+        tc_commit(smem_u32(k_empty + 0));
       }
-    }
-    int j = 0;
-    for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
-      const int kn = pair_next(p, pi, kt);
-      const int sv = j % NSV;
-      const bool a0 = half_active(p, pi, 0, kt), a1 = half_active(p, pi, 1, kt);
-      const bool n0 = kn < pi.kt_hi && half_active(p, pi, 0, kn);
-      const bool n1 = kn < pi.kt_hi && half_active(p, pi, 1, kn);
-      ok = mbar_wait(smem_u32(v_full + sv), (j / NSV) & 1, abort_flag, p.err);
-      if (!ok) break;
-      // Keys past the sequence end may be NaN-poisoned; clear those V rows.
-      const int valid = pi.sk - kt * kBlockN;
-      if (valid < kBlockN) {
-        uint8_t *vt = sV + sv * Cfg::kVBytes;
-#pragma unroll
-        for (int cb = 0; cb < DV / 64; ++cb) {
-          uint4 *z = reinterpret_cast<uint4 *>(vt + cb * kBlockN * 128 + valid * 128);
-          const int n16 = (kBlockN - valid) * 8;
-          for (int i = lane; i < n16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (a0) {
-        ok = mbar_wait(smem_u32(p_full + 0), n_pv[0] & 1, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) pv(0, sv);
-        ++n_pv[0];
-        __syncwarp();
-      }
-      if (kn < pi.kt_hi) {
+      int j = 0;
+      for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
+        const int kn = pair_next(p, pi, kt);
+        const bool more = kn < pi.kt_hi;
+        const bool n0 = more && half_active(p, pi, 0, kn);
+        const bool n1 = more && half_active(p, pi, 1, kn);
+        const int sv = j % NSV;
         const int st = (j + 1) % NSK;
-        ok = mbar_wait(smem_u32(k_full + st), ((j + 1) / NSK) & 1, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0 && n0) qk(0, st);
-        __syncwarp();
-      }
-      if (a1) {
-        ok = mbar_wait(smem_u32(p_full + 1), n_pv[1] & 1, abort_flag, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) pv(1, sv);
-        ++n_pv[1];
-        __syncwarp();
-      }
-      if (lane == 0) tc_commit(smem_u32(v_empty + sv));
-      if (kn < pi.kt_hi) {
-        const int st = (j + 1) % NSK;
-        if (lane == 0) {
+        // V of this tile; rows past the sequence end were cleared by the
+        // softmax warpgroup before it released P (see the softmax loop).
+        if (!(ok = mbar_wait(smem_u32(v_full + sv), (j / NSV) & 1, abort_flag, p.err))) break;
+        if (a0) {
+          if (!(ok = mbar_wait(smem_u32(p_full + 0), n_pv[0] & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          pv(0, sv);
+          ++n_pv[0];
+        }
+        if (more) {
+          if (!(ok = mbar_wait(smem_u32(k_full + st), ((j + 1) / NSK) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          if (n0) qk(0, st);
+        }
+        if (a1) {
+          if (!(ok = mbar_wait(smem_u32(p_full + 1), n_pv[1] & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          pv(1, sv);
+          ++n_pv[1];
+        }
+        tc_commit(smem_u32(v_empty + sv));
+        if (more) {
           if (n1) qk(1, st);
           tc_commit(smem_u32(k_empty + st));
         }
+        a0 = n0;
+        a1 = n1;
+        kt = kn;
       }
-      __syncwarp();
-      kt = kn;
     }
   } else if (warp < 8) {
     // ---------------------------------------------------------- softmax --
+    if constexpr (BIGREG) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsSoftmax));
     const int X = warp >> 2;                  // 0: tile A, 1: tile B
     const int r = threadIdx.x & 127;          // row in the tile == TMEM lane
     const Half hx = X ? pi.x[1] : pi.x[0];
@@ -375,8 +379,26 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     int cnt = 0;
     bool ok = true;
-    const bool fast = (MOD == 0) && (p.scale_log2 > 0.f);
+    // MOD 0 runs with a positive scale only (the host routes other scales to
+    // the general path), so raw scores can be maxed before scaling.
+    constexpr bool fast = (MOD == 0);
+    // Exponentials 2^(c*v - m) of a 32-column chunk with packed fp32 math,
+    // their row sums and the bf16 packing of P.
+    auto chunk_exp = [&](const float (&v)[32], float c, float m, uint32_t (&pk)[16], float (&acc)[4]) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float t0, t1;
+        fma2(t0, t1, v[e], v[e + 1], c, -m);
+        const float a0 = ex2(t0), a1 = ex2(t1);
+        const int q = ((e >> 1) & 1) * 2;
+        add2(acc[q], acc[q + 1], a0, a1);
+        pk[e >> 1] = pack_bf16x2(a0, a1);
+      }
+    };
+    const float cexp = fast ? p.scale_log2 : 1.f;
+    int j = -1;   // index of the tile in the pair's list (K/V ring position)
     for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
+      ++j;
       if (!half_active_h(p, pi, hx, kt)) continue;
       ok = mbar_wait(smem_u32(s_full + X), cnt & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -418,77 +440,118 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
           }
         }
       };
-      // Pass 1: tile max (chunks of 32 columns, 8 independent max chains).
-      float mx[8];
+      float alpha_tile = 1.f;
+      bool warp_need = false;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (BIGREG) {
+        // One pass: the whole S row comes out of TMEM with a single wait.
+        float sv[4][32];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        float s0[32], s1[32];
-        tmem_ld32(sa + c * 32, s0);
-        tmem_ld32(sa + c * 32 + 32, s1);
+        for (int c = 0; c < 4; ++c) tmem_ld32(sa + c * 32, sv[c]);
         tmem_wait_ld();
-        scores(s0, j0 + c * 32);
-        scores(s1, j0 + c * 32 + 32);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          mx[e & 7] = fmaxf(mx[e & 7], s0[e]);
-          mx[e & 7] = fmaxf(mx[e & 7], s1[e]);
+        for (int c = 0; c < 4; ++c) scores(sv[c], j0 + c * 32);
+        // Balanced tree of 3-input maxima over the 128 scores (depth 5).
+        float t1[43];
+#pragma unroll
+        for (int k = 0; k < 42; ++k) {
+          const int e = 3 * k;
+          t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+        }
+        t1[42] = fmaxf(sv[3][30], sv[3][31]);
+        float t2[15];
+#pragma unroll
+        for (int k = 0; k < 14; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+        t2[14] = t1[42];
+        float t3[5];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
+        float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
+        if (fast && tmax != -INFINITY) tmax *= p.scale_log2;
+        const float m_new = fmaxf(m_ref, tmax);
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        warp_need = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha_tile = ex2(m_ref - m_new);
+          l *= alpha_tile;
+          m_ref = m_new;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+          chunk_exp(sv[c], cexp, m_use, pk, sum);
+          tmem_st16(sa + c * 16, pk);
+        }
+      } else {
+        // The S row is processed in two halves of 64 columns.  Each half moves
+        // the reference max only when its max exceeds it by the lazy threshold;
+        // if the second half does so, the first half's P (already in TMEM) is
+        // rescaled too -- rare once a row's max has settled.
+  #pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float sv[2][32];
+          tmem_ld32(sa + hf * 64, sv[0]);
+          tmem_ld32(sa + hf * 64 + 32, sv[1]);
+          tmem_wait_ld();
+          scores(sv[0], j0 + hf * 64);
+          scores(sv[1], j0 + hf * 64 + 32);
+          // tree of 3-input maxima over the 64 scores of this half
+          float t1[22];
+#pragma unroll
+          for (int k = 0; k < 21; ++k) {
+            const int e = 3 * k;
+            t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+          }
+          t1[21] = sv[1][31];
+          float t2[8];
+#pragma unroll
+          for (int k = 0; k < 7; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+          t2[7] = t1[21];
+          float hmax = fmaxf(max3(t2[0], t2[1], t2[2]), fmaxf(max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7])));
+          if (fast && hmax != -INFINITY) hmax *= p.scale_log2;
+          const float m_new = fmaxf(m_ref, hmax);
+          const bool need = m_new > m_ref + kRescaleThreshold;
+          const bool wneed = __any_sync(0xffffffffu, need);
+          if (wneed) {
+            const float alpha = need ? ex2(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
+            if (need) {
+              m_ref = m_new;
+              l *= alpha;
+              sum[0] *= alpha;
+              sum[1] *= alpha;
+              sum[2] *= alpha;
+              sum[3] *= alpha;
+            }
+            alpha_tile *= alpha;
+            warp_need = true;
+            if (hf == 1) {
+              // P of the first half was computed against the old reference.
+              tmem_wait_st();
+              float pw[32];
+              tmem_ld32(sa, pw);
+              tmem_wait_ld();
+              uint32_t w[32];
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const uint32_t u = __float_as_uint(pw[e]);
+                const float lo = __uint_as_float(u << 16) * alpha, hi = __uint_as_float(u & 0xFFFF0000u) * alpha;
+                w[e] = pack_bf16x2(lo, hi);
+              }
+              tmem_st32(sa, w);
+            }
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+  #pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+            chunk_exp(sv[c], cexp, m_use, pk, sum);
+            tmem_st16(sa + hf * 32 + c * 16, pk);
+          }
         }
       }
-      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      if (fast && tmax != -INFINITY) tmax *= p.scale_log2;
-
-      const float m_new = fmaxf(m_ref, tmax);
-      const bool need = m_new > m_ref + kRescaleThreshold;
-      const bool warp_need = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_ref - m_new);
-        l *= alpha;
-        m_ref = m_new;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // Pass 2: p = 2^(x - m), row sum, bf16 P written over the S columns
-      // already read (P chunk c occupies columns [16c, 16c+16)).
-      float sum[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sum[k] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        float s0[32], s1[32];
-        tmem_ld32(sa + c * 32, s0);
-        tmem_ld32(sa + c * 32 + 32, s1);
-        tmem_wait_ld();
-        scores(s0, j0 + c * 32);
-        scores(s1, j0 + c * 32 + 32);
-        uint32_t pk0[16], pk1[16];
-        if (fast) {
-          const float c2 = p.scale_log2;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float a0 = ex2(fmaf(s0[e], c2, -m_use)), a1 = ex2(fmaf(s0[e + 1], c2, -m_use));
-            const float b0 = ex2(fmaf(s1[e], c2, -m_use)), b1 = ex2(fmaf(s1[e + 1], c2, -m_use));
-            sum[(e >> 1) & 3] += a0 + a1;
-            sum[4 + ((e >> 1) & 3)] += b0 + b1;
-            pk0[e >> 1] = pack_bf16x2(a0, a1);
-            pk1[e >> 1] = pack_bf16x2(b0, b1);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float a0 = ex2(s0[e] - m_use), a1 = ex2(s0[e + 1] - m_use);
-            const float b0 = ex2(s1[e] - m_use), b1 = ex2(s1[e + 1] - m_use);
-            sum[(e >> 1) & 3] += a0 + a1;
-            sum[4 + ((e >> 1) & 3)] += b0 + b1;
-            pk0[e >> 1] = pack_bf16x2(a0, a1);
-            pk1[e >> 1] = pack_bf16x2(b0, b1);
-          }
-        }
-        tmem_st16(sa + c * 16, pk0);
-        tmem_st16(sa + c * 16 + 16, pk1);
-      }
-      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      const float alpha = alpha_tile;
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       if (warp_need && cnt > 0) {
         // O_X must hold PV_X(cnt-1) before it is rescaled.
         ok = mbar_wait(smem_u32(o_done + X), (cnt - 1) & 1, abort_flag, p.err);
@@ -505,6 +568,22 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD>::kThreads, 1)
           for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(o[e] * alpha);
           tmem_st32(oa + c * 32, w);
         }
+      }
+      // Keys past the sequence end may hold anything (NaN-poisoned page
+      // slots): P is 0 there, but 0 * NaN is NaN, so those V rows are cleared
+      // before P is released -- by warpgroup A, or by B when A skips the tile.
+      const int valid = pi.sk - j0;
+      if (valid < kBlockN && (X == 0 || !half_active(p, pi, 0, kt))) {
+        const int sv = j % NSV;
+        ok = mbar_wait(smem_u32(v_full + sv), (j / NSV) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        uint8_t *vt = sV + sv * Cfg::kVBytes;
+        const int per_cb = (kBlockN - valid) * 8;            // 16-byte chunks per column block
+        for (int idx = r; idx < per_cb * (DV / 64); idx += kBlockM) {
+          const int cb = idx / per_cb, rem = idx - cb * per_cb;
+          *reinterpret_cast<uint4 *>(vt + cb * kBlockN * 128 + valid * 128 + rem * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
       }
       tmem_wait_st();
       tc_fence_before();

@@ -135,6 +135,10 @@ typedef struct {
  *  launch       host scalars (required).
  *  stream       cudaStream_t.
  *
+ * Environment: FA_GB300_PREFILL_VARIANT=1 makes the Dk <= 128 prefill use its
+ * 10-warp two-pass softmax instead of the register-rebalanced one-pass one
+ * (a test and diagnosis knob; results agree within rounding).
+ *
  * Supported head dims: (Dk, Dv) in {(64,64), (128,128), (192,128)}.  Hq must
  * be a multiple of Hkv (query head h reads kv head h / (Hq/Hkv)).
  * Returns FA_OK or an error status; see fa_last_error().

@@ -76,6 +76,8 @@ EDGE = [
     dict(lens_q=[300, 129], lens_k=[330, 400], hq=4, hkv=2, dk=128, block_mask_density=0.5),
     dict(lens_q=[257, 33], lens_k=[600, 33], hq=4, hkv=4, dk=192, dv=128, causal=True),
     dict(lens_q=[257, 33], lens_k=[600, 33], hq=4, hkv=2, dk=192, dv=128, page_size=64, spare_pages=3),
+    dict(lens_q=[300, 70], lens_k=[300, 200], hq=4, dk=128, softmax_scale=-0.05, causal=True),  # negative scale
+    dict(lens_q=[513, 40, 900], lens_k=[513, 700, 900], hq=8, hkv=2, dk=64, causal=True),       # 3 pairs, GQA
 ]
 
 
@@ -206,3 +208,11 @@ def test_guard_bands_untouched():
     assert torch.all(big_l[p.hq:] == 777.0)
     ro, rl = oracle.forward(p)
     compare(*host(o, l), ro, rl)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_two_pass_softmax_variant(monkeypatch, causal):
+    """The 10-warp two-pass softmax (used when the register split does not fit)."""
+    monkeypatch.setenv("FA_GB300_PREFILL_VARIANT", "1")
+    check(fi.make_problem([300, 129, 700], [300, 400, 700], hq=4, hkv=2, dk=128, seed=31, causal=causal))
+    check(fi.make_problem([200, 64], [500, 64], hq=4, dk=64, seed=32, causal=causal, mod="alibi"))
