@@ -423,6 +423,17 @@ def other_workloads(dev, warmup, steps, flush, pk):
     res["paged_decode_64seq_hq32_hkv8_p16"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
                                                "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16),
                                                "bytes": fi.decode_bytes(p)}
+    # paged e4m3 KV, Q/K 192, V/O 128, page 64, 16 seqs U{1..4096}, causal
+    p = fi.config4()
+    t = dev_tensors(p, dev)
+    call, _, _, _ = make_call(p, t, num_splits=0)
+    times = time_calls([call], warmup, steps, flush)
+    ms = statistics.mean(times)
+    fl = fi.prefill_flops(p)
+    res["paged_fp8_d192_v128_16seq_h16_p64_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                                        "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+                                                        "gflop": fl / 1e9}
+    del t
     # flex runs at B=4, H=16, S=8192
     for run in fi.CONFIG5_RUNS:
         p = fi.config5(run)
@@ -458,6 +469,8 @@ def profile_only(name, warmup, steps):
         p, splits = fi.config1(), 0
     elif name == "long_noncausal":
         p, splits = fi.make_problem([8192] * 4, hq=16, dk=128, name="long_noncausal"), 0
+    elif name == "fp8":
+        p, splits = fi.config4(), 0
     elif name.startswith("flex_"):
         p, splits = fi.config5(name[5:]), 0
     else:

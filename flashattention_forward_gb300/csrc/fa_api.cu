@@ -50,12 +50,13 @@ EncodeTiledFn encode_fn() {
 
 // Tiled map with 128-byte swizzle; strides in bytes for dims 1..rank-1.
 fa_status_t make_map(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base, const uint64_t *dims,
-                     const uint64_t *strides, const uint32_t *box, const char *what) {
+                     const uint64_t *strides, const uint32_t *box, const char *what,
+                     CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
   return FA_OK;
 }
@@ -308,7 +309,6 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   if (launch->max_seqlen_q <= 0) return fail(FA_ERR_INVALID_ARG, "max_seqlen_q must be > 0 when total_q > 0");
   if (!q->data || !out->data || !cu_seqlens_q->data || !cu_seqlens_k->data)
     return fail(FA_ERR_INVALID_ARG, "a required data pointer is NULL");
-  if (fp8) return fail(FA_ERR_UNSUPPORTED, "e4m3 KV is not compiled in this build");
 
   cudaStream_t s = (cudaStream_t)stream;
   const CUtensorMapDataType kv_tmdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -321,6 +321,7 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
     if ((int64_t)launch->max_seqlen_q * group > fa::kDecRows)
       return fail(FA_ERR_UNSUPPORTED, "split-KV needs max_seqlen_q * Hq/Hkv <= %d", fa::kDecRows);
     if (Dk != Dv || (Dk != 64 && Dk != 128)) return fail(FA_ERR_UNSUPPORTED, "split-KV supports Dk = Dv in {64, 128}");
+    if (fp8) return fail(FA_ERR_UNSUPPORTED, "split-KV runs on bf16 caches; use num_splits = 0 for e4m3");
     if (mod != 0 || block_mask) return fail(FA_ERR_UNSUPPORTED, "split-KV does not take score mods or block masks");
     if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "too many sequences or kv heads for split-KV");
     fa::DecodeLaunch L;
@@ -409,7 +410,29 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
     if ((st = make_map(&L.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dq, sq, box, "q"))) return st;
   }
   const int rows_box = paged ? (page_size < fa::kBlockN ? page_size : fa::kBlockN) : fa::kBlockN;
-  if (have_keys) {
+  if (have_keys && fp8) {
+    // e4m3: whole rows (Dk or Dv bytes) per box, no swizzle; the kernel
+    // converts them into the swizzled bf16 operand layout.
+    if (paged) {
+      const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
+      const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
+      const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
+      const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2]), (uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
+      const uint32_t bk[4] = {(uint32_t)Dk, 1, (uint32_t)rows_box, 1};
+      const uint32_t bv[4] = {(uint32_t)Dv, 1, (uint32_t)rows_box, 1};
+      if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, bk, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+      if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dv, sv, bv, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+    } else {
+      const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)k_cache->shape[0]};
+      const uint64_t dv[3] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)v_cache->shape[0]};
+      const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
+      const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
+      const uint32_t bk[3] = {(uint32_t)Dk, 1, (uint32_t)fa::kBlockN};
+      const uint32_t bv[3] = {(uint32_t)Dv, 1, (uint32_t)fa::kBlockN};
+      if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, bk, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+      if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dv, sv, bv, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+    }
+  } else if (have_keys) {
     if (paged) {
       const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
@@ -482,6 +505,8 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   if (Dk == 64) e = fa::launch_prefill_64_64(L);
   else if (Dk == 128) e = fa::launch_prefill_128_128(L);
   else e = fa::launch_prefill_192_128(L);
+  if (e == cudaErrorNotSupported && fp8)
+    return fail(FA_ERR_UNSUPPORTED, "the e4m3 kernel's register split does not fit this build's launch registers");
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }

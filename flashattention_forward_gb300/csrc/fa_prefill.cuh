@@ -82,28 +82,46 @@ __device__ __forceinline__ bool decode_block(const PrefillParams &p, int &b, int
   return h < p.hq;
 }
 
+// e4m3 -> bf16 for two values (exact: every e4m3 value is a normal f16 or
+// zero, and every such f16 is a bf16).  The f16 pair is rebiased field-wise:
+// bf16 = sign | ((f16 & 0x7fff) >> 3) + (112 << 7) for non-zero magnitudes.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(two));
+  const uint32_t sign = h & 0x80008000u;
+  uint32_t mag = ((h & 0x7FFF7FFFu) >> 3) & 0x0FFF0FFFu;
+  mag += 0x38003800u & __vcmpne2(mag, 0u);
+  return sign | mag;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int DK, int DV, bool PAGED, bool FP8, int MOD>
 struct PrefillCfg {
   static constexpr int NS = (DK <= 64) ? 4 : 2;                 // K/V ring stages
   static constexpr int kQBytes = kBlockM * DK * 2;
   static constexpr int kKBytes = kBlockN * DK * 2;               // bf16 operand tile
   static constexpr int kVBytes = kBlockN * DV * 2;
-  static constexpr int kK8Bytes = FP8 ? kBlockN * DK : 0;        // e4m3 staging tile
-  static constexpr int kV8Bytes = FP8 ? kBlockN * DV : 0;
+  // e4m3 tiles are staged (unswizzled, row-major) in the upper half of the
+  // bf16 operand buffer they are converted into.
+  static constexpr int kK8Off = kKBytes / 2, kV8Off = kVBytes / 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + NS * kKBytes;
-  static constexpr int kOffK8 = kOffV + NS * kVBytes;
-  static constexpr int kOffV8 = kOffK8 + NS * kK8Bytes;
-  static constexpr int kOffKs = kOffV8 + NS * kV8Bytes;          // k scales [NS][128]
-  static constexpr int kOffVs = kOffKs + (FP8 ? NS * kBlockN * 4 : 0);
-  static constexpr int kOffBar = kOffVs + (FP8 ? NS * kBlockN * 4 : 0);
-  static constexpr int kNumBars = 1 + 4 * NS + 8 + (FP8 ? 4 * NS : 0);
+  static constexpr int kOffSc = kOffV + NS * kVBytes;            // softmax scales [2][2][128]
+  static constexpr int kOffBar = kOffSc + (FP8 ? 2 * 2 * kBlockN * 4 : 0);
+  static constexpr int kNumBars = 1 + 4 * NS + 8 + (FP8 ? 2 * NS : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;        // + alignment slack
-  static constexpr int kSoftmaxWarps = 4;
-  static constexpr int kConvWarps = FP8 ? 4 : 0;
-  static constexpr int kThreads = (7 + kConvWarps) * 32;
+  // Warp roles.  bf16: softmax 0-3, K 4, V 5, MMA 6.  e4m3: softmax 0-3,
+  // converters 4-7, K 8, V 9, MMA 10, one idle warp (12 warps = 3 warpgroups
+  // so that setmaxnreg can move registers to the softmax warpgroup).
+  static constexpr int kWarpK = FP8 ? 8 : 4, kWarpV = FP8 ? 9 : 5, kWarpMMA = FP8 ? 10 : 6;
+  static constexpr int kThreads = (FP8 ? 12 : 7) * 32;
+  static constexpr int kRegsSoftmax = 232, kRegsProd = 56;       // e4m3 variant only
+  static constexpr int kPoolNeeded = 128 * kRegsSoftmax + 128 * 168 + 128 * kRegsProd;
   // TMEM columns
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
@@ -212,16 +230,24 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
   uint64_t *s_free = s_full + 2;     // [2]
   uint64_t *p_full = s_free + 2;     // [2]
   uint64_t *p_empty = p_full + 2;    // [2]
+  uint64_t *k8_full = p_empty + 2;   // [NS] e4m3 staging landed (FP8 only)
+  uint64_t *v8_full = k8_full + NS;
+  float *sc = reinterpret_cast<float *>(smem + Cfg::kOffSc);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 8);
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(k_full + s), 1);
+      // bf16: filled by TMA (one arrive + bytes); e4m3: by the 128 converter threads
+      mbar_init(smem_u32(k_full + s), FP8 ? 128 : 1);
       mbar_init(smem_u32(k_empty + s), 1);
-      mbar_init(smem_u32(v_full + s), 1);
+      mbar_init(smem_u32(v_full + s), FP8 ? 128 : 1);
       mbar_init(smem_u32(v_empty + s), 1);
+      if (FP8) {
+        mbar_init(smem_u32(k8_full + s), 1);
+        mbar_init(smem_u32(v8_full + s), 1);
+      }
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(s_full + s), 1);
@@ -232,7 +258,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 6) {
+  if (warp == Cfg::kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -240,8 +266,11 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // e4m3 variant: the host launches it only when the launch register count
+  // makes kPoolNeeded fit the CTA's pool (see the launcher).
+  if (FP8 && warp >= 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsProd));
 
-  if (warp == 4) {
+  if (warp == Cfg::kWarpK) {
     // ------------------------------------------------ producer: Q and K --
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -255,6 +284,24 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
         const int st = it % NS;
         const uint32_t ph = (it / NS) & 1;
         if (it >= NS && !mbar_wait(smem_u32(k_empty + st), ph ^ 1, abort_flag, p.err)) break;
+        if constexpr (FP8) {
+          // e4m3 rows (DK bytes each) into the upper half of the operand buffer
+          uint64_t *bar = k8_full + st;
+          mbar_expect_tx(smem_u32(bar), kBlockN * DK);
+          uint8_t *dst = sK + st * Cfg::kKBytes + Cfg::kK8Off;
+          if constexpr (PAGED) {
+            const int32_t *bt = p.block_table + (int64_t)ti.b * p.bt_stride;
+            for (int pg = 0; pg < p.pages_per_tile; ++pg) {
+              const int key0 = kt * kBlockN + pg * p.rows_per_box;
+              const int page = key0 < ti.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+              tma_load_4d(smem_u32(dst + pg * p.rows_per_box * DK), &tm_k, smem_u32(bar), 0, ti.hk,
+                          key0 & (p.page_size - 1), page);
+            }
+          } else {
+            tma_load_3d(smem_u32(dst), &tm_k, smem_u32(bar), 0, ti.hk, ti.k_row0 + kt * kBlockN);
+          }
+          continue;
+        }
         mbar_expect_tx(smem_u32(k_full + st), Cfg::kKBytes);
         uint8_t *dst = sK + st * Cfg::kKBytes;
         if constexpr (PAGED) {
@@ -276,7 +323,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == Cfg::kWarpV) {
     // ---------------------------------------------------- producer: V --
     if (lane == 0) {
       prefetch_tmap(&tm_v);
@@ -285,6 +332,23 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
         const int st = it % NS;
         const uint32_t ph = (it / NS) & 1;
         if (it >= NS && !mbar_wait(smem_u32(v_empty + st), ph ^ 1, abort_flag, p.err)) break;
+        if constexpr (FP8) {
+          uint64_t *bar = v8_full + st;
+          mbar_expect_tx(smem_u32(bar), kBlockN * DV);
+          uint8_t *dst = sV + st * Cfg::kVBytes + Cfg::kV8Off;
+          if constexpr (PAGED) {
+            const int32_t *bt = p.block_table + (int64_t)ti.b * p.bt_stride;
+            for (int pg = 0; pg < p.pages_per_tile; ++pg) {
+              const int key0 = kt * kBlockN + pg * p.rows_per_box;
+              const int page = key0 < ti.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+              tma_load_4d(smem_u32(dst + pg * p.rows_per_box * DV), &tm_v, smem_u32(bar), 0, ti.hk,
+                          key0 & (p.page_size - 1), page);
+            }
+          } else {
+            tma_load_3d(smem_u32(dst), &tm_v, smem_u32(bar), 0, ti.hk, ti.k_row0 + kt * kBlockN);
+          }
+          continue;
+        }
         mbar_expect_tx(smem_u32(v_full + st), Cfg::kVBytes);
         uint8_t *dst = sV + st * Cfg::kVBytes;
         if constexpr (PAGED) {
@@ -306,10 +370,88 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
         }
       }
     }
-  } else if (warp == 6) {
+  } else if (FP8 && warp >= 4 && warp < 8) {
+    // --------------------------------------------- e4m3 -> bf16 converters --
+    // Each tile: read the staged e4m3 rows into registers (all 128 threads),
+    // sync, then write exact bf16 into the 128-byte-swizzled operand layout
+    // that the MMA reads (the staging area is overwritten, hence the sync).
+    const int c = threadIdx.x - 128;
+    int it = 0;
+    bool ok = true;
+    for (int kt = first_kt; ok && kt < ti.kt_hi; kt = next_tile<Cfg>(p, ti, kt), ++it) {
+      const int st = it % NS;
+      const uint32_t ph = (it / NS) & 1;
+#pragma unroll
+      for (int opnd = 0; opnd < 2; ++opnd) {
+        const int D = opnd == 0 ? DK : DV;
+        constexpr int kMaxChunks = (DK > DV ? DK : DV) / 16;     // 16-byte e4m3 chunks per thread
+        uint8_t *buf = opnd == 0 ? sK + st * Cfg::kKBytes : sV + st * Cfg::kVBytes;
+        const uint8_t *stage = buf + (opnd == 0 ? Cfg::kK8Off : Cfg::kV8Off);
+        ok = mbar_wait(smem_u32((opnd == 0 ? k8_full : v8_full) + st), ph, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const int per_row = D / 16;
+        // V rows are scaled here, in fp32, before their single rounding: the
+        // V operand is f16 RNE(e4m3(v) * v_scale).  (K keeps e4m3(k) exactly
+        // as bf16; k_scale multiplies S in fp32 in the softmax.)
+        float vsr[kMaxChunks];
+        if (opnd == 1) {
+          const int32_t *bt = PAGED ? p.block_table + (int64_t)ti.b * p.bt_stride : nullptr;
+#pragma unroll
+          for (int q = 0; q < kMaxChunks; ++q) {
+            vsr[q] = 0.f;
+            if (q < per_row) {
+              const int key = kt * kBlockN + (c + 128 * q) / per_row;
+              if (key < ti.sk) {
+                int64_t tok;
+                if constexpr (PAGED) {
+                  const int page = __ldg(bt + (key >> p.page_shift));
+                  tok = (int64_t)page * p.page_size + (key & (p.page_size - 1));
+                } else {
+                  tok = (int64_t)ti.k_row0 + key;
+                }
+                vsr[q] = __ldg(p.v_scale + tok * p.hkv + ti.hk);
+              }
+            }
+          }
+        }
+        uint4 raw[kMaxChunks];
+#pragma unroll
+        for (int q = 0; q < kMaxChunks; ++q)
+          if (q < per_row) raw[q] = *reinterpret_cast<const uint4 *>(stage + (size_t)(c + 128 * q) * 16);
+        named_bar_sync(2, 128);
+#pragma unroll
+        for (int q = 0; q < kMaxChunks; ++q) {
+          if (q >= per_row) break;
+          const int idx = c + 128 * q;
+          const int row = idx / per_row, ch = idx - row * per_row;   // 16 dims starting at 16*ch
+          const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            o[2 * k] = e4m3x2_to_bf16x2(w[k] & 0xFFFFu);
+            o[2 * k + 1] = e4m3x2_to_bf16x2(w[k] >> 16);
+          }
+          if (opnd == 1) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o[k] = pack_f16x2(__uint_as_float(o[k] << 16) * vsr[q], __uint_as_float(o[k] & 0xFFFF0000u) * vsr[q]);
+          }
+          const int d0 = ch * 16, cb = d0 >> 6, c8 = (d0 & 63) >> 3;
+          uint8_t *blk = buf + cb * kBlockN * 128 + row * 128;
+          *reinterpret_cast<uint4 *>(blk + (((c8) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(blk + (((c8 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32((opnd == 0 ? k_full : v_full) + st));
+        named_bar_sync(2, 128);   // staging of the next operand may reuse registers only
+      }
+    }
+  } else if (warp == Cfg::kWarpMMA) {
     // ------------------------------------------------------- MMA issuer --
     constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, DV, 0, 1);
+    // e4m3 K/V: PV runs on f16 operands (P and the scaled V), whose 11-bit
+    // mantissas keep the two extra roundings of that path well below bf16's.
+    constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kBlockM, DV, 0, 1) : idesc_bf16_f32(kBlockM, DV, 0, 1);
     const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
     bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
 
@@ -376,6 +518,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------- softmax --
+    if constexpr (FP8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsSoftmax));
     const int r = threadIdx.x;               // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int i = ti.q0 + r;                 // sequence-local query row
@@ -384,8 +527,28 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
     float l = 0.f;
     int it = 0;
     bool ok = true;
+    const int32_t *btab = PAGED ? p.block_table + (int64_t)ti.b * p.bt_stride : nullptr;
     for (int kt = first_kt; kt < ti.kt_hi; kt = next_tile<Cfg>(p, ti, kt), ++it) {
       const int sb = it & 1;
+      float *ksc = sc + (it & 1) * 2 * kBlockN;   // k scales of this tile's keys
+      if constexpr (FP8) {
+        // Per-token k scales of the tile's 128 keys: thread r fetches key j0 + r
+        // (0 past the sequence end), shared through a softmax-only barrier.
+        const int key = kt * kBlockN + r;
+        float ks = 0.f;
+        if (key < ti.sk) {
+          int64_t tok;
+          if constexpr (PAGED) {
+            const int page = __ldg(btab + (key >> p.page_shift));
+            tok = (int64_t)page * p.page_size + (key & (p.page_size - 1));
+          } else {
+            tok = (int64_t)ti.k_row0 + key;
+          }
+          ks = __ldg(p.k_scale + tok * p.hkv + ti.hk);
+        }
+        ksc[r] = ks;
+        named_bar_sync(1, kBlockM);
+      }
       ok = mbar_wait(smem_u32(s_full + sb), (it >> 1) & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -404,6 +567,19 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
       if (p.window > 0) {
         if (j0 < ti.ip_max - p.window + 1) need_mask = true;
         if (!p.causal && j0 + kBlockN - 1 > ti.ip_min + p.window - 1) need_mask = true;
+      }
+      if constexpr (FP8) {
+        // S_ij = <q_i, e4m3(k_j)> * k_scale_j  (scale folded after the MMA)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 k4 = *reinterpret_cast<const float4 *>(ksc + c * 32 + e);
+            s[c][e] *= k4.x;
+            s[c][e + 1] *= k4.y;
+            s[c][e + 2] *= k4.z;
+            s[c][e + 3] *= k4.w;
+          }
       }
       float tmax = -INFINITY;
 #pragma unroll
@@ -456,7 +632,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
           const float p0 = ex2(s[c][e] - m_use);
           const float p1 = ex2(s[c][e + 1] - m_use);
           lsum += p0 + p1;
-          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
       }
       l += lsum;
@@ -527,7 +703,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 6) {
+  if (warp == Cfg::kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }

@@ -1,30 +1,10 @@
-// Prefill kernel instantiations for (Dk, Dv) = (192, 128).
-#include "fa_internal.h"
+// Prefill kernel instantiations for (Dk, Dv) = (192, 128): the single-query-
+// tile kernel, bf16 or e4m3 K/V.
+#include "fa_prefill1_launch.cuh"
 
 namespace fa {
-namespace {
-template <bool PAGED, bool FP8, int MOD>
-cudaError_t launch_one(const PrefillLaunch &L) {
-  using Cfg = PrefillCfg<192, 128, PAGED, FP8, MOD>;
-  static unsigned long long done = 0;
-  auto kern = fa_prefill_kernel<192, 128, PAGED, FP8, MOD>;
-  cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
-  if (e != cudaSuccess) return e;
-  kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
-  return cudaGetLastError();
-}
-template <bool PAGED, bool FP8>
-cudaError_t by_mod(const PrefillLaunch &L) {
-  switch (L.mod) {
-    case 0: return launch_one<PAGED, FP8, 0>(L);
-    case 1: return launch_one<PAGED, FP8, 1>(L);
-    default: return launch_one<PAGED, FP8, 2>(L);
-  }
-}
-}  // namespace
-
 cudaError_t launch_prefill_192_128(const PrefillLaunch &L) {
-  if (L.fp8) return cudaErrorNotSupported;
-  return L.paged ? by_mod<true, false>(L) : by_mod<false, false>(L);
+  if (L.fp8) return launch_prefill1_fp8<192, 128>(L);
+  return L.paged ? launch_prefill1_mod<192, 128, true, false>(L) : launch_prefill1_mod<192, 128, false, false>(L);
 }
 }  // namespace fa
