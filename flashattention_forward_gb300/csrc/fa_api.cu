@@ -499,6 +499,9 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   }
   p.head_group = (int)head_group;
   p.n_hgroups = (int)n_hgroups;
+  p.n_items = (int)n_blocks;
+  // One CTA per work item: the hardware hands items to SMs as they free up,
+  // which balances ragged batches.
   L.grid = dim3((unsigned)n_blocks, 1, 1);
   L.stream = s;
   cudaError_t e;

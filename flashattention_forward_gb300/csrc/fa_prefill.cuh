@@ -63,14 +63,15 @@ struct PrefillParams {
   int *err;             // device error word
   int32_t head_group;   // heads interleaved per group in the block order
   int32_t n_hgroups;    // ceil(hq / head_group)
+  int32_t n_items;      // work items (persistent kernels stride over them)
 };
 
 // Block order: for each sequence, for each group of `head_group` heads, query
 // tiles from the latest (longest under a causal mask) to the first, the heads
 // of the group interleaved.  Concurrent CTAs then share the K/V of a few
 // heads through L2, and long tiles start first.  Returns false for padding.
-__device__ __forceinline__ bool decode_block(const PrefillParams &p, int &b, int &h, int &qt) {
-  unsigned L = blockIdx.x;
+__device__ __forceinline__ bool decode_block(const PrefillParams &p, int item, int &b, int &h, int &qt) {
+  unsigned L = (unsigned)item;
   const int g_in = (int)(L % (unsigned)p.head_group);
   L /= (unsigned)p.head_group;
   const int pr = (int)(L % (unsigned)p.n_qtiles);
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV, PAGED, FP8, MOD>::kThreads,
 
   // ------------------------------------------------------------ work tile --
   TileInfo ti;
-  if (!decode_block(p, ti.b, ti.h, ti.qt)) return;
+  if (!decode_block(p, (int)blockIdx.x, ti.b, ti.h, ti.qt)) return;
   ti.hk = ti.h / p.group;
   {
     const int qa = __ldg(p.cu_q + ti.b), qb = __ldg(p.cu_q + ti.b + 1);

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
   // ------------------------------------------------------------ work tile --
   PairInfo pi;
   int pt;
-  if (!decode_block(p, pi.b, pi.h, pt)) return;
+  if (!decode_block(p, (int)blockIdx.x, pi.b, pi.h, pt)) return;
   pi.hk = pi.h / p.group;
   {
     const int qa = __ldg(p.cu_q + pi.b), qb = __ldg(p.cu_q + pi.b + 1);
