@@ -154,19 +154,21 @@ def make_call(p, t, num_splits=0):
     lse = torch.empty((p.hq, p.total_q), dtype=torch.float32, device=dev)
     ws = None
     if num_splits is None:
-        num_splits = fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size)
+        num_splits = fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size,
+                                       p.total_k)
     if num_splits > 1:
         ws = torch.empty(fa.workspace_bytes(p.num_seqs, p.total_q, p.hq, p.dv, num_splits), dtype=torch.uint8,
                          device=dev)
 
-    def call(tt=t, o=out, l=lse):
-        fa.fwd_varlen(tt["q"], tt["k"], tt["v"], tt["cu_q"], tt["cu_k"], max_seqlen_q=p.max_seqlen_q,
-                      max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, block_table=tt.get("bt"),
-                      page_size=p.page_size, k_scale=tt.get("k_scale"), v_scale=tt.get("v_scale"),
+    plan = fa.FwdPlan(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
+                      max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, block_table=t.get("bt"),
+                      page_size=p.page_size, k_scale=t.get("k_scale"), v_scale=t.get("v_scale"),
                       softmax_scale=p.softmax_scale, causal=p.causal, window=p.window, score_mod=p.mod_kind,
-                      alibi_slope=p.alibi_slope, softcap=p.softcap, block_mask=tt.get("bm"),
-                      num_splits=num_splits, out=o, lse=l, workspace=ws)
-        return o, l
+                      alibi_slope=p.alibi_slope, softcap=p.softcap, block_mask=t.get("bm"),
+                      num_splits=num_splits, out=out, lse=lse, workspace=ws)
+
+    def call():
+        return plan.run()
     launches = 1 + (1 if num_splits > 1 else 0)
     return call, launches, out, lse
 
@@ -434,8 +436,17 @@ def other_workloads(dev, warmup, steps, flush, pk):
         call()
     torch.cuda.synchronize()
     wall_us = (time.perf_counter() - w0) / 200 * 1e6
-    res["dense_causal_b2_h4_s128_d64"] = {"device_us": 1e3 * statistics.median(times), "wall_us_per_call": wall_us,
-                                          "tflops": fi.prefill_flops(p) / (statistics.median(times) * 1e-3) / 1e12}
+    # device time per launch: events around 200 back-to-back launches
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record()
+    for _ in range(200):
+        call()
+    e_ev.record()
+    e_ev.synchronize()
+    dev_us = s_ev.elapsed_time(e_ev) / 200 * 1e3
+    res["dense_causal_b2_h4_s128_d64"] = {"device_us_per_launch": dev_us, "wall_us_per_call": wall_us,
+                                          "single_call_event_us": 1e3 * statistics.median(times),
+                                          "tflops": fi.prefill_flops(p) / (dev_us * 1e-6) / 1e12}
     # paged split-KV decode: KV-cache GB/s
     p = fi.config3()
     t = dev_tensors(p, dev)
@@ -444,7 +455,7 @@ def other_workloads(dev, warmup, steps, flush, pk):
     ms = statistics.mean(times)
     gbs = fi.decode_bytes(p) / (ms * 1e-3) / 1e9
     res["paged_decode_64seq_hq32_hkv8_p16"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
-                                               "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16),
+                                               "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16, p.total_k),
                                                "bytes": fi.decode_bytes(p)}
     # paged e4m3 KV, Q/K 192, V/O 128, page 64, 16 seqs U{1..4096}, causal
     p = fi.config4()

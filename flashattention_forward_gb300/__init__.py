@@ -80,7 +80,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.c_int32]
             L.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
-            L.fa_fwd_default_splits.argtypes = [ctypes.c_int32] * 6
+            L.fa_fwd_default_splits.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
             L.fa_fwd_default_splits.restype = ctypes.c_int32
             L.fa_combine.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -113,10 +114,10 @@ def as_tensor(t: Optional[torch.Tensor], fa_dtype: Optional[int] = None) -> Opti
     d = Tensor()
     d.data = t.data_ptr() if t.numel() else 0
     d.dtype = _DT[t.dtype] if fa_dtype is None else fa_dtype
-    d.ndim = t.dim()
-    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
-        d.shape[i] = s
-        d.stride[i] = st
+    n = t.dim()
+    d.ndim = n
+    d.shape[:n] = t.shape
+    d.stride[:n] = t.stride()
     return d
 
 
@@ -129,8 +130,8 @@ def _stream_ptr(stream) -> int:
     return s.cuda_stream
 
 
-def default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size=0) -> int:
-    return int(lib().fa_fwd_default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size))
+def default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size=0, total_k=0) -> int:
+    return int(lib().fa_fwd_default_splits(num_seqs, max_seqlen_q, max_seqlen_k, int(total_k), hq, hkv, page_size))
 
 
 def workspace_bytes(num_seqs, total_q, hq, dv, num_splits) -> int:
@@ -171,7 +172,7 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     if total_k is None:
         total_k = k_cache.shape[0] if block_table is None else 0
     if num_splits is None:
-        num_splits = default_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, page_size)
+        num_splits = default_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, page_size, total_k)
         if kv_dt != FA_BF16 or Dk != Dv or score_mod != MOD_NONE or block_mask is not None:
             num_splits = 0
     launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
@@ -223,6 +224,75 @@ def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                                    int(window), ctypes.byref(sm), None, int(page_size), ctypes.byref(launch),
                                    ctypes.c_void_p(_stream_ptr(stream))))
     return out, lse
+
+
+class FwdPlan:
+    """A prepared fwd_varlen call: the argument descriptors are built once and
+    run() re-issues the C call with them (for repeated calls on the same
+    buffers -- serving loops, benchmarks -- where per-call marshalling would
+    dominate small problems).  Takes the arguments of fwd_varlen; the tensors
+    must stay alive and keep their storage while the plan is used."""
+
+    def __init__(self, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, **kw):
+        L = lib()
+        self._keep = [q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k] + [v for v in kw.values()
+                                                                           if isinstance(v, torch.Tensor)]
+        B = cu_seqlens_q.shape[0] - 1
+        Tq, Hq, Dk = q.shape
+        Dv = v_cache.shape[-1]
+        Hkv = k_cache.shape[-2]
+        kv_dt = FA_BF16 if k_cache.dtype == torch.bfloat16 else FA_E4M3
+        self.out = kw.get("out")
+        if self.out is None:
+            self.out = torch.empty((Tq, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+        self.lse = kw.get("lse")
+        if self.lse is None and kw.get("return_lse", True):
+            self.lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+        scale = kw.get("softmax_scale")
+        if scale is None:
+            scale = 1.0 / math.sqrt(Dk)
+        block_table = kw.get("block_table")
+        total_k = kw.get("total_k")
+        if total_k is None:
+            total_k = k_cache.shape[0] if block_table is None else 0
+        page_size = kw.get("page_size", 0)
+        score_mod = kw.get("score_mod", MOD_NONE)
+        block_mask = kw.get("block_mask")
+        num_splits = kw.get("num_splits")
+        if num_splits is None:
+            num_splits = default_splits(B, kw["max_seqlen_q"], kw["max_seqlen_k"], Hq, Hkv, page_size, total_k)
+            if kv_dt != FA_BF16 or Dk != Dv or score_mod != MOD_NONE or block_mask is not None:
+                num_splits = 0
+        self.launch = Launch(num_seqs=B, max_seqlen_q=kw["max_seqlen_q"], max_seqlen_k=kw["max_seqlen_k"],
+                             num_splits=num_splits, total_q=Tq, total_k=total_k)
+        ws = kw.get("workspace")
+        if num_splits > 1:
+            need = workspace_bytes(B, Tq, Hq, Dv, num_splits)
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+            self.launch.workspace = ws.data_ptr()
+            self.launch.workspace_bytes = ws.numel()
+        self._ws = ws
+        self._sm = ScoreMod(kind=score_mod, alibi_slope=kw.get("alibi_slope", 0.0), softcap=kw.get("softcap", 0.0))
+        self._bm = None
+        if block_mask is not None:
+            self._bm = BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1],
+                                 n_kblk=block_mask.shape[2], blk_q=128, blk_k=128)
+        descs = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
+                 as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(kw.get("k_scale")),
+                 as_tensor(kw.get("v_scale")), as_tensor(self.out), as_tensor(self.lse)]
+        self._descs = descs
+        self._head = tuple(_ref(a) for a in descs) + (
+            ctypes.c_float(scale), ctypes.c_int32(int(bool(kw.get("causal", False)))),
+            ctypes.c_int32(int(kw.get("window", 0))), ctypes.byref(self._sm), _ref(self._bm),
+            ctypes.c_int32(int(page_size)), ctypes.byref(self.launch))
+        self._fn = L.fa_fwd_varlen
+
+    def run(self, stream=None):
+        st = self._fn(*self._head, ctypes.c_void_p(_stream_ptr(stream)))
+        if st != FA_OK:
+            _check(st)
+        return self.out, self.lse
 
 
 def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -155,16 +155,25 @@ size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int
   return align256(o) + align256(l);
 }
 
-int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t hq, int32_t hkv,
-                              int32_t page_size) {
+int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k, int64_t total_k,
+                              int32_t hq, int32_t hkv, int32_t page_size) {
   (void)page_size;
   if (num_seqs <= 0 || hq <= 0 || hkv <= 0 || hq % hkv) return 0;
   const int64_t rows = (int64_t)max_seqlen_q * (hq / hkv);
   if (rows <= 0 || rows > fa::kDecRows) return 0;
   if (max_seqlen_k < 256) return 0;
-  // Fixed-size key ranges of about 512 keys keep the work per CTA uniform;
-  // ranges past a shorter sequence's end cost one LSE store each.
-  int64_t s = (max_seqlen_k + 511) / 512;
+  // Key ranges sized so that the non-empty (split, kv head, sequence) CTAs
+  // make about three waves at two CTAs per SM: long ranges keep each CTA's
+  // pipeline fill and partial-output traffic small, three waves bound the tail.
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const double mean_k = total_k > 0 ? (double)total_k / num_seqs : 0.5 * max_seqlen_k;
+  const double key_units = mean_k * num_seqs * hkv;
+  const double target_ctas = 3.0 * 2.0 * sms;
+  double keys_per_split = key_units / target_ctas;
+  if (keys_per_split < 256) keys_per_split = 256;
+  int64_t s = (int64_t)((max_seqlen_k + keys_per_split - 1) / keys_per_split);
   if (s > 64) s = 64;
   if (s < 1) s = 1;
   return (int32_t)s;

@@ -73,7 +73,8 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tens
   const int32_t dv = (int32_t)v_cache->shape[v_cache->ndim - 1];
   int32_t splits = launch->num_splits;
   if (splits <= 0)
-    splits = fa_fwd_default_splits(launch->num_seqs, launch->max_seqlen_q, launch->max_seqlen_k, hq, hkv, page_size);
+    splits = fa_fwd_default_splits(launch->num_seqs, launch->max_seqlen_q, launch->max_seqlen_k, launch->total_k, hq,
+                                   hkv, page_size);
   if (splits <= 1)
     return fa::set_host_error(FA_ERR_UNSUPPORTED,
                               "the allocation-free entry runs the split-KV decode only (needs 2 or more splits)");

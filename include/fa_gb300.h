@@ -163,10 +163,12 @@ size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int
 /*
  * Recommended split count for a problem (0 = single pass).  Split-KV applies
  * when few query rows share each kv head (decode: max_seqlen_q * Hq/Hkv <= 16)
- * and keys are long; the count spreads the key ranges over the SMs.
+ * and keys are long.  The key ranges are sized so that the non-empty CTAs make
+ * about three waves at two CTAs per SM of the current device; total_k (the
+ * sum of key lengths, 0 if unknown) refines the estimate of non-empty ranges.
  */
 int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
-                              int32_t hq, int32_t hkv, int32_t page_size);
+                              int64_t total_k, int32_t hq, int32_t hkv, int32_t page_size);
 
 /*
  * fa_combine -- merge of partial results over disjoint key ranges (the

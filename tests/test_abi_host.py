@@ -43,7 +43,9 @@ def test_workspace_bytes_and_default_splits(L):
     assert fa.workspace_bytes(4, 10, 8, 128, 0) == 0
     n = fa.workspace_bytes(64, 64, 32, 128, 16)
     assert n >= 16 * 64 * 32 * 128 * 4 + 16 * 32 * 64 * 4 and n % 256 == 0
-    assert fa.default_splits(64, 1, 8192, 32, 8, 16) == 16        # decode shape
+    s = fa.default_splits(64, 1, 8192, 32, 8, 16, 64 * 4400)   # decode shape
+    assert 2 <= s <= 8
+    assert fa.default_splits(64, 1, 8192, 32, 8, 16, 0) >= 1      # total unknown
     assert fa.default_splits(8, 2048, 2048, 16, 16, 0) == 0       # prefill shape
     assert fa.default_splits(64, 8, 8192, 32, 8, 16) == 0         # 8 * 4 rows > 16
 

@@ -216,3 +216,36 @@ def test_two_pass_softmax_variant(monkeypatch, causal):
     monkeypatch.setenv("FA_GB300_PREFILL_VARIANT", "1")
     check(fi.make_problem([300, 129, 700], [300, 400, 700], hq=4, hkv=2, dk=128, seed=31, causal=causal))
     check(fi.make_problem([200, 64], [500, 64], hq=4, dk=64, seed=32, causal=causal, mod="alibi"))
+
+
+# ------------------------------------------------------------- prepared call --
+
+@pytest.mark.parametrize("case", ["prefill_paged_causal", "decode_split", "fp8_alibi"])
+def test_fwd_plan_matches_call_and_oracle(case):
+    """FwdPlan (descriptors marshalled once, re-issued by run()) gives the
+    bit-identical result of fwd_varlen, on every re-run, and matches the oracle."""
+    import flashattention_forward_gb300 as fa
+    if case == "prefill_paged_causal":
+        p = fi.make_problem([300, 0, 129], [700, 5, 129], hq=8, hkv=2, dk=128, seed=41, causal=True,
+                            page_size=64)
+    elif case == "decode_split":
+        p = fi.make_problem([1] * 6, [3000, 1, 257, 4096, 0, 900], hq=16, hkv=2, dk=128, seed=42,
+                            page_size=16)
+    else:
+        p = fi.make_problem([200, 77], [450, 300], hq=4, hkv=2, dk=128, seed=43, kv_dtype="e4m3",
+                            mod="alibi")
+    t = to_device(p)
+    plan = fa.FwdPlan(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
+                      max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, block_table=t.get("bt"),
+                      page_size=p.page_size, k_scale=t.get("k_scale"), v_scale=t.get("v_scale"),
+                      softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
+                      score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap,
+                      block_mask=t.get("bm"))
+    if case == "decode_split":
+        assert plan.launch.num_splits > 1
+    ref_o, ref_l = host(*run_gpu(p, t, num_splits=plan.launch.num_splits))
+    for _ in range(3):
+        o, l = host(*plan.run())
+        assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l)
+    ro, rl = oracle.forward(p)
+    compare(o, l, ro, rl)

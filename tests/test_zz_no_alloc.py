@@ -41,7 +41,8 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
                              seed=21, page_size=32, spare_pages=4, causal=True)
     for p, splits in ((first, 0), (second, 5)):
         t = to_device(p)
-        want = splits or fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size)
+        want = splits or fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size,
+                                           p.total_k)
         assert want > 1
         ref_o, ref_l = host(*run_gpu(p, t, num_splits=want))     # existing entry, torch workspace
         got_o, got_l = host(*_noalloc(p, t, splits))
