@@ -33,7 +33,7 @@ import fa_inputs as fi  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (prefill) & KV-cache GB/s (decode), % of GB300 roofline"
 KERNEL_SOURCES = ["flashattention_forward_gb300/csrc/fa_prefill.cuh", "flashattention_forward_gb300/csrc/fa_prefill2.cuh",
-                  "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
+                  "flashattention_forward_gb300/csrc/fa_prefill3.cuh", "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
 
 
 def kernel_hash():

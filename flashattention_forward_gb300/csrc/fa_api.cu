@@ -402,8 +402,8 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   }
 
   // ------------------------------------------------------------ prefill --
-  // Dk <= 128 with bf16 K/V runs the two-query-tile kernel (256 rows per CTA).
-  const int64_t rows_per_cta = (Dk <= 128 && !fp8) ? 2 * fa::kBlockM : fa::kBlockM;
+  // Every prefill kernel computes two 128-row query tiles per CTA.
+  const int64_t rows_per_cta = 2 * fa::kBlockM;
   const int64_t n_qtiles = (launch->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   const int64_t head_group = Hq < 8 ? Hq : 8;
   const int64_t n_hgroups = (Hq + head_group - 1) / head_group;
@@ -419,16 +419,18 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
     if ((st = make_map(&L.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dq, sq, box, "q"))) return st;
   }
   const int rows_box = paged ? (page_size < fa::kBlockN ? page_size : fa::kBlockN) : fa::kBlockN;
+  // e4m3: 64-byte row pieces (one 64-column block) in boxes of at most 32
+  // rows, unswizzled; the converter warps turn each 32-row slice into the
+  // swizzled f16 operand in place.
+  const int rows_box8 = paged ? (page_size < 32 ? page_size : 32) : 32;
   if (have_keys && fp8) {
-    // e4m3: whole rows (Dk or Dv bytes) per box, no swizzle; the kernel
-    // converts them into the swizzled bf16 operand layout.
     if (paged) {
       const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
       const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2]), (uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
-      const uint32_t bk[4] = {(uint32_t)Dk, 1, (uint32_t)rows_box, 1};
-      const uint32_t bv[4] = {(uint32_t)Dv, 1, (uint32_t)rows_box, 1};
+      const uint32_t bk[4] = {64, 1, (uint32_t)rows_box8, 1};
+      const uint32_t bv[4] = {64, 1, (uint32_t)rows_box8, 1};
       if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, bk, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
       if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dv, sv, bv, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     } else {
@@ -436,8 +438,8 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
       const uint64_t dv[3] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)v_cache->shape[0]};
       const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
       const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
-      const uint32_t bk[3] = {(uint32_t)Dk, 1, (uint32_t)fa::kBlockN};
-      const uint32_t bv[3] = {(uint32_t)Dv, 1, (uint32_t)fa::kBlockN};
+      const uint32_t bk[3] = {64, 1, (uint32_t)rows_box8};
+      const uint32_t bv[3] = {64, 1, (uint32_t)rows_box8};
       if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, bk, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
       if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dv, sv, bv, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     }
@@ -481,8 +483,8 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   p.group = group;
   p.page_size = paged ? page_size : fa::kBlockN;
   p.page_shift = ilog2(p.page_size);
-  p.rows_per_box = rows_box;
-  p.pages_per_tile = fa::kBlockN / rows_box;
+  p.rows_per_box = fp8 ? rows_box8 : rows_box;
+  p.pages_per_tile = fa::kBlockN / p.rows_per_box;
   p.n_qtiles = (int)n_qtiles;
   p.causal = causal != 0;
   p.window = window;

@@ -29,6 +29,7 @@ struct DecodeLaunch {
 cudaError_t launch_prefill_64_64(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128(const PrefillLaunch &L);
 cudaError_t launch_prefill_192_128(const PrefillLaunch &L);
+cudaError_t launch_prefill_192_128_fp8(const PrefillLaunch &L);
 cudaError_t launch_decode(int d, const DecodeLaunch &L);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
                            int dv, void *out, float *lse, cudaStream_t stream);

@@ -1,0 +1,756 @@
+// fa_prefill3.cuh -- two-query-tile (ping-pong) tcgen05 FlashAttention forward
+// with a chunked K ring: the kernel for Q/K head dim 192 (V/O 128) and for
+// e4m3 K/V caches of every head dim.
+//
+// The schedule is the one of fa_prefill2.cuh: one CTA computes 256 query rows
+// of one (sequence, head) as two 128-row tiles A and B, each owned by a softmax
+// warpgroup, while the tensor core alternates between them:
+//
+//   MMA order:  QK_A(0) QK_B(0) | PV_A(0) QK_A(1) PV_B(0) QK_B(1) | PV_A(1) ...
+//
+// What changes is the staging of K.  With Dk = 192 the two Q tiles alone take
+// 96 KB of shared memory, so K is kept as a ring of 16 KB chunks (one 64-column
+// block of 128 keys each) rather than whole-tile stages: a chunk is refilled as
+// soon as the last QK that reads it completes, and the QK of the next tile can
+// start on its first chunk while the others still load.  V keeps whole-tile
+// stages (the PV operand spans its 64-column blocks at a fixed stride).
+//
+// e4m3 caches (FlyDSL PR #1066: paged FP8 K/V with per-token scales) are
+// staged by TMA as raw bytes and turned into f16 MMA operands in shared memory
+// by six converter warps:
+//   K' = RN_f16(e4m3(k) * k_scale),  V' = RN_f16(e4m3(v) * v_scale)
+// (one rounding each, fp32 product).  Q is brought to f16 in place with a
+// per-row power-of-two factor 2^e (exact for every bf16 value within 2^-28 of
+// the row maximum; the factor 2^-e returns in the softmax scale), so both
+// contractions run as kind::f16 with fp32 accumulation and P is packed as f16.
+// Each converted 32-row slice is staged in the upper half of its own output
+// region, so one warp converts it in place without waiting for other warps.
+//
+// TMEM (512 columns):  S_A [0,128)  S_B [128,256)  O_A [256,384)  O_B [384,512)
+// with P_X (16-bit, the A operand of PV) written over the first 64 columns of S_X.
+//
+// Warps: 0-3 softmax A, 4-7 softmax B, 8 TMA producer, 9 TMEM allocation + MMA
+// issue; e4m3: 10-15 converters (16 warps); bf16: 10-11 idle in the 12-warp
+// variant (warpgroup 2 hands its registers to the softmax warpgroups).
+#pragma once
+#include "fa_prefill2.cuh"
+
+namespace fa {
+
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
+struct Prefill3Cfg {
+  static constexpr int KC = DK / 64;              // 16 KB chunks per K tile
+  static constexpr int VC = DV / 64;              // 64-column blocks per V tile
+  static constexpr int kChunkBytes = kBlockN * 128;
+  static constexpr int kQTileBytes = kBlockM * DK * 2;
+  static constexpr int kVBytes = VC * kChunkBytes;
+  static constexpr int kRing = 229376 - 2 * kQTileBytes;   // 224 KB minus the Q tiles
+  static constexpr int NSV = (DV <= 64) ? 6 : 2;
+  static constexpr int NCK_raw = (kRing - NSV * kVBytes) / kChunkBytes;
+  static constexpr int NCK = NCK_raw > 8 ? 8 : NCK_raw;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = 2 * kQTileBytes;
+  static constexpr int kOffV = kOffK + NCK * kChunkBytes;
+  static constexpr int kOffBar = kOffV + NSV * kVBytes;
+  // q_full, q_conv[2], kc_full/kc_empty/kc_stage[NCK], v_full/v_empty/v_stage[NSV],
+  // s_full[2], p_full[2], o_done[2]
+  static constexpr int kNumBars = 3 + 3 * NCK + 3 * NSV + 6;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64;
+  // e4m3: 16 warps, always with the register split; bf16: BIGREG selects the
+  // 12-warp split variant, otherwise 10 warps without setmaxnreg.
+  static constexpr bool kSplitRegs = FP8 || BIGREG;
+  static constexpr int kWarps = FP8 ? 16 : (BIGREG ? 12 : 10);
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kRegsSoftmax = 208;
+  static constexpr int kRegsOther = FP8 ? 48 : 80;
+  static constexpr int kPoolNeeded = 8 * 32 * kRegsSoftmax + (kWarps - 8) * 32 * kRegsOther;
+  static constexpr int kConverters = 6;
+  static constexpr int kSlicesPerTile = (KC + VC) * 4;   // 32-row slices
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dims");
+  static_assert(NCK >= KC, "the K ring holds at least one tile");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(!kSplitRegs || kPoolNeeded <= 65536, "register split exceeds the register file");
+};
+
+// f16 pair (packed) -> two fp32 values.
+__device__ __forceinline__ void unpack_f16x2(uint32_t h, float &lo, float &hi) {
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+}
+
+// Two e4m3 bytes (low 16 bits of `two`) -> f16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(two));
+  return h;
+}
+
+// Four e4m3 bytes times an fp32 scale -> two f16 pairs (one rounding each).
+__device__ __forceinline__ void e4m3x4_scaled_f16(uint32_t w, float s, uint32_t &o0, uint32_t &o1) {
+  float a, b, c, d;
+  unpack_f16x2(e4m3x2_to_f16x2(w & 0xFFFFu), a, b);
+  unpack_f16x2(e4m3x2_to_f16x2(w >> 16), c, d);
+  o0 = pack_f16x2(a * s, b * s);
+  o1 = pack_f16x2(c * s, d * s);
+}
+
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
+__global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::kThreads, 1)
+    fa_prefill3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>;
+  constexpr int KC = Cfg::KC, VC = Cfg::VC, NCK = Cfg::NCK, NSV = Cfg::NSV;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 128-byte-swizzled operands need 1024-byte aligned chunks.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_error(p.err, kErrBounds);
+    return;
+  }
+
+  // ------------------------------------------------------------ work tile --
+  PairInfo pi;
+  int pt;
+  if (!decode_block(p, (int)blockIdx.x, pi.b, pi.h, pt)) return;
+  pi.hk = pi.h / p.group;
+  {
+    const int qa = __ldg(p.cu_q + pi.b), qb = __ldg(p.cu_q + pi.b + 1);
+    const int ka = __ldg(p.cu_k + pi.b), kb = __ldg(p.cu_k + pi.b + 1);
+    pi.sq = qb - qa;
+    pi.sk = kb - ka;
+    pi.q_row0 = qa + pt * 2 * kBlockM;
+    pi.k_row0 = ka;
+  }
+  if (pt * 2 * kBlockM >= pi.sq) return;
+  pi.kt_lo = 1 << 30;
+  pi.kt_hi = 0;
+#pragma unroll
+  for (int X = 0; X < 2; ++X) {
+    Half &hx = pi.x[X];
+    hx.qt = pt * 2 + X;
+    hx.q0 = hx.qt * kBlockM;
+    hx.valid = hx.q0 < pi.sq;
+    hx.klo = hx.khi = 0;
+    if (!hx.valid) continue;
+    const int last = min(hx.q0 + kBlockM, pi.sq) - 1;
+    hx.ip_min = hx.q0 + pi.sk - pi.sq;
+    hx.ip_max = last + pi.sk - pi.sq;
+    int lo = 0, hi = pi.sk;
+    if (p.causal) hi = min(hi, hx.ip_max + 1);
+    if (p.window > 0) {
+      lo = max(lo, hx.ip_min - p.window + 1);
+      if (!p.causal) hi = min(hi, hx.ip_max + p.window);
+    }
+    if (hi > lo) {
+      hx.klo = lo / kBlockN;
+      hx.khi = (hi + kBlockN - 1) / kBlockN;
+      pi.kt_lo = min(pi.kt_lo, hx.klo);
+      pi.kt_hi = max(pi.kt_hi, hx.khi);
+    }
+  }
+  if (pi.kt_hi == 0) pi.kt_lo = 0;
+  int first_kt = pi.kt_lo;
+  if (first_kt < pi.kt_hi && !half_active(p, pi, 0, first_kt) && !half_active(p, pi, 1, first_kt))
+    first_kt = pair_next(p, pi, first_kt);
+  int n_tiles = 0;
+  for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt)) ++n_tiles;
+
+  if (n_tiles == 0) {
+    for (int e = threadIdx.x; e < 2 * kBlockM; e += blockDim.x) {
+      const int i = pt * 2 * kBlockM + e;
+      if (i >= pi.sq) break;
+      const int64_t t = (int64_t)pi.q_row0 + e;
+      __nv_bfloat16 *o = p.out + t * p.out_stride_t + (int64_t)pi.h * p.out_stride_h;
+      for (int d = 0; d < DV; d += 8) *reinterpret_cast<uint4 *>(o + d) = make_uint4(0, 0, 0, 0);
+      if (p.lse) p.lse[(int64_t)pi.h * p.total_q + t] = -INFINITY;
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- shared mem --
+  uint8_t *sQ = smem + Cfg::kOffQ;
+  uint8_t *sK = smem + Cfg::kOffK;
+  uint8_t *sV = smem + Cfg::kOffV;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+  uint64_t *q_full = bars;
+  uint64_t *q_conv = bars + 1;          // [2] Q tile in f16 (e4m3 caches)
+  uint64_t *kc_full = bars + 3;         // [NCK] chunk holds its MMA operand
+  uint64_t *kc_empty = kc_full + NCK;   // [NCK] last QK reading it completed
+  uint64_t *kc_stage = kc_empty + NCK;  // [NCK] e4m3 bytes landed
+  uint64_t *v_full = kc_stage + NCK;
+  uint64_t *v_empty = v_full + NSV;
+  uint64_t *v_stage = v_empty + NSV;
+  uint64_t *s_full = v_stage + NSV;     // [2]
+  uint64_t *p_full = s_full + 2;        // [2]
+  uint64_t *o_done = p_full + 2;        // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 8);
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(q_conv + 0), kBlockM);
+    mbar_init(smem_u32(q_conv + 1), kBlockM);
+    for (int s = 0; s < NCK; ++s) {
+      mbar_init(smem_u32(kc_full + s), FP8 ? 4 : 1);         // e4m3: one arrive per converted slice
+      mbar_init(smem_u32(kc_empty + s), 1);
+      mbar_init(smem_u32(kc_stage + s), 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(smem_u32(v_full + s), FP8 ? 4 * VC : 1);
+      mbar_init(smem_u32(v_empty + s), 1);
+      mbar_init(smem_u32(v_stage + s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(s_full + x), 1);
+      mbar_init(smem_u32(p_full + x), kBlockM);
+      mbar_init(smem_u32(o_done + x), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Register split: the softmax warpgroups take what the other warpgroups
+  // release.  The host launches a split variant only when the kernel's launch
+  // register count makes Cfg::kPoolNeeded fit the CTA's register pool.
+  if (Cfg::kSplitRegs && warp >= 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsOther));
+
+  const int32_t *bt = PAGED ? p.block_table + (int64_t)pi.b * p.bt_stride : nullptr;
+
+  if (warp == 8) {
+    // ------------------------------------------------ producer: Q, K, V --
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      mbar_expect_tx(smem_u32(q_full), 2 * Cfg::kQTileBytes);
+#pragma unroll
+      for (int X = 0; X < 2; ++X)
+#pragma unroll
+        for (int cb = 0; cb < KC; ++cb)
+          tma_load_3d(smem_u32(sQ + X * Cfg::kQTileBytes + cb * kBlockM * 128), &tm_q, smem_u32(q_full), cb * 64,
+                      pi.h, pi.q_row0 + X * kBlockM);
+      // One 64-column block of a K or V tile into a 16 KB chunk: bf16 rows
+      // land swizzled (the MMA operand); e4m3 rows land raw, 64 bytes each, in
+      // the upper half of their 32-row slice, for the converters.
+      auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int cb, int kt) {
+        const int rb = p.rows_per_box;
+        for (int r0 = 0; r0 < kBlockN; r0 += rb) {
+          const uint32_t at = FP8 ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64)
+                                  : smem_u32(dst + r0 * 128);
+          if constexpr (PAGED) {
+            const int key0 = kt * kBlockN + r0;
+            const int page = key0 < pi.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+            tma_load_4d(at, tm, smem_u32(bar), cb * 64, pi.hk, key0 & (p.page_size - 1), page);
+          } else {
+            tma_load_3d(at, tm, smem_u32(bar), cb * 64, pi.hk, pi.k_row0 + kt * kBlockN + r0);
+          }
+        }
+      };
+      constexpr uint32_t kBlockBytes = FP8 ? kBlockN * 64 : kBlockN * 128;
+      int j = 0;
+      bool ok = true;
+      for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt), ++j) {
+#pragma unroll 1
+        for (int c = 0; c < KC; ++c) {
+          const int n = j * KC + c, slot = n % NCK;
+          if (n >= NCK && !(ok = mbar_wait(smem_u32(kc_empty + slot), ((n / NCK) - 1) & 1, abort_flag, p.err)))
+            break;
+          uint64_t *bar = FP8 ? kc_stage + slot : kc_full + slot;
+          mbar_expect_tx(smem_u32(bar), kBlockBytes);
+          load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c, kt);
+        }
+        if (!ok) break;
+        const int sv = j % NSV;
+        if (j >= NSV && !(ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err))) break;
+        uint64_t *vbar = FP8 ? v_stage + sv : v_full + sv;
+        mbar_expect_tx(smem_u32(vbar), VC * kBlockBytes);
+#pragma unroll 1
+        for (int c = 0; c < VC; ++c) load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c, kt);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer --
+    constexpr uint32_t idesc_qk = FP8 ? idesc_f16_f32(kBlockM, kBlockN, 0, 0) : idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+    constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kBlockM, DV, 0, 1) : idesc_bf16_f32(kBlockM, DV, 0, 1);
+    const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+    int n_pv[2] = {0, 0};
+    bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
+    bool q_ready[2] = {!FP8, !FP8};
+
+    // Descriptor words, computed once.  K-major 128-byte-swizzled operands
+    // step 32 bytes per K=16 slice inside a 64-column block; a Q tile's blocks
+    // are 16 KB apart and each K block sits in its own ring chunk.  V
+    // (MN-major) has its two 64-column blocks 16 KB apart and steps 16 rows.
+    const uint64_t dq0 = smem_desc_sw128(sQa, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sKa, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sVa, Cfg::kChunkBytes, 1024);
+    const uint32_t q_lo = (uint32_t)dq0, k_lo = (uint32_t)dk0, qk_hi = (uint32_t)(dq0 >> 32);
+    const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
+    // QK_X of the j-th tile.  `first`: wait for each chunk to be filled;
+    // `last`: release each chunk once this QK has read it.
+    auto qk = [&](int X, int j, bool first, bool last) -> bool {
+      if (!q_ready[X]) {
+        if (!mbar_wait(smem_u32(q_conv + X), 0, abort_flag, p.err)) return false;
+        q_ready[X] = true;
+      }
+      const uint32_t d = tmem + (X ? 128u : 0u);
+      const uint32_t a0 = q_lo + (uint32_t)(X * (Cfg::kQTileBytes >> 4));
+#pragma unroll
+      for (int c = 0; c < KC; ++c) {
+        const int n = j * KC + c, slot = n % NCK;
+        if (first) {
+          if (!mbar_wait(smem_u32(kc_full + slot), (n / NCK) & 1, abort_flag, p.err)) return false;
+          tc_fence_after();
+        }
+        const uint32_t a = a0 + (uint32_t)(c * ((kBlockM * 128) >> 4));
+        const uint32_t b = k_lo + (uint32_t)(slot * (Cfg::kChunkBytes >> 4));
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          if (c == 0 && ks == 0) mma_ss_w<0>(d, a, qk_hi, b, qk_hi, idesc_qk);
+          else mma_ss_w<1>(d, a + 2 * ks, qk_hi, b + 2 * ks, qk_hi, idesc_qk);
+        }
+        if (last) tc_commit(smem_u32(kc_empty + slot));
+      }
+      tc_commit(smem_u32(s_full + X));
+      return true;
+    };
+    auto pv = [&](int X, int sv) {
+      const uint32_t a = tmem + (X ? 128u : 0u);                 // P_X aliases S_X
+      const uint32_t d = tmem + 256u + (X ? 128u : 0u);
+      uint32_t b = v_lo + (uint32_t)(sv * (Cfg::kVBytes >> 4));
+      const uint32_t acc0 = n_pv[X] > 0 ? 1u : 0u;
+#pragma unroll
+      for (int ks = 0; ks < kBlockN / 16; ++ks) {
+        mma_ts_w(d, a + ks * 8, b, v_hi, idesc_pv, ks > 0 ? 1u : acc0);
+        b += (16 * 128) >> 4;
+      }
+      tc_commit(smem_u32(o_done + X));
+    };
+
+    if (lane == 0 && ok) {
+      bool a0 = half_active(p, pi, 0, first_kt), a1 = half_active(p, pi, 1, first_kt);
+      if (a0) ok = qk(0, 0, true, !a1);
+      if (ok && a1) ok = qk(1, 0, !a0, true);
+      int j = 0;
+      for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
+        const int kn = pair_next(p, pi, kt);
+        const bool more = kn < pi.kt_hi;
+        const bool n0 = more && half_active(p, pi, 0, kn);
+        const bool n1 = more && half_active(p, pi, 1, kn);
+        const int sv = j % NSV;
+        if (!(ok = mbar_wait(smem_u32(v_full + sv), (j / NSV) & 1, abort_flag, p.err))) break;
+        if (a0) {
+          if (!(ok = mbar_wait(smem_u32(p_full + 0), n_pv[0] & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          pv(0, sv);
+          ++n_pv[0];
+        }
+        if (n0 && !(ok = qk(0, j + 1, true, !n1))) break;
+        if (a1) {
+          if (!(ok = mbar_wait(smem_u32(p_full + 1), n_pv[1] & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          pv(1, sv);
+          ++n_pv[1];
+        }
+        tc_commit(smem_u32(v_empty + sv));
+        if (n1 && !(ok = qk(1, j + 1, !n0, true))) break;
+        a0 = n0;
+        a1 = n1;
+        kt = kn;
+      }
+    }
+  } else if (warp >= 10) {
+    if constexpr (FP8) {
+      // ----------------------------------------- e4m3 -> f16 converters --
+      // Slice g (32 rows of one 64-column block; K blocks of a tile first,
+      // then V blocks) goes to warp g mod 6.  Lane l loads the scale of row l;
+      // each step converts 8 rows, 16 dims per lane, into the swizzled layout.
+      // Rows past the sequence end are written as zeros.
+      const int cw = warp - 10;
+      int j = 0;
+      int g = 0;
+      bool ok = true;
+      for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt), ++j) {
+        for (int s = 0; s < Cfg::kSlicesPerTile; ++s, ++g) {
+          if (g % Cfg::kConverters != cw) continue;
+          const bool isv = s >= KC * 4;
+          const int c = isv ? (s - KC * 4) >> 2 : s >> 2, q = s & 3;
+          uint8_t *base;
+          uint64_t *stage_bar, *full_bar;
+          uint32_t par;
+          if (!isv) {
+            const int n = j * KC + c, slot = n % NCK;
+            base = sK + slot * Cfg::kChunkBytes;
+            stage_bar = kc_stage + slot;
+            full_bar = kc_full + slot;
+            par = (n / NCK) & 1;
+          } else {
+            const int sv = j % NSV;
+            base = sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes;
+            stage_bar = v_stage + sv;
+            full_bar = v_full + sv;
+            par = (j / NSV) & 1;
+          }
+          const int key = kt * kBlockN + q * 32 + lane;
+          float sc = 0.f;
+          if (key < pi.sk) {
+            int64_t tok;
+            if constexpr (PAGED) {
+              const int page = __ldg(bt + (key >> p.page_shift));
+              tok = (int64_t)page * p.page_size + (key & (p.page_size - 1));
+            } else {
+              tok = (int64_t)pi.k_row0 + key;
+            }
+            sc = __ldg((isv ? p.v_scale : p.k_scale) + tok * p.hkv + pi.hk);
+          }
+          ok = mbar_wait(smem_u32(stage_bar), par, abort_flag, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          const uint8_t *stg = base + q * 4096 + 2048;
+          const int part = lane & 3;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int rr = 8 * t + (lane >> 2);              // row within the slice
+            const uint4 raw = *reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16);
+            const float s_row = __shfl_sync(0xffffffffu, sc, rr);
+            const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
+            uint32_t o[8];
+            e4m3x4_scaled_f16(raw.x, s_row, o[0], o[1]);
+            e4m3x4_scaled_f16(raw.y, s_row, o[2], o[3]);
+            e4m3x4_scaled_f16(raw.z, s_row, o[4], o[5]);
+            e4m3x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+            if (!live) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) o[k] = 0u;
+            }
+            const int r = q * 32 + rr;
+            uint8_t *row = base + r * 128;
+            *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(full_bar));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax --
+    if constexpr (Cfg::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsSoftmax));
+    const int X = warp >> 2;                  // 0: tile A, 1: tile B
+    const int r = threadIdx.x & 127;          // row in the tile == TMEM lane
+    const Half hx = X ? pi.x[1] : pi.x[0];
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colS = X ? 128u : 0u, colO = 256u + (X ? 128u : 0u);
+    const int i = hx.q0 + r;
+    const int ip = i + pi.sk - pi.sq;
+    float m_ref = -INFINITY, l = 0.f;
+    int cnt = 0;
+    bool ok = true;
+    // Row factor of the f16 Q row (e4m3 caches): S carries 2^e, undone here.
+    float rowf = 1.f;
+    if constexpr (FP8) {
+      ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
+      if (ok) {
+        // Row r owns 128 bytes of each 64-column block; its 16-byte units are
+        // visited from unit r mod 8 on, so a warp's accesses spread over all banks.
+        uint8_t *qrow = sQ + X * Cfg::kQTileBytes + r * 128;
+        float amax = 0.f;
+#pragma unroll
+        for (int cb = 0; cb < KC; ++cb)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + cb * kBlockM * 128 + ((u + r) & 7) * 16);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(ww[k] << 16)), fabsf(__uint_as_float(ww[k] & 0xFFFF0000u))));
+          }
+        int sh = 0;
+        if (amax > 0.f && amax <= 3.0e38f) {
+          const int E = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+          sh = min(141 - E, 126);               // amax * 2^sh in [2^14, 2^15)
+        }
+        const float up = __uint_as_float((uint32_t)(sh + 127) << 23);
+        rowf = __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+        for (int cb = 0; cb < KC; ++cb)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(qrow + cb * kBlockM * 128 + ((u + r) & 7) * 16);
+            const uint4 w = *ptr;
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            uint32_t hh[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              hh[k] = pack_f16x2(__uint_as_float(ww[k] << 16) * up, __uint_as_float(ww[k] & 0xFFFF0000u) * up);
+            *ptr = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+          }
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(smem_u32(q_conv + X));
+    }
+    // MOD 0 runs with a positive scale only (the host routes other scales to
+    // the general path), so raw scores can be maxed before scaling.
+    constexpr bool fast = (MOD == 0);
+    const float sl2 = p.scale_log2 * rowf;
+    const float sca = p.softcap_arg * rowf;
+    auto pack_p = [](float a, float b) -> uint32_t { return FP8 ? pack_f16x2(a, b) : pack_bf16x2(a, b); };
+    auto chunk_exp = [&](const float (&v)[32], float c, float m, uint32_t (&pk)[16], float (&acc)[4]) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float t0, t1;
+        fma2(t0, t1, v[e], v[e + 1], c, -m);
+        const float a0 = ex2(t0), a1 = ex2(t1);
+        const int q = ((e >> 1) & 1) * 2;
+        add2(acc[q], acc[q + 1], a0, a1);
+        pk[e >> 1] = pack_p(a0, a1);
+      }
+    };
+    const float cexp = fast ? sl2 : 1.f;
+    int j = -1;   // index of the tile in the pair's list (ring position)
+    for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
+      ++j;
+      if (!half_active_h(p, pi, hx, kt)) continue;
+      ok = mbar_wait(smem_u32(s_full + X), cnt & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = tmem + lane_base + colS;
+      const int j0 = kt * kBlockN;
+      bool need_mask = (j0 + kBlockN > pi.sk);
+      if (p.causal && j0 + kBlockN - 1 > hx.ip_min) need_mask = true;
+      if (p.window > 0) {
+        if (j0 < hx.ip_max - p.window + 1) need_mask = true;
+        if (!p.causal && j0 + kBlockN - 1 > hx.ip_min + p.window - 1) need_mask = true;
+      }
+      auto scores = [&](float (&v)[32], int jc) {
+        if (!fast) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x;
+            if constexpr (MOD == 2) {
+              const float t = v[e] * sca;
+              const float em = ex2(-2.f * kLog2e * fabsf(t));
+              x = copysignf(__fdividef(1.f - em, 1.f + em), t) * p.softcap_log2;
+            } else {
+              x = v[e] * sl2;
+            }
+            if constexpr (MOD == 1) x -= p.alibi_log2 * (float)abs(ip - (jc + e));
+            v[e] = x;
+          }
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int jj = jc + e;
+            bool allowed = jj < pi.sk;
+            if (p.causal) allowed = allowed && (jj <= ip);
+            if (p.window > 0) allowed = allowed && (p.causal ? (ip - jj < p.window) : (abs(ip - jj) < p.window));
+            v[e] = allowed ? v[e] : -INFINITY;
+          }
+        }
+      };
+      float alpha_tile = 1.f;
+      bool warp_need = false;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (BIGREG || FP8) {
+        float sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(sa + c * 32, sv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) scores(sv[c], j0 + c * 32);
+        float t1[43];
+#pragma unroll
+        for (int k = 0; k < 42; ++k) {
+          const int e = 3 * k;
+          t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+        }
+        t1[42] = fmaxf(sv[3][30], sv[3][31]);
+        float t2[15];
+#pragma unroll
+        for (int k = 0; k < 14; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+        t2[14] = t1[42];
+        float t3[5];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
+        float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
+        if (fast && tmax != -INFINITY) tmax *= sl2;
+        const float m_new = fmaxf(m_ref, tmax);
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        warp_need = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha_tile = ex2(m_ref - m_new);
+          l *= alpha_tile;
+          m_ref = m_new;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+          chunk_exp(sv[c], cexp, m_use, pk, sum);
+          tmem_st16(sa + c * 16, pk);
+        }
+      } else {
+        // Two halves of 64 columns, each moving the reference max only past
+        // the lazy threshold; the first half's P is rescaled if the second
+        // half moves it.
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float sv[2][32];
+          tmem_ld32(sa + hf * 64, sv[0]);
+          tmem_ld32(sa + hf * 64 + 32, sv[1]);
+          tmem_wait_ld();
+          scores(sv[0], j0 + hf * 64);
+          scores(sv[1], j0 + hf * 64 + 32);
+          float t1[22];
+#pragma unroll
+          for (int k = 0; k < 21; ++k) {
+            const int e = 3 * k;
+            t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+          }
+          t1[21] = sv[1][31];
+          float t2[8];
+#pragma unroll
+          for (int k = 0; k < 7; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+          t2[7] = t1[21];
+          float hmax = fmaxf(max3(t2[0], t2[1], t2[2]), fmaxf(max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7])));
+          if (fast && hmax != -INFINITY) hmax *= sl2;
+          const float m_new = fmaxf(m_ref, hmax);
+          const bool need = m_new > m_ref + kRescaleThreshold;
+          const bool wneed = __any_sync(0xffffffffu, need);
+          if (wneed) {
+            const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+            if (need) {
+              m_ref = m_new;
+              l *= alpha;
+              sum[0] *= alpha;
+              sum[1] *= alpha;
+              sum[2] *= alpha;
+              sum[3] *= alpha;
+            }
+            alpha_tile *= alpha;
+            warp_need = true;
+            if (hf == 1) {
+              tmem_wait_st();
+              float pw[32];
+              tmem_ld32(sa, pw);
+              tmem_wait_ld();
+              uint32_t w[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const uint32_t u = __float_as_uint(pw[e]);
+                const float lo = __uint_as_float(u << 16) * alpha, hi = __uint_as_float(u & 0xFFFF0000u) * alpha;
+                w[e] = pack_bf16x2(lo, hi);
+              }
+              tmem_st32(sa, w);
+            }
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+            chunk_exp(sv[c], cexp, m_use, pk, sum);
+            tmem_st16(sa + hf * 32 + c * 16, pk);
+          }
+        }
+      }
+      const float alpha = alpha_tile;
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      if (warp_need && cnt > 0) {
+        ok = mbar_wait(smem_u32(o_done + X), (cnt - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t oa = tmem + lane_base + colO;
+#pragma unroll
+        for (int c = 0; c < DV / 32; ++c) {
+          float o[32];
+          tmem_ld32(oa + c * 32, o);
+          tmem_wait_ld();
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(o[e] * alpha);
+          tmem_st32(oa + c * 32, w);
+        }
+      }
+      if constexpr (!FP8) {
+        // bf16 keys past the sequence end may hold anything (NaN-poisoned
+        // page slots): their V rows are cleared before P is released, by
+        // warpgroup A, or by B when A skips the tile.  (The e4m3 converters
+        // write those rows as zeros.)
+        const int valid = pi.sk - j0;
+        if (valid < kBlockN && (X == 0 || !half_active(p, pi, 0, kt))) {
+          const int sv = j % NSV;
+          ok = mbar_wait(smem_u32(v_full + sv), (j / NSV) & 1, abort_flag, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          uint8_t *vt = sV + sv * Cfg::kVBytes;
+          const int per_cb = (kBlockN - valid) * 8;
+          for (int idx = r; idx < per_cb * VC; idx += kBlockM) {
+            const int cb = idx / per_cb, rem = idx - cb * per_cb;
+            *reinterpret_cast<uint4 *>(vt + cb * Cfg::kChunkBytes + valid * 128 + rem * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(p_full + X));
+      ++cnt;
+    }
+
+    // -------------------------------------------------------- epilogue --
+    if (hx.valid) {
+      const bool row_ok = i < pi.sq;
+      const int64_t t = (int64_t)pi.q_row0 + X * kBlockM + r;
+      __nv_bfloat16 *orow = p.out + t * p.out_stride_t + (int64_t)pi.h * p.out_stride_h;
+      if (cnt == 0) {
+        if (row_ok && ok) {
+          for (int d = 0; d < DV; d += 8) *reinterpret_cast<uint4 *>(orow + d) = make_uint4(0, 0, 0, 0);
+          if (p.lse) p.lse[(int64_t)pi.h * p.total_q + t] = -INFINITY;
+        }
+      } else if (ok) {
+        ok = mbar_wait(smem_u32(o_done + X), (cnt - 1) & 1, abort_flag, p.err);
+        if (__all_sync(0xffffffffu, ok)) {
+          tc_fence_after();
+          const bool has = l > 0.f;
+          const float inv_l = has ? 1.f / l : 0.f;
+          const uint32_t oa = tmem + lane_base + colO;
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            float o[32];
+            tmem_ld32(oa + c * 32, o);
+            tmem_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = has ? pack_bf16x2(o[2 * e] * inv_l, o[2 * e + 1] * inv_l) : 0u;
+            if (row_ok) {
+              uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            }
+          }
+          if (row_ok && p.lse)
+            p.lse[(int64_t)pi.h * p.total_q + t] = has ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace fa

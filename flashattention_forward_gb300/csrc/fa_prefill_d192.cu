@@ -1,10 +1,10 @@
-// Prefill kernel instantiations for (Dk, Dv) = (192, 128): the single-query-
-// tile kernel, bf16 or e4m3 K/V.
-#include "fa_prefill1_launch.cuh"
+// Prefill kernel instantiations for (Dk, Dv) = (192, 128): the chunked-ring
+// ping-pong kernel, bf16 K/V.
+#include "fa_prefill3_launch.cuh"
 
 namespace fa {
 cudaError_t launch_prefill_192_128(const PrefillLaunch &L) {
-  if (L.fp8) return launch_prefill1_fp8<192, 128>(L);
-  return L.paged ? launch_prefill1_mod<192, 128, true, false>(L) : launch_prefill1_mod<192, 128, false, false>(L);
+  if (L.fp8) return launch_prefill_192_128_fp8(L);
+  return launch_prefill3<192, 128, false>(L);
 }
 }  // namespace fa

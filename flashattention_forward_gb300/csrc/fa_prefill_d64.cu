@@ -1,7 +1,7 @@
 // Prefill kernel instantiations for (Dk, Dv) = (64, 64): the two-query-tile
-// ping-pong kernel for bf16 K/V; e4m3 K/V runs the single-query-tile kernel.
-#include "fa_prefill1_launch.cuh"
+// ping-pong kernel for bf16 K/V; e4m3 K/V runs its converter-warp form.
 #include "fa_prefill2.cuh"
+#include "fa_prefill3_launch.cuh"
 
 namespace fa {
 namespace {
@@ -49,7 +49,7 @@ cudaError_t by_mod(const PrefillLaunch &L) {
 }  // namespace
 
 cudaError_t launch_prefill_64_64(const PrefillLaunch &L) {
-  if (L.fp8) return launch_prefill1_fp8<64, 64>(L);   // e4m3 K/V: single-query-tile kernel
+  if (L.fp8) return launch_prefill3<64, 64, true>(L);   // e4m3 K/V: converter-warp kernel
   return L.paged ? by_mod<true>(L) : by_mod<false>(L);
 }
 }  // namespace fa
