@@ -62,8 +62,12 @@ struct Prefill3Cfg {
   static constexpr bool kSplitRegs = FP8 || BIGREG;
   static constexpr int kWarps = FP8 ? 16 : (BIGREG ? 12 : 10);
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kRegsSoftmax = 208;
-  static constexpr int kRegsOther = FP8 ? 48 : 80;
+  static constexpr int kRegsSoftmax = FP8 ? 168 : 208;
+  static constexpr int kRegsOther = FP8 ? 88 : 80;
+  // Softmax over the whole S row at once (BIGREG, e4m3 with kOnePassFP8) or
+  // in two 64-column halves.
+  static constexpr bool kOnePassFP8 = false;
+  static constexpr bool kOnePass = FP8 ? kOnePassFP8 : BIGREG;
   static constexpr int kPoolNeeded = 8 * 32 * kRegsSoftmax + (kWarps - 8) * 32 * kRegsOther;
   static constexpr int kConverters = 6;
   static constexpr int kSlicesPerTile = (KC + VC) * 4;   // 32-row slices
@@ -93,8 +97,10 @@ __device__ __forceinline__ void e4m3x4_scaled_f16(uint32_t w, float s, uint32_t 
   float a, b, c, d;
   unpack_f16x2(e4m3x2_to_f16x2(w & 0xFFFFu), a, b);
   unpack_f16x2(e4m3x2_to_f16x2(w >> 16), c, d);
-  o0 = pack_f16x2(a * s, b * s);
-  o1 = pack_f16x2(c * s, d * s);
+  fma2(a, b, a, b, s, 0.f);   // packed fp32 products, rounded once
+  fma2(c, d, c, d, s, 0.f);
+  o0 = pack_f16x2(a, b);
+  o1 = pack_f16x2(c, d);
 }
 
 template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
@@ -228,6 +234,9 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
 
   if (warp == 8) {
     // ------------------------------------------------ producer: Q, K, V --
+    // Lane 0 waits for ring slots and arms the barriers; the boxes of a
+    // 64-column block (one per `rows_per_box` keys) are issued by lanes
+    // 0..n-1 in parallel, each with its own page id, looked up one tile ahead.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -239,44 +248,64 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         for (int cb = 0; cb < KC; ++cb)
           tma_load_3d(smem_u32(sQ + X * Cfg::kQTileBytes + cb * kBlockM * 128), &tm_q, smem_u32(q_full), cb * 64,
                       pi.h, pi.q_row0 + X * kBlockM);
-      // One 64-column block of a K or V tile into a 16 KB chunk: bf16 rows
-      // land swizzled (the MMA operand); e4m3 rows land raw, 64 bytes each, in
-      // the upper half of their 32-row slice, for the converters.
-      auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int cb, int kt) {
-        const int rb = p.rows_per_box;
-        for (int r0 = 0; r0 < kBlockN; r0 += rb) {
-          const uint32_t at = FP8 ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64)
-                                  : smem_u32(dst + r0 * 128);
-          if constexpr (PAGED) {
-            const int key0 = kt * kBlockN + r0;
-            const int page = key0 < pi.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
-            tma_load_4d(at, tm, smem_u32(bar), cb * 64, pi.hk, key0 & (p.page_size - 1), page);
-          } else {
-            tma_load_3d(at, tm, smem_u32(bar), cb * 64, pi.hk, pi.k_row0 + kt * kBlockN + r0);
-          }
-        }
-      };
-      constexpr uint32_t kBlockBytes = FP8 ? kBlockN * 64 : kBlockN * 128;
-      int j = 0;
-      bool ok = true;
-      for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt), ++j) {
-#pragma unroll 1
-        for (int c = 0; c < KC; ++c) {
-          const int n = j * KC + c, slot = n % NCK;
-          if (n >= NCK && !(ok = mbar_wait(smem_u32(kc_empty + slot), ((n / NCK) - 1) & 1, abort_flag, p.err)))
-            break;
-          uint64_t *bar = FP8 ? kc_stage + slot : kc_full + slot;
-          mbar_expect_tx(smem_u32(bar), kBlockBytes);
-          load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c, kt);
-        }
-        if (!ok) break;
-        const int sv = j % NSV;
-        if (j >= NSV && !(ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err))) break;
-        uint64_t *vbar = FP8 ? v_stage + sv : v_full + sv;
-        mbar_expect_tx(smem_u32(vbar), VC * kBlockBytes);
-#pragma unroll 1
-        for (int c = 0; c < VC; ++c) load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c, kt);
+    }
+    const int rb = p.rows_per_box;
+    const int nbox = kBlockN / rb;                    // 1..8 boxes per 64-column block
+    const int r0 = lane * rb;                         // this lane's first key row in a tile
+    const bool boxer = lane < nbox;
+    auto page_at = [&](int kt) -> int {
+      if constexpr (PAGED) {
+        const int key0 = kt * kBlockN + r0;
+        return (boxer && kt < pi.kt_hi && key0 < pi.sk) ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+      } else {
+        return 0;
       }
+    };
+    // One 64-column block of a K or V tile into a 16 KB chunk: bf16 rows land
+    // swizzled (the MMA operand); e4m3 rows land raw, 64 bytes each, in the
+    // upper half of their 32-row slice, for the converters.
+    auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int cb, int kt, int page) {
+      if (!boxer) return;
+      const uint32_t at = FP8 ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64) : smem_u32(dst + r0 * 128);
+      if constexpr (PAGED) {
+        tma_load_4d(at, tm, smem_u32(bar), cb * 64, pi.hk, (kt * kBlockN + r0) & (p.page_size - 1), page);
+      } else {
+        tma_load_3d(at, tm, smem_u32(bar), cb * 64, pi.hk, pi.k_row0 + kt * kBlockN + r0);
+      }
+    };
+    constexpr uint32_t kBlockBytes = FP8 ? kBlockN * 64 : kBlockN * 128;
+    int j = 0;
+    bool ok = true;
+    int page = page_at(first_kt);
+    for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
+      const int kn = pair_next(p, pi, kt);
+      const int page_next = page_at(kn);
+#pragma unroll 1
+      for (int c = 0; c < KC; ++c) {
+        const int n = j * KC + c, slot = n % NCK;
+        uint64_t *bar = FP8 ? kc_stage + slot : kc_full + slot;
+        if (lane == 0) {
+          if (n >= NCK) ok = mbar_wait(smem_u32(kc_empty + slot), ((n / NCK) - 1) & 1, abort_flag, p.err);
+          if (ok) mbar_expect_tx(smem_u32(bar), kBlockBytes);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c, kt, page);
+      }
+      if (!ok) break;
+      const int sv = j % NSV;
+      uint64_t *vbar = FP8 ? v_stage + sv : v_full + sv;
+      if (lane == 0) {
+        if (j >= NSV) ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err);
+        if (ok) mbar_expect_tx(smem_u32(vbar), VC * kBlockBytes);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < VC; ++c)
+        load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c, kt, page);
+      kt = kn;
+      page = page_next;
     }
   } else if (warp == 9) {
     // ------------------------------------------------------- MMA issuer --
@@ -373,74 +402,101 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
     if constexpr (FP8) {
       // ----------------------------------------- e4m3 -> f16 converters --
       // Slice g (32 rows of one 64-column block; K blocks of a tile first,
-      // then V blocks) goes to warp g mod 6.  Lane l loads the scale of row l;
-      // each step converts 8 rows, 16 dims per lane, into the swizzled layout.
-      // Rows past the sequence end are written as zeros.
+      // then V blocks; g counts slices over the pair's tile list) goes to warp
+      // g mod 6.  Lane l handles the scale of row l; each step converts 8
+      // rows, 16 dims per lane, into the swizzled layout.  Rows past the
+      // sequence end are written as zeros.  The scale loads are software
+      // pipelined: the page of a slice two ahead and the scale of the next
+      // slice are in flight while the current slice is converted.
+      constexpr int S = Cfg::kSlicesPerTile;
+      static_assert(S >= Cfg::kConverters, "a warp's first slice lies in the first tile");
       const int cw = warp - 10;
-      int j = 0;
-      int g = 0;
-      bool ok = true;
-      for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt), ++j) {
-        for (int s = 0; s < Cfg::kSlicesPerTile; ++s, ++g) {
-          if (g % Cfg::kConverters != cw) continue;
-          const bool isv = s >= KC * 4;
-          const int c = isv ? (s - KC * 4) >> 2 : s >> 2, q = s & 3;
-          uint8_t *base;
-          uint64_t *stage_bar, *full_bar;
-          uint32_t par;
-          if (!isv) {
-            const int n = j * KC + c, slot = n % NCK;
-            base = sK + slot * Cfg::kChunkBytes;
-            stage_bar = kc_stage + slot;
-            full_bar = kc_full + slot;
-            par = (n / NCK) & 1;
-          } else {
-            const int sv = j % NSV;
-            base = sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes;
-            stage_bar = v_stage + sv;
-            full_bar = v_full + sv;
-            par = (j / NSV) & 1;
-          }
-          const int key = kt * kBlockN + q * 32 + lane;
-          float sc = 0.f;
-          if (key < pi.sk) {
-            int64_t tok;
-            if constexpr (PAGED) {
-              const int page = __ldg(bt + (key >> p.page_shift));
-              tok = (int64_t)page * p.page_size + (key & (p.page_size - 1));
-            } else {
-              tok = (int64_t)pi.k_row0 + key;
-            }
-            sc = __ldg((isv ? p.v_scale : p.k_scale) + tok * p.hkv + pi.hk);
-          }
-          ok = mbar_wait(smem_u32(stage_bar), par, abort_flag, p.err);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          const uint8_t *stg = base + q * 4096 + 2048;
-          const int part = lane & 3;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int rr = 8 * t + (lane >> 2);              // row within the slice
-            const uint4 raw = *reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16);
-            const float s_row = __shfl_sync(0xffffffffu, sc, rr);
-            const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
-            uint32_t o[8];
-            e4m3x4_scaled_f16(raw.x, s_row, o[0], o[1]);
-            e4m3x4_scaled_f16(raw.y, s_row, o[2], o[3]);
-            e4m3x4_scaled_f16(raw.z, s_row, o[4], o[5]);
-            e4m3x4_scaled_f16(raw.w, s_row, o[6], o[7]);
-            if (!live) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) o[k] = 0u;
-            }
-            const int r = q * 32 + rr;
-            uint8_t *row = base + r * 128;
-            *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(full_bar));
+      struct It { int g, j, kt; };
+      auto adv = [&](It &it) {
+        it.g += Cfg::kConverters;
+        const int jn = it.g / S;
+        while (it.j < jn && it.kt < pi.kt_hi) { it.kt = pair_next(p, pi, it.kt); ++it.j; }
+      };
+      auto key_of = [&](const It &it) { return it.kt * kBlockN + ((it.g % S) & 3) * 32 + lane; };
+      auto page_of = [&](const It &it) -> int {
+        if constexpr (PAGED) {
+          const int key = key_of(it);
+          return (it.kt < pi.kt_hi && key < pi.sk) ? __ldg(bt + (key >> p.page_shift)) : 0;
+        } else {
+          return 0;
         }
+      };
+      auto scale_of = [&](const It &it, int page) -> float {
+        const int key = key_of(it);
+        if (!(it.kt < pi.kt_hi && key < pi.sk)) return 0.f;
+        int64_t tok;
+        if constexpr (PAGED) tok = (int64_t)page * p.page_size + (key & (p.page_size - 1));
+        else tok = (int64_t)pi.k_row0 + key;
+        const bool isv = (it.g % S) >= KC * 4;
+        return __ldg((isv ? p.v_scale : p.k_scale) + tok * p.hkv + pi.hk);
+      };
+      It a{cw, 0, first_kt};
+      It b = a;
+      adv(b);
+      It c = b;
+      adv(c);
+      float sa = scale_of(a, page_of(a));
+      int pb = page_of(b);
+      bool ok = true;
+      while (ok && a.kt < pi.kt_hi) {
+        const float sb = scale_of(b, pb);
+        const int pc = page_of(c);
+        const int s = a.g % S, j = a.j, kt = a.kt;
+        const bool isv = s >= KC * 4;
+        const int cb = isv ? (s - KC * 4) >> 2 : s >> 2, q = s & 3;
+        uint8_t *base;
+        uint64_t *stage_bar, *full_bar;
+        uint32_t par;
+        if (!isv) {
+          const int n = j * KC + cb, slot = n % NCK;
+          base = sK + slot * Cfg::kChunkBytes;
+          stage_bar = kc_stage + slot;
+          full_bar = kc_full + slot;
+          par = (n / NCK) & 1;
+        } else {
+          const int sv = j % NSV;
+          base = sV + sv * Cfg::kVBytes + cb * Cfg::kChunkBytes;
+          stage_bar = v_stage + sv;
+          full_bar = v_full + sv;
+          par = (j / NSV) & 1;
+        }
+        ok = mbar_wait(smem_u32(stage_bar), par, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t *stg = base + q * 4096 + 2048;
+        const int part = lane & 3;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int rr = 8 * t + (lane >> 2);              // row within the slice
+          const uint4 raw = *reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16);
+          const float s_row = __shfl_sync(0xffffffffu, sa, rr);
+          const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
+          uint32_t o[8];
+          e4m3x4_scaled_f16(raw.x, s_row, o[0], o[1]);
+          e4m3x4_scaled_f16(raw.y, s_row, o[2], o[3]);
+          e4m3x4_scaled_f16(raw.z, s_row, o[4], o[5]);
+          e4m3x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+          if (!live) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = 0u;
+          }
+          const int r = q * 32 + rr;
+          uint8_t *row = base + r * 128;
+          *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(full_bar));
+        a = b;
+        sa = sb;
+        b = c;
+        pb = pc;
+        adv(c);
       }
     }
   } else {
@@ -562,7 +618,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
       float alpha_tile = 1.f;
       bool warp_need = false;
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (BIGREG || FP8) {
+      if constexpr (Cfg::kOnePass) {
         float sv[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(sa + c * 32, sv[c]);
@@ -649,8 +705,14 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
                 const uint32_t u = __float_as_uint(pw[e]);
-                const float lo = __uint_as_float(u << 16) * alpha, hi = __uint_as_float(u & 0xFFFF0000u) * alpha;
-                w[e] = pack_bf16x2(lo, hi);
+                float lo, hi;
+                if constexpr (FP8) {
+                  unpack_f16x2(u, lo, hi);
+                } else {
+                  lo = __uint_as_float(u << 16);
+                  hi = __uint_as_float(u & 0xFFFF0000u);
+                }
+                w[e] = pack_p(lo * alpha, hi * alpha);
               }
               tmem_st32(sa, w);
             }

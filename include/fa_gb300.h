@@ -135,9 +135,12 @@ typedef struct {
  *  launch       host scalars (required).
  *  stream       cudaStream_t.
  *
- * Environment: FA_GB300_PREFILL_VARIANT=1 makes the Dk <= 128 prefill use its
+ * Environment: FA_GB300_PREFILL_VARIANT=1 makes the bf16 prefill use its
  * 10-warp two-pass softmax instead of the register-rebalanced one-pass one
  * (a test and diagnosis knob; results agree within rounding).
+ *
+ * e4m3 caches: K and V become f16 operands RN(e4m3 * scale) inside the
+ * kernel, so |e4m3 value * scale| must stay below 65504 (scales below 146).
  *
  * Supported head dims: (Dk, Dv) in {(64,64), (128,128), (192,128)}.  Hq must
  * be a multiple of Hkv (query head h reads kv head h / (Hq/Hkv)).
