@@ -32,8 +32,10 @@ import torch  # noqa: E402
 import fa_inputs as fi  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (prefill) & KV-cache GB/s (decode), % of GB300 roofline"
+# sources of the headline kernel (fa_prefill2_kernel): `traffic` is reported only
+# while profiles/traffic.json was captured from these exact files
 KERNEL_SOURCES = ["flashattention_forward_gb300/csrc/fa_prefill.cuh", "flashattention_forward_gb300/csrc/fa_prefill2.cuh",
-                  "flashattention_forward_gb300/csrc/fa_prefill3.cuh", "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
+                  "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
 
 
 def kernel_hash():
@@ -277,6 +279,21 @@ def cpu_oracle_sample(p, seconds_target=15.0, seed=0):
     return rate, len(units), threads, dt, flops
 
 
+def max_over_ranks(ms, dist=None, device="cpu"):
+    """The slowest rank's step time: every replica's work counts only once all
+    ranks have finished it."""
+    if dist is None:
+        return ms
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(flops_per_step, world, ms):
+    """Whole-job TFLOP/s: `world` replicas each did `flops_per_step` in `ms`."""
+    return flops_per_step * world / (ms * 1e-3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -363,12 +380,8 @@ def main():
     if dist:
         dist.barrier()
     step_ms = [a + b for a, b in zip(*each)]
-    ms = statistics.mean(step_ms)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = flops_step * world / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
+    value = whole_job_rate(flops_step, world, ms)
     # dominant kernel: the non-causal launch (largest share of the step)
     ms_f = statistics.mean(each[1])
     ach = fi.prefill_flops(p_full) / (ms_f * 1e-3) / 1e12

@@ -25,7 +25,8 @@ FA_BF16, FA_E4M3, FA_F32, FA_I32, FA_U8 = 0, 1, 2, 3, 4
 MOD_NONE, MOD_ALIBI, MOD_SOFTCAP = 0, 1, 2
 
 EXPORTED = ("fa_fwd_varlen", "fa_fwd_workspace_bytes", "fa_fwd_default_splits", "fa_combine",
-            "fa_last_error", "fa_get_device_error", "fa_version", "fa_fwd_varlen_noalloc")
+            "fa_last_error", "fa_get_device_error", "fa_version", "fa_fwd_varlen_noalloc",
+            "fa_fwd_plan_create", "fa_fwd_plan_launch", "fa_fwd_plan_destroy")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -93,6 +94,12 @@ def lib() -> ctypes.CDLL:
             L.fa_version.restype = ctypes.c_char_p
             L.fa_fwd_varlen_noalloc.argtypes = L.fa_fwd_varlen.argtypes
             L.fa_fwd_varlen_noalloc.restype = ctypes.c_int
+            L.fa_fwd_plan_create.argtypes = L.fa_fwd_varlen.argtypes[:-1] + [P(ctypes.c_void_p)]
+            L.fa_fwd_plan_create.restype = ctypes.c_int
+            L.fa_fwd_plan_launch.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+            L.fa_fwd_plan_launch.restype = ctypes.c_int
+            L.fa_fwd_plan_destroy.argtypes = [ctypes.c_void_p]
+            L.fa_fwd_plan_destroy.restype = None
             _lib = L
     return _lib
 
@@ -227,11 +234,12 @@ def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
 
 
 class FwdPlan:
-    """A prepared fwd_varlen call: the argument descriptors are built once and
-    run() re-issues the C call with them (for repeated calls on the same
-    buffers -- serving loops, benchmarks -- where per-call marshalling would
-    dominate small problems).  Takes the arguments of fwd_varlen; the tensors
-    must stay alive and keep their storage while the plan is used."""
+    """A prepared fwd_varlen call through ``fa_fwd_plan_create``: validation,
+    tensor maps and kernel parameters are built once, and run() only enqueues
+    the kernels (``fa_fwd_plan_launch``) -- for repeated calls on the same
+    buffers (serving loops, benchmarks) where the per-call host work would
+    dominate small problems.  Takes the arguments of fwd_varlen; the tensors
+    must stay alive, unmoved and of the same shape while the plan is used."""
 
     def __init__(self, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, **kw):
         L = lib()
@@ -273,26 +281,34 @@ class FwdPlan:
             self.launch.workspace = ws.data_ptr()
             self.launch.workspace_bytes = ws.numel()
         self._ws = ws
-        self._sm = ScoreMod(kind=score_mod, alibi_slope=kw.get("alibi_slope", 0.0), softcap=kw.get("softcap", 0.0))
-        self._bm = None
+        sm = ScoreMod(kind=score_mod, alibi_slope=kw.get("alibi_slope", 0.0), softcap=kw.get("softcap", 0.0))
+        bm = None
         if block_mask is not None:
-            self._bm = BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1],
-                                 n_kblk=block_mask.shape[2], blk_q=128, blk_k=128)
+            bm = BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1], n_kblk=block_mask.shape[2],
+                           blk_q=128, blk_k=128)
         descs = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
                  as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(kw.get("k_scale")),
                  as_tensor(kw.get("v_scale")), as_tensor(self.out), as_tensor(self.lse)]
-        self._descs = descs
-        self._head = tuple(_ref(a) for a in descs) + (
-            ctypes.c_float(scale), ctypes.c_int32(int(bool(kw.get("causal", False)))),
-            ctypes.c_int32(int(kw.get("window", 0))), ctypes.byref(self._sm), _ref(self._bm),
-            ctypes.c_int32(int(page_size)), ctypes.byref(self.launch))
-        self._fn = L.fa_fwd_varlen
+        handle = ctypes.c_void_p(0)
+        _check(L.fa_fwd_plan_create(*[_ref(a) for a in descs], ctypes.c_float(scale),
+                                    ctypes.c_int32(int(bool(kw.get("causal", False)))),
+                                    ctypes.c_int32(int(kw.get("window", 0))), ctypes.byref(sm), _ref(bm),
+                                    ctypes.c_int32(int(page_size)), ctypes.byref(self.launch), ctypes.byref(handle)))
+        self._plan = handle
+        self._launch_fn = L.fa_fwd_plan_launch
+        self._destroy_fn = L.fa_fwd_plan_destroy
 
     def run(self, stream=None):
-        st = self._fn(*self._head, ctypes.c_void_p(_stream_ptr(stream)))
+        st = self._launch_fn(self._plan, ctypes.c_void_p(_stream_ptr(stream)))
         if st != FA_OK:
             _check(st)
         return self.out, self.lse
+
+    def __del__(self):
+        plan = getattr(self, "_plan", None)
+        if plan is not None and plan.value:
+            self._destroy_fn(plan)
+            self._plan = None
 
 
 def combine(o_part: torch.Tensor, lse_part: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <new>
 
 #include "../../include/fa_gb300.h"
 #include "fa_internal.h"
@@ -141,6 +142,54 @@ namespace fa {
 fa_status_t set_host_error(fa_status_t st, const char *msg) { return fail(st, "%s", msg); }
 }  // namespace fa
 
+// A prepared forward call (fa_fwd_plan_create): the launch descriptors that
+// fa_fwd_varlen would enqueue, kept for repeated launches.
+struct fa_fwd_plan_s {
+  int kind = 0;              // 0: nothing to launch, 1: split-KV decode (+ combine), 2: prefill
+  int dk = 0, fp8 = 0;
+  fa::DecodeLaunch dl;
+  int splits = 0, hq = 0, dv = 0;
+  int64_t rows = 0;
+  void *out = nullptr;
+  fa::PrefillLaunch pl;
+};
+
+namespace {
+
+fa_status_t run_decode(fa::DecodeLaunch L, const fa_fwd_plan_s &P, cudaStream_t s) {
+  L.stream = s;
+  cudaError_t e = fa::launch_decode(P.dk, L);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (P.splits > 1) {
+    e = fa::launch_combine(L.p.o_part, L.p.lse_part, P.splits, P.rows, P.hq, P.dv, P.out, L.p.lse, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return FA_OK;
+}
+
+fa_status_t run_prefill(fa::PrefillLaunch L, const fa_fwd_plan_s &P, cudaStream_t s) {
+  L.stream = s;
+  cudaError_t e;
+  if (P.dk == 64) e = fa::launch_prefill_64_64(L);
+  else if (P.dk == 128) e = fa::launch_prefill_128_128(L);
+  else e = fa::launch_prefill_192_128(L);
+  if (e == cudaErrorNotSupported && P.fp8)
+    return fail(FA_ERR_UNSUPPORTED, "the e4m3 kernel's register split does not fit this build's launch registers");
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return FA_OK;
+}
+
+// Validates a forward call and builds its launch descriptors; launches them on
+// `stream` unless `plan` is given, in which case they are stored there.
+fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
+                      const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
+                      const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
+                      fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
+                      const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
+                      const fa_launch_t *launch, void *stream, fa_fwd_plan_s *plan);
+
+}  // namespace
+
 extern "C" {
 
 const char *fa_last_error(void) { return g_msg; }
@@ -211,6 +260,52 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
                           fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
                           const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
                           const fa_launch_t *launch, void *stream) {
+  return fwd_build(q, k_cache, v_cache, block_table, cu_seqlens_q, cu_seqlens_k, k_scale, v_scale, out, lse,
+                   softmax_scale, causal, window, score_mod, block_mask, page_size, launch, stream, nullptr);
+}
+
+fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
+                               const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
+                               const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale,
+                               const fa_tensor_t *v_scale, fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
+                               int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
+                               const fa_block_mask_t *block_mask, int32_t page_size, const fa_launch_t *launch,
+                               fa_fwd_plan_t *plan) {
+  if (!plan) return fail(FA_ERR_INVALID_ARG, "plan is NULL");
+  *plan = nullptr;
+  fa_fwd_plan_s *P = new (std::nothrow) fa_fwd_plan_s();
+  if (!P) return fail(FA_ERR_INVALID_ARG, "out of host memory");
+  const fa_status_t st = fwd_build(q, k_cache, v_cache, block_table, cu_seqlens_q, cu_seqlens_k, k_scale, v_scale,
+                                   out, lse, softmax_scale, causal, window, score_mod, block_mask, page_size, launch,
+                                   nullptr, P);
+  if (st != FA_OK) {
+    delete P;
+    return st;
+  }
+  *plan = P;
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_plan_launch(fa_fwd_plan_t plan, void *stream) {
+  g_msg[0] = 0;
+  if (!plan) return fail(FA_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->kind == 1) return run_decode(plan->dl, *plan, (cudaStream_t)stream);
+  if (plan->kind == 2) return run_prefill(plan->pl, *plan, (cudaStream_t)stream);
+  return FA_OK;
+}
+
+void fa_fwd_plan_destroy(fa_fwd_plan_t plan) { delete plan; }
+
+}  // extern "C"
+
+namespace {
+
+fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
+                      const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
+                      const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
+                      fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
+                      const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
+                      const fa_launch_t *launch, void *stream, fa_fwd_plan_s *plan) {
   fa_status_t st;
   g_msg[0] = 0;
   if (!launch) return fail(FA_ERR_INVALID_ARG, "launch is NULL");
@@ -391,14 +486,17 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
       p.lse_part = (float *)((char *)launch->workspace + align256((size_t)S * Tq * Hq * Dv * sizeof(float)));
     }
     L.grid = dim3((unsigned)S, (unsigned)Hkv, (unsigned)B);
-    L.stream = s;
-    cudaError_t e = fa::launch_decode((int)Dk, L);
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    if (S > 1) {
-      e = fa::launch_combine(p.o_part, p.lse_part, S, Tq, (int)Hq, (int)Dv, out->data, p.lse, s);
-      if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-    }
-    return FA_OK;
+    fa_fwd_plan_s local;
+    fa_fwd_plan_s &P = plan ? *plan : local;
+    P.kind = 1;
+    P.dk = (int)Dk;
+    P.splits = S;
+    P.rows = Tq;
+    P.hq = (int)Hq;
+    P.dv = (int)Dv;
+    P.out = out->data;
+    P.dl = L;
+    return plan ? FA_OK : run_decode(L, P, s);
   }
 
   // ------------------------------------------------------------ prefill --
@@ -514,15 +612,13 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
   // One CTA per work item: the hardware hands items to SMs as they free up,
   // which balances ragged batches.
   L.grid = dim3((unsigned)n_blocks, 1, 1);
-  L.stream = s;
-  cudaError_t e;
-  if (Dk == 64) e = fa::launch_prefill_64_64(L);
-  else if (Dk == 128) e = fa::launch_prefill_128_128(L);
-  else e = fa::launch_prefill_192_128(L);
-  if (e == cudaErrorNotSupported && fp8)
-    return fail(FA_ERR_UNSUPPORTED, "the e4m3 kernel's register split does not fit this build's launch registers");
-  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  return FA_OK;
+  fa_fwd_plan_s local;
+  fa_fwd_plan_s &P = plan ? *plan : local;
+  P.kind = 2;
+  P.dk = (int)Dk;
+  P.fp8 = fp8;
+  P.pl = L;
+  return plan ? FA_OK : run_prefill(L, P, s);
 }
 
-}  // extern "C"
+}  // namespace

@@ -156,6 +156,32 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache,
                           const fa_launch_t *launch, void *stream);
 
 /*
+ * Prepared calls.  fa_fwd_plan_create validates a forward call exactly like
+ * fa_fwd_varlen (same arguments except the stream) and records the launches
+ * it would make -- tensor maps, kernel parameters, grid -- without enqueuing
+ * anything.  fa_fwd_plan_launch enqueues them on `stream`: the host work of a
+ * call drops to the kernel launches, which matters for small problems issued
+ * repeatedly (decode loops, serving).  The plan keeps the device addresses of
+ * every tensor and of the workspace: they must stay allocated, unmoved and of
+ * the same shape while the plan is used, and their contents are read at each
+ * launch.  A plan runs on the device that was current at creation.  Launching
+ * a plan on two streams at once is allowed only without a workspace (split-KV
+ * partials would race).  fa_fwd_plan_destroy frees the host-side plan (NULL is
+ * a no-op).  Status and error reporting as for fa_fwd_varlen.
+ */
+typedef struct fa_fwd_plan_s *fa_fwd_plan_t;
+
+fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
+                               const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
+                               const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale,
+                               const fa_tensor_t *v_scale, fa_tensor_t *out, fa_tensor_t *lse,
+                               float softmax_scale, int32_t causal, int32_t window,
+                               const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask,
+                               int32_t page_size, const fa_launch_t *launch, fa_fwd_plan_t *plan);
+fa_status_t fa_fwd_plan_launch(fa_fwd_plan_t plan, void *stream);
+void fa_fwd_plan_destroy(fa_fwd_plan_t plan);
+
+/*
  * Workspace size in bytes for split-KV with `num_splits` key ranges: partial
  * outputs fp32 [num_splits, T_q, Hq, Dv] and partial LSEs fp32
  * [num_splits, Hq, T_q], each 256-byte aligned.  0 when num_splits <= 0.

@@ -161,3 +161,25 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         fa.lib()
+
+
+def test_plan_create_validates_like_the_call(L):
+    """fa_fwd_plan_create rejects what fa_fwd_varlen rejects, with the same
+    message, and leaves the plan handle NULL; launch/destroy of NULL."""
+    T, H, D = 256, 4, 64
+    q = _t(FAKE, fa.FA_F32, [T, H, D])
+    k, v = _t(FAKE * 2, fa.FA_BF16, [T, H, D]), _t(FAKE * 3, fa.FA_BF16, [T, H, D])
+    cq, ck = _t(FAKE * 4, fa.FA_I32, [3]), _t(FAKE * 5, fa.FA_I32, [3])
+    out, lse = _t(FAKE * 6, fa.FA_BF16, [T, H, D]), _t(FAKE * 7, fa.FA_F32, [H, T])
+    launch = fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=0, total_q=T, total_k=T)
+    handle = ctypes.c_void_p(12345)
+    r = ctypes.byref
+    st = L.fa_fwd_plan_create(r(q), r(k), r(v), None, r(cq), r(ck), None, None, r(out), r(lse), 0.125, 1, 0,
+                              None, None, 0, r(launch), r(handle))
+    assert st == fa.FA_ERR_INVALID_ARG and "dtype" in L.fa_last_error().decode()
+    assert not handle.value
+    st = L.fa_fwd_plan_create(r(q), r(k), r(v), None, r(cq), r(ck), None, None, r(out), r(lse), 0.125, 1, 0,
+                              None, None, 0, r(launch), None)
+    assert st == fa.FA_ERR_INVALID_ARG and "plan" in L.fa_last_error().decode()
+    assert L.fa_fwd_plan_launch(None, None) == fa.FA_ERR_INVALID_ARG
+    L.fa_fwd_plan_destroy(None)

@@ -249,3 +249,40 @@ def test_fwd_plan_matches_call_and_oracle(case):
         assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l)
     ro, rl = oracle.forward(p)
     compare(o, l, ro, rl)
+
+
+def test_graph_capture_of_call_and_plan():
+    """The forward enqueues kernels only (no allocation, copy or sync inside),
+    so both the plain call and a prepared plan can be captured in a CUDA graph
+    and replayed on new inputs written into the same buffers."""
+    import flashattention_forward_gb300 as fa
+    p = fi.make_problem([300, 129, 64], [300, 500, 64], hq=8, hkv=2, dk=128, seed=51, causal=True)
+    p2 = fi.make_problem([300, 129, 64], [300, 500, 64], hq=8, hkv=2, dk=128, seed=52, causal=True)
+    t, t2 = to_device(p), to_device(p2)
+    o_ref, l_ref = host(*run_gpu(p2, t2))
+    out = torch.empty((p.total_q, p.hq, p.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((p.hq, p.total_q), dtype=torch.float32, device="cuda")
+    plan = fa.FwdPlan(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
+                      max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, softmax_scale=p.softmax_scale, causal=True,
+                      num_splits=0)
+    run_gpu(p, t, out=out, lse=lse)       # warm up (module load, attributes) outside the capture
+    plan.run()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    for use_plan in (False, True):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            if use_plan:
+                plan.run(stream=s)
+            else:
+                run_gpu(p, t, out=out, lse=lse, stream=s)
+        for name in ("q", "k", "v"):
+            t[name].copy_(t2[name])
+        out.zero_()
+        plan.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        o, l = host(out, lse) if not use_plan else host(plan.out, plan.lse)
+        assert np.array_equal(o, o_ref) and np.array_equal(l, l_ref)
+        for name in ("q", "k", "v"):
+            t[name].copy_(to_device(p)[name])
