@@ -19,6 +19,7 @@ namespace fa {
 constexpr int kBlockM = 128;   // query rows per tile (MMA M)
 constexpr int kBlockN = 128;   // keys per tile (MMA N of QK^T, K of PV)
 constexpr float kRescaleThreshold = 8.0f;   // lazy O rescale, scaled log2 units
+constexpr float kGuardSum = 0x1p64f;        // tile row sum above which the deferred max is taken
 
 struct PrefillParams {
   const int32_t *cu_q;

@@ -396,6 +396,10 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
       }
     };
     const float cexp = fast ? p.scale_log2 : 1.f;
+    // The deferred max (below) shortens the softmax; it pays where the
+    // softmax is the critical path, i.e. with a score mod.  Plain scores keep
+    // the max-first order.
+    constexpr bool kDeferredMax = (MOD != 0);
     int j = -1;   // index of the tile in the pair's list (K/V ring position)
     for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
       ++j;
@@ -451,44 +455,68 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) scores(sv[c], j0 + c * 32);
-        // Balanced tree of 3-input maxima over the 128 scores (depth 5).
-        float t1[43];
+        // Exponentials against the running reference, stored as P; the row
+        // sum of the tile comes back in `acc`.
+        auto exp_store = [&](float m_use, float (&acc)[4]) {
 #pragma unroll
-        for (int k = 0; k < 42; ++k) {
-          const int e = 3 * k;
-          t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+            chunk_exp(sv[c], cexp, m_use, pk, acc);
+            tmem_st16(sa + c * 16, pk);
+          }
+        };
+        // Deferred max: once a row has a reference, the tile's exponentials
+        // are taken against it directly.  Only if the tile's sum exceeds
+        // 2^64 (a score more than ~57 log2 units above the reference) is its
+        // max computed and P redone -- fp32 O and l stay far from overflow in
+        // between, and bf16 P keeps its relative precision at any magnitude.
+        // A row's first tile (no reference yet) takes the max first.
+        bool slow = !kDeferredMax || __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!slow) {
+          exp_store(m_ref, sum);
+          const float ts = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+          slow = __any_sync(0xffffffffu, !(ts <= kGuardSum));
+          if (slow) {
+            tmem_wait_st();   // P is written again below
+            sum[0] = sum[1] = sum[2] = sum[3] = 0.f;
+          }
         }
-        t1[42] = fmaxf(sv[3][30], sv[3][31]);
-        float t2[15];
+        if (slow) {
+          // Balanced tree of 3-input maxima over the 128 scores (depth 5).
+          float t1[43];
 #pragma unroll
-        for (int k = 0; k < 14; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
-        t2[14] = t1[42];
-        float t3[5];
+          for (int k = 0; k < 42; ++k) {
+            const int e = 3 * k;
+            t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+          }
+          t1[42] = fmaxf(sv[3][30], sv[3][31]);
+          float t2[15];
 #pragma unroll
-        for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
-        float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
-        if (fast && tmax != -INFINITY) tmax *= p.scale_log2;
-        const float m_new = fmaxf(m_ref, tmax);
-        const bool need = m_new > m_ref + kRescaleThreshold;
-        warp_need = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha_tile = ex2(m_ref - m_new);
-          l *= alpha_tile;
-          m_ref = m_new;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          for (int k = 0; k < 14; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+          t2[14] = t1[42];
+          float t3[5];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-          chunk_exp(sv[c], cexp, m_use, pk, sum);
-          tmem_st16(sa + c * 16, pk);
+          for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
+          float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
+          if (fast && tmax != -INFINITY) tmax *= p.scale_log2;
+          const float m_new = fmaxf(m_ref, tmax);
+          const bool need = m_new > m_ref + kRescaleThreshold;
+          warp_need = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha_tile = ex2(m_ref - m_new);
+            l *= alpha_tile;
+            m_ref = m_new;
+          }
+          exp_store((m_ref == -INFINITY) ? 0.f : m_ref, sum);
         }
       } else {
-        // The S row is processed in two halves of 64 columns.  Each half moves
-        // the reference max only when its max exceeds it by the lazy threshold;
-        // if the second half does so, the first half's P (already in TMEM) is
-        // rescaled too -- rare once a row's max has settled.
-  #pragma unroll
+        // The S row is processed in two halves of 64 columns, each with the
+        // deferred max of the one-pass form: exponentials against the
+        // running reference unless the row has none yet or the half's sum
+        // exceeds 2^64; then the half's max moves the reference (lazily, by
+        // the rescale threshold) and, for the second half, the first half's
+        // P (already in TMEM) is rescaled too.
+#pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float sv[2][32];
           tmem_ld32(sa + hf * 64, sv[0]);
@@ -496,58 +524,75 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
           tmem_wait_ld();
           scores(sv[0], j0 + hf * 64);
           scores(sv[1], j0 + hf * 64 + 32);
-          // tree of 3-input maxima over the 64 scores of this half
-          float t1[22];
+          float hsum[4] = {0.f, 0.f, 0.f, 0.f};
+          auto exp_store = [&](float m_use) {
 #pragma unroll
-          for (int k = 0; k < 21; ++k) {
-            const int e = 3 * k;
-            t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
-          }
-          t1[21] = sv[1][31];
-          float t2[8];
-#pragma unroll
-          for (int k = 0; k < 7; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
-          t2[7] = t1[21];
-          float hmax = fmaxf(max3(t2[0], t2[1], t2[2]), fmaxf(max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7])));
-          if (fast && hmax != -INFINITY) hmax *= p.scale_log2;
-          const float m_new = fmaxf(m_ref, hmax);
-          const bool need = m_new > m_ref + kRescaleThreshold;
-          const bool wneed = __any_sync(0xffffffffu, need);
-          if (wneed) {
-            const float alpha = need ? ex2(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
-            if (need) {
-              m_ref = m_new;
-              l *= alpha;
-              sum[0] *= alpha;
-              sum[1] *= alpha;
-              sum[2] *= alpha;
-              sum[3] *= alpha;
+            for (int c = 0; c < 2; ++c) {
+              uint32_t pk[16];
+              chunk_exp(sv[c], cexp, m_use, pk, hsum);
+              tmem_st16(sa + hf * 32 + c * 16, pk);
             }
-            alpha_tile *= alpha;
-            warp_need = true;
-            if (hf == 1) {
-              // P of the first half was computed against the old reference.
+          };
+          bool slow = !kDeferredMax || __any_sync(0xffffffffu, m_ref == -INFINITY);
+          if (!slow) {
+            exp_store(m_ref);
+            const float hs = (hsum[0] + hsum[1]) + (hsum[2] + hsum[3]);
+            slow = __any_sync(0xffffffffu, !(hs <= kGuardSum));
+            if (slow) {
               tmem_wait_st();
-              float pw[32];
-              tmem_ld32(sa, pw);
-              tmem_wait_ld();
-              uint32_t w[32];
-  #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const uint32_t u = __float_as_uint(pw[e]);
-                const float lo = __uint_as_float(u << 16) * alpha, hi = __uint_as_float(u & 0xFFFF0000u) * alpha;
-                w[e] = pack_bf16x2(lo, hi);
-              }
-              tmem_st32(sa, w);
+              hsum[0] = hsum[1] = hsum[2] = hsum[3] = 0.f;
             }
           }
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-  #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
-            chunk_exp(sv[c], cexp, m_use, pk, sum);
-            tmem_st16(sa + hf * 32 + c * 16, pk);
+          if (slow) {
+            // tree of 3-input maxima over the 64 scores of this half
+            float t1[22];
+#pragma unroll
+            for (int k = 0; k < 21; ++k) {
+              const int e = 3 * k;
+              t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+            }
+            t1[21] = sv[1][31];
+            float t2[8];
+#pragma unroll
+            for (int k = 0; k < 7; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+            t2[7] = t1[21];
+            float hmax = fmaxf(max3(t2[0], t2[1], t2[2]), fmaxf(max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7])));
+            if (fast && hmax != -INFINITY) hmax *= p.scale_log2;
+            const float m_new = fmaxf(m_ref, hmax);
+            const bool need = m_new > m_ref + kRescaleThreshold;
+            const bool wneed = __any_sync(0xffffffffu, need);
+            if (wneed) {
+              const float alpha = need ? ex2(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
+              if (need) {
+                m_ref = m_new;
+                l *= alpha;
+                sum[0] *= alpha;
+                sum[1] *= alpha;
+                sum[2] *= alpha;
+                sum[3] *= alpha;
+              }
+              alpha_tile *= alpha;
+              warp_need = true;
+              if (hf == 1) {
+                // P of the first half was computed against the old reference.
+                tmem_wait_st();
+                float pw[32];
+                tmem_ld32(sa, pw);
+                tmem_wait_ld();
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const uint32_t u = __float_as_uint(pw[e]);
+                  const float lo = __uint_as_float(u << 16) * alpha, hi = __uint_as_float(u & 0xFFFF0000u) * alpha;
+                  w[e] = pack_bf16x2(lo, hi);
+                }
+                tmem_st32(sa, w);
+              }
+            }
+            exp_store((m_ref == -INFINITY) ? 0.f : m_ref);
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sum[q] += hsum[q];
         }
       }
       const float alpha = alpha_tile;

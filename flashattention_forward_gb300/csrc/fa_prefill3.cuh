@@ -558,6 +558,9 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
     // MOD 0 runs with a positive scale only (the host routes other scales to
     // the general path), so raw scores can be maxed before scaling.
     constexpr bool fast = (MOD == 0);
+    // Deferred-max guard on a tile's row sum: P must stay finite in its
+    // packed type (f16 for e4m3 caches: below 65504; bf16: any fp32 value).
+    constexpr float kGuard = FP8 ? 0x1p15f : kGuardSum;
     const float sl2 = p.scale_log2 * rowf;
     const float sca = p.softcap_arg * rowf;
     auto pack_p = [](float a, float b) -> uint32_t { return FP8 ? pack_f16x2(a, b) : pack_bf16x2(a, b); };
@@ -573,6 +576,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
       }
     };
     const float cexp = fast ? sl2 : 1.f;
+    constexpr bool kDeferredMax = (MOD != 0);   // as in fa_prefill2.cuh
     int j = -1;   // index of the tile in the pair's list (ring position)
     for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
       ++j;
@@ -625,41 +629,58 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) scores(sv[c], j0 + c * 32);
-        float t1[43];
+        auto exp_store = [&](float m_use, float (&acc)[4]) {
 #pragma unroll
-        for (int k = 0; k < 42; ++k) {
-          const int e = 3 * k;
-          t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+            chunk_exp(sv[c], cexp, m_use, pk, acc);
+            tmem_st16(sa + c * 16, pk);
+          }
+        };
+        // Deferred max (as in fa_prefill2.cuh): exponentials against the
+        // running reference unless the row has none yet or the tile's sum
+        // exceeds kGuard, in which case the max is taken and P redone.
+        bool slow = !kDeferredMax || __any_sync(0xffffffffu, m_ref == -INFINITY);
+        if (!slow) {
+          exp_store(m_ref, sum);
+          const float ts = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+          slow = __any_sync(0xffffffffu, !(ts <= kGuard));
+          if (slow) {
+            tmem_wait_st();
+            sum[0] = sum[1] = sum[2] = sum[3] = 0.f;
+          }
         }
-        t1[42] = fmaxf(sv[3][30], sv[3][31]);
-        float t2[15];
+        if (slow) {
+          float t1[43];
 #pragma unroll
-        for (int k = 0; k < 14; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
-        t2[14] = t1[42];
-        float t3[5];
+          for (int k = 0; k < 42; ++k) {
+            const int e = 3 * k;
+            t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+          }
+          t1[42] = fmaxf(sv[3][30], sv[3][31]);
+          float t2[15];
 #pragma unroll
-        for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
-        float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
-        if (fast && tmax != -INFINITY) tmax *= sl2;
-        const float m_new = fmaxf(m_ref, tmax);
-        const bool need = m_new > m_ref + kRescaleThreshold;
-        warp_need = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha_tile = ex2(m_ref - m_new);
-          l *= alpha_tile;
-          m_ref = m_new;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          for (int k = 0; k < 14; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+          t2[14] = t1[42];
+          float t3[5];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-          chunk_exp(sv[c], cexp, m_use, pk, sum);
-          tmem_st16(sa + c * 16, pk);
+          for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
+          float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
+          if (fast && tmax != -INFINITY) tmax *= sl2;
+          const float m_new = fmaxf(m_ref, tmax);
+          const bool need = m_new > m_ref + kRescaleThreshold;
+          warp_need = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha_tile = ex2(m_ref - m_new);
+            l *= alpha_tile;
+            m_ref = m_new;
+          }
+          exp_store((m_ref == -INFINITY) ? 0.f : m_ref, sum);
         }
       } else {
-        // Two halves of 64 columns, each moving the reference max only past
-        // the lazy threshold; the first half's P is rescaled if the second
-        // half moves it.
+        // Two halves of 64 columns with the deferred max of the one-pass form;
+        // when the second half moves the reference, the first half's P
+        // (already in TMEM) is rescaled too.
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float sv[2][32];
@@ -668,62 +689,79 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
           tmem_wait_ld();
           scores(sv[0], j0 + hf * 64);
           scores(sv[1], j0 + hf * 64 + 32);
-          float t1[22];
+          float hsum[4] = {0.f, 0.f, 0.f, 0.f};
+          auto exp_store = [&](float m_use) {
 #pragma unroll
-          for (int k = 0; k < 21; ++k) {
-            const int e = 3 * k;
-            t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
-          }
-          t1[21] = sv[1][31];
-          float t2[8];
-#pragma unroll
-          for (int k = 0; k < 7; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
-          t2[7] = t1[21];
-          float hmax = fmaxf(max3(t2[0], t2[1], t2[2]), fmaxf(max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7])));
-          if (fast && hmax != -INFINITY) hmax *= sl2;
-          const float m_new = fmaxf(m_ref, hmax);
-          const bool need = m_new > m_ref + kRescaleThreshold;
-          const bool wneed = __any_sync(0xffffffffu, need);
-          if (wneed) {
-            const float alpha = need ? ex2(m_ref - m_new) : 1.f;
-            if (need) {
-              m_ref = m_new;
-              l *= alpha;
-              sum[0] *= alpha;
-              sum[1] *= alpha;
-              sum[2] *= alpha;
-              sum[3] *= alpha;
+            for (int c = 0; c < 2; ++c) {
+              uint32_t pk[16];
+              chunk_exp(sv[c], cexp, m_use, pk, hsum);
+              tmem_st16(sa + hf * 32 + c * 16, pk);
             }
-            alpha_tile *= alpha;
-            warp_need = true;
-            if (hf == 1) {
+          };
+          bool slow = !kDeferredMax || __any_sync(0xffffffffu, m_ref == -INFINITY);
+          if (!slow) {
+            exp_store(m_ref);
+            const float hs = (hsum[0] + hsum[1]) + (hsum[2] + hsum[3]);
+            slow = __any_sync(0xffffffffu, !(hs <= kGuard));
+            if (slow) {
               tmem_wait_st();
-              float pw[32];
-              tmem_ld32(sa, pw);
-              tmem_wait_ld();
-              uint32_t w[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const uint32_t u = __float_as_uint(pw[e]);
-                float lo, hi;
-                if constexpr (FP8) {
-                  unpack_f16x2(u, lo, hi);
-                } else {
-                  lo = __uint_as_float(u << 16);
-                  hi = __uint_as_float(u & 0xFFFF0000u);
-                }
-                w[e] = pack_p(lo * alpha, hi * alpha);
-              }
-              tmem_st32(sa, w);
+              hsum[0] = hsum[1] = hsum[2] = hsum[3] = 0.f;
             }
           }
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          if (slow) {
+            float t1[22];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
-            chunk_exp(sv[c], cexp, m_use, pk, sum);
-            tmem_st16(sa + hf * 32 + c * 16, pk);
+            for (int k = 0; k < 21; ++k) {
+              const int e = 3 * k;
+              t1[k] = max3(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31], sv[(e + 2) >> 5][(e + 2) & 31]);
+            }
+            t1[21] = sv[1][31];
+            float t2[8];
+#pragma unroll
+            for (int k = 0; k < 7; ++k) t2[k] = max3(t1[3 * k], t1[3 * k + 1], t1[3 * k + 2]);
+            t2[7] = t1[21];
+            float hmax = fmaxf(max3(t2[0], t2[1], t2[2]), fmaxf(max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7])));
+            if (fast && hmax != -INFINITY) hmax *= sl2;
+            const float m_new = fmaxf(m_ref, hmax);
+            const bool need = m_new > m_ref + kRescaleThreshold;
+            const bool wneed = __any_sync(0xffffffffu, need);
+            if (wneed) {
+              const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+              if (need) {
+                m_ref = m_new;
+                l *= alpha;
+                sum[0] *= alpha;
+                sum[1] *= alpha;
+                sum[2] *= alpha;
+                sum[3] *= alpha;
+              }
+              alpha_tile *= alpha;
+              warp_need = true;
+              if (hf == 1) {
+                tmem_wait_st();
+                float pw[32];
+                tmem_ld32(sa, pw);
+                tmem_wait_ld();
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const uint32_t u = __float_as_uint(pw[e]);
+                  float lo, hi;
+                  if constexpr (FP8) {
+                    unpack_f16x2(u, lo, hi);
+                  } else {
+                    lo = __uint_as_float(u << 16);
+                    hi = __uint_as_float(u & 0xFFFF0000u);
+                  }
+                  w[e] = pack_p(lo * alpha, hi * alpha);
+                }
+                tmem_st32(sa, w);
+              }
+            }
+            exp_store((m_ref == -INFINITY) ? 0.f : m_ref);
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sum[q] += hsum[q];
         }
       }
       const float alpha = alpha_tile;

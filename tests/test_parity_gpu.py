@@ -286,3 +286,60 @@ def test_graph_capture_of_call_and_plan():
         assert np.array_equal(o, o_ref) and np.array_equal(l, l_ref)
         for name in ("q", "k", "v"):
             t[name].copy_(to_device(p)[name])
+
+
+# ---------------------------------------------------------- deferred row max --
+
+def _escalating_scores(p, boosts, kv_dtype="bf16"):
+    """Key tile t of every sequence gets its scores raised by boosts[t] (scaled
+    log2 units, approximately): K rows of tile t are offset along q's mean
+    direction (bf16), or their per-token scales multiplied (e4m3)."""
+    rng = np.random.default_rng(7)
+    q = fi.bf16_to_f32(p.q).copy()
+    q[:] = 0.5 + 0.05 * rng.standard_normal(q.shape).astype(np.float32)
+    p = p.replace(q=fi.bf16_bits(q))
+    lens = np.diff(p.cu_seqlens_k)
+    if kv_dtype == "bf16":
+        k = fi.bf16_to_f32(p.k).copy()
+        for b, L in enumerate(lens):
+            for t, boost in enumerate(boosts):
+                lo, hi = t * 128, min((t + 1) * 128, L)
+                if lo >= hi:
+                    break
+                # q.k ~ 0.5 * sum(k); raise each score by boost/(scale*log2e)
+                shift = boost / (p.softmax_scale * 1.4426950408889634) / (0.5 * p.dk)
+                k[p.cu_seqlens_k[b] + lo:p.cu_seqlens_k[b] + hi] += shift
+        return p.replace(k=fi.bf16_bits(k))
+    ks = p.k_scale.copy()
+    for b, L in enumerate(lens):
+        for t, boost in enumerate(boosts):
+            lo, hi = t * 128, min((t + 1) * 128, L)
+            if lo >= hi:
+                break
+            for key in range(lo, hi):
+                page = p.block_table[b, key // p.page_size]
+                ks[page, key % p.page_size] *= boost
+    return p.replace(k_scale=ks)
+
+
+@pytest.mark.parametrize("variant", ["onepass_d128", "twohalf_d128", "onepass_d192", "e4m3_d128", "plain_d128"])
+def test_deferred_max_large_and_overflowing_tiles(monkeypatch, variant):
+    """Scores that jump by ~46 log2 units after the first key tile (P values
+    near 2^46 through the fast path) and by ~140 later (the 2^64 guard fires,
+    the row max is taken and P redone) match the oracle.  The deferred max
+    runs with a score mod: ALiBi with slope 0 gives plain attention through
+    that path; `plain_d128` checks the max-first path on the same scores."""
+    if variant == "twohalf_d128":
+        monkeypatch.setenv("FA_GB300_PREFILL_VARIANT", "1")
+    mod = dict(mod="none") if variant == "plain_d128" else dict(mod="alibi", alibi_slope=0.0)
+    if variant == "e4m3_d128":
+        p = fi.make_problem([300, 200], [700, 450], hq=2, dk=128, seed=61, kv_dtype="e4m3", page_size=64, **mod)
+        # e4m3 K becomes f16 RN(e4m3 * k_scale): its 2^-12 relative rounding
+        # puts an absolute error proportional to |q.k| on each score, so this
+        # case stays at moderate scores (P up to ~2^20 on the fast path).
+        p = _escalating_scores(p, [1.0, 6.0, 1.0, 6.0, 1.0, 1.0], kv_dtype="e4m3")
+    else:
+        dk = 192 if variant == "onepass_d192" else 128
+        p = fi.make_problem([300, 200], [700, 450], hq=2, dk=dk, dv=128, seed=61, **mod)
+        p = _escalating_scores(p, [0.0, 46.0, 10.0, 140.0, 20.0, 0.0])
+    check(p)
