@@ -348,8 +348,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if (block_table->stride[1] != 1 && block_table->shape[1] > 1) return fail(FA_ERR_INVALID_ARG, "block_table rows must be contiguous");
     max_pages = block_table->shape[1];
     n_pages = k_cache->shape[0];
-    if (!is_pow2(page_size) || page_size < 16 || page_size > 256)
-      return fail(FA_ERR_UNSUPPORTED, "page_size %d: supported sizes are powers of two from 16 to 256", page_size);
+    // Page sizes from 16 keep every TMA box's shared-memory destination
+    // 1024-byte aligned (bf16 boxes of >= 8 rows, e4m3 staging boxes of >= 16
+    // rows); smaller pages would need a row-gather path.
+    if (!is_pow2(page_size) || page_size < 16 || page_size > 1024)
+      return fail(FA_ERR_UNSUPPORTED, "page_size %d: supported sizes are powers of two from 16 to 1024", page_size);
     if (k_cache->shape[1] != page_size) return fail(FA_ERR_INVALID_ARG, "k_cache.shape[1]=%lld != page_size=%d", (long long)k_cache->shape[1], page_size);
     if ((int64_t)launch->max_seqlen_k > max_pages * page_size) return fail(FA_ERR_INVALID_ARG, "max_seqlen_k exceeds block_table capacity");
     if (n_pages >= (int64_t(1) << 31)) return fail(FA_ERR_OVERFLOW, "num_pages must fit int32");

@@ -155,36 +155,43 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
   if (warp == kDecWarps) {
     // ------------------------------------------------------- producer --
+    // Lane 0 waits for the stage and arms its barrier; the stage's boxes (up
+    // to 64 with page size 1, one page-table read each) are issued by all
+    // lanes in parallel.
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
-      const int krow0 = __ldg(p.cu_k + b);
-      for (int st = first_stage; st < n_stages; ++st) {
-        const int it = st - first_stage;
-        const int slot_i = it % kDecStages;
-        if (it >= kDecStages && !mbar_wait(smem_u32(empty + slot_i), ((it / kDecStages) - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(smem_u32(full + slot_i), Cfg::kStageBytes);
-        uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
-        uint8_t *vd = kd + Cfg::kKBytes;
-        for (int bx = 0; bx < p.boxes_per_stage; ++bx) {
-          const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
-          if (bt) {
-            const int page = key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
-            const int slot = key0 & (p.page_size - 1);
+    }
+    const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
+    const int krow0 = __ldg(p.cu_k + b);
+    bool ok = true;
+    for (int st = first_stage; st < n_stages; ++st) {
+      const int it = st - first_stage;
+      const int slot_i = it % kDecStages;
+      if (lane == 0) {
+        if (it >= kDecStages) ok = mbar_wait(smem_u32(empty + slot_i), ((it / kDecStages) - 1) & 1, abort_flag, p.err);
+        if (ok) mbar_expect_tx(smem_u32(full + slot_i), Cfg::kStageBytes);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
+      uint8_t *vd = kd + Cfg::kKBytes;
+      for (int bx = lane; bx < p.boxes_per_stage; bx += 32) {
+        const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
+        if (bt) {
+          const int page = key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+          const int slot = key0 & (p.page_size - 1);
 #pragma unroll
-            for (int cb = 0; cb < NCB; ++cb) {
-              const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
-              tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, slot, page);
-              tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, slot, page);
-            }
-          } else {
+          for (int cb = 0; cb < NCB; ++cb) {
+            const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
+            tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, slot, page);
+            tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, slot, page);
+          }
+        } else {
 #pragma unroll
-            for (int cb = 0; cb < NCB; ++cb) {
-              const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
-              tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
-              tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
-            }
+          for (int cb = 0; cb < NCB; ++cb) {
+            const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
+            tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
+            tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
           }
         }
       }

@@ -224,7 +224,40 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         for (int cb = 0; cb < DK / 64; ++cb)
           tma_load_3d(smem_u32(sQ + X * Cfg::kQTileBytes + cb * kBlockM * 128), &tm_q, smem_u32(q_full), cb * 64,
                       pi.h, pi.q_row0 + X * kBlockM);
-      const int32_t *bt = PAGED ? p.block_table + (int64_t)pi.b * p.bt_stride : nullptr;
+    }
+    if constexpr (PAGED) {
+      // Paged K/V: a tile spans up to 128 pages (page size 1), one TMA box
+      // and one page-table read each.  Lane 0 waits for the ring slot and
+      // arms its barrier; the boxes are then issued by all lanes in parallel.
+      const int32_t *bt = p.block_table + (int64_t)pi.b * p.bt_stride;
+      auto load_pages = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int ncb, int kt) {
+        for (int pg = lane; pg < p.pages_per_tile; pg += 32) {
+          const int key0 = kt * kBlockN + pg * p.rows_per_box;
+          const int page = key0 < pi.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+          const int slot = key0 & (p.page_size - 1);
+          for (int cb = 0; cb < ncb; ++cb)
+            tma_load_4d(smem_u32(dst + cb * kBlockN * 128 + pg * p.rows_per_box * 128), tm, smem_u32(bar), cb * 64,
+                        pi.hk, slot, page);
+        }
+      };
+      int j = 0;
+      bool ok = true;
+      for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt), ++j) {
+        const int st = j % NSK, sv = j % NSV;
+        if (lane == 0) {
+          if (j >= NSK) ok = mbar_wait(smem_u32(k_empty + st), ((j / NSK) - 1) & 1, abort_flag, p.err);
+          if (ok) mbar_expect_tx(smem_u32(k_full + st), Cfg::kKBytes);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        load_pages(&tm_k, sK + st * Cfg::kKBytes, k_full + st, DK / 64, kt);
+        if (lane == 0) {
+          if (j >= NSV) ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err);
+          if (ok) mbar_expect_tx(smem_u32(v_full + sv), Cfg::kVBytes);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        load_pages(&tm_v, sV + sv * Cfg::kVBytes, v_full + sv, DV / 64, kt);
+      }
+    } else if (lane == 0) {
       int j = 0;
       for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt), ++j) {
         {
@@ -232,44 +265,20 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
           if (j >= NSK && !mbar_wait(smem_u32(k_empty + st), ((j / NSK) - 1) & 1, abort_flag, p.err)) break;
           mbar_expect_tx(smem_u32(k_full + st), Cfg::kKBytes);
           uint8_t *dst = sK + st * Cfg::kKBytes;
-          if constexpr (PAGED) {
-            for (int pg = 0; pg < p.pages_per_tile; ++pg) {
-              const int key0 = kt * kBlockN + pg * p.rows_per_box;
-              const int page = key0 < pi.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
-              const int slot = key0 & (p.page_size - 1);
 #pragma unroll
-              for (int cb = 0; cb < DK / 64; ++cb)
-                tma_load_4d(smem_u32(dst + cb * kBlockN * 128 + pg * p.rows_per_box * 128), &tm_k,
-                            smem_u32(k_full + st), cb * 64, pi.hk, slot, page);
-            }
-          } else {
-#pragma unroll
-            for (int cb = 0; cb < DK / 64; ++cb)
-              tma_load_3d(smem_u32(dst + cb * kBlockN * 128), &tm_k, smem_u32(k_full + st), cb * 64, pi.hk,
-                          pi.k_row0 + kt * kBlockN);
-          }
+          for (int cb = 0; cb < DK / 64; ++cb)
+            tma_load_3d(smem_u32(dst + cb * kBlockN * 128), &tm_k, smem_u32(k_full + st), cb * 64, pi.hk,
+                        pi.k_row0 + kt * kBlockN);
         }
         {
           const int sv = j % NSV;
           if (j >= NSV && !mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err)) break;
           mbar_expect_tx(smem_u32(v_full + sv), Cfg::kVBytes);
           uint8_t *dst = sV + sv * Cfg::kVBytes;
-          if constexpr (PAGED) {
-            for (int pg = 0; pg < p.pages_per_tile; ++pg) {
-              const int key0 = kt * kBlockN + pg * p.rows_per_box;
-              const int page = key0 < pi.sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
-              const int slot = key0 & (p.page_size - 1);
 #pragma unroll
-              for (int cb = 0; cb < DV / 64; ++cb)
-                tma_load_4d(smem_u32(dst + cb * kBlockN * 128 + pg * p.rows_per_box * 128), &tm_v,
-                            smem_u32(v_full + sv), cb * 64, pi.hk, slot, page);
-            }
-          } else {
-#pragma unroll
-            for (int cb = 0; cb < DV / 64; ++cb)
-              tma_load_3d(smem_u32(dst + cb * kBlockN * 128), &tm_v, smem_u32(v_full + sv), cb * 64, pi.hk,
-                          pi.k_row0 + kt * kBlockN);
-          }
+          for (int cb = 0; cb < DV / 64; ++cb)
+            tma_load_3d(smem_u32(dst + cb * kBlockN * 128), &tm_v, smem_u32(v_full + sv), cb * 64, pi.hk,
+                        pi.k_row0 + kt * kBlockN);
         }
       }
     }

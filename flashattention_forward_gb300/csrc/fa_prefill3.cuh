@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
                       pi.h, pi.q_row0 + X * kBlockM);
     }
     const int rb = p.rows_per_box;
-    const int nbox = kBlockN / rb;                    // 1..8 boxes per 64-column block
+    const int nbox = kBlockN / rb;                    // 1..8 boxes per 64-column block (pages >= 16 keys)
     const int r0 = lane * rb;                         // this lane's first key row in a tile
     const bool boxer = lane < nbox;
     auto page_at = [&](int kt) -> int {

@@ -131,7 +131,7 @@ typedef struct {
  *               (causal: i' - j < window; otherwise |i' - j| < window).
  *  score_mod    NULL or fa_score_mod_t.
  *  block_mask   NULL or fa_block_mask_t.
- *  page_size    tokens per page when paged: a power of two, 16 ... 256.
+ *  page_size    tokens per page when paged: a power of two, 16 ... 1024.
  *  launch       host scalars (required).
  *  stream       cudaStream_t.
  *

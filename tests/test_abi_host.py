@@ -121,6 +121,10 @@ def test_paged_validation(L):
     v = _t(FAKE * 3, fa.FA_BF16, [32, 16, 4, 64])
     st, msg = _call(L, bt=bt, k=k, v=v, page=24)
     assert st == fa.FA_ERR_UNSUPPORTED and "page_size" in msg
+    st, msg = _call(L, bt=bt, k=k, v=v, page=2048)
+    assert st == fa.FA_ERR_UNSUPPORTED and "16 to 1024" in msg
+    st, msg = _call(L, bt=bt, k=k, v=v, page=8)
+    assert st == fa.FA_ERR_UNSUPPORTED and "16 to 1024" in msg
     st, msg = _call(L, bt=bt, k=k, v=v, page=32)
     assert st == fa.FA_ERR_INVALID_ARG and "page_size" in msg
     st, msg = _call(L, bt=_t(FAKE * 10, fa.FA_I32, [3, 8]), k=k, v=v, page=16)

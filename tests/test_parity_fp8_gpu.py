@@ -37,6 +37,8 @@ def test_config4_paged_fp8_sampled():
 
 
 FP8_EDGE = [
+    dict(lens_q=[300, 129, 1], lens_k=[700, 129, 300], hq=4, hkv=2, dk=192, dv=128, page_size=1024, causal=True),
+    dict(lens_q=[300, 129], lens_k=[300, 400], hq=4, hkv=2, dk=128, page_size=512, spare_pages=2),
     dict(lens_q=[300, 129, 1], lens_k=[300, 400, 77], hq=4, hkv=4, dk=192, dv=128, page_size=64, causal=True),
     dict(lens_q=[300, 129], lens_k=[300, 400], hq=4, hkv=2, dk=128, page_size=16, spare_pages=4),
     dict(lens_q=[200, 64, 3], lens_k=[260, 64, 500], hq=8, hkv=1, dk=64, page_size=32, causal=True, window=90),

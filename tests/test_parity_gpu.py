@@ -89,7 +89,7 @@ def test_edge_cases_packed_and_paged(case):
     check(fi.make_problem(lens_q, lens_k, seed=100 + case, **kw))
 
 
-@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256, 512, 1024])
 @pytest.mark.parametrize("causal", [False, True])
 def test_paged_page_sizes_with_poisoned_slots(page_size, causal):
     p = fi.make_problem([70, 300, 1, 129], [200, 300, 1000, 129], hq=8, hkv=2, dk=128, seed=7,
@@ -343,3 +343,25 @@ def test_deferred_max_large_and_overflowing_tiles(monkeypatch, variant):
         p = fi.make_problem([300, 200], [700, 450], hq=2, dk=dk, dv=128, seed=61, **mod)
         p = _escalating_scores(p, [0.0, 46.0, 10.0, 140.0, 20.0, 0.0])
     check(p)
+
+
+@pytest.mark.parametrize("page_size", [16, 1024])
+@pytest.mark.parametrize("case", ["d192_bf16", "d64_bf16", "decode_splits"])
+def test_extreme_page_sizes_other_paths(page_size, case):
+    """The smallest and largest page sizes (16: eight TMA boxes per 128-key
+    tile, issued by the producer warp's lanes in parallel; 1024: a tile inside
+    one page) on the chunked-ring kernel (Dk 192), the Dk 64 ping-pong kernel
+    and the split-KV decode."""
+    if case == "d192_bf16":
+        p = fi.make_problem([300, 129, 1], [700, 129, 300], hq=4, hkv=2, dk=192, dv=128, seed=81,
+                            page_size=page_size, spare_pages=3, causal=True)
+        check(p)
+    elif case == "d64_bf16":
+        p = fi.make_problem([200, 3], [260, 500], hq=8, hkv=1, dk=64, seed=82, page_size=page_size,
+                            spare_pages=3, causal=True, window=90)
+        check(p)
+    else:
+        p = fi.make_problem([1] * 5, [1, 64, 65, 700, 2100], hq=8, hkv=2, dk=128, seed=83, page_size=page_size,
+                            spare_pages=4)
+        check(p, num_splits=3)
+
