@@ -70,6 +70,23 @@ def e4m3_quantize_per_token(x: np.ndarray):
     return b, scale
 
 
+def int8_quantize_per_token(x: np.ndarray):
+    """Per-token symmetric int8 encoding of the last axis: scale = max|row| /
+    127, value = round-to-nearest-even(x / scale) in [-127, 127].
+
+    Returns ``(int8 same shape, scale fp32 x.shape[:-1])``.  An all-zero row
+    gets scale 0 and bytes 0.  This produces the cache; it is not a step of
+    the forward pass.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0))
+    q = np.clip(np.rint(x / safe[..., None]), -127, 127).astype(np.int8)
+    q[scale == 0] = 0
+    return q, scale
+
+
 def block_causal_mask(bh: int, nqb: int, nkb: int) -> np.ndarray:
     """Block-causal 128x128 mask: block (qb, kb) active iff kb <= qb."""
     qb = np.arange(nqb)[:, None]
@@ -190,7 +207,7 @@ def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = 
                  block_mask_density: Optional[float] = None,
                  softmax_scale: Optional[float] = None, name: str = "custom",
                  q_std: float = 1.0) -> Problem:
-    """General seeded problem: N(0,1) Q/K/V rounded to bf16 (or e4m3 per token).
+    """General seeded problem: N(0,1) Q/K/V rounded to bf16 (or e4m3 / int8 per token).
 
     Draw order (fixed): Q, K, V, page permutation, block mask.
     """
@@ -211,6 +228,10 @@ def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = 
         k_tok, k_scale = e4m3_quantize_per_token(kf)
         v_tok, v_scale = e4m3_quantize_per_token(vf)
         fill = E4M3_NAN
+    elif kv_dtype == "int8":
+        k_tok, k_scale = int8_quantize_per_token(kf)
+        v_tok, v_scale = int8_quantize_per_token(vf)
+        fill = np.int8(-128)          # never produced by the encoder: poisons unused slots
     else:
         raise ValueError(kv_dtype)
     block_table = None
@@ -218,7 +239,7 @@ def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = 
         block_table, n_pg = page_pool(np.asarray(seqlens_k), page_size, rng, spare_pages, max_pages)
         k = scatter_pages(k_tok, cu_k, block_table, n_pg, page_size, fill)
         v = scatter_pages(v_tok, cu_k, block_table, n_pg, page_size, fill)
-        if kv_dtype == "e4m3":
+        if kv_dtype in ("e4m3", "int8"):
             k_scale = scatter_pages(k_scale, cu_k, block_table, n_pg, page_size, np.float32(np.nan))
             v_scale = scatter_pages(v_scale, cu_k, block_table, n_pg, page_size, np.float32(np.nan))
     else:

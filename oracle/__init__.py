@@ -28,7 +28,7 @@ _LIB = os.path.join(_BUILD, "libfa_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-KV_BF16, KV_E4M3, KV_F64 = 0, 1, 2
+KV_BF16, KV_E4M3, KV_F64, KV_I8 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -75,6 +75,8 @@ def lib():
             L.fa_oracle_combine.restype = None
             L.fa_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             L.fa_oracle_e4m3_decode.restype = ctypes.c_double
+            L.fa_oracle_i8_decode.argtypes = [ctypes.c_uint8]
+            L.fa_oracle_i8_decode.restype = ctypes.c_double
             L.fa_oracle_bf16_decode.argtypes = [ctypes.c_uint16]
             L.fa_oracle_bf16_decode.restype = ctypes.c_double
             _lib = L
@@ -83,6 +85,10 @@ def lib():
 
 def e4m3_decode(byte: int) -> float:
     return lib().fa_oracle_e4m3_decode(int(byte) & 0xFF)
+
+
+def i8_decode(byte: int) -> float:
+    return lib().fa_oracle_i8_decode(int(byte) & 0xFF)
 
 
 def bf16_decode(bits: int) -> float:
@@ -120,7 +126,8 @@ def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = Non
     elif p.kv_dtype == "bf16":
         kd, k, v, ks, vs = KV_BF16, c(p.k, np.uint16), c(p.v, np.uint16), None, None
     else:
-        kd, k, v = KV_E4M3, c(p.k, np.uint8), c(p.v, np.uint8)
+        kd = KV_E4M3 if p.kv_dtype == "e4m3" else KV_I8
+        k, v = c(p.k.view(np.uint8), np.uint8), c(p.v.view(np.uint8), np.uint8)
         ks, vs = c(p.k_scale, np.float32), c(p.v_scale, np.float32)
     bt = c(p.block_table, np.int32)
     cq, ck = c(p.cu_seqlens_q, np.int32), c(p.cu_seqlens_k, np.int32)

@@ -29,6 +29,9 @@
  *  - paged KV through block_table, FP8 e4m3 KV with per-token scales, Q/K 192
  *    and V/O 128: FlyDSL PR #1066 overview and PR description; fkl_python PR #7,
  *    fp8 KV commit (scale = max|row|/448);
+ *  - int8 KV with per-token dequantisation (value = int8 * scale): fkl_python
+ *    PR #7, prologue-fusion commit (int8 token dequant read) and fp8 KV commit
+ *    (int8's 127 uniform levels);
  *  - bottom-right causal alignment: FlyDSL PR #1066 review (COMMENT, "What I
  *    verified": bottom-right causal mask, cross_seqlen=True);
  *  - ALiBi, SoftCap, SlidingWindow and 128x128 block masks: fkl_python PR #7,
@@ -41,7 +44,7 @@
  * sequence-local i, j; GQA head hk = h / (Hq/Hkv); per-token scales are one
  * fp32 per (page, slot, kv head).
  *
- * All arithmetic is double precision; bf16 and e4m3 inputs are widened exactly.
+ * All arithmetic is double precision; bf16, e4m3 and int8 inputs are widened exactly.
  * Threads (pthreads) only split the independent rows between cores.
  */
 #include <math.h>
@@ -50,18 +53,18 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { KV_BF16 = 0, KV_E4M3 = 1, KV_F64 = 2 };
+enum { KV_BF16 = 0, KV_E4M3 = 1, KV_F64 = 2, KV_I8 = 3 };
 enum { MOD_NONE = 0, MOD_ALIBI = 1, MOD_SOFTCAP = 2 };
 
 typedef struct {
     const uint16_t *q;            /* bf16 bits [T_q][Hq][Dk] */
     const void *k, *v;            /* packed [T_k][Hkv][D] or paged [N_pg][P_s][Hkv][D] */
-    int32_t kv_dtype;             /* KV_BF16 | KV_E4M3 | KV_F64 */
+    int32_t kv_dtype;             /* KV_BF16 | KV_E4M3 | KV_F64 | KV_I8 */
     const int32_t *block_table;   /* [B][bt_stride] or NULL (packed K/V) */
     int64_t bt_stride;
     const int32_t *cu_q, *cu_k;   /* [B+1] */
     int32_t num_seqs;
-    const float *k_scale, *v_scale; /* per token and kv head; NULL unless e4m3 */
+    const float *k_scale, *v_scale; /* per token and kv head; NULL unless e4m3 / int8 */
     int32_t hq, hkv, dk, dv, page_size;
     double softmax_scale;
     int32_t causal, window, mod_kind;
@@ -81,6 +84,11 @@ double fa_oracle_bf16_decode(uint16_t b) {
 
 /* OCP FP8 E4M3 (the "OCP E4M3" of FlyDSL PR #1066): 1 sign bit, 4 exponent
  * bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN. */
+/* A stored int8 byte (two's complement) as its integer value. */
+double fa_oracle_i8_decode(uint8_t x) {
+    return (double)(x < 128 ? (int)x : (int)x - 256);
+}
+
 double fa_oracle_e4m3_decode(uint8_t x) {
     int s = (x >> 7) & 1, e = (x >> 3) & 0xF, m = x & 7;
     double mag;
@@ -102,11 +110,12 @@ static void fetch_row(const fa_oracle_problem *p, const void *base, const float 
     }
     int64_t off = (tok * p->hkv + hk) * (int64_t)d;
     double sc = 1.0;
-    if (p->kv_dtype == KV_E4M3) sc = (double)scale[tok * p->hkv + hk];
+    if (p->kv_dtype == KV_E4M3 || p->kv_dtype == KV_I8) sc = (double)scale[tok * p->hkv + hk];
     for (int x = 0; x < d; x++) {
         double val;
         if (p->kv_dtype == KV_BF16) val = fa_oracle_bf16_decode(((const uint16_t *)base)[off + x]);
         else if (p->kv_dtype == KV_E4M3) val = fa_oracle_e4m3_decode(((const uint8_t *)base)[off + x]);
+        else if (p->kv_dtype == KV_I8) val = fa_oracle_i8_decode(((const uint8_t *)base)[off + x]);
         else val = ((const double *)base)[off + x];
         dst[x] = val * sc;
     }

@@ -417,3 +417,55 @@ def test_big_pool_geometry_matches_the_page():
     assert mine["key_page_bytes"] + mine["value_page_bytes"] == g["cache_bytes_per_page"]
     assert mine["high_page"] * mine["key_page_bytes"] >= 2 ** 32
     assert mine["high_page"] * mine["value_page_bytes"] >= 2 ** 32
+
+
+# --------------------------------------------------------------- int8 KV --
+
+def test_i8_decode_all_bytes_are_twos_complement():
+    """Every stored byte decodes to the int8 value numpy assigns it."""
+    ref = np.arange(256, dtype=np.uint8).view(np.int8).astype(np.float64)
+    for b in range(256):
+        assert oracle.i8_decode(b) == ref[b], b
+
+
+def test_int8_encoder_bounds():
+    """The generator's per-token int8 codes stay in [-127, 127], hit 127 in
+    magnitude on every non-zero row, and round to nearest (|x - q*s| <= s/2)."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((50, 3, 40)).astype(np.float32)
+    x[7, 1] = 0.0
+    q, s = fi.int8_quantize_per_token(x)
+    assert q.dtype == np.int8 and q.min() >= -127 and q.max() <= 127
+    nz = s > 0
+    assert np.all(np.abs(q).max(axis=-1)[nz] == 127) and not nz[7, 1] and np.all(q[7, 1] == 0)
+    err = np.abs(x - q.astype(np.float32) * s[..., None])
+    assert np.all(err <= s[..., None] * 0.5000001)
+
+
+def test_int8_with_scales_matches_torch_sdpa_on_dequantised_values():
+    """int8 K/V with per-token scales against torch's scaled-dot-product
+    attention and logsumexp on the dequantised doubles (an implementation that
+    shares nothing with the oracle): pins the decode and where each scale
+    applies; swapping the two scales must change the answer."""
+    p = fi.make_problem([37, 64], [45, 64], hq=4, hkv=2, dk=48, dv=32, seed=22,
+                        page_size=16, kv_dtype="int8", spare_pages=2)
+    o1, l1 = oracle.forward(p)
+    for b in range(p.num_seqs):
+        q0, q1 = int(p.cu_seqlens_q[b]), int(p.cu_seqlens_q[b + 1])
+        sk = int(p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b])
+        keys = np.arange(sk)
+        pages = p.block_table[b, keys // p.page_size]
+        slots = keys % p.page_size
+        k = p.k[pages, slots].astype(np.float64) * p.k_scale[pages, slots].astype(np.float64)[..., None]
+        v = p.v[pages, slots].astype(np.float64) * p.v_scale[pages, slots].astype(np.float64)[..., None]
+        q = fi.bf16_to_f32(p.q[q0:q1]).astype(np.float64)
+        kk = torch.from_numpy(np.repeat(k, 2, axis=1)).permute(1, 0, 2)     # [Hq, sk, dk]
+        vv = torch.from_numpy(np.repeat(v, 2, axis=1)).permute(1, 0, 2)
+        qq = torch.from_numpy(q).permute(1, 0, 2)
+        s = torch.matmul(qq, kk.transpose(1, 2)) * p.softmax_scale
+        ref_o = torch.softmax(s, dim=-1) @ vv
+        ref_l = torch.logsumexp(s, dim=-1)
+        assert_close(o1[q0:q1], ref_o.permute(1, 0, 2).numpy(), 1e-12)
+        assert_close(l1[:, q0:q1], ref_l.numpy(), 1e-12)
+    o3, _ = oracle.forward(p.replace(k_scale=p.v_scale, v_scale=p.k_scale))
+    assert np.max(np.abs(o3 - o1)) > 1e-3
