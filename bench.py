@@ -127,8 +127,9 @@ def dev_tensors(p, dev):
         t["k"] = torch.from_numpy(p.k.view(np.int16).copy()).view(torch.bfloat16).to(dev)
         t["v"] = torch.from_numpy(p.v.view(np.int16).copy()).view(torch.bfloat16).to(dev)
     else:
-        t["k"] = torch.from_numpy(p.k.copy()).view(torch.float8_e4m3fn).to(dev)
-        t["v"] = torch.from_numpy(p.v.copy()).view(torch.float8_e4m3fn).to(dev)
+        kvt = torch.int8 if p.kv_dtype == "int8" else torch.float8_e4m3fn
+        t["k"] = torch.from_numpy(p.k.copy()).view(kvt).to(dev)
+        t["v"] = torch.from_numpy(p.v.copy()).view(kvt).to(dev)
         t["k_scale"] = torch.from_numpy(p.k_scale.copy()).to(dev)
         t["v_scale"] = torch.from_numpy(p.v_scale.copy()).to(dev)
     t["cu_q"] = torch.from_numpy(p.cu_seqlens_q.copy()).to(dev)
@@ -478,6 +479,17 @@ def other_workloads(dev, warmup, steps, flush, pk):
     ms = statistics.mean(times)
     fl = fi.prefill_flops(p)
     res["paged_fp8_d192_v128_16seq_h16_p64_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                                        "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+                                                        "gflop": fl / 1e9}
+    del t
+    # the same geometry with an int8 cache (per-token scales)
+    p = fi.make_problem([int(x) for x in np.diff(p.cu_seqlens_q)], hq=16, hkv=16, dk=192, dv=128, seed=1,
+                        page_size=64, kv_dtype="int8", causal=True, name="config4_int8")
+    t = dev_tensors(p, dev)
+    call, _, _, _ = make_call(p, t, num_splits=0)
+    ms = statistics.mean(time_calls([call], warmup, steps, flush))
+    fl = fi.prefill_flops(p)
+    res["paged_int8_d192_v128_16seq_h16_p64_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                                                         "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
                                                         "gflop": fl / 1e9}
     del t

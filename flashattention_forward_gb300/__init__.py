@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libfa_gb300.so")
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_OVERFLOW, FA_ERR_CUDA = 0, 1, 2, 3, 4
 FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_BOUNDS = 5, 6
-FA_BF16, FA_E4M3, FA_F32, FA_I32, FA_U8 = 0, 1, 2, 3, 4
+FA_BF16, FA_E4M3, FA_F32, FA_I32, FA_U8, FA_I8 = 0, 1, 2, 3, 4, 5
 MOD_NONE, MOD_ALIBI, MOD_SOFTCAP = 0, 1, 2
 
 EXPORTED = ("fa_fwd_varlen", "fa_fwd_workspace_bytes", "fa_fwd_default_splits", "fa_combine",
@@ -109,9 +109,18 @@ def _check(status: int):
         raise FaError(status, lib().fa_last_error().decode())
 
 
-_DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int32: FA_I32, torch.uint8: FA_U8}
+_DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int32: FA_I32, torch.uint8: FA_U8, torch.int8: FA_I8}
 if hasattr(torch, "float8_e4m3fn"):
     _DT[torch.float8_e4m3fn] = FA_E4M3
+
+
+def _kv_dtype(k_cache: torch.Tensor) -> int:
+    """bf16, int8 (per-token scaled) or e4m3 (float8_e4m3fn or raw uint8 bytes)."""
+    if k_cache.dtype == torch.bfloat16:
+        return FA_BF16
+    if k_cache.dtype == torch.int8:
+        return FA_I8
+    return FA_E4M3
 
 
 def as_tensor(t: Optional[torch.Tensor], fa_dtype: Optional[int] = None) -> Optional[Tensor]:
@@ -169,7 +178,7 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     Tq, Hq, Dk = q.shape
     Dv = v_cache.shape[-1]
     Hkv = k_cache.shape[-2]
-    kv_dt = FA_BF16 if k_cache.dtype == torch.bfloat16 else FA_E4M3
+    kv_dt = _kv_dtype(k_cache)
     if out is None:
         out = torch.empty((Tq, Hq, Dv), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
@@ -249,7 +258,7 @@ class FwdPlan:
         Tq, Hq, Dk = q.shape
         Dv = v_cache.shape[-1]
         Hkv = k_cache.shape[-2]
-        kv_dt = FA_BF16 if k_cache.dtype == torch.bfloat16 else FA_E4M3
+        kv_dt = _kv_dtype(k_cache)
         self.out = kw.get("out")
         if self.out is None:
             self.out = torch.empty((Tq, Hq, Dv), dtype=torch.bfloat16, device=q.device)

@@ -66,6 +66,7 @@ int dtype_size(int dt) {
   switch (dt) {
     case FA_BF16: return 2;
     case FA_E4M3: return 1;
+    case FA_I8: return 1;
     case FA_F32: return 4;
     case FA_I32: return 4;
     case FA_U8: return 1;
@@ -174,7 +175,7 @@ fa_status_t run_prefill(fa::PrefillLaunch L, const fa_fwd_plan_s &P, cudaStream_
   else if (P.dk == 128) e = fa::launch_prefill_128_128(L);
   else e = fa::launch_prefill_192_128(L);
   if (e == cudaErrorNotSupported && P.fp8)
-    return fail(FA_ERR_UNSUPPORTED, "the e4m3 kernel's register split does not fit this build's launch registers");
+    return fail(FA_ERR_UNSUPPORTED, "the e4m3/int8 kernel's register split does not fit this build's launch registers");
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }
@@ -322,7 +323,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const int kvnd = paged ? 4 : 3;
   if (!k_cache || !v_cache) return fail(FA_ERR_INVALID_ARG, "k_cache/v_cache is NULL");
   const int kv_dt = k_cache->dtype;
-  if (kv_dt != FA_BF16 && kv_dt != FA_E4M3) return fail(FA_ERR_INVALID_ARG, "k_cache dtype must be bf16 or e4m3");
+  if (kv_dt != FA_BF16 && kv_dt != FA_E4M3 && kv_dt != FA_I8)
+    return fail(FA_ERR_INVALID_ARG, "k_cache dtype must be bf16, e4m3 or int8");
   if ((st = check_tensor(k_cache, "k_cache", kv_dt, kvnd))) return st;
   if ((st = check_tensor(v_cache, "v_cache", kv_dt, kvnd))) return st;
   const int64_t Hkv = k_cache->shape[kvnd - 2];
@@ -368,9 +370,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     return fail(FA_ERR_OVERFLOW, "total tokens must fit the int32 cu_seqlens");
   if (!paged && k_cache->shape[0] < launch->total_k) return fail(FA_ERR_INVALID_ARG, "packed k_cache has fewer rows than total_k");
   // ---- scales
-  const bool fp8 = kv_dt == FA_E4M3;
+  // e4m3 and int8 caches (byte values with per-token scales) share the
+  // converter-warp kernel; `fp8` below means either.
+  const bool fp8 = kv_dt == FA_E4M3 || kv_dt == FA_I8;
   if (fp8) {
-    if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "e4m3 caches need k_scale and v_scale");
+    if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "e4m3 and int8 caches need k_scale and v_scale");
     for (const fa_tensor_t *s : {k_scale, v_scale}) {
       if ((st = check_tensor(s, "kv scale", FA_F32, kvnd - 1))) return st;
       for (int i = 0; i < kvnd - 1; ++i)
@@ -378,7 +382,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
       if (!contiguous(s)) return fail(FA_ERR_INVALID_ARG, "kv scales must be contiguous");
     }
   } else if (k_scale || v_scale) {
-    return fail(FA_ERR_INVALID_ARG, "k_scale/v_scale are only valid with an e4m3 cache");
+    return fail(FA_ERR_INVALID_ARG, "k_scale/v_scale are only valid with an e4m3 or int8 cache");
   }
   // ---- out, lse
   if ((st = check_tensor(out, "out", FA_BF16, 3))) return st;
@@ -428,7 +432,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if ((int64_t)launch->max_seqlen_q * group > fa::kDecRows)
       return fail(FA_ERR_UNSUPPORTED, "split-KV needs max_seqlen_q * Hq/Hkv <= %d", fa::kDecRows);
     if (Dk != Dv || (Dk != 64 && Dk != 128)) return fail(FA_ERR_UNSUPPORTED, "split-KV supports Dk = Dv in {64, 128}");
-    if (fp8) return fail(FA_ERR_UNSUPPORTED, "split-KV runs on bf16 caches; use num_splits = 0 for e4m3");
+    if (fp8) return fail(FA_ERR_UNSUPPORTED, "split-KV runs on bf16 caches; use num_splits = 0 for e4m3/int8");
     if (mod != 0 || block_mask) return fail(FA_ERR_UNSUPPORTED, "split-KV does not take score mods or block masks");
     if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "too many sequences or kv heads for split-KV");
     fa::DecodeLaunch L;
@@ -596,6 +600,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   p.err = error_word();
   L.paged = paged;
   L.fp8 = fp8;
+  L.int8 = kv_dt == FA_I8;
   {
     // Test knob: FA_GB300_PREFILL_VARIANT=1 forces the 10-warp two-pass softmax.
     const char *v = getenv("FA_GB300_PREFILL_VARIANT");

@@ -15,10 +15,11 @@
 // start on its first chunk while the others still load.  V keeps whole-tile
 // stages (the PV operand spans its 64-column blocks at a fixed stride).
 //
-// e4m3 caches (FlyDSL PR #1066: paged FP8 K/V with per-token scales) are
-// staged by TMA as raw bytes and turned into f16 MMA operands in shared memory
-// by six converter warps:
-//   K' = RN_f16(e4m3(k) * k_scale),  V' = RN_f16(e4m3(v) * v_scale)
+// e4m3 caches (FlyDSL PR #1066: paged FP8 K/V with per-token scales) and int8
+// caches (fkl_python PR #7: per-token int8 KV dequantisation) are staged by
+// TMA as raw bytes and turned into f16 MMA operands in shared memory by six
+// converter warps:
+//   K' = RN_f16(dec(k) * k_scale),  V' = RN_f16(dec(v) * v_scale)
 // (one rounding each, fp32 product).  Q is brought to f16 in place with a
 // per-row power-of-two factor 2^e (exact for every bf16 value within 2^-28 of
 // the row maximum; the factor 2^-e returns in the softmax scale), so both
@@ -103,7 +104,26 @@ __device__ __forceinline__ void e4m3x4_scaled_f16(uint32_t w, float s, uint32_t 
   o1 = pack_f16x2(c, d);
 }
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
+// Four int8 bytes times an fp32 scale -> two f16 pairs.  Each byte becomes an
+// exact fp32 through the float 2^23 + (x + 128) -- the byte, offset by 128,
+// in the low mantissa bits -- minus 2^23 + 128; then one product and one
+// rounding to f16.
+__device__ __forceinline__ void i8x4_scaled_f16(uint32_t w, float s, uint32_t &o0, uint32_t &o1) {
+  const uint32_t u = w ^ 0x80808080u;
+  float a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650));
+  float b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651));
+  float c = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652));
+  float d = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653));
+  add2(a, b, -8388736.f, -8388736.f);
+  add2(c, d, -8388736.f, -8388736.f);
+  fma2(a, b, a, b, s, 0.f);
+  fma2(c, d, c, d, s, 0.f);
+  o0 = pack_f16x2(a, b);
+  o1 = pack_f16x2(c, d);
+}
+
+// I8 (with FP8): the byte cache holds int8 values instead of e4m3.
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8>
 __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::kThreads, 1)
     fa_prefill3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -476,10 +496,17 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
           const float s_row = __shfl_sync(0xffffffffu, sa, rr);
           const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
           uint32_t o[8];
-          e4m3x4_scaled_f16(raw.x, s_row, o[0], o[1]);
-          e4m3x4_scaled_f16(raw.y, s_row, o[2], o[3]);
-          e4m3x4_scaled_f16(raw.z, s_row, o[4], o[5]);
-          e4m3x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+          if constexpr (I8) {
+            i8x4_scaled_f16(raw.x, s_row, o[0], o[1]);
+            i8x4_scaled_f16(raw.y, s_row, o[2], o[3]);
+            i8x4_scaled_f16(raw.z, s_row, o[4], o[5]);
+            i8x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+          } else {
+            e4m3x4_scaled_f16(raw.x, s_row, o[0], o[1]);
+            e4m3x4_scaled_f16(raw.y, s_row, o[2], o[3]);
+            e4m3x4_scaled_f16(raw.z, s_row, o[4], o[5]);
+            e4m3x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+          }
           if (!live) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) o[k] = 0u;

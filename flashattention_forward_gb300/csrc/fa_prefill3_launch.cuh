@@ -9,14 +9,14 @@ namespace fa {
 // A register-split variant raises the softmax warps with setmaxnreg.inc,
 // which waits until other warps of the CTA release registers: it may run only
 // when the compiled launch register count covers the whole split.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8>
 bool prefill3_split_fits() {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>;
   if constexpr (!Cfg::kSplitRegs) return true;
   static int verdict = -1;   // per process: all devices run the same binary
   if (verdict < 0) {
     cudaFuncAttributes a;
-    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG>) == cudaSuccess &&
+    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8>) == cudaSuccess &&
                a.numRegs * Cfg::kThreads >= Cfg::kPoolNeeded)
                   ? 1
                   : 0;
@@ -24,12 +24,12 @@ bool prefill3_split_fits() {
   return verdict == 1;
 }
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8>
 cudaError_t launch_prefill3_one(const PrefillLaunch &L) {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>;
-  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG>()) return cudaErrorNotSupported;
+  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8>()) return cudaErrorNotSupported;
   static unsigned long long done = 0;
-  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG>;
+  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
@@ -38,25 +38,26 @@ cudaError_t launch_prefill3_one(const PrefillLaunch &L) {
 
 // bf16: the 12-warp split variant when it fits (and is not overridden), else
 // the 10-warp two-half softmax.  e4m3: the 16-warp split variant only.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool I8>
 cudaError_t launch_prefill3_pick(const PrefillLaunch &L) {
   if constexpr (FP8) {
-    return launch_prefill3_one<DK, DV, PAGED, true, MOD, false>(L);
+    return launch_prefill3_one<DK, DV, PAGED, true, MOD, false, I8>(L);
   } else {
-    if (L.variant != 1 && prefill3_split_fits<DK, DV, PAGED, false, MOD, true>())
-      return launch_prefill3_one<DK, DV, PAGED, false, MOD, true>(L);
-    return launch_prefill3_one<DK, DV, PAGED, false, MOD, false>(L);
+    if (L.variant != 1 && prefill3_split_fits<DK, DV, PAGED, false, MOD, true, false>())
+      return launch_prefill3_one<DK, DV, PAGED, false, MOD, true, false>(L);
+    return launch_prefill3_one<DK, DV, PAGED, false, MOD, false, false>(L);
   }
 }
 
-template <int DK, int DV, bool FP8>
+// FP8: byte caches with per-token scales; I8 selects int8 values over e4m3.
+template <int DK, int DV, bool FP8, bool I8 = false>
 cudaError_t launch_prefill3(const PrefillLaunch &L) {
   auto by_mod = [&](auto paged_tag) -> cudaError_t {
     constexpr bool PG = decltype(paged_tag)::value;
     switch (L.mod) {
-      case 0: return launch_prefill3_pick<DK, DV, PG, FP8, 0>(L);
-      case 1: return launch_prefill3_pick<DK, DV, PG, FP8, 1>(L);
-      default: return launch_prefill3_pick<DK, DV, PG, FP8, 2>(L);
+      case 0: return launch_prefill3_pick<DK, DV, PG, FP8, 0, I8>(L);
+      case 1: return launch_prefill3_pick<DK, DV, PG, FP8, 1, I8>(L);
+      default: return launch_prefill3_pick<DK, DV, PG, FP8, 2, I8>(L);
     }
   };
   return L.paged ? by_mod(std::true_type{}) : by_mod(std::false_type{});

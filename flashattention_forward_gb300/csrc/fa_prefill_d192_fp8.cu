@@ -4,5 +4,7 @@
 #include "fa_prefill3_launch.cuh"
 
 namespace fa {
-cudaError_t launch_prefill_192_128_fp8(const PrefillLaunch &L) { return launch_prefill3<192, 128, true>(L); }
+cudaError_t launch_prefill_192_128_fp8(const PrefillLaunch &L) {
+  return L.int8 ? launch_prefill_192_128_i8(L) : launch_prefill3<192, 128, true>(L);
+}
 }  // namespace fa

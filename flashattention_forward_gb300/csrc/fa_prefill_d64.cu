@@ -49,7 +49,7 @@ cudaError_t by_mod(const PrefillLaunch &L) {
 }  // namespace
 
 cudaError_t launch_prefill_64_64(const PrefillLaunch &L) {
-  if (L.fp8) return launch_prefill3<64, 64, true>(L);   // e4m3 K/V: converter-warp kernel
+  if (L.fp8) return L.int8 ? launch_prefill_64_64_i8(L) : launch_prefill3<64, 64, true>(L);   // byte K/V
   return L.paged ? by_mod<true>(L) : by_mod<false>(L);
 }
 }  // namespace fa

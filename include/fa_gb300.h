@@ -61,7 +61,7 @@ typedef enum {
     FA_ERR_DEVICE_BOUNDS = 6   /* (device word) an index was out of range */
 } fa_status_t;
 
-typedef enum { FA_BF16 = 0, FA_E4M3 = 1, FA_F32 = 2, FA_I32 = 3, FA_U8 = 4 } fa_dtype_t;
+typedef enum { FA_BF16 = 0, FA_E4M3 = 1, FA_F32 = 2, FA_I32 = 3, FA_U8 = 4, FA_I8 = 5 } fa_dtype_t;
 
 /* A strided device tensor.  Strides are in ELEMENTS; shape[ndim..4] unused. */
 typedef struct {

@@ -22,8 +22,9 @@ def to_device(p, dev="cuda"):
         t["k"] = torch.from_numpy(p.k.view(np.int16).copy()).view(torch.bfloat16).to(dev)
         t["v"] = torch.from_numpy(p.v.view(np.int16).copy()).view(torch.bfloat16).to(dev)
     else:
-        t["k"] = torch.from_numpy(p.k.copy()).view(torch.float8_e4m3fn).to(dev)
-        t["v"] = torch.from_numpy(p.v.copy()).view(torch.float8_e4m3fn).to(dev)
+        kvt = torch.int8 if p.kv_dtype == "int8" else torch.float8_e4m3fn
+        t["k"] = torch.from_numpy(p.k.copy()).view(kvt).to(dev)
+        t["v"] = torch.from_numpy(p.v.copy()).view(kvt).to(dev)
         t["k_scale"] = torch.from_numpy(p.k_scale.copy()).to(dev)
         t["v_scale"] = torch.from_numpy(p.v_scale.copy()).to(dev)
     t["cu_q"] = torch.from_numpy(p.cu_seqlens_q.copy()).to(dev)

@@ -133,11 +133,14 @@ def test_paged_validation(L):
     assert st == fa.FA_ERR_INVALID_ARG and "capacity" in msg
 
 
-def test_e4m3_needs_scales(L):
-    k = _t(FAKE * 2, fa.FA_E4M3, [256, 4, 64])
-    v = _t(FAKE * 3, fa.FA_E4M3, [256, 4, 64])
+@pytest.mark.parametrize("dt", [fa.FA_E4M3, fa.FA_I8])
+def test_byte_caches_need_scales(L, dt):
+    k = _t(FAKE * 2, dt, [256, 4, 64])
+    v = _t(FAKE * 3, dt, [256, 4, 64])
     st, msg = _call(L, k=k, v=v)
     assert st == fa.FA_ERR_INVALID_ARG and "scale" in msg
+    st, msg = _call(L, k=_t(FAKE * 2, fa.FA_U8, [256, 4, 64]), v=_t(FAKE * 3, fa.FA_U8, [256, 4, 64]))
+    assert st == fa.FA_ERR_INVALID_ARG and "int8" in msg
 
 
 def test_overflow_guard(L):
