@@ -121,6 +121,8 @@ class Problem:
     alibi_slope: float = 0.0
     softcap: float = 0.0
     block_mask: Optional[np.ndarray] = None    # uint8 [B*Hq, nqb, nkb]
+    q_dtype: str = "bf16"                      # "bf16" (uint16 bits) or "e4m3" (uint8 bytes; its
+                                               # per-tensor scale is folded into softmax_scale)
 
     @property
     def num_seqs(self) -> int:
@@ -206,7 +208,7 @@ def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = 
                  alibi_slope: float = 0.0625, softcap: float = 20.0,
                  block_mask_density: Optional[float] = None,
                  softmax_scale: Optional[float] = None, name: str = "custom",
-                 q_std: float = 1.0) -> Problem:
+                 q_std: float = 1.0, q_dtype: str = "bf16") -> Problem:
     """General seeded problem: N(0,1) Q/K/V rounded to bf16 (or e4m3 / int8 per token).
 
     Draw order (fixed): Q, K, V, page permutation, block mask.
@@ -218,7 +220,18 @@ def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = 
     rng = np.random.default_rng(seed)
     cu_q, cu_k = _cu(seqlens_q), _cu(seqlens_k)
     tq, tk = int(cu_q[-1]), int(cu_k[-1])
-    q = bf16_bits(rng.standard_normal((tq, hq, dk), dtype=np.float32) * np.float32(q_std))
+    qf = rng.standard_normal((tq, hq, dk), dtype=np.float32) * np.float32(q_std)
+    q = bf16_bits(qf)
+    q_scale = 1.0
+    if q_dtype == "e4m3":
+        # one scale for the whole tensor: max|Q| / 448; the forward pass sees
+        # it only through softmax_scale
+        amax = float(np.abs(qf).max()) if qf.size else 0.0
+        q_scale = amax / E4M3_MAX if amax > 0 else 1.0
+        q = torch.from_numpy(np.ascontiguousarray(qf / np.float32(q_scale))).to(torch.float8_e4m3fn) \
+            .view(torch.uint8).numpy().copy()
+    elif q_dtype != "bf16":
+        raise ValueError(q_dtype)
     kf = bf16_to_f32(bf16_bits(rng.standard_normal((tk, hkv, dk), dtype=np.float32)))
     vf = bf16_to_f32(bf16_bits(rng.standard_normal((tk, hkv, dv), dtype=np.float32)))
     k_scale = v_scale = None
@@ -254,10 +267,10 @@ def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = 
         name=name, q=q, k=k, v=v, kv_dtype=kv_dtype, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
         hq=hq, hkv=hkv, dk=dk, dv=dv, block_table=block_table, page_size=page_size,
         k_scale=k_scale, v_scale=v_scale,
-        softmax_scale=(1.0 / math.sqrt(dk)) if softmax_scale is None else float(softmax_scale),
+        softmax_scale=((1.0 / math.sqrt(dk)) if softmax_scale is None else float(softmax_scale)) * q_scale,
         causal=causal, window=window, mod_kind=mk,
         alibi_slope=alibi_slope if mk == MOD_ALIBI else 0.0,
-        softcap=softcap if mk == MOD_SOFTCAP else 0.0, block_mask=bm)
+        softcap=softcap if mk == MOD_SOFTCAP else 0.0, block_mask=bm, q_dtype=q_dtype)
 
 
 # --------------------------------------------------------------------------

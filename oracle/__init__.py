@@ -58,6 +58,7 @@ class _Problem(ctypes.Structure):
         ("n_qblk", ctypes.c_int32), ("n_kblk", ctypes.c_int32),
         ("blk_q", ctypes.c_int32), ("blk_k", ctypes.c_int32),
         ("kv_lo", ctypes.c_int64), ("kv_hi", ctypes.c_int64),
+        ("q_dtype", ctypes.c_int32),
     ]
 
 
@@ -120,7 +121,8 @@ def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = Non
         keep.append(a)
         return a
 
-    q = c(p.q, np.uint16)
+    q_e4m3 = getattr(p, "q_dtype", "bf16") == "e4m3"
+    q = c(p.q, np.uint8 if q_e4m3 else np.uint16)
     if k_f64 is not None:
         kd, k, v, ks, vs = KV_F64, c(k_f64, np.float64), c(v_f64, np.float64), None, None
     elif p.kv_dtype == "bf16":
@@ -143,7 +145,8 @@ def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = Non
         block_mask=_ptr(bm),
         n_qblk=(bm.shape[1] if bm is not None else 0), n_kblk=(bm.shape[2] if bm is not None else 0),
         blk_q=128, blk_k=128,
-        kv_lo=(kv_range[0] if kv_range else 0), kv_hi=(kv_range[1] if kv_range else -1))
+        kv_lo=(kv_range[0] if kv_range else 0), kv_hi=(kv_range[1] if kv_range else -1),
+        q_dtype=1 if q_e4m3 else 0)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     if units is None:

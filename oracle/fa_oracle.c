@@ -29,6 +29,8 @@
  *  - paged KV through block_table, FP8 e4m3 KV with per-token scales, Q/K 192
  *    and V/O 128: FlyDSL PR #1066 overview and PR description; fkl_python PR #7,
  *    fp8 KV commit (scale = max|row|/448);
+ *  - e4m3 Q with a scalar descale (folded into softmax_scale): FlyDSL PR #1066
+ *    description (OCP E4M3 Q/K/V with scalar descales);
  *  - int8 KV with per-token dequantisation (value = int8 * scale): fkl_python
  *    PR #7, prologue-fusion commit (int8 token dequant read) and fp8 KV commit
  *    (int8's 127 uniform levels);
@@ -57,7 +59,7 @@ enum { KV_BF16 = 0, KV_E4M3 = 1, KV_F64 = 2, KV_I8 = 3 };
 enum { MOD_NONE = 0, MOD_ALIBI = 1, MOD_SOFTCAP = 2 };
 
 typedef struct {
-    const uint16_t *q;            /* bf16 bits [T_q][Hq][Dk] */
+    const void *q;                /* [T_q][Hq][Dk]: bf16 bits, or e4m3 bytes (q_dtype) */
     const void *k, *v;            /* packed [T_k][Hkv][D] or paged [N_pg][P_s][Hkv][D] */
     int32_t kv_dtype;             /* KV_BF16 | KV_E4M3 | KV_F64 | KV_I8 */
     const int32_t *block_table;   /* [B][bt_stride] or NULL (packed K/V) */
@@ -72,7 +74,10 @@ typedef struct {
     const uint8_t *block_mask;    /* [B*Hq][n_qblk][n_kblk] or NULL */
     int32_t n_qblk, n_kblk, blk_q, blk_k;
     int64_t kv_lo, kv_hi;         /* restrict keys to [kv_lo, kv_hi) when kv_hi >= 0 */
+    int32_t q_dtype;              /* Q_BF16 | Q_E4M3 (a per-tensor Q scale is folded into softmax_scale) */
 } fa_oracle_problem;
+
+enum { Q_BF16 = 0, Q_E4M3 = 1 };
 
 /* bf16 -> double: the bf16 bits are the upper half of an IEEE binary32. */
 double fa_oracle_bf16_decode(uint16_t b) {
@@ -156,8 +161,11 @@ static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, d
     int64_t ip = i + sk - sq;
     int hk = h / (p->hq / p->hkv);
 
-    for (int x = 0; x < p->dk; x++)
-        qrow[x] = fa_oracle_bf16_decode(p->q[(t * p->hq + h) * (int64_t)p->dk + x]);
+    for (int x = 0; x < p->dk; x++) {
+        const int64_t at = (t * p->hq + h) * (int64_t)p->dk + x;
+        qrow[x] = p->q_dtype == Q_E4M3 ? fa_oracle_e4m3_decode(((const uint8_t *)p->q)[at])
+                                       : fa_oracle_bf16_decode(((const uint16_t *)p->q)[at]);
+    }
 
     int any = 0;
     double m = -INFINITY;

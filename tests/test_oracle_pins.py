@@ -66,7 +66,10 @@ def brute_mask(p, b, h, sq, sk):
 
 def sdpa_reference(p, bias_fn=None):
     """torch fp64 SDPA per sequence (GQA by repeat_interleave) and logsumexp."""
-    q = fi.bf16_to_f32(p.q).astype(np.float64)
+    if p.q_dtype == "e4m3":
+        q = torch.from_numpy(p.q.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    else:
+        q = fi.bf16_to_f32(p.q).astype(np.float64)
     k = kv_tokens_f64(p, "k")
     v = kv_tokens_f64(p, "v")
     g = p.hq // p.hkv
@@ -469,3 +472,40 @@ def test_int8_with_scales_matches_torch_sdpa_on_dequantised_values():
         assert_close(l1[:, q0:q1], ref_l.numpy(), 1e-12)
     o3, _ = oracle.forward(p.replace(k_scale=p.v_scale, v_scale=p.k_scale))
     assert np.max(np.abs(o3 - o1)) > 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_e4m3_q_matches_torch_sdpa(causal):
+    """e4m3 Q bytes (decoded by torch) with paged e4m3 K/V against torch's
+    fp64 SDPA: pins the Q decode and the Q byte layout."""
+    p = fi.make_problem([37, 0, 64], [45, 3, 64], hq=4, hkv=2, dk=32, dv=16, seed=23,
+                        page_size=16, kv_dtype="e4m3", spare_pages=2, causal=causal,
+                        q_dtype="e4m3")
+    assert p.q.dtype == np.uint8 and p.q.shape == (101, 4, 32)
+    out, lse = oracle.forward(p)
+    ro, rl = sdpa_reference(p)
+    assert_close(out, ro, 1e-12)
+    assert_close(lse, rl, 1e-12)
+
+
+def test_e4m3_q_scale_is_folded_into_softmax_scale():
+    """The per-tensor Q scale (max|Q|/448) reaches the scores only through
+    softmax_scale: the e4m3-Q problem must agree with the bf16-Q problem of the
+    same seed to within e4m3's rounding (3 mantissa bits), and must not once the
+    fold is undone."""
+    kw = dict(hq=2, hkv=1, dk=64, dv=64, seed=24, causal=True)
+    pb = fi.make_problem([96, 40], [128, 40], **kw)
+    pe = fi.make_problem([96, 40], [128, 40], q_dtype="e4m3", **kw)
+    qb = fi.bf16_to_f32(pb.q)
+    qe = torch.from_numpy(pe.q.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    qs = pe.softmax_scale / pb.softmax_scale
+    assert qs == pytest.approx(np.abs(qb).max() / 448.0, rel=1e-2)
+    assert np.abs(qe).max() <= 448.0
+    # every decoded Q element times the scale is within e4m3's half-ulp of Q
+    err = np.abs(qe * qs - qb)
+    assert np.all(err <= np.maximum(np.abs(qb) * 2.0 ** -4, 2.0 ** -10 * qs) + 1e-2 * np.abs(qb))
+    ob, lb = oracle.forward(pb)
+    oe, le = oracle.forward(pe)
+    assert np.max(np.abs(oe - ob)) < 0.1 and np.max(np.abs(le - lb)) < 0.1
+    ou, lu = oracle.forward(pe.replace(softmax_scale=pb.softmax_scale))
+    assert np.max(np.abs(lu - lb)) > 1.0
