@@ -122,7 +122,10 @@ class ClockSampler:
 
 
 def dev_tensors(p, dev):
-    t = {"q": torch.from_numpy(p.q.view(np.int16).copy()).view(torch.bfloat16).to(dev)}
+    if p.q_dtype == "e4m3":
+        t = {"q": torch.from_numpy(p.q.copy()).view(torch.float8_e4m3fn).to(dev)}
+    else:
+        t = {"q": torch.from_numpy(p.q.view(np.int16).copy()).view(torch.bfloat16).to(dev)}
     if p.kv_dtype == "bf16":
         t["k"] = torch.from_numpy(p.k.view(np.int16).copy()).view(torch.bfloat16).to(dev)
         t["v"] = torch.from_numpy(p.v.view(np.int16).copy()).view(torch.bfloat16).to(dev)
@@ -493,6 +496,19 @@ def other_workloads(dev, warmup, steps, flush, pk):
                                                         "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
                                                         "gflop": fl / 1e9}
     del t
+    # the same lengths at Dk = Dv = 128 with e4m3 K/V: bf16 Q (f16 QK) and
+    # e4m3 Q (QK on the e4m3 bytes)
+    for qd in ("bf16", "e4m3"):
+        p = fi.make_problem([int(x) for x in np.diff(p.cu_seqlens_q)], hq=16, hkv=16, dk=128, dv=128, seed=1,
+                            page_size=64, kv_dtype="e4m3", q_dtype=qd, causal=True, name="config4_d128_" + qd)
+        t = dev_tensors(p, dev)
+        call, _, _, _ = make_call(p, t, num_splits=0)
+        ms = statistics.mean(time_calls([call], warmup, steps, flush))
+        fl = fi.prefill_flops(p)
+        res[f"paged_fp8kv_q{qd}_d128_16seq_h16_p64_causal"] = {
+            "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+            "gflop": fl / 1e9}
+        del t
     # flex runs at B=4, H=16, S=8192
     for run in fi.CONFIG5_RUNS:
         p = fi.config5(run)
@@ -530,6 +546,14 @@ def profile_only(name, warmup, steps):
         p, splits = fi.make_problem([8192] * 4, hq=16, dk=128, name="long_noncausal"), 0
     elif name == "fp8":
         p, splits = fi.config4(), 0
+    elif name in ("fp8kv_d128", "e4m3q_d128"):
+        lens = [int(x) for x in np.diff(fi.config4().cu_seqlens_q)]
+        p = fi.make_problem(lens, hq=16, hkv=16, dk=128, dv=128, seed=1, page_size=64, kv_dtype="e4m3",
+                            q_dtype="e4m3" if name == "e4m3q_d128" else "bf16", causal=True, name=name)
+        splits = 0
+    elif name == "long_e4m3q":
+        p, splits = fi.make_problem([4096] * 4, hq=16, dk=128, dv=128, kv_dtype="e4m3", q_dtype="e4m3",
+                                    name="long_e4m3q"), 0
     elif name.startswith("flex_"):
         p, splits = fi.config5(name[5:]), 0
     else:

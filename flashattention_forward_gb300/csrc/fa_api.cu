@@ -313,11 +313,15 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const int64_t B = launch->num_seqs;
   if (B < 0) return fail(FA_ERR_INVALID_ARG, "num_seqs < 0");
   // ---- q
-  if ((st = check_tensor(q, "q", FA_BF16, 3))) return st;
+  if (!q) return fail(FA_ERR_INVALID_ARG, "q is NULL");
+  const int q_dt = q->dtype;
+  if (q_dt != FA_BF16 && q_dt != FA_E4M3) return fail(FA_ERR_INVALID_ARG, "q dtype must be bf16 or e4m3");
+  if ((st = check_tensor(q, "q", q_dt, 3))) return st;
   const int64_t Tq = q->shape[0], Hq = q->shape[1], Dk = q->shape[2];
+  const int qsz = dtype_size(q_dt);
   if (Tq != launch->total_q) return fail(FA_ERR_INVALID_ARG, "q.shape[0]=%lld != launch.total_q=%lld", (long long)Tq, (long long)launch->total_q);
-  if (q->stride[2] != 1 || q->stride[1] % 8 || q->stride[0] % 8)
-    return fail(FA_ERR_INVALID_ARG, "q needs a contiguous last dim and strides that are multiples of 8 elements");
+  if (q->stride[2] != 1 || (q->stride[1] * qsz) % 16 || (q->stride[0] * qsz) % 16)
+    return fail(FA_ERR_INVALID_ARG, "q needs a contiguous last dim and strides that are multiples of 16 bytes");
   // ---- k/v
   const bool paged = block_table != nullptr;
   const int kvnd = paged ? 4 : 3;
@@ -335,6 +339,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if (v_cache->shape[i] != k_cache->shape[i]) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache shapes disagree");
   if (Hkv <= 0 || Hq <= 0 || Hq % Hkv) return fail(FA_ERR_INVALID_ARG, "Hq=%lld must be a positive multiple of Hkv=%lld", (long long)Hq, (long long)Hkv);
   if (!supported_dims(Dk, Dv)) return fail(FA_ERR_UNSUPPORTED, "(Dk, Dv) = (%lld, %lld) is not compiled", (long long)Dk, (long long)Dv);
+  // e4m3 Q: QK on the e4m3 bytes, which needs e4m3 keys; one head-dim pair.
+  const bool q8 = q_dt == FA_E4M3;
+  if (q8 && kv_dt != FA_E4M3) return fail(FA_ERR_UNSUPPORTED, "e4m3 q needs e4m3 k_cache/v_cache");
+  if (q8 && (Dk != 128 || Dv != 128)) return fail(FA_ERR_UNSUPPORTED, "e4m3 q is compiled for Dk = Dv = 128 only");
+  if (q8 && launch->num_splits > 0) return fail(FA_ERR_UNSUPPORTED, "split-KV takes bf16 q; use num_splits = 0 with e4m3 q");
   const int esz = dtype_size(kv_dt);
   for (const fa_tensor_t *t : {k_cache, v_cache}) {
     if (t->stride[kvnd - 1] != 1) return fail(FA_ERR_INVALID_ARG, "k/v caches need a contiguous last dim");
@@ -517,35 +526,41 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   fa::PrefillLaunch L;
   memset(&L, 0, sizeof L);
   {
+    // bf16 Q: boxes of 64 columns (128 bytes); e4m3 Q: 128 columns.
     const uint64_t dq[3] = {(uint64_t)Dk, (uint64_t)Hq, (uint64_t)Tq};
-    const uint64_t sq[2] = {(uint64_t)(q->stride[1] * 2), (uint64_t)(q->stride[0] * 2)};
-    const uint32_t box[3] = {64, 1, (uint32_t)fa::kBlockM};
+    const uint64_t sq[2] = {(uint64_t)(q->stride[1] * qsz), (uint64_t)(q->stride[0] * qsz)};
+    const uint32_t box[3] = {q8 ? 128u : 64u, 1, (uint32_t)fa::kBlockM};
     if (((uintptr_t)q->data) & 15) return fail(FA_ERR_INVALID_ARG, "q must be 16-byte aligned");
-    if ((st = make_map(&L.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dq, sq, box, "q"))) return st;
+    if ((st = make_map(&L.tm_q, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data,
+                       dq, sq, box, "q")))
+      return st;
   }
   const int rows_box = paged ? (page_size < fa::kBlockN ? page_size : fa::kBlockN) : fa::kBlockN;
   // e4m3: 64-byte row pieces (one 64-column block) in boxes of at most 32
   // rows, unswizzled; the converter warps turn each 32-row slice into the
-  // swizzled f16 operand in place.
+  // swizzled f16 operand in place.  With e4m3 Q the keys are the MMA operand
+  // as stored: whole 128-byte rows, 128-byte swizzled, in the same boxes.
   const int rows_box8 = paged ? (page_size < 32 ? page_size : 32) : 32;
+  const uint32_t k8_cols = q8 ? 128u : 64u;
+  const CUtensorMapSwizzle k8_swz = q8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   if (have_keys && fp8) {
     if (paged) {
       const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
       const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2]), (uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
-      const uint32_t bk[4] = {64, 1, (uint32_t)rows_box8, 1};
+      const uint32_t bk[4] = {k8_cols, 1, (uint32_t)rows_box8, 1};
       const uint32_t bv[4] = {64, 1, (uint32_t)rows_box8, 1};
-      if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, bk, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+      if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, bk, "k8", k8_swz))) return st;
       if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dv, sv, bv, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     } else {
       const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)k_cache->shape[0]};
       const uint64_t dv[3] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)v_cache->shape[0]};
       const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
       const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
-      const uint32_t bk[3] = {64, 1, (uint32_t)rows_box8};
+      const uint32_t bk[3] = {k8_cols, 1, (uint32_t)rows_box8};
       const uint32_t bv[3] = {64, 1, (uint32_t)rows_box8};
-      if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, bk, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+      if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, bk, "k8", k8_swz))) return st;
       if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dv, sv, bv, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
     }
   } else if (have_keys) {
@@ -601,6 +616,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   L.paged = paged;
   L.fp8 = fp8;
   L.int8 = kv_dt == FA_I8;
+  L.q8 = q8;
   {
     // Test knob: FA_GB300_PREFILL_VARIANT=1 forces the 10-warp two-pass softmax.
     const char *v = getenv("FA_GB300_PREFILL_VARIANT");

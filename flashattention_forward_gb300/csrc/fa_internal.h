@@ -15,6 +15,7 @@ struct PrefillLaunch {
   PrefillParams p;
   int paged, fp8, mod;
   int int8;      // with fp8: the byte cache holds int8 values (else e4m3)
+  int q8;        // with fp8 (e4m3): Q is e4m3 and QK runs on the bytes
   int variant;   // 0: fastest available, 1: force the 10-warp two-pass softmax
   dim3 grid;
   cudaStream_t stream;
@@ -34,6 +35,7 @@ cudaError_t launch_prefill_192_128_fp8(const PrefillLaunch &L);
 cudaError_t launch_prefill_64_64_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_192_128_i8(const PrefillLaunch &L);
+cudaError_t launch_prefill_128_128_q8(const PrefillLaunch &L);
 cudaError_t launch_decode(int d, const DecodeLaunch &L);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
                            int dv, void *out, float *lse, cudaStream_t stream);

@@ -33,26 +33,39 @@
 // Warps: 0-3 softmax A, 4-7 softmax B, 8 TMA producer, 9 TMEM allocation + MMA
 // issue; e4m3: 10-15 converters (16 warps); bf16: 10-11 idle in the 12-warp
 // variant (warpgroup 2 hands its registers to the softmax warpgroups).
+//
+// Q8 (e4m3 Q with e4m3 K/V, Dk = Dv = 128; FlyDSL PR #1066 description: OCP
+// E4M3 Q/K/V with scalar descales): Q and K are the operands of a
+// kind::f8f6f4 QK as stored -- TMA drops them 128-byte swizzled, no
+// conversion -- so S' = sum_d q8 k8 and the score is S'_ij * k_scale_j (the
+// per-tensor Q scale is part of softmax_scale).  The producer lanes copy the
+// 128 K scales of a tile into a small array beside its ring chunk with
+// cp.async, tracked by the chunk's barrier; the softmax multiplies each S
+// column by its scale before the max.  V is still converted to f16 and PV
+// runs kind::f16 with P in f16.
 #pragma once
 #include "fa_prefill2.cuh"
 
 namespace fa {
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool Q8 = false>
 struct Prefill3Cfg {
-  static constexpr int KC = DK / 64;              // 16 KB chunks per K tile
+  // 16 KB chunks per K tile: 64 bf16/f16 columns, or (Q8) 128 e4m3 columns
+  static constexpr int KC = Q8 ? DK / 128 : DK / 64;
   static constexpr int VC = DV / 64;              // 64-column blocks per V tile
   static constexpr int kChunkBytes = kBlockN * 128;
-  static constexpr int kQTileBytes = kBlockM * DK * 2;
+  static constexpr int kQTileBytes = kBlockM * DK * (Q8 ? 1 : 2);
   static constexpr int kVBytes = VC * kChunkBytes;
+  static constexpr int kKsBytes = Q8 ? kBlockN * 4 : 0;    // per chunk: the K scales of its keys
   static constexpr int kRing = 229376 - 2 * kQTileBytes;   // 224 KB minus the Q tiles
   static constexpr int NSV = (DV <= 64) ? 6 : 2;
-  static constexpr int NCK_raw = (kRing - NSV * kVBytes) / kChunkBytes;
+  static constexpr int NCK_raw = (kRing - NSV * kVBytes) / (kChunkBytes + kKsBytes);
   static constexpr int NCK = NCK_raw > 8 ? 8 : NCK_raw;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + NCK * kChunkBytes;
-  static constexpr int kOffBar = kOffV + NSV * kVBytes;
+  static constexpr int kOffKs = kOffV + NSV * kVBytes;
+  static constexpr int kOffBar = kOffKs + NCK * kKsBytes;
   // q_full, q_conv[2], kc_full/kc_empty/kc_stage[NCK], v_full/v_empty/v_stage[NSV],
   // s_full[2], p_full[2], o_done[2]
   static constexpr int kNumBars = 3 + 3 * NCK + 3 * NSV + 6;
@@ -71,13 +84,53 @@ struct Prefill3Cfg {
   static constexpr bool kOnePass = FP8 ? kOnePassFP8 : BIGREG;
   static constexpr int kPoolNeeded = 8 * 32 * kRegsSoftmax + (kWarps - 8) * 32 * kRegsOther;
   static constexpr int kConverters = 6;
-  static constexpr int kSlicesPerTile = (KC + VC) * 4;   // 32-row slices
+  static constexpr int kKSlices = Q8 ? 0 : KC * 4;      // 32-row K slices to convert per tile
+  static constexpr int kSlicesPerTile = kKSlices + VC * 4;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dims");
   static_assert(NCK >= KC, "the K ring holds at least one tile");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(!kSplitRegs || kPoolNeeded <= 65536, "register split exceeds the register file");
+  static_assert(!Q8 || (FP8 && DK == 128 && DV == 128), "e4m3 Q runs with e4m3 K/V at Dk = Dv = 128");
+  // Q8: the scales of a chunk are read by the softmax after its QK; the chunk
+  // is refilled only after the producer has passed the V stage of a later
+  // tile, whose release follows that softmax.
+  static_assert(!Q8 || NCK >= NSV + 1, "K scales outlive their readers");
 };
+
+// tcgen05 MMA with A and B from shared memory, e4m3 x e4m3 -> fp32 (K = 32 per
+// instruction); descriptor words as in mma_ss_w.
+template <int ACC>
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
+// 4-byte global -> shared copy (cp.async); `bytes` 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
+// One arrival on `bar` once this thread's earlier cp.async copies have landed
+// (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Packed fp32 products a *= b (one rounding each).
+__device__ __forceinline__ void mul2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, r;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "mul.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
 
 // f16 pair (packed) -> two fp32 values.
 __device__ __forceinline__ void unpack_f16x2(uint32_t h, float &lo, float &hi) {
@@ -123,11 +176,13 @@ __device__ __forceinline__ void i8x4_scaled_f16(uint32_t w, float s, uint32_t &o
 }
 
 // I8 (with FP8): the byte cache holds int8 values instead of e4m3.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8>
-__global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::kThreads, 1)
+// Q8 (with FP8, not I8): Q is e4m3 too and QK runs on the e4m3 bytes.
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8 = false>
+__global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>::kThreads, 1)
     fa_prefill3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>;
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
+  static_assert(!(Q8 && I8), "int8 keys have no e4m3 QK");
   constexpr int KC = Cfg::KC, VC = Cfg::VC, NCK = Cfg::NCK, NSV = Cfg::NSV;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,6 +255,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
   uint8_t *sQ = smem + Cfg::kOffQ;
   uint8_t *sK = smem + Cfg::kOffK;
   uint8_t *sV = smem + Cfg::kOffV;
+  float *sKs = reinterpret_cast<float *>(smem + Cfg::kOffKs);   // Q8: [NCK][kBlockN]
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
   uint64_t *q_full = bars;
   uint64_t *q_conv = bars + 1;          // [2] Q tile in f16 (e4m3 caches)
@@ -220,7 +276,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
     mbar_init(smem_u32(q_conv + 0), kBlockM);
     mbar_init(smem_u32(q_conv + 1), kBlockM);
     for (int s = 0; s < NCK; ++s) {
-      mbar_init(smem_u32(kc_full + s), FP8 ? 4 : 1);         // e4m3: one arrive per converted slice
+      // converted K: one arrive per slice; Q8: the TMA arrive + one per producer lane (scales)
+      mbar_init(smem_u32(kc_full + s), Q8 ? 1 + 32 : (FP8 ? 4 : 1));
       mbar_init(smem_u32(kc_empty + s), 1);
       mbar_init(smem_u32(kc_stage + s), 1);
     }
@@ -266,8 +323,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
       for (int X = 0; X < 2; ++X)
 #pragma unroll
         for (int cb = 0; cb < KC; ++cb)
-          tma_load_3d(smem_u32(sQ + X * Cfg::kQTileBytes + cb * kBlockM * 128), &tm_q, smem_u32(q_full), cb * 64,
-                      pi.h, pi.q_row0 + X * kBlockM);
+          tma_load_3d(smem_u32(sQ + X * Cfg::kQTileBytes + cb * kBlockM * 128), &tm_q, smem_u32(q_full),
+                      cb * (Q8 ? 128 : 64), pi.h, pi.q_row0 + X * kBlockM);
     }
     const int rb = p.rows_per_box;
     const int nbox = kBlockN / rb;                    // 1..8 boxes per 64-column block (pages >= 16 keys)
@@ -281,63 +338,98 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         return 0;
       }
     };
-    // One 64-column block of a K or V tile into a 16 KB chunk: bf16 rows land
-    // swizzled (the MMA operand); e4m3 rows land raw, 64 bytes each, in the
-    // upper half of their 32-row slice, for the converters.
-    auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int cb, int kt, int page) {
+    // One 128-byte-row block of a K or V tile into a 16 KB chunk: bf16 rows
+    // (64 columns) and Q8 key rows (128 e4m3 columns) land swizzled, the MMA
+    // operand; staged byte rows (64 columns) land raw in the upper half of
+    // their 32-row slice, for the converters.
+    auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int x, int kt, int page, bool staged) {
       if (!boxer) return;
-      const uint32_t at = FP8 ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64) : smem_u32(dst + r0 * 128);
+      const uint32_t at = staged ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64) : smem_u32(dst + r0 * 128);
       if constexpr (PAGED) {
-        tma_load_4d(at, tm, smem_u32(bar), cb * 64, pi.hk, (kt * kBlockN + r0) & (p.page_size - 1), page);
+        tma_load_4d(at, tm, smem_u32(bar), x, pi.hk, (kt * kBlockN + r0) & (p.page_size - 1), page);
       } else {
-        tma_load_3d(at, tm, smem_u32(bar), cb * 64, pi.hk, pi.k_row0 + kt * kBlockN + r0);
+        tma_load_3d(at, tm, smem_u32(bar), x, pi.hk, pi.k_row0 + kt * kBlockN + r0);
       }
     };
-    constexpr uint32_t kBlockBytes = FP8 ? kBlockN * 64 : kBlockN * 128;
+    constexpr bool kStageK = FP8 && !Q8;
+    constexpr uint32_t kKBlockBytes = kStageK ? kBlockN * 64 : kBlockN * 128;
+    constexpr uint32_t kVBlockBytes = FP8 ? kBlockN * 64 : kBlockN * 128;
+    // Q8: lane l copies the scales of keys 4l .. 4l+3 of a tile (one page:
+    // pages hold >= 16 keys), looked up one tile ahead like the box pages.
+    auto ks_page_at = [&](int kt) -> int {
+      if constexpr (Q8 && PAGED) {
+        const int key0 = kt * kBlockN + 4 * lane;
+        return (kt < pi.kt_hi && key0 < pi.sk) ? __ldg(bt + (key0 >> p.page_shift)) : 0;
+      } else {
+        return 0;
+      }
+    };
+    auto load_scales = [&](int slot, int kt, int kpage) {
+      const uint32_t dst = smem_u32(sKs + slot * kBlockN + 4 * lane);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int key = kt * kBlockN + 4 * lane + u;
+        const bool live = key < pi.sk;
+        int64_t tok;
+        if constexpr (PAGED) tok = (int64_t)kpage * p.page_size + (key & (p.page_size - 1));
+        else tok = (int64_t)pi.k_row0 + key;
+        cp_async_4(dst + 4 * u, live ? p.k_scale + tok * p.hkv + pi.hk : p.k_scale, live ? 4u : 0u);
+      }
+      cp_async_arrive_noinc(smem_u32(kc_full + slot));
+    };
     int j = 0;
     bool ok = true;
     int page = page_at(first_kt);
+    int kpage = ks_page_at(first_kt);
     for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
       const int kn = pair_next(p, pi, kt);
       const int page_next = page_at(kn);
+      const int kpage_next = ks_page_at(kn);
 #pragma unroll 1
       for (int c = 0; c < KC; ++c) {
         const int n = j * KC + c, slot = n % NCK;
-        uint64_t *bar = FP8 ? kc_stage + slot : kc_full + slot;
+        uint64_t *bar = kStageK ? kc_stage + slot : kc_full + slot;
         if (lane == 0) {
           if (n >= NCK) ok = mbar_wait(smem_u32(kc_empty + slot), ((n / NCK) - 1) & 1, abort_flag, p.err);
-          if (ok) mbar_expect_tx(smem_u32(bar), kBlockBytes);
+          if (ok) mbar_expect_tx(smem_u32(bar), kKBlockBytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c, kt, page);
+        load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c * (Q8 ? 128 : 64), kt, page, kStageK);
+        if constexpr (Q8) load_scales(slot, kt, kpage);
       }
       if (!ok) break;
       const int sv = j % NSV;
       uint64_t *vbar = FP8 ? v_stage + sv : v_full + sv;
       if (lane == 0) {
         if (j >= NSV) ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err);
-        if (ok) mbar_expect_tx(smem_u32(vbar), VC * kBlockBytes);
+        if (ok) mbar_expect_tx(smem_u32(vbar), VC * kVBlockBytes);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
 #pragma unroll
       for (int c = 0; c < VC; ++c)
-        load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c, kt, page);
+        load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c * 64, kt, page, FP8);
       kt = kn;
       page = page_next;
+      kpage = kpage_next;
     }
+    // Q8: no scale copy may still be in flight when the CTA ends (error exits).
+    if constexpr (Q8) asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 9) {
     // ------------------------------------------------------- MMA issuer --
+    // Q8: kind::f8f6f4 with A = B = e4m3 (format code 0 in the A and B fields,
+    // as f16 is for kind::f16) and an fp32 accumulator: the same word.
     constexpr uint32_t idesc_qk = FP8 ? idesc_f16_f32(kBlockM, kBlockN, 0, 0) : idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
     constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(kBlockM, DV, 0, 1) : idesc_bf16_f32(kBlockM, DV, 0, 1);
     const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
     int n_pv[2] = {0, 0};
     bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
-    bool q_ready[2] = {!FP8, !FP8};
+    bool q_ready[2] = {!FP8 || Q8, !FP8 || Q8};   // converted Q (e4m3 / int8 caches with bf16 Q)
 
     // Descriptor words, computed once.  K-major 128-byte-swizzled operands
-    // step 32 bytes per K=16 slice inside a 64-column block; a Q tile's blocks
+    // step 32 bytes per K slice (16 two-byte or 32 one-byte columns) inside a
+    // 128-byte block; a Q tile's blocks
     // are 16 KB apart and each K block sits in its own ring chunk.  V
     // (MN-major) has its two 64-column blocks 16 KB apart and steps 16 rows.
     const uint64_t dq0 = smem_desc_sw128(sQa, 16, 1024);
@@ -365,8 +457,13 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         const uint32_t b = k_lo + (uint32_t)(slot * (Cfg::kChunkBytes >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          if (c == 0 && ks == 0) mma_ss_w<0>(d, a, qk_hi, b, qk_hi, idesc_qk);
-          else mma_ss_w<1>(d, a + 2 * ks, qk_hi, b + 2 * ks, qk_hi, idesc_qk);
+          if constexpr (Q8) {
+            if (c == 0 && ks == 0) mma_ss_f8_w<0>(d, a, qk_hi, b, qk_hi, idesc_qk);
+            else mma_ss_f8_w<1>(d, a + 2 * ks, qk_hi, b + 2 * ks, qk_hi, idesc_qk);
+          } else {
+            if (c == 0 && ks == 0) mma_ss_w<0>(d, a, qk_hi, b, qk_hi, idesc_qk);
+            else mma_ss_w<1>(d, a + 2 * ks, qk_hi, b + 2 * ks, qk_hi, idesc_qk);
+          }
         }
         if (last) tc_commit(smem_u32(kc_empty + slot));
       }
@@ -421,8 +518,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
   } else if (warp >= 10) {
     if constexpr (FP8) {
       // ----------------------------------------- e4m3 -> f16 converters --
-      // Slice g (32 rows of one 64-column block; K blocks of a tile first,
-      // then V blocks; g counts slices over the pair's tile list) goes to warp
+      // Slice g (32 rows of one 64-column block; K blocks of a tile first --
+      // none with Q8 -- then V blocks; g counts slices over the pair's tile list) goes to warp
       // g mod 6.  Lane l handles the scale of row l; each step converts 8
       // rows, 16 dims per lane, into the swizzled layout.  Rows past the
       // sequence end are written as zeros.  The scale loads are software
@@ -452,7 +549,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         int64_t tok;
         if constexpr (PAGED) tok = (int64_t)page * p.page_size + (key & (p.page_size - 1));
         else tok = (int64_t)pi.k_row0 + key;
-        const bool isv = (it.g % S) >= KC * 4;
+        const bool isv = (it.g % S) >= Cfg::kKSlices;
         return __ldg((isv ? p.v_scale : p.k_scale) + tok * p.hkv + pi.hk);
       };
       It a{cw, 0, first_kt};
@@ -467,8 +564,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         const float sb = scale_of(b, pb);
         const int pc = page_of(c);
         const int s = a.g % S, j = a.j, kt = a.kt;
-        const bool isv = s >= KC * 4;
-        const int cb = isv ? (s - KC * 4) >> 2 : s >> 2, q = s & 3;
+        const bool isv = s >= Cfg::kKSlices;
+        const int cb = isv ? (s - Cfg::kKSlices) >> 2 : s >> 2, q = s & 3;
         uint8_t *base;
         uint64_t *stage_bar, *full_bar;
         uint32_t par;
@@ -541,7 +638,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
     bool ok = true;
     // Row factor of the f16 Q row (e4m3 caches): S carries 2^e, undone here.
     float rowf = 1.f;
-    if constexpr (FP8) {
+    if constexpr (FP8 && !Q8) {
       ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
       if (ok) {
         // Row r owns 128 bytes of each 64-column block; its 16-byte units are
@@ -612,6 +709,13 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const uint32_t sa = tmem + lane_base + colS;
+      // Q8: the tile's K scales (their cp.async copies completed on the
+      // chunk's barrier, which the QK waited for too).
+      const float *ks_tile = sKs + (j % NCK) * kBlockN;
+      if constexpr (Q8) {
+        ok = mbar_wait(smem_u32(kc_full + j % NCK), (j / NCK) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
       const int j0 = kt * kBlockN;
       bool need_mask = (j0 + kBlockN > pi.sk);
       if (p.causal && j0 + kBlockN - 1 > hx.ip_min) need_mask = true;
@@ -620,6 +724,15 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>::
         if (!p.causal && j0 + kBlockN - 1 > hx.ip_min + p.window - 1) need_mask = true;
       }
       auto scores = [&](float (&v)[32], int jc) {
+        if constexpr (Q8) {
+          const float4 *kp = reinterpret_cast<const float4 *>(ks_tile + (jc - j0));
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 s4 = kp[e >> 2];
+            mul2(v[e], v[e + 1], s4.x, s4.y);
+            mul2(v[e + 2], v[e + 3], s4.z, s4.w);
+          }
+        }
         if (!fast) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {

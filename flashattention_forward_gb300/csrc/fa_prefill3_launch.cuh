@@ -1,5 +1,6 @@
 // Launcher of the chunked-ring ping-pong kernel (fa_prefill3.cuh), shared by
-// the per-head-dim translation units: bf16 K/V with Dk = 192 and e4m3 K/V.
+// the per-head-dim translation units: bf16 K/V with Dk = 192, e4m3 and int8
+// K/V, and e4m3 Q with e4m3 K/V.
 #pragma once
 #include "fa_internal.h"
 #include "fa_prefill3.cuh"
@@ -9,14 +10,14 @@ namespace fa {
 // A register-split variant raises the softmax warps with setmaxnreg.inc,
 // which waits until other warps of the CTA release registers: it may run only
 // when the compiled launch register count covers the whole split.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8>
 bool prefill3_split_fits() {
-  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>;
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
   if constexpr (!Cfg::kSplitRegs) return true;
   static int verdict = -1;   // per process: all devices run the same binary
   if (verdict < 0) {
     cudaFuncAttributes a;
-    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8>) == cudaSuccess &&
+    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8>) == cudaSuccess &&
                a.numRegs * Cfg::kThreads >= Cfg::kPoolNeeded)
                   ? 1
                   : 0;
@@ -24,12 +25,12 @@ bool prefill3_split_fits() {
   return verdict == 1;
 }
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8>
 cudaError_t launch_prefill3_one(const PrefillLaunch &L) {
-  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG>;
-  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8>()) return cudaErrorNotSupported;
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
+  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8>()) return cudaErrorNotSupported;
   static unsigned long long done = 0;
-  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8>;
+  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
@@ -38,26 +39,27 @@ cudaError_t launch_prefill3_one(const PrefillLaunch &L) {
 
 // bf16: the 12-warp split variant when it fits (and is not overridden), else
 // the 10-warp two-half softmax.  e4m3: the 16-warp split variant only.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool I8>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool I8, bool Q8>
 cudaError_t launch_prefill3_pick(const PrefillLaunch &L) {
   if constexpr (FP8) {
-    return launch_prefill3_one<DK, DV, PAGED, true, MOD, false, I8>(L);
+    return launch_prefill3_one<DK, DV, PAGED, true, MOD, false, I8, Q8>(L);
   } else {
-    if (L.variant != 1 && prefill3_split_fits<DK, DV, PAGED, false, MOD, true, false>())
-      return launch_prefill3_one<DK, DV, PAGED, false, MOD, true, false>(L);
-    return launch_prefill3_one<DK, DV, PAGED, false, MOD, false, false>(L);
+    if (L.variant != 1 && prefill3_split_fits<DK, DV, PAGED, false, MOD, true, false, false>())
+      return launch_prefill3_one<DK, DV, PAGED, false, MOD, true, false, false>(L);
+    return launch_prefill3_one<DK, DV, PAGED, false, MOD, false, false, false>(L);
   }
 }
 
-// FP8: byte caches with per-token scales; I8 selects int8 values over e4m3.
-template <int DK, int DV, bool FP8, bool I8 = false>
+// FP8: byte caches with per-token scales; I8 selects int8 values over e4m3;
+// Q8 (e4m3 caches) takes e4m3 Q and runs QK on the bytes.
+template <int DK, int DV, bool FP8, bool I8 = false, bool Q8 = false>
 cudaError_t launch_prefill3(const PrefillLaunch &L) {
   auto by_mod = [&](auto paged_tag) -> cudaError_t {
     constexpr bool PG = decltype(paged_tag)::value;
     switch (L.mod) {
-      case 0: return launch_prefill3_pick<DK, DV, PG, FP8, 0, I8>(L);
-      case 1: return launch_prefill3_pick<DK, DV, PG, FP8, 1, I8>(L);
-      default: return launch_prefill3_pick<DK, DV, PG, FP8, 2, I8>(L);
+      case 0: return launch_prefill3_pick<DK, DV, PG, FP8, 0, I8, Q8>(L);
+      case 1: return launch_prefill3_pick<DK, DV, PG, FP8, 1, I8, Q8>(L);
+      default: return launch_prefill3_pick<DK, DV, PG, FP8, 2, I8, Q8>(L);
     }
   };
   return L.paged ? by_mod(std::true_type{}) : by_mod(std::false_type{});

@@ -49,7 +49,10 @@ cudaError_t by_mod(const PrefillLaunch &L) {
 }  // namespace
 
 cudaError_t launch_prefill_128_128(const PrefillLaunch &L) {
-  if (L.fp8) return L.int8 ? launch_prefill_128_128_i8(L) : launch_prefill3<128, 128, true>(L);   // byte K/V
+  if (L.fp8) {   // byte K/V
+    if (L.q8) return launch_prefill_128_128_q8(L);
+    return L.int8 ? launch_prefill_128_128_i8(L) : launch_prefill3<128, 128, true>(L);
+  }
   return L.paged ? by_mod<true>(L) : by_mod<false>(L);
 }
 }  // namespace fa

@@ -107,10 +107,14 @@ typedef struct {
 /*
  * fa_fwd_varlen -- the attention forward pass.
  *
- *  q            bf16 [T_q, Hq, Dk], last dim contiguous, row stride a multiple
- *               of 8 elements.
+ *  q            bf16 [T_q, Hq, Dk], or e4m3 [T_q, Hq, 128] with e4m3 caches
+ *               and Dv = 128 (FlyDSL PR #1066 description: E4M3 Q/K/V with
+ *               scalar descales; the caller folds the Q descale into
+ *               softmax_scale, and QK runs on the e4m3 bytes with the per-key
+ *               scale applied to each score).  Last dim contiguous, the other
+ *               strides multiples of 16 bytes.  Split-KV takes bf16 q only.
  *  k_cache      paged: [N_pg, P_s, Hkv, Dk]; packed (block_table NULL):
- *               [T_k, Hkv, Dk].  bf16 or e4m3.  Last three dims contiguous.
+ *               [T_k, Hkv, Dk].  bf16, e4m3 or int8.  Last three dims contiguous.
  *  v_cache      same layout and dtype with Dv (Dv may differ from Dk).
  *  block_table  int32 [num_seqs, max_pages], or NULL for packed K/V.  Entries
  *               for pages past a sequence's length are never read.

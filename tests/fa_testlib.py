@@ -17,7 +17,10 @@ LSE_TOL = 1e-3
 
 def to_device(p, dev="cuda"):
     t = {}
-    t["q"] = torch.from_numpy(p.q.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    if p.q_dtype == "e4m3":
+        t["q"] = torch.from_numpy(p.q.copy()).view(torch.float8_e4m3fn).to(dev)
+    else:
+        t["q"] = torch.from_numpy(p.q.view(np.int16).copy()).view(torch.bfloat16).to(dev)
     if p.kv_dtype == "bf16":
         t["k"] = torch.from_numpy(p.k.view(np.int16).copy()).view(torch.bfloat16).to(dev)
         t["v"] = torch.from_numpy(p.v.view(np.int16).copy()).view(torch.bfloat16).to(dev)

@@ -143,6 +143,32 @@ def test_byte_caches_need_scales(L, dt):
     assert st == fa.FA_ERR_INVALID_ARG and "int8" in msg
 
 
+def test_e4m3_q_limits(L):
+    """e4m3 Q runs only with e4m3 K/V at Dk = Dv = 128 and without split-KV."""
+    T, H = 256, 4
+    q8 = _t(FAKE, fa.FA_E4M3, [T, H, 128])
+    k8 = _t(FAKE * 2, fa.FA_E4M3, [T, H, 128])
+    v8 = _t(FAKE * 3, fa.FA_E4M3, [T, H, 128])
+    ks = _t(FAKE * 8, fa.FA_F32, [T, H])
+    vs = _t(FAKE * 9, fa.FA_F32, [T, H])
+    out = _t(FAKE * 6, fa.FA_BF16, [T, H, 128])
+    st, msg = _call(L, q=q8, k=_t(FAKE * 2, fa.FA_BF16, [T, H, 128]), v=_t(FAKE * 3, fa.FA_BF16, [T, H, 128]),
+                    out=out)
+    assert st == fa.FA_ERR_UNSUPPORTED and "e4m3 k_cache" in msg
+    st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 64]), k=_t(FAKE * 2, fa.FA_E4M3, [T, H, 64]),
+                    v=_t(FAKE * 3, fa.FA_E4M3, [T, H, 64]), ks=ks, vs=vs)
+    assert st == fa.FA_ERR_UNSUPPORTED and "Dk = Dv = 128" in msg
+    st, msg = _call(L, q=q8, k=k8, v=v8, ks=ks, vs=vs, out=out,
+                    launch=fa.Launch(num_seqs=2, max_seqlen_q=1, max_seqlen_k=128, num_splits=4,
+                                     total_q=T, total_k=T))
+    assert st == fa.FA_ERR_UNSUPPORTED and "split-KV" in msg
+    # a row stride of 8 one-byte elements is not a multiple of 16 bytes
+    st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 128], [H * 136, 136, 1]), k=k8, v=v8, ks=ks, vs=vs, out=out)
+    assert st == fa.FA_ERR_INVALID_ARG and "16 bytes" in msg
+    st, msg = _call(L, q=_t(FAKE, fa.FA_U8, [T, H, 128]), k=k8, v=v8, ks=ks, vs=vs, out=out)
+    assert st == fa.FA_ERR_INVALID_ARG and "q dtype" in msg
+
+
 def test_overflow_guard(L):
     big = (1 << 31)
     st, msg = _call(L, q=_t(FAKE, fa.FA_BF16, [big, 4, 64]), out=_t(FAKE * 6, fa.FA_BF16, [big, 4, 64]),
