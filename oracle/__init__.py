@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the attention forward pass -- TEST INFRASTRUCTURE ONLY.
+"""fp64 CPU oracle for the attention forward and backward passes -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never imports, links or
@@ -74,6 +74,9 @@ def lib():
                                             ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                                             ctypes.c_void_p]
             L.fa_oracle_combine.restype = None
+            L.fa_oracle_bwd.argtypes = [ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            L.fa_oracle_bwd.restype = ctypes.c_int
             L.fa_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             L.fa_oracle_e4m3_decode.restype = ctypes.c_double
             L.fa_oracle_i8_decode.argtypes = [ctypes.c_uint8]
@@ -100,20 +103,8 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data
 
 
-def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = None,
-            kv_range: Optional[tuple] = None, k_f64: Optional[np.ndarray] = None,
-            v_f64: Optional[np.ndarray] = None):
-    """Run the oracle on a ``fa_inputs.Problem``.
-
-    units   : None for all rows, else int64 array [n, 2] of (query token, head).
-    kv_range: optional (lo, hi) restriction of sequence-local key indices.
-    k_f64/v_f64 : optional double K/V with the problem's layout, replacing the
-                  stored bf16/e4m3 values (no scales applied).
-    Returns (out, lse): out float64 [T_q, Hq, Dv] and lse float64 [Hq, T_q] for
-    all rows, or out [n, Dv] and lse [n] for a unit list.
-    """
-    keep = []
-
+def _problem(p, keep, kv_range=None, q_f64=None, k_f64=None, v_f64=None):
+    """The C problem descriptor for a ``fa_inputs.Problem`` (arrays kept alive in ``keep``)."""
     def c(a, dt):
         if a is None:
             return None
@@ -122,7 +113,10 @@ def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = Non
         return a
 
     q_e4m3 = getattr(p, "q_dtype", "bf16") == "e4m3"
-    q = c(p.q, np.uint8 if q_e4m3 else np.uint16)
+    if q_f64 is not None:
+        q, qd = c(q_f64, np.float64), 2
+    else:
+        q, qd = c(p.q, np.uint8 if q_e4m3 else np.uint16), (1 if q_e4m3 else 0)
     if k_f64 is not None:
         kd, k, v, ks, vs = KV_F64, c(k_f64, np.float64), c(v_f64, np.float64), None, None
     elif p.kv_dtype == "bf16":
@@ -146,7 +140,24 @@ def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = Non
         n_qblk=(bm.shape[1] if bm is not None else 0), n_kblk=(bm.shape[2] if bm is not None else 0),
         blk_q=128, blk_k=128,
         kv_lo=(kv_range[0] if kv_range else 0), kv_hi=(kv_range[1] if kv_range else -1),
-        q_dtype=1 if q_e4m3 else 0)
+        q_dtype=qd)
+    return prob, c
+
+
+def forward(p, units: Optional[np.ndarray] = None, nthreads: Optional[int] = None,
+            kv_range: Optional[tuple] = None, k_f64: Optional[np.ndarray] = None,
+            v_f64: Optional[np.ndarray] = None, q_f64: Optional[np.ndarray] = None):
+    """Run the oracle on a ``fa_inputs.Problem``.
+
+    units   : None for all rows, else int64 array [n, 2] of (query token, head).
+    kv_range: optional (lo, hi) restriction of sequence-local key indices.
+    q_f64, k_f64/v_f64 : optional double Q, K/V with the problem's layout,
+                  replacing the stored values (no scales applied).
+    Returns (out, lse): out float64 [T_q, Hq, Dv] and lse float64 [Hq, T_q] for
+    all rows, or out [n, Dv] and lse [n] for a unit list.
+    """
+    keep = []
+    prob, c = _problem(p, keep, kv_range, q_f64, k_f64, v_f64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     if units is None:
@@ -177,3 +188,25 @@ def combine(o_part: np.ndarray, lse_part: np.ndarray):
     lib().fa_oracle_combine(o_part.ctypes.data, lse_part.ctypes.data, s, n, dv,
                             out.ctypes.data, lse.ctypes.data)
     return out, lse
+
+
+def backward(p, dout: np.ndarray, nthreads: Optional[int] = None, q_f64: Optional[np.ndarray] = None,
+             k_f64: Optional[np.ndarray] = None, v_f64: Optional[np.ndarray] = None):
+    """Gradients of sum(dout * out) with respect to q, k and v (packed K/V).
+
+    dout: float64 [T_q, Hq, Dv].  Returns (dq [T_q, Hq, Dk], dk [T_k, Hkv, Dk],
+    dv [T_k, Hkv, Dv]) in float64.
+    """
+    keep = []
+    prob, _ = _problem(p, keep, None, q_f64, k_f64, v_f64)
+    d = np.ascontiguousarray(dout, dtype=np.float64).reshape(p.total_q, p.hq, p.dv)
+    dq = np.zeros((max(p.total_q, 1), p.hq, p.dk))
+    dk = np.zeros((max(p.total_k, 1), p.hkv, p.dk))
+    dv = np.zeros((max(p.total_k, 1), p.hkv, p.dv))
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = lib().fa_oracle_bwd(ctypes.byref(prob), d.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                             int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle backward rejected the problem")
+    return dq[:p.total_q], dk[:p.total_k], dv[:p.total_k]

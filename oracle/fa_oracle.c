@@ -1,5 +1,5 @@
 /*
- * fa_oracle.c -- plain fp64 CPU oracle for the attention forward pass.
+ * fa_oracle.c -- plain fp64 CPU oracle for the attention forward and backward passes.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file; only the tests, the smoke check and the benchmark's CPU
@@ -74,10 +74,10 @@ typedef struct {
     const uint8_t *block_mask;    /* [B*Hq][n_qblk][n_kblk] or NULL */
     int32_t n_qblk, n_kblk, blk_q, blk_k;
     int64_t kv_lo, kv_hi;         /* restrict keys to [kv_lo, kv_hi) when kv_hi >= 0 */
-    int32_t q_dtype;              /* Q_BF16 | Q_E4M3 (a per-tensor Q scale is folded into softmax_scale) */
+    int32_t q_dtype;              /* Q_BF16 | Q_E4M3 (a per-tensor Q scale is folded into softmax_scale) | Q_F64 */
 } fa_oracle_problem;
 
-enum { Q_BF16 = 0, Q_E4M3 = 1 };
+enum { Q_BF16 = 0, Q_E4M3 = 1, Q_F64 = 2 };
 
 /* bf16 -> double: the bf16 bits are the upper half of an IEEE binary32. */
 double fa_oracle_bf16_decode(uint16_t b) {
@@ -126,6 +126,16 @@ static void fetch_row(const fa_oracle_problem *p, const void *base, const float 
     }
 }
 
+/* Query row (token t, head h) widened to double. */
+static void fetch_q(const fa_oracle_problem *p, int64_t t, int h, double *qrow) {
+    for (int x = 0; x < p->dk; x++) {
+        const int64_t at = (t * p->hq + h) * (int64_t)p->dk + x;
+        if (p->q_dtype == Q_E4M3) qrow[x] = fa_oracle_e4m3_decode(((const uint8_t *)p->q)[at]);
+        else if (p->q_dtype == Q_F64) qrow[x] = ((const double *)p->q)[at];
+        else qrow[x] = fa_oracle_bf16_decode(((const uint16_t *)p->q)[at]);
+    }
+}
+
 /* Is key j visible from query row i of sequence b, head h? */
 static int allowed(const fa_oracle_problem *p, int b, int h, int64_t i, int64_t j,
                    int64_t sq, int64_t sk) {
@@ -161,11 +171,7 @@ static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, d
     int64_t ip = i + sk - sq;
     int hk = h / (p->hq / p->hkv);
 
-    for (int x = 0; x < p->dk; x++) {
-        const int64_t at = (t * p->hq + h) * (int64_t)p->dk + x;
-        qrow[x] = p->q_dtype == Q_E4M3 ? fa_oracle_e4m3_decode(((const uint8_t *)p->q)[at])
-                                       : fa_oracle_bf16_decode(((const uint16_t *)p->q)[at]);
-    }
+    fetch_q(p, t, h, qrow);
 
     int any = 0;
     double m = -INFINITY;
@@ -287,4 +293,136 @@ void fa_oracle_combine(const double *o_part, const double *lse_part, int n_split
             for (int x = 0; x < dv; x++) out[r * dv + x] += w * o_part[((int64_t)s * n + r) * dv + x];
         }
     }
+}
+
+/*
+ * Backward pass: the gradients of L = sum_{i,x} dO[i][x] * out[i][x] with
+ * respect to q, k and v, by the chain rule through the definition above
+ * (RL-Kernel PR #237, backward commit: recompute the probabilities from the
+ * forward's saved statistics, then dQ, dK, dV).  For one row i with allowed
+ * set A_i and probabilities P_j = exp(s_j - LSE_i):
+ *
+ *   dV_j  += P_j * dO_i                        (out_i = sum_j P_j v_j)
+ *   dP_j   = <dO_i, v_j>
+ *   dS_j   = P_j * (dP_j - sum_{l in A_i} P_l dP_l)    (softmax Jacobian)
+ *   dU_j   = dS_j * d s_j / d u_j              (u_j = scale <q_i, k_j>;
+ *            1 - tanh^2(u_j / cap) under the soft-cap, 1 otherwise; ALiBi
+ *            adds a constant, so its derivative is 1)
+ *   dQ_i  += scale * dU_j * k_j,   dK_j += scale * dU_j * q_i
+ *
+ * Rows with an empty A_i contribute nothing.  GQA: the q heads of a kv head's
+ * group all add into its dK, dV.  Packed K/V only (block_table NULL), K/V
+ * bf16 or f64.  Work is split by (sequence, kv head), so each thread owns the
+ * rows it accumulates.
+ *   dout: [T_q][Hq][Dv] doubles
+ *   dq: [T_q][Hq][Dk], dk: [T_k][Hkv][Dk], dv: [T_k][Hkv][Dv] doubles (overwritten)
+ */
+typedef struct {
+    const fa_oracle_problem *p;
+    const double *dout;
+    double *dq, *dk, *dv;
+    int tid, nthreads;
+    int64_t max_sk;
+} bwd_arg;
+
+static void *bwd_worker(void *argp) {
+    bwd_arg *a = (bwd_arg *)argp;
+    const fa_oracle_problem *p = a->p;
+    const int g = p->hq / p->hkv;
+    int64_t cap_k = a->max_sk > 0 ? a->max_sk : 1;
+    double *qrow = (double *)malloc(sizeof(double) * p->dk);
+    double *krow = (double *)malloc(sizeof(double) * p->dk);
+    double *vrow = (double *)malloc(sizeof(double) * p->dv);
+    double *s = (double *)malloc(sizeof(double) * cap_k);
+    double *u = (double *)malloc(sizeof(double) * cap_k);
+    double *dp = (double *)malloc(sizeof(double) * cap_k);
+    unsigned char *ok = (unsigned char *)malloc(cap_k);
+    for (int64_t unit = a->tid; unit < (int64_t)p->num_seqs * p->hkv; unit += a->nthreads) {
+        const int b = (int)(unit / p->hkv), hk = (int)(unit % p->hkv);
+        const int64_t sq = p->cu_q[b + 1] - p->cu_q[b], sk = p->cu_k[b + 1] - p->cu_k[b];
+        for (int h = hk * g; h < (hk + 1) * g; h++) {
+            for (int64_t i = 0; i < sq; i++) {
+                const int64_t t = p->cu_q[b] + i, ip = i + sk - sq;
+                fetch_q(p, t, h, qrow);
+                const double *dorow = a->dout + (t * p->hq + h) * (int64_t)p->dv;
+                double m = -INFINITY;
+                int any = 0;
+                for (int64_t j = 0; j < sk; j++) {
+                    ok[j] = (unsigned char)allowed(p, b, h, i, j, sq, sk);
+                    if (!ok[j]) continue;
+                    fetch_row(p, p->k, p->k_scale, b, j, hk, p->dk, krow);
+                    double dot = 0.0;
+                    for (int x = 0; x < p->dk; x++) dot += qrow[x] * krow[x];
+                    double sj = p->softmax_scale * dot;
+                    u[j] = sj;
+                    if (p->mod_kind == MOD_SOFTCAP) sj = p->softcap * tanh(sj / p->softcap);
+                    if (p->mod_kind == MOD_ALIBI) sj -= p->alibi_slope * (double)(ip > j ? ip - j : j - ip);
+                    s[j] = sj;
+                    if (sj > m) m = sj;
+                    any = 1;
+                }
+                if (!any) continue;
+                double l = 0.0;
+                for (int64_t j = 0; j < sk; j++)
+                    if (ok[j]) l += exp(s[j] - m);
+                const double lse = m + log(l);
+                double dsum = 0.0;
+                for (int64_t j = 0; j < sk; j++) {
+                    if (!ok[j]) continue;
+                    fetch_row(p, p->v, p->v_scale, b, j, hk, p->dv, vrow);
+                    double d = 0.0;
+                    for (int x = 0; x < p->dv; x++) d += dorow[x] * vrow[x];
+                    dp[j] = d;
+                    const double pj = exp(s[j] - lse);
+                    dsum += pj * d;
+                    double *dvrow = a->dv + ((p->cu_k[b] + j) * p->hkv + hk) * (int64_t)p->dv;
+                    for (int x = 0; x < p->dv; x++) dvrow[x] += pj * dorow[x];
+                }
+                double *dqrow = a->dq + (t * p->hq + h) * (int64_t)p->dk;
+                for (int64_t j = 0; j < sk; j++) {
+                    if (!ok[j]) continue;
+                    const double pj = exp(s[j] - lse);
+                    double du = pj * (dp[j] - dsum);
+                    if (p->mod_kind == MOD_SOFTCAP) {
+                        const double th = tanh(u[j] / p->softcap);
+                        du *= 1.0 - th * th;
+                    }
+                    fetch_row(p, p->k, p->k_scale, b, j, hk, p->dk, krow);
+                    double *dkrow = a->dk + ((p->cu_k[b] + j) * p->hkv + hk) * (int64_t)p->dk;
+                    for (int x = 0; x < p->dk; x++) {
+                        dqrow[x] += p->softmax_scale * du * krow[x];
+                        dkrow[x] += p->softmax_scale * du * qrow[x];
+                    }
+                }
+            }
+        }
+    }
+    free(qrow); free(krow); free(vrow); free(s); free(u); free(dp); free(ok);
+    return NULL;
+}
+
+int fa_oracle_bwd(const fa_oracle_problem *p, const double *dout, double *dq, double *dk, double *dv,
+                  int nthreads) {
+    if (!p || p->hq <= 0 || p->hkv <= 0 || p->hq % p->hkv || p->num_seqs < 0) return -1;
+    if (p->block_table || (p->kv_dtype != KV_BF16 && p->kv_dtype != KV_F64)) return -1;
+    const int64_t tq = p->cu_q[p->num_seqs], tk = p->cu_k[p->num_seqs];
+    memset(dq, 0, sizeof(double) * tq * p->hq * p->dk);
+    memset(dk, 0, sizeof(double) * tk * p->hkv * p->dk);
+    memset(dv, 0, sizeof(double) * tk * p->hkv * p->dv);
+    int64_t max_sk = 0;
+    for (int b = 0; b < p->num_seqs; b++) {
+        int64_t sk = p->cu_k[b + 1] - p->cu_k[b];
+        if (sk > max_sk) max_sk = sk;
+    }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    pthread_t th[1024];
+    bwd_arg args[1024];
+    for (int i = 0; i < nthreads; i++) {
+        args[i] = (bwd_arg){p, dout, dq, dk, dv, i, nthreads, max_sk};
+        if (nthreads > 1) pthread_create(&th[i], NULL, bwd_worker, &args[i]);
+    }
+    if (nthreads == 1) bwd_worker(&args[0]);
+    else for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
+    return 0;
 }
