@@ -179,6 +179,27 @@ def make_call(p, t, num_splits=0):
     return call, launches, out, lse
 
 
+def make_bwd_call(p, t):
+    """A backward call (fa_bwd_varlen) on preallocated buffers: out and LSE from
+    one forward call, a seeded N(0,1) dout."""
+    import flashattention_forward_gb300 as fa
+    dev = t["q"].device
+    out, lse = fa.fwd_varlen(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
+                             max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, softmax_scale=p.softmax_scale,
+                             causal=p.causal, window=p.window, num_splits=0)
+    g = torch.Generator(device="cpu").manual_seed(17)
+    dout = torch.randn(out.shape, generator=g).to(torch.bfloat16).to(dev)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    ws = torch.empty(max(fa.bwd_workspace_bytes(p.total_q, p.hq), 256), dtype=torch.uint8, device=dev)
+
+    def call():
+        return fa.bwd_varlen(t["q"], t["k"], t["v"], out, dout, lse, t["cu_q"], t["cu_k"],
+                             max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
+                             softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
+                             dq=dq, dk=dk, dv=dv, workspace=ws)
+    return call
+
+
 class Flusher:
     def __init__(self, dev):
         self.buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -509,6 +530,19 @@ def other_workloads(dev, warmup, steps, flush, pk):
             "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
             "gflop": fl / 1e9}
         del t
+    # backward (fa_bwd_varlen: Delta, dK/dV, dQ kernels): config-2 lengths and
+    # 4 x 4096; algorithmic flops = 2.5 x the forward's (S, dP, dV, dK, dQ)
+    for name, p in (("bwd_varlen_8seq_h16_d128_causal", fi.config2(causal=True)),
+                    ("bwd_varlen_8seq_h16_d128_noncausal", fi.config2(causal=False)),
+                    ("bwd_4x4096_h16_d128_causal", fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, causal=True)),
+                    ("bwd_4x4096_h16_d128_noncausal", fi.make_problem([4096] * 4, hq=16, dk=128, seed=3))):
+        t = dev_tensors(p, dev)
+        call = make_bwd_call(p, t)
+        ms = statistics.mean(time_calls([call], warmup, steps, flush))
+        fl = 2.5 * fi.prefill_flops(p)
+        res[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+                     "gflop": fl / 1e9}
+        del t
     # flex runs at B=4, H=16, S=8192
     for run in fi.CONFIG5_RUNS:
         p = fi.config5(run)
@@ -556,10 +590,17 @@ def profile_only(name, warmup, steps):
                                     name="long_e4m3q"), 0
     elif name.startswith("flex_"):
         p, splits = fi.config5(name[5:]), 0
+    elif name in ("bwd_varlen_noncausal", "bwd_long_causal"):
+        p = fi.config2(causal=False) if name == "bwd_varlen_noncausal" else \
+            fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, causal=True)
+        splits = "bwd"
     else:
         raise SystemExit(f"unknown workload {name}")
     t = dev_tensors(p, dev)
-    call, _, _, _ = make_call(p, t, num_splits=splits)
+    if splits == "bwd":
+        call = make_bwd_call(p, t)
+    else:
+        call, _, _, _ = make_call(p, t, num_splits=splits)
     for _ in range(warmup + steps):
         call()
     torch.cuda.synchronize()

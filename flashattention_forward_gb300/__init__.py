@@ -26,7 +26,8 @@ MOD_NONE, MOD_ALIBI, MOD_SOFTCAP = 0, 1, 2
 
 EXPORTED = ("fa_fwd_varlen", "fa_fwd_workspace_bytes", "fa_fwd_default_splits", "fa_combine",
             "fa_last_error", "fa_get_device_error", "fa_version", "fa_fwd_varlen_noalloc",
-            "fa_fwd_plan_create", "fa_fwd_plan_launch", "fa_fwd_plan_destroy")
+            "fa_fwd_plan_create", "fa_fwd_plan_launch", "fa_fwd_plan_destroy", "fa_bwd_varlen",
+            "fa_bwd_workspace_bytes")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -100,6 +101,11 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_plan_launch.restype = ctypes.c_int
             L.fa_fwd_plan_destroy.argtypes = [ctypes.c_void_p]
             L.fa_fwd_plan_destroy.restype = None
+            L.fa_bwd_varlen.argtypes = [P(Tensor)] * 11 + [ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
+                                                          P(Launch), ctypes.c_void_p]
+            L.fa_bwd_varlen.restype = ctypes.c_int
+            L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
+            L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
             _lib = L
     return _lib
 
@@ -346,3 +352,38 @@ def device_error(stream=None) -> int:
 
 def version() -> str:
     return lib().fa_version().decode()
+
+
+def bwd_workspace_bytes(total_q: int, hq: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(int(total_q), int(hq)))
+
+
+def bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, dout: torch.Tensor,
+               lse: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, *,
+               max_seqlen_q: int, max_seqlen_k: int, softmax_scale: Optional[float] = None,
+               causal: bool = False, window: int = 0, dq: Optional[torch.Tensor] = None,
+               dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward pass through ``fa_bwd_varlen``: returns (dq, dk, dv), bf16 with
+    the shapes of q, k, v.  ``lse`` is the forward's fp32 [Hq, T_q] LSE for the
+    same inputs and masks; K/V packed [T_k, Hkv, D]; D = 64 or 128."""
+    L = lib()
+    B = cu_seqlens_q.shape[0] - 1
+    Tq, Hq, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(Tq, Hq)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, num_splits=0,
+                    total_q=Tq, total_k=k.shape[0])
+    if need:
+        launch.workspace = workspace.data_ptr()
+        launch.workspace_bytes = workspace.numel()
+    args = [as_tensor(x) for x in (q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, dq, dk, dv)]
+    _check(L.fa_bwd_varlen(*[_ref(a) for a in args], ctypes.c_float(softmax_scale), int(bool(causal)),
+                           int(window), ctypes.byref(launch), ctypes.c_void_p(_stream_ptr(stream))))
+    return dq, dk, dv

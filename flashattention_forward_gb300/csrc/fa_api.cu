@@ -646,3 +646,140 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
 }
 
 }  // namespace
+
+// ------------------------------------------------------------- backward --
+namespace {
+
+// A bf16 [rows, heads, D] operand with a contiguous last dim and 16-byte
+// aligned rows, as the TMA maps and the 16-byte stores need.
+fa_status_t check_rows(const fa_tensor_t *t, const char *name, int64_t rows, int64_t heads, int64_t d) {
+  fa_status_t st = check_tensor(t, name, FA_BF16, 3);
+  if (st) return st;
+  if (t->shape[0] != rows || t->shape[1] != heads || t->shape[2] != d)
+    return fail(FA_ERR_INVALID_ARG, "%s has shape [%lld, %lld, %lld], expected [%lld, %lld, %lld]", name,
+                (long long)t->shape[0], (long long)t->shape[1], (long long)t->shape[2], (long long)rows,
+                (long long)heads, (long long)d);
+  if (t->stride[2] != 1) return fail(FA_ERR_INVALID_ARG, "%s: last dim must be contiguous", name);
+  if ((t->stride[0] % 8) || (t->stride[1] % 8) || (((uintptr_t)t->data) & 15))
+    return fail(FA_ERR_INVALID_ARG, "%s: strides must be multiples of 8 elements and the base 16-byte aligned", name);
+  if (!t->data && rows > 0) return fail(FA_ERR_INVALID_ARG, "%s data is NULL", name);
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq) {
+  if (total_q <= 0 || hq <= 0) return 0;
+  return align256((size_t)total_q * hq * sizeof(float));
+}
+
+fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_tensor_t *v, const fa_tensor_t *out,
+                          const fa_tensor_t *dout, const fa_tensor_t *lse, const fa_tensor_t *cu_seqlens_q,
+                          const fa_tensor_t *cu_seqlens_k, fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv,
+                          float softmax_scale, int32_t causal, int32_t window, const fa_launch_t *launch,
+                          void *stream) {
+  g_msg[0] = 0;
+  fa_status_t st;
+  if (!launch) return fail(FA_ERR_INVALID_ARG, "launch is NULL");
+  if (!q || !k || !v) return fail(FA_ERR_INVALID_ARG, "q, k and v are required");
+  if ((st = check_tensor(q, "q", FA_BF16, 3))) return st;
+  const int64_t B = launch->num_seqs, Tq = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  if (k->ndim != 3) return fail(FA_ERR_INVALID_ARG, "k must be packed [T_k, Hkv, D] (no paged backward)");
+  const int64_t Tk = k->shape[0], Hkv = k->shape[1];
+  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "backward supports Dk = Dv in {64, 128}, got %lld", (long long)D);
+  if (Hkv <= 0 || Hq % Hkv) return fail(FA_ERR_INVALID_ARG, "Hq (%lld) must be a multiple of Hkv (%lld)", (long long)Hq, (long long)Hkv);
+  if ((st = check_rows(q, "q", Tq, Hq, D)) || (st = check_rows(k, "k", Tk, Hkv, D)) ||
+      (st = check_rows(v, "v", Tk, Hkv, D)) || (st = check_rows(out, "out", Tq, Hq, D)) ||
+      (st = check_rows(dout, "dout", Tq, Hq, D)) || (st = check_rows(dq, "dq", Tq, Hq, D)) ||
+      (st = check_rows(dk, "dk", Tk, Hkv, D)) || (st = check_rows(dv, "dv", Tk, Hkv, D)))
+    return st;
+  if ((st = check_tensor(lse, "lse", FA_F32, 2))) return st;
+  if (lse->shape[0] != Hq || lse->shape[1] != Tq || !contiguous(lse))
+    return fail(FA_ERR_INVALID_ARG, "lse must be contiguous fp32 [Hq, T_q] (the forward's LSE)");
+  if ((st = check_tensor(cu_seqlens_q, "cu_seqlens_q", FA_I32, 1)) || (st = check_tensor(cu_seqlens_k, "cu_seqlens_k", FA_I32, 1)))
+    return st;
+  if (cu_seqlens_q->shape[0] != B + 1 || cu_seqlens_k->shape[0] != B + 1)
+    return fail(FA_ERR_INVALID_ARG, "cu_seqlens must have num_seqs + 1 entries");
+  if (launch->total_q != Tq) return fail(FA_ERR_INVALID_ARG, "launch->total_q != q.shape[0]");
+  if (Tq >= (int64_t(1) << 31) || Tk >= (int64_t(1) << 31)) return fail(FA_ERR_OVERFLOW, "token counts must fit int32");
+  const fa_tensor_t *outs[3] = {dq, dk, dv};
+  const fa_tensor_t *ins[8] = {q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k};
+  for (const fa_tensor_t *o : outs)
+    for (const fa_tensor_t *i : ins)
+      if (overlaps(o, i)) return fail(FA_ERR_INVALID_ARG, "gradient buffers must not overlap the inputs");
+  if (overlaps(dq, dk) || overlaps(dq, dv) || overlaps(dk, dv)) return fail(FA_ERR_INVALID_ARG, "dq, dk, dv overlap");
+  if (window < 0) window = 0;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return fail(FA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+  if (B == 0 || Tq == 0) return FA_OK;
+  if (launch->max_seqlen_q <= 0 || launch->max_seqlen_k < 0) return fail(FA_ERR_INVALID_ARG, "bad max_seqlen");
+  if (B > 65535 || Hq > 65535) return fail(FA_ERR_UNSUPPORTED, "num_seqs and Hq must be at most 65535");
+  const size_t need = fa_bwd_workspace_bytes(Tq, (int)Hq);
+  if (!launch->workspace || launch->workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "the backward needs a workspace of %zu bytes (fa_bwd_workspace_bytes)", need);
+  if ((uintptr_t)launch->workspace & 255) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+
+  fa::BwdLaunch L;
+  memset(&L, 0, sizeof L);
+  {
+    const uint32_t box[3] = {64, 1, 128};
+    const fa_tensor_t *ts[4] = {q, k, v, dout};
+    CUtensorMap *ms[4] = {&L.tm_q, &L.tm_k, &L.tm_v, &L.tm_do};
+    const char *names[4] = {"q", "k", "v", "dout"};
+    for (int x = 0; x < 4; ++x) {
+      const fa_tensor_t *t = ts[x];
+      const uint64_t dims[3] = {(uint64_t)D, (uint64_t)t->shape[1], (uint64_t)t->shape[0]};
+      const uint64_t strides[2] = {(uint64_t)(t->stride[1] * 2), (uint64_t)(t->stride[0] * 2)};
+      if (t->shape[0] == 0) continue;
+      if ((st = make_map(ms[x], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, names[x]))) return st;
+    }
+  }
+  float *delta = (float *)launch->workspace;
+  fa::BwdParams &p = L.p;
+  p.cu_q = (const int32_t *)cu_seqlens_q->data;
+  p.cu_k = (const int32_t *)cu_seqlens_k->data;
+  p.lse = (const float *)lse->data;
+  p.delta = delta;
+  p.dq = (__nv_bfloat16 *)dq->data;
+  p.dq_stride_t = dq->stride[0];
+  p.dq_stride_h = dq->stride[1];
+  p.dk = (__nv_bfloat16 *)dk->data;
+  p.dk_stride_t = dk->stride[0];
+  p.dk_stride_h = dk->stride[1];
+  p.dv = (__nv_bfloat16 *)dv->data;
+  p.dv_stride_t = dv->stride[0];
+  p.dv_stride_h = dv->stride[1];
+  p.total_q = Tq;
+  p.num_seqs = (int)B;
+  p.hq = (int)Hq;
+  p.hkv = (int)Hkv;
+  p.group = (int)(Hq / Hkv);
+  p.n_qtiles = (launch->max_seqlen_q + 127) / 128;
+  p.n_ktiles = (launch->max_seqlen_k + 127) / 128;
+  p.causal = causal != 0;
+  p.window = window;
+  p.scale = softmax_scale;
+  p.scale_log2 = softmax_scale * fa::kLog2e;
+  p.err = error_word();
+  fa::BwdDeltaParams &dp = L.dp;
+  dp.out = (const __nv_bfloat16 *)out->data;
+  dp.dout = (const __nv_bfloat16 *)dout->data;
+  dp.o_stride_t = out->stride[0];
+  dp.o_stride_h = out->stride[1];
+  dp.do_stride_t = dout->stride[0];
+  dp.do_stride_h = dout->stride[1];
+  dp.delta = delta;
+  dp.total_q = Tq;
+  dp.hq = (int)Hq;
+  dp.d = (int)D;
+  L.delta_blocks = (unsigned)((Tq * Hq + 7) / 8);
+  L.grid_q = dim3((unsigned)p.n_qtiles, (unsigned)Hq, (unsigned)B);
+  L.grid_kv = dim3((unsigned)(p.n_ktiles > 0 ? p.n_ktiles : 1), (unsigned)Hkv, (unsigned)B);
+  L.stream = (cudaStream_t)stream;
+  cudaError_t e = fa::launch_bwd((int)D, L);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return FA_OK;
+}
+
+}  // extern "C"

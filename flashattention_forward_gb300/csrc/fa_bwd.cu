@@ -1,0 +1,30 @@
+// Backward-pass kernel instantiations (Dk = Dv in {64, 128}) and launchers.
+#include "fa_bwd.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+template <int D>
+cudaError_t launch_d(const BwdLaunch &L) {
+  using Cfg = BwdCfg<D>;
+  // tiles, statistics ring, barriers, TMEM slot and the 1024-byte alignment slack
+  constexpr int kSmem = 6 * Cfg::kTileBytes + Cfg::NS * 256 * 4 + 256 + 1024;
+  static unsigned long long done_dq = 0, done_kv = 0;
+  cudaError_t e = ensure_smem_attr(fa_bwd_dq_kernel<D>, kSmem, &done_dq);
+  if (e == cudaSuccess) e = ensure_smem_attr(fa_bwd_dkdv_kernel<D>, kSmem, &done_kv);
+  if (e != cudaSuccess) return e;
+  fa_bwd_delta_kernel<<<L.delta_blocks, 256, 0, L.stream>>>(L.dp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fa_bwd_dkdv_kernel<D><<<L.grid_kv, Cfg::kThreads, kSmem, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fa_bwd_dq_kernel<D><<<L.grid_q, Cfg::kThreads, kSmem, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_bwd(int d, const BwdLaunch &L) {
+  return d == 64 ? launch_d<64>(L) : launch_d<128>(L);
+}
+}  // namespace fa

@@ -1,0 +1,615 @@
+// fa_bwd.cuh -- FlashAttention backward on tcgen05: gradients of
+// L = sum(dO * out) with respect to Q, K and V from the forward's saved
+// per-row log-sum-exp (RL-Kernel PR #237, backward commit: a Delta
+// preprocess, then dQ/dK/dV recomputed from the saved LSE).
+//
+//   Delta_i = sum_x dO_ix * O_ix                       (fa_bwd_delta_kernel)
+//   P_ij    = exp(scale * <q_i, k_j> - LSE_i)          (allowed (i, j) only)
+//   dP_ij   = <dO_i, v_j>,   dS_ij = P_ij * (dP_ij - Delta_i)
+//   dV_j    = sum_i P_ij dO_i,   dK_j = scale * sum_i dS_ij q_i
+//   dQ_i    = scale * sum_j dS_ij k_j
+//
+// Two kernels share the arithmetic and split the outputs so that no output
+// needs an atomic: fa_bwd_dq_kernel (one 128-row query tile per CTA, looping
+// over key tiles) and fa_bwd_dkdv_kernel (one 128-key tile per CTA, looping
+// over the q heads of its kv head's group and their query tiles).  Each
+// recomputes S and dP; the results are deterministic.
+//
+// Operands are the 128-byte-swizzled 64-column TMA tiles of the forward
+// kernels.  A [rows, D] tile serves as a K-major operand (for S = Q K^T and
+// dP = dO V^T, contraction over D) and as an MN-major B operand (for
+// dQ += dS K, dV += P^T dO and dK += dS^T Q, contraction over the rows).
+// P, dS and their transposes go from registers to TMEM as bf16 and are the
+// A operand of the accumulating MMAs (A from TMEM).
+#pragma once
+#include "fa_prefill.cuh"
+#include "fa_bwd_params.h"
+
+namespace fa {
+
+// Delta_i = <dO_i, O_i> in fp32, one warp per (token, head) row.
+__global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const BwdDeltaParams p) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.total_q * p.hq) return;
+  const int64_t t = row / p.hq;
+  const int h = (int)(row - t * p.hq);
+  const __nv_bfloat16 *o = p.out + t * p.o_stride_t + (int64_t)h * p.o_stride_h;
+  const __nv_bfloat16 *g = p.dout + t * p.do_stride_t + (int64_t)h * p.do_stride_h;
+  float acc = 0.f;
+  for (int x = lane * 4; x < p.d; x += 128) {
+    const uint2 ov = *reinterpret_cast<const uint2 *>(o + x);
+    const uint2 gv = *reinterpret_cast<const uint2 *>(g + x);
+    const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
+    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float2 a = __bfloat1622float2(o2[e]), b = __bfloat1622float2(g2[e]);
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) p.delta[(int64_t)h * p.total_q + t] = acc;
+}
+
+// Is key j visible from query row i (sequence-local; bottom-right causal)?
+__device__ __forceinline__ bool bwd_allowed(const BwdParams &p, int i, int j, int sq, int sk) {
+  if (i >= sq || j >= sk || i < 0 || j < 0) return false;
+  const int ip = i + sk - sq;
+  if (p.causal && j > ip) return false;
+  if (p.window > 0) {
+    if (p.causal) return ip - j < p.window;
+    return abs(ip - j) < p.window;
+  }
+  return true;
+}
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTile = 128;
+  static constexpr int kTileBytes = kTile * D * 2;   // one [128, D] bf16 tile
+  static constexpr int NS = 2;                       // ring stages
+  static constexpr int kThreads = 6 * 32;            // 4 softmax warps, producer, MMA
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// The K-major descriptor walk of a [128, D] tile: 32 bytes per K=16 slice,
+// then the next 64-column block every fourth slice.
+__device__ __forceinline__ uint32_t kmajor_step(int ks) {
+  return ((ks + 1) & 3) ? 2u : (uint32_t)((128 * 128 - 96) >> 4);
+}
+
+// D[tmem] (+)= A[smem, K-major 128 x D] * B[smem, K-major 128 x D]^T: an
+// M = N = 128 product contracted over the D columns of both tiles.
+template <int D>
+__device__ __forceinline__ void mma_rows_rows(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                              uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    if (ks == 0) mma_ss_w<0>(d_tmem, a_lo, hi, b_lo, hi, idesc);
+    else mma_ss_w<1>(d_tmem, a_lo, hi, b_lo, hi, idesc);
+    const uint32_t st = kmajor_step(ks);
+    a_lo += st;
+    b_lo += st;
+  }
+}
+
+// D[tmem] (+)= A[tmem, 128 x 128 bf16] * B[smem, MN-major 128 x D]: contracted
+// over the 128 rows of the B tile.  acc0 = 0 overwrites D.
+__device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                              uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+  for (int ks = 0; ks < 128 / 16; ++ks) {
+    mma_ts_w(d_tmem, a_tmem + ks * 8, b_lo, b_hi, idesc, ks > 0 ? 1u : acc0);
+    b_lo += (16 * 128) >> 4;
+  }
+}
+
+
+__device__ __forceinline__ void bwd_tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Loads a [128, D] bf16 tile (rows row0.., head `head`) as D/64 boxes of 64
+// columns, 128-byte swizzled, onto barrier `bar`.
+template <int D>
+__device__ __forceinline__ void bwd_load_tile(uint8_t *dst, const CUtensorMap *tm, uint64_t *bar, int head, int row0) {
+#pragma unroll
+  for (int cb = 0; cb < D / 64; ++cb)
+    tma_load_3d(smem_u32(dst + cb * 128 * 128), tm, smem_u32(bar), cb * 64, head, row0);
+}
+
+// ------------------------------------------------------------------- dQ --
+// CTA (query tile, q head, sequence).  TMEM: S [0,128), dP [128,256) with dS
+// (bf16) written over its first 64 columns, dQ [256, 256+D).  Warps 0-3 own
+// the tile's rows (TMEM lanes), warp 4 loads, warp 5 issues the MMAs:
+//   S(0) dP(0) | S(t+1) once S(t) is read | dQ += dS(t) K(t) | dP(t+1)
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  constexpr int NS = Cfg::NS, TB = Cfg::kTileBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qs = __ldg(p.cu_q + b), sq = __ldg(p.cu_q + b + 1) - qs;
+  const int ks = __ldg(p.cu_k + b), sk = __ldg(p.cu_k + b + 1) - ks;
+  const int q0 = qt * 128;
+  if (q0 >= sq) return;
+  const int hk = h / p.group;
+  // key tiles that rows q0.. of this tile may see
+  const int last = min(q0 + 128, sq) - 1;
+  const int ip_min = q0 + sk - sq, ip_max = last + sk - sq;
+  int lo = 0, hi = sk;
+  if (p.causal) hi = min(hi, ip_max + 1);
+  if (p.window > 0) {
+    lo = max(lo, ip_min - p.window + 1);
+    if (!p.causal) hi = min(hi, ip_max + p.window);
+  }
+  const int klo = lo / 128;
+  const int n_tiles = hi > lo ? (hi + 127) / 128 - klo : 0;
+  if (n_tiles == 0) {   // no key visible: dQ = 0
+    for (int idx = threadIdx.x; idx < (last - q0 + 1) * (D / 8); idx += blockDim.x) {
+      const int r = idx / (D / 8), c = idx - r * (D / 8);
+      __nv_bfloat16 *o = p.dq + (int64_t)(qs + q0 + r) * p.dq_stride_t + (int64_t)h * p.dq_stride_h;
+      *reinterpret_cast<uint4 *>(o + c * 8) = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+
+  uint8_t *sQ = smem, *sDO = smem + TB, *sK = smem + 2 * TB, *sV = smem + (2 + NS) * TB;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + 2 * NS) * TB);
+  uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = k_full + NS, *v_full = k_empty + NS,
+           *v_empty = v_full + NS, *s_full = v_empty + NS, *dp_full = s_full + 1, *s_read = dp_full + 1,
+           *ds_full = s_read + 1, *dq_done = ds_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dq_done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(k_full + s), 1);
+      mbar_init(smem_u32(k_empty + s), 1);
+      mbar_init(smem_u32(v_full + s), 1);
+      mbar_init(smem_u32(v_empty + s), 1);
+    }
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(dp_full), 1);
+    mbar_init(smem_u32(s_read), 128);
+    mbar_init(smem_u32(ds_full), 128);
+    mbar_init(smem_u32(dq_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------- producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_expect_tx(smem_u32(q_full), 2 * TB);
+      bwd_load_tile<D>(sQ, &tm_q, q_full, h, qs + q0);
+      bwd_load_tile<D>(sDO, &tm_do, q_full, h, qs + q0);
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % NS, row = ks + (klo + t) * 128;
+        if (t >= NS && !mbar_wait(smem_u32(k_empty + st), ((t / NS) - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(smem_u32(k_full + st), TB);
+        bwd_load_tile<D>(sK + st * TB, &tm_k, k_full + st, hk, row);
+        if (t >= NS && !mbar_wait(smem_u32(v_empty + st), ((t / NS) - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(smem_u32(v_full + st), TB);
+        bwd_load_tile<D>(sV + st * TB, &tm_v, v_full + st, hk, row);
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------- MMAs --
+    if (lane == 0) {
+      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, D, 0, 1);
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint32_t hi_k = (uint32_t)(dq0 >> 32);
+      const uint32_t lo_q = (uint32_t)dq0, lo_do = (uint32_t)smem_desc_sw128(smem_u32(sDO), 16, 1024);
+      const uint32_t lo_k = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint32_t lo_v = (uint32_t)smem_desc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dkmn = smem_desc_sw128(smem_u32(sK), 128 * 128, 1024);
+      const uint32_t lo_kmn = (uint32_t)dkmn, hi_kmn = (uint32_t)(dkmn >> 32);
+      const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+      bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
+      if (ok) ok = mbar_wait(smem_u32(k_full), 0, abort_flag, p.err);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_rows<D>(tS, lo_q, lo_k, hi_k, id_ss);
+        tc_commit(smem_u32(s_full));
+        ok = mbar_wait(smem_u32(v_full), 0, abort_flag, p.err);
+      }
+      if (ok) {
+        tc_fence_after();
+        mma_rows_rows<D>(tP, lo_do, lo_v, hi_k, id_ss);
+        tc_commit(smem_u32(dp_full));
+        tc_commit(smem_u32(v_empty));
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % NS, nt = (t + 1) % NS;
+        const bool more = t + 1 < n_tiles;
+        if (more) {
+          if (!(ok = mbar_wait(smem_u32(s_read), t & 1, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(smem_u32(k_full + nt), ((t + 1) / NS) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          mma_rows_rows<D>(tS, lo_q, lo_k + (uint32_t)(nt * (TB >> 4)), hi_k, id_ss);
+          tc_commit(smem_u32(s_full));
+        }
+        if (!(ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        mma_tmem_rows(tQ, tP, lo_kmn + (uint32_t)(st * (TB >> 4)), hi_kmn, id_dq, t > 0 ? 1u : 0u);
+        tc_commit(smem_u32(k_empty + st));
+        if (more) {
+          if (!(ok = mbar_wait(smem_u32(v_full + nt), ((t + 1) / NS) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          mma_rows_rows<D>(tP, lo_do, lo_v + (uint32_t)(nt * (TB >> 4)), hi_k, id_ss);
+          tc_commit(smem_u32(dp_full));
+          tc_commit(smem_u32(v_empty + nt));
+        }
+      }
+      tc_commit(smem_u32(dq_done));
+    }
+  } else {
+    // ------------------------------------------------ rows: P, dS, dQ --
+    const int r = threadIdx.x;               // row of the tile == TMEM lane
+    const int i = q0 + r;
+    const bool row_ok = i < sq;
+    const int64_t t_glob = (int64_t)qs + i;
+    const float lse = row_ok ? __ldg(p.lse + (int64_t)h * p.total_q + t_glob) : 0.f;
+    const float delta = row_ok ? __ldg(p.delta + (int64_t)h * p.total_q + t_glob) : 0.f;
+    const bool live = row_ok && lse != -INFINITY;
+    const float lse2 = lse * kLog2e;
+    const int ip = i + sk - sq;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t rS = tmem + lane_base, rP = tmem + lane_base + 128, rQ = tmem + lane_base + 256;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int j0 = (klo + t) * 128;
+      ok = mbar_wait(smem_u32(s_full), t & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float pr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(rS + c * 32, *reinterpret_cast<float(*)[32]>(pr + c * 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(s_read));
+      const bool full = (q0 + 127 < sq) && (j0 + 127 < sk) && (!p.causal || ip_min >= j0 + 127) && p.window <= 0;
+#pragma unroll
+      for (int e = 0; e < 128; ++e) {
+        float x = ex2(fmaf(pr[e], p.scale_log2, -lse2));
+        if (!full) {
+          const int j = j0 + e;
+          bool a = live && j < sk;
+          if (p.causal) a = a && j <= ip;
+          if (p.window > 0) a = a && (p.causal ? (ip - j < p.window) : (abs(ip - j) < p.window));
+          x = a ? x : 0.f;
+        } else if (!live) {
+          x = 0.f;
+        }
+        pr[e] = x;
+      }
+      ok = mbar_wait(smem_u32(dp_full), t & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float dp[32];
+        tmem_ld32(rP + c * 32, dp);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(pr[c * 32 + 2 * e] * (dp[2 * e] - delta), pr[c * 32 + 2 * e + 1] * (dp[2 * e + 1] - delta));
+        bwd_tmem_st16(rP + c * 16, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(ds_full));
+    }
+    if (ok) {
+      ok = mbar_wait(smem_u32(dq_done), 0, abort_flag, p.err);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        __nv_bfloat16 *orow = p.dq + t_glob * p.dq_stride_t + (int64_t)h * p.dq_stride_h;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(rQ + c * 32, o);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(o[2 * e] * p.scale, o[2 * e + 1] * p.scale);
+          if (row_ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------- dK, dV --
+// CTA (key tile, kv head, sequence); it loops over the q heads of the kv
+// head's group and, for each, over the query tiles that may see its keys.
+// TMEM: S^T [0,128), dP^T [128,256) -- dS^T (bf16) over its first 64 columns,
+// P^T (bf16) over the last 64 -- dV [256, 256+D), dK [384, 384+D).  Warps 0-3
+// own the tile's keys (TMEM lanes); warp 4 loads K and V once and then Q, dO,
+// LSE and Delta per step into a two-stage ring; warp 5 issues the MMAs:
+//   S^T(0) dP^T(0) | S^T(s+1) once S^T(s) is read | dV += P^T(s) dO(s),
+//   dK += dS^T(s) Q(s) | dP^T(s+1)
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  constexpr int NS = Cfg::NS, TB = Cfg::kTileBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int qs = __ldg(p.cu_q + b), sq = __ldg(p.cu_q + b + 1) - qs;
+  const int ks = __ldg(p.cu_k + b), sk = __ldg(p.cu_k + b + 1) - ks;
+  const int kj0 = kt * 128;
+  if (kj0 >= sk) return;
+  const int kl = min(kj0 + 128, sk) - 1;
+  // query rows that may see keys kj0..kl: i' = i + sk - sq
+  const int off = sk - sq;
+  int qlo = 0, qhi = sq;
+  if (p.causal) qlo = max(qlo, kj0 - off);
+  if (p.window > 0) {
+    qhi = min(qhi, kl + p.window - off);
+    if (!p.causal) qlo = max(qlo, kj0 - p.window + 1 - off);
+  }
+  const int tlo = qlo / 128;
+  const int nqt = qhi > qlo ? (qhi + 127) / 128 - tlo : 0;
+  const int steps = nqt * p.group;
+  if (steps == 0) {   // no query sees these keys: dK = dV = 0
+    for (int idx = threadIdx.x; idx < (kl - kj0 + 1) * (D / 8); idx += blockDim.x) {
+      const int r = idx / (D / 8), c = idx - r * (D / 8);
+      const int64_t tok = (int64_t)ks + kj0 + r;
+      __nv_bfloat16 *a = p.dk + tok * p.dk_stride_t + (int64_t)hk * p.dk_stride_h;
+      __nv_bfloat16 *v = p.dv + tok * p.dv_stride_t + (int64_t)hk * p.dv_stride_h;
+      *reinterpret_cast<uint4 *>(a + c * 8) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(v + c * 8) = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+
+  uint8_t *sK = smem, *sV = smem + TB, *sQ = smem + 2 * TB, *sDO = smem + (2 + NS) * TB;
+  float *sStat = reinterpret_cast<float *>(smem + (2 + 2 * NS) * TB);   // [NS][2][128]: LSE*log2e, Delta
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStat + NS * 256);
+  uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = qd_full + NS, *st_full = qd_empty + NS,
+           *dpt_full = st_full + 1, *st_read = dpt_full + 1, *pds_full = st_read + 1, *done = pds_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(kv_full), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(qd_full + s), 1);
+      mbar_init(smem_u32(qd_empty + s), 1);
+    }
+    mbar_init(smem_u32(st_full), 1);
+    mbar_init(smem_u32(dpt_full), 1);
+    mbar_init(smem_u32(st_read), 128);
+    mbar_init(smem_u32(pds_full), 128);
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------- producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_expect_tx(smem_u32(kv_full), 2 * TB);
+      bwd_load_tile<D>(sK, &tm_k, kv_full, hk, ks + kj0);
+      bwd_load_tile<D>(sV, &tm_v, kv_full, hk, ks + kj0);
+    }
+    bool ok = true;
+    for (int s = 0; s < steps; ++s) {
+      const int st = s % NS;
+      const int h = hk * p.group + s / nqt, q0 = (tlo + s % nqt) * 128;
+      if (lane == 0 && s >= NS) ok = mbar_wait(smem_u32(qd_empty + st), ((s / NS) - 1) & 1, abort_flag, p.err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      // per-query statistics of this step; rows past the sequence get
+      // LSE = +inf, so that their probabilities are 0
+      float *stat = sStat + st * 256;
+      for (int r = lane; r < 128; r += 32) {
+        const int i = q0 + r;
+        const int64_t at = (int64_t)h * p.total_q + qs + i;
+        stat[r] = i < sq ? __ldg(p.lse + at) * kLog2e : INFINITY;
+        stat[128 + r] = i < sq ? __ldg(p.delta + at) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_expect_tx(smem_u32(qd_full + st), 2 * TB);
+        bwd_load_tile<D>(sQ + st * TB, &tm_q, qd_full + st, h, qs + q0);
+        bwd_load_tile<D>(sDO + st * TB, &tm_do, qd_full + st, h, qs + q0);
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------- MMAs --
+    if (lane == 0) {
+      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint32_t hi = (uint32_t)(dk0 >> 32), lo_k = (uint32_t)dk0;
+      const uint32_t lo_v = (uint32_t)smem_desc_sw128(smem_u32(sV), 16, 1024);
+      const uint32_t lo_q = (uint32_t)smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint32_t lo_do = (uint32_t)smem_desc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t dqmn = smem_desc_sw128(smem_u32(sQ), 128 * 128, 1024);
+      const uint32_t lo_qmn = (uint32_t)dqmn, hi_mn = (uint32_t)(dqmn >> 32);
+      const uint32_t lo_domn = (uint32_t)smem_desc_sw128(smem_u32(sDO), 128 * 128, 1024);
+      const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 384;
+      bool ok = mbar_wait(smem_u32(kv_full), 0, abort_flag, p.err);
+      if (ok) ok = mbar_wait(smem_u32(qd_full), 0, abort_flag, p.err);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_rows<D>(tS, lo_k, lo_q, hi, id_ss);
+        tc_commit(smem_u32(st_full));
+        mma_rows_rows<D>(tP, lo_v, lo_do, hi, id_ss);
+        tc_commit(smem_u32(dpt_full));
+      }
+      for (int s = 0; ok && s < steps; ++s) {
+        const int st = s % NS, nt = (s + 1) % NS;
+        const uint32_t so = (uint32_t)(st * (TB >> 4)), no = (uint32_t)(nt * (TB >> 4));
+        const bool more = s + 1 < steps;
+        if (more) {
+          if (!(ok = mbar_wait(smem_u32(st_read), s & 1, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(smem_u32(qd_full + nt), ((s + 1) / NS) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          mma_rows_rows<D>(tS, lo_k, lo_q + no, hi, id_ss);
+          tc_commit(smem_u32(st_full));
+        }
+        if (!(ok = mbar_wait(smem_u32(pds_full), s & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        mma_tmem_rows(tV, tP + 64, lo_domn + so, hi_mn, id_acc, s > 0 ? 1u : 0u);
+        mma_tmem_rows(tK, tP, lo_qmn + so, hi_mn, id_acc, s > 0 ? 1u : 0u);
+        tc_commit(smem_u32(qd_empty + st));
+        if (more) {
+          mma_rows_rows<D>(tP, lo_v, lo_do + no, hi, id_ss);
+          tc_commit(smem_u32(dpt_full));
+        }
+      }
+      tc_commit(smem_u32(done));
+    }
+  } else {
+    // ------------------------------------------ keys: P^T, dS^T, dK, dV --
+    const int r = threadIdx.x;               // key of the tile == TMEM lane
+    const int j = kj0 + r;
+    const bool key_ok = j < sk;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t rS = tmem + lane_base, rP = tmem + lane_base + 128;
+    bool ok = true;
+    for (int s = 0; s < steps; ++s) {
+      const int st = s % NS, q0 = (tlo + s % nqt) * 128;
+      const float *stat = sStat + st * 256;
+      ok = mbar_wait(smem_u32(st_full), s & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float pr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(rS + c * 32, *reinterpret_cast<float(*)[32]>(pr + c * 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(st_read));
+      // the step's statistics were stored by the producer before it armed
+      // this stage's barrier (at most one phase ahead: the stage is reloaded
+      // only after this step's dV/dK)
+      ok = mbar_wait(smem_u32(qd_full + st), (s / NS) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const bool full = (q0 + 127 < sq) && (kj0 + 127 < sk) && (!p.causal || q0 + off >= kj0 + 127) &&
+                        p.window <= 0;
+#pragma unroll
+      for (int e = 0; e < 128; ++e) {
+        float x = ex2(fmaf(pr[e], p.scale_log2, -stat[e]));
+        if (!full) x = (key_ok && bwd_allowed(p, q0 + e, j, sq, sk)) ? x : 0.f;
+        pr[e] = x;
+      }
+      ok = mbar_wait(smem_u32(dpt_full), s & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float dp[32];
+        tmem_ld32(rP + c * 32, dp);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = c * 32 + 2 * e;
+          w[e] = pack_bf16x2(pr[q] * (dp[2 * e] - stat[128 + q]), pr[q + 1] * (dp[2 * e + 1] - stat[128 + q + 1]));
+        }
+        bwd_tmem_st16(rP + c * 16, w);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pr[c * 32 + 2 * e], pr[c * 32 + 2 * e + 1]);
+        bwd_tmem_st16(rP + 64 + c * 16, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(pds_full));
+    }
+    if (ok) {
+      ok = mbar_wait(smem_u32(done), 0, abort_flag, p.err);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const int64_t tok = (int64_t)ks + j;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t src = tmem + lane_base + (which ? 384u : 256u);
+          const float f = which ? p.scale : 1.f;
+          __nv_bfloat16 *orow = which ? p.dk + tok * p.dk_stride_t + (int64_t)hk * p.dk_stride_h
+                                      : p.dv + tok * p.dv_stride_t + (int64_t)hk * p.dv_stride_h;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(src + c * 32, o);
+            tmem_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(o[2 * e] * f, o[2 * e + 1] * f);
+            if (key_ok) {
+              uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -7,6 +7,7 @@
 #include "../../include/fa_gb300.h"
 #include "fa_decode.cuh"
 #include "fa_prefill.cuh"
+#include "fa_bwd_params.h"
 
 namespace fa {
 
@@ -28,6 +29,16 @@ struct DecodeLaunch {
   cudaStream_t stream;
 };
 
+struct BwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  BwdParams p;
+  BwdDeltaParams dp;
+  unsigned delta_blocks;
+  dim3 grid_q, grid_kv;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_bwd(int d, const BwdLaunch &L);
 cudaError_t launch_prefill_64_64(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128(const PrefillLaunch &L);
 cudaError_t launch_prefill_192_128(const PrefillLaunch &L);

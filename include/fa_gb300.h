@@ -217,6 +217,45 @@ fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_s
                        void *stream);
 
 /*
+ * fa_bwd_varlen -- the backward pass: gradients of L = sum(dout * out) with
+ * respect to q, k and v, recomputed from the forward's saved LSE
+ * (RL-Kernel PR #237, backward commit: a Delta preprocess, then dQ/dK/dV from
+ * the saved LSE):
+ *   Delta_i = <dout_i, out_i>,   P_ij = exp(softmax_scale * <q_i, k_j> - LSE_i)
+ *   dP_ij = <dout_i, v_j>,   dS_ij = P_ij * (dP_ij - Delta_i)
+ *   dv_j = sum_i P_ij dout_i,  dk_j = softmax_scale * sum_i dS_ij q_i,
+ *   dq_i = softmax_scale * sum_j dS_ij k_j      (allowed (i, j) only)
+ *
+ *  q, out, dout, dq   bf16 [T_q, Hq, D];  k, v, dk, dv   bf16 [T_k, Hkv, D],
+ *                     packed varlen (no block table).  D = 64 or 128 (Dk = Dv).
+ *                     Last dim contiguous, other strides multiples of 8
+ *                     elements, bases 16-byte aligned.  GQA: Hq % Hkv == 0;
+ *                     dk, dv sum over the q heads of each kv head's group.
+ *  lse                fp32 [Hq, T_q] contiguous, the forward's LSE for the
+ *                     same (q, k, v, masks).
+ *  cu_seqlens_q/k     int32 [num_seqs + 1] (row offsets of q and of k/v).
+ *  softmax_scale      > 0;  causal, window as in fa_fwd_varlen (score mods and
+ *                     block masks are not supported here).
+ *  launch             num_seqs, max_seqlen_q/k, total_q (= T_q) and a
+ *                     workspace of fa_bwd_workspace_bytes(T_q, Hq) bytes,
+ *                     256-byte aligned, for Delta (fp32 [Hq, T_q]).
+ * Outputs are overwritten (rows of keys or queries that see nothing get 0)
+ * and must not overlap any input or each other.  Three kernels are enqueued
+ * on `stream` (Delta, dK/dV, dQ); no allocation, copy or synchronisation.
+ * Errors as for fa_fwd_varlen: FA_ERR_INVALID_ARG for shapes, dtypes,
+ * strides, alignment or a missing workspace, FA_ERR_UNSUPPORTED for other
+ * head dims, FA_ERR_CUDA for launch failures.
+ */
+fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_tensor_t *v,
+                          const fa_tensor_t *out, const fa_tensor_t *dout, const fa_tensor_t *lse,
+                          const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
+                          fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv, float softmax_scale,
+                          int32_t causal, int32_t window, const fa_launch_t *launch, void *stream);
+
+/* Workspace bytes of fa_bwd_varlen: Delta, fp32 [Hq, T_q], rounded up to 256. */
+size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);
+
+/*
  * fa_fwd_varlen_noalloc -- the split-KV decode of fa_fwd_varlen for callers
  * that cannot allocate device memory.  (The pages have no counterpart: this
  * entry exists for deployment, not for the method.)

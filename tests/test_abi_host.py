@@ -216,3 +216,53 @@ def test_plan_create_validates_like_the_call(L):
     assert st == fa.FA_ERR_INVALID_ARG and "plan" in L.fa_last_error().decode()
     assert L.fa_fwd_plan_launch(None, None) == fa.FA_ERR_INVALID_ARG
     L.fa_fwd_plan_destroy(None)
+
+
+def _bcall(L, **over):
+    T, H, D = 256, 4, 64
+    ws = 1 << 30
+    args = dict(
+        q=_t(FAKE, fa.FA_BF16, [T, H, D]), k=_t(FAKE * 2, fa.FA_BF16, [T, H, D]),
+        v=_t(FAKE * 3, fa.FA_BF16, [T, H, D]), out=_t(FAKE * 4, fa.FA_BF16, [T, H, D]),
+        dout=_t(FAKE * 5, fa.FA_BF16, [T, H, D]), lse=_t(FAKE * 6, fa.FA_F32, [H, T]),
+        cq=_t(FAKE * 7, fa.FA_I32, [3]), ck=_t(FAKE * 8, fa.FA_I32, [3]),
+        dq=_t(FAKE * 9, fa.FA_BF16, [T, H, D]), dk=_t(FAKE * 10, fa.FA_BF16, [T, H, D]),
+        dv=_t(FAKE * 11, fa.FA_BF16, [T, H, D]), scale=0.125, causal=1, window=0,
+        launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=0, total_q=T, total_k=T,
+                         workspace=ws, workspace_bytes=fa.bwd_workspace_bytes(T, H)))
+    args.update(over)
+    r = lambda x: None if x is None else ctypes.byref(x)
+    st = L.fa_bwd_varlen(*[r(args[n]) for n in ("q", "k", "v", "out", "dout", "lse", "cq", "ck", "dq", "dk", "dv")],
+                         args["scale"], args["causal"], args["window"], r(args["launch"]), None)
+    return st, L.fa_last_error().decode()
+
+
+def test_bwd_workspace_bytes(L):
+    assert fa.bwd_workspace_bytes(0, 4) == 0
+    n = fa.bwd_workspace_bytes(1000, 16)
+    assert n >= 1000 * 16 * 4 and n % 256 == 0
+
+
+@pytest.mark.parametrize("over,status,words", [
+    (dict(q=_t(FAKE, fa.FA_BF16, [256, 4, 96])), fa.FA_ERR_UNSUPPORTED, "Dk = Dv in {64, 128}"),
+    (dict(k=_t(FAKE * 2, fa.FA_BF16, [256, 3, 64]), v=_t(FAKE * 3, fa.FA_BF16, [256, 3, 64]),
+          dk=_t(FAKE * 10, fa.FA_BF16, [256, 3, 64]), dv=_t(FAKE * 11, fa.FA_BF16, [256, 3, 64])),
+     fa.FA_ERR_INVALID_ARG, "multiple of Hkv"),
+    (dict(k=_t(FAKE * 2, fa.FA_BF16, [16, 16, 4, 64])), fa.FA_ERR_INVALID_ARG, "packed"),
+    (dict(dout=_t(FAKE * 5, fa.FA_BF16, [255, 4, 64])), fa.FA_ERR_INVALID_ARG, "dout has shape"),
+    (dict(dq=_t(FAKE * 9, fa.FA_BF16, [256, 4, 64], [256, 64, 2])), fa.FA_ERR_INVALID_ARG, "contiguous"),
+    (dict(lse=_t(FAKE * 6, fa.FA_F32, [256, 4])), fa.FA_ERR_INVALID_ARG, "lse must be"),
+    (dict(dk=_t(FAKE * 2, fa.FA_BF16, [256, 4, 64])), fa.FA_ERR_INVALID_ARG, "overlap"),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG, "softmax_scale"),
+    (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=256, total_k=256)),
+     fa.FA_ERR_INVALID_ARG, "workspace"),
+    (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=256, total_k=256,
+                           workspace=(1 << 30) + 8, workspace_bytes=1 << 20)),
+     fa.FA_ERR_INVALID_ARG, "256-byte aligned"),
+    (dict(cq=_t(FAKE * 7, fa.FA_I32, [4])), fa.FA_ERR_INVALID_ARG, "num_seqs + 1"),
+    (dict(launch=None), fa.FA_ERR_INVALID_ARG, "launch"),
+])
+def test_bwd_validation_rejects_before_launch(L, over, status, words):
+    st, msg = _bcall(L, **over)
+    assert st == status, msg
+    assert words in msg, msg
