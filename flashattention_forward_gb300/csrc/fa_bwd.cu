@@ -7,8 +7,7 @@ namespace {
 template <int D>
 cudaError_t launch_d(const BwdLaunch &L) {
   using Cfg = BwdCfg<D>;
-  // tiles, statistics ring, barriers, TMEM slot and the 1024-byte alignment slack
-  constexpr int kSmem = 6 * Cfg::kTileBytes + Cfg::NS * 256 * 4 + 256 + 1024;
+  constexpr int kSmem = Cfg::kSmemBytes;
   static unsigned long long done_dq = 0, done_kv = 0;
   cudaError_t e = ensure_smem_attr(fa_bwd_dq_kernel<D>, kSmem, &done_dq);
   if (e == cudaSuccess) e = ensure_smem_attr(fa_bwd_dkdv_kernel<D>, kSmem, &done_kv);

@@ -54,25 +54,19 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const BwdDeltaParams 
   if (lane == 0) p.delta[(int64_t)h * p.total_q + t] = acc;
 }
 
-// Is key j visible from query row i (sequence-local; bottom-right causal)?
-__device__ __forceinline__ bool bwd_allowed(const BwdParams &p, int i, int j, int sq, int sk) {
-  if (i >= sq || j >= sk || i < 0 || j < 0) return false;
-  const int ip = i + sk - sq;
-  if (p.causal && j > ip) return false;
-  if (p.window > 0) {
-    if (p.causal) return ip - j < p.window;
-    return abs(ip - j) < p.window;
-  }
-  return true;
-}
-
 template <int D>
 struct BwdCfg {
   static constexpr int kTile = 128;
   static constexpr int kTileBytes = kTile * D * 2;   // one [128, D] bf16 tile
-  static constexpr int NS = 2;                       // ring stages
+  // Ring depths.  The operand of the MMA that is issued ahead (K for S in the
+  // dQ kernel, Q for S^T in the dK/dV kernel) gets three stages, the other
+  // (V, dO) two: a stage is refilled only once the step that frees it has
+  // run its accumulating MMAs, and three stages keep that refill off the path
+  // of the MMA issued ahead.  Two [128, D] tiles + 3 + 2 stages: 224 KB at D = 128.
+  static constexpr int NS3 = 3, NS2 = 2;
   static constexpr int kThreads = 6 * 32;            // 4 softmax warps, producer, MMA
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kSmemBytes = (2 + NS3 + NS2) * kTileBytes + 1024 + 256 + 1024;
 };
 
 // The K-major descriptor walk of a [128, D] tile: 32 bytes per K=16 slice,
@@ -108,6 +102,11 @@ __device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 
+// Barrier among `count` threads (whole warps) of the CTA, id 1..15.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void bwd_tmem_st16(uint32_t taddr, const uint32_t *r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -137,7 +136,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdParams p) {
   using Cfg = BwdCfg<D>;
-  constexpr int NS = Cfg::NS, TB = Cfg::kTileBytes;
+  constexpr int NSK = Cfg::NS3, NSV = Cfg::NS2, TB = Cfg::kTileBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,18 +166,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     return;
   }
 
-  uint8_t *sQ = smem, *sDO = smem + TB, *sK = smem + 2 * TB, *sV = smem + (2 + NS) * TB;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + 2 * NS) * TB);
-  uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = k_full + NS, *v_full = k_empty + NS,
-           *v_empty = v_full + NS, *s_full = v_empty + NS, *dp_full = s_full + 1, *s_read = dp_full + 1,
+  uint8_t *sQ = smem, *sDO = smem + TB, *sK = smem + 2 * TB, *sV = smem + (2 + NSK) * TB;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + NSK + NSV) * TB);
+  uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = k_full + NSK, *v_full = k_empty + NSK,
+           *v_empty = v_full + NSV, *s_full = v_empty + NSV, *dp_full = s_full + 1, *s_read = dp_full + 1,
            *ds_full = s_read + 1, *dq_done = ds_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dq_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(smem_u32(k_full + s), 1);
       mbar_init(smem_u32(k_empty + s), 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(smem_u32(v_full + s), 1);
       mbar_init(smem_u32(v_empty + s), 1);
     }
@@ -209,14 +210,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_expect_tx(smem_u32(q_full), 2 * TB);
       bwd_load_tile<D>(sQ, &tm_q, q_full, h, qs + q0);
       bwd_load_tile<D>(sDO, &tm_do, q_full, h, qs + q0);
-      for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % NS, row = ks + (klo + t) * 128;
-        if (t >= NS && !mbar_wait(smem_u32(k_empty + st), ((t / NS) - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(smem_u32(k_full + st), TB);
-        bwd_load_tile<D>(sK + st * TB, &tm_k, k_full + st, hk, row);
-        if (t >= NS && !mbar_wait(smem_u32(v_empty + st), ((t / NS) - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(smem_u32(v_full + st), TB);
-        bwd_load_tile<D>(sV + st * TB, &tm_v, v_full + st, hk, row);
+      // K runs ahead of V (its ring is deeper); issue order K(t), V(t - 1)
+      for (int t = 0; t <= n_tiles; ++t) {
+        if (t < n_tiles) {
+          const int st = t % NSK, row = ks + (klo + t) * 128;
+          if (t >= NSK && !mbar_wait(smem_u32(k_empty + st), ((t / NSK) - 1) & 1, abort_flag, p.err)) break;
+          mbar_expect_tx(smem_u32(k_full + st), TB);
+          bwd_load_tile<D>(sK + st * TB, &tm_k, k_full + st, hk, row);
+        }
+        if (t >= 1) {
+          const int u = t - 1, sv = u % NSV, row = ks + (klo + u) * 128;
+          if (u >= NSV && !mbar_wait(smem_u32(v_empty + sv), ((u / NSV) - 1) & 1, abort_flag, p.err)) break;
+          mbar_expect_tx(smem_u32(v_full + sv), TB);
+          bwd_load_tile<D>(sV + sv * TB, &tm_v, v_full + sv, hk, row);
+        }
       }
     }
   } else if (warp == 5) {
@@ -247,13 +254,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_commit(smem_u32(v_empty));
       }
       for (int t = 0; ok && t < n_tiles; ++t) {
-        const int st = t % NS, nt = (t + 1) % NS;
+        const int st = t % NSK, nk = (t + 1) % NSK, nv = (t + 1) % NSV;
         const bool more = t + 1 < n_tiles;
         if (more) {
           if (!(ok = mbar_wait(smem_u32(s_read), t & 1, abort_flag, p.err))) break;
-          if (!(ok = mbar_wait(smem_u32(k_full + nt), ((t + 1) / NS) & 1, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(smem_u32(k_full + nk), ((t + 1) / NSK) & 1, abort_flag, p.err))) break;
           tc_fence_after();
-          mma_rows_rows<D>(tS, lo_q, lo_k + (uint32_t)(nt * (TB >> 4)), hi_k, id_ss);
+          mma_rows_rows<D>(tS, lo_q, lo_k + (uint32_t)(nk * (TB >> 4)), hi_k, id_ss);
           tc_commit(smem_u32(s_full));
         }
         if (!(ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, p.err))) break;
@@ -261,11 +268,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_tmem_rows(tQ, tP, lo_kmn + (uint32_t)(st * (TB >> 4)), hi_kmn, id_dq, t > 0 ? 1u : 0u);
         tc_commit(smem_u32(k_empty + st));
         if (more) {
-          if (!(ok = mbar_wait(smem_u32(v_full + nt), ((t + 1) / NS) & 1, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(smem_u32(v_full + nv), ((t + 1) / NSV) & 1, abort_flag, p.err))) break;
           tc_fence_after();
-          mma_rows_rows<D>(tP, lo_do, lo_v + (uint32_t)(nt * (TB >> 4)), hi_k, id_ss);
+          mma_rows_rows<D>(tP, lo_do, lo_v + (uint32_t)(nv * (TB >> 4)), hi_k, id_ss);
           tc_commit(smem_u32(dp_full));
-          tc_commit(smem_u32(v_empty + nt));
+          tc_commit(smem_u32(v_empty + nv));
         }
       }
       tc_commit(smem_u32(dq_done));
@@ -281,6 +288,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const bool live = row_ok && lse != -INFINITY;
     const float lse2 = lse * kLog2e;
     const int ip = i + sk - sq;
+    // keys [row_jlo, row_jhi) of the sequence that row i sees (empty if none)
+    int row_jlo = 0, row_jhi = sk;
+    if (p.causal) row_jhi = min(row_jhi, ip + 1);
+    if (p.window > 0) {
+      row_jlo = max(row_jlo, ip - p.window + 1);
+      if (!p.causal) row_jhi = min(row_jhi, ip + p.window);
+    }
+    if (!live) row_jhi = row_jlo;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t rS = tmem + lane_base, rP = tmem + lane_base + 128, rQ = tmem + lane_base + 256;
     bool ok = true;
@@ -295,20 +310,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(s_read));
-      const bool full = (q0 + 127 < sq) && (j0 + 127 < sk) && (!p.causal || ip_min >= j0 + 127) && p.window <= 0;
+      // the row's allowed keys are one interval; as tile columns: [elo, ehi)
+      const int elo = row_jlo - j0, ehi = row_jhi - j0;
 #pragma unroll
       for (int e = 0; e < 128; ++e) {
-        float x = ex2(fmaf(pr[e], p.scale_log2, -lse2));
-        if (!full) {
-          const int j = j0 + e;
-          bool a = live && j < sk;
-          if (p.causal) a = a && j <= ip;
-          if (p.window > 0) a = a && (p.causal ? (ip - j < p.window) : (abs(ip - j) < p.window));
-          x = a ? x : 0.f;
-        } else if (!live) {
-          x = 0.f;
-        }
-        pr[e] = x;
+        const float x = ex2(fmaf(pr[e], p.scale_log2, -lse2));
+        pr[e] = (e >= elo && e < ehi) ? x : 0.f;
       }
       ok = mbar_wait(smem_u32(dp_full), t & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -363,8 +370,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 // head's group and, for each, over the query tiles that may see its keys.
 // TMEM: S^T [0,128), dP^T [128,256) -- dS^T (bf16) over its first 64 columns,
 // P^T (bf16) over the last 64 -- dV [256, 256+D), dK [384, 384+D).  Warps 0-3
-// own the tile's keys (TMEM lanes); warp 4 loads K and V once and then Q, dO,
-// LSE and Delta per step into a two-stage ring; warp 5 issues the MMAs:
+// own the tile's keys (TMEM lanes) and stage each step's LSE and Delta in
+// shared memory; warp 4 loads K and V once and then Q (three stages) and dO
+// (two stages) per step; warp 5 issues the MMAs:
 //   S^T(0) dP^T(0) | S^T(s+1) once S^T(s) is read | dV += P^T(s) dO(s),
 //   dK += dS^T(s) Q(s) | dP^T(s+1)
 template <int D>
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
   using Cfg = BwdCfg<D>;
-  constexpr int NS = Cfg::NS, TB = Cfg::kTileBytes;
+  constexpr int NSQ = Cfg::NS3, NSO = Cfg::NS2, TB = Cfg::kTileBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -406,18 +414,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     return;
   }
 
-  uint8_t *sK = smem, *sV = smem + TB, *sQ = smem + 2 * TB, *sDO = smem + (2 + NS) * TB;
-  float *sStat = reinterpret_cast<float *>(smem + (2 + 2 * NS) * TB);   // [NS][2][128]: LSE*log2e, Delta
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sStat + NS * 256);
-  uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = qd_full + NS, *st_full = qd_empty + NS,
-           *dpt_full = st_full + 1, *st_read = dpt_full + 1, *pds_full = st_read + 1, *done = pds_full + 1;
+  uint8_t *sK = smem, *sV = smem + TB, *sQ = smem + 2 * TB, *sDO = smem + (2 + NSQ) * TB;
+  float *sStat = reinterpret_cast<float *>(smem + (2 + NSQ + NSO) * TB);   // [2][128]: LSE*log2e, Delta
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStat + 256);
+  uint64_t *kv_full = bars, *q_full = bars + 1, *q_empty = q_full + NSQ, *o_full = q_empty + NSQ,
+           *o_empty = o_full + NSO, *st_full = o_empty + NSO, *dpt_full = st_full + 1, *st_read = dpt_full + 1,
+           *pds_full = st_read + 1, *done = pds_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(kv_full), 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(qd_full + s), 1);
-      mbar_init(smem_u32(qd_empty + s), 1);
+    for (int s = 0; s < NSQ; ++s) {
+      mbar_init(smem_u32(q_full + s), 1);
+      mbar_init(smem_u32(q_empty + s), 1);
+    }
+    for (int s = 0; s < NSO; ++s) {
+      mbar_init(smem_u32(o_full + s), 1);
+      mbar_init(smem_u32(o_empty + s), 1);
     }
     mbar_init(smem_u32(st_full), 1);
     mbar_init(smem_u32(dpt_full), 1);
@@ -447,26 +460,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       bwd_load_tile<D>(sK, &tm_k, kv_full, hk, ks + kj0);
       bwd_load_tile<D>(sV, &tm_v, kv_full, hk, ks + kj0);
     }
-    bool ok = true;
-    for (int s = 0; s < steps; ++s) {
-      const int st = s % NS;
-      const int h = hk * p.group + s / nqt, q0 = (tlo + s % nqt) * 128;
-      if (lane == 0 && s >= NS) ok = mbar_wait(smem_u32(qd_empty + st), ((s / NS) - 1) & 1, abort_flag, p.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      // per-query statistics of this step; rows past the sequence get
-      // LSE = +inf, so that their probabilities are 0
-      float *stat = sStat + st * 256;
-      for (int r = lane; r < 128; r += 32) {
-        const int i = q0 + r;
-        const int64_t at = (int64_t)h * p.total_q + qs + i;
-        stat[r] = i < sq ? __ldg(p.lse + at) * kLog2e : INFINITY;
-        stat[128 + r] = i < sq ? __ldg(p.delta + at) : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_expect_tx(smem_u32(qd_full + st), 2 * TB);
-        bwd_load_tile<D>(sQ + st * TB, &tm_q, qd_full + st, h, qs + q0);
-        bwd_load_tile<D>(sDO + st * TB, &tm_do, qd_full + st, h, qs + q0);
+    // Q runs ahead of dO (its ring is deeper): issue order Q(s), dO(s - 1)
+    if (lane == 0) {
+      for (int s = 0; s <= steps; ++s) {
+        if (s < steps) {
+          const int st = s % NSQ, h = hk * p.group + s / nqt, q0 = (tlo + s % nqt) * 128;
+          if (s >= NSQ && !mbar_wait(smem_u32(q_empty + st), ((s / NSQ) - 1) & 1, abort_flag, p.err)) break;
+          mbar_expect_tx(smem_u32(q_full + st), TB);
+          bwd_load_tile<D>(sQ + st * TB, &tm_q, q_full + st, h, qs + q0);
+        }
+        if (s >= 1) {
+          const int u = s - 1, so = u % NSO, h = hk * p.group + u / nqt, q0 = (tlo + u % nqt) * 128;
+          if (u >= NSO && !mbar_wait(smem_u32(o_empty + so), ((u / NSO) - 1) & 1, abort_flag, p.err)) break;
+          mbar_expect_tx(smem_u32(o_full + so), TB);
+          bwd_load_tile<D>(sDO + so * TB, &tm_do, o_full + so, h, qs + q0);
+        }
       }
     }
   } else if (warp == 5) {
@@ -484,32 +492,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const uint32_t lo_domn = (uint32_t)smem_desc_sw128(smem_u32(sDO), 128 * 128, 1024);
       const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 384;
       bool ok = mbar_wait(smem_u32(kv_full), 0, abort_flag, p.err);
-      if (ok) ok = mbar_wait(smem_u32(qd_full), 0, abort_flag, p.err);
+      if (ok) ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
       if (ok) {
         tc_fence_after();
         mma_rows_rows<D>(tS, lo_k, lo_q, hi, id_ss);
         tc_commit(smem_u32(st_full));
+        ok = mbar_wait(smem_u32(o_full), 0, abort_flag, p.err);
+      }
+      if (ok) {
+        tc_fence_after();
         mma_rows_rows<D>(tP, lo_v, lo_do, hi, id_ss);
         tc_commit(smem_u32(dpt_full));
       }
       for (int s = 0; ok && s < steps; ++s) {
-        const int st = s % NS, nt = (s + 1) % NS;
-        const uint32_t so = (uint32_t)(st * (TB >> 4)), no = (uint32_t)(nt * (TB >> 4));
+        const int sq_ = s % NSQ, so_ = s % NSO, nq = (s + 1) % NSQ, no = (s + 1) % NSO;
         const bool more = s + 1 < steps;
         if (more) {
           if (!(ok = mbar_wait(smem_u32(st_read), s & 1, abort_flag, p.err))) break;
-          if (!(ok = mbar_wait(smem_u32(qd_full + nt), ((s + 1) / NS) & 1, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(smem_u32(q_full + nq), ((s + 1) / NSQ) & 1, abort_flag, p.err))) break;
           tc_fence_after();
-          mma_rows_rows<D>(tS, lo_k, lo_q + no, hi, id_ss);
+          mma_rows_rows<D>(tS, lo_k, lo_q + (uint32_t)(nq * (TB >> 4)), hi, id_ss);
           tc_commit(smem_u32(st_full));
         }
         if (!(ok = mbar_wait(smem_u32(pds_full), s & 1, abort_flag, p.err))) break;
         tc_fence_after();
-        mma_tmem_rows(tV, tP + 64, lo_domn + so, hi_mn, id_acc, s > 0 ? 1u : 0u);
-        mma_tmem_rows(tK, tP, lo_qmn + so, hi_mn, id_acc, s > 0 ? 1u : 0u);
-        tc_commit(smem_u32(qd_empty + st));
+        mma_tmem_rows(tV, tP + 64, lo_domn + (uint32_t)(so_ * (TB >> 4)), hi_mn, id_acc, s > 0 ? 1u : 0u);
+        tc_commit(smem_u32(o_empty + so_));
+        mma_tmem_rows(tK, tP, lo_qmn + (uint32_t)(sq_ * (TB >> 4)), hi_mn, id_acc, s > 0 ? 1u : 0u);
+        tc_commit(smem_u32(q_empty + sq_));
         if (more) {
-          mma_rows_rows<D>(tP, lo_v, lo_do + no, hi, id_ss);
+          if (!(ok = mbar_wait(smem_u32(o_full + no), ((s + 1) / NSO) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          mma_rows_rows<D>(tP, lo_v, lo_do + (uint32_t)(no * (TB >> 4)), hi, id_ss);
           tc_commit(smem_u32(dpt_full));
         }
       }
@@ -520,14 +534,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int r = threadIdx.x;               // key of the tile == TMEM lane
     const int j = kj0 + r;
     const bool key_ok = j < sk;
+    // queries [key_qlo, key_qhi) of the sequence that see key j: i' = i + off
+    int key_qlo = 0, key_qhi = sq;
+    if (p.causal) key_qlo = max(key_qlo, j - off);
+    if (p.window > 0) {
+      key_qhi = min(key_qhi, j + p.window - off);
+      if (!p.causal) key_qlo = max(key_qlo, j - p.window + 1 - off);
+    }
+    if (!key_ok) key_qhi = key_qlo;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t rS = tmem + lane_base, rP = tmem + lane_base + 128;
     bool ok = true;
+    const float *stat = sStat;
     for (int s = 0; s < steps; ++s) {
-      const int st = s % NS, q0 = (tlo + s % nqt) * 128;
-      const float *stat = sStat + st * 256;
+      const int h = hk * p.group + s / nqt, q0 = (tlo + s % nqt) * 128;
+      {
+        // this step's per-query LSE (log2 units) and Delta; queries past the
+        // sequence get LSE = +inf, so that their probabilities are 0
+        const int i = q0 + r;
+        const int64_t at = (int64_t)h * p.total_q + qs + i;
+        const float lv = i < sq ? __ldg(p.lse + at) * kLog2e : INFINITY;
+        const float dv = i < sq ? __ldg(p.delta + at) : 0.f;
+        named_bar_sync(1, 128);   // the previous step's reads are done
+        sStat[r] = lv;
+        sStat[128 + r] = dv;
+        named_bar_sync(1, 128);
+      }
+      // after a failed wait the loop still runs every step's two barriers
+      // (no warp may leave while the others wait there), skipping the work
+      if (!ok) continue;
       ok = mbar_wait(smem_u32(st_full), s & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
       float pr[128];
 #pragma unroll
@@ -535,21 +572,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(st_read));
-      // the step's statistics were stored by the producer before it armed
-      // this stage's barrier (at most one phase ahead: the stage is reloaded
-      // only after this step's dV/dK)
-      ok = mbar_wait(smem_u32(qd_full + st), (s / NS) & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const bool full = (q0 + 127 < sq) && (kj0 + 127 < sk) && (!p.causal || q0 + off >= kj0 + 127) &&
-                        p.window <= 0;
+      // the key's allowed queries are one interval; as tile columns: [elo, ehi)
+      // (queries past the sequence already have P = 0 through LSE = +inf)
+      const int elo = key_qlo - q0, ehi = key_qhi - q0;
 #pragma unroll
       for (int e = 0; e < 128; ++e) {
-        float x = ex2(fmaf(pr[e], p.scale_log2, -stat[e]));
-        if (!full) x = (key_ok && bwd_allowed(p, q0 + e, j, sq, sk)) ? x : 0.f;
-        pr[e] = x;
+        const float x = ex2(fmaf(pr[e], p.scale_log2, -stat[e]));
+        pr[e] = (e >= elo && e < ehi) ? x : 0.f;
       }
       ok = mbar_wait(smem_u32(dpt_full), s & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
