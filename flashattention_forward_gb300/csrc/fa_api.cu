@@ -773,7 +773,7 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
   dp.total_q = Tq;
   dp.hq = (int)Hq;
   dp.d = (int)D;
-  L.delta_blocks = (unsigned)((Tq * Hq + 7) / 8);
+  L.delta_blocks = (unsigned)((Tq * Hq + 31) / 32);   // 32 rows per 256-thread block
   L.grid_q = dim3((unsigned)p.n_qtiles, (unsigned)Hq, (unsigned)B);
   L.grid_kv = dim3((unsigned)(p.n_ktiles > 0 ? p.n_ktiles : 1), (unsigned)Hkv, (unsigned)B);
   L.stream = (cudaStream_t)stream;

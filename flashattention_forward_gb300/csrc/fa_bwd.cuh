@@ -27,31 +27,45 @@
 
 namespace fa {
 
-// Delta_i = <dO_i, O_i> in fp32, one warp per (token, head) row.
+// Delta_i = <dO_i, O_i> in fp32.  Eight lanes per (token, head) row, each
+// with 16-byte loads of O and dO (D/64 of them), four rows per warp.
 __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const BwdDeltaParams p) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= p.total_q * p.hq) return;
-  const int64_t t = row / p.hq;
-  const int h = (int)(row - t * p.hq);
-  const __nv_bfloat16 *o = p.out + t * p.o_stride_t + (int64_t)h * p.o_stride_h;
-  const __nv_bfloat16 *g = p.dout + t * p.do_stride_t + (int64_t)h * p.do_stride_h;
+  const int64_t row = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * 4 + (lane >> 3);
+  const int sub = lane & 7;
   float acc = 0.f;
-  for (int x = lane * 4; x < p.d; x += 128) {
-    const uint2 ov = *reinterpret_cast<const uint2 *>(o + x);
-    const uint2 gv = *reinterpret_cast<const uint2 *>(g + x);
-    const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
-    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+  const bool live = row < p.total_q * p.hq;
+  if (live) {
+    const int64_t t = row / p.hq;
+    const int h = (int)(row - t * p.hq);
+    const __nv_bfloat16 *o = p.out + t * p.o_stride_t + (int64_t)h * p.o_stride_h;
+    const __nv_bfloat16 *g = p.dout + t * p.do_stride_t + (int64_t)h * p.do_stride_h;
+    uint4 ov[2], gv[2];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float2 a = __bfloat1622float2(o2[e]), b = __bfloat1622float2(g2[e]);
-      acc = fmaf(a.x, b.x, acc);
-      acc = fmaf(a.y, b.y, acc);
-    }
+    for (int c = 0; c < 2; ++c)
+      if (c * 64 + sub * 8 < p.d) {
+        ov[c] = *reinterpret_cast<const uint4 *>(o + c * 64 + sub * 8);
+        gv[c] = *reinterpret_cast<const uint4 *>(g + c * 64 + sub * 8);
+      }
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      if (c * 64 + sub * 8 < p.d) {
+        const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov[c]);
+        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv[c]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = __bfloat1622float2(o2[e]), b = __bfloat1622float2(g2[e]);
+          acc = fmaf(a.x, b.x, acc);
+          acc = fmaf(a.y, b.y, acc);
+        }
+      }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) p.delta[(int64_t)h * p.total_q + t] = acc;
+  for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (live && sub == 0) {
+    const int64_t t = row / p.hq;
+    p.delta[(row - t * p.hq) * p.total_q + t] = acc;
+  }
 }
 
 template <int D>
@@ -126,10 +140,12 @@ __device__ __forceinline__ void bwd_load_tile(uint8_t *dst, const CUtensorMap *t
 }
 
 // ------------------------------------------------------------------- dQ --
-// CTA (query tile, q head, sequence).  TMEM: S [0,128), dP [128,256) with dS
-// (bf16) written over its first 64 columns, dQ [256, 256+D).  Warps 0-3 own
-// the tile's rows (TMEM lanes), warp 4 loads, warp 5 issues the MMAs:
-//   S(0) dP(0) | S(t+1) once S(t) is read | dQ += dS(t) K(t) | dP(t+1)
+// CTA (query tile, q head, sequence).  TMEM: S [0,128), dP [128,256),
+// dQ [256, 256+D), dS (bf16) in two 64-column buffers [384,448), [448,512).
+// Warps 0-3 own the tile's rows (TMEM lanes), warp 4 loads, warp 5 issues:
+//   S(0) dP(0) | S(t+1) once S(t) is read | dP(t+1) once dP(t) is read |
+//   dQ += dS(t) K(t)
+// so the next tile's contractions run while the rows form dS(t).
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -170,8 +186,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + NSK + NSV) * TB);
   uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = k_full + NSK, *v_full = k_empty + NSK,
            *v_empty = v_full + NSV, *s_full = v_empty + NSV, *dp_full = s_full + 1, *s_read = dp_full + 1,
-           *ds_full = s_read + 1, *dq_done = ds_full + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dq_done + 1);
+           *ds_full = s_read + 1, *dq_done = ds_full + 1, *dp_read = dq_done + 1, *ds_free = dp_read + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ds_free + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -188,6 +204,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(smem_u32(s_read), 128);
     mbar_init(smem_u32(ds_full), 128);
     mbar_init(smem_u32(dq_done), 1);
+    mbar_init(smem_u32(dp_read), 128);
+    mbar_init(smem_u32(ds_free), 1);
+    mbar_init(smem_u32(ds_free + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const uint32_t lo_v = (uint32_t)smem_desc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dkmn = smem_desc_sw128(smem_u32(sK), 128 * 128, 1024);
       const uint32_t lo_kmn = (uint32_t)dkmn, hi_kmn = (uint32_t)(dkmn >> 32);
-      const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+      const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256, tD = tmem + 384;
       bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.err);
       if (ok) ok = mbar_wait(smem_u32(k_full), 0, abort_flag, p.err);
       if (ok) {
@@ -263,17 +282,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_rows_rows<D>(tS, lo_q, lo_k + (uint32_t)(nk * (TB >> 4)), hi_k, id_ss);
           tc_commit(smem_u32(s_full));
         }
-        if (!(ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, p.err))) break;
-        tc_fence_after();
-        mma_tmem_rows(tQ, tP, lo_kmn + (uint32_t)(st * (TB >> 4)), hi_kmn, id_dq, t > 0 ? 1u : 0u);
-        tc_commit(smem_u32(k_empty + st));
         if (more) {
+          if (!(ok = mbar_wait(smem_u32(dp_read), t & 1, abort_flag, p.err))) break;
           if (!(ok = mbar_wait(smem_u32(v_full + nv), ((t + 1) / NSV) & 1, abort_flag, p.err))) break;
           tc_fence_after();
           mma_rows_rows<D>(tP, lo_do, lo_v + (uint32_t)(nv * (TB >> 4)), hi_k, id_ss);
           tc_commit(smem_u32(dp_full));
           tc_commit(smem_u32(v_empty + nv));
         }
+        if (!(ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        mma_tmem_rows(tQ, tD + (uint32_t)((t & 1) * 64), lo_kmn + (uint32_t)(st * (TB >> 4)), hi_kmn, id_dq,
+                      t > 0 ? 1u : 0u);
+        tc_commit(smem_u32(k_empty + st));
+        tc_commit(smem_u32(ds_free + (t & 1)));
       }
       tc_commit(smem_u32(dq_done));
     }
@@ -320,17 +342,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ok = mbar_wait(smem_u32(dp_full), t & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      // dS in two halves of 64 columns; once the second half of dP is in
+      // registers the MMA warp may overwrite dP with the next tile's
+      uint32_t ds[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float dp[32];
-        tmem_ld32(rP + c * 32, dp);
+      for (int hf = 0; hf < 2; ++hf) {
+        float dp[64];
+        tmem_ld32(rP + hf * 64, *reinterpret_cast<float(*)[32]>(dp));
+        tmem_ld32(rP + hf * 64 + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
         tmem_wait_ld();
-        uint32_t w[16];
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(dp_read));
+        }
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack_bf16x2(pr[c * 32 + 2 * e] * (dp[2 * e] - delta), pr[c * 32 + 2 * e + 1] * (dp[2 * e + 1] - delta));
-        bwd_tmem_st16(rP + c * 16, w);
+        for (int e = 0; e < 32; ++e)
+          ds[hf * 32 + e] = pack_bf16x2(pr[hf * 64 + 2 * e] * (dp[2 * e] - delta),
+                                        pr[hf * 64 + 2 * e + 1] * (dp[2 * e + 1] - delta));
       }
+      // dS buffer t % 2 was last read by dQ(t - 2)
+      if (t >= 2) {
+        ok = mbar_wait(smem_u32(ds_free + (t & 1)), ((t >> 1) - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const uint32_t rD = tmem + lane_base + 384 + (uint32_t)((t & 1) * 64);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bwd_tmem_st16(rD + c * 16, ds + c * 16);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(ds_full));
@@ -368,13 +406,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 // ----------------------------------------------------------------- dK, dV --
 // CTA (key tile, kv head, sequence); it loops over the q heads of the kv
 // head's group and, for each, over the query tiles that may see its keys.
-// TMEM: S^T [0,128), dP^T [128,256) -- dS^T (bf16) over its first 64 columns,
-// P^T (bf16) over the last 64 -- dV [256, 256+D), dK [384, 384+D).  Warps 0-3
-// own the tile's keys (TMEM lanes) and stage each step's LSE and Delta in
-// shared memory; warp 4 loads K and V once and then Q (three stages) and dO
-// (two stages) per step; warp 5 issues the MMAs:
-//   S^T(0) dP^T(0) | S^T(s+1) once S^T(s) is read | dV += P^T(s) dO(s),
-//   dK += dS^T(s) Q(s) | dP^T(s+1)
+// TMEM: S^T [0,128) with P^T (bf16) written over its last 64 columns once S^T
+// is in registers, dP^T [128,256) with dS^T (bf16) over its first 64, dV
+// [256, 256+D), dK [384, 384+D).  Warps 0-3 own the tile's keys (TMEM lanes)
+// and stage each step's LSE and Delta in shared memory; warp 4 loads K and V
+// once and then Q (three stages) and dO (two stages) per step; warp 5 issues:
+//   S^T(0) dP^T(0) | dV += P^T(s) dO(s) once P^T is stored, S^T(s+1) |
+//   dK += dS^T(s) Q(s) once dS^T is stored, dP^T(s+1)
+// so dV and the next S^T run while the keys' warps form dS^T(s).
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -507,8 +546,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       for (int s = 0; ok && s < steps; ++s) {
         const int sq_ = s % NSQ, so_ = s % NSO, nq = (s + 1) % NSQ, no = (s + 1) % NSO;
         const bool more = s + 1 < steps;
+        // P^T(s) is in S^T's last 64 columns (S^T(s) itself already read)
+        if (!(ok = mbar_wait(smem_u32(st_read), s & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        mma_tmem_rows(tV, tS + 64, lo_domn + (uint32_t)(so_ * (TB >> 4)), hi_mn, id_acc, s > 0 ? 1u : 0u);
+        tc_commit(smem_u32(o_empty + so_));
         if (more) {
-          if (!(ok = mbar_wait(smem_u32(st_read), s & 1, abort_flag, p.err))) break;
           if (!(ok = mbar_wait(smem_u32(q_full + nq), ((s + 1) / NSQ) & 1, abort_flag, p.err))) break;
           tc_fence_after();
           mma_rows_rows<D>(tS, lo_k, lo_q + (uint32_t)(nq * (TB >> 4)), hi, id_ss);
@@ -516,8 +559,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         if (!(ok = mbar_wait(smem_u32(pds_full), s & 1, abort_flag, p.err))) break;
         tc_fence_after();
-        mma_tmem_rows(tV, tP + 64, lo_domn + (uint32_t)(so_ * (TB >> 4)), hi_mn, id_acc, s > 0 ? 1u : 0u);
-        tc_commit(smem_u32(o_empty + so_));
         mma_tmem_rows(tK, tP, lo_qmn + (uint32_t)(sq_ * (TB >> 4)), hi_mn, id_acc, s > 0 ? 1u : 0u);
         tc_commit(smem_u32(q_empty + sq_));
         if (more) {
@@ -546,15 +587,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t rS = tmem + lane_base, rP = tmem + lane_base + 128;
     bool ok = true;
     const float *stat = sStat;
+    // Per-query LSE (log2 units) and Delta of a step, one query per thread;
+    // queries past the sequence get LSE = +inf, so that their P is 0.  Loaded
+    // a step ahead so that the global-load latency stays off the step.
+    auto load_stat = [&](int s, float &lv, float &dv) {
+      const int h = hk * p.group + s / nqt, i = (tlo + s % nqt) * 128 + r;
+      const int64_t at = (int64_t)h * p.total_q + qs + i;
+      lv = i < sq ? __ldg(p.lse + at) * kLog2e : INFINITY;
+      dv = i < sq ? __ldg(p.delta + at) : 0.f;
+    };
+    float lv_next, dv_next;
+    load_stat(0, lv_next, dv_next);
     for (int s = 0; s < steps; ++s) {
-      const int h = hk * p.group + s / nqt, q0 = (tlo + s % nqt) * 128;
+      const int q0 = (tlo + s % nqt) * 128;
       {
-        // this step's per-query LSE (log2 units) and Delta; queries past the
-        // sequence get LSE = +inf, so that their probabilities are 0
-        const int i = q0 + r;
-        const int64_t at = (int64_t)h * p.total_q + qs + i;
-        const float lv = i < sq ? __ldg(p.lse + at) * kLog2e : INFINITY;
-        const float dv = i < sq ? __ldg(p.delta + at) : 0.f;
+        const float lv = lv_next, dv = dv_next;
+        if (s + 1 < steps) load_stat(s + 1, lv_next, dv_next);
         named_bar_sync(1, 128);   // the previous step's reads are done
         sStat[r] = lv;
         sStat[128 + r] = dv;
@@ -570,38 +618,45 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(rS + c * 32, *reinterpret_cast<float(*)[32]>(pr + c * 32));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(smem_u32(st_read));
       // the key's allowed queries are one interval; as tile columns: [elo, ehi)
       // (queries past the sequence already have P = 0 through LSE = +inf)
       const int elo = key_qlo - q0, ehi = key_qhi - q0;
+      // P^T rounded to bf16 at once (the operand of dV += P^T dO; dS^T is
+      // formed from the same rounded values), which halves its registers
+      uint32_t ppk[64];
 #pragma unroll
-      for (int e = 0; e < 128; ++e) {
-        const float x = ex2(fmaf(pr[e], p.scale_log2, -stat[e]));
-        pr[e] = (e >= elo && e < ehi) ? x : 0.f;
+      for (int e = 0; e < 128; e += 2) {
+        const float x0 = ex2(fmaf(pr[e], p.scale_log2, -stat[e]));
+        const float x1 = ex2(fmaf(pr[e + 1], p.scale_log2, -stat[e + 1]));
+        ppk[e >> 1] = pack_bf16x2((e >= elo && e < ehi) ? x0 : 0.f, (e + 1 >= elo && e + 1 < ehi) ? x1 : 0.f);
       }
+      // P^T over S^T's last 64 columns: dV(s) may start
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bwd_tmem_st16(rS + 64 + c * 16, ppk + c * 16);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(st_read));
       ok = mbar_wait(smem_u32(dpt_full), s & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; continue; }
       tc_fence_after();
+      // dS^T in two halves of 64 columns, each read with one wait; half hf
+      // writes dS^T columns [32 hf, 32 hf + 32), all read already
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float dp[32];
-        tmem_ld32(rP + c * 32, dp);
+      for (int hf = 0; hf < 2; ++hf) {
+        float dp[64];
+        tmem_ld32(rP + hf * 64, *reinterpret_cast<float(*)[32]>(dp));
+        tmem_ld32(rP + hf * 64 + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
         tmem_wait_ld();
-        uint32_t w[16];
+        uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = c * 32 + 2 * e;
-          w[e] = pack_bf16x2(pr[q] * (dp[2 * e] - stat[128 + q]), pr[q + 1] * (dp[2 * e + 1] - stat[128 + q + 1]));
+        for (int e = 0; e < 32; ++e) {
+          const int q = hf * 64 + 2 * e;
+          const uint32_t u = ppk[q >> 1];
+          const float p0 = __uint_as_float(u << 16), p1 = __uint_as_float(u & 0xFFFF0000u);
+          w[e] = pack_bf16x2(p0 * (dp[2 * e] - stat[128 + q]), p1 * (dp[2 * e + 1] - stat[128 + q + 1]));
         }
-        bwd_tmem_st16(rP + c * 16, w);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pr[c * 32 + 2 * e], pr[c * 32 + 2 * e + 1]);
-        bwd_tmem_st16(rP + 64 + c * 16, w);
+        bwd_tmem_st16(rP + hf * 32, w);
+        bwd_tmem_st16(rP + hf * 32 + 16, w + 16);
       }
       tmem_wait_st();
       tc_fence_before();
