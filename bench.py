@@ -590,9 +590,10 @@ def profile_only(name, warmup, steps):
                                     name="long_e4m3q"), 0
     elif name.startswith("flex_"):
         p, splits = fi.config5(name[5:]), 0
-    elif name in ("bwd_varlen_noncausal", "bwd_long_causal"):
-        p = fi.config2(causal=False) if name == "bwd_varlen_noncausal" else \
-            fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, causal=True)
+    elif name in ("bwd_varlen_noncausal", "bwd_long_causal", "bwd_mid_noncausal"):
+        p = {"bwd_varlen_noncausal": lambda: fi.config2(causal=False),
+             "bwd_long_causal": lambda: fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, causal=True),
+             "bwd_mid_noncausal": lambda: fi.make_problem([2048] * 4, hq=16, dk=128, seed=3)}[name]()
         splits = "bwd"
     else:
         raise SystemExit(f"unknown workload {name}")
