@@ -495,6 +495,20 @@ def other_workloads(dev, warmup, steps, flush, pk):
     res["paged_decode_64seq_hq32_hkv8_p16"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
                                                "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16, p.total_k),
                                                "bytes": fi.decode_bytes(p)}
+    # the same decode geometry on byte caches (e4m3, int8; per-token scales)
+    for kvd in ("e4m3", "int8"):
+        rng = np.random.default_rng(0)
+        lens_k = [int(x) for x in rng.integers(512, 8193, size=64)]
+        p = fi.make_problem([1] * 64, lens_k, hq=32, hkv=8, dk=128, seed=1, page_size=16, spare_pages=64,
+                            max_pages=512, kv_dtype=kvd, name=f"paged_decode_{kvd}")
+        t = dev_tensors(p, dev)
+        call, n, _, _ = make_call(p, t, num_splits=None)
+        ms = statistics.mean(time_calls([call], warmup, steps, flush))
+        gbs = fi.decode_bytes(p) / (ms * 1e-3) / 1e9
+        res[f"paged_decode_{kvd}_64seq_hq32_hkv8_p16"] = {
+            "ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"], "bytes": fi.decode_bytes(p),
+            "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16, p.total_k)}
+        del t
     # paged e4m3 KV, Q/K 192, V/O 128, page 64, 16 seqs U{1..4096}, causal
     p = fi.config4()
     t = dev_tensors(p, dev)

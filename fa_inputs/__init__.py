@@ -444,8 +444,8 @@ def decode_bytes(p: Problem) -> float:
     esize = 2 if p.kv_dtype == "bf16" else 1
     tok = float(p.seqlens_k.sum())
     kv = tok * p.hkv * (p.dk + p.dv) * esize
-    if p.kv_dtype == "e4m3":
-        kv += tok * p.hkv * 8
+    if p.kv_dtype in ("e4m3", "int8"):
+        kv += tok * p.hkv * 8           # one fp32 k and v scale per token and kv head
     qo = p.total_q * p.hq * (p.dk * 2 + p.dv * 2 + 4)
     pages = sum(int(math.ceil(s / p.page_size)) for s in p.seqlens_k) * 4 if p.paged else 0
     return kv + qo + pages

@@ -441,13 +441,30 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if ((int64_t)launch->max_seqlen_q * group > fa::kDecRows)
       return fail(FA_ERR_UNSUPPORTED, "split-KV needs max_seqlen_q * Hq/Hkv <= %d", fa::kDecRows);
     if (Dk != Dv || (Dk != 64 && Dk != 128)) return fail(FA_ERR_UNSUPPORTED, "split-KV supports Dk = Dv in {64, 128}");
-    if (fp8) return fail(FA_ERR_UNSUPPORTED, "split-KV runs on bf16 caches; use num_splits = 0 for e4m3/int8");
     if (mod != 0 || block_mask) return fail(FA_ERR_UNSUPPORTED, "split-KV does not take score mods or block masks");
     if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "too many sequences or kv heads for split-KV");
     fa::DecodeLaunch L;
     memset(&L, 0, sizeof L);
+    L.kv = kv_dt == FA_E4M3 ? 1 : (kv_dt == FA_I8 ? 2 : 0);
     const int rows_box = paged ? (page_size < fa::kDecStageKeys ? page_size : fa::kDecStageKeys) : fa::kDecStageKeys;
-    if (have_keys) {
+    if (have_keys && fp8) {
+      // byte caches: one box per page piece, all D bytes of a key, unswizzled
+      if (paged) {
+        const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
+        const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
+        const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2]), (uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
+        const uint32_t box[4] = {(uint32_t)Dk, 1, (uint32_t)rows_box, 1};
+        if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, box, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+        if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dk, sv, box, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+      } else {
+        const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)k_cache->shape[0]};
+        const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
+        const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
+        const uint32_t box[3] = {(uint32_t)Dk, 1, (uint32_t)rows_box};
+        if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, box, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+        if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dk, sv, box, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+      }
+    } else if (have_keys) {
       if (paged) {
         const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
         const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2] * esz), (uint64_t)(k_cache->stride[1] * esz), (uint64_t)(k_cache->stride[0] * esz)};
@@ -493,6 +510,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.out_stride_h = out->stride[1];
     p.lse = lse ? (float *)lse->data : nullptr;
     p.err = error_word();
+    p.k_scale = fp8 ? (const float *)k_scale->data : nullptr;
+    p.v_scale = fp8 ? (const float *)v_scale->data : nullptr;
     if (S > 1) {
       const size_t need = fa_fwd_workspace_bytes((int)B, Tq, (int)Hq, (int)Dv, S);
       if (!launch->workspace || launch->workspace_bytes < need)

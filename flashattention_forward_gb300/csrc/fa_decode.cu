@@ -3,20 +3,27 @@
 
 namespace fa {
 
-template <int D>
+template <int D, int KV>
 static cudaError_t launch_decode_d(const DecodeLaunch &L) {
   static unsigned long long done = 0;
-  auto kern = fa_decode_kernel<D>;
-  cudaError_t e = ensure_smem_attr(kern, DecodeCfg<D>::kSmemBytes, &done);
+  auto kern = fa_decode_kernel<D, KV>;
+  cudaError_t e = ensure_smem_attr(kern, DecodeCfg<D, KV>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, kDecThreads, DecodeCfg<D>::kSmemBytes, L.stream>>>(L.tm_k, L.tm_v, L.p);
+  kern<<<L.grid, kDecThreads, DecodeCfg<D, KV>::kSmemBytes, L.stream>>>(L.tm_k, L.tm_v, L.p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(int d, const DecodeLaunch &L) {
-  if (d == 64) return launch_decode_d<64>(L);
-  if (d == 128) return launch_decode_d<128>(L);
+template <int KV>
+static cudaError_t launch_decode_kv(int d, const DecodeLaunch &L) {
+  if (d == 64) return launch_decode_d<64, KV>(L);
+  if (d == 128) return launch_decode_d<128, KV>(L);
   return cudaErrorNotSupported;
+}
+
+cudaError_t launch_decode(int d, const DecodeLaunch &L) {
+  if (L.kv == 1) return launch_decode_kv<1>(d, L);
+  if (L.kv == 2) return launch_decode_kv<2>(d, L);
+  return launch_decode_kv<0>(d, L);
 }
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,

@@ -15,8 +15,18 @@
 // finalising m_max*ln2 + ln(den); FlyDSL PR #1066 lists split-K/combine as
 // the long-KV decode form).  With a single split the kernel writes the final
 // bf16 output and LSE itself.
+//
+// Byte caches (KV = 1: e4m3, KV = 2: int8; per-token scales, fkl_python PR #7:
+// fp8 KV decode from the raw quantised bytes, half the traffic of bf16).  TMA
+// lands the bytes, the producer lanes copy the stage's per-token k/v scales
+// with cp.async beside them, and each consumer warp turns its own 16 keys into
+// f16 exactly (e4m3 and int8 values are f16 numbers) in a private swizzled
+// buffer.  Q is brought to f16 with a per-row power-of-two factor.  The scales
+// stay in fp32: k_scale multiplies each score column, v_scale each P column
+// before the f16 P V product, so the cached values are never rounded.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sm103_ptx.cuh"
 
@@ -48,18 +58,27 @@ struct DecodeParams {
   int64_t out_stride_t, out_stride_h;
   float *lse;                         // [Hq, T_q] or null
   int *err;                           // device error word
+  const float *k_scale, *v_scale;     // byte caches: per (token, kv head), in the cache's token order
 };
 
-template <int D>
+template <int D, int KV = 0>
 struct DecodeCfg {
-  static constexpr int kKBytes = kDecStageKeys * D * 2;   // per stage
-  static constexpr int kVBytes = kDecStageKeys * D * 2;
-  static constexpr int kStageBytes = kKBytes + kVBytes;
+  static constexpr int kElt = KV ? 1 : 2;                  // cache bytes per element
+  static constexpr int kKBytes = kDecStageKeys * D * kElt;   // per stage
+  static constexpr int kVBytes = kDecStageKeys * D * kElt;
+  static constexpr int kScaleBytes = KV ? 2 * kDecStageKeys * 4 : 0;   // k then v scales of the stage
+  static constexpr int kStageBytes = kKBytes + kVBytes + kScaleBytes;
   static constexpr int kOffStages = 0;
-  static constexpr int kOffQ = kDecStages * kStageBytes;      // 16 x D bf16
-  static constexpr int kOffBar = kOffQ + kDecRows * D * 2;
+  // byte caches: per consumer warp, its 16 keys of K and V as swizzled f16
+  static constexpr int kConvWarpBytes = KV ? 2 * 16 * D * 2 : 0;
+  static constexpr int kOffConv = ((kDecStages * kStageBytes + 1023) / 1024) * 1024;
+  static constexpr int kOffQ = kOffConv + kDecWarps * kConvWarpBytes;   // 16 x D bf16 (f16 for byte caches)
+  static constexpr int kOffQInv = kOffQ + kDecRows * D * 2;            // byte caches: 2^-e per Q row
+  static constexpr int kOffBar = kOffQInv + kDecRows * 4;
   static constexpr int kOffMisc = kOffBar + 2 * kDecStages * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+  static_assert(kDecStages * kStageBytes >= kDecWarps * kDecRows * D * 4 + kDecWarps * kDecRows * 8,
+                "the stage ring doubles as the cross-warp reduction buffer");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -79,17 +98,55 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <int KV>
+__device__ __forceinline__ void dec_mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (KV) mma_f16_16816(c, a, b0, b1);
+  else mma_bf16_16816(c, a, b0, b1);
+}
+
+// 4-byte global -> shared copy; `bytes` 0 writes zeros and reads nothing.
+__device__ __forceinline__ void dec_cp_async_4(uint32_t dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+// One arrival on `bar` once this thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void dec_cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Four cache bytes -> four f16 values (two packed pairs), exactly: e4m3 by the
+// hardware conversion, int8 through the fp32 2^23 + (x + 128) - (2^23 + 128).
+template <int KV>
+__device__ __forceinline__ void dec_bytes4_to_f16(uint32_t w, uint32_t &o0, uint32_t &o1) {
+  if constexpr (KV == 1) {
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(o0) : "r"(w & 0xFFFFu));
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(o1) : "r"(w >> 16));
+  } else {
+    const uint32_t u = w ^ 0x80808080u;
+    const float a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.f;
+    const float b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.f;
+    const float c = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.f;
+    const float d = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.f;
+    o0 = pack_f16x2(a, b);
+    o1 = pack_f16x2(c, d);
+  }
+}
 
 // Byte offset of (row, 16-byte chunk) in a 128-byte-swizzled [rows x 64] bf16 block.
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
+template <int D, int KV = 0>
 __global__ void __launch_bounds__(kDecThreads, 2)
     fa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p) {
-  using Cfg = DecodeCfg<D>;
+  using Cfg = DecodeCfg<D, KV>;
   constexpr int NCB = D / 64;          // 64-dim column blocks
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -132,24 +189,57 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   uint64_t *empty = full + kDecStages;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc);
 
+  float *sQinv = reinterpret_cast<float *>(smem + Cfg::kOffQInv);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kDecStages; ++s) {
-      mbar_init(smem_u32(full + s), 1);
+      // byte caches: the producer's arrival plus one cp.async arrival per lane (scales)
+      mbar_init(smem_u32(full + s), KV ? 1 + 32 : 1);
       mbar_init(smem_u32(empty + s), kDecWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // Q rows -> shared memory (zero rows past `rows`), plain layout [16][D].
-  for (int e = threadIdx.x; e < kDecRows * D / 8; e += blockDim.x) {
-    const int r = e / (D / 8), c8 = e % (D / 8);
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (r < rows) {
-      const int tq = r / p.group, h = hk * p.group + r % p.group;
-      const __nv_bfloat16 *src = p.q + (int64_t)(qa + tq) * p.q_stride_t + (int64_t)h * p.q_stride_h + c8 * 8;
-      val = *reinterpret_cast<const uint4 *>(src);
+  if constexpr (KV == 0) {
+    // Q rows -> shared memory (zero rows past `rows`), plain layout [16][D].
+    for (int e = threadIdx.x; e < kDecRows * D / 8; e += blockDim.x) {
+      const int r = e / (D / 8), c8 = e % (D / 8);
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (r < rows) {
+        const int tq = r / p.group, h = hk * p.group + r % p.group;
+        const __nv_bfloat16 *src = p.q + (int64_t)(qa + tq) * p.q_stride_t + (int64_t)h * p.q_stride_h + c8 * 8;
+        val = *reinterpret_cast<const uint4 *>(src);
+      }
+      *reinterpret_cast<uint4 *>(sQ + r * D + c8 * 8) = val;
     }
-    *reinterpret_cast<uint4 *>(sQ + r * D + c8 * 8) = val;
+  } else {
+    // Q rows as f16 with a per-row factor 2^e, max|q| * 2^e in [2^14, 2^15):
+    // every bf16 element within 2^-24 of the row maximum is exact in f16.
+    // One warp per row, D/32 elements per lane; 2^-e is kept for the scores.
+    for (int r = warp; r < kDecRows; r += kDecWarps + 1) {
+      constexpr int kPer = D / 32;
+      float v[kPer];
+      float mx = 0.f;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) v[e] = 0.f;
+      if (r < rows) {
+        const int tq = r / p.group, h = hk * p.group + r % p.group;
+        const __nv_bfloat16 *src = p.q + (int64_t)(qa + tq) * p.q_stride_t + (int64_t)h * p.q_stride_h + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          v[e] = __bfloat162float(src[e]);
+          mx = fmaxf(mx, fabsf(v[e]));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      int ex = 0;
+      if (mx > 0.f) ex = 14 - ilogbf(mx);        // mx * 2^ex in [2^14, 2^15)
+      const float f = ldexpf(1.f, ex);
+      __half *dst = reinterpret_cast<__half *>(sQ) + r * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) dst[e] = __float2half_rn(v[e] * f);
+      if (lane == 0) sQinv[r] = ldexpf(1.f, -ex);
+    }
   }
   __syncthreads();
 
@@ -170,11 +260,43 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       const int slot_i = it % kDecStages;
       if (lane == 0) {
         if (it >= kDecStages) ok = mbar_wait(smem_u32(empty + slot_i), ((it / kDecStages) - 1) & 1, abort_flag, p.err);
-        if (ok) mbar_expect_tx(smem_u32(full + slot_i), Cfg::kStageBytes);
+        if (ok) mbar_expect_tx(smem_u32(full + slot_i), Cfg::kKBytes + Cfg::kVBytes);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
       uint8_t *vd = kd + Cfg::kKBytes;
+      if constexpr (KV) {
+        // the stage's k and v scales (keys lane and lane + 32) beside the bytes
+        const uint32_t sdst = smem_u32(vd + Cfg::kVBytes);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int kk = lane + 32 * u;
+          const int key = key_lo + st * kDecStageKeys + kk;
+          const bool live = key < sk;
+          int64_t tok = 0;
+          if (live) tok = bt ? (int64_t)__ldg(bt + (key >> p.page_shift)) * p.page_size + (key & (p.page_size - 1))
+                             : (int64_t)krow0 + key;
+          const int64_t at = tok * p.hkv + hk;
+          dec_cp_async_4(sdst + 4 * kk, live ? p.k_scale + at : p.k_scale, live ? 4u : 0u);
+          dec_cp_async_4(sdst + 4 * (kDecStageKeys + kk), live ? p.v_scale + at : p.v_scale, live ? 4u : 0u);
+        }
+        dec_cp_async_arrive_noinc(smem_u32(full + slot_i));
+        // one box per page piece: rows_per_box keys x D bytes, unswizzled
+        for (int bx = lane; bx < p.boxes_per_stage; bx += 32) {
+          const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
+          const uint32_t off = bx * p.rows_per_box * D;
+          if (bt) {
+            const int page = key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+            const int slot = key0 & (p.page_size - 1);
+            tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, hk, slot, page);
+            tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, hk, slot, page);
+          } else {
+            tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, hk, krow0 + key0);
+            tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, hk, krow0 + key0);
+          }
+        }
+        continue;
+      }
       for (int bx = lane; bx < p.boxes_per_stage; bx += 32) {
         const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
         if (bt) {
@@ -214,6 +336,11 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int r0 = lane >> 2, r1 = r0 + 8;
     const int ip0 = (r0 / p.group) + sk - sq;   // bottom-right aligned positions
     const int ip1 = (r1 / p.group) + sk - sq;
+    // byte caches: Q rows carry a factor 2^e that the score scale removes
+    const float sc0 = KV ? p.scale_log2 * sQinv[r0] : p.scale_log2;
+    const float sc1 = KV ? p.scale_log2 * sQinv[r1] : p.scale_log2;
+    uint8_t *convK = smem + Cfg::kOffConv + warp * Cfg::kConvWarpBytes;   // byte caches only
+    uint8_t *convV = convK + Cfg::kConvWarpBytes / 2;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[D / 8][4];
 #pragma unroll
@@ -229,8 +356,50 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       uint8_t *vd = kd + Cfg::kKBytes;
       const int kw0 = warp * 16;                               // this warp's 16 keys in the stage
       const int key_base = key_lo + st * kDecStageKeys + kw0;  // sequence-local key of row kw0
+      float ksc[2][2], vsc[2][2];                              // byte caches: scales of the lane's 4 keys
+      if constexpr (KV) {
+        // This warp's 16 keys of K and V -> f16 in its private swizzled
+        // buffer; two lanes per key, D/2 bytes each.  Keys at or past key_hi
+        // become zeros (their bytes may be anything, NaN included).
+        const int lr = lane >> 1, hh = lane & 1;
+        const bool live = key_base + lr < key_hi;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint8_t *src = (which ? vd : kd) + (kw0 + lr) * D + hh * (D / 2);
+          uint8_t *dst = which ? convV : convK;
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {          // 16 source bytes -> 16 f16 (two chunks)
+            const uint4 raw = live ? *reinterpret_cast<const uint4 *>(src + q4 * 16) : make_uint4(0, 0, 0, 0);
+            uint32_t h[8];
+            dec_bytes4_to_f16<KV>(raw.x, h[0], h[1]);
+            dec_bytes4_to_f16<KV>(raw.y, h[2], h[3]);
+            dec_bytes4_to_f16<KV>(raw.z, h[4], h[5]);
+            dec_bytes4_to_f16<KV>(raw.w, h[6], h[7]);
+            const int c0 = hh * (D / 2) + q4 * 16;        // first element of the 16
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int c = c0 + half * 8;
+              const int cb = c >> 6, ch = (c & 63) >> 3;
+              *reinterpret_cast<uint4 *>(dst + cb * 16 * 128 + sw128(lr, ch)) =
+                  make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+            }
+          }
+        }
+        const float *sct = reinterpret_cast<const float *>(vd + Cfg::kVBytes);
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = kw0 + n * 8 + (lane & 3) * 2 + e;
+            ksc[n][e] = sct[col];
+            vsc[n][e] = sct[kDecStageKeys + col];
+          }
+        __syncwarp();
+        // the stage's bytes and scales are no longer needed by this warp
+        if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
+      }
       // Clear V rows of keys outside [key_lo, key_hi) (0 * NaN would be NaN).
-      if (key_base + 16 > key_hi) {
+      if (KV == 0 && key_base + 16 > key_hi) {
         for (int e = lane; e < 16 * NCB * 8; e += 32) {
           const int rr = e / (NCB * 8), rest = e % (NCB * 8);
           const int cb = rest / 8, ch = rest % 8;
@@ -247,13 +416,15 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         // matrices: (keys 0-7, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 0-7), (keys 8-15, dims 8-15)
-        const int krow = kw0 + (lane & 7) + (lane >> 4) * 8;
+        const int krow = (lane & 7) + (lane >> 4) * 8;   // key within the warp's 16
         const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
         const int cb = dim >> 6, ch = (dim & 63) >> 3;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(kd + cb * kDecStageKeys * 128) + sw128(krow, ch), b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qf[ks], b0, b1);
-        mma_bf16_16816(s[1], qf[ks], b2, b3);
+        const uint32_t kaddr = KV ? smem_u32(convK + cb * 16 * 128) + sw128(krow, ch)
+                                  : smem_u32(kd + cb * kDecStageKeys * 128) + sw128(kw0 + krow, ch);
+        ldsm_x4(kaddr, b0, b1, b2, b3);
+        dec_mma<KV>(s[0], qf[ks], b0, b1);
+        dec_mma<KV>(s[1], qf[ks], b2, b3);
       }
       // Scale, mask, online softmax for rows r0 and r1.
       float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -269,8 +440,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             if (p.causal) { ok0 = ok0 && ip0 - j < p.window; ok1 = ok1 && ip1 - j < p.window; }
             else { ok0 = ok0 && abs(ip0 - j) < p.window; ok1 = ok1 && abs(ip1 - j) < p.window; }
           }
-          s[n][e] = ok0 ? s[n][e] * p.scale_log2 : -INFINITY;
-          s[n][2 + e] = ok1 ? s[n][2 + e] * p.scale_log2 : -INFINITY;
+          const float kf = KV ? ksc[n][e] : 1.f;   // per-key scale of a byte cache
+          s[n][e] = ok0 ? s[n][e] * kf * sc0 : -INFINITY;
+          s[n][2 + e] = ok1 ? s[n][2 + e] * kf * sc1 : -INFINITY;
           mx0 = fmaxf(mx0, s[n][e]);
           mx1 = fmaxf(mx1, s[n][2 + e]);
         }
@@ -305,24 +477,34 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         o[n][3] *= a1;
       }
       uint32_t pa[4];
-      pa[0] = pack_bf16x2(ps[0][0], ps[0][1]);
-      pa[1] = pack_bf16x2(ps[0][2], ps[0][3]);
-      pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
-      pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
+      if constexpr (KV) {
+        // P times the keys' v scales (f16; the row sums above use P itself)
+        pa[0] = pack_f16x2(ps[0][0] * vsc[0][0], ps[0][1] * vsc[0][1]);
+        pa[1] = pack_f16x2(ps[0][2] * vsc[0][0], ps[0][3] * vsc[0][1]);
+        pa[2] = pack_f16x2(ps[1][0] * vsc[1][0], ps[1][1] * vsc[1][1]);
+        pa[3] = pack_f16x2(ps[1][2] * vsc[1][0], ps[1][3] * vsc[1][1]);
+      } else {
+        pa[0] = pack_bf16x2(ps[0][0], ps[0][1]);
+        pa[1] = pack_bf16x2(ps[0][2], ps[0][3]);
+        pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
+        pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
+      }
       // O += P V : D/8 n-tiles of 8 dims, one k-step of 16 keys.
 #pragma unroll
       for (int nd = 0; nd < D / 16; ++nd) {
         // matrices: (keys 0-7, dims 0-7), (keys 8-15, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 8-15)
-        const int krow = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // key within the warp's 16
         const int dim = nd * 16 + (lane >> 4) * 8;
         const int cb = dim >> 6, ch = (dim & 63) >> 3;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(vd + cb * kDecStageKeys * 128) + sw128(krow, ch), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * nd], pa, b0, b1);
-        mma_bf16_16816(o[2 * nd + 1], pa, b2, b3);
+        const uint32_t vaddr = KV ? smem_u32(convV + cb * 16 * 128) + sw128(krow, ch)
+                                  : smem_u32(vd + cb * kDecStageKeys * 128) + sw128(kw0 + krow, ch);
+        ldsm_x4_t(vaddr, b0, b1, b2, b3);
+        dec_mma<KV>(o[2 * nd], pa, b0, b1);
+        dec_mma<KV>(o[2 * nd + 1], pa, b2, b3);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
+      if (KV == 0 && lane == 0) mbar_arrive(smem_u32(empty + slot_i));
     }
 
     // Reduce l over the quad (the 4 lanes sharing a row).

@@ -25,6 +25,7 @@ struct PrefillLaunch {
 struct DecodeLaunch {
   CUtensorMap tm_k, tm_v;
   DecodeParams p;
+  int kv;        // cache: 0 bf16, 1 e4m3, 2 int8 (the last two with per-token scales)
   dim3 grid;
   cudaStream_t stream;
 };
