@@ -68,16 +68,19 @@ struct DecodeCfg {
   static constexpr int kVBytes = kDecStageKeys * D * kElt;
   static constexpr int kScaleBytes = KV ? 2 * kDecStageKeys * 4 : 0;   // k then v scales of the stage
   static constexpr int kStageBytes = kKBytes + kVBytes + kScaleBytes;
+  // byte caches: a deeper ring of half-size stages keeps as many bytes in
+  // flight as the bf16 ring does
+  static constexpr int NST = KV ? 5 : kDecStages;
   static constexpr int kOffStages = 0;
-  // byte caches: per consumer warp, its 16 keys of K and V as swizzled f16
-  static constexpr int kConvWarpBytes = KV ? 2 * 16 * D * 2 : 0;
-  static constexpr int kOffConv = ((kDecStages * kStageBytes + 1023) / 1024) * 1024;
+  // byte caches: per consumer warp, its 16 keys of K, then of V, as swizzled f16
+  static constexpr int kConvWarpBytes = KV ? 16 * D * 2 : 0;
+  static constexpr int kOffConv = ((NST * kStageBytes + 1023) / 1024) * 1024;
   static constexpr int kOffQ = kOffConv + kDecWarps * kConvWarpBytes;   // 16 x D bf16 (f16 for byte caches)
   static constexpr int kOffQInv = kOffQ + kDecRows * D * 2;            // byte caches: 2^-e per Q row
   static constexpr int kOffBar = kOffQInv + kDecRows * 4;
-  static constexpr int kOffMisc = kOffBar + 2 * kDecStages * 8;
+  static constexpr int kOffMisc = kOffBar + 2 * NST * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;
-  static_assert(kDecStages * kStageBytes >= kDecWarps * kDecRows * D * 4 + kDecWarps * kDecRows * 8,
+  static_assert(NST * kStageBytes >= kDecWarps * kDecRows * D * 4 + kDecWarps * kDecRows * 8,
                 "the stage ring doubles as the cross-warp reduction buffer");
 };
 
@@ -186,12 +189,13 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   uint8_t *stages = smem + Cfg::kOffStages;
   __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + Cfg::kOffQ);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
-  uint64_t *empty = full + kDecStages;
+  constexpr int NST = Cfg::NST;
+  uint64_t *empty = full + NST;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc);
 
   float *sQinv = reinterpret_cast<float *>(smem + Cfg::kOffQInv);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       // byte caches: the producer's arrival plus one cp.async arrival per lane (scales)
       mbar_init(smem_u32(full + s), KV ? 1 + 32 : 1);
       mbar_init(smem_u32(empty + s), kDecWarps);
@@ -254,12 +258,32 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
     const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
     const int krow0 = __ldg(p.cu_k + b);
+    // Page ids are read one stage ahead, so that the block-table latency
+    // overlaps the wait for a free stage.  Lane bx < boxes_per_stage (<= 4,
+    // pages of 16 keys or more) owns box bx; with byte caches lane l also
+    // copies the scales of keys l and l + 32.
+    auto box_page = [&](int st) -> int {
+      if (!bt || lane >= p.boxes_per_stage || st >= n_stages) return -1;
+      const int key0 = key_lo + st * kDecStageKeys + lane * p.rows_per_box;
+      return key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
+    };
+    auto scale_page = [&](int st, int u) -> int {
+      if (!KV || !bt || st >= n_stages) return 0;
+      const int key = key_lo + st * kDecStageKeys + lane + 32 * u;
+      return key < sk ? __ldg(bt + (key >> p.page_shift)) : 0;
+    };
+    int pg_next = box_page(first_stage);
+    int sp_next[2] = {scale_page(first_stage, 0), scale_page(first_stage, 1)};
     bool ok = true;
     for (int st = first_stage; st < n_stages; ++st) {
       const int it = st - first_stage;
-      const int slot_i = it % kDecStages;
+      const int slot_i = it % NST;
+      const int pg = pg_next, sp[2] = {sp_next[0], sp_next[1]};
+      pg_next = box_page(st + 1);
+      sp_next[0] = scale_page(st + 1, 0);
+      sp_next[1] = scale_page(st + 1, 1);
       if (lane == 0) {
-        if (it >= kDecStages) ok = mbar_wait(smem_u32(empty + slot_i), ((it / kDecStages) - 1) & 1, abort_flag, p.err);
+        if (it >= NST) ok = mbar_wait(smem_u32(empty + slot_i), ((it / NST) - 1) & 1, abort_flag, p.err);
         if (ok) mbar_expect_tx(smem_u32(full + slot_i), Cfg::kKBytes + Cfg::kVBytes);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -273,47 +297,38 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           const int kk = lane + 32 * u;
           const int key = key_lo + st * kDecStageKeys + kk;
           const bool live = key < sk;
-          int64_t tok = 0;
-          if (live) tok = bt ? (int64_t)__ldg(bt + (key >> p.page_shift)) * p.page_size + (key & (p.page_size - 1))
-                             : (int64_t)krow0 + key;
+          const int64_t tok = bt ? (int64_t)sp[u] * p.page_size + (key & (p.page_size - 1)) : (int64_t)krow0 + key;
           const int64_t at = tok * p.hkv + hk;
           dec_cp_async_4(sdst + 4 * kk, live ? p.k_scale + at : p.k_scale, live ? 4u : 0u);
           dec_cp_async_4(sdst + 4 * (kDecStageKeys + kk), live ? p.v_scale + at : p.v_scale, live ? 4u : 0u);
         }
         dec_cp_async_arrive_noinc(smem_u32(full + slot_i));
-        // one box per page piece: rows_per_box keys x D bytes, unswizzled
-        for (int bx = lane; bx < p.boxes_per_stage; bx += 32) {
-          const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
+      }
+      if (lane < p.boxes_per_stage) {
+        const int bx = lane;
+        const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
+        const int slot = key0 & (p.page_size - 1);
+        if constexpr (KV) {
+          // one box per page piece: rows_per_box keys x D bytes, unswizzled
           const uint32_t off = bx * p.rows_per_box * D;
           if (bt) {
-            const int page = key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
-            const int slot = key0 & (p.page_size - 1);
-            tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, hk, slot, page);
-            tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, hk, slot, page);
+            tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, hk, slot, pg);
+            tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, hk, slot, pg);
           } else {
             tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, hk, krow0 + key0);
             tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, hk, krow0 + key0);
-          }
-        }
-        continue;
-      }
-      for (int bx = lane; bx < p.boxes_per_stage; bx += 32) {
-        const int key0 = key_lo + st * kDecStageKeys + bx * p.rows_per_box;
-        if (bt) {
-          const int page = key0 < sk ? __ldg(bt + (key0 >> p.page_shift)) : -1;
-          const int slot = key0 & (p.page_size - 1);
-#pragma unroll
-          for (int cb = 0; cb < NCB; ++cb) {
-            const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
-            tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, slot, page);
-            tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, slot, page);
           }
         } else {
 #pragma unroll
           for (int cb = 0; cb < NCB; ++cb) {
             const uint32_t off = cb * kDecStageKeys * 128 + bx * p.rows_per_box * 128;
-            tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
-            tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
+            if (bt) {
+              tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, slot, pg);
+              tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, slot, pg);
+            } else {
+              tma_load_3d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
+              tma_load_3d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), cb * 64, hk, krow0 + key0);
+            }
           }
         }
       }
@@ -339,8 +354,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     // byte caches: Q rows carry a factor 2^e that the score scale removes
     const float sc0 = KV ? p.scale_log2 * sQinv[r0] : p.scale_log2;
     const float sc1 = KV ? p.scale_log2 * sQinv[r1] : p.scale_log2;
-    uint8_t *convK = smem + Cfg::kOffConv + warp * Cfg::kConvWarpBytes;   // byte caches only
-    uint8_t *convV = convK + Cfg::kConvWarpBytes / 2;
+    uint8_t *conv = smem + Cfg::kOffConv + warp * Cfg::kConvWarpBytes;   // byte caches only
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[D / 8][4];
 #pragma unroll
@@ -349,42 +363,42 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     bool ok = true;
     for (int st = first_stage; st < n_stages; ++st) {
       const int it = st - first_stage;
-      const int slot_i = it % kDecStages;
-      ok = mbar_wait(smem_u32(full + slot_i), (it / kDecStages) & 1, abort_flag, p.err);
+      const int slot_i = it % NST;
+      ok = mbar_wait(smem_u32(full + slot_i), (it / NST) & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
       uint8_t *vd = kd + Cfg::kKBytes;
       const int kw0 = warp * 16;                               // this warp's 16 keys in the stage
       const int key_base = key_lo + st * kDecStageKeys + kw0;  // sequence-local key of row kw0
       float ksc[2][2], vsc[2][2];                              // byte caches: scales of the lane's 4 keys
-      if constexpr (KV) {
-        // This warp's 16 keys of K and V -> f16 in its private swizzled
-        // buffer; two lanes per key, D/2 bytes each.  Keys at or past key_hi
-        // become zeros (their bytes may be anything, NaN included).
-        const int lr = lane >> 1, hh = lane & 1;
-        const bool live = key_base + lr < key_hi;
+      // byte caches: this warp's 16 keys (16 x D bytes) -> f16 in its private
+      // swizzled buffer, K first and V after the QK product.  Each pass, the
+      // 32 lanes read 512 consecutive bytes (16 per lane, no bank conflicts);
+      // keys at or past key_hi become zeros (their bytes may be anything).
+      auto convert = [&](const uint8_t *src) {
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint8_t *src = (which ? vd : kd) + (kw0 + lr) * D + hh * (D / 2);
-          uint8_t *dst = which ? convV : convK;
+        for (int ps_ = 0; ps_ < D / 32; ++ps_) {
+          const int off = ps_ * 512 + lane * 16;
+          const int lr = off / D, c0 = off % D;             // key within the 16, first element
+          const bool live = key_base + lr < key_hi;
+          const uint4 raw = live ? *reinterpret_cast<const uint4 *>(src + kw0 * D + off) : make_uint4(0, 0, 0, 0);
+          uint32_t h[8];
+          dec_bytes4_to_f16<KV>(raw.x, h[0], h[1]);
+          dec_bytes4_to_f16<KV>(raw.y, h[2], h[3]);
+          dec_bytes4_to_f16<KV>(raw.z, h[4], h[5]);
+          dec_bytes4_to_f16<KV>(raw.w, h[6], h[7]);
 #pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {          // 16 source bytes -> 16 f16 (two chunks)
-            const uint4 raw = live ? *reinterpret_cast<const uint4 *>(src + q4 * 16) : make_uint4(0, 0, 0, 0);
-            uint32_t h[8];
-            dec_bytes4_to_f16<KV>(raw.x, h[0], h[1]);
-            dec_bytes4_to_f16<KV>(raw.y, h[2], h[3]);
-            dec_bytes4_to_f16<KV>(raw.z, h[4], h[5]);
-            dec_bytes4_to_f16<KV>(raw.w, h[6], h[7]);
-            const int c0 = hh * (D / 2) + q4 * 16;        // first element of the 16
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int c = c0 + half * 8;
-              const int cb = c >> 6, ch = (c & 63) >> 3;
-              *reinterpret_cast<uint4 *>(dst + cb * 16 * 128 + sw128(lr, ch)) =
-                  make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
-            }
+          for (int half = 0; half < 2; ++half) {
+            const int c = c0 + half * 8;
+            const int cb = c >> 6, ch = (c & 63) >> 3;
+            *reinterpret_cast<uint4 *>(conv + cb * 16 * 128 + sw128(lr, ch)) =
+                make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
           }
         }
+        __syncwarp();
+      };
+      if constexpr (KV) {
+        convert(kd);
         const float *sct = reinterpret_cast<const float *>(vd + Cfg::kVBytes);
 #pragma unroll
         for (int n = 0; n < 2; ++n)
@@ -394,9 +408,6 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             ksc[n][e] = sct[col];
             vsc[n][e] = sct[kDecStageKeys + col];
           }
-        __syncwarp();
-        // the stage's bytes and scales are no longer needed by this warp
-        if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
       }
       // Clear V rows of keys outside [key_lo, key_hi) (0 * NaN would be NaN).
       if (KV == 0 && key_base + 16 > key_hi) {
@@ -420,7 +431,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
         const int cb = dim >> 6, ch = (dim & 63) >> 3;
         uint32_t b0, b1, b2, b3;
-        const uint32_t kaddr = KV ? smem_u32(convK + cb * 16 * 128) + sw128(krow, ch)
+        const uint32_t kaddr = KV ? smem_u32(conv + cb * 16 * 128) + sw128(krow, ch)
                                   : smem_u32(kd + cb * kDecStageKeys * 128) + sw128(kw0 + krow, ch);
         ldsm_x4(kaddr, b0, b1, b2, b3);
         dec_mma<KV>(s[0], qf[ks], b0, b1);
@@ -489,6 +500,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
         pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
       }
+      if constexpr (KV) {
+        __syncwarp();                 // the QK product has read K from the buffer
+        convert(vd);
+        // the stage's bytes and scales are no longer needed by this warp
+        if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
+      }
       // O += P V : D/8 n-tiles of 8 dims, one k-step of 16 keys.
 #pragma unroll
       for (int nd = 0; nd < D / 16; ++nd) {
@@ -497,7 +514,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const int dim = nd * 16 + (lane >> 4) * 8;
         const int cb = dim >> 6, ch = (dim & 63) >> 3;
         uint32_t b0, b1, b2, b3;
-        const uint32_t vaddr = KV ? smem_u32(convV + cb * 16 * 128) + sw128(krow, ch)
+        const uint32_t vaddr = KV ? smem_u32(conv + cb * 16 * 128) + sw128(krow, ch)
                                   : smem_u32(vd + cb * kDecStageKeys * 128) + sw128(kw0 + krow, ch);
         ldsm_x4_t(vaddr, b0, b1, b2, b3);
         dec_mma<KV>(o[2 * nd], pa, b0, b1);
