@@ -186,7 +186,8 @@ def make_bwd_call(p, t):
     dev = t["q"].device
     out, lse = fa.fwd_varlen(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
                              max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, softmax_scale=p.softmax_scale,
-                             causal=p.causal, window=p.window, num_splits=0)
+                             causal=p.causal, window=p.window, num_splits=0, score_mod=p.mod_kind,
+                             alibi_slope=p.alibi_slope, softcap=p.softcap)
     g = torch.Generator(device="cpu").manual_seed(17)
     dout = torch.randn(out.shape, generator=g).to(torch.bfloat16).to(dev)
     dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
@@ -196,6 +197,7 @@ def make_bwd_call(p, t):
         return fa.bwd_varlen(t["q"], t["k"], t["v"], out, dout, lse, t["cu_q"], t["cu_k"],
                              max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
                              softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
+                             score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap,
                              dq=dq, dk=dk, dv=dv, workspace=ws)
     return call
 

@@ -102,7 +102,7 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_plan_destroy.argtypes = [ctypes.c_void_p]
             L.fa_fwd_plan_destroy.restype = None
             L.fa_bwd_varlen.argtypes = [P(Tensor)] * 11 + [ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
-                                                          P(Launch), ctypes.c_void_p]
+                                                          P(ScoreMod), P(Launch), ctypes.c_void_p]
             L.fa_bwd_varlen.restype = ctypes.c_int
             L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -361,12 +361,13 @@ def bwd_workspace_bytes(total_q: int, hq: int) -> int:
 def bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, dout: torch.Tensor,
                lse: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, *,
                max_seqlen_q: int, max_seqlen_k: int, softmax_scale: Optional[float] = None,
-               causal: bool = False, window: int = 0, dq: Optional[torch.Tensor] = None,
+               causal: bool = False, window: int = 0, score_mod: int = MOD_NONE,
+               alibi_slope: float = 0.0, softcap: float = 0.0, dq: Optional[torch.Tensor] = None,
                dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
                workspace: Optional[torch.Tensor] = None, stream=None):
     """Backward pass through ``fa_bwd_varlen``: returns (dq, dk, dv), bf16 with
     the shapes of q, k, v.  ``lse`` is the forward's fp32 [Hq, T_q] LSE for the
-    same inputs and masks; K/V packed [T_k, Hkv, D]; D = 64 or 128."""
+    same inputs, masks and score mod; K/V packed [T_k, Hkv, D]; D = 64 or 128."""
     L = lib()
     B = cu_seqlens_q.shape[0] - 1
     Tq, Hq, D = q.shape
@@ -384,6 +385,8 @@ def bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Ten
         launch.workspace = workspace.data_ptr()
         launch.workspace_bytes = workspace.numel()
     args = [as_tensor(x) for x in (q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, dq, dk, dv)]
+    sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
     _check(L.fa_bwd_varlen(*[_ref(a) for a in args], ctypes.c_float(softmax_scale), int(bool(causal)),
-                           int(window), ctypes.byref(launch), ctypes.c_void_p(_stream_ptr(stream))))
+                           int(window), ctypes.byref(sm), ctypes.byref(launch),
+                           ctypes.c_void_p(_stream_ptr(stream))))
     return dq, dk, dv

@@ -697,8 +697,8 @@ size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq) {
 fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_tensor_t *v, const fa_tensor_t *out,
                           const fa_tensor_t *dout, const fa_tensor_t *lse, const fa_tensor_t *cu_seqlens_q,
                           const fa_tensor_t *cu_seqlens_k, fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv,
-                          float softmax_scale, int32_t causal, int32_t window, const fa_launch_t *launch,
-                          void *stream) {
+                          float softmax_scale, int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
+                          const fa_launch_t *launch, void *stream) {
   g_msg[0] = 0;
   fa_status_t st;
   if (!launch) return fail(FA_ERR_INVALID_ARG, "launch is NULL");
@@ -731,6 +731,16 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
   if (overlaps(dq, dk) || overlaps(dq, dv) || overlaps(dk, dv)) return fail(FA_ERR_INVALID_ARG, "dq, dk, dv overlap");
   if (window < 0) window = 0;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return fail(FA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+  int mod = 0;
+  float slope = 0.f, cap = 0.f;
+  if (score_mod) {
+    mod = score_mod->kind;
+    if (mod < 0 || mod > 2) return fail(FA_ERR_INVALID_ARG, "score_mod.kind %d", mod);
+    slope = score_mod->alibi_slope;
+    cap = score_mod->softcap;
+    if (mod == 1 && !std::isfinite(slope)) return fail(FA_ERR_INVALID_ARG, "alibi_slope must be finite");
+    if (mod == 2 && !(cap > 0.f && std::isfinite(cap))) return fail(FA_ERR_INVALID_ARG, "softcap must be positive and finite");
+  }
   if (B == 0 || Tq == 0) return FA_OK;
   if (launch->max_seqlen_q <= 0 || launch->max_seqlen_k < 0) return fail(FA_ERR_INVALID_ARG, "bad max_seqlen");
   if (B > 65535 || Hq > 65535) return fail(FA_ERR_UNSUPPORTED, "num_seqs and Hq must be at most 65535");
@@ -781,6 +791,10 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * fa::kLog2e;
   p.err = error_word();
+  p.softcap_arg = mod == 2 ? softmax_scale / cap : 0.f;
+  p.softcap_log2 = mod == 2 ? cap * fa::kLog2e : 0.f;
+  p.alibi_log2 = mod == 1 ? slope * fa::kLog2e : 0.f;
+  L.mod = mod;
   fa::BwdDeltaParams &dp = L.dp;
   dp.out = (const __nv_bfloat16 *)out->data;
   dp.dout = (const __nv_bfloat16 *)dout->data;

@@ -9,6 +9,11 @@
 //   dV_j    = sum_i P_ij dO_i,   dK_j = scale * sum_i dS_ij q_i
 //   dQ_i    = scale * sum_j dS_ij k_j
 //
+// Score mods (fkl_python PR #7, flex commit), as in the forward: ALiBi adds
+// -slope*|i' - j| to the scaled score, which leaves dS as it is; the soft-cap
+// s = cap*tanh(u/cap), u = scale*<q, k>, multiplies the gradient by
+// ds/du = 1 - tanh^2(u/cap), which the kernels fold into P before forming dS.
+//
 // Two kernels share the arithmetic and split the outputs so that no output
 // needs an atomic: fa_bwd_dq_kernel (one 128-row query tile per CTA, looping
 // over key tiles) and fa_bwd_dkdv_kernel (one 128-key tile per CTA, looping
@@ -116,6 +121,26 @@ __device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 
+// exp(s - LSE) of one (query, key) pair from the raw product <q, k>, with the
+// score mod MOD (0 none, 1 ALiBi at distance `dist` = |i' - j|, exact in fp32,
+// 2 soft-cap); `dfac` returns ds/du (1 unless soft-capped).  lse2 = LSE * log2(e).
+template <int MOD>
+__device__ __forceinline__ float bwd_prob(const BwdParams &p, float sraw, float lse2, float dist, float &dfac) {
+  if constexpr (MOD == 2) {
+    const float u = sraw * p.softcap_arg;                 // (scale / cap) <q, k>
+    const float em = ex2(-2.f * kLog2e * fabsf(u));       // tanh from e^{-2|u|}
+    const float th = copysignf(__fdividef(1.f - em, 1.f + em), u);
+    dfac = 1.f - th * th;
+    return ex2(fmaf(th, p.softcap_log2, -lse2));
+  } else if constexpr (MOD == 1) {
+    dfac = 1.f;
+    return ex2(fmaf(sraw, p.scale_log2, -fmaf(p.alibi_log2, dist, lse2)));
+  } else {
+    dfac = 1.f;
+    return ex2(fmaf(sraw, p.scale_log2, -lse2));
+  }
+}
+
 // Barrier among `count` threads (whole warps) of the CTA, id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -146,7 +171,7 @@ __device__ __forceinline__ void bwd_load_tile(uint8_t *dst, const CUtensorMap *t
 //   S(0) dP(0) | S(t+1) once S(t) is read | dP(t+1) once dP(t) is read |
 //   dQ += dS(t) K(t)
 // so the next tile's contractions run while the rows form dS(t).
-template <int D>
+template <int D, int MOD>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -334,10 +359,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_arrive(smem_u32(s_read));
       // the row's allowed keys are one interval; as tile columns: [elo, ehi)
       const int elo = row_jlo - j0, ehi = row_jhi - j0;
+      // P times ds/du (only dS is formed from it here); ALiBi distance
+      // |i' - j0 - e| from one integer conversion per tile
+      const float dbase = (float)(ip - j0);
 #pragma unroll
       for (int e = 0; e < 128; ++e) {
-        const float x = ex2(fmaf(pr[e], p.scale_log2, -lse2));
-        pr[e] = (e >= elo && e < ehi) ? x : 0.f;
+        float df;
+        const float x = bwd_prob<MOD>(p, pr[e], lse2, fabsf(dbase - (float)e), df);
+        pr[e] = (e >= elo && e < ehi) ? x * df : 0.f;
       }
       ok = mbar_wait(smem_u32(dp_full), t & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -414,7 +443,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 //   S^T(0) dP^T(0) | dV += P^T(s) dO(s) once P^T is stored, S^T(s+1) |
 //   dK += dS^T(s) Q(s) once dS^T is stored, dP^T(s+1)
 // so dV and the next S^T run while the keys' warps form dS^T(s).
-template <int D>
+template <int D, int MOD>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -623,12 +652,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int elo = key_qlo - q0, ehi = key_qhi - q0;
       // P^T rounded to bf16 at once (the operand of dV += P^T dO; dS^T is
       // formed from the same rounded values), which halves its registers
+      // soft-cap: dS^T is formed from P times ds/du, kept apart in ptk
       uint32_t ppk[64];
+      uint32_t ptk[MOD == 2 ? 64 : 1];
+      const float dbase = (float)(q0 + off - j);   // ALiBi: |i' - j| = |dbase + e|
 #pragma unroll
       for (int e = 0; e < 128; e += 2) {
-        const float x0 = ex2(fmaf(pr[e], p.scale_log2, -stat[e]));
-        const float x1 = ex2(fmaf(pr[e + 1], p.scale_log2, -stat[e + 1]));
-        ppk[e >> 1] = pack_bf16x2((e >= elo && e < ehi) ? x0 : 0.f, (e + 1 >= elo && e + 1 < ehi) ? x1 : 0.f);
+        float d0, d1;
+        const float x0 = bwd_prob<MOD>(p, pr[e], stat[e], fabsf(dbase + (float)e), d0);
+        const float x1 = bwd_prob<MOD>(p, pr[e + 1], stat[e + 1], fabsf(dbase + (float)(e + 1)), d1);
+        const bool a0 = e >= elo && e < ehi, a1 = e + 1 >= elo && e + 1 < ehi;
+        ppk[e >> 1] = pack_bf16x2(a0 ? x0 : 0.f, a1 ? x1 : 0.f);
+        if constexpr (MOD == 2) ptk[e >> 1] = pack_bf16x2(a0 ? x0 * d0 : 0.f, a1 ? x1 * d1 : 0.f);
       }
       // P^T over S^T's last 64 columns: dV(s) may start
 #pragma unroll
@@ -651,7 +686,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int q = hf * 64 + 2 * e;
-          const uint32_t u = ppk[q >> 1];
+          uint32_t u;
+          if constexpr (MOD == 2) u = ptk[q >> 1];
+          else u = ppk[q >> 1];
           const float p0 = __uint_as_float(u << 16), p1 = __uint_as_float(u & 0xFFFF0000u);
           w[e] = pack_bf16x2(p0 * (dp[2 * e] - stat[128 + q]), p1 * (dp[2 * e + 1] - stat[128 + q + 1]));
         }

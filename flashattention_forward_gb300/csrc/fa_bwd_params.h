@@ -21,6 +21,9 @@ struct BwdParams {
   float scale_log2;             // softmax_scale * log2(e)
   float scale;                  // softmax_scale
   int *err;
+  float softcap_arg;            // soft-cap: softmax_scale / cap
+  float softcap_log2;           // soft-cap: cap * log2(e)
+  float alibi_log2;             // ALiBi: slope * log2(e)
 };
 
 struct BwdDeltaParams {

@@ -35,6 +35,7 @@ struct BwdLaunch {
   BwdParams p;
   BwdDeltaParams dp;
   unsigned delta_blocks;
+  int mod;       // score mod: 0 none, 1 ALiBi, 2 soft-cap
   dim3 grid_q, grid_kv;
   cudaStream_t stream;
 };

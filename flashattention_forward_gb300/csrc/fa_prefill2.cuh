@@ -428,6 +428,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
       // path keeps raw scores and folds the scale into the exponent's FMA).
       auto scores = [&](float (&v)[32], int jc) {
         if (!fast) {
+          const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float x;
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
             } else {
               x = v[e] * p.scale_log2;
             }
-            if constexpr (MOD == 1) x -= p.alibi_log2 * (float)abs(ip - (jc + e));
+            if constexpr (MOD == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
             v[e] = x;
           }
         }

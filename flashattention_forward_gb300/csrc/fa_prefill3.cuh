@@ -734,6 +734,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
           }
         }
         if (!fast) {
+          const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float x;
@@ -744,7 +745,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
             } else {
               x = v[e] * sl2;
             }
-            if constexpr (MOD == 1) x -= p.alibi_log2 * (float)abs(ip - (jc + e));
+            if constexpr (MOD == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
             v[e] = x;
           }
         }

@@ -225,6 +225,9 @@ fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_s
  *   dP_ij = <dout_i, v_j>,   dS_ij = P_ij * (dP_ij - Delta_i)
  *   dv_j = sum_i P_ij dout_i,  dk_j = softmax_scale * sum_i dS_ij q_i,
  *   dq_i = softmax_scale * sum_j dS_ij k_j      (allowed (i, j) only)
+ * With a score mod, P uses the modified score s_ij.  ALiBi leaves dS as
+ * written; the soft-cap s = cap * tanh(u / cap), u = softmax_scale <q, k>,
+ * multiplies dS_ij by ds/du = 1 - tanh^2(u_ij / cap).
  *
  *  q, out, dout, dq   bf16 [T_q, Hq, D];  k, v, dk, dv   bf16 [T_k, Hkv, D],
  *                     packed varlen (no block table).  D = 64 or 128 (Dk = Dv).
@@ -234,8 +237,8 @@ fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_s
  *  lse                fp32 [Hq, T_q] contiguous, the forward's LSE for the
  *                     same (q, k, v, masks).
  *  cu_seqlens_q/k     int32 [num_seqs + 1] (row offsets of q and of k/v).
- *  softmax_scale      > 0;  causal, window as in fa_fwd_varlen (score mods and
- *                     block masks are not supported here).
+ *  softmax_scale      > 0;  causal, window, score_mod (NULL or kind 0, 1, 2)
+ *                     as in fa_fwd_varlen; block masks are not supported here.
  *  launch             num_seqs, max_seqlen_q/k, total_q (= T_q) and a
  *                     workspace of fa_bwd_workspace_bytes(T_q, Hq) bytes,
  *                     256-byte aligned, for Delta (fp32 [Hq, T_q]).
@@ -250,7 +253,8 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
                           const fa_tensor_t *out, const fa_tensor_t *dout, const fa_tensor_t *lse,
                           const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
                           fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv, float softmax_scale,
-                          int32_t causal, int32_t window, const fa_launch_t *launch, void *stream);
+                          int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
+                          const fa_launch_t *launch, void *stream);
 
 /* Workspace bytes of fa_bwd_varlen: Delta, fp32 [Hq, T_q], rounded up to 256. */
 size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);

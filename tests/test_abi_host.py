@@ -227,13 +227,13 @@ def _bcall(L, **over):
         dout=_t(FAKE * 5, fa.FA_BF16, [T, H, D]), lse=_t(FAKE * 6, fa.FA_F32, [H, T]),
         cq=_t(FAKE * 7, fa.FA_I32, [3]), ck=_t(FAKE * 8, fa.FA_I32, [3]),
         dq=_t(FAKE * 9, fa.FA_BF16, [T, H, D]), dk=_t(FAKE * 10, fa.FA_BF16, [T, H, D]),
-        dv=_t(FAKE * 11, fa.FA_BF16, [T, H, D]), scale=0.125, causal=1, window=0,
+        dv=_t(FAKE * 11, fa.FA_BF16, [T, H, D]), scale=0.125, causal=1, window=0, mod=None,
         launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=0, total_q=T, total_k=T,
                          workspace=ws, workspace_bytes=fa.bwd_workspace_bytes(T, H)))
     args.update(over)
     r = lambda x: None if x is None else ctypes.byref(x)
     st = L.fa_bwd_varlen(*[r(args[n]) for n in ("q", "k", "v", "out", "dout", "lse", "cq", "ck", "dq", "dk", "dv")],
-                         args["scale"], args["causal"], args["window"], r(args["launch"]), None)
+                         args["scale"], args["causal"], args["window"], r(args["mod"]), r(args["launch"]), None)
     return st, L.fa_last_error().decode()
 
 
@@ -254,6 +254,9 @@ def test_bwd_workspace_bytes(L):
     (dict(lse=_t(FAKE * 6, fa.FA_F32, [256, 4])), fa.FA_ERR_INVALID_ARG, "lse must be"),
     (dict(dk=_t(FAKE * 2, fa.FA_BF16, [256, 4, 64])), fa.FA_ERR_INVALID_ARG, "overlap"),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG, "softmax_scale"),
+    (dict(mod=fa.ScoreMod(kind=2, softcap=-1.0)), fa.FA_ERR_INVALID_ARG, "softcap"),
+    (dict(mod=fa.ScoreMod(kind=1, alibi_slope=float("inf"))), fa.FA_ERR_INVALID_ARG, "alibi_slope"),
+    (dict(mod=fa.ScoreMod(kind=3)), fa.FA_ERR_INVALID_ARG, "kind"),
     (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=256, total_k=256)),
      fa.FA_ERR_INVALID_ARG, "workspace"),
     (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=256, total_k=256,

@@ -47,7 +47,8 @@ def run_bwd(p, seed=11):
     dout = torch.from_numpy(dob.view(np.int16).copy()).view(torch.bfloat16).cuda()
     dq, dk, dv = fa.bwd_varlen(t["q"], t["k"], t["v"], out, dout, lse, t["cu_q"], t["cu_k"],
                                max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
-                               softmax_scale=p.softmax_scale, causal=p.causal, window=p.window)
+                               softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
+                               score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap)
     torch.cuda.synchronize()
     g = [x.float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
     return g, fi.bf16_to_f32(dob).astype(np.float64)
@@ -79,6 +80,14 @@ CASES = {
     "window_causal": dict(lens_q=[600, 130], hq=2, dk=128, causal=True, window=100),
     "window_noncausal": dict(lens_q=[400], lens_k=[500], hq=2, dk=64, window=70),
     "long_multi_tile": dict(lens_q=[900], hq=2, dk=128, causal=True),
+    # score mods: ALiBi leaves dS as it is, the soft-cap scales it by 1 - tanh^2
+    "alibi_causal_d128": dict(lens_q=[300, 129], hq=4, dk=128, causal=True, mod="alibi", alibi_slope=0.05),
+    "alibi_gqa_sq_lt_sk_d64": dict(lens_q=[70, 200], lens_k=[260, 333], hq=8, hkv=2, dk=64, mod="alibi",
+                                   alibi_slope=0.02),
+    "softcap_causal_d128": dict(lens_q=[257, 64], hq=4, dk=128, causal=True, mod="softcap", softcap=2.0,
+                                softmax_scale=0.25),
+    "softcap_window_gqa_d64": dict(lens_q=[400], lens_k=[500], hq=4, hkv=2, dk=64, window=90, mod="softcap",
+                                   softcap=5.0),
 }
 
 
