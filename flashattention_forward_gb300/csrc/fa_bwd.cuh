@@ -127,11 +127,11 @@ __device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, 
 template <int MOD>
 __device__ __forceinline__ float bwd_prob(const BwdParams &p, float sraw, float lse2, float dist, float &dfac) {
   if constexpr (MOD == 2) {
-    const float u = sraw * p.softcap_arg;                 // (scale / cap) <q, k>
-    const float em = ex2(-2.f * kLog2e * fabsf(u));       // tanh from e^{-2|u|}
-    const float th = copysignf(__fdividef(1.f - em, 1.f + em), u);
-    dfac = 1.f - th * th;
-    return ex2(fmaf(th, p.softcap_log2, -lse2));
+    // the soft-capped score as the forward forms it; ds/du = 4 r (1 - r)
+    float r;
+    const float s2 = softcap_log2_score(ex2(sraw * (2.f * kLog2e * p.softcap_arg)), p.softcap_log2, r);
+    dfac = 4.f * r * (1.f - r);
+    return ex2(s2 - lse2);
   } else if constexpr (MOD == 1) {
     dfac = 1.f;
     return ex2(fmaf(sraw, p.scale_log2, -fmaf(p.alibi_log2, dist, lse2)));

@@ -429,13 +429,13 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
       auto scores = [&](float (&v)[32], int jc) {
         if (!fast) {
           const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
+          const float c2u = 2.f * kLog2e * p.softcap_arg;   // soft-cap: raw score -> 2u log2(e)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float x;
             if constexpr (MOD == 2) {
-              const float t = v[e] * p.softcap_arg;
-              const float em = ex2(-2.f * kLog2e * fabsf(t));
-              x = copysignf(__fdividef(1.f - em, 1.f + em), t) * p.softcap_log2;
+              float r;
+              x = softcap_log2_score(ex2(v[e] * c2u), p.softcap_log2, r);
             } else {
               x = v[e] * p.scale_log2;
             }

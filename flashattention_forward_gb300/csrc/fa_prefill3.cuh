@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     // packed type (f16 for e4m3 caches: below 65504; bf16: any fp32 value).
     constexpr float kGuard = FP8 ? 0x1p15f : kGuardSum;
     const float sl2 = p.scale_log2 * rowf;
-    const float sca = p.softcap_arg * rowf;
+    const float c2u = 2.f * kLog2e * p.softcap_arg * rowf;   // soft-cap: raw score -> 2u log2(e)
     auto pack_p = [](float a, float b) -> uint32_t { return FP8 ? pack_f16x2(a, b) : pack_bf16x2(a, b); };
     auto chunk_exp = [&](const float (&v)[32], float c, float m, uint32_t (&pk)[16], float (&acc)[4]) {
 #pragma unroll
@@ -739,9 +739,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
           for (int e = 0; e < 32; ++e) {
             float x;
             if constexpr (MOD == 2) {
-              const float t = v[e] * sca;
-              const float em = ex2(-2.f * kLog2e * fabsf(t));
-              x = copysignf(__fdividef(1.f - em, 1.f + em), t) * p.softcap_log2;
+              float r;
+              x = softcap_log2_score(ex2(v[e] * c2u), p.softcap_log2, r);
             } else {
               x = v[e] * sl2;
             }

@@ -229,6 +229,22 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Soft-capped score in log2 units, cap*log2(e) * tanh(u), from e2u = exp(2u):
+// tanh(u) = 1 - 2 / (1 + e^{2u}), so the value is cl - 2 cl / (1 + e2u).
+// e2u = +inf gives cl and e2u = 0 gives -cl; near u = 0 the absolute error
+// stays at a few fp32 ulps of cl.  Also returns r = 1 / (1 + e2u), from which
+// d tanh / du = 1 - tanh^2 = 4 r (1 - r).
+__device__ __forceinline__ float softcap_log2_score(float e2u, float cl, float &r) {
+  r = rcp_approx(1.f + e2u);
+  return fmaf(r, -2.f * cl, cl);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

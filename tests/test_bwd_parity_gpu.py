@@ -88,6 +88,7 @@ CASES = {
                                 softmax_scale=0.25),
     "softcap_window_gqa_d64": dict(lens_q=[400], lens_k=[500], hq=4, hkv=2, dk=64, window=90, mod="softcap",
                                    softcap=5.0),
+    "softcap_saturated_d64": dict(lens_q=[200, 130], hq=4, dk=64, mod="softcap", softcap=0.5, softmax_scale=1.0),
 }
 
 

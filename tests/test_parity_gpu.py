@@ -78,6 +78,9 @@ EDGE = [
     dict(lens_q=[257, 33], lens_k=[600, 33], hq=4, hkv=2, dk=192, dv=128, page_size=64, spare_pages=3),
     dict(lens_q=[300, 70], lens_k=[300, 200], hq=4, dk=128, softmax_scale=-0.05, causal=True),  # negative scale
     dict(lens_q=[513, 40, 900], lens_k=[513, 700, 900], hq=8, hkv=2, dk=64, causal=True),       # 3 pairs, GQA
+    dict(lens_q=[257, 33], lens_k=[600, 33], hq=4, hkv=2, dk=192, dv=128, mod="softcap", softcap=3.0,
+         causal=True),                                                                           # soft-cap, Dk 192
+    dict(lens_q=[200, 130], hq=4, dk=64, mod="softcap", softcap=0.5, softmax_scale=1.0),        # tanh saturated
 ]
 
 
