@@ -41,7 +41,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
         return LIB
     cc = nvcc()
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+                    "--expt-relaxed-constexpr",
                     "-I", os.path.join(HERE, "..", "include")]
     if ptxas_v:
         flags += ["-Xptxas", "-v"]

@@ -47,6 +47,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* Every entry point below is exported; the library is built with hidden
+ * visibility for everything else (kernels, templates, helpers), so that two
+ * copies loaded into one process do not bind to each other's internals. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -150,7 +159,7 @@ typedef struct {
  * be a multiple of Hkv (query head h reads kv head h / (Hq/Hkv)).
  * Returns FA_OK or an error status; see fa_last_error().
  */
-fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache,
+FA_API fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache,
                           const fa_tensor_t *v_cache, const fa_tensor_t *block_table,
                           const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
                           const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
@@ -175,22 +184,22 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache,
  */
 typedef struct fa_fwd_plan_s *fa_fwd_plan_t;
 
-fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
+FA_API fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
                                const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
                                const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale,
                                const fa_tensor_t *v_scale, fa_tensor_t *out, fa_tensor_t *lse,
                                float softmax_scale, int32_t causal, int32_t window,
                                const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask,
                                int32_t page_size, const fa_launch_t *launch, fa_fwd_plan_t *plan);
-fa_status_t fa_fwd_plan_launch(fa_fwd_plan_t plan, void *stream);
-void fa_fwd_plan_destroy(fa_fwd_plan_t plan);
+FA_API fa_status_t fa_fwd_plan_launch(fa_fwd_plan_t plan, void *stream);
+FA_API void fa_fwd_plan_destroy(fa_fwd_plan_t plan);
 
 /*
  * Workspace size in bytes for split-KV with `num_splits` key ranges: partial
  * outputs fp32 [num_splits, T_q, Hq, Dv] and partial LSEs fp32
  * [num_splits, Hq, T_q], each 256-byte aligned.  0 when num_splits <= 0.
  */
-size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int32_t dv,
+FA_API size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int32_t dv,
                               int32_t num_splits);
 
 /*
@@ -200,7 +209,7 @@ size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int
  * about three waves at two CTAs per SM of the current device; total_k (the
  * sum of key lengths, 0 if unknown) refines the estimate of non-empty ranges.
  */
-int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+FA_API int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
                               int64_t total_k, int32_t hq, int32_t hkv, int32_t page_size);
 
 /*
@@ -212,7 +221,7 @@ int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t ma
  *  lse_part fp32 [num_splits, Hq, n_rows] contiguous
  *  out      bf16 [n_rows, Hq, Dv] contiguous;  lse fp32 [Hq, n_rows] or NULL.
  */
-fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_splits,
+FA_API fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_splits,
                        int64_t n_rows, int32_t hq, int32_t dv, void *out_bf16, float *lse,
                        void *stream);
 
@@ -249,7 +258,7 @@ fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_t num_s
  * strides, alignment or a missing workspace, FA_ERR_UNSUPPORTED for other
  * head dims, FA_ERR_CUDA for launch failures.
  */
-fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_tensor_t *v,
+FA_API fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_tensor_t *v,
                           const fa_tensor_t *out, const fa_tensor_t *dout, const fa_tensor_t *lse,
                           const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
                           fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv, float softmax_scale,
@@ -257,7 +266,7 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
                           const fa_launch_t *launch, void *stream);
 
 /* Workspace bytes of fa_bwd_varlen: Delta, fp32 [Hq, T_q], rounded up to 256. */
-size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);
+FA_API size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);
 
 /*
  * fa_fwd_varlen_noalloc -- the split-KV decode of fa_fwd_varlen for callers
@@ -287,7 +296,7 @@ size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);
  * start at zero.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
-fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tensor_t *k_cache,
+FA_API fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tensor_t *k_cache,
                                   const fa_tensor_t *v_cache, const fa_tensor_t *block_table,
                                   const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
                                   const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
@@ -297,14 +306,14 @@ fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tensor_t *k_cac
                                   const fa_launch_t *launch, void *stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
-const char *fa_last_error(void);
+FA_API const char *fa_last_error(void);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word into *code (FA_OK when no kernel recorded a problem). */
-fa_status_t fa_get_device_error(void *stream, int32_t *code);
+FA_API fa_status_t fa_get_device_error(void *stream, int32_t *code);
 
 /* Library version string. */
-const char *fa_version(void);
+FA_API const char *fa_version(void);
 
 #ifdef __cplusplus
 }

@@ -33,6 +33,19 @@ def test_header_symbols_are_exported(L):
     assert set(syms) <= set(fa.EXPORTED) | set(syms)
 
 
+def test_only_the_header_entry_points_are_exported(L):
+    """Kernels, templates and helpers have hidden visibility: the dynamic
+    symbol table's functions are exactly the declared entry points."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", fa_build.LIB], capture_output=True, text=True, check=True)
+    funcs = sorted(ln.split()[-1] for ln in out.stdout.splitlines() if len(ln.split()) == 3 and ln.split()[1] == "T")
+    assert funcs == declared_symbols()
+
+
 def test_version_and_last_error(L):
     assert "sm_103a" in fa.version()
     assert isinstance(L.fa_last_error(), bytes)
