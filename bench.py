@@ -497,6 +497,16 @@ def other_workloads(dev, warmup, steps, flush, pk):
     res["paged_decode_64seq_hq32_hkv8_p16"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
                                                "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16, p.total_k),
                                                "bytes": fi.decode_bytes(p)}
+    # the same decode one key per page (rows gathered by cp.async)
+    p1 = fi.make_problem([1] * 64, [int(x) for x in p.seqlens_k], hq=32, hkv=8, dk=128, seed=1, page_size=1,
+                         spare_pages=64, max_pages=8192, name="paged_decode_p1")
+    t = dev_tensors(p1, dev)
+    call, n, _, _ = make_call(p1, t, num_splits=None)
+    ms = statistics.mean(time_calls([call], warmup, steps, flush))
+    gbs = fi.decode_bytes(p1) / (ms * 1e-3) / 1e9
+    res["paged_decode_64seq_hq32_hkv8_p1"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
+                                              "bytes": fi.decode_bytes(p1)}
+    del t, p1
     # the same decode geometry on byte caches (e4m3, int8; per-token scales)
     for kvd in ("e4m3", "int8"):
         rng = np.random.default_rng(0)
@@ -522,6 +532,17 @@ def other_workloads(dev, warmup, steps, flush, pk):
                                                         "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
                                                         "gflop": fl / 1e9}
     del t
+    # the same tokens one key per page (rows gathered by cp.async, no TMA boxes)
+    lens4 = [int(x) for x in np.diff(p.cu_seqlens_q)]
+    p1 = fi.make_problem(lens4, hq=16, hkv=16, dk=192, dv=128, seed=1, page_size=1, spare_pages=16,
+                         kv_dtype="e4m3", causal=True, name="config4_page1")
+    t = dev_tensors(p1, dev)
+    call, _, _, _ = make_call(p1, t, num_splits=0)
+    ms = statistics.mean(time_calls([call], warmup, steps, flush))
+    res["paged_fp8_d192_v128_16seq_h16_p1_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                                       "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+                                                       "gflop": fl / 1e9}
+    del t, p1
     # the same geometry with an int8 cache (per-token scales)
     p = fi.make_problem([int(x) for x in np.diff(p.cu_seqlens_q)], hq=16, hkv=16, dk=192, dv=128, seed=1,
                         page_size=64, kv_dtype="int8", causal=True, name="config4_int8")

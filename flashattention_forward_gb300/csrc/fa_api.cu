@@ -133,6 +133,16 @@ int *error_word() {
   return addr[dev];
 }
 
+// Byte geometry of a paged cache [N_pg, P_s, Hkv, D] for the row gather.
+fa::KvGather kv_gather(const fa_tensor_t *t, int esz) {
+  fa::KvGather g;
+  g.base = (const uint8_t *)t->data;
+  g.page_stride = t->stride[0] * esz;
+  g.slot_stride = t->stride[1] * esz;
+  g.head_stride = t->stride[2] * esz;
+  return g;
+}
+
 bool supported_dims(int64_t dk, int64_t dv) {
   return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
 }
@@ -359,11 +369,13 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if (block_table->stride[1] != 1 && block_table->shape[1] > 1) return fail(FA_ERR_INVALID_ARG, "block_table rows must be contiguous");
     max_pages = block_table->shape[1];
     n_pages = k_cache->shape[0];
-    // Page sizes from 16 keep every TMA box's shared-memory destination
-    // 1024-byte aligned (bf16 boxes of >= 8 rows, e4m3 staging boxes of >= 16
-    // rows); smaller pages would need a row-gather path.
-    if (!is_pow2(page_size) || page_size < 16 || page_size > 1024)
-      return fail(FA_ERR_UNSUPPORTED, "page_size %d: supported sizes are powers of two from 16 to 1024", page_size);
+    // Pages of >= 16 keys are landed by TMA boxes whose shared-memory
+    // destinations stay 1024-byte aligned; pages of 1..8 keys take the row
+    // gather (fa_gather.cuh), which e4m3 Q (keys straight into the MMA
+    // operand with their scales) does not have.
+    if (!is_pow2(page_size) || page_size < 1 || page_size > 1024)
+      return fail(FA_ERR_UNSUPPORTED, "page_size %d: supported sizes are powers of two from 1 to 1024", page_size);
+    if (q8 && page_size < 16) return fail(FA_ERR_UNSUPPORTED, "e4m3 q needs pages of at least 16 keys");
     if (k_cache->shape[1] != page_size) return fail(FA_ERR_INVALID_ARG, "k_cache.shape[1]=%lld != page_size=%d", (long long)k_cache->shape[1], page_size);
     if ((int64_t)launch->max_seqlen_k > max_pages * page_size) return fail(FA_ERR_INVALID_ARG, "max_seqlen_k exceeds block_table capacity");
     if (n_pages >= (int64_t(1) << 31)) return fail(FA_ERR_OVERFLOW, "num_pages must fit int32");
@@ -493,6 +505,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.page_shift = ilog2(p.page_size);
     p.rows_per_box = rows_box;
     p.boxes_per_stage = fa::kDecStageKeys / rows_box;
+    p.gather = paged && page_size < 16;
+    if (p.gather) {
+      p.gk = kv_gather(k_cache, esz);
+      p.gv = kv_gather(v_cache, esz);
+    }
     p.hq = (int)Hq;
     p.hkv = (int)Hkv;
     p.group = group;
@@ -623,6 +640,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   p.page_size = paged ? page_size : fa::kBlockN;
   p.page_shift = ilog2(p.page_size);
   p.rows_per_box = fp8 ? rows_box8 : rows_box;
+  p.gather = paged && page_size < 16;
+  if (p.gather) {
+    p.gk = kv_gather(k_cache, esz);
+    p.gv = kv_gather(v_cache, esz);
+  }
   p.pages_per_tile = fa::kBlockN / p.rows_per_box;
   p.n_qtiles = (int)n_qtiles;
   p.causal = causal != 0;

@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fa_gather.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -59,6 +60,8 @@ struct DecodeParams {
   float *lse;                         // [Hq, T_q] or null
   int *err;                           // device error word
   const float *k_scale, *v_scale;     // byte caches: per (token, kv head), in the cache's token order
+  int32_t gather;                     // pages of < 16 keys: K/V rows by cp.async (fa_gather.cuh)
+  KvGather gk, gv;
 };
 
 template <int D, int KV = 0>
@@ -196,8 +199,11 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   float *sQinv = reinterpret_cast<float *>(smem + Cfg::kOffQInv);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      // byte caches: the producer's arrival plus one cp.async arrival per lane (scales)
-      mbar_init(smem_u32(full + s), KV ? 1 + 32 : 1);
+      // byte caches: the producer's arrival plus one cp.async arrival per lane
+      // (scales); gathered rows (pages of < 16 keys): one arrival per lane
+      // in place of the producer's
+      const uint32_t n_fill = p.gather ? 32u : 1u;
+      mbar_init(smem_u32(full + s), KV ? n_fill + 32 : n_fill);
       mbar_init(smem_u32(empty + s), kDecWarps);
     }
     *abort_flag = 0;
@@ -272,10 +278,64 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       const int key = key_lo + st * kDecStageKeys + lane + 32 * u;
       return key < sk ? __ldg(bt + (key >> p.page_shift)) : 0;
     };
-    int pg_next = box_page(first_stage);
-    int sp_next[2] = {scale_page(first_stage, 0), scale_page(first_stage, 1)};
     bool ok = true;
-    for (int st = first_stage; st < n_stages; ++st) {
+    if (p.gather && bt) {
+      // Pages of < 16 keys: every key row by its own page-table read and
+      // 16-byte copies (fa_gather.cuh): swizzled bf16 blocks or plain byte
+      // rows, the layouts the boxes fill.  pg[u] is the page of key
+      // lane + 32u of a stage; byte caches take their scales through it too.
+      auto pages_of = [&](int st, int (&pg)[2]) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int key = key_lo + st * kDecStageKeys + lane + 32 * u;
+          pg[u] = (st < n_stages && key < sk) ? __ldg(bt + (key >> p.page_shift)) : -1;
+        }
+      };
+      // one stage in flight: the stage the producer waits for frees once
+      // the consumers are done with stage it - NST (NST >= 3), older than
+      // the newest (two in flight would also be safe, but measured slower)
+      GatherPipe<1> gp;
+      int pg[2], pgn[2];
+      pages_of(first_stage, pg);
+      for (int st = first_stage; st < n_stages; ++st) {
+        const int it = st - first_stage;
+        const int slot_i = it % NST;
+        pages_of(st + 1, pgn);
+        if (lane == 0 && it >= NST) ok = mbar_wait(smem_u32(empty + slot_i), ((it / NST) - 1) & 1, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        uint8_t *kd = stages + slot_i * Cfg::kStageBytes;
+        uint8_t *vd = kd + Cfg::kKBytes;
+        const int key0 = key_lo + st * kDecStageKeys;
+        if constexpr (KV) {
+          const uint32_t sdst = smem_u32(vd + Cfg::kVBytes);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int kk = lane + 32 * u;
+            const bool live = pg[u] >= 0;
+            const int64_t at = ((int64_t)pg[u] * p.page_size + ((key0 + kk) & (p.page_size - 1))) * p.hkv + hk;
+            dec_cp_async_4(sdst + 4 * kk, live ? p.k_scale + at : p.k_scale, live ? 4u : 0u);
+            dec_cp_async_4(sdst + 4 * (kDecStageKeys + kk), live ? p.v_scale + at : p.v_scale, live ? 4u : 0u);
+          }
+          dec_cp_async_arrive_noinc(smem_u32(full + slot_i));
+          gather_block<kDecStageKeys, D, kGatherPlain>(kd, p.gk, hk, key0, p.page_size - 1, 0, pg, lane);
+          gather_block<kDecStageKeys, D, kGatherPlain>(vd, p.gv, hk, key0, p.page_size - 1, 0, pg, lane);
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < NCB; ++cb) {
+            const uint32_t off = cb * kDecStageKeys * 128;
+            gather_block<kDecStageKeys, 128, kGatherSw128>(kd + off, p.gk, hk, key0, p.page_size - 1, cb * 128, pg, lane);
+            gather_block<kDecStageKeys, 128, kGatherSw128>(vd + off, p.gv, hk, key0, p.page_size - 1, cb * 128, pg, lane);
+          }
+        }
+        gp.commit(smem_u32(full + slot_i));
+#pragma unroll
+        for (int u = 0; u < 2; ++u) pg[u] = pgn[u];
+      }
+      gp.drain();
+    }
+    int pg_next = ok && !(p.gather && bt) ? box_page(first_stage) : -1;
+    int sp_next[2] = {scale_page(first_stage, 0), scale_page(first_stage, 1)};
+    for (int st = first_stage; ok && !(p.gather && bt) && st < n_stages; ++st) {
       const int it = st - first_stage;
       const int slot_i = it % NST;
       const int pg = pg_next, sp[2] = {sp_next[0], sp_next[1]};

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "fa_gather.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -46,6 +47,8 @@ struct PrefillParams {
   int32_t head_group;   // heads interleaved per group in the block order
   int32_t n_hgroups;    // ceil(hq / head_group)
   int32_t n_items;      // work items (persistent kernels stride over them)
+  int32_t gather;       // pages of < 16 keys: K/V rows by cp.async (fa_gather.cuh), not TMA boxes
+  KvGather gk, gv;      // the caches' byte geometry for the gather
 };
 
 // Block order: for each sequence, for each group of `head_group` heads, query

@@ -181,12 +181,15 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
+    // full barriers: one arrival with the TMA bytes, or one per producer lane
+    // for gathered rows
+    const uint32_t n_fill = (PAGED && p.gather) ? 32u : 1u;
     for (int s = 0; s < NSK; ++s) {
-      mbar_init(smem_u32(k_full + s), 1);
+      mbar_init(smem_u32(k_full + s), n_fill);
       mbar_init(smem_u32(k_empty + s), 1);
     }
     for (int s = 0; s < NSV; ++s) {
-      mbar_init(smem_u32(v_full + s), 1);
+      mbar_init(smem_u32(v_full + s), n_fill);
       mbar_init(smem_u32(v_empty + s), 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -226,9 +229,54 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
                       pi.h, pi.q_row0 + X * kBlockM);
     }
     if constexpr (PAGED) {
-      // Paged K/V: a tile spans up to 128 pages (page size 1), one TMA box
-      // and one page-table read each.  Lane 0 waits for the ring slot and
-      // arms its barrier; the boxes are then issued by all lanes in parallel.
+      if (p.gather) {
+        // Pages of < 16 keys: every key row by its own page-table read and
+        // 16-byte copies (fa_gather.cuh), page ids read one tile ahead.
+        const int32_t *bt = p.block_table + (int64_t)pi.b * p.bt_stride;
+        auto pages_of = [&](int kt, int (&pg)[4]) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int key = kt * kBlockN + lane + 32 * u;
+            pg[u] = (kt < pi.kt_hi && key < pi.sk) ? __ldg(bt + (key >> p.page_shift)) : -1;
+          }
+        };
+        // one slot in flight: a K slot frees after QK_B(j-3), which needs
+        // K(j-3) and V(j-4); a V slot after PV_B(j-2), issued after
+        // QK_A(j-1), so it needs K(j-1) and V(j-2); the newest slot before
+        // those waits is V(j-1) or K(j) (two in flight would also be safe,
+        // but measured slower)
+        GatherPipe<1> gp;
+        int pg[4], pgn[4];
+        pages_of(first_kt, pg);
+        int j = 0;
+        bool ok = true;
+        for (int kt = first_kt; kt < pi.kt_hi; ++j) {
+          const int kn = pair_next(p, pi, kt);
+          pages_of(kn, pgn);
+          const int st = j % NSK, sv = j % NSV;
+          if (lane == 0 && j >= NSK) ok = mbar_wait(smem_u32(k_empty + st), ((j / NSK) - 1) & 1, abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+#pragma unroll
+          for (int cb = 0; cb < DK / 64; ++cb)
+            gather_block<kBlockN, 128, kGatherSw128>(sK + st * Cfg::kKBytes + cb * kBlockN * 128, p.gk, pi.hk,
+                                                     kt * kBlockN, p.page_size - 1, cb * 128, pg, lane);
+          gp.commit(smem_u32(k_full + st));
+          if (lane == 0 && j >= NSV) ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+#pragma unroll
+          for (int cb = 0; cb < DV / 64; ++cb)
+            gather_block<kBlockN, 128, kGatherSw128>(sV + sv * Cfg::kVBytes + cb * kBlockN * 128, p.gv, pi.hk,
+                                                     kt * kBlockN, p.page_size - 1, cb * 128, pg, lane);
+          gp.commit(smem_u32(v_full + sv));
+          kt = kn;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pg[u] = pgn[u];
+        }
+        gp.drain();
+      } else {
+      // Paged K/V with pages of >= 16 keys: one TMA box and one page-table
+      // read per page piece.  Lane 0 waits for the ring slot and arms its
+      // barrier; the boxes are then issued by all lanes in parallel.
       const int32_t *bt = p.block_table + (int64_t)pi.b * p.bt_stride;
       auto load_pages = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int ncb, int kt) {
         for (int pg = lane; pg < p.pages_per_tile; pg += 32) {
@@ -256,6 +304,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         load_pages(&tm_v, sV + sv * Cfg::kVBytes, v_full + sv, DV / 64, kt);
+      }
       }
     } else if (lane == 0) {
       int j = 0;

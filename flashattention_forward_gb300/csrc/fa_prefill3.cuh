@@ -275,16 +275,19 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(q_conv + 0), kBlockM);
     mbar_init(smem_u32(q_conv + 1), kBlockM);
+    // barriers the producer fills: one arrival with the TMA bytes, or one per
+    // producer lane for gathered rows (pages of < 16 keys, never with Q8)
+    const uint32_t n_fill = (PAGED && !Q8 && p.gather) ? 32u : 1u;
     for (int s = 0; s < NCK; ++s) {
       // converted K: one arrive per slice; Q8: the TMA arrive + one per producer lane (scales)
-      mbar_init(smem_u32(kc_full + s), Q8 ? 1 + 32 : (FP8 ? 4 : 1));
+      mbar_init(smem_u32(kc_full + s), Q8 ? 1 + 32 : (FP8 ? 4 : n_fill));
       mbar_init(smem_u32(kc_empty + s), 1);
-      mbar_init(smem_u32(kc_stage + s), 1);
+      mbar_init(smem_u32(kc_stage + s), n_fill);
     }
     for (int s = 0; s < NSV; ++s) {
-      mbar_init(smem_u32(v_full + s), FP8 ? 4 * VC : 1);
+      mbar_init(smem_u32(v_full + s), FP8 ? 4 * VC : n_fill);
       mbar_init(smem_u32(v_empty + s), 1);
-      mbar_init(smem_u32(v_stage + s), 1);
+      mbar_init(smem_u32(v_stage + s), n_fill);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(s_full + x), 1);
@@ -377,9 +380,70 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       }
       cp_async_arrive_noinc(smem_u32(kc_full + slot));
     };
+    bool gathered = false;
+    if constexpr (PAGED && !Q8) {
+      if (p.gather) {
+        // Pages of < 16 keys: every key row by its own page-table read and
+        // 16-byte copies (fa_gather.cuh) into the layout a box would fill:
+        // swizzled bf16 blocks, or staged byte rows for the converters.
+        gathered = true;
+        auto pages_of = [&](int kt, int (&pg)[4]) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int key = kt * kBlockN + lane + 32 * u;
+            pg[u] = (kt < pi.kt_hi && key < pi.sk) ? __ldg(bt + (key >> p.page_shift)) : -1;
+          }
+        };
+        // one slot in flight: with Dk 192 a tile has KC = 3 chunks in a
+        // ring of NCK = 4, so the chunk slot the producer waits for frees
+        // only after a QK that reads the chunk committed just before
+        GatherPipe<1> gp;
+        int pg[4], pgn[4];
+        pages_of(first_kt, pg);
+        int j = 0;
+        bool ok = true;
+        for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
+          const int kn = pair_next(p, pi, kt);
+          pages_of(kn, pgn);
+#pragma unroll 1
+          for (int c = 0; c < KC; ++c) {
+            const int n = j * KC + c, slot = n % NCK;
+            if (lane == 0 && n >= NCK) ok = mbar_wait(smem_u32(kc_empty + slot), ((n / NCK) - 1) & 1, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            uint8_t *dst = sK + slot * Cfg::kChunkBytes;
+            if constexpr (kStageK)
+              gather_block<kBlockN, 64, kGatherStage>(dst, p.gk, pi.hk, kt * kBlockN, p.page_size - 1, c * 64, pg, lane);
+            else
+              gather_block<kBlockN, 128, kGatherSw128>(dst, p.gk, pi.hk, kt * kBlockN, p.page_size - 1, c * 128, pg,
+                                                       lane);
+            gp.commit(smem_u32(kStageK ? kc_stage + slot : kc_full + slot));
+          }
+          if (!ok) break;
+          const int sv = j % NSV;
+          if (lane == 0 && j >= NSV) ok = mbar_wait(smem_u32(v_empty + sv), ((j / NSV) - 1) & 1, abort_flag, p.err);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+#pragma unroll
+          for (int c = 0; c < VC; ++c) {
+            uint8_t *dst = sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes;
+            if constexpr (FP8)
+              gather_block<kBlockN, 64, kGatherStage>(dst, p.gv, pi.hk, kt * kBlockN, p.page_size - 1, c * 64, pg, lane);
+            else
+              gather_block<kBlockN, 128, kGatherSw128>(dst, p.gv, pi.hk, kt * kBlockN, p.page_size - 1, c * 128, pg,
+                                                       lane);
+          }
+          gp.commit(smem_u32(FP8 ? v_stage + sv : v_full + sv));
+          kt = kn;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pg[u] = pgn[u];
+        }
+        gp.drain();
+      }
+    }
     int j = 0;
-    bool ok = true;
-    int page = page_at(first_kt);
+    bool ok = !gathered;
+    int page = gathered ? -1 : page_at(first_kt);
     int kpage = ks_page_at(first_kt);
     for (int kt = first_kt; ok && kt < pi.kt_hi; ++j) {
       const int kn = pair_next(p, pi, kt);

@@ -144,7 +144,10 @@ typedef struct {
  *               (causal: i' - j < window; otherwise |i' - j| < window).
  *  score_mod    NULL or fa_score_mod_t.
  *  block_mask   NULL or fa_block_mask_t.
- *  page_size    tokens per page when paged: a power of two, 16 ... 1024.
+ *  page_size    tokens per page when paged: a power of two, 1 ... 1024.
+ *               Pages of 16 or more keys are landed by TMA boxes; pages of
+ *               1 ... 8 keys are gathered key row by key row (same results,
+ *               bit for bit; slower).  e4m3 q needs pages of >= 16 keys.
  *  launch       host scalars (required).
  *  stream       cudaStream_t.
  *

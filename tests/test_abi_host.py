@@ -135,9 +135,9 @@ def test_paged_validation(L):
     st, msg = _call(L, bt=bt, k=k, v=v, page=24)
     assert st == fa.FA_ERR_UNSUPPORTED and "page_size" in msg
     st, msg = _call(L, bt=bt, k=k, v=v, page=2048)
-    assert st == fa.FA_ERR_UNSUPPORTED and "16 to 1024" in msg
-    st, msg = _call(L, bt=bt, k=k, v=v, page=8)
-    assert st == fa.FA_ERR_UNSUPPORTED and "16 to 1024" in msg
+    assert st == fa.FA_ERR_UNSUPPORTED and "1 to 1024" in msg
+    st, msg = _call(L, bt=bt, k=k, v=v, page=8)         # a valid size, but not the cache's
+    assert st == fa.FA_ERR_INVALID_ARG and "page_size" in msg
     st, msg = _call(L, bt=bt, k=k, v=v, page=32)
     assert st == fa.FA_ERR_INVALID_ARG and "page_size" in msg
     st, msg = _call(L, bt=_t(FAKE * 10, fa.FA_I32, [3, 8]), k=k, v=v, page=16)
@@ -175,6 +175,11 @@ def test_e4m3_q_limits(L):
                     launch=fa.Launch(num_seqs=2, max_seqlen_q=1, max_seqlen_k=128, num_splits=4,
                                      total_q=T, total_k=T))
     assert st == fa.FA_ERR_UNSUPPORTED and "split-KV" in msg
+    # pages of < 16 keys are gathered row by row, which e4m3 Q does not have
+    st, msg = _call(L, q=q8, k=_t(FAKE * 2, fa.FA_E4M3, [64, 8, H, 128]), v=_t(FAKE * 3, fa.FA_E4M3, [64, 8, H, 128]),
+                    ks=_t(FAKE * 8, fa.FA_F32, [64, 8, H]), vs=_t(FAKE * 9, fa.FA_F32, [64, 8, H]), out=out,
+                    bt=_t(FAKE * 10, fa.FA_I32, [2, 32]), page=8)
+    assert st == fa.FA_ERR_UNSUPPORTED and "at least 16 keys" in msg
     # a row stride of 8 one-byte elements is not a multiple of 16 bytes
     st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 128], [H * 136, 136, 1]), k=k8, v=v8, ks=ks, vs=vs, out=out)
     assert st == fa.FA_ERR_INVALID_ARG and "16 bytes" in msg
