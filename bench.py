@@ -275,6 +275,68 @@ def e2e_measure(p, steps, dev):
     return statistics.mean(ts), h2d, d2h
 
 
+def e2e_pipelined(problems, steps, dev):
+    """The same end-to-end step (pinned H2D of every input, the forward calls,
+    D2H of out + LSE for every problem) run as a serving loop would: two device
+    buffer sets, so that step i+1's H2D (copy stream) overlaps step i's
+    forward passes (compute stream) and its D2H (return stream).  Every step
+    still moves all of its inputs and results; returns ms per step over the
+    whole loop (first H2D to last D2H)."""
+    sets = []
+    for p in problems:
+        hq = {k: v.cpu().pin_memory() for k, v in dev_tensors(p, "cpu").items()}
+        bufs = []
+        for _ in range(2):
+            dd = {k: torch.empty_like(v, device=dev) for k, v in hq.items()}
+            call, _, out, lse = make_call(p, dd, num_splits=0)
+            out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+            bufs.append((dd, call, out, lse, out_h, lse_h))
+        sets.append((hq, bufs))
+    s_copy, s_comp, s_back = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def loop(n):
+        ev_comp, ev_back = [], []
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(s_copy)
+        for i in range(n):
+            b = i % 2
+            h2d = torch.cuda.Event()
+            with torch.cuda.stream(s_copy):
+                if i >= 2:
+                    s_copy.wait_event(ev_comp[i - 2])      # step i-2 no longer reads buffer set b
+                for hq, bufs in sets:
+                    for k, v in hq.items():
+                        bufs[b][0][k].copy_(v, non_blocking=True)
+                h2d.record(s_copy)
+            ec = torch.cuda.Event()
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(h2d)
+                if i >= 2:
+                    s_comp.wait_event(ev_back[i - 2])      # step i-2's results are home
+                for hq, bufs in sets:
+                    bufs[b][1]()
+                ec.record(s_comp)
+            ev_comp.append(ec)
+            eb = torch.cuda.Event()
+            with torch.cuda.stream(s_back):
+                s_back.wait_event(ec)
+                for hq, bufs in sets:
+                    _, _, out, lse, out_h, lse_h = bufs[b]
+                    out_h.copy_(out, non_blocking=True)
+                    lse_h.copy_(lse, non_blocking=True)
+                eb.record(s_back)
+            ev_back.append(eb)
+        end.record(s_back)
+        end.synchronize()
+        return start.elapsed_time(end) / n
+
+    loop(3)
+    return loop(steps)
+
+
 def cpu_oracle_sample(p, seconds_target=15.0, seed=0):
     """Time the oracle on a bounded seeded row sample; return (flop/s, rows, threads, secs)."""
     import oracle
@@ -440,9 +502,14 @@ def main():
     if rank == 0:
         e2e_c, h2d_c, d2h_c = e2e_measure(p_causal, max(3, args.steps // 2), dev)
         e2e_f, h2d_f, d2h_f = e2e_measure(p_full, max(3, args.steps // 2), dev)
-        e2e = {"value": flops_step / ((e2e_c + e2e_f) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_p = e2e_pipelined([p_causal, p_full], max(6, args.steps // 2), dev)
+        e2e = {"value": flops_step / (e2e_p * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d_c + h2d_f, "d2h_bytes_per_step": d2h_c + d2h_f,
-               "ms_per_step": e2e_c + e2e_f}
+               "ms_per_step": e2e_p,
+               "schedule": "two buffer sets: step i+1's pinned H2D overlaps step i's forward calls and D2H",
+               "serial": {"value": flops_step / ((e2e_c + e2e_f) * 1e-3) / 1e12,
+                          "ms_per_step": e2e_c + e2e_f,
+                          "schedule": "H2D, forward, D2H in sequence on one stream, per problem"}}
         if not args.quick:
             extra = other_workloads(dev, warmup, max(5, args.steps // 2), flush, pk)
         rate, nrows, threads, secs, _ = cpu_oracle_sample(p_full, seed=1)
