@@ -187,7 +187,7 @@ def make_bwd_call(p, t):
     out, lse = fa.fwd_varlen(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
                              max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, softmax_scale=p.softmax_scale,
                              causal=p.causal, window=p.window, num_splits=0, score_mod=p.mod_kind,
-                             alibi_slope=p.alibi_slope, softcap=p.softcap)
+                             alibi_slope=p.alibi_slope, softcap=p.softcap, block_mask=t.get("bm"))
     g = torch.Generator(device="cpu").manual_seed(17)
     dout = torch.randn(out.shape, generator=g).to(torch.bfloat16).to(dev)
     dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
@@ -198,7 +198,7 @@ def make_bwd_call(p, t):
                              max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
                              softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
                              score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap,
-                             dq=dq, dk=dk, dv=dv, workspace=ws)
+                             block_mask=t.get("bm"), dq=dq, dk=dk, dv=dv, workspace=ws)
     return call
 
 
@@ -639,7 +639,9 @@ def other_workloads(dev, warmup, steps, flush, pk):
     for name, p in (("bwd_varlen_8seq_h16_d128_causal", fi.config2(causal=True)),
                     ("bwd_varlen_8seq_h16_d128_noncausal", fi.config2(causal=False)),
                     ("bwd_4x4096_h16_d128_causal", fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, causal=True)),
-                    ("bwd_4x4096_h16_d128_noncausal", fi.make_problem([4096] * 4, hq=16, dk=128, seed=3))):
+                    ("bwd_4x4096_h16_d128_noncausal", fi.make_problem([4096] * 4, hq=16, dk=128, seed=3)),
+                    ("bwd_4x4096_h16_d128_blocksparse50", fi.make_problem([4096] * 4, hq=16, dk=128, seed=3,
+                                                                           block_mask_density=0.5))):
         t = dev_tensors(p, dev)
         call = make_bwd_call(p, t)
         ms = statistics.mean(time_calls([call], warmup, steps, flush))

@@ -102,7 +102,7 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_plan_destroy.argtypes = [ctypes.c_void_p]
             L.fa_fwd_plan_destroy.restype = None
             L.fa_bwd_varlen.argtypes = [P(Tensor)] * 11 + [ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
-                                                          P(ScoreMod), P(Launch), ctypes.c_void_p]
+                                                          P(ScoreMod), P(BlockMask), P(Launch), ctypes.c_void_p]
             L.fa_bwd_varlen.restype = ctypes.c_int
             L.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -145,6 +145,14 @@ def as_tensor(t: Optional[torch.Tensor], fa_dtype: Optional[int] = None) -> Opti
 
 def _ref(x):
     return None if x is None else ctypes.byref(x)
+
+
+def _block_mask(block_mask: Optional[torch.Tensor]):
+    """A uint8 [B*Hq, n_qblk, n_kblk] tensor of 128 x 128 blocks as the C struct (None passes NULL)."""
+    if block_mask is None:
+        return None
+    return BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1], n_kblk=block_mask.shape[2],
+                     blk_q=128, blk_k=128)
 
 
 def _stream_ptr(stream) -> int:
@@ -208,10 +216,7 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         launch.workspace = workspace.data_ptr()
         launch.workspace_bytes = workspace.numel()
     sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
-    bm = None
-    if block_mask is not None:
-        bm = BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1], n_kblk=block_mask.shape[2],
-                       blk_q=128, blk_k=128)
+    bm = _block_mask(block_mask)
     args = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
             as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(k_scale), as_tensor(v_scale),
             as_tensor(out), as_tensor(lse)]
@@ -299,10 +304,7 @@ class FwdPlan:
             self.launch.workspace_bytes = ws.numel()
         self._ws = ws
         sm = ScoreMod(kind=score_mod, alibi_slope=kw.get("alibi_slope", 0.0), softcap=kw.get("softcap", 0.0))
-        bm = None
-        if block_mask is not None:
-            bm = BlockMask(data=block_mask.data_ptr(), n_qblk=block_mask.shape[1], n_kblk=block_mask.shape[2],
-                           blk_q=128, blk_k=128)
+        bm = _block_mask(block_mask)
         descs = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
                  as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(kw.get("k_scale")),
                  as_tensor(kw.get("v_scale")), as_tensor(self.out), as_tensor(self.lse)]
@@ -362,7 +364,8 @@ def bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Ten
                lse: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, *,
                max_seqlen_q: int, max_seqlen_k: int, softmax_scale: Optional[float] = None,
                causal: bool = False, window: int = 0, score_mod: int = MOD_NONE,
-               alibi_slope: float = 0.0, softcap: float = 0.0, dq: Optional[torch.Tensor] = None,
+               alibi_slope: float = 0.0, softcap: float = 0.0, block_mask: Optional[torch.Tensor] = None,
+               dq: Optional[torch.Tensor] = None,
                dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
                workspace: Optional[torch.Tensor] = None, stream=None):
     """Backward pass through ``fa_bwd_varlen``: returns (dq, dk, dv), bf16 with
@@ -386,7 +389,8 @@ def bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Ten
         launch.workspace_bytes = workspace.numel()
     args = [as_tensor(x) for x in (q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, dq, dk, dv)]
     sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
+    bm = _block_mask(block_mask)
     _check(L.fa_bwd_varlen(*[_ref(a) for a in args], ctypes.c_float(softmax_scale), int(bool(causal)),
-                           int(window), ctypes.byref(sm), ctypes.byref(launch),
+                           int(window), ctypes.byref(sm), _ref(bm), ctypes.byref(launch),
                            ctypes.c_void_p(_stream_ptr(stream))))
     return dq, dk, dv

@@ -720,7 +720,7 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
                           const fa_tensor_t *dout, const fa_tensor_t *lse, const fa_tensor_t *cu_seqlens_q,
                           const fa_tensor_t *cu_seqlens_k, fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv,
                           float softmax_scale, int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
-                          const fa_launch_t *launch, void *stream) {
+                          const fa_block_mask_t *block_mask, const fa_launch_t *launch, void *stream) {
   g_msg[0] = 0;
   fa_status_t st;
   if (!launch) return fail(FA_ERR_INVALID_ARG, "launch is NULL");
@@ -762,6 +762,12 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
     cap = score_mod->softcap;
     if (mod == 1 && !std::isfinite(slope)) return fail(FA_ERR_INVALID_ARG, "alibi_slope must be finite");
     if (mod == 2 && !(cap > 0.f && std::isfinite(cap))) return fail(FA_ERR_INVALID_ARG, "softcap must be positive and finite");
+  }
+  if (block_mask) {
+    if (!block_mask->data) return fail(FA_ERR_INVALID_ARG, "block_mask.data is NULL");
+    if (block_mask->blk_q != 128 || block_mask->blk_k != 128) return fail(FA_ERR_UNSUPPORTED, "block masks use 128x128 blocks");
+    if ((int64_t)block_mask->n_qblk * 128 < launch->max_seqlen_q || (int64_t)block_mask->n_kblk * 128 < launch->max_seqlen_k)
+      return fail(FA_ERR_INVALID_ARG, "block_mask does not cover max_seqlen_q/k");
   }
   if (B == 0 || Tq == 0) return FA_OK;
   if (launch->max_seqlen_q <= 0 || launch->max_seqlen_k < 0) return fail(FA_ERR_INVALID_ARG, "bad max_seqlen");
@@ -816,6 +822,9 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
   p.softcap_arg = mod == 2 ? softmax_scale / cap : 0.f;
   p.softcap_log2 = mod == 2 ? cap * fa::kLog2e : 0.f;
   p.alibi_log2 = mod == 1 ? slope * fa::kLog2e : 0.f;
+  p.block_mask = block_mask ? (const uint8_t *)block_mask->data : nullptr;
+  p.n_qblk = block_mask ? block_mask->n_qblk : 0;
+  p.n_kblk = block_mask ? block_mask->n_kblk : 0;
   L.mod = mod;
   fa::BwdDeltaParams &dp = L.dp;
   dp.out = (const __nv_bfloat16 *)out->data;

@@ -141,6 +141,26 @@ __device__ __forceinline__ float bwd_prob(const BwdParams &p, float sraw, float 
   }
 }
 
+// Block sparsity (fkl_python PR #7, flex commit; the forward's 128 x 128
+// block mask): whether block (query tile qb, key tile kb) of head h of
+// sequence b is computed.  Blocks outside the mask's extent are not.
+__device__ __forceinline__ bool bwd_block_live(const BwdParams &p, int b, int h, int qb, int kb) {
+  if (p.block_mask == nullptr) return true;
+  if (qb >= p.n_qblk || kb >= p.n_kblk) return false;
+  return p.block_mask[((int64_t)(b * p.hq + h) * p.n_qblk + qb) * p.n_kblk + kb] != 0;
+}
+
+// The raw step after `raw` (of `n`) whose block is live; n if none.  Every
+// role walks the same live steps with its own cursor, so they agree on the
+// order without a shared list.  Without a block mask (kernel parameter BM
+// false) every block is live and the cursor is raw + 1.
+template <class Live>
+__device__ __forceinline__ int bwd_next_live(int raw, int n, Live live) {
+  ++raw;
+  while (raw < n && !live(raw)) ++raw;
+  return raw;
+}
+
 // Barrier among `count` threads (whole warps) of the CTA, id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -171,7 +191,7 @@ __device__ __forceinline__ void bwd_load_tile(uint8_t *dst, const CUtensorMap *t
 //   S(0) dP(0) | S(t+1) once S(t) is read | dP(t+1) once dP(t) is read |
 //   dQ += dS(t) K(t)
 // so the next tile's contractions run while the rows form dS(t).
-template <int D, int MOD>
+template <int D, int MOD, bool BM>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -197,7 +217,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (!p.causal) hi = min(hi, ip_max + p.window);
   }
   const int klo = lo / 128;
-  const int n_tiles = hi > lo ? (hi + 127) / 128 - klo : 0;
+  const int n_raw = hi > lo ? (hi + 127) / 128 - klo : 0;
+  // key tiles klo + r, r in [0, n_raw), whose block is live
+  auto blk_live = [&](int r) { return !BM || bwd_block_live(p, b, h, qt, klo + r); };
+  int n_tiles = 0;
+  for (int r = bwd_next_live(-1, n_raw, blk_live); r < n_raw; r = bwd_next_live(r, n_raw, blk_live)) ++n_tiles;
   if (n_tiles == 0) {   // no key visible: dQ = 0
     for (int idx = threadIdx.x; idx < (last - q0 + 1) * (D / 8); idx += blockDim.x) {
       const int r = idx / (D / 8), c = idx - r * (D / 8);
@@ -254,16 +278,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_expect_tx(smem_u32(q_full), 2 * TB);
       bwd_load_tile<D>(sQ, &tm_q, q_full, h, qs + q0);
       bwd_load_tile<D>(sDO, &tm_do, q_full, h, qs + q0);
-      // K runs ahead of V (its ring is deeper); issue order K(t), V(t - 1)
+      // K runs ahead of V (its ring is deeper); issue order K(t), V(t - 1);
+      // rk, rv: raw key-tile indices of K(t) and V(t - 1)
+      int rk = bwd_next_live(-1, n_raw, blk_live), rv = rk;
       for (int t = 0; t <= n_tiles; ++t) {
         if (t < n_tiles) {
-          const int st = t % NSK, row = ks + (klo + t) * 128;
+          const int st = t % NSK, row = ks + (klo + rk) * 128;
+          rk = bwd_next_live(rk, n_raw, blk_live);
           if (t >= NSK && !mbar_wait(smem_u32(k_empty + st), ((t / NSK) - 1) & 1, abort_flag, p.err)) break;
           mbar_expect_tx(smem_u32(k_full + st), TB);
           bwd_load_tile<D>(sK + st * TB, &tm_k, k_full + st, hk, row);
         }
         if (t >= 1) {
-          const int u = t - 1, sv = u % NSV, row = ks + (klo + u) * 128;
+          const int u = t - 1, sv = u % NSV, row = ks + (klo + rv) * 128;
+          rv = bwd_next_live(rv, n_raw, blk_live);
           if (u >= NSV && !mbar_wait(smem_u32(v_empty + sv), ((u / NSV) - 1) & 1, abort_flag, p.err)) break;
           mbar_expect_tx(smem_u32(v_full + sv), TB);
           bwd_load_tile<D>(sV + sv * TB, &tm_v, v_full + sv, hk, row);
@@ -346,8 +374,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t rS = tmem + lane_base, rP = tmem + lane_base + 128, rQ = tmem + lane_base + 256;
     bool ok = true;
+    int rt = bwd_next_live(-1, n_raw, blk_live);
     for (int t = 0; t < n_tiles; ++t) {
-      const int j0 = (klo + t) * 128;
+      const int j0 = (klo + rt) * 128;
+      rt = bwd_next_live(rt, n_raw, blk_live);
       ok = mbar_wait(smem_u32(s_full), t & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -443,7 +473,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 //   S^T(0) dP^T(0) | dV += P^T(s) dO(s) once P^T is stored, S^T(s+1) |
 //   dK += dS^T(s) Q(s) once dS^T is stored, dP^T(s+1)
 // so dV and the next S^T run while the keys' warps form dS^T(s).
-template <int D, int MOD>
+template <int D, int MOD, bool BM>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -469,7 +499,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
   const int tlo = qlo / 128;
   const int nqt = qhi > qlo ? (qhi + 127) / 128 - tlo : 0;
-  const int steps = nqt * p.group;
+  // raw step r: q head hk * group + r / nqt, query tile tlo + r % nqt; the
+  // steps taken are the raw steps whose block is live
+  const int n_raw = nqt * p.group;
+  auto blk_live = [&](int r) { return !BM || bwd_block_live(p, b, hk * p.group + r / nqt, tlo + r % nqt, kt); };
+  int steps = 0;
+  for (int r = bwd_next_live(-1, n_raw, blk_live); r < n_raw; r = bwd_next_live(r, n_raw, blk_live)) ++steps;
   if (steps == 0) {   // no query sees these keys: dK = dV = 0
     for (int idx = threadIdx.x; idx < (kl - kj0 + 1) * (D / 8); idx += blockDim.x) {
       const int r = idx / (D / 8), c = idx - r * (D / 8);
@@ -530,15 +565,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     // Q runs ahead of dO (its ring is deeper): issue order Q(s), dO(s - 1)
     if (lane == 0) {
+      int rq = bwd_next_live(-1, n_raw, blk_live), ro = rq;   // raw steps of Q(s) and dO(s - 1)
       for (int s = 0; s <= steps; ++s) {
         if (s < steps) {
-          const int st = s % NSQ, h = hk * p.group + s / nqt, q0 = (tlo + s % nqt) * 128;
+          const int st = s % NSQ, h = hk * p.group + rq / nqt, q0 = (tlo + rq % nqt) * 128;
+          rq = bwd_next_live(rq, n_raw, blk_live);
           if (s >= NSQ && !mbar_wait(smem_u32(q_empty + st), ((s / NSQ) - 1) & 1, abort_flag, p.err)) break;
           mbar_expect_tx(smem_u32(q_full + st), TB);
           bwd_load_tile<D>(sQ + st * TB, &tm_q, q_full + st, h, qs + q0);
         }
         if (s >= 1) {
-          const int u = s - 1, so = u % NSO, h = hk * p.group + u / nqt, q0 = (tlo + u % nqt) * 128;
+          const int u = s - 1, so = u % NSO, h = hk * p.group + ro / nqt, q0 = (tlo + ro % nqt) * 128;
+          ro = bwd_next_live(ro, n_raw, blk_live);
           if (u >= NSO && !mbar_wait(smem_u32(o_empty + so), ((u / NSO) - 1) & 1, abort_flag, p.err)) break;
           mbar_expect_tx(smem_u32(o_full + so), TB);
           bwd_load_tile<D>(sDO + so * TB, &tm_do, o_full + so, h, qs + q0);
@@ -619,19 +657,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // Per-query LSE (log2 units) and Delta of a step, one query per thread;
     // queries past the sequence get LSE = +inf, so that their P is 0.  Loaded
     // a step ahead so that the global-load latency stays off the step.
-    auto load_stat = [&](int s, float &lv, float &dv) {
-      const int h = hk * p.group + s / nqt, i = (tlo + s % nqt) * 128 + r;
+    auto load_stat = [&](int rs, float &lv, float &dv) {   // rs: raw step
+      const int h = hk * p.group + rs / nqt, i = (tlo + rs % nqt) * 128 + r;
       const int64_t at = (int64_t)h * p.total_q + qs + i;
       lv = i < sq ? __ldg(p.lse + at) * kLog2e : INFINITY;
       dv = i < sq ? __ldg(p.delta + at) : 0.f;
     };
     float lv_next, dv_next;
-    load_stat(0, lv_next, dv_next);
+    int rs = bwd_next_live(-1, n_raw, blk_live);   // raw step of step s
+    load_stat(rs, lv_next, dv_next);
     for (int s = 0; s < steps; ++s) {
-      const int q0 = (tlo + s % nqt) * 128;
+      const int q0 = (tlo + rs % nqt) * 128;
+      rs = bwd_next_live(rs, n_raw, blk_live);
       {
         const float lv = lv_next, dv = dv_next;
-        if (s + 1 < steps) load_stat(s + 1, lv_next, dv_next);
+        if (s + 1 < steps) load_stat(rs, lv_next, dv_next);
         named_bar_sync(1, 128);   // the previous step's reads are done
         sStat[r] = lv;
         sStat[128 + r] = dv;

@@ -21,6 +21,8 @@ struct BwdParams {
   float scale_log2;             // softmax_scale * log2(e)
   float scale;                  // softmax_scale
   int *err;
+  const uint8_t *block_mask;    // [B*Hq, n_qblk, n_kblk] (128 x 128 blocks, 0 = skipped) or null
+  int n_qblk, n_kblk;
   float softcap_arg;            // soft-cap: softmax_scale / cap
   float softcap_log2;           // soft-cap: cap * log2(e)
   float alibi_log2;             // ALiBi: slope * log2(e)

@@ -250,7 +250,9 @@ FA_API fa_status_t fa_combine(const float *o_part, const float *lse_part, int32_
  *                     same (q, k, v, masks).
  *  cu_seqlens_q/k     int32 [num_seqs + 1] (row offsets of q and of k/v).
  *  softmax_scale      > 0;  causal, window, score_mod (NULL or kind 0, 1, 2)
- *                     as in fa_fwd_varlen; block masks are not supported here.
+ *                     and block_mask (NULL or 128 x 128 blocks) as in
+ *                     fa_fwd_varlen: a skipped block adds nothing to any
+ *                     gradient.
  *  launch             num_seqs, max_seqlen_q/k, total_q (= T_q) and a
  *                     workspace of fa_bwd_workspace_bytes(T_q, Hq) bytes,
  *                     256-byte aligned, for Delta (fp32 [Hq, T_q]).
@@ -266,7 +268,7 @@ FA_API fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, con
                           const fa_tensor_t *cu_seqlens_q, const fa_tensor_t *cu_seqlens_k,
                           fa_tensor_t *dq, fa_tensor_t *dk, fa_tensor_t *dv, float softmax_scale,
                           int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
-                          const fa_launch_t *launch, void *stream);
+                          const fa_block_mask_t *block_mask, const fa_launch_t *launch, void *stream);
 
 /* Workspace bytes of fa_bwd_varlen: Delta, fp32 [Hq, T_q], rounded up to 256. */
 FA_API size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);

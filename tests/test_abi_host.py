@@ -245,13 +245,14 @@ def _bcall(L, **over):
         dout=_t(FAKE * 5, fa.FA_BF16, [T, H, D]), lse=_t(FAKE * 6, fa.FA_F32, [H, T]),
         cq=_t(FAKE * 7, fa.FA_I32, [3]), ck=_t(FAKE * 8, fa.FA_I32, [3]),
         dq=_t(FAKE * 9, fa.FA_BF16, [T, H, D]), dk=_t(FAKE * 10, fa.FA_BF16, [T, H, D]),
-        dv=_t(FAKE * 11, fa.FA_BF16, [T, H, D]), scale=0.125, causal=1, window=0, mod=None,
+        dv=_t(FAKE * 11, fa.FA_BF16, [T, H, D]), scale=0.125, causal=1, window=0, mod=None, bm=None,
         launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=0, total_q=T, total_k=T,
                          workspace=ws, workspace_bytes=fa.bwd_workspace_bytes(T, H)))
     args.update(over)
     r = lambda x: None if x is None else ctypes.byref(x)
     st = L.fa_bwd_varlen(*[r(args[n]) for n in ("q", "k", "v", "out", "dout", "lse", "cq", "ck", "dq", "dk", "dv")],
-                         args["scale"], args["causal"], args["window"], r(args["mod"]), r(args["launch"]), None)
+                         args["scale"], args["causal"], args["window"], r(args["mod"]), r(args["bm"]),
+                         r(args["launch"]), None)
     return st, L.fa_last_error().decode()
 
 
@@ -275,6 +276,9 @@ def test_bwd_workspace_bytes(L):
     (dict(mod=fa.ScoreMod(kind=2, softcap=-1.0)), fa.FA_ERR_INVALID_ARG, "softcap"),
     (dict(mod=fa.ScoreMod(kind=1, alibi_slope=float("inf"))), fa.FA_ERR_INVALID_ARG, "alibi_slope"),
     (dict(mod=fa.ScoreMod(kind=3)), fa.FA_ERR_INVALID_ARG, "kind"),
+    (dict(bm=fa.BlockMask(data=FAKE * 12, n_qblk=1, n_kblk=0, blk_q=128, blk_k=128)), fa.FA_ERR_INVALID_ARG,
+     "does not cover"),
+    (dict(bm=fa.BlockMask(data=FAKE * 12, n_qblk=2, n_kblk=2, blk_q=64, blk_k=64)), fa.FA_ERR_UNSUPPORTED, "128x128"),
     (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=256, total_k=256)),
      fa.FA_ERR_INVALID_ARG, "workspace"),
     (dict(launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=256, total_k=256,

@@ -48,7 +48,8 @@ def run_bwd(p, seed=11):
     dq, dk, dv = fa.bwd_varlen(t["q"], t["k"], t["v"], out, dout, lse, t["cu_q"], t["cu_k"],
                                max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
                                softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
-                               score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap)
+                               score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap,
+                               block_mask=t.get("bm"))
     torch.cuda.synchronize()
     g = [x.float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
     return g, fi.bf16_to_f32(dob).astype(np.float64)
@@ -89,6 +90,12 @@ CASES = {
     "softcap_window_gqa_d64": dict(lens_q=[400], lens_k=[500], hq=4, hkv=2, dk=64, window=90, mod="softcap",
                                    softcap=5.0),
     "softcap_saturated_d64": dict(lens_q=[200, 130], hq=4, dk=64, mod="softcap", softcap=0.5, softmax_scale=1.0),
+    # 128 x 128 block sparsity: skipped blocks add nothing; rows whose blocks
+    # are all skipped have LSE = -inf and zero gradients
+    "blocksparse_d128": dict(lens_q=[300, 129], lens_k=[330, 400], hq=4, hkv=2, dk=128, block_mask_density=0.5),
+    "blocksparse_causal_d64": dict(lens_q=[520, 70], hq=4, dk=64, causal=True, block_mask_density=0.4),
+    "blocksparse_alibi_gqa": dict(lens_q=[260, 390], hq=8, hkv=2, dk=128, mod="alibi", alibi_slope=0.03,
+                                  block_mask_density=0.6),
 }
 
 

@@ -4,7 +4,7 @@ things other than itself, on the CPU.
 * Central finite differences of the forward oracle (itself pinned in
   test_oracle_pins.py): the gradient of L = sum(dO * out) in q, k and v is
   checked entry by entry, including the soft-cap and ALiBi score mods, windows,
-  GQA and Sq != Sk.
+  GQA, Sq != Sk and a 128 x 128 block mask.
 * torch autograd in float64 on an explicit masked softmax attention.
 * Closed forms: with identical keys every row's scores are equal, so dQ = 0
   and dV_j is the mean of dO over the rows that see key j; a single key gives
@@ -39,6 +39,8 @@ FD_CASES = [
     dict(lens_q=[5, 3], hq=2, dk=8, mod="softcap", softcap=0.7, causal=True),    # cap in the curved part
     dict(lens_q=[5], hq=2, dk=8, mod="alibi", alibi_slope=0.5),
     dict(lens_q=[4], lens_k=[2], hq=2, dk=8, causal=True),                       # Sq > Sk: masked rows
+    dict(lens_q=[200, 140], lens_k=[260, 140], hq=2, dk=8, causal=True,          # 128 x 128 block mask
+         block_mask_density=0.5),
 ]
 
 
