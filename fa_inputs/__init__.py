@@ -123,6 +123,9 @@ class Problem:
     block_mask: Optional[np.ndarray] = None    # uint8 [B*Hq, nqb, nkb]
     q_dtype: str = "bf16"                      # "bf16" (uint16 bits) or "e4m3" (uint8 bytes; its
                                                # per-tensor scale is folded into softmax_scale)
+    # prologue maps x -> mul * x + add on Q, K, V as read:
+    # (q_mul, q_add, k_mul, k_add, v_mul, v_add); None = identity
+    prologue: Optional[tuple] = None
 
     @property
     def num_seqs(self) -> int:

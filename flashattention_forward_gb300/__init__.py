@@ -51,6 +51,38 @@ class BlockMask(ctypes.Structure):
                 ("blk_q", ctypes.c_int32), ("blk_k", ctypes.c_int32)]
 
 
+class Prologue(ctypes.Structure):
+    _fields_ = [("q_mul", ctypes.c_float), ("q_add", ctypes.c_float), ("k_mul", ctypes.c_float),
+                ("k_add", ctypes.c_float), ("v_mul", ctypes.c_float), ("v_add", ctypes.c_float)]
+
+
+def make_prologue(prologue) -> Optional[Prologue]:
+    """The C prologue for ``prologue``: None, a Prologue, or a dict mapping
+    "q", "k", "v" to op chains applied in order to each element as read --
+    ("mul", c), ("div", c), ("add", c), ("sub", c) -- composed into one map
+    x -> mul * x + add per tensor."""
+    if prologue is None or isinstance(prologue, Prologue):
+        return prologue
+    maps = {}
+    for name in ("q", "k", "v"):
+        m, a = 1.0, 0.0
+        for op, c in prologue.get(name, ()):
+            c = float(c)
+            if op == "mul":
+                m, a = m * c, a * c
+            elif op == "div":
+                m, a = m / c, a / c
+            elif op == "add":
+                a = a + c
+            elif op == "sub":
+                a = a - c
+            else:
+                raise ValueError(f"prologue op {op!r}: mul, div, add or sub")
+        maps[name] = (m, a)
+    return Prologue(q_mul=maps["q"][0], q_add=maps["q"][1], k_mul=maps["k"][0], k_add=maps["k"][1],
+                    v_mul=maps["v"][0], v_add=maps["v"][1])
+
+
 class Launch(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
                 ("max_seqlen_k", ctypes.c_int32), ("num_splits", ctypes.c_int32),
@@ -76,8 +108,8 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             P = ctypes.POINTER
             L.fa_fwd_varlen.argtypes = [P(Tensor)] * 8 + [P(Tensor), P(Tensor), ctypes.c_float, ctypes.c_int32,
-                                                         ctypes.c_int32, P(ScoreMod), P(BlockMask), ctypes.c_int32,
-                                                         P(Launch), ctypes.c_void_p]
+                                                         ctypes.c_int32, P(ScoreMod), P(BlockMask), P(Prologue),
+                                                         ctypes.c_int32, P(Launch), ctypes.c_void_p]
             L.fa_fwd_varlen.restype = ctypes.c_int
             L.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.c_int32]
@@ -177,7 +209,7 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                score_mod: int = MOD_NONE, alibi_slope: float = 0.0, softcap: float = 0.0,
                block_mask: Optional[torch.Tensor] = None, num_splits: Optional[int] = None,
                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-               return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None):
+               return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None, prologue=None):
     """Attention forward over packed varlen Q and packed or paged K/V.
 
     q [T_q, Hq, Dk] bf16, or float8_e4m3fn with e4m3 caches at Dk = Dv = 128
@@ -187,7 +219,8 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     k_scale/v_scale); cu_seqlens int32 [B+1].  ``max_seqlen_q/k`` are host ints (no
     device read-back).  Returns ``(out [T_q, Hq, Dv] bf16, lse [Hq, T_q] fp32
     or None)``.  ``num_splits=None`` picks the library's default (split-KV for
-    decode shapes); 0 forces the single-pass kernel.
+    decode shapes); 0 forces the single-pass kernel.  ``prologue``: op chains
+    on Q/K/V reads (see make_prologue and fa_prologue_t).
     """
     L = lib()
     B = cu_seqlens_q.shape[0] - 1
@@ -217,11 +250,12 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         launch.workspace_bytes = workspace.numel()
     sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
     bm = _block_mask(block_mask)
+    pro = make_prologue(prologue)
     args = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
             as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(k_scale), as_tensor(v_scale),
             as_tensor(out), as_tensor(lse)]
     st = L.fa_fwd_varlen(*[_ref(a) for a in args], float(softmax_scale), int(bool(causal)), int(window),
-                         ctypes.byref(sm), _ref(bm), int(page_size), ctypes.byref(launch),
+                         ctypes.byref(sm), _ref(bm), _ref(pro), int(page_size), ctypes.byref(launch),
                          ctypes.c_void_p(_stream_ptr(stream)))
     _check(st)
     return out, lse
@@ -250,8 +284,8 @@ def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
             as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), None, None, as_tensor(out), as_tensor(lse)]
     sm = ScoreMod(kind=MOD_NONE)
     _check(L.fa_fwd_varlen_noalloc(*[_ref(a) for a in args], float(softmax_scale), int(bool(causal)),
-                                   int(window), ctypes.byref(sm), None, int(page_size), ctypes.byref(launch),
-                                   ctypes.c_void_p(_stream_ptr(stream))))
+                                   int(window), ctypes.byref(sm), None, None, int(page_size),
+                                   ctypes.byref(launch), ctypes.c_void_p(_stream_ptr(stream))))
     return out, lse
 
 
@@ -305,6 +339,7 @@ class FwdPlan:
         self._ws = ws
         sm = ScoreMod(kind=score_mod, alibi_slope=kw.get("alibi_slope", 0.0), softcap=kw.get("softcap", 0.0))
         bm = _block_mask(block_mask)
+        pro = make_prologue(kw.get("prologue"))
         descs = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
                  as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(kw.get("k_scale")),
                  as_tensor(kw.get("v_scale")), as_tensor(self.out), as_tensor(self.lse)]
@@ -312,7 +347,8 @@ class FwdPlan:
         _check(L.fa_fwd_plan_create(*[_ref(a) for a in descs], ctypes.c_float(scale),
                                     ctypes.c_int32(int(bool(kw.get("causal", False)))),
                                     ctypes.c_int32(int(kw.get("window", 0))), ctypes.byref(sm), _ref(bm),
-                                    ctypes.c_int32(int(page_size)), ctypes.byref(self.launch), ctypes.byref(handle)))
+                                    _ref(pro), ctypes.c_int32(int(page_size)), ctypes.byref(self.launch),
+                                    ctypes.byref(handle)))
         self._plan = handle
         self._launch_fn = L.fa_fwd_plan_launch
         self._destroy_fn = L.fa_fwd_plan_destroy

@@ -196,8 +196,9 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
                       const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
                       const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
                       fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
-                      const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
-                      const fa_launch_t *launch, void *stream, fa_fwd_plan_s *plan);
+                      const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask,
+                      const fa_prologue_t *prologue, int32_t page_size, const fa_launch_t *launch, void *stream,
+                      fa_fwd_plan_s *plan);
 
 }  // namespace
 
@@ -269,10 +270,10 @@ fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cache, cons
                           const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
                           const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
                           fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
-                          const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
-                          const fa_launch_t *launch, void *stream) {
+                          const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask,
+                          const fa_prologue_t *prologue, int32_t page_size, const fa_launch_t *launch, void *stream) {
   return fwd_build(q, k_cache, v_cache, block_table, cu_seqlens_q, cu_seqlens_k, k_scale, v_scale, out, lse,
-                   softmax_scale, causal, window, score_mod, block_mask, page_size, launch, stream, nullptr);
+                   softmax_scale, causal, window, score_mod, block_mask, prologue, page_size, launch, stream, nullptr);
 }
 
 fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa_tensor_t *v_cache,
@@ -280,15 +281,15 @@ fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k_cache,
                                const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale,
                                const fa_tensor_t *v_scale, fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
                                int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
-                               const fa_block_mask_t *block_mask, int32_t page_size, const fa_launch_t *launch,
-                               fa_fwd_plan_t *plan) {
+                               const fa_block_mask_t *block_mask, const fa_prologue_t *prologue, int32_t page_size,
+                               const fa_launch_t *launch, fa_fwd_plan_t *plan) {
   if (!plan) return fail(FA_ERR_INVALID_ARG, "plan is NULL");
   *plan = nullptr;
   fa_fwd_plan_s *P = new (std::nothrow) fa_fwd_plan_s();
   if (!P) return fail(FA_ERR_INVALID_ARG, "out of host memory");
   const fa_status_t st = fwd_build(q, k_cache, v_cache, block_table, cu_seqlens_q, cu_seqlens_k, k_scale, v_scale,
-                                   out, lse, softmax_scale, causal, window, score_mod, block_mask, page_size, launch,
-                                   nullptr, P);
+                                   out, lse, softmax_scale, causal, window, score_mod, block_mask, prologue, page_size,
+                                   launch, nullptr, P);
   if (st != FA_OK) {
     delete P;
     return st;
@@ -315,8 +316,9 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
                       const fa_tensor_t *block_table, const fa_tensor_t *cu_seqlens_q,
                       const fa_tensor_t *cu_seqlens_k, const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
                       fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale, int32_t causal, int32_t window,
-                      const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, int32_t page_size,
-                      const fa_launch_t *launch, void *stream, fa_fwd_plan_s *plan) {
+                      const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask,
+                      const fa_prologue_t *prologue, int32_t page_size, const fa_launch_t *launch, void *stream,
+                      fa_fwd_plan_s *plan) {
   fa_status_t st;
   g_msg[0] = 0;
   if (!launch) return fail(FA_ERR_INVALID_ARG, "launch is NULL");
@@ -436,6 +438,25 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if ((int64_t)block_mask->n_qblk * 128 < launch->max_seqlen_q || (int64_t)block_mask->n_kblk * 128 < launch->max_seqlen_k)
       return fail(FA_ERR_INVALID_ARG, "block_mask does not cover max_seqlen_q/k");
   }
+  // ---- prologue: folded (see fa_prologue_t) -- q_mul * k_mul into the
+  // score scale, k_add into an LSE term per unit of sum_d q, v_* into the
+  // output
+  float pro_vmul = 1.f, pro_vadd = 0.f, pro_lse_k = 0.f;
+  if (prologue) {
+    const float vals[6] = {prologue->q_mul, prologue->q_add, prologue->k_mul,
+                           prologue->k_add, prologue->v_mul, prologue->v_add};
+    for (float x : vals)
+      if (!std::isfinite(x)) return fail(FA_ERR_INVALID_ARG, "prologue values must be finite");
+    if (prologue->q_add != 0.f)
+      return fail(FA_ERR_UNSUPPORTED, "prologue q_add must be 0 (it would add a per-key term to the scores)");
+    if (prologue->k_add != 0.f && mod == 2)
+      return fail(FA_ERR_UNSUPPORTED, "prologue k_add with the soft-cap (the cap is not shift-invariant)");
+    if (prologue->k_add != 0.f && q8) return fail(FA_ERR_UNSUPPORTED, "prologue k_add with e4m3 q");
+    pro_lse_k = softmax_scale * prologue->q_mul * prologue->k_add;
+    softmax_scale = softmax_scale * (prologue->q_mul * prologue->k_mul);
+    pro_vmul = prologue->v_mul;
+    pro_vadd = prologue->v_add;
+  }
   if (window < 0) window = 0;
   if (B == 0 || Tq == 0) return FA_OK;
   if (launch->max_seqlen_q <= 0) return fail(FA_ERR_INVALID_ARG, "max_seqlen_q must be > 0 when total_q > 0");
@@ -510,6 +531,9 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
       p.gk = kv_gather(k_cache, esz);
       p.gv = kv_gather(v_cache, esz);
     }
+    p.pro_vmul = pro_vmul;
+    p.pro_vadd = pro_vadd;
+    p.pro_lse_k = pro_lse_k;
     p.hq = (int)Hq;
     p.hkv = (int)Hkv;
     p.group = group;
@@ -645,6 +669,12 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.gk = kv_gather(k_cache, esz);
     p.gv = kv_gather(v_cache, esz);
   }
+  p.pro_vmul = pro_vmul;
+  p.pro_vadd = pro_vadd;
+  p.pro_lse_k = pro_lse_k;
+  p.q = (const __nv_bfloat16 *)q->data;
+  p.q_stride_t = q->stride[0];
+  p.q_stride_h = q->stride[1];
   p.pages_per_tile = fa::kBlockN / p.rows_per_box;
   p.n_qtiles = (int)n_qtiles;
   p.causal = causal != 0;

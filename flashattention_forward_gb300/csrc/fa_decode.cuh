@@ -62,6 +62,9 @@ struct DecodeParams {
   const float *k_scale, *v_scale;     // byte caches: per (token, kv head), in the cache's token order
   int32_t gather;                     // pages of < 16 keys: K/V rows by cp.async (fa_gather.cuh)
   KvGather gk, gv;
+  // folded prologue: partial or final out = pro_vmul * o + pro_vadd on rows
+  // that see keys; LSE += pro_lse_k * sum_d q[d]
+  float pro_vmul, pro_vadd, pro_lse_k;
 };
 
 template <int D, int KV = 0>
@@ -630,9 +633,16 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         }
         const bool has = L > 0.f;
         const float inv = has ? 1.f / L : 0.f;
+        const float sc = inv * p.pro_vmul;   // prologue's V map folded into the normalisation
         const int tq = row / p.group, h = hk * p.group + row % p.group;
         const int64_t t = (int64_t)qa + tq;
-        const float lse_v = has ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        float lse_v = has ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        if (has && p.pro_lse_k != 0.f) {   // prologue's K shift, carried by the LSE
+          const __nv_bfloat16 *qrow = p.q + t * p.q_stride_t + (int64_t)h * p.q_stride_h;
+          float qs = 0.f;
+          for (int d = 0; d < D; ++d) qs += __bfloat162float(qrow[d]);
+          lse_v += p.pro_lse_k * qs;
+        }
         if (p.o_part) {
           float *dst = p.o_part + (((int64_t)split * p.total_q + t) * p.hq + h) * D + sl * kSlice;
 #pragma unroll
@@ -644,7 +654,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
               float acc = 0.f;
 #pragma unroll
               for (int w = 0; w < kDecWarps; ++w) acc += wgt[w] * red_o[(w * kDecRows + row) * D + sl * kSlice + d + e];
-              vv[e] = acc * inv;
+              vv[e] = has ? fmaf(acc, sc, p.pro_vadd) : 0.f;
             }
             *reinterpret_cast<float4 *>(dst + d) = v;
           }
@@ -659,7 +669,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
               acc0 += wgt[w] * red_o[(w * kDecRows + row) * D + sl * kSlice + d];
               acc1 += wgt[w] * red_o[(w * kDecRows + row) * D + sl * kSlice + d + 1];
             }
-            *reinterpret_cast<uint32_t *>(dst + d) = pack_bf16x2(acc0 * inv, acc1 * inv);
+            *reinterpret_cast<uint32_t *>(dst + d) =
+                has ? pack_bf16x2(fmaf(acc0, sc, p.pro_vadd), fmaf(acc1, sc, p.pro_vadd)) : 0u;
           }
           if (sl == 0 && p.lse) p.lse[(int64_t)h * p.total_q + t] = lse_v;
         }

@@ -62,8 +62,8 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tens
                                              const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
                                              fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
                                              int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
-                                             const fa_block_mask_t *block_mask, int32_t page_size,
-                                             const fa_launch_t *launch, void *stream) {
+                                             const fa_block_mask_t *block_mask, const fa_prologue_t *prologue,
+                                             int32_t page_size, const fa_launch_t *launch, void *stream) {
   if (!launch || !q || !k_cache || !v_cache)
     return fa::set_host_error(FA_ERR_INVALID_ARG, "launch, q, k_cache and v_cache are required");
   if (q->ndim != 3 || k_cache->ndim < 3 || v_cache->ndim != k_cache->ndim)
@@ -93,5 +93,5 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tens
   L.workspace = scratch;
   L.workspace_bytes = (size_t)FA_NOALLOC_SCRATCH_BYTES;
   return fa_fwd_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, cu_seqlens_k, k_scale, v_scale, out, lse,
-                       softmax_scale, causal, window, score_mod, block_mask, page_size, &L, stream);
+                       softmax_scale, causal, window, score_mod, block_mask, prologue, page_size, &L, stream);
 }

@@ -49,7 +49,26 @@ struct PrefillParams {
   int32_t n_items;      // work items (persistent kernels stride over them)
   int32_t gather;       // pages of < 16 keys: K/V rows by cp.async (fa_gather.cuh), not TMA boxes
   KvGather gk, gv;      // the caches' byte geometry for the gather
+  // folded prologue: out = pro_vmul * o + pro_vadd on rows that see keys;
+  // LSE += pro_lse_k * sum_d q[d] (bf16 q read back only when pro_lse_k != 0)
+  float pro_vmul, pro_vadd, pro_lse_k;
+  const __nv_bfloat16 *q;
+  int64_t q_stride_t, q_stride_h;   // elements
 };
+
+// sum_d q[d] of one bf16 query row (16-byte loads), for the prologue's LSE term.
+template <int D>
+__device__ __forceinline__ float q_row_sum(const __nv_bfloat16 *row) {
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(row + c * 8);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+  return acc;
+}
 
 // Block order: for each sequence, for each group of `head_group` heads, query
 // tiles from the latest (longest under a causal mask) to the first, the heads

@@ -1027,6 +1027,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
           tc_fence_after();
           const bool has = l > 0.f;
           const float inv_l = has ? 1.f / l : 0.f;
+          const float sc = inv_l * p.pro_vmul;   // prologue's V map folded into the normalisation
           const uint32_t oa = tmem + lane_base + colO;
 #pragma unroll
           for (int c = 0; c < DV / 32; ++c) {
@@ -1035,15 +1036,21 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
             tmem_wait_ld();
             uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = has ? pack_bf16x2(o[2 * e] * inv_l, o[2 * e + 1] * inv_l) : 0u;
+            for (int e = 0; e < 16; ++e)
+              w[e] = has ? pack_bf16x2(fmaf(o[2 * e], sc, p.pro_vadd), fmaf(o[2 * e + 1], sc, p.pro_vadd)) : 0u;
             if (row_ok) {
               uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
               for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
             }
           }
-          if (row_ok && p.lse)
-            p.lse[(int64_t)pi.h * p.total_q + t] = has ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+          if (row_ok && p.lse) {
+            float lv = has ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+            // prologue's K shift: the softmax cancels it, the LSE carries it
+            if (has && p.pro_lse_k != 0.f)
+              lv += p.pro_lse_k * q_row_sum<DK>(p.q + t * p.q_stride_t + (int64_t)pi.h * p.q_stride_h);
+            p.lse[(int64_t)pi.h * p.total_q + t] = lv;
+          }
         }
       }
     }

@@ -90,6 +90,23 @@ typedef struct {
     float softcap;
 } fa_score_mod_t;
 
+/* Prologue (fkl_python PR #7, prologue commit: op chains fused onto the
+ * Q/K/V reads, values passed at run time): each element x of Q, K and V is
+ * read as mul * x + add -- a chain of Mul/Add/Sub/Div by scalars composes to
+ * one such map per tensor.  The kernels fold the maps instead of rewriting
+ * the operands, which is exact in real arithmetic:
+ *   q_mul * k_mul scales the scores (it multiplies softmax_scale);
+ *   k_add adds softmax_scale * q_mul * k_add * sum_d q_i[d] to every score
+ *     of row i: the softmax cancels it and the LSE carries it;
+ *   v_mul, v_add act on the output (the softmax weights sum to 1).
+ * Limits (FA_ERR_UNSUPPORTED): q_add must be 0 (it would add a per-key term
+ * q_add * k_mul * sum_d k_j[d]); k_add must be 0 with the soft-cap (not
+ * shift-invariant) and with e4m3 q.  Rows that see no key keep out = 0 and
+ * LSE = -inf.  NULL, or mul = 1 and add = 0 everywhere, is no prologue. */
+typedef struct {
+    float q_mul, q_add, k_mul, k_add, v_mul, v_add;
+} fa_prologue_t;
+
 /* 128x128 block-sparsity mask, uint8 [num_seqs * Hq][n_qblk][n_kblk],
  * contiguous; block (qb, kb) of sequence b, head h is active when
  * data[((b*Hq + h)*n_qblk + qb)*n_kblk + kb] != 0, with qb = i/128 and
@@ -144,6 +161,7 @@ typedef struct {
  *               (causal: i' - j < window; otherwise |i' - j| < window).
  *  score_mod    NULL or fa_score_mod_t.
  *  block_mask   NULL or fa_block_mask_t.
+ *  prologue     NULL or fa_prologue_t.
  *  page_size    tokens per page when paged: a power of two, 1 ... 1024.
  *               Pages of 16 or more keys are landed by TMA boxes; pages of
  *               1 ... 8 keys are gathered key row by key row (same results,
@@ -168,8 +186,8 @@ FA_API fa_status_t fa_fwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k_cach
                           const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
                           fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
                           int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
-                          const fa_block_mask_t *block_mask, int32_t page_size,
-                          const fa_launch_t *launch, void *stream);
+                          const fa_block_mask_t *block_mask, const fa_prologue_t *prologue,
+                          int32_t page_size, const fa_launch_t *launch, void *stream);
 
 /*
  * Prepared calls.  fa_fwd_plan_create validates a forward call exactly like
@@ -193,7 +211,8 @@ FA_API fa_status_t fa_fwd_plan_create(const fa_tensor_t *q, const fa_tensor_t *k
                                const fa_tensor_t *v_scale, fa_tensor_t *out, fa_tensor_t *lse,
                                float softmax_scale, int32_t causal, int32_t window,
                                const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask,
-                               int32_t page_size, const fa_launch_t *launch, fa_fwd_plan_t *plan);
+                               const fa_prologue_t *prologue, int32_t page_size, const fa_launch_t *launch,
+                               fa_fwd_plan_t *plan);
 FA_API fa_status_t fa_fwd_plan_launch(fa_fwd_plan_t plan, void *stream);
 FA_API void fa_fwd_plan_destroy(fa_fwd_plan_t plan);
 
@@ -307,8 +326,8 @@ FA_API fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tensor_t
                                   const fa_tensor_t *k_scale, const fa_tensor_t *v_scale,
                                   fa_tensor_t *out, fa_tensor_t *lse, float softmax_scale,
                                   int32_t causal, int32_t window, const fa_score_mod_t *score_mod,
-                                  const fa_block_mask_t *block_mask, int32_t page_size,
-                                  const fa_launch_t *launch, void *stream);
+                                  const fa_block_mask_t *block_mask, const fa_prologue_t *prologue,
+                                  int32_t page_size, const fa_launch_t *launch, void *stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 FA_API const char *fa_last_error(void);

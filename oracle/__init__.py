@@ -59,6 +59,8 @@ class _Problem(ctypes.Structure):
         ("blk_q", ctypes.c_int32), ("blk_k", ctypes.c_int32),
         ("kv_lo", ctypes.c_int64), ("kv_hi", ctypes.c_int64),
         ("q_dtype", ctypes.c_int32),
+        ("q_mul", ctypes.c_double), ("q_add", ctypes.c_double), ("k_mul", ctypes.c_double),
+        ("k_add", ctypes.c_double), ("v_mul", ctypes.c_double), ("v_add", ctypes.c_double),
     ]
 
 
@@ -141,6 +143,8 @@ def _problem(p, keep, kv_range=None, q_f64=None, k_f64=None, v_f64=None):
         blk_q=128, blk_k=128,
         kv_lo=(kv_range[0] if kv_range else 0), kv_hi=(kv_range[1] if kv_range else -1),
         q_dtype=qd)
+    pro = getattr(p, "prologue", None) or (1.0, 0.0, 1.0, 0.0, 1.0, 0.0)
+    prob.q_mul, prob.q_add, prob.k_mul, prob.k_add, prob.v_mul, prob.v_add = (float(x) for x in pro)
     return prob, c
 
 

@@ -37,7 +37,11 @@
  *  - bottom-right causal alignment: FlyDSL PR #1066 review (COMMENT, "What I
  *    verified": bottom-right causal mask, cross_seqlen=True);
  *  - ALiBi, SoftCap, SlidingWindow and 128x128 block masks: fkl_python PR #7,
- *    flex attention commit.
+ *    flex attention commit;
+ *  - prologue: every element of Q, K and V taken as mul * x + add as it is
+ *    read (an op chain of Mul/Add by scalars, composed), before anything
+ *    else: fkl_python PR #7, prologue-fusion commit (op chains fused onto the
+ *    Q/K/V reads, values at run time).
  *
  * Readings where the pages are silent (each also listed in the design notes):
  * i' = i + Sk - Sq; window W>0 keeps 0 <= i'-j < W when causal, |i'-j| < W
@@ -75,6 +79,7 @@ typedef struct {
     int32_t n_qblk, n_kblk, blk_q, blk_k;
     int64_t kv_lo, kv_hi;         /* restrict keys to [kv_lo, kv_hi) when kv_hi >= 0 */
     int32_t q_dtype;              /* Q_BF16 | Q_E4M3 (a per-tensor Q scale is folded into softmax_scale) | Q_F64 */
+    double q_mul, q_add, k_mul, k_add, v_mul, v_add;   /* prologue maps (1, 0 = none) */
 } fa_oracle_problem;
 
 enum { Q_BF16 = 0, Q_E4M3 = 1, Q_F64 = 2 };
@@ -103,8 +108,9 @@ double fa_oracle_e4m3_decode(uint8_t x) {
     return s ? -mag : mag;
 }
 
-/* Row j of the sequence's keys (or values) for kv head hk, widened to double. */
-static void fetch_row(const fa_oracle_problem *p, const void *base, const float *scale,
+/* Row j of the sequence's keys (or values) for kv head hk, widened to double
+ * and taken through the tensor's prologue map x -> mul * x + add. */
+static void fetch_row(const fa_oracle_problem *p, const void *base, const float *scale, double mul, double add,
                       int b, int64_t j, int hk, int d, double *dst) {
     int64_t tok;       /* flat token index in the [*, Hkv] view of the pool */
     if (p->block_table) {
@@ -122,17 +128,20 @@ static void fetch_row(const fa_oracle_problem *p, const void *base, const float 
         else if (p->kv_dtype == KV_E4M3) val = fa_oracle_e4m3_decode(((const uint8_t *)base)[off + x]);
         else if (p->kv_dtype == KV_I8) val = fa_oracle_i8_decode(((const uint8_t *)base)[off + x]);
         else val = ((const double *)base)[off + x];
-        dst[x] = val * sc;
+        dst[x] = mul * (val * sc) + add;
     }
 }
 
-/* Query row (token t, head h) widened to double. */
+/* Query row (token t, head h) widened to double and taken through q's
+ * prologue map. */
 static void fetch_q(const fa_oracle_problem *p, int64_t t, int h, double *qrow) {
     for (int x = 0; x < p->dk; x++) {
         const int64_t at = (t * p->hq + h) * (int64_t)p->dk + x;
-        if (p->q_dtype == Q_E4M3) qrow[x] = fa_oracle_e4m3_decode(((const uint8_t *)p->q)[at]);
-        else if (p->q_dtype == Q_F64) qrow[x] = ((const double *)p->q)[at];
-        else qrow[x] = fa_oracle_bf16_decode(((const uint16_t *)p->q)[at]);
+        double val;
+        if (p->q_dtype == Q_E4M3) val = fa_oracle_e4m3_decode(((const uint8_t *)p->q)[at]);
+        else if (p->q_dtype == Q_F64) val = ((const double *)p->q)[at];
+        else val = fa_oracle_bf16_decode(((const uint16_t *)p->q)[at]);
+        qrow[x] = p->q_mul * val + p->q_add;
     }
 }
 
@@ -178,7 +187,7 @@ static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, d
     for (int64_t j = 0; j < sk; j++) {
         ok[j] = (unsigned char)allowed(p, b, h, i, j, sq, sk);
         if (!ok[j]) continue;
-        fetch_row(p, p->k, p->k_scale, b, j, hk, p->dk, krow);
+        fetch_row(p, p->k, p->k_scale, p->k_mul, p->k_add, b, j, hk, p->dk, krow);
         double dot = 0.0;
         for (int x = 0; x < p->dk; x++) dot += qrow[x] * krow[x];
         double sj = p->softmax_scale * dot;
@@ -198,7 +207,7 @@ static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, d
         if (!ok[j]) continue;
         double w = exp(s[j] - m);
         l += w;
-        fetch_row(p, p->v, p->v_scale, b, j, hk, p->dv, vrow);
+        fetch_row(p, p->v, p->v_scale, p->v_mul, p->v_add, b, j, hk, p->dv, vrow);
         for (int x = 0; x < p->dv; x++) out[x] += w * vrow[x];
     }
     for (int x = 0; x < p->dv; x++) out[x] /= l;
@@ -350,7 +359,7 @@ static void *bwd_worker(void *argp) {
                 for (int64_t j = 0; j < sk; j++) {
                     ok[j] = (unsigned char)allowed(p, b, h, i, j, sq, sk);
                     if (!ok[j]) continue;
-                    fetch_row(p, p->k, p->k_scale, b, j, hk, p->dk, krow);
+                    fetch_row(p, p->k, p->k_scale, p->k_mul, p->k_add, b, j, hk, p->dk, krow);
                     double dot = 0.0;
                     for (int x = 0; x < p->dk; x++) dot += qrow[x] * krow[x];
                     double sj = p->softmax_scale * dot;
@@ -369,7 +378,7 @@ static void *bwd_worker(void *argp) {
                 double dsum = 0.0;
                 for (int64_t j = 0; j < sk; j++) {
                     if (!ok[j]) continue;
-                    fetch_row(p, p->v, p->v_scale, b, j, hk, p->dv, vrow);
+                    fetch_row(p, p->v, p->v_scale, p->v_mul, p->v_add, b, j, hk, p->dv, vrow);
                     double d = 0.0;
                     for (int x = 0; x < p->dv; x++) d += dorow[x] * vrow[x];
                     dp[j] = d;
@@ -387,7 +396,7 @@ static void *bwd_worker(void *argp) {
                         const double th = tanh(u[j] / p->softcap);
                         du *= 1.0 - th * th;
                     }
-                    fetch_row(p, p->k, p->k_scale, b, j, hk, p->dk, krow);
+                    fetch_row(p, p->k, p->k_scale, p->k_mul, p->k_add, b, j, hk, p->dk, krow);
                     double *dkrow = a->dk + ((p->cu_k[b] + j) * p->hkv + hk) * (int64_t)p->dk;
                     for (int x = 0; x < p->dk; x++) {
                         dqrow[x] += p->softmax_scale * du * krow[x];
@@ -405,6 +414,10 @@ int fa_oracle_bwd(const fa_oracle_problem *p, const double *dout, double *dq, do
                   int nthreads) {
     if (!p || p->hq <= 0 || p->hkv <= 0 || p->hq % p->hkv || p->num_seqs < 0) return -1;
     if (p->block_table || (p->kv_dtype != KV_BF16 && p->kv_dtype != KV_F64)) return -1;
+    /* gradients with respect to the stored tensors: no prologue */
+    if (p->q_mul != 1.0 || p->q_add != 0.0 || p->k_mul != 1.0 || p->k_add != 0.0 || p->v_mul != 1.0 ||
+        p->v_add != 0.0)
+        return -1;
     const int64_t tq = p->cu_q[p->num_seqs], tk = p->cu_k[p->num_seqs];
     memset(dq, 0, sizeof(double) * tq * p->hq * p->dk);
     memset(dk, 0, sizeof(double) * tk * p->hkv * p->dk);

@@ -51,7 +51,7 @@ def run_gpu(p, t=None, num_splits=0, out=None, lse=None, stream=None, workspace=
         softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
         score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap,
         block_mask=t.get("bm"), num_splits=num_splits, out=out, lse=lse, stream=stream,
-        workspace=workspace)
+        workspace=workspace, prologue=(fa.Prologue(*p.prologue) if p.prologue is not None else None))
     return o, l
 
 

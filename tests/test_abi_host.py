@@ -89,14 +89,14 @@ def _call(L, **over):
         v=_t(FAKE * 3, fa.FA_BF16, [T, H, D]), bt=None,
         cq=_t(FAKE * 4, fa.FA_I32, [3]), ck=_t(FAKE * 5, fa.FA_I32, [3]), ks=None, vs=None,
         out=_t(FAKE * 6, fa.FA_BF16, [T, H, D]), lse=_t(FAKE * 7, fa.FA_F32, [H, T]),
-        scale=0.125, causal=1, window=0, mod=None, bm=None, page=0,
+        scale=0.125, causal=1, window=0, mod=None, bm=None, pro=None, page=0,
         launch=fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, num_splits=0, total_q=T, total_k=T))
     args.update(over)
     r = lambda x: None if x is None else ctypes.byref(x)
     st = L.fa_fwd_varlen(r(args["q"]), r(args["k"]), r(args["v"]), r(args["bt"]), r(args["cq"]), r(args["ck"]),
                          r(args["ks"]), r(args["vs"]), r(args["out"]), r(args["lse"]), args["scale"],
-                         args["causal"], args["window"], r(args["mod"]), r(args["bm"]), args["page"],
-                         r(args["launch"]), None)
+                         args["causal"], args["window"], r(args["mod"]), r(args["bm"]), r(args["pro"]),
+                         args["page"], r(args["launch"]), None)
     return st, L.fa_last_error().decode()
 
 
@@ -119,6 +119,10 @@ def _call(L, **over):
     (dict(mod=fa.ScoreMod(kind=2, softcap=0.0)), fa.FA_ERR_INVALID_ARG, "softcap"),
     (dict(mod=fa.ScoreMod(kind=7)), fa.FA_ERR_INVALID_ARG, "kind"),
     (dict(bm=fa.BlockMask(data=FAKE * 9, n_qblk=1, n_kblk=1, blk_q=64, blk_k=64)), fa.FA_ERR_UNSUPPORTED, "128x128"),
+    (dict(pro=fa.Prologue(q_mul=1, q_add=0.5, k_mul=1, v_mul=1)), fa.FA_ERR_UNSUPPORTED, "q_add"),
+    (dict(pro=fa.Prologue(q_mul=1, k_mul=1, k_add=0.5, v_mul=1), mod=fa.ScoreMod(kind=2, softcap=5.0)),
+     fa.FA_ERR_UNSUPPORTED, "soft-cap"),
+    (dict(pro=fa.Prologue(q_mul=float("nan"), k_mul=1, v_mul=1)), fa.FA_ERR_INVALID_ARG, "finite"),
     (dict(bm=fa.BlockMask(data=FAKE * 9, n_qblk=0, n_kblk=1, blk_q=128, blk_k=128)), fa.FA_ERR_INVALID_ARG, "cover"),
     (dict(launch=None), fa.FA_ERR_INVALID_ARG, "launch"),
 ])
@@ -226,11 +230,11 @@ def test_plan_create_validates_like_the_call(L):
     handle = ctypes.c_void_p(12345)
     r = ctypes.byref
     st = L.fa_fwd_plan_create(r(q), r(k), r(v), None, r(cq), r(ck), None, None, r(out), r(lse), 0.125, 1, 0,
-                              None, None, 0, r(launch), r(handle))
+                              None, None, None, 0, r(launch), r(handle))
     assert st == fa.FA_ERR_INVALID_ARG and "dtype" in L.fa_last_error().decode()
     assert not handle.value
     st = L.fa_fwd_plan_create(r(q), r(k), r(v), None, r(cq), r(ck), None, None, r(out), r(lse), 0.125, 1, 0,
-                              None, None, 0, r(launch), None)
+                              None, None, None, 0, r(launch), None)
     assert st == fa.FA_ERR_INVALID_ARG and "plan" in L.fa_last_error().decode()
     assert L.fa_fwd_plan_launch(None, None) == fa.FA_ERR_INVALID_ARG
     L.fa_fwd_plan_destroy(None)

@@ -64,14 +64,18 @@ def brute_mask(p, b, h, sq, sk):
     return m
 
 
-def sdpa_reference(p, bias_fn=None):
-    """torch fp64 SDPA per sequence (GQA by repeat_interleave) and logsumexp."""
+def sdpa_reference(p, bias_fn=None, maps=None):
+    """torch fp64 SDPA per sequence (GQA by repeat_interleave) and logsumexp.
+    ``maps``: (q_mul, q_add, k_mul, k_add, v_mul, v_add) applied to the
+    widened tensors first."""
     if p.q_dtype == "e4m3":
         q = torch.from_numpy(p.q.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
     else:
         q = fi.bf16_to_f32(p.q).astype(np.float64)
     k = kv_tokens_f64(p, "k")
     v = kv_tokens_f64(p, "v")
+    if maps is not None:
+        q, k, v = maps[0] * q + maps[1], maps[2] * k + maps[3], maps[4] * v + maps[5]
     g = p.hq // p.hkv
     outs = np.zeros((p.total_q, p.hq, p.dv))
     lses = np.zeros((p.hq, p.total_q))
@@ -509,3 +513,62 @@ def test_e4m3_q_scale_is_folded_into_softmax_scale():
     assert np.max(np.abs(oe - ob)) < 0.1 and np.max(np.abs(le - lb)) < 0.1
     ou, lu = oracle.forward(pe.replace(softmax_scale=pb.softmax_scale))
     assert np.max(np.abs(lu - lb)) > 1.0
+
+
+# ---------------------------------------------------------------- prologue ----
+# Element maps x -> mul * x + add on Q, K, V as read (fkl_python PR #7,
+# prologue-fusion commit).
+
+PRO = (0.75, 0.2, -1.5, 0.3, 2.0, -0.25)
+
+
+@pytest.mark.parametrize("causal,paged", [(False, False), (True, False), (True, True)])
+def test_prologue_matches_sdpa_on_transformed_inputs(causal, paged):
+    p = fi.make_problem([33, 0, 70, 20], [33, 4, 90, 0], hq=4, hkv=2, dk=32, dv=16, seed=21, causal=causal,
+                        page_size=16 if paged else 0, spare_pages=3).replace(prologue=PRO)
+    out, lse = oracle.forward(p)
+    ro, rl = sdpa_reference(p, maps=PRO)
+    assert_close(out, ro, 1e-12)
+    assert_close(lse, rl, 1e-12)
+
+
+def test_prologue_k_shift_moves_only_the_lse():
+    """Adding c to every key element adds scale * c * sum_d q_i[d] to every
+    score of row i: the softmax is unchanged and the LSE moves by that much."""
+    base = fi.make_problem([50, 9], [64, 30], hq=2, dk=16, seed=22, causal=True, mod="alibi", alibi_slope=0.1)
+    c = 0.7
+    out0, lse0 = oracle.forward(base)
+    out1, lse1 = oracle.forward(base.replace(prologue=(1.0, 0.0, 1.0, c, 1.0, 0.0)))
+    q = fi.bf16_to_f32(base.q).astype(np.float64)                  # [T, H, D]
+    shift = base.softmax_scale * c * q.sum(-1).T                   # [H, T]
+    assert_close(out1, out0, 1e-12)
+    assert_close(lse1, lse0 + np.where(np.isneginf(lse0), 0.0, shift), 1e-11)
+
+
+def test_prologue_v_map_acts_on_the_output():
+    base = fi.make_problem([40, 5], [40, 0], hq=2, dk=16, seed=23, window=6)
+    out0, lse0 = oracle.forward(base)
+    out1, lse1 = oracle.forward(base.replace(prologue=(1.0, 0.0, 1.0, 0.0, -3.0, 0.5)))
+    empty = np.isneginf(lse0).T[..., None]                         # [T, H, 1]
+    assert_close(out1, np.where(empty, 0.0, -3.0 * out0 + 0.5), 1e-12)
+    assert_close(lse1, lse0, 0.0)
+
+
+def test_prologue_scales_equal_a_softmax_scale():
+    base = fi.make_problem([30], [45], hq=2, dk=16, seed=24, mod="softcap", softcap=3.0)
+    out0, lse0 = oracle.forward(base.replace(softmax_scale=base.softmax_scale * 0.5 * 3.0))
+    out1, lse1 = oracle.forward(base.replace(prologue=(0.5, 0.0, 3.0, 0.0, 1.0, 0.0)))
+    assert_close(out1, out0, 1e-12)
+    assert_close(lse1, lse0, 1e-12)
+
+
+def test_make_prologue_composes_op_chains():
+    import flashattention_forward_gb300 as fa
+    pro = fa.make_prologue({"q": [("mul", 2.0), ("add", 1.0)], "k": [("add", 1.0), ("mul", 2.0)],
+                            "v": [("sub", 0.5), ("div", 4.0)]})
+    got = (pro.q_mul, pro.q_add, pro.k_mul, pro.k_add, pro.v_mul, pro.v_add)
+    assert got == (2.0, 1.0, 2.0, 2.0, 0.25, -0.125)
+    ident = fa.make_prologue({})
+    assert (ident.q_mul, ident.q_add, ident.k_mul, ident.k_add, ident.v_mul, ident.v_add) == (1, 0, 1, 0, 1, 0)
+    with pytest.raises(ValueError):
+        fa.make_prologue({"q": [("pow", 2.0)]})

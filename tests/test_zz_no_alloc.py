@@ -70,6 +70,6 @@ def test_noalloc_rejects_oversized_scratch_before_launch():
     launch = fa.Launch(num_seqs=T, max_seqlen_q=1, max_seqlen_k=64 * 512, num_splits=64, total_q=T,
                        total_k=T * 64)
     st = L.fa_fwd_varlen_noalloc(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), None, None, None, None,
-                                 None, None, None, 0.1, 0, 0, None, None, 0, ctypes.byref(launch), None)
+                                 None, None, None, 0.1, 0, 0, None, None, None, 0, ctypes.byref(launch), None)
     assert st == fa.FA_ERR_UNSUPPORTED
     assert b"exceeds the static" in L.fa_last_error()
