@@ -702,6 +702,14 @@ def profile_only(name, warmup, steps):
         p = fi.make_problem([1] * 64, lens_k, hq=32, hkv=8, dk=128, seed=1, page_size=16, spare_pages=64,
                             max_pages=512, kv_dtype=name[7:], name=name)
         splits = None
+    elif name == "decode_p1":
+        rng = np.random.default_rng(0)
+        lens_k = [int(x) for x in rng.integers(512, 8193, size=64)]
+        p = fi.make_problem([1] * 64, lens_k, hq=32, hkv=8, dk=128, seed=1, page_size=1, spare_pages=64,
+                            max_pages=8192, name=name)
+        splits = None
+    elif name == "prefill_p1":
+        p, splits = fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, page_size=1, causal=True, name=name), 0
     elif name in ("bwd_varlen_noncausal", "bwd_long_causal", "bwd_mid_noncausal"):
         p = {"bwd_varlen_noncausal": lambda: fi.config2(causal=False),
              "bwd_long_causal": lambda: fi.make_problem([4096] * 4, hq=16, dk=128, seed=3, causal=True),
