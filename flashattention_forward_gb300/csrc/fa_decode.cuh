@@ -320,14 +320,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             dec_cp_async_4(sdst + 4 * (kDecStageKeys + kk), live ? p.v_scale + at : p.v_scale, live ? 4u : 0u);
           }
           dec_cp_async_arrive_noinc(smem_u32(full + slot_i));
-          gather_block<kDecStageKeys, D, kGatherPlain>(kd, p.gk, hk, key0, p.page_size - 1, 0, pg, lane);
-          gather_block<kDecStageKeys, D, kGatherPlain>(vd, p.gv, hk, key0, p.page_size - 1, 0, pg, lane);
+          gather_block<kDecStageKeys, D, kGatherPlain, 4>(kd, p.gk, hk, key0, p.page_size - 1, 0, pg, lane);
+          gather_block<kDecStageKeys, D, kGatherPlain, 4>(vd, p.gv, hk, key0, p.page_size - 1, 0, pg, lane);
         } else {
 #pragma unroll
           for (int cb = 0; cb < NCB; ++cb) {
             const uint32_t off = cb * kDecStageKeys * 128;
-            gather_block<kDecStageKeys, 128, kGatherSw128>(kd + off, p.gk, hk, key0, p.page_size - 1, cb * 128, pg, lane);
-            gather_block<kDecStageKeys, 128, kGatherSw128>(vd + off, p.gv, hk, key0, p.page_size - 1, cb * 128, pg, lane);
+            gather_block<kDecStageKeys, 128, kGatherSw128, 4>(kd + off, p.gk, hk, key0, p.page_size - 1, cb * 128, pg, lane);
+            gather_block<kDecStageKeys, 128, kGatherSw128, 4>(vd + off, p.gv, hk, key0, p.page_size - 1, cb * 128, pg, lane);
           }
         }
         gp.commit(smem_u32(full + slot_i));

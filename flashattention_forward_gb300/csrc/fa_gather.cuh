@@ -8,9 +8,9 @@
 // Pages of one key are the lookup-bound case of the paged layout (FlyDSL
 // PR #1066, the page-size note: page 1 against page 16); there every key row is
 // fetched by its own page-table read and row copy, which is what this does:
-// one warp, one key row per lane, 16 bytes per copy, written straight into
-// the layout the consumers read (the swizzle is applied by address, as TMA
-// would).
+// one warp, one or four lanes per key row, 16 bytes per copy, written
+// straight into the layout the consumers read (the swizzle is applied by
+// address, as TMA would).
 //
 // Completion: the copies of one ring slot form one cp.async group.  After the
 // next slot's group is committed, each lane waits for all but that newest
@@ -51,36 +51,51 @@ enum GatherLayout : int {
 
 // Warp-collective: copy ROWS key rows x ROW_BYTES bytes, starting at byte
 // `col0` of each key's row, of kv head `hk` into `dst`.  Key row r is the
-// sequence key key0 + r and is copied by lane r & 31, whose pg[r >> 5] is its
-// page id (-1 for a key past the sequence: the row is zero-filled, so that
-// P = 0 never meets a stale non-finite value in the PV product).  One address
-// per row, then one copy per 16-byte chunk.
-template <int ROWS, int ROW_BYTES, int LAYOUT>
+// sequence key key0 + r; lane r & 31 holds its page id in pg[r >> 5] (-1 for
+// a key past the sequence: the row is zero-filled, so that P = 0 never meets
+// a stale non-finite value in the PV product).
+//
+// LPR lanes copy one row together.  LPR = 1: each lane copies whole rows
+// (one address per row, no shuffles), for producers that run on few
+// registers and read mostly from L2 (prefill).  LPR = 4: four lanes share a
+// row, so a warp-wide copy touches 8 rows instead of 32 (fewer L1
+// wavefronts), at one shuffle and one address per row and lane; measured
+// 1.8x faster for the page-1 decode, which streams from HBM, and slower for
+// the prefill kernels.
+template <int ROWS, int ROW_BYTES, int LAYOUT, int LPR = 1>
 __device__ __forceinline__ void gather_block(uint8_t *dst, const KvGather &g, int hk, int key0, int page_mask,
                                              int col0, const int (&pg)[ROWS / 32], int lane) {
   static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "rows of 4 or 8 chunks");
   static_assert(LAYOUT != kGatherSw128 || ROW_BYTES == 128, "swizzled rows are 128 bytes");
   static_assert(LAYOUT != kGatherStage || ROW_BYTES == 64, "staged rows are 64 bytes");
+  static_assert(LPR == 1 || LPR == 4, "one or four lanes per row");
   constexpr int CH = ROW_BYTES / 16;   // chunks per row
+  constexpr int CPL = CH / LPR;        // chunks per lane
+  constexpr int RPI = 32 / LPR;        // rows per warp-wide copy
+  const int sub = lane % LPR, rs = lane / LPR;
   const uint32_t dbase = smem_u32(dst);
-  const uint8_t *head = g.base + (int64_t)hk * g.head_stride + col0;
-  const int x = lane & 7;              // r & 7 of every row this lane copies (swizzle phase)
+  const uint8_t *head = g.base + (int64_t)hk * g.head_stride + col0 + sub * CPL * 16;
 #pragma unroll
   for (int u = 0; u < ROWS / 32; ++u) {
-    const int r = 32 * u + lane;
-    const int page = pg[u];
-    const bool live = page >= 0;
-    const uint8_t *src = live ? head + (int64_t)page * g.page_stride + (int64_t)((key0 + r) & page_mask) * g.slot_stride
-                              : g.base;
-    const uint32_t bytes = live ? 16u : 0u;
-    uint32_t row;
-    if constexpr (LAYOUT == kGatherSw128) row = dbase + r * 128;
-    else if constexpr (LAYOUT == kGatherPlain) row = dbase + r * ROW_BYTES;
-    else row = dbase + (r >> 5) * 4096 + 2048 + (r & 31) * 64;
+    const int pgu = pg[u];
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const uint32_t at = LAYOUT == kGatherSw128 ? row + ((c ^ x) << 4) : row + c * 16;
-      cp_async_16(at, live ? src + c * 16 : src, bytes);
+    for (int i = 0; i < 32 / RPI; ++i) {
+      const int r32 = i * RPI + rs;   // row within the 32: the lane that holds its page id
+      const int r = 32 * u + r32;
+      const int page = LPR == 1 ? pgu : __shfl_sync(0xffffffffu, pgu, r32);
+      const bool live = page >= 0;
+      const uint8_t *src = live ? head + (int64_t)page * g.page_stride + (int64_t)((key0 + r) & page_mask) * g.slot_stride
+                                : g.base;
+      uint32_t row;
+      if constexpr (LAYOUT == kGatherSw128) row = dbase + r * 128;
+      else if constexpr (LAYOUT == kGatherPlain) row = dbase + r * ROW_BYTES;
+      else row = dbase + (r >> 5) * 4096 + 2048 + (r & 31) * 64;
+#pragma unroll
+      for (int cc = 0; cc < CPL; ++cc) {
+        const int c = sub * CPL + cc;
+        const uint32_t at = LAYOUT == kGatherSw128 ? row + ((c ^ (r & 7)) << 4) : row + c * 16;
+        cp_async_16(at, live ? src + cc * 16 : src, live ? 16u : 0u);
+      }
     }
   }
 }
