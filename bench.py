@@ -35,7 +35,8 @@ METRIC = "attn fwd TFLOP/s (prefill) & KV-cache GB/s (decode), % of GB300 roofli
 # sources of the headline kernel (fa_prefill2_kernel): `traffic` is reported only
 # while profiles/traffic.json was captured from these exact files
 KERNEL_SOURCES = ["flashattention_forward_gb300/csrc/fa_prefill.cuh", "flashattention_forward_gb300/csrc/fa_prefill2.cuh",
-                  "flashattention_forward_gb300/csrc/sm103_ptx.cuh"]
+                  "flashattention_forward_gb300/csrc/sm103_ptx.cuh",
+                  "flashattention_forward_gb300/csrc/fa_gather.cuh"]
 
 
 def kernel_hash():
