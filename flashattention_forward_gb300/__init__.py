@@ -266,7 +266,7 @@ def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                        lse: Optional[torch.Tensor], *, max_seqlen_q: int, max_seqlen_k: int,
                        total_k: Optional[int] = None, block_table: Optional[torch.Tensor] = None,
                        page_size: int = 0, softmax_scale: Optional[float] = None, causal: bool = False,
-                       window: int = 0, num_splits: int = 0, stream=None):
+                       window: int = 0, num_splits: int = 0, stream=None, prologue=None):
     """Split-KV decode through ``fa_fwd_varlen_noalloc``: for callers that cannot
     allocate device memory (the partials go to the library's static scratch of
     NOALLOC_SCRATCH_BYTES).  ``out`` (and ``lse`` if wanted) are caller-provided;
@@ -284,8 +284,8 @@ def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
             as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), None, None, as_tensor(out), as_tensor(lse)]
     sm = ScoreMod(kind=MOD_NONE)
     _check(L.fa_fwd_varlen_noalloc(*[_ref(a) for a in args], float(softmax_scale), int(bool(causal)),
-                                   int(window), ctypes.byref(sm), None, None, int(page_size),
-                                   ctypes.byref(launch), ctypes.c_void_p(_stream_ptr(stream))))
+                                   int(window), ctypes.byref(sm), None, _ref(make_prologue(prologue)),
+                                   int(page_size), ctypes.byref(launch), ctypes.c_void_p(_stream_ptr(stream))))
     return out, lse
 
 

@@ -341,13 +341,14 @@ def test_softcap_huge_and_alibi_zero_reduce_to_plain():
 
 # ------------------------------------------------------- invariants ---------
 
-def test_paged_equals_packed_bit_identical():
+@pytest.mark.parametrize("page_size", [1, 2, 16])
+def test_paged_equals_packed_bit_identical(page_size):
     """Same K/V placed in shuffled pages (with NaN-poisoned spare slots and -1
     block-table padding) gives bit-identical fp64 results."""
     kw = dict(hq=4, hkv=2, dk=32, dv=16, seed=13, causal=True)
     packed = fi.make_problem([20, 37, 1], [50, 37, 70], **kw)
-    paged = fi.make_problem([20, 37, 1], [50, 37, 70], page_size=16, spare_pages=5,
-                            max_pages=9, **kw)
+    paged = fi.make_problem([20, 37, 1], [50, 37, 70], page_size=page_size, spare_pages=5,
+                            max_pages=(70 + page_size - 1) // page_size + 2, **kw)
     assert np.array_equal(kv_tokens_f64(paged, "k"), kv_tokens_f64(packed, "k"))
     o1, l1 = oracle.forward(packed)
     o2, l2 = oracle.forward(paged)
