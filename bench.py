@@ -565,6 +565,17 @@ def other_workloads(dev, warmup, steps, flush, pk):
     res["paged_decode_64seq_hq32_hkv8_p16"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
                                                "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16, p.total_k),
                                                "bytes": fi.decode_bytes(p)}
+    # the same decode with a soft-cap of 50 (Gemma-style) and with ALiBi
+    for run, kw in (("softcap50", dict(mod="softcap", softcap=50.0)), ("alibi", dict(mod="alibi"))):
+        pm = fi.make_problem([1] * 64, [int(x) for x in p.seqlens_k], hq=32, hkv=8, dk=128, seed=1, page_size=16,
+                             spare_pages=64, max_pages=512, name="paged_decode_" + run, **kw)
+        t = dev_tensors(pm, dev)
+        call, n, _, _ = make_call(pm, t, num_splits=None)
+        ms = statistics.mean(time_calls([call], warmup, steps, flush))
+        gbs = fi.decode_bytes(pm) / (ms * 1e-3) / 1e9
+        res[f"paged_decode_64seq_hq32_hkv8_p16_{run}"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
+                                                          "bytes": fi.decode_bytes(pm)}
+        del t, pm
     # the same decode one key per page (rows gathered by cp.async)
     p1 = fi.make_problem([1] * 64, [int(x) for x in p.seqlens_k], hq=32, hkv=8, dk=128, seed=1, page_size=1,
                          spare_pages=64, max_pages=8192, name="paged_decode_p1")

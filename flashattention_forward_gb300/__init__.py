@@ -238,7 +238,7 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         total_k = k_cache.shape[0] if block_table is None else 0
     if num_splits is None:
         num_splits = default_splits(B, max_seqlen_q, max_seqlen_k, Hq, Hkv, page_size, total_k)
-        if q.dtype != torch.bfloat16 or Dk != Dv or score_mod != MOD_NONE or block_mask is not None:
+        if q.dtype != torch.bfloat16 or Dk != Dv:
             num_splits = 0
     launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                     num_splits=num_splits, total_q=Tq, total_k=total_k)
@@ -325,7 +325,7 @@ class FwdPlan:
         num_splits = kw.get("num_splits")
         if num_splits is None:
             num_splits = default_splits(B, kw["max_seqlen_q"], kw["max_seqlen_k"], Hq, Hkv, page_size, total_k)
-            if q.dtype != torch.bfloat16 or Dk != Dv or score_mod != MOD_NONE or block_mask is not None:
+            if q.dtype != torch.bfloat16 or Dk != Dv:
                 num_splits = 0
         self.launch = Launch(num_seqs=B, max_seqlen_q=kw["max_seqlen_q"], max_seqlen_k=kw["max_seqlen_k"],
                              num_splits=num_splits, total_q=Tq, total_k=total_k)

@@ -474,7 +474,6 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if ((int64_t)launch->max_seqlen_q * group > fa::kDecRows)
       return fail(FA_ERR_UNSUPPORTED, "split-KV needs max_seqlen_q * Hq/Hkv <= %d", fa::kDecRows);
     if (Dk != Dv || (Dk != 64 && Dk != 128)) return fail(FA_ERR_UNSUPPORTED, "split-KV supports Dk = Dv in {64, 128}");
-    if (mod != 0 || block_mask) return fail(FA_ERR_UNSUPPORTED, "split-KV does not take score mods or block masks");
     if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "too many sequences or kv heads for split-KV");
     fa::DecodeLaunch L;
     memset(&L, 0, sizeof L);
@@ -534,6 +533,13 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.pro_vmul = pro_vmul;
     p.pro_vadd = pro_vadd;
     p.pro_lse_k = pro_lse_k;
+    p.mod = mod;
+    p.alibi_log2 = mod == 1 ? slope * fa::kLog2e : 0.f;
+    p.softcap_arg = mod == 2 ? softmax_scale / cap : 0.f;
+    p.softcap_log2 = mod == 2 ? cap * fa::kLog2e : 0.f;
+    p.block_mask = block_mask ? (const uint8_t *)block_mask->data : nullptr;
+    p.n_qblk = block_mask ? block_mask->n_qblk : 0;
+    p.n_kblk = block_mask ? block_mask->n_kblk : 0;
     p.hq = (int)Hq;
     p.hkv = (int)Hkv;
     p.group = group;

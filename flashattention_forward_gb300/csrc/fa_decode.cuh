@@ -65,6 +65,13 @@ struct DecodeParams {
   // folded prologue: partial or final out = pro_vmul * o + pro_vadd on rows
   // that see keys; LSE += pro_lse_k * sum_d q[d]
   float pro_vmul, pro_vadd, pro_lse_k;
+  // score mods (0 none, 1 ALiBi, 2 soft-cap) and 128 x 128 block masks, as
+  // in the prefill kernels
+  int32_t mod;
+  float alibi_log2;                   // slope * log2(e)
+  float softcap_arg, softcap_log2;    // softmax_scale / cap, cap * log2(e)
+  const uint8_t *block_mask;          // [B*Hq, n_qblk, n_kblk] or null
+  int32_t n_qblk, n_kblk;
 };
 
 template <int D, int KV = 0>
@@ -417,6 +424,25 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     // byte caches: Q rows carry a factor 2^e that the score scale removes
     const float sc0 = KV ? p.scale_log2 * sQinv[r0] : p.scale_log2;
     const float sc1 = KV ? p.scale_log2 * sQinv[r1] : p.scale_log2;
+    // score mods: the raw product <q, k> of row r is s * kf * qf_r
+    const float qf0 = KV ? sQinv[r0] : 1.f, qf1 = KV ? sQinv[r1] : 1.f;
+    const float c2u = 2.f * kLog2e * p.softcap_arg;   // soft-cap: raw product -> 2u log2(e)
+    // block masks: the heads and query blocks of rows r0 and r1
+    const int h0 = hk * p.group + r0 % p.group, h1 = hk * p.group + r1 % p.group;
+    const int qb0 = (r0 / p.group) / 128, qb1 = (r1 / p.group) / 128;
+    auto block_live = [&](int h, int qb, int kb) -> bool {
+      if (p.block_mask == nullptr) return true;
+      if (qb >= p.n_qblk || kb >= p.n_kblk) return false;
+      return p.block_mask[((int64_t)(b * p.hq + h) * p.n_qblk + qb) * p.n_kblk + kb] != 0;
+    };
+    // one modified score in log2 units from the raw product x of row (ip, .)
+    auto mod_score = [&](float x, int ip, int j) -> float {
+      if (p.mod == 2) {
+        float r;
+        return softcap_log2_score(ex2(x * c2u), p.softcap_log2, r);
+      }
+      return fmaf(x, p.scale_log2, -p.alibi_log2 * fabsf((float)(ip - j)));
+    };
     uint8_t *conv = smem + Cfg::kOffConv + warp * Cfg::kConvWarpBytes;   // byte caches only
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[D / 8][4];
@@ -500,7 +526,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         dec_mma<KV>(s[0], qf[ks], b0, b1);
         dec_mma<KV>(s[1], qf[ks], b2, b3);
       }
-      // Scale, mask, online softmax for rows r0 and r1.
+      // Scale, mask, online softmax for rows r0 and r1.  The warp's 16 keys
+      // lie in one 128-key block.
+      const bool blk0 = block_live(h0, qb0, key_base / 128), blk1 = block_live(h1, qb1, key_base / 128);
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
@@ -508,15 +536,20 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         for (int e = 0; e < 2; ++e) {
           const int j = key_base + n * 8 + (lane & 3) * 2 + e;
           const bool in = j < key_hi;
-          bool ok0 = in && r0 < rows, ok1 = in && r1 < rows;
+          bool ok0 = in && r0 < rows && blk0, ok1 = in && r1 < rows && blk1;
           if (p.causal) { ok0 = ok0 && j <= ip0; ok1 = ok1 && j <= ip1; }
           if (p.window > 0) {
             if (p.causal) { ok0 = ok0 && ip0 - j < p.window; ok1 = ok1 && ip1 - j < p.window; }
             else { ok0 = ok0 && abs(ip0 - j) < p.window; ok1 = ok1 && abs(ip1 - j) < p.window; }
           }
           const float kf = KV ? ksc[n][e] : 1.f;   // per-key scale of a byte cache
-          s[n][e] = ok0 ? s[n][e] * kf * sc0 : -INFINITY;
-          s[n][2 + e] = ok1 ? s[n][2 + e] * kf * sc1 : -INFINITY;
+          if (p.mod == 0) {
+            s[n][e] = ok0 ? s[n][e] * kf * sc0 : -INFINITY;
+            s[n][2 + e] = ok1 ? s[n][2 + e] * kf * sc1 : -INFINITY;
+          } else {
+            s[n][e] = ok0 ? mod_score(s[n][e] * kf * qf0, ip0, j) : -INFINITY;
+            s[n][2 + e] = ok1 ? mod_score(s[n][2 + e] * kf * qf1, ip1, j) : -INFINITY;
+          }
           mx0 = fmaxf(mx0, s[n][e]);
           mx1 = fmaxf(mx1, s[n][2 + e]);
         }
