@@ -133,6 +133,31 @@ int *error_word() {
   return addr[dev];
 }
 
+// Score mod (kind 0 none, 1 ALiBi, 2 soft-cap; NULL = none) and 128 x 128
+// block mask checks shared by the forward and backward entry points.
+fa_status_t check_mods(const fa_score_mod_t *score_mod, const fa_block_mask_t *block_mask, const fa_launch_t *launch,
+                       int *mod, float *slope, float *cap) {
+  *mod = 0;
+  *slope = *cap = 0.f;
+  if (score_mod) {
+    *mod = score_mod->kind;
+    if (*mod < 0 || *mod > 2) return fail(FA_ERR_INVALID_ARG, "score_mod.kind %d", *mod);
+    *slope = score_mod->alibi_slope;
+    *cap = score_mod->softcap;
+    if (*mod == 1 && !std::isfinite(*slope)) return fail(FA_ERR_INVALID_ARG, "alibi_slope must be finite");
+    if (*mod == 2 && !(*cap > 0.f && std::isfinite(*cap)))
+      return fail(FA_ERR_INVALID_ARG, "softcap must be positive and finite");
+  }
+  if (block_mask) {
+    if (!block_mask->data) return fail(FA_ERR_INVALID_ARG, "block_mask.data is NULL");
+    if (block_mask->blk_q != 128 || block_mask->blk_k != 128)
+      return fail(FA_ERR_UNSUPPORTED, "block masks use 128x128 blocks");
+    if ((int64_t)block_mask->n_qblk * 128 < launch->max_seqlen_q || (int64_t)block_mask->n_kblk * 128 < launch->max_seqlen_k)
+      return fail(FA_ERR_INVALID_ARG, "block_mask does not cover max_seqlen_q/k");
+  }
+  return FA_OK;
+}
+
 // Byte geometry of a paged cache [N_pg, P_s, Hkv, D] for the row gather.
 fa::KvGather kv_gather(const fa_tensor_t *t, int esz) {
   fa::KvGather g;
@@ -424,20 +449,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   if (!std::isfinite(softmax_scale)) return fail(FA_ERR_INVALID_ARG, "softmax_scale must be finite");
   int mod = 0;
   float slope = 0.f, cap = 0.f;
-  if (score_mod) {
-    mod = score_mod->kind;
-    if (mod < 0 || mod > 2) return fail(FA_ERR_INVALID_ARG, "score_mod.kind %d", mod);
-    slope = score_mod->alibi_slope;
-    cap = score_mod->softcap;
-    if (mod == 1 && !std::isfinite(slope)) return fail(FA_ERR_INVALID_ARG, "alibi_slope must be finite");
-    if (mod == 2 && !(cap > 0.f && std::isfinite(cap))) return fail(FA_ERR_INVALID_ARG, "softcap must be positive and finite");
-  }
-  if (block_mask) {
-    if (!block_mask->data) return fail(FA_ERR_INVALID_ARG, "block_mask.data is NULL");
-    if (block_mask->blk_q != 128 || block_mask->blk_k != 128) return fail(FA_ERR_UNSUPPORTED, "block masks use 128x128 blocks");
-    if ((int64_t)block_mask->n_qblk * 128 < launch->max_seqlen_q || (int64_t)block_mask->n_kblk * 128 < launch->max_seqlen_k)
-      return fail(FA_ERR_INVALID_ARG, "block_mask does not cover max_seqlen_q/k");
-  }
+  if ((st = check_mods(score_mod, block_mask, launch, &mod, &slope, &cap))) return st;
   // ---- prologue: folded (see fa_prologue_t) -- q_mul * k_mul into the
   // score scale, k_add into an LSE term per unit of sum_d q, v_* into the
   // output
@@ -791,20 +803,7 @@ fa_status_t fa_bwd_varlen(const fa_tensor_t *q, const fa_tensor_t *k, const fa_t
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return fail(FA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
   int mod = 0;
   float slope = 0.f, cap = 0.f;
-  if (score_mod) {
-    mod = score_mod->kind;
-    if (mod < 0 || mod > 2) return fail(FA_ERR_INVALID_ARG, "score_mod.kind %d", mod);
-    slope = score_mod->alibi_slope;
-    cap = score_mod->softcap;
-    if (mod == 1 && !std::isfinite(slope)) return fail(FA_ERR_INVALID_ARG, "alibi_slope must be finite");
-    if (mod == 2 && !(cap > 0.f && std::isfinite(cap))) return fail(FA_ERR_INVALID_ARG, "softcap must be positive and finite");
-  }
-  if (block_mask) {
-    if (!block_mask->data) return fail(FA_ERR_INVALID_ARG, "block_mask.data is NULL");
-    if (block_mask->blk_q != 128 || block_mask->blk_k != 128) return fail(FA_ERR_UNSUPPORTED, "block masks use 128x128 blocks");
-    if ((int64_t)block_mask->n_qblk * 128 < launch->max_seqlen_q || (int64_t)block_mask->n_kblk * 128 < launch->max_seqlen_k)
-      return fail(FA_ERR_INVALID_ARG, "block_mask does not cover max_seqlen_q/k");
-  }
+  if ((st = check_mods(score_mod, block_mask, launch, &mod, &slope, &cap))) return st;
   if (B == 0 || Tq == 0) return FA_OK;
   if (launch->max_seqlen_q <= 0 || launch->max_seqlen_k < 0) return fail(FA_ERR_INVALID_ARG, "bad max_seqlen");
   if (B > 65535 || Hq > 65535) return fail(FA_ERR_UNSUPPORTED, "num_seqs and Hq must be at most 65535");
