@@ -138,7 +138,9 @@ typedef struct {
  *               scalar descales; the caller folds the Q descale into
  *               softmax_scale, and QK runs on the e4m3 bytes with the per-key
  *               scale applied to each score).  Last dim contiguous, the other
- *               strides multiples of 16 bytes.  Split-KV takes bf16 q only.
+ *               strides multiples of 16 bytes.  Split-KV takes bf16 q only
+ *               (Dk = Dv in {64, 128}); score mods, block masks and
+ *               prologues apply to it as to the single pass.
  *  k_cache      paged: [N_pg, P_s, Hkv, Dk]; packed (block_table NULL):
  *               [T_k, Hkv, Dk].  bf16, e4m3 or int8.  Last three dims contiguous.
  *  v_cache      same layout and dtype with Dv (Dv may differ from Dk).
