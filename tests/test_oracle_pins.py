@@ -311,6 +311,55 @@ def test_block_mask_matches_sdpa_boolean_mask():
     assert_close(lse, rl, 1e-12)
 
 
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 150), (False, 200)])
+def test_alibi_gqa_window_block_mask_together_match_sdpa(causal, window):
+    """Every mask and the ALiBi bias at once, with GQA and Sq != Sk, against
+    torch SDPA with the brute-force mask and the bias written out."""
+    slope = 0.03
+    p = fi.make_problem([300, 129, 0], [420, 129, 50], hq=4, hkv=2, dk=16, seed=31, causal=causal,
+                        window=window, mod="alibi", alibi_slope=slope, block_mask_density=0.6,
+                        page_size=16, spare_pages=3)
+
+    def bias(sq, sk):
+        i = torch.arange(sq, dtype=torch.float64)[:, None] + (sk - sq)
+        j = torch.arange(sk, dtype=torch.float64)[None, :]
+        return -slope * (i - j).abs()
+
+    out, lse = oracle.forward(p)
+    ro, rl = sdpa_reference(p, bias)
+    assert_close(out, ro, 1e-12)
+    assert_close(lse, rl, 1e-12)
+
+
+def test_softcap_with_masks_matches_explicit_scores():
+    """The soft-cap under causal, window and block masks against scores formed
+    one by one (cap * tanh(scale * q.k / cap), then the masks) and a plain
+    softmax: the cap applies to the scaled score, before masking."""
+    cap = 2.5
+    p = fi.make_problem([200, 7], [260, 7], hq=2, hkv=1, dk=16, seed=32, causal=True, window=120,
+                        mod="softcap", softcap=cap, block_mask_density=0.7)
+    out, lse = oracle.forward(p)
+    q = fi.bf16_to_f32(p.q).astype(np.float64)
+    k = kv_tokens_f64(p, "k")
+    v = kv_tokens_f64(p, "v")
+    for b in range(p.num_seqs):
+        q0, q1 = int(p.cu_seqlens_q[b]), int(p.cu_seqlens_q[b + 1])
+        k0, k1 = int(p.cu_seqlens_k[b]), int(p.cu_seqlens_k[b + 1])
+        sq, sk = q1 - q0, k1 - k0
+        for h in range(p.hq):
+            allow = brute_mask(p, b, h, sq, sk)
+            s = cap * np.tanh(p.softmax_scale * (q[q0:q1, h] @ k[k0:k1, 0].T) / cap)
+            for i in range(sq):
+                a = allow[i]
+                if not a.any():
+                    assert np.isneginf(lse[h, q0 + i]) and not out[q0 + i, h].any()
+                    continue
+                m = s[i, a].max()
+                w = np.exp(s[i, a] - m)
+                np.testing.assert_allclose(out[q0 + i, h], (w @ v[k0:k1, 0][a]) / w.sum(), atol=1e-12)
+                np.testing.assert_allclose(lse[h, q0 + i], m + np.log(w.sum()), atol=1e-12)
+
+
 def test_block_causal_mask_equals_causal_on_block_level():
     """BlockMask.causal with Sq = Sk multiples of 128 keeps exactly the blocks kb <= qb."""
     p = fi.make_problem([256, 384], hq=2, dk=16, seed=11)
