@@ -46,6 +46,30 @@ def test_only_the_header_entry_points_are_exported(L):
     assert funcs == declared_symbols()
 
 
+def _header_prototypes():
+    """{function name: parameter count} of the header's declarations."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(fa_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = " ".join(m.group(2).split())
+        protos[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return protos
+
+
+def test_binding_argtypes_match_header_prototypes(L):
+    """The ctypes argument lists have as many entries as the C prototypes
+    (guards the binding against a drifted signature)."""
+    protos = _header_prototypes()
+    assert set(fa.EXPORTED) <= set(protos), set(fa.EXPORTED) - set(protos)
+    for name in fa.EXPORTED:
+        argtypes = getattr(L, name).argtypes
+        if argtypes is None:                       # no-argument functions keep ctypes' default
+            assert protos[name] == 0, name
+            continue
+        assert len(argtypes) == protos[name], (name, len(argtypes), protos[name])
+
+
 def test_version_and_last_error(L):
     assert "sm_103a" in fa.version()
     assert isinstance(L.fa_last_error(), bytes)
