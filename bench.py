@@ -1,16 +1,19 @@
 """Benchmark of the attention forward pass on one GB300 (replicas for N > 1).
 
-Headline workload: the packed varlen bf16 prefill (8 sequences of length
-U{0..2048} with seed 0, H=16, D=128).  One step runs it causal and non-causal
-(two launches of the prefill kernel) over inputs already resident in HBM.
-The metric is algorithmic TFLOP/s: 2*Dk + 2*Dv flops per (head, query, key)
-pair the mask allows.  L2 is flushed (a 256 MiB write) between timed steps,
-outside the timed events.
+Headline workload: config 5, the flex bf16 prefill at B=4, H=16, S=8192,
+D=128 (N(0,1) inputs, seed 0).  One step runs its six variants once each over
+inputs already resident in HBM: ALiBi (slope 0.0625) causal and non-causal,
+soft-cap 20 causal and non-causal, sliding window 256 causal, and a seeded
+50% random 128x128 block mask.  The metric is algorithmic TFLOP/s: 2*Dk +
+2*Dv flops per (head, query, key) pair the mask allows.  L2 is flushed (a
+256 MiB write) before every launch, outside the timed events.
 
-Extra lines of the same JSON object report the other workloads: the dense
-causal latency case, the paged split-KV decode (KV-cache GB/s), and the flex
-runs.  ``--impl reference`` times the fp64 CPU oracle instead (bounded samples
-of the same workload, on the host cores).
+Other workloads are reported under ``workloads`` (full figures) and
+``summary`` (compact, last in the line): the packed varlen prefill of config
+2, the dense causal latency case, the paged split-KV decodes (KV-cache GB/s),
+the paged e4m3 prefill of config 4, and the backward pass.  ``--impl
+reference`` times the fp64 CPU oracle instead (bounded row samples of the
+same six runs, on the host cores).
 """
 import argparse
 import hashlib
@@ -163,9 +166,11 @@ def make_call(p, t, num_splits=0):
     if num_splits is None:
         num_splits = fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size,
                                        p.total_k)
-    if num_splits > 1:
-        ws = torch.empty(fa.workspace_bytes(p.num_seqs, p.total_q, p.hq, p.dv, num_splits), dtype=torch.uint8,
-                         device=dev)
+    launch = fa.Launch(num_seqs=p.num_seqs, max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
+                       num_splits=num_splits, total_q=p.total_q, total_k=p.total_k)
+    need = fa.workspace_bytes(launch, p.hq, p.hkv, p.dv, p.prologue)
+    if need:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
 
     plan = fa.FwdPlan(t["q"], t["k"], t["v"], t["cu_q"], t["cu_k"], max_seqlen_q=p.max_seqlen_q,
                       max_seqlen_k=p.max_seqlen_k, total_k=p.total_k, block_table=t.get("bt"),
@@ -338,35 +343,53 @@ def e2e_pipelined(problems, steps, dev):
     return loop(steps)
 
 
-def cpu_oracle_sample(p, seconds_target=15.0, seed=0):
-    """Time the oracle on a bounded seeded row sample; return (flop/s, rows, threads, secs)."""
+def row_flops(p, units):
+    """Algorithmic flops of (token, head) rows: allowed keys * (2 Dk + 2 Dv),
+    with the causal, window and block masks counted exactly."""
+    sk, sq = p.seqlens_k, p.seqlens_q
+    seq_of = np.searchsorted(p.cu_seqlens_q[1:], units[:, 0], side="right")
+    total = 0
+    for (t, h), b in zip(units, seq_of):
+        i = int(t - p.cu_seqlens_q[b])
+        ip = i + int(sk[b]) - int(sq[b])
+        lo, hi = 0, int(sk[b])
+        if p.causal:
+            hi = min(hi, ip + 1)
+        if p.window > 0:
+            lo = max(lo, ip - p.window + 1)
+            if not p.causal:
+                hi = min(hi, ip + p.window)
+        if hi <= lo:
+            continue
+        if p.block_mask is None:
+            total += hi - lo
+        else:
+            m = p.block_mask[b * p.hq + int(h), i // fi.BLOCK]
+            for kb in range(lo // fi.BLOCK, (hi - 1) // fi.BLOCK + 1):
+                if kb < m.shape[0] and m[kb]:
+                    total += min(hi, (kb + 1) * fi.BLOCK) - max(lo, kb * fi.BLOCK)
+    return float(total) * (2 * p.dk + 2 * p.dv)
+
+
+def cpu_oracle_sample(p, seconds_target=2.0, seed=0, n0=256):
+    """Time the oracle on a seeded row sample of about ``seconds_target``
+    seconds; return (flop/s, rows, threads, secs, flops)."""
     import oracle
     rng = np.random.default_rng(seed)
-    units_all = np.stack(np.meshgrid(np.arange(p.total_q), np.arange(p.hq), indexing="ij"), -1).reshape(-1, 2)
-    # flops of each row: allowed keys * (2 Dk + 2 Dv); sample rows until about the target
-    n = 256
+    n_all = p.total_q * p.hq
     threads = os.cpu_count() or 1
+    n = max(16, n0)
     while True:
-        idx = rng.choice(len(units_all), size=min(n, len(units_all)), replace=False)
-        units = units_all[idx]
+        idx = rng.choice(n_all, size=min(n, n_all), replace=False)
+        units = np.stack([idx // p.hq, idx % p.hq], -1).astype(np.int64)
         t0 = time.time()
         oracle.forward(p, units=units, nthreads=threads)
         dt = time.time() - t0
-        if dt > 2.0 or n >= len(units_all):
+        if dt > 0.5 * seconds_target or n >= n_all:
             break
-        n *= 4
-    # flops of the sample: count allowed keys per sampled row exactly
-    sk = p.seqlens_k
-    sq = p.seqlens_q
-    seq_of = np.searchsorted(p.cu_seqlens_q[1:], units[:, 0], side="right")
-    flops = 0.0
-    for (t, h), b in zip(units, seq_of):
-        i = t - p.cu_seqlens_q[b]
-        ip = i + sk[b] - sq[b]
-        hi = min(sk[b], ip + 1) if p.causal else sk[b]
-        flops += max(hi, 0) * (2 * p.dk + 2 * p.dv)
-    rate = flops / dt
-    return rate, len(units), threads, dt, flops
+        n = int(n * min(8.0, max(2.0, seconds_target / max(dt, 1e-3))))
+    flops = row_flops(p, units)
+    return flops / dt, len(units), threads, dt, flops
 
 
 def max_over_ranks(ms, dist=None, device="cpu"):
@@ -384,16 +407,158 @@ def whole_job_rate(flops_per_step, world, ms):
     return flops_per_step * world / (ms * 1e-3) / 1e12
 
 
+HEADLINE = ("flex_prefill_b4_h16_s8192_d128_bf16: 6 runs (ALiBi 0.0625 causal and non-causal, soft-cap 20 "
+            "causal and non-causal, sliding window 256 causal, 50% random 128x128 block mask)")
+
+
+def headline_problems():
+    """The six config-5 runs (one shared set of Q, K, V; only the mods and
+    masks differ)."""
+    return fi.config5_runs()
+
+
+def headline_calls(probs, t, dev):
+    calls, outs = [], []
+    for p in probs:
+        tp = dict(t)
+        if p.block_mask is not None:
+            tp["bm"] = torch.from_numpy(p.block_mask.copy()).to(dev)
+        call, n, out, lse = make_call(p, tp, num_splits=0)
+        assert n == 1
+        calls.append(call)
+        outs.append((out, lse))
+    return calls, outs
+
+
+def e2e_headline(probs, steps, dev):
+    """The headline step end to end through the public API with HOST inputs:
+    every step copies the batch (Q, K, V, cu_seqlens, block mask) from pinned
+    host memory, runs the six calls and copies every output and LSE back.
+    Pipelined as a serving loop: two device buffer sets, step i+1's H2D (copy
+    stream) overlaps step i's calls (compute stream) and D2H (return stream).
+    Returns (ms per step pipelined, ms per step serial, H2D bytes, D2H bytes)."""
+    host_in = {k: v.cpu().pin_memory() for k, v in dev_tensors(probs[0], "cpu").items()}
+    bm_p = next(p for p in probs if p.block_mask is not None)
+    host_in["bm"] = torch.from_numpy(bm_p.block_mask.copy()).pin_memory()
+    sets = []
+    for _ in range(2):
+        dd = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+        calls = []
+        for p in probs:
+            tp = {k: v for k, v in dd.items() if k != "bm"}
+            if p.block_mask is not None:
+                tp["bm"] = dd["bm"]
+            call, _, out, lse = make_call(p, tp, num_splits=0)
+            calls.append((call, out, lse, torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                          torch.empty(lse.shape, dtype=lse.dtype).pin_memory()))
+        sets.append((dd, calls))
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(c[3].numel() * c[3].element_size() + c[4].numel() * c[4].element_size() for c in sets[0][1])
+    s_copy, s_comp, s_back = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def loop(n):
+        ev_comp, ev_back = [], []
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(s_copy)
+        for i in range(n):
+            dd, calls = sets[i % 2]
+            h2d_ev = torch.cuda.Event()
+            with torch.cuda.stream(s_copy):
+                if i >= 2:
+                    s_copy.wait_event(ev_comp[i - 2])      # step i-2 no longer reads this buffer set
+                for k, v in host_in.items():
+                    dd[k].copy_(v, non_blocking=True)
+                h2d_ev.record(s_copy)
+            ec = torch.cuda.Event()
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(h2d_ev)
+                if i >= 2:
+                    s_comp.wait_event(ev_back[i - 2])      # step i-2's results are home
+                for c in calls:
+                    c[0]()
+                ec.record(s_comp)
+            ev_comp.append(ec)
+            eb = torch.cuda.Event()
+            with torch.cuda.stream(s_back):
+                s_back.wait_event(ec)
+                for _, out, lse, out_h, lse_h in calls:
+                    out_h.copy_(out, non_blocking=True)
+                    lse_h.copy_(lse, non_blocking=True)
+                eb.record(s_back)
+            ev_back.append(eb)
+        end.record(s_back)
+        end.synchronize()
+        return start.elapsed_time(end) / n
+
+    def serial(n):
+        dd, calls = sets[0]
+        ts = []
+        for i in range(n + 1):
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ev.record()
+            for k, v in host_in.items():
+                dd[k].copy_(v, non_blocking=True)
+            for c in calls:
+                c[0]()
+            for _, out, lse, out_h, lse_h in calls:
+                out_h.copy_(out, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+            e_ev.record()
+            e_ev.synchronize()
+            if i:
+                ts.append(s_ev.elapsed_time(e_ev))
+        return statistics.mean(ts)
+
+    loop(3)
+    piped = loop(steps)
+    return piped, serial(max(2, steps // 2)), h2d, d2h
+
+
+def reference_arm(args, warmup, probs, flops_runs, workload):
+    """The fp64 CPU oracle as the reference arm: each step times a seeded row
+    sample of every run of the headline step, sized so that the whole run
+    (warm-up included) takes about a minute of host time."""
+    per_step = min(12.0, max(0.3, 60.0 / (args.steps + warmup)))
+    per_run = per_step / len(probs)
+    n_cal = [256] * len(probs)
+    for w in range(warmup):
+        for j, p in enumerate(probs):
+            n_cal[j] = cpu_oracle_sample(p, per_run, seed=1000 + 10 * w + j, n0=n_cal[j])[1]
+    rates, t_steps, rows, threads = [], [], 0, os.cpu_count() or 1
+    for k in range(args.steps):
+        flops = secs = 0.0
+        for j, p in enumerate(probs):
+            r = cpu_oracle_sample(p, per_run, seed=10 * k + j, n0=n_cal[j])
+            n_cal[j], threads = r[1], r[2]
+            flops += r[4]
+            secs += r[3]
+            rows += r[1]
+        rates.append(flops / secs / 1e12)
+        t_steps.append(secs * 1e3)
+    val = statistics.mean(rates)
+    line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": statistics.mean(t_steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload,
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"per step, a seeded sample of (token, head) rows of each of the six runs "
+                                       f"(about {per_run:.2f} s of fp64 C each, {threads} threads); "
+                                       f"{rows} rows over the {args.steps} timed steps"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--profile", default=None,
                     help="run only `warmup + steps` launches of one workload (for ncu captures): "
-                         "varlen_causal, varlen_noncausal, decode, dense, flex_<run>")
+                         "varlen_causal, varlen_noncausal, decode, dense, flex_<run>, ...")
     args = ap.parse_args()
     if args.profile:
         return profile_only(args.profile, args.warmup, args.steps)
@@ -407,36 +572,18 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    p_causal = fi.config2(causal=True)
-    p_full = fi.config2(causal=False)
-    flops_step = fi.prefill_flops(p_causal) + fi.prefill_flops(p_full)
-    workload = {"workload": "varlen_prefill_8seq_U0-2048_seed0_h16_d128_bf16_causal+noncausal",
-                "seqlens": [int(x) for x in p_causal.seqlens_q], "hq": 16, "hkv": 16, "d": 128,
-                "l2": "flushed between steps (256 MiB write)"}
+    probs = headline_problems()
+    flops_runs = [fi.prefill_flops(p) for p in probs]
+    flops_step = sum(flops_runs)
+    workload = {"workload": HEADLINE, "runs": list(fi.CONFIG5_RUNS), "batch": 4, "seq_len": 8192, "hq": 16,
+                "hkv": 16, "d": 128, "gflop_per_step": flops_step / 1e9,
+                "l2": "flushed before every launch (256 MiB write)"}
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        rates = []
-        for _ in range(warmup):
-            pass
-        t_steps = []
-        for k in range(args.steps):
-            r1 = cpu_oracle_sample(p_causal, seed=k)
-            r2 = cpu_oracle_sample(p_full, seed=k)
-            flops = r1[4] + r2[4]
-            secs = r1[3] + r2[3]
-            rates.append(flops / secs / 1e12)
-            t_steps.append(secs * 1e3)
-        val = statistics.mean(rates)
-        line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": warmup, "ms_per_step": statistics.mean(t_steps),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": workload,
-                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                 "sample": "seeded row samples (about 2-8 s each) of the causal and non-causal runs"},
-                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        if rank == 0:
+            reference_arm(args, warmup, probs, flops_runs, workload)
+        if dist:
+            dist.destroy_process_group()
         return
 
     import flashattention_forward_gb300 as fa
@@ -452,87 +599,129 @@ def main():
     pk = peaks()
 
     # ------------------------------------------------------- headline step --
-    tc, tf = dev_tensors(p_causal, dev), dev_tensors(p_full, dev)
-    call_c, n_c, _, _ = make_call(p_causal, tc)
-    call_f, n_f, _, _ = make_call(p_full, tf)
+    t = dev_tensors(probs[0], dev)
+    t.pop("bm", None)
+    calls, _ = headline_calls(probs, t, dev)
     for _ in range(warmup):
-        call_c()
-        call_f()
+        for c in calls:
+            c()
     torch.cuda.synchronize()
+    assert fa.device_error() == 0
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0 = time.time()
-        each = time_each([call_c, call_f], 0, args.steps, flush)
+        each = time_each(calls, 0, args.steps, flush)
         clk.mark(t0, time.time())
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    step_ms = [a + b for a, b in zip(*each)]
+    step_ms = [sum(x) for x in zip(*each)]
     ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
     value = whole_job_rate(flops_step, world, ms)
-    # dominant kernel: the non-causal launch (largest share of the step)
-    ms_f = statistics.mean(each[1])
-    ach = fi.prefill_flops(p_full) / (ms_f * 1e-3) / 1e12
-    # Roofline of the dominant launch: with L2 flushed every input comes from
-    # HBM, so the floor is the larger of the tensor time and the HBM time of
-    # the algorithmic bytes (Q, K, V read once; O, LSE written once).
-    alg_bytes = prefill_bytes(p_full)
-    t_tensor = fi.prefill_flops(p_full) / (pk["bf16"] * 1e12)
-    t_hbm = alg_bytes / (pk["hbm"] * 1e9)
+    runs = {}
+    for j, (run, p) in enumerate(zip(fi.CONFIG5_RUNS, probs)):
+        mj = statistics.mean(each[j])
+        tf = flops_runs[j] / (mj * 1e-3) / 1e12
+        ent = {"ms": mj, "tflops": tf, "frac_bf16": tf / pk["bf16"], "gflop": flops_runs[j] / 1e9}
+        if run == "window_causal":
+            gbs = prefill_bytes(p) / (mj * 1e-3) / 1e9
+            ent.update({"GB/s": gbs, "frac_hbm": gbs / pk["hbm"], "algorithmic_bytes": prefill_bytes(p)})
+        runs[run] = ent
+    # dominant launch: the run with the largest share of the step
+    jd = max(range(len(probs)), key=lambda j: statistics.mean(each[j]))
+    pd, run_d = probs[jd], fi.CONFIG5_RUNS[jd]
+    ms_d = statistics.mean(each[jd])
+    ach = flops_runs[jd] / (ms_d * 1e-3) / 1e12
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         tj = json.load(open(tpath))
-        if tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == "varlen_noncausal":
+        if tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == "flex_" + run_d:
             traffic = tj.get("dram_bytes_per_launch")
-    if t_hbm > t_tensor:
-        gbs = alg_bytes / (ms_f * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / pk["hbm"],
-                    "traffic": traffic, "algorithmic_bytes": alg_bytes, "tflops": ach,
-                    "tensor_frac": ach / pk["bf16"],
-                    "kernel": "fa_prefill2_kernel<128,128,packed,none>, non-causal launch",
-                    "peak_source": f"{pk['src']} HBM copy bandwidth; tensor peak {pk['bf16']} TFLOP/s bf16 burst"}
-    else:
-        roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
-                    "frac": ach / pk["bf16"], "traffic": traffic, "algorithmic_bytes": alg_bytes,
-                    "kernel": "fa_prefill2_kernel<128,128,packed,none>, non-causal launch",
-                    "peak_source": f"{pk['src']} bf16 burst (cuBLAS 8192^3)"}
-    extra = {}
+    mod_name = {0: "none", 1: "alibi", 2: "softcap"}[pd.mod_kind]
+    roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16"], "traffic": traffic, "algorithmic_bytes": prefill_bytes(pd),
+                "kernel": f"fa_prefill2_kernel<128,128,packed,{mod_name}>, config-5 run '{run_d}'",
+                "share_of_step": ms_d / statistics.mean(step_ms),
+                "peak_source": f"{pk['src']} bf16 burst (cuBLAS 8192^3)"}
+    extra, summary, e2e, cpu = {}, {}, None, None
     if rank == 0:
-        e2e_c, h2d_c, d2h_c = e2e_measure(p_causal, max(3, args.steps // 2), dev)
-        e2e_f, h2d_f, d2h_f = e2e_measure(p_full, max(3, args.steps // 2), dev)
-        e2e_p = e2e_pipelined([p_causal, p_full], max(6, args.steps // 2), dev)
-        e2e = {"value": flops_step / (e2e_p * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d_c + h2d_f, "d2h_bytes_per_step": d2h_c + d2h_f,
-               "ms_per_step": e2e_p,
-               "schedule": "two buffer sets: step i+1's pinned H2D overlaps step i's forward calls and D2H",
-               "serial": {"value": flops_step / ((e2e_c + e2e_f) * 1e-3) / 1e12,
-                          "ms_per_step": e2e_c + e2e_f,
-                          "schedule": "H2D, forward, D2H in sequence on one stream, per problem"}}
+        piped, serial, h2d, d2h = e2e_headline(probs, max(4, args.steps // 2), dev)
+        e2e = {"value": flops_step / (piped * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": piped,
+               "schedule": "two buffer sets: step i+1's pinned H2D overlaps step i's six calls and D2H",
+               "serial": {"value": flops_step / (serial * 1e-3) / 1e12, "ms_per_step": serial,
+                          "schedule": "H2D, six calls, D2H in sequence on one stream"}}
+        torch.cuda.empty_cache()
         if not args.quick:
             extra = other_workloads(dev, warmup, max(5, args.steps // 2), flush, pk)
-        rate, nrows, threads, secs, _ = cpu_oracle_sample(p_full, seed=1)
-        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{nrows} seeded (token, head) rows of the non-causal run, {secs:.1f} s, fp64 C with "
-                         f"{threads} threads"}
+        if world == 1:
+            flops = secs = 0.0
+            rows = threads = 0
+            for j, p in enumerate(probs):
+                r = cpu_oracle_sample(p, 2.0, seed=j)
+                flops += r[4]
+                secs += r[3]
+                rows += r[1]
+                threads = r[2]
+            cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{rows} seeded (token, head) rows across the six runs (about 2 s each), "
+                             f"{secs:.1f} s of fp64 C with {threads} threads"}
+        summary = compact_summary(runs, extra, pk)
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": (n_c + n_f) * args.steps, "clocks": clk.summary(),
-                "pct_of_peak": 100.0 * value / world / pk["bf16"], "workloads": extra,
-                "kernel_hash": kernel_hash()}
+                "gpu_launches": len(calls) * args.steps, "clocks": clk.summary(),
+                "pct_of_peak": 100.0 * value / world / pk["bf16"], "kernel_hash": kernel_hash(),
+                "runs": runs, "workloads": extra, "summary": summary}
         print(json.dumps(line))
     if dist:
         dist.barrier()
         dist.destroy_process_group()
 
 
+def compact_summary(runs, extra, pk):
+    """Short per-workload figures (ms, TFLOP/s or GB/s, fraction of the
+    roofline) placed last in the printed line."""
+    r3 = lambda x: round(float(x), 3)
+    out = {"c5": {k: [r3(v["ms"]), r3(v["tflops"]), r3(v.get("frac_hbm", v["frac_bf16"]))] for k, v in runs.items()}}
+    key = {"varlen_prefill_8seq_h16_d128_causal": "c2_causal", "varlen_prefill_8seq_h16_d128_noncausal": "c2",
+           "paged_decode_64seq_hq32_hkv8_p16": "c3", "paged_decode_e4m3_64seq_hq32_hkv8_p16": "c3_e4m3",
+           "paged_decode_int8_64seq_hq32_hkv8_p16": "c3_int8", "paged_fp8_d192_v128_16seq_h16_p64_causal": "c4",
+           "paged_fp8kv_qe4m3_d128_16seq_h16_p64_causal": "c4_q8_d128",
+           "bwd_4x4096_h16_d128_noncausal": "bwd_4x4096"}
+    for name, short in key.items():
+        v = extra.get(name)
+        if not v:
+            continue
+        if "GB/s" in v:
+            out[short] = [r3(v["ms"]), r3(v["GB/s"]), r3(v["frac_hbm"])]
+        else:
+            out[short] = [r3(v["ms"]), r3(v["tflops"]), r3(v["frac_bf16"])]
+    d = extra.get("dense_causal_b2_h4_s128_d64")
+    if d:
+        out["c1_us"] = [r3(d["device_us_per_launch"]), r3(d["wall_us_per_call"])]
+    out["fields"] = "c5 and prefill: [ms, TFLOP/s, frac of bf16 peak]; decode and window: [ms, GB/s, frac of HBM]"
+    return out
+
+
 def other_workloads(dev, warmup, steps, flush, pk):
     import flashattention_forward_gb300 as fa
     res = {}
+    # config 2: packed varlen bf16 prefill, 8 seqs U{0..2048}, H 16, D 128
+    for causal in (True, False):
+        p = fi.config2(causal=causal)
+        t = dev_tensors(p, dev)
+        call, _, _, _ = make_call(p, t, num_splits=0)
+        ms = statistics.mean(time_calls([call], warmup, steps, flush))
+        fl = fi.prefill_flops(p)
+        res["varlen_prefill_8seq_h16_d128_" + ("causal" if causal else "noncausal")] = {
+            "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+            "gflop": fl / 1e9, "seqlens": [int(x) for x in p.seqlens_q]}
+        del t
     # dense causal latency case (launch-latency bound): wall and device time
     p = fi.config1()
     t = dev_tensors(p, dev)
@@ -661,22 +850,6 @@ def other_workloads(dev, warmup, steps, flush, pk):
         res[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
                      "gflop": fl / 1e9}
         del t
-    # flex runs at B=4, H=16, S=8192
-    for run in fi.CONFIG5_RUNS:
-        p = fi.config5(run)
-        t = dev_tensors(p, dev)
-        call, _, _, _ = make_call(p, t)
-        times = time_calls([call], 2, max(3, steps // 2), flush)
-        ms = statistics.mean(times)
-        fl = fi.prefill_flops(p)
-        ent = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"]}
-        if run == "window_causal":
-            byt = (p.q.nbytes + p.k.nbytes + p.v.nbytes + p.total_q * p.hq * p.dv * 2 + p.total_q * p.hq * 4)
-            ent["GB/s"] = byt / (ms * 1e-3) / 1e9
-            ent["frac_hbm"] = ent["GB/s"] / pk["hbm"]
-        res["flex_" + run] = ent
-        del t
-        torch.cuda.empty_cache()
     return res
 
 

@@ -123,9 +123,10 @@ class Problem:
     block_mask: Optional[np.ndarray] = None    # uint8 [B*Hq, nqb, nkb]
     q_dtype: str = "bf16"                      # "bf16" (uint16 bits) or "e4m3" (uint8 bytes; its
                                                # per-tensor scale is folded into softmax_scale)
-    # prologue maps x -> mul * x + add on Q, K, V as read:
-    # (q_mul, q_add, k_mul, k_add, v_mul, v_add); None = identity
-    prologue: Optional[tuple] = None
+    # prologue op chains on Q, K, V as read: {"q": [("mul", 0.5), ("add", 1.0)],
+    # "k": [...], "v": [...]}, each op ("mul" | "add" | "sub" | "div", value)
+    # applied in order to every element; None or missing keys = no ops
+    prologue: Optional[dict] = None
 
     @property
     def num_seqs(self) -> int:
@@ -376,24 +377,45 @@ def config4_big(seed: int = 0, lens: Optional[Sequence[int]] = None):
 CONFIG5_RUNS = ("alibi_causal", "alibi", "softcap_causal", "softcap", "window_causal", "blocksparse")
 
 
+def _config5_kw(run: str) -> dict:
+    if run == "alibi_causal":
+        return dict(mod="alibi", causal=True)
+    if run == "alibi":
+        return dict(mod="alibi")
+    if run == "softcap_causal":
+        return dict(mod="softcap", causal=True)
+    if run == "softcap":
+        return dict(mod="softcap")
+    if run == "window_causal":
+        return dict(window=256, causal=True)
+    if run == "blocksparse":
+        return dict(block_mask_density=0.5)
+    raise ValueError(run)
+
+
 def config5(run: str = "alibi_causal", seed: int = 0, seq: int = 8192, batch: int = 4) -> Problem:
     """Flex bf16 prefill: B=4, H=16, S=8192, D=128 with one score mod or mask per run."""
-    kw = dict(hq=16, dk=128, seed=seed, name=f"flex_{run}_b{batch}_h16_s{seq}_d128")
-    if run == "alibi_causal":
-        kw.update(mod="alibi", causal=True)
-    elif run == "alibi":
-        kw.update(mod="alibi")
-    elif run == "softcap_causal":
-        kw.update(mod="softcap", causal=True)
-    elif run == "softcap":
-        kw.update(mod="softcap")
-    elif run == "window_causal":
-        kw.update(window=256, causal=True)
-    elif run == "blocksparse":
-        kw.update(block_mask_density=0.5)
-    else:
-        raise ValueError(run)
-    return make_problem([seq] * batch, **kw)
+    return make_problem([seq] * batch, hq=16, dk=128, seed=seed, name=f"flex_{run}_b{batch}_h16_s{seq}_d128",
+                        **_config5_kw(run))
+
+
+def config5_runs(seed: int = 0, seq: int = 8192, batch: int = 4) -> list:
+    """The six config-5 runs in CONFIG5_RUNS order, sharing one set of Q, K, V
+    arrays: every run draws the same Q, K, V (same seed and shapes, drawn
+    first), so each equals config5(run) field by field."""
+    base = config5("blocksparse", seed, seq, batch)
+    runs = []
+    for run in CONFIG5_RUNS:
+        if run == "blocksparse":
+            runs.append(base)
+            continue
+        kw = _config5_kw(run)
+        mk = {"none": MOD_NONE, "alibi": MOD_ALIBI, "softcap": MOD_SOFTCAP}[kw.get("mod", "none")]
+        runs.append(base.replace(name=f"flex_{run}_b{batch}_h16_s{seq}_d128", block_mask=None,
+                                 causal=kw.get("causal", False), window=kw.get("window", 0), mod_kind=mk,
+                                 alibi_slope=0.0625 if mk == MOD_ALIBI else 0.0,
+                                 softcap=20.0 if mk == MOD_SOFTCAP else 0.0))
+    return runs
 
 
 # --------------------------------------------------------------------------

@@ -51,36 +51,41 @@ class BlockMask(ctypes.Structure):
                 ("blk_q", ctypes.c_int32), ("blk_k", ctypes.c_int32)]
 
 
+PROLOGUE_MAX_OPS = 8
+FA_OP_MUL, FA_OP_ADD, FA_OP_SUB, FA_OP_DIV = 1, 2, 3, 4
+_OPS = {"mul": FA_OP_MUL, "add": FA_OP_ADD, "sub": FA_OP_SUB, "div": FA_OP_DIV}
+
+
+class PrologueOp(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int32), ("value", ctypes.c_float)]
+
+
 class Prologue(ctypes.Structure):
-    _fields_ = [("q_mul", ctypes.c_float), ("q_add", ctypes.c_float), ("k_mul", ctypes.c_float),
-                ("k_add", ctypes.c_float), ("v_mul", ctypes.c_float), ("v_add", ctypes.c_float)]
+    _fields_ = [("n_q", ctypes.c_int32), ("n_k", ctypes.c_int32), ("n_v", ctypes.c_int32),
+                ("q", PrologueOp * PROLOGUE_MAX_OPS), ("k", PrologueOp * PROLOGUE_MAX_OPS),
+                ("v", PrologueOp * PROLOGUE_MAX_OPS)]
 
 
 def make_prologue(prologue) -> Optional[Prologue]:
-    """The C prologue for ``prologue``: None, a Prologue, or a dict mapping
-    "q", "k", "v" to op chains applied in order to each element as read --
-    ("mul", c), ("div", c), ("add", c), ("sub", c) -- composed into one map
-    x -> mul * x + add per tensor."""
+    """The C ``fa_prologue_t`` for ``prologue``: None, a Prologue, or a dict
+    mapping "q", "k", "v" to op chains -- lists of ("mul" | "add" | "sub" |
+    "div", value), applied in order to each element as it is read.  The ops
+    are copied as given; the library composes and folds them."""
     if prologue is None or isinstance(prologue, Prologue):
         return prologue
-    maps = {}
+    pro = Prologue()
     for name in ("q", "k", "v"):
-        m, a = 1.0, 0.0
-        for op, c in prologue.get(name, ()):
-            c = float(c)
-            if op == "mul":
-                m, a = m * c, a * c
-            elif op == "div":
-                m, a = m / c, a / c
-            elif op == "add":
-                a = a + c
-            elif op == "sub":
-                a = a - c
-            else:
-                raise ValueError(f"prologue op {op!r}: mul, div, add or sub")
-        maps[name] = (m, a)
-    return Prologue(q_mul=maps["q"][0], q_add=maps["q"][1], k_mul=maps["k"][0], k_add=maps["k"][1],
-                    v_mul=maps["v"][0], v_add=maps["v"][1])
+        ops = list(prologue.get(name, ()))
+        if len(ops) > PROLOGUE_MAX_OPS:
+            raise ValueError(f"at most {PROLOGUE_MAX_OPS} prologue ops per tensor")
+        arr = getattr(pro, name)
+        for i, (op, value) in enumerate(ops):
+            if op not in _OPS:
+                raise ValueError(f"prologue op {op!r}: mul, add, sub or div")
+            arr[i].op = _OPS[op]
+            arr[i].value = float(value)
+        setattr(pro, "n_" + name, len(ops))
+    return pro
 
 
 class Launch(ctypes.Structure):
@@ -111,8 +116,8 @@ def lib() -> ctypes.CDLL:
                                                          ctypes.c_int32, P(ScoreMod), P(BlockMask), P(Prologue),
                                                          ctypes.c_int32, P(Launch), ctypes.c_void_p]
             L.fa_fwd_varlen.restype = ctypes.c_int
-            L.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
-                                                 ctypes.c_int32]
+            L.fa_fwd_workspace_bytes.argtypes = [P(Launch), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                 P(Prologue)]
             L.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
             L.fa_fwd_default_splits.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
@@ -196,8 +201,9 @@ def default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size=0, t
     return int(lib().fa_fwd_default_splits(num_seqs, max_seqlen_q, max_seqlen_k, int(total_k), hq, hkv, page_size))
 
 
-def workspace_bytes(num_seqs, total_q, hq, dv, num_splits) -> int:
-    return int(lib().fa_fwd_workspace_bytes(num_seqs, total_q, hq, dv, num_splits))
+def workspace_bytes(launch: "Launch", hq: int, hkv: int, dv: int, prologue=None) -> int:
+    """Workspace bytes of a forward call (split-KV partials, a Q add's per-key terms)."""
+    return int(lib().fa_fwd_workspace_bytes(ctypes.byref(launch), hq, hkv, dv, _ref(make_prologue(prologue))))
 
 
 def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -220,7 +226,8 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     device read-back).  Returns ``(out [T_q, Hq, Dv] bf16, lse [Hq, T_q] fp32
     or None)``.  ``num_splits=None`` picks the library's default (split-KV for
     decode shapes); 0 forces the single-pass kernel.  ``prologue``: op chains
-    on Q/K/V reads (see make_prologue and fa_prologue_t).
+    on the Q/K/V reads, {"q": [("mul", c), ("add", d), ...], "k": ..., "v": ...}
+    (see make_prologue and fa_prologue_t).
     """
     L = lib()
     B = cu_seqlens_q.shape[0] - 1
@@ -242,15 +249,15 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             num_splits = 0
     launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                     num_splits=num_splits, total_q=Tq, total_k=total_k)
-    if num_splits > 1:
-        need = workspace_bytes(B, Tq, Hq, Dv, num_splits)
+    pro = make_prologue(prologue)
+    need = workspace_bytes(launch, Hq, Hkv, Dv, pro)
+    if need:
         if workspace is None or workspace.numel() < need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         launch.workspace = workspace.data_ptr()
         launch.workspace_bytes = workspace.numel()
     sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
     bm = _block_mask(block_mask)
-    pro = make_prologue(prologue)
     args = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
             as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(k_scale), as_tensor(v_scale),
             as_tensor(out), as_tensor(lse)]
@@ -265,27 +272,37 @@ def fwd_varlen_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                        cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, out: torch.Tensor,
                        lse: Optional[torch.Tensor], *, max_seqlen_q: int, max_seqlen_k: int,
                        total_k: Optional[int] = None, block_table: Optional[torch.Tensor] = None,
-                       page_size: int = 0, softmax_scale: Optional[float] = None, causal: bool = False,
-                       window: int = 0, num_splits: int = 0, stream=None, prologue=None):
-    """Split-KV decode through ``fa_fwd_varlen_noalloc``: for callers that cannot
-    allocate device memory (the partials go to the library's static scratch of
-    NOALLOC_SCRATCH_BYTES).  ``out`` (and ``lse`` if wanted) are caller-provided;
-    this wrapper allocates nothing.  ``num_splits=0`` uses the library default."""
+                       page_size: int = 0, k_scale: Optional[torch.Tensor] = None,
+                       v_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+                       causal: bool = False, window: int = 0, score_mod: int = MOD_NONE,
+                       alibi_slope: float = 0.0, softcap: float = 0.0,
+                       block_mask: Optional[torch.Tensor] = None, num_splits: int = 0, stream=None,
+                       prologue=None):
+    """Split-KV decode through ``fa_fwd_varlen_noalloc``, for callers that cannot
+    allocate device memory when they run attention: the split partials (and a
+    Q add's per-key terms) go to the library's static scratch of
+    NOALLOC_SCRATCH_BYTES.  Takes the arguments of fwd_varlen, including byte
+    caches with their scales, score mods, block masks and prologues; ``out``
+    (and ``lse`` if wanted) are caller-provided and this wrapper allocates
+    nothing.  ``num_splits=0`` uses the library default."""
     L = lib()
     B = cu_seqlens_q.shape[0] - 1
     Tq, Hq, Dk = q.shape
+    kv_dt = _kv_dtype(k_cache)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(Dk)
     if total_k is None:
         total_k = k_cache.shape[0] if block_table is None else 0
     launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                     num_splits=num_splits, total_q=Tq, total_k=total_k)
-    args = [as_tensor(q), as_tensor(k_cache), as_tensor(v_cache), as_tensor(block_table),
-            as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), None, None, as_tensor(out), as_tensor(lse)]
-    sm = ScoreMod(kind=MOD_NONE)
+    args = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
+            as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(k_scale), as_tensor(v_scale),
+            as_tensor(out), as_tensor(lse)]
+    sm = ScoreMod(kind=score_mod, alibi_slope=alibi_slope, softcap=softcap)
     _check(L.fa_fwd_varlen_noalloc(*[_ref(a) for a in args], float(softmax_scale), int(bool(causal)),
-                                   int(window), ctypes.byref(sm), None, _ref(make_prologue(prologue)),
-                                   int(page_size), ctypes.byref(launch), ctypes.c_void_p(_stream_ptr(stream))))
+                                   int(window), ctypes.byref(sm), _ref(_block_mask(block_mask)),
+                                   _ref(make_prologue(prologue)), int(page_size), ctypes.byref(launch),
+                                   ctypes.c_void_p(_stream_ptr(stream))))
     return out, lse
 
 
@@ -330,8 +347,9 @@ class FwdPlan:
         self.launch = Launch(num_seqs=B, max_seqlen_q=kw["max_seqlen_q"], max_seqlen_k=kw["max_seqlen_k"],
                              num_splits=num_splits, total_q=Tq, total_k=total_k)
         ws = kw.get("workspace")
-        if num_splits > 1:
-            need = workspace_bytes(B, Tq, Hq, Dv, num_splits)
+        pro = make_prologue(kw.get("prologue"))
+        need = workspace_bytes(self.launch, Hq, Hkv, Dv, pro)
+        if need:
             if ws is None or ws.numel() < need:
                 ws = torch.empty(need, dtype=torch.uint8, device=q.device)
             self.launch.workspace = ws.data_ptr()
@@ -339,7 +357,6 @@ class FwdPlan:
         self._ws = ws
         sm = ScoreMod(kind=score_mod, alibi_slope=kw.get("alibi_slope", 0.0), softcap=kw.get("softcap", 0.0))
         bm = _block_mask(block_mask)
-        pro = make_prologue(kw.get("prologue"))
         descs = [as_tensor(q), as_tensor(k_cache, kv_dt), as_tensor(v_cache, kv_dt), as_tensor(block_table),
                  as_tensor(cu_seqlens_q), as_tensor(cu_seqlens_k), as_tensor(kw.get("k_scale")),
                  as_tensor(kw.get("v_scale")), as_tensor(self.out), as_tensor(self.lse)]

@@ -158,6 +158,18 @@ fa_status_t check_mods(const fa_score_mod_t *score_mod, const fa_block_mask_t *b
   return FA_OK;
 }
 
+// The bf16 prefill runs its register-rebalanced one-pass softmax when the
+// build's launch registers allow it; FA_GB300_PREFILL_VARIANT=1 in the
+// environment at the first forward call of the process selects the 10-warp
+// two-pass form instead (a diagnosis switch; results agree to rounding).
+int prefill_variant() {
+  static const int v = [] {
+    const char *e = getenv("FA_GB300_PREFILL_VARIANT");
+    return (e && e[0] == '1') ? 1 : 0;
+  }();
+  return v;
+}
+
 // Byte geometry of a paged cache [N_pg, P_s, Hkv, D] for the row gather.
 fa::KvGather kv_gather(const fa_tensor_t *t, int esz) {
   fa::KvGather g;
@@ -172,6 +184,61 @@ bool supported_dims(int64_t dk, int64_t dv) {
   return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
 }
 
+// A prologue's op chains, each composed into one map x -> a * x + b.
+struct Folded {
+  double aq = 1, bq = 0, ak = 1, bk = 0, av = 1, bv = 0;
+};
+
+fa_status_t compose_chain(const fa_prologue_op_t *ops, int32_t n, const char *name, double *a, double *b) {
+  *a = 1.0;
+  *b = 0.0;
+  if (n < 0 || n > FA_PROLOGUE_MAX_OPS)
+    return fail(FA_ERR_INVALID_ARG, "prologue %s chain has %d ops (0 ... %d)", name, n, FA_PROLOGUE_MAX_OPS);
+  for (int i = 0; i < n; ++i) {
+    const double c = ops[i].value;
+    if (!std::isfinite(ops[i].value)) return fail(FA_ERR_INVALID_ARG, "prologue values must be finite");
+    switch (ops[i].op) {
+      case FA_OP_MUL: *a *= c; *b *= c; break;
+      case FA_OP_ADD: *b += c; break;
+      case FA_OP_SUB: *b -= c; break;
+      case FA_OP_DIV:
+        if (c == 0.0) return fail(FA_ERR_INVALID_ARG, "prologue %s chain divides by 0", name);
+        *a /= c;
+        *b /= c;
+        break;
+      default: return fail(FA_ERR_INVALID_ARG, "prologue %s op %d: use FA_OP_MUL, ADD, SUB or DIV", name, ops[i].op);
+    }
+  }
+  if (!std::isfinite(*a) || !std::isfinite(*b)) return fail(FA_ERR_INVALID_ARG, "prologue %s chain overflows", name);
+  return FA_OK;
+}
+
+fa_status_t fold_prologue(const fa_prologue_t *pro, Folded *f) {
+  *f = Folded();
+  if (!pro) return FA_OK;
+  fa_status_t st;
+  if ((st = compose_chain(pro->q, pro->n_q, "q", &f->aq, &f->bq))) return st;
+  if ((st = compose_chain(pro->k, pro->n_k, "k", &f->ak, &f->bk))) return st;
+  return compose_chain(pro->v, pro->n_v, "v", &f->av, &f->bv);
+}
+
+// A Q add contributes scale * b_q * a_k * sum_d k_j[d] to score j.
+bool needs_col_bias(const Folded &f) { return f.bq != 0.0 && f.ak != 0.0; }
+
+int64_t col_bias_ld(int32_t max_seqlen_k) { return ((int64_t)max_seqlen_k + 127) / 128 * 128; }
+
+size_t split_part_bytes(const fa_launch_t *L, int32_t hq, int32_t dv) {
+  if (L->num_splits < 2 || L->total_q <= 0 || hq <= 0 || dv <= 0) return 0;
+  const size_t o = (size_t)L->num_splits * L->total_q * hq * dv * sizeof(float);
+  const size_t l = (size_t)L->num_splits * hq * L->total_q * sizeof(float);
+  return align256(o) + align256(l);
+}
+
+size_t col_part_bytes(const fa_launch_t *L, int32_t hkv, const Folded &f) {
+  if (!needs_col_bias(f) || L->num_seqs <= 0 || hkv <= 0 || L->max_seqlen_k <= 0) return 0;
+  return align256((size_t)L->num_seqs * hkv * col_bias_ld(L->max_seqlen_k) * sizeof(float));
+}
+
 }  // namespace
 
 namespace fa {
@@ -183,6 +250,8 @@ fa_status_t set_host_error(fa_status_t st, const char *msg) { return fail(st, "%
 struct fa_fwd_plan_s {
   int kind = 0;              // 0: nothing to launch, 1: split-KV decode (+ combine), 2: prefill
   int dk = 0, fp8 = 0;
+  int has_cb = 0;            // the prologue's per-key term is computed first
+  fa::ColBiasParams cb;
   fa::DecodeLaunch dl;
   int splits = 0, hq = 0, dv = 0;
   int64_t rows = 0;
@@ -192,8 +261,17 @@ struct fa_fwd_plan_s {
 
 namespace {
 
+fa_status_t run_col_bias(const fa_fwd_plan_s &P, cudaStream_t s) {
+  if (!P.has_cb) return FA_OK;
+  cudaError_t e = fa::launch_col_bias(P.cb, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prologue key-term launch");
+  return FA_OK;
+}
+
 fa_status_t run_decode(fa::DecodeLaunch L, const fa_fwd_plan_s &P, cudaStream_t s) {
   L.stream = s;
+  fa_status_t st = run_col_bias(P, s);
+  if (st != FA_OK) return st;
   cudaError_t e = fa::launch_decode(P.dk, L);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (P.splits > 1) {
@@ -205,6 +283,8 @@ fa_status_t run_decode(fa::DecodeLaunch L, const fa_fwd_plan_s &P, cudaStream_t 
 
 fa_status_t run_prefill(fa::PrefillLaunch L, const fa_fwd_plan_s &P, cudaStream_t s) {
   L.stream = s;
+  fa_status_t st = run_col_bias(P, s);
+  if (st != FA_OK) return st;
   cudaError_t e;
   if (P.dk == 64) e = fa::launch_prefill_64_64(L);
   else if (P.dk == 128) e = fa::launch_prefill_128_128(L);
@@ -233,12 +313,15 @@ const char *fa_last_error(void) { return g_msg; }
 
 const char *fa_version(void) { return "fa_gb300 0.1 (sm_103a)"; }
 
-size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int32_t dv, int32_t num_splits) {
-  (void)num_seqs;
-  if (num_splits <= 0 || total_q <= 0 || hq <= 0 || dv <= 0) return 0;
-  const size_t o = (size_t)num_splits * total_q * hq * dv * sizeof(float);
-  const size_t l = (size_t)num_splits * hq * total_q * sizeof(float);
-  return align256(o) + align256(l);
+size_t fa_fwd_workspace_bytes(const fa_launch_t *launch, int32_t hq, int32_t hkv, int32_t dv,
+                              const fa_prologue_t *prologue) {
+  if (!launch) return 0;
+  Folded f;
+  char saved[sizeof g_msg];
+  memcpy(saved, g_msg, sizeof g_msg);
+  if (fold_prologue(prologue, &f) != FA_OK) f = Folded();   // the call itself reports a malformed prologue
+  memcpy(g_msg, saved, sizeof g_msg);
+  return split_part_bytes(launch, hq, dv) + col_part_bytes(launch, hkv, f);
 }
 
 int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k, int64_t total_k,
@@ -450,24 +533,34 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   int mod = 0;
   float slope = 0.f, cap = 0.f;
   if ((st = check_mods(score_mod, block_mask, launch, &mod, &slope, &cap))) return st;
-  // ---- prologue: folded (see fa_prologue_t) -- q_mul * k_mul into the
-  // score scale, k_add into an LSE term per unit of sum_d q, v_* into the
-  // output
-  float pro_vmul = 1.f, pro_vadd = 0.f, pro_lse_k = 0.f;
-  if (prologue) {
-    const float vals[6] = {prologue->q_mul, prologue->q_add, prologue->k_mul,
-                           prologue->k_add, prologue->v_mul, prologue->v_add};
-    for (float x : vals)
-      if (!std::isfinite(x)) return fail(FA_ERR_INVALID_ARG, "prologue values must be finite");
-    if (prologue->q_add != 0.f)
-      return fail(FA_ERR_UNSUPPORTED, "prologue q_add must be 0 (it would add a per-key term to the scores)");
-    if (prologue->k_add != 0.f && mod == 2)
-      return fail(FA_ERR_UNSUPPORTED, "prologue k_add with the soft-cap (the cap is not shift-invariant)");
-    if (prologue->k_add != 0.f && q8) return fail(FA_ERR_UNSUPPORTED, "prologue k_add with e4m3 q");
-    pro_lse_k = softmax_scale * prologue->q_mul * prologue->k_add;
-    softmax_scale = softmax_scale * (prologue->q_mul * prologue->k_mul);
-    pro_vmul = prologue->v_mul;
-    pro_vadd = prologue->v_add;
+  // ---- prologue: each chain composed to x -> a * x + b and folded (see
+  // fa_prologue_t): a_q a_k into the score scale, the row term into the LSE
+  // (or, under the soft-cap, into the capped score), the key term of a Q add
+  // into a per-key array computed by a pre-pass, a_v and b_v into the output
+  Folded fo;
+  if ((st = fold_prologue(prologue, &fo))) return st;
+  const bool col_bias = needs_col_bias(fo);
+  if (q8 && (fo.bq != 0.0 || fo.bk != 0.0))
+    return fail(FA_ERR_UNSUPPORTED, "prologue adds on q or k with e4m3 q");
+  float pro_vmul = (float)fo.av, pro_vadd = (float)fo.bv;
+  float pro_lse_k = 0.f, pro_lse_c = 0.f, pro_row_k = 0.f, pro_row_c = 0.f, cb_factor = 0.f;
+  {
+    const double sc = softmax_scale;
+    const double row_k = sc * fo.aq * fo.bk, row_c = sc * fo.bq * fo.bk * (double)Dk;
+    // score units: log2 (the kernels' exponent), or 2u*log2(e) under the soft-cap
+    const double unit = mod == 2 ? 2.0 * (double)fa::kLog2e / (double)cap : (double)fa::kLog2e;
+    if (mod == 2) {
+      pro_row_k = (float)(row_k * unit);
+      pro_row_c = (float)(row_c * unit);
+    } else {
+      pro_lse_k = (float)row_k;
+      pro_lse_c = (float)row_c;
+    }
+    cb_factor = (float)(sc * fo.bq * fo.ak * unit);
+    softmax_scale = (float)(sc * fo.aq * fo.ak);
+    if (!std::isfinite(softmax_scale) || !std::isfinite(cb_factor) || !std::isfinite(pro_row_k) ||
+        !std::isfinite(pro_row_c) || !std::isfinite(pro_lse_k) || !std::isfinite(pro_lse_c))
+      return fail(FA_ERR_INVALID_ARG, "prologue maps overflow the score scale");
   }
   if (window < 0) window = 0;
   if (B == 0 || Tq == 0) return FA_OK;
@@ -479,6 +572,45 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const CUtensorMapDataType kv_tmdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int group = (int)(Hq / Hkv);
   const bool have_keys = launch->total_k > 0 || (paged && n_pages > 0);
+  // ---- workspace: [split-KV partials][prologue key terms]
+  const size_t ws_split = split_part_bytes(launch, (int32_t)Hq, (int32_t)Dv);
+  const size_t ws_need = ws_split + col_part_bytes(launch, (int32_t)Hkv, fo);
+  // checked by each path after its own limits
+  auto check_workspace = [&]() -> fa_status_t {
+    if (ws_need == 0) return FA_OK;
+    if (!launch->workspace || launch->workspace_bytes < ws_need)
+      return fail(FA_ERR_INVALID_ARG, "this call needs a workspace of %zu bytes (fa_fwd_workspace_bytes)", ws_need);
+    if ((uintptr_t)launch->workspace & 255) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    return FA_OK;
+  };
+  fa::ColBiasParams cbp;
+  memset(&cbp, 0, sizeof cbp);
+  float *col_bias_ptr = nullptr;
+  const int64_t cb_ld = col_bias_ld(launch->max_seqlen_k);
+  if (col_bias && launch->max_seqlen_k > 0 && have_keys) {
+    if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "a Q add needs num_seqs and Hkv <= 65535");
+    col_bias_ptr = (float *)((char *)launch->workspace + ws_split);
+    cbp.k = (const uint8_t *)k_cache->data;
+    cbp.kv = kv_dt == FA_E4M3 ? 1 : (kv_dt == FA_I8 ? 2 : 0);
+    cbp.s_page = k_cache->stride[0] * esz;
+    cbp.s_slot = paged ? k_cache->stride[1] * esz : 0;
+    cbp.s_head = k_cache->stride[kvnd - 2] * esz;
+    cbp.block_table = paged ? (const int32_t *)block_table->data : nullptr;
+    cbp.bt_stride = paged ? block_table->stride[0] : 0;
+    cbp.max_pages = max_pages;
+    cbp.page_size = paged ? page_size : 1;
+    cbp.page_shift = paged ? ilog2(page_size) : 0;
+    cbp.n_pages = paged ? n_pages : k_cache->shape[0];
+    cbp.cu_k = (const int32_t *)cu_seqlens_k->data;
+    cbp.k_scale = fp8 ? (const float *)k_scale->data : nullptr;
+    cbp.dk = (int32_t)Dk;
+    cbp.hkv = (int32_t)Hkv;
+    cbp.num_seqs = (int32_t)B;
+    cbp.ld = cb_ld;
+    cbp.factor = cb_factor;
+    cbp.out = col_bias_ptr;
+    cbp.err = error_word();
+  }
 
   // ------------------------------------------------------------ split-KV --
   if (launch->num_splits > 0) {
@@ -487,6 +619,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
       return fail(FA_ERR_UNSUPPORTED, "split-KV needs max_seqlen_q * Hq/Hkv <= %d", fa::kDecRows);
     if (Dk != Dv || (Dk != 64 && Dk != 128)) return fail(FA_ERR_UNSUPPORTED, "split-KV supports Dk = Dv in {64, 128}");
     if (B > 65535 || Hkv > 65535) return fail(FA_ERR_UNSUPPORTED, "too many sequences or kv heads for split-KV");
+    if ((st = check_workspace())) return st;
     fa::DecodeLaunch L;
     memset(&L, 0, sizeof L);
     L.kv = kv_dt == FA_E4M3 ? 1 : (kv_dt == FA_I8 ? 2 : 0);
@@ -545,7 +678,14 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.pro_vmul = pro_vmul;
     p.pro_vadd = pro_vadd;
     p.pro_lse_k = pro_lse_k;
-    p.mod = mod;
+    p.pro_lse_c = pro_lse_c;
+    p.pro_row_k = pro_row_k;
+    p.pro_row_c = pro_row_c;
+    p.col_bias = col_bias_ptr;
+    p.cb_ld = cb_ld;
+    // the plain score loop has no per-key term: a Q add takes the general
+    // path (ALiBi with slope 0)
+    p.mod = (mod == 0 && col_bias_ptr) ? 1 : mod;
     p.alibi_log2 = mod == 1 ? slope * fa::kLog2e : 0.f;
     p.softcap_arg = mod == 2 ? softmax_scale / cap : 0.f;
     p.softcap_log2 = mod == 2 ? cap * fa::kLog2e : 0.f;
@@ -572,10 +712,6 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.k_scale = fp8 ? (const float *)k_scale->data : nullptr;
     p.v_scale = fp8 ? (const float *)v_scale->data : nullptr;
     if (S > 1) {
-      const size_t need = fa_fwd_workspace_bytes((int)B, Tq, (int)Hq, (int)Dv, S);
-      if (!launch->workspace || launch->workspace_bytes < need)
-        return fail(FA_ERR_INVALID_ARG, "split-KV with %d splits needs a workspace of %zu bytes", S, need);
-      if ((uintptr_t)launch->workspace & 255) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
       p.o_part = (float *)launch->workspace;
       p.lse_part = (float *)((char *)launch->workspace + align256((size_t)S * Tq * Hq * Dv * sizeof(float)));
     }
@@ -584,6 +720,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     fa_fwd_plan_s &P = plan ? *plan : local;
     P.kind = 1;
     P.dk = (int)Dk;
+    P.has_cb = col_bias_ptr != nullptr;
+    P.cb = cbp;
     P.splits = S;
     P.rows = Tq;
     P.hq = (int)Hq;
@@ -601,6 +739,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const int64_t n_hgroups = (Hq + head_group - 1) / head_group;
   const int64_t n_blocks = B * n_hgroups * n_qtiles * head_group;
   if (n_blocks >= (int64_t(1) << 31)) return fail(FA_ERR_UNSUPPORTED, "grid too large");
+  if ((st = check_workspace())) return st;
   fa::PrefillLaunch L;
   memset(&L, 0, sizeof L);
   {
@@ -690,6 +829,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   p.pro_vmul = pro_vmul;
   p.pro_vadd = pro_vadd;
   p.pro_lse_k = pro_lse_k;
+  p.pro_lse_c = pro_lse_c;
+  p.pro_row_k = pro_row_k;
+  p.pro_row_c = pro_row_c;
+  p.col_bias = col_bias_ptr;
+  p.cb_ld = cb_ld;
   p.q = (const __nv_bfloat16 *)q->data;
   p.q_stride_t = q->stride[0];
   p.q_stride_h = q->stride[1];
@@ -706,14 +850,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   L.fp8 = fp8;
   L.int8 = kv_dt == FA_I8;
   L.q8 = q8;
-  {
-    // Test knob: FA_GB300_PREFILL_VARIANT=1 forces the 10-warp two-pass softmax.
-    const char *v = getenv("FA_GB300_PREFILL_VARIANT");
-    L.variant = (v && v[0] == '1') ? 1 : 0;
-  }
-  // The plain-softmax kernels fold a positive scale into the exponent; any
-  // other scale takes the general score path (ALiBi with slope 0).
-  if (mod == 0 && !(softmax_scale > 0.f)) {
+  L.variant = prefill_variant();
+  // The plain-softmax kernels fold a positive scale into the exponent and
+  // have no per-key term; any other scale, and a Q add, take the general
+  // score path (ALiBi with slope 0).
+  if (mod == 0 && (!(softmax_scale > 0.f) || col_bias_ptr)) {
     L.mod = 1;
     p.alibi_log2 = 0.f;
   } else {
@@ -730,6 +871,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   P.kind = 2;
   P.dk = (int)Dk;
   P.fp8 = fp8;
+  P.has_cb = col_bias_ptr != nullptr;
+  P.cb = cbp;
   P.pl = L;
   return plan ? FA_OK : run_prefill(L, P, s);
 }

@@ -63,8 +63,13 @@ struct DecodeParams {
   int32_t gather;                     // pages of < 16 keys: K/V rows by cp.async (fa_gather.cuh)
   KvGather gk, gv;
   // folded prologue: partial or final out = pro_vmul * o + pro_vadd on rows
-  // that see keys; LSE += pro_lse_k * sum_d q[d]
-  float pro_vmul, pro_vadd, pro_lse_k;
+  // that see keys; the row term pro_lse_k * sum_d q[d] + pro_lse_c is added
+  // to the LSE, or under the soft-cap enters the capped score as
+  // pro_row_k * sum_d q[d] + pro_row_c (2u*log2(e) units); col_bias holds the
+  // per-key term of a Q add, [B][Hkv][cb_ld] in the score's units, or null
+  float pro_vmul, pro_vadd, pro_lse_k, pro_lse_c, pro_row_k, pro_row_c;
+  const float *col_bias;
+  int64_t cb_ld;
   // score mods (0 none, 1 ALiBi, 2 soft-cap) and 128 x 128 block masks, as
   // in the prefill kernels
   int32_t mod;
@@ -435,13 +440,31 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       if (qb >= p.n_qblk || kb >= p.n_kblk) return false;
       return p.block_mask[((int64_t)(b * p.hq + h) * p.n_qblk + qb) * p.n_kblk + kb] != 0;
     };
-    // one modified score in log2 units from the raw product x of row (ip, .)
-    auto mod_score = [&](float x, int ip, int j) -> float {
+    // Prologue terms: under the soft-cap, each row's term (pro_row_k *
+    // sum_d q + pro_row_c) enters the capped score; a Q add's per-key term
+    // comes from col_bias (already in the score's units).
+    float rt0 = 0.f, rt1 = 0.f;
+    if (p.mod == 2 && (p.pro_row_k != 0.f || p.pro_row_c != 0.f)) {
+      auto row_sum = [&](int r) -> float {
+        if (r >= rows || p.pro_row_k == 0.f) return 0.f;
+        const __nv_bfloat16 *qrow =
+            p.q + ((int64_t)qa + r / p.group) * p.q_stride_t + (int64_t)(hk * p.group + r % p.group) * p.q_stride_h;
+        float qs = 0.f;
+        for (int d = 0; d < D; ++d) qs += __bfloat162float(qrow[d]);
+        return qs;
+      };
+      rt0 = fmaf(p.pro_row_k, row_sum(r0), p.pro_row_c);
+      rt1 = fmaf(p.pro_row_k, row_sum(r1), p.pro_row_c);
+    }
+    const float *cb_row = p.col_bias ? p.col_bias + ((int64_t)b * p.hkv + hk) * p.cb_ld : nullptr;
+    // one modified score in log2 units from the raw product x of row (ip, .),
+    // with the row's and the key's prologue terms rt and cb
+    auto mod_score = [&](float x, int ip, int j, float rt, float cb) -> float {
       if (p.mod == 2) {
         float r;
-        return softcap_log2_score(ex2(x * c2u), p.softcap_log2, r);
+        return softcap_log2_score(ex2(fmaf(x, c2u, rt + cb)), p.softcap_log2, r);
       }
-      return fmaf(x, p.scale_log2, -p.alibi_log2 * fabsf((float)(ip - j)));
+      return fmaf(x, p.scale_log2, cb - p.alibi_log2 * fabsf((float)(ip - j)));
     };
     uint8_t *conv = smem + Cfg::kOffConv + warp * Cfg::kConvWarpBytes;   // byte caches only
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -547,8 +570,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             s[n][e] = ok0 ? s[n][e] * kf * sc0 : -INFINITY;
             s[n][2 + e] = ok1 ? s[n][2 + e] * kf * sc1 : -INFINITY;
           } else {
-            s[n][e] = ok0 ? mod_score(s[n][e] * kf * qf0, ip0, j) : -INFINITY;
-            s[n][2 + e] = ok1 ? mod_score(s[n][2 + e] * kf * qf1, ip1, j) : -INFINITY;
+            const float cb = (cb_row && in && j < p.cb_ld) ? cb_row[j] : 0.f;
+            s[n][e] = ok0 ? mod_score(s[n][e] * kf * qf0, ip0, j, rt0, cb) : -INFINITY;
+            s[n][2 + e] = ok1 ? mod_score(s[n][2 + e] * kf * qf1, ip1, j, rt1, cb) : -INFINITY;
           }
           mx0 = fmaxf(mx0, s[n][e]);
           mx1 = fmaxf(mx1, s[n][2 + e]);
@@ -670,7 +694,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const int tq = row / p.group, h = hk * p.group + row % p.group;
         const int64_t t = (int64_t)qa + tq;
         float lse_v = has ? (M + __log2f(L)) * kLn2 : -INFINITY;
-        if (has && p.pro_lse_k != 0.f) {   // prologue's K shift, carried by the LSE
+        if (has) lse_v += p.pro_lse_c;     // the prologue's row term, carried by the LSE
+        if (has && p.pro_lse_k != 0.f) {
           const __nv_bfloat16 *qrow = p.q + t * p.q_stride_t + (int64_t)h * p.q_stride_h;
           float qs = 0.f;
           for (int d = 0; d < D; ++d) qs += __bfloat162float(qrow[d]);

@@ -40,6 +40,26 @@ struct BwdLaunch {
   cudaStream_t stream;
 };
 
+// The per-key score term of a Q add (fa_prologue.cu): col_bias[b][hk][j] =
+// factor * k_scale * sum_d k_j[d] for j < Sk_b, 0 for Sk_b <= j < ld.
+struct ColBiasParams {
+  const uint8_t *k;             // cache base
+  int kv;                       // 0 bf16, 1 e4m3, 2 int8
+  int64_t s_page, s_slot, s_head;   // byte strides: page (packed: token row), slot, kv head
+  const int32_t *block_table;   // [B, bt_stride] or null (packed)
+  int64_t bt_stride, max_pages; // block-table row stride and entries per row
+  int32_t page_size, page_shift;
+  int64_t n_pages;              // pages in the pool (packed: rows of the cache)
+  const int32_t *cu_k;
+  const float *k_scale;         // byte caches: per (token, kv head)
+  int32_t dk, hkv, num_seqs;
+  int64_t ld;
+  float factor;
+  float *out;
+  int *err;
+};
+cudaError_t launch_col_bias(const ColBiasParams &p, cudaStream_t stream);
+
 cudaError_t launch_bwd(int d, const BwdLaunch &L);
 cudaError_t launch_prefill_64_64(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128(const PrefillLaunch &L);

@@ -68,6 +68,10 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tens
     return fa::set_host_error(FA_ERR_INVALID_ARG, "launch, q, k_cache and v_cache are required");
   if (q->ndim != 3 || k_cache->ndim < 3 || v_cache->ndim != k_cache->ndim)
     return fa::set_host_error(FA_ERR_INVALID_ARG, "q must be rank 3 and k/v caches rank 3 or 4");
+  // Sizes come from q itself, so that every request too large for the static
+  // scratch is refused here with that reason.
+  if (q->shape[0] != launch->total_q)
+    return fa::set_host_error(FA_ERR_INVALID_ARG, "q.shape[0] differs from launch->total_q");
   const int32_t hq = (int32_t)q->shape[1];
   const int32_t hkv = (int32_t)k_cache->shape[k_cache->ndim - 2];
   const int32_t dv = (int32_t)v_cache->shape[v_cache->ndim - 1];
@@ -78,7 +82,9 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tens
   if (splits <= 1)
     return fa::set_host_error(FA_ERR_UNSUPPORTED,
                               "the allocation-free entry runs the split-KV decode only (needs 2 or more splits)");
-  const size_t need = fa_fwd_workspace_bytes(launch->num_seqs, launch->total_q, hq, dv, splits);
+  fa_launch_t L = *launch;
+  L.num_splits = splits;
+  const size_t need = fa_fwd_workspace_bytes(&L, hq, hkv, dv, prologue);
   if (need > (size_t)FA_NOALLOC_SCRATCH_BYTES) {
     char m[200];
     snprintf(m, sizeof m, "split-KV scratch of %zu bytes exceeds the static %zu-byte scratch; use fewer splits, fewer rows or fa_fwd_varlen",
@@ -88,8 +94,6 @@ extern "C" fa_status_t fa_fwd_varlen_noalloc(const fa_tensor_t *q, const fa_tens
   void *scratch = nullptr;
   fa_status_t st = scratch_address(&scratch);
   if (st != FA_OK) return st;
-  fa_launch_t L = *launch;
-  L.num_splits = splits;
   L.workspace = scratch;
   L.workspace_bytes = (size_t)FA_NOALLOC_SCRATCH_BYTES;
   return fa_fwd_varlen(q, k_cache, v_cache, block_table, cu_seqlens_q, cu_seqlens_k, k_scale, v_scale, out, lse,

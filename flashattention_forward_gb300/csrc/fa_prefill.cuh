@@ -50,11 +50,20 @@ struct PrefillParams {
   int32_t gather;       // pages of < 16 keys: K/V rows by cp.async (fa_gather.cuh), not TMA boxes
   KvGather gk, gv;      // the caches' byte geometry for the gather
   // folded prologue: out = pro_vmul * o + pro_vadd on rows that see keys;
-  // LSE += pro_lse_k * sum_d q[d] (bf16 q read back only when pro_lse_k != 0)
-  float pro_vmul, pro_vadd, pro_lse_k;
+  // the row term of the score, pro_lse_k * sum_d q[d] + pro_lse_c, is added
+  // to the LSE (bf16 q read back only when pro_lse_k != 0); under the
+  // soft-cap it enters the capped score instead, as pro_row_k * sum_d q[d] +
+  // pro_row_c in 2u*log2(e) units
+  float pro_vmul, pro_vadd, pro_lse_k, pro_lse_c, pro_row_k, pro_row_c;
   const __nv_bfloat16 *q;
   int64_t q_stride_t, q_stride_h;   // elements
+  // the prologue's per-key score term (a Q add), [B][Hkv][cb_ld] fp32 in the
+  // units of the kernel's score (log2, or 2u*log2(e) under the soft-cap);
+  // null when there is none
+  const float *col_bias;
+  int64_t cb_ld;
 };
+
 
 // sum_d q[d] of one bf16 query row (16-byte loads), for the prologue's LSE term.
 template <int D>
@@ -68,6 +77,14 @@ __device__ __forceinline__ float q_row_sum(const __nv_bfloat16 *row) {
     for (int e = 0; e < 4; ++e) acc += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
   }
   return acc;
+}
+
+// Row term of the prologue inside the soft-cap argument (0 without one).
+template <int D>
+__device__ __forceinline__ float softcap_row_term(const PrefillParams &p, int64_t t, int h) {
+  float rb = p.pro_row_c;
+  if (p.pro_row_k != 0.f) rb += p.pro_row_k * q_row_sum<D>(p.q + t * p.q_stride_t + (int64_t)h * p.q_stride_h);
+  return rb;
 }
 
 // Block order: for each sequence, for each group of `head_group` heads, query

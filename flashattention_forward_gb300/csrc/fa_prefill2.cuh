@@ -434,6 +434,12 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     const uint32_t colS = X ? 128u : 0u, colO = 256u + (X ? 128u : 0u);
     const int i = hx.q0 + r;
     const int ip = i + pi.sk - pi.sq;
+    // Prologue terms (see PrefillParams): the row term enters the scores
+    // under the soft-cap only; the per-key term of a Q add, when present, is
+    // read per 32-key chunk (all lanes read the same addresses; the address
+    // is formed from the parameter block there, so nothing stays live).
+    const float row_term =
+        (MOD == 2 && i < pi.sq) ? softcap_row_term<DK>(p, (int64_t)pi.q_row0 + X * kBlockM + r, pi.h) : 0.f;
     float m_ref = -INFINITY, l = 0.f;
     int cnt = 0;
     bool ok = true;
@@ -479,14 +485,30 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         if (!fast) {
           const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
           const float c2u = 2.f * kLog2e * p.softcap_arg;   // soft-cap: raw score -> 2u log2(e)
+          // Scaled score (log2 units; soft-cap: its argument 2u log2(e)) plus
+          // the prologue's row term (soft-cap only) and per-key term.
+          const float lin = MOD == 2 ? c2u : p.scale_log2;
+          if (p.col_bias && jc + 32 <= p.cb_ld) {   // no term is read past cb_ld (the pre-pass flags such keys)
+            const float4 *c4 =
+                reinterpret_cast<const float4 *>(p.col_bias + ((int64_t)pi.b * p.hkv + pi.hk) * p.cb_ld + jc);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 c = c4[e >> 2];
+              v[e] = fmaf(v[e], lin, c.x + row_term);
+              v[e + 1] = fmaf(v[e + 1], lin, c.y + row_term);
+              v[e + 2] = fmaf(v[e + 2], lin, c.z + row_term);
+              v[e + 3] = fmaf(v[e + 3], lin, c.w + row_term);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = fmaf(v[e], lin, row_term);
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            float x;
+            float x = v[e];
             if constexpr (MOD == 2) {
               float r;
-              x = softcap_log2_score(ex2(v[e] * c2u), p.softcap_log2, r);
-            } else {
-              x = v[e] * p.scale_log2;
+              x = softcap_log2_score(ex2(x), p.softcap_log2, r);
             }
             if constexpr (MOD == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
             v[e] = x;
@@ -730,7 +752,8 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
           }
           if (row_ok && p.lse) {
             float lv = has ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-            // prologue's K shift: the softmax cancels it, the LSE carries it
+            // the prologue's row term: the softmax cancels it, the LSE carries it
+            if (has) lv += p.pro_lse_c;
             if (has && p.pro_lse_k != 0.f)
               lv += p.pro_lse_k * q_row_sum<DK>(p.q + t * p.q_stride_t + (int64_t)pi.h * p.q_stride_h);
             p.lse[(int64_t)pi.h * p.total_q + t] = lv;

@@ -90,21 +90,41 @@ typedef struct {
     float softcap;
 } fa_score_mod_t;
 
-/* Prologue (fkl_python PR #7, prologue commit: op chains fused onto the
- * Q/K/V reads, values passed at run time): each element x of Q, K and V is
- * read as mul * x + add -- a chain of Mul/Add/Sub/Div by scalars composes to
- * one such map per tensor.  The kernels fold the maps instead of rewriting
- * the operands, which is exact in real arithmetic:
- *   q_mul * k_mul scales the scores (it multiplies softmax_scale);
- *   k_add adds softmax_scale * q_mul * k_add * sum_d q_i[d] to every score
- *     of row i: the softmax cancels it and the LSE carries it;
- *   v_mul, v_add act on the output (the softmax weights sum to 1).
- * Limits (FA_ERR_UNSUPPORTED): q_add must be 0 (it would add a per-key term
- * q_add * k_mul * sum_d k_j[d]); k_add must be 0 with the soft-cap (not
- * shift-invariant) and with e4m3 q.  Rows that see no key keep out = 0 and
- * LSE = -inf.  NULL, or mul = 1 and add = 0 everywhere, is no prologue. */
+/* Prologue (fkl_python PR #7, prologue-fusion commit: op chains fused onto
+ * the Q/K/V reads, values passed at run time).  Each tensor has a chain of
+ * up to FA_PROLOGUE_MAX_OPS scalar ops, applied in order to every element as
+ * it is read: FA_OP_MUL (x * value), FA_OP_ADD (x + value), FA_OP_SUB
+ * (x - value), FA_OP_DIV (x / value).  n_q, n_k, n_v give the chain lengths
+ * (0 = no op on that tensor).
+ *
+ * The library composes each chain into one map x -> a * x + b (in double
+ * precision, on the host) and folds the maps instead of rewriting the
+ * operands, which is exact in real arithmetic.  With q' = a_q q + b_q and
+ * k' = a_k k + b_k the score scale * <q'_i, k'_j> is
+ *   scale a_q a_k <q_i, k_j>                 (the scale is multiplied)
+ *   + scale (a_q b_k sum_d q_i[d] + b_q b_k Dk)   (one term per query row)
+ *   + scale b_q a_k sum_d k_j[d]             (one term per key),
+ * and with v' = a_v v + b_v the output is a_v out + b_v (softmax weights sum
+ * to 1).  The row term cancels in the softmax and is added to the LSE, or,
+ * under the soft-cap (not shift-invariant), enters the capped score.  The key
+ * term (a Q add) is computed by a pre-pass over the keys into the caller's
+ * workspace (fa_fwd_workspace_bytes() includes it) and added to each score.
+ * Rows that see no key keep out = 0 and LSE = -inf.
+ * Limits: FA_ERR_INVALID_ARG for an unknown op, a chain longer than
+ * FA_PROLOGUE_MAX_OPS, a value that is not finite or a division by 0;
+ * FA_ERR_UNSUPPORTED for b_q or b_k != 0 with e4m3 q.  NULL, or empty chains,
+ * is no prologue. */
+enum { FA_OP_MUL = 1, FA_OP_ADD = 2, FA_OP_SUB = 3, FA_OP_DIV = 4 };
+#define FA_PROLOGUE_MAX_OPS 8
 typedef struct {
-    float q_mul, q_add, k_mul, k_add, v_mul, v_add;
+    int32_t op;          /* FA_OP_* */
+    float value;
+} fa_prologue_op_t;
+typedef struct {
+    int32_t n_q, n_k, n_v;
+    fa_prologue_op_t q[FA_PROLOGUE_MAX_OPS];
+    fa_prologue_op_t k[FA_PROLOGUE_MAX_OPS];
+    fa_prologue_op_t v[FA_PROLOGUE_MAX_OPS];
 } fa_prologue_t;
 
 /* 128x128 block-sparsity mask, uint8 [num_seqs * Hq][n_qblk][n_kblk],
@@ -118,7 +138,8 @@ typedef struct {
 
 /* Host-side scalars, so that no length is read back from the device.
  * num_splits: 0 = single pass; > 0 = split-KV over that many key ranges
- * followed by the combine (needs `workspace` of fa_fwd_workspace_bytes()). */
+ * followed by the combine.  workspace: fa_fwd_workspace_bytes() bytes, needed
+ * by split-KV with 2 or more splits and by a prologue with a Q add. */
 typedef struct {
     int32_t num_seqs;
     int32_t max_seqlen_q;
@@ -171,10 +192,6 @@ typedef struct {
  *  launch       host scalars (required).
  *  stream       cudaStream_t.
  *
- * Environment: FA_GB300_PREFILL_VARIANT=1 makes the bf16 prefill use its
- * 10-warp two-pass softmax instead of the register-rebalanced one-pass one
- * (a test and diagnosis knob; results agree within rounding).
- *
  * e4m3 caches: K and V become f16 operands RN(e4m3 * scale) inside the
  * kernel, so |e4m3 value * scale| must stay below 65504 (scales below 146).
  *
@@ -219,12 +236,16 @@ FA_API fa_status_t fa_fwd_plan_launch(fa_fwd_plan_t plan, void *stream);
 FA_API void fa_fwd_plan_destroy(fa_fwd_plan_t plan);
 
 /*
- * Workspace size in bytes for split-KV with `num_splits` key ranges: partial
- * outputs fp32 [num_splits, T_q, Hq, Dv] and partial LSEs fp32
- * [num_splits, Hq, T_q], each 256-byte aligned.  0 when num_splits <= 0.
+ * Workspace size in bytes of a forward call with these host scalars, head
+ * counts and prologue (NULL = none): for split-KV with launch->num_splits >= 2,
+ * partial outputs fp32 [num_splits, T_q, Hq, Dv] and partial LSEs fp32
+ * [num_splits, Hq, T_q]; for a prologue whose Q chain adds a constant (see
+ * fa_prologue_t), the per-key score terms fp32 [num_seqs, Hkv,
+ * ceil(max_seqlen_k / 128) * 128].  Each part is 256-byte aligned.  0 when
+ * neither applies or launch is NULL.
  */
-FA_API size_t fa_fwd_workspace_bytes(int32_t num_seqs, int64_t total_q, int32_t hq, int32_t dv,
-                              int32_t num_splits);
+FA_API size_t fa_fwd_workspace_bytes(const fa_launch_t *launch, int32_t hq, int32_t hkv, int32_t dv,
+                              const fa_prologue_t *prologue);
 
 /*
  * Recommended split count for a problem (0 = single pass).  Split-KV applies
@@ -304,13 +325,19 @@ FA_API size_t fa_bwd_workspace_bytes(int64_t total_q, int32_t hq);
  * request paths that must not call cudaMalloc because it may synchronise the
  * device or fail under memory pressure.  Instead of launch->workspace, the
  * per-split partials go to a static device array of FA_NOALLOC_SCRATCH_BYTES
- * owned by the library; every GPU that loads the library holds that array
- * until the process exits.  Nothing is allocated by this call.
+ * owned by the library.  The array is part of the library's device code:
+ * CUDA reserves it on a device when it loads the library's code there, which
+ * under lazy module loading (the default since CUDA 12) happens at the first
+ * use on that device -- possibly this entry's first call -- and it stays
+ * reserved until the process exits.  Callers with no spare device memory
+ * should therefore make one call per device at start-up.  The call itself
+ * asks for no memory: no cudaMalloc, no allocating library routine.
  *
  * Arguments and layouts are those of fa_fwd_varlen; launch->workspace and
  * launch->workspace_bytes are ignored.  launch->num_splits <= 0 picks
  * fa_fwd_default_splits(); the problem must be a split-KV decode shape with
- * at least 2 splits, and fa_fwd_workspace_bytes() for it must not exceed
+ * at least 2 splits, and fa_fwd_workspace_bytes() for it (with q.shape[0]
+ * rows, which must equal launch->total_q) must not exceed
  * FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_UNSUPPORTED is returned with nothing
  * enqueued.
  *

@@ -42,6 +42,30 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+_MAX_OPS = 8
+_OP_CODES = {"mul": 1, "add": 2, "sub": 3, "div": 4}
+
+
+class _Chain(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("op", ctypes.c_int32 * _MAX_OPS), ("c", ctypes.c_double * _MAX_OPS)]
+
+
+def _chain(ops) -> _Chain:
+    """One tensor's prologue op chain, e.g. [("mul", 2.0), ("add", 1.0)], as
+    the C struct; the oracle applies the ops one after the other."""
+    ch = _Chain()
+    ops = list(ops or ())
+    if len(ops) > _MAX_OPS:
+        raise ValueError(f"at most {_MAX_OPS} prologue ops per tensor")
+    ch.n = len(ops)
+    for i, (name, c) in enumerate(ops):
+        if name not in _OP_CODES:
+            raise ValueError(f"prologue op {name!r}: mul, add, sub or div")
+        ch.op[i] = _OP_CODES[name]
+        ch.c[i] = float(c)
+    return ch
+
+
 class _Problem(ctypes.Structure):
     _fields_ = [
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
@@ -59,8 +83,7 @@ class _Problem(ctypes.Structure):
         ("blk_q", ctypes.c_int32), ("blk_k", ctypes.c_int32),
         ("kv_lo", ctypes.c_int64), ("kv_hi", ctypes.c_int64),
         ("q_dtype", ctypes.c_int32),
-        ("q_mul", ctypes.c_double), ("q_add", ctypes.c_double), ("k_mul", ctypes.c_double),
-        ("k_add", ctypes.c_double), ("v_mul", ctypes.c_double), ("v_add", ctypes.c_double),
+        ("pro_q", _Chain), ("pro_k", _Chain), ("pro_v", _Chain),
     ]
 
 
@@ -143,8 +166,8 @@ def _problem(p, keep, kv_range=None, q_f64=None, k_f64=None, v_f64=None):
         blk_q=128, blk_k=128,
         kv_lo=(kv_range[0] if kv_range else 0), kv_hi=(kv_range[1] if kv_range else -1),
         q_dtype=qd)
-    pro = getattr(p, "prologue", None) or (1.0, 0.0, 1.0, 0.0, 1.0, 0.0)
-    prob.q_mul, prob.q_add, prob.k_mul, prob.k_add, prob.v_mul, prob.v_add = (float(x) for x in pro)
+    pro = getattr(p, "prologue", None) or {}
+    prob.pro_q, prob.pro_k, prob.pro_v = _chain(pro.get("q")), _chain(pro.get("k")), _chain(pro.get("v"))
     return prob, c
 
 

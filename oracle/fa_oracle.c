@@ -38,12 +38,14 @@
  *    verified": bottom-right causal mask, cross_seqlen=True);
  *  - ALiBi, SoftCap, SlidingWindow and 128x128 block masks: fkl_python PR #7,
  *    flex attention commit;
- *  - prologue: every element of Q, K and V taken as mul * x + add as it is
- *    read (an op chain of Mul/Add by scalars, composed), before anything
- *    else: fkl_python PR #7, prologue-fusion commit (op chains fused onto the
- *    Q/K/V reads, values at run time).
+ *  - prologue: every element of Q, K and V is put through its tensor's op
+ *    chain (Mul, Add, Sub or Div by a scalar, one op after the other, in the
+ *    order given) as it is read, before anything else: fkl_python PR #7,
+ *    prologue-fusion commit (op chains fused onto the Q/K/V reads, values at
+ *    run time).  The ops are applied literally, one by one; nothing is
+ *    composed here.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings taken where the pages are silent:
  * i' = i + Sk - Sq; window W>0 keeps 0 <= i'-j < W when causal, |i'-j| < W
  * otherwise; ALiBi bias -slope*|i'-j| for every head; soft-cap acts on the
  * scaled score before ALiBi; block-mask index (b*Hq + h, i/128, j/128) with
@@ -62,6 +64,15 @@
 enum { KV_BF16 = 0, KV_E4M3 = 1, KV_F64 = 2, KV_I8 = 3 };
 enum { MOD_NONE = 0, MOD_ALIBI = 1, MOD_SOFTCAP = 2 };
 
+/* One prologue op chain: x -> op_{n-1}(... op_1(op_0(x, c_0), c_1) ..., c_{n-1}). */
+enum { ORACLE_OP_MUL = 1, ORACLE_OP_ADD = 2, ORACLE_OP_SUB = 3, ORACLE_OP_DIV = 4 };
+#define ORACLE_MAX_OPS 8
+typedef struct {
+    int32_t n;
+    int32_t op[ORACLE_MAX_OPS];
+    double c[ORACLE_MAX_OPS];
+} fa_oracle_chain;
+
 typedef struct {
     const void *q;                /* [T_q][Hq][Dk]: bf16 bits, or e4m3 bytes (q_dtype) */
     const void *k, *v;            /* packed [T_k][Hkv][D] or paged [N_pg][P_s][Hkv][D] */
@@ -79,7 +90,7 @@ typedef struct {
     int32_t n_qblk, n_kblk, blk_q, blk_k;
     int64_t kv_lo, kv_hi;         /* restrict keys to [kv_lo, kv_hi) when kv_hi >= 0 */
     int32_t q_dtype;              /* Q_BF16 | Q_E4M3 (a per-tensor Q scale is folded into softmax_scale) | Q_F64 */
-    double q_mul, q_add, k_mul, k_add, v_mul, v_add;   /* prologue maps (1, 0 = none) */
+    fa_oracle_chain pro_q, pro_k, pro_v;   /* prologue op chains (n = 0: none) */
 } fa_oracle_problem;
 
 enum { Q_BF16 = 0, Q_E4M3 = 1, Q_F64 = 2 };
@@ -108,9 +119,34 @@ double fa_oracle_e4m3_decode(uint8_t x) {
     return s ? -mag : mag;
 }
 
+/* The op chain applied to one element, op after op. */
+static double apply_chain(const fa_oracle_chain *ch, double x) {
+    for (int i = 0; i < ch->n; i++) {
+        const double c = ch->c[i];
+        switch (ch->op[i]) {
+            case ORACLE_OP_MUL: x = x * c; break;
+            case ORACLE_OP_ADD: x = x + c; break;
+            case ORACLE_OP_SUB: x = x - c; break;
+            case ORACLE_OP_DIV: x = x / c; break;
+            default: x = NAN; break;
+        }
+    }
+    return x;
+}
+
+static int chain_is_empty(const fa_oracle_chain *ch) { return ch->n == 0; }
+
+static int chain_valid(const fa_oracle_chain *ch) {
+    if (ch->n < 0 || ch->n > ORACLE_MAX_OPS) return 0;
+    for (int i = 0; i < ch->n; i++)
+        if (ch->op[i] < ORACLE_OP_MUL || ch->op[i] > ORACLE_OP_DIV) return 0;
+    return 1;
+}
+
 /* Row j of the sequence's keys (or values) for kv head hk, widened to double
- * and taken through the tensor's prologue map x -> mul * x + add. */
-static void fetch_row(const fa_oracle_problem *p, const void *base, const float *scale, double mul, double add,
+ * (dequantised with the token's scale for byte caches) and put through the
+ * tensor's prologue op chain. */
+static void fetch_row(const fa_oracle_problem *p, const void *base, const float *scale, const fa_oracle_chain *ch,
                       int b, int64_t j, int hk, int d, double *dst) {
     int64_t tok;       /* flat token index in the [*, Hkv] view of the pool */
     if (p->block_table) {
@@ -128,12 +164,12 @@ static void fetch_row(const fa_oracle_problem *p, const void *base, const float 
         else if (p->kv_dtype == KV_E4M3) val = fa_oracle_e4m3_decode(((const uint8_t *)base)[off + x]);
         else if (p->kv_dtype == KV_I8) val = fa_oracle_i8_decode(((const uint8_t *)base)[off + x]);
         else val = ((const double *)base)[off + x];
-        dst[x] = mul * (val * sc) + add;
+        dst[x] = apply_chain(ch, val * sc);
     }
 }
 
-/* Query row (token t, head h) widened to double and taken through q's
- * prologue map. */
+/* Query row (token t, head h) widened to double and put through q's
+ * prologue op chain. */
 static void fetch_q(const fa_oracle_problem *p, int64_t t, int h, double *qrow) {
     for (int x = 0; x < p->dk; x++) {
         const int64_t at = (t * p->hq + h) * (int64_t)p->dk + x;
@@ -141,7 +177,7 @@ static void fetch_q(const fa_oracle_problem *p, int64_t t, int h, double *qrow) 
         if (p->q_dtype == Q_E4M3) val = fa_oracle_e4m3_decode(((const uint8_t *)p->q)[at]);
         else if (p->q_dtype == Q_F64) val = ((const double *)p->q)[at];
         else val = fa_oracle_bf16_decode(((const uint16_t *)p->q)[at]);
-        qrow[x] = p->q_mul * val + p->q_add;
+        qrow[x] = apply_chain(&p->pro_q, val);
     }
 }
 
@@ -187,7 +223,7 @@ static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, d
     for (int64_t j = 0; j < sk; j++) {
         ok[j] = (unsigned char)allowed(p, b, h, i, j, sq, sk);
         if (!ok[j]) continue;
-        fetch_row(p, p->k, p->k_scale, p->k_mul, p->k_add, b, j, hk, p->dk, krow);
+        fetch_row(p, p->k, p->k_scale, &p->pro_k, b, j, hk, p->dk, krow);
         double dot = 0.0;
         for (int x = 0; x < p->dk; x++) dot += qrow[x] * krow[x];
         double sj = p->softmax_scale * dot;
@@ -207,7 +243,7 @@ static void one_row(const fa_oracle_problem *p, int64_t t, int h, double *out, d
         if (!ok[j]) continue;
         double w = exp(s[j] - m);
         l += w;
-        fetch_row(p, p->v, p->v_scale, p->v_mul, p->v_add, b, j, hk, p->dv, vrow);
+        fetch_row(p, p->v, p->v_scale, &p->pro_v, b, j, hk, p->dv, vrow);
         for (int x = 0; x < p->dv; x++) out[x] += w * vrow[x];
     }
     for (int x = 0; x < p->dv; x++) out[x] /= l;
@@ -252,6 +288,7 @@ int fa_oracle_fwd(const fa_oracle_problem *p, const int64_t *units, int64_t n_un
                   double *out, double *lse, int nthreads) {
     if (!p || p->hq <= 0 || p->hkv <= 0 || p->hq % p->hkv || p->num_seqs < 0) return -1;
     if (p->block_table && p->page_size <= 0) return -1;
+    if (!chain_valid(&p->pro_q) || !chain_valid(&p->pro_k) || !chain_valid(&p->pro_v)) return -1;
     if (!units) n_units = (int64_t)p->cu_q[p->num_seqs] * p->hq;
     int64_t max_sk = 0;
     for (int b = 0; b < p->num_seqs; b++) {
@@ -359,7 +396,7 @@ static void *bwd_worker(void *argp) {
                 for (int64_t j = 0; j < sk; j++) {
                     ok[j] = (unsigned char)allowed(p, b, h, i, j, sq, sk);
                     if (!ok[j]) continue;
-                    fetch_row(p, p->k, p->k_scale, p->k_mul, p->k_add, b, j, hk, p->dk, krow);
+                    fetch_row(p, p->k, p->k_scale, &p->pro_k, b, j, hk, p->dk, krow);
                     double dot = 0.0;
                     for (int x = 0; x < p->dk; x++) dot += qrow[x] * krow[x];
                     double sj = p->softmax_scale * dot;
@@ -378,7 +415,7 @@ static void *bwd_worker(void *argp) {
                 double dsum = 0.0;
                 for (int64_t j = 0; j < sk; j++) {
                     if (!ok[j]) continue;
-                    fetch_row(p, p->v, p->v_scale, p->v_mul, p->v_add, b, j, hk, p->dv, vrow);
+                    fetch_row(p, p->v, p->v_scale, &p->pro_v, b, j, hk, p->dv, vrow);
                     double d = 0.0;
                     for (int x = 0; x < p->dv; x++) d += dorow[x] * vrow[x];
                     dp[j] = d;
@@ -396,7 +433,7 @@ static void *bwd_worker(void *argp) {
                         const double th = tanh(u[j] / p->softcap);
                         du *= 1.0 - th * th;
                     }
-                    fetch_row(p, p->k, p->k_scale, p->k_mul, p->k_add, b, j, hk, p->dk, krow);
+                    fetch_row(p, p->k, p->k_scale, &p->pro_k, b, j, hk, p->dk, krow);
                     double *dkrow = a->dk + ((p->cu_k[b] + j) * p->hkv + hk) * (int64_t)p->dk;
                     for (int x = 0; x < p->dk; x++) {
                         dqrow[x] += p->softmax_scale * du * krow[x];
@@ -415,9 +452,7 @@ int fa_oracle_bwd(const fa_oracle_problem *p, const double *dout, double *dq, do
     if (!p || p->hq <= 0 || p->hkv <= 0 || p->hq % p->hkv || p->num_seqs < 0) return -1;
     if (p->block_table || (p->kv_dtype != KV_BF16 && p->kv_dtype != KV_F64)) return -1;
     /* gradients with respect to the stored tensors: no prologue */
-    if (p->q_mul != 1.0 || p->q_add != 0.0 || p->k_mul != 1.0 || p->k_add != 0.0 || p->v_mul != 1.0 ||
-        p->v_add != 0.0)
-        return -1;
+    if (!chain_is_empty(&p->pro_q) || !chain_is_empty(&p->pro_k) || !chain_is_empty(&p->pro_v)) return -1;
     const int64_t tq = p->cu_q[p->num_seqs], tk = p->cu_k[p->num_seqs];
     memset(dq, 0, sizeof(double) * tq * p->hq * p->dk);
     memset(dk, 0, sizeof(double) * tk * p->hkv * p->dk);

@@ -51,7 +51,7 @@ def run_gpu(p, t=None, num_splits=0, out=None, lse=None, stream=None, workspace=
         softmax_scale=p.softmax_scale, causal=p.causal, window=p.window,
         score_mod=p.mod_kind, alibi_slope=p.alibi_slope, softcap=p.softcap,
         block_mask=t.get("bm"), num_splits=num_splits, out=out, lse=lse, stream=stream,
-        workspace=workspace, prologue=(fa.Prologue(*p.prologue) if p.prologue is not None else None))
+        workspace=workspace, prologue=p.prologue)
     return o, l
 
 
@@ -80,16 +80,21 @@ def compare(out_g, lse_g, out_o, lse_o, out_tol=OUT_TOL, lse_tol=LSE_TOL):
 
 
 def sample_units(p, n, seed=0):
-    """Seeded sample of (token, head) rows plus every row at a tile or sequence boundary."""
+    """(token, head) rows to check: every head of every row at a 128-row tile
+    boundary or a sequence end, plus ``n`` distinct seeded random rows
+    elsewhere."""
     rng = np.random.default_rng(seed)
     units = set()
     for b in range(p.num_seqs):
         q0, sq = int(p.cu_seqlens_q[b]), int(p.seqlens_q[b])
         for i in list(range(0, sq, 128)) + list(range(127, sq, 128)) + [sq - 1]:
             if 0 <= i < sq:
-                units.add((q0 + i, int(rng.integers(p.hq))))
+                for h in range(p.hq):
+                    units.add((q0 + i, h))
+    boundary = len(units)
     tq = p.total_q
-    for _ in range(n):
+    n = min(n, tq * p.hq - boundary)
+    while len(units) < boundary + n:
         units.add((int(rng.integers(tq)), int(rng.integers(p.hq))))
     return np.array(sorted(units), dtype=np.int64)
 

@@ -75,11 +75,18 @@ def test_version_and_last_error(L):
     assert isinstance(L.fa_last_error(), bytes)
 
 
+def _launch(num_seqs, total_q, num_splits, max_seqlen_k=0):
+    return fa.Launch(num_seqs=num_seqs, max_seqlen_q=1, max_seqlen_k=max_seqlen_k, num_splits=num_splits,
+                     total_q=total_q, total_k=0)
+
+
 def test_workspace_bytes_and_default_splits(L):
-    assert fa.workspace_bytes(4, 0, 8, 128, 4) == 0
-    assert fa.workspace_bytes(4, 10, 8, 128, 0) == 0
-    n = fa.workspace_bytes(64, 64, 32, 128, 16)
-    assert n >= 16 * 64 * 32 * 128 * 4 + 16 * 32 * 64 * 4 and n % 256 == 0
+    assert fa.workspace_bytes(_launch(4, 0, 4), 8, 8, 128) == 0
+    assert fa.workspace_bytes(_launch(4, 10, 0), 8, 8, 128) == 0
+    assert fa.workspace_bytes(_launch(4, 10, 1), 8, 8, 128) == 0          # one split writes out directly
+    n = fa.workspace_bytes(_launch(64, 64, 16), 32, 8, 128)
+    assert n == 16 * 64 * 32 * 128 * 4 + 16 * 32 * 64 * 4 and n % 256 == 0
+    assert L.fa_fwd_workspace_bytes(None, 8, 8, 128, None) == 0
     s = fa.default_splits(64, 1, 8192, 32, 8, 16, 64 * 4400)   # decode shape
     assert 2 <= s <= 8
     assert fa.default_splits(64, 1, 8192, 32, 8, 16, 0) >= 1      # total unknown
@@ -124,6 +131,38 @@ def _call(L, **over):
     return st, L.fa_last_error().decode()
 
 
+def _raw_prologue(n_q=0, n_v=0, q_op=1):
+    pro = fa.Prologue()
+    pro.n_q, pro.n_v = n_q, n_v
+    pro.q[0].op, pro.q[0].value = q_op, 1.0
+    return pro
+
+
+def test_workspace_bytes_counts_a_q_add(L):
+    """A Q add needs fp32 [num_seqs, Hkv, ceil(max_seqlen_k / 128) * 128] of
+    per-key terms after the split partials; a K add or a Q add on keys
+    multiplied by 0 needs nothing."""
+    lau = _launch(3, 10, 0, max_seqlen_k=300)
+    assert fa.workspace_bytes(lau, 8, 2, 128, {"k": [("add", 1.0)]}) == 0
+    assert fa.workspace_bytes(lau, 8, 2, 128, {"q": [("add", 1.0)], "k": [("mul", 0.0)]}) == 0
+    assert fa.workspace_bytes(lau, 8, 2, 128, {"q": [("add", 1.0)]}) == 3 * 2 * 384 * 4
+    lau2 = _launch(3, 10, 4, max_seqlen_k=300)
+    split = fa.workspace_bytes(lau2, 8, 2, 128)
+    assert split > 0 and split % 256 == 0
+    assert fa.workspace_bytes(lau2, 8, 2, 128, {"q": [("sub", 2.0), ("mul", 3.0)]}) == split + 3 * 2 * 384 * 4
+
+
+def test_make_prologue_only_copies_the_ops():
+    pro = fa.make_prologue({"q": [("mul", 2.0), ("add", 1.0)], "v": [("sub", 0.5), ("div", 4.0)]})
+    assert (pro.n_q, pro.n_k, pro.n_v) == (2, 0, 2)
+    assert [(pro.q[i].op, pro.q[i].value) for i in range(2)] == [(fa.FA_OP_MUL, 2.0), (fa.FA_OP_ADD, 1.0)]
+    assert [(pro.v[i].op, pro.v[i].value) for i in range(2)] == [(fa.FA_OP_SUB, 0.5), (fa.FA_OP_DIV, 4.0)]
+    with pytest.raises(ValueError):
+        fa.make_prologue({"q": [("pow", 2.0)]})
+    with pytest.raises(ValueError):
+        fa.make_prologue({"k": [("mul", 1.0)] * 9})
+
+
 @pytest.mark.parametrize("over,status,words", [
     (dict(q=_t(FAKE, fa.FA_F32, [256, 4, 64])), fa.FA_ERR_INVALID_ARG, "dtype"),
     (dict(q=_t(FAKE, fa.FA_BF16, [256, 4, 96]), k=_t(FAKE * 2, fa.FA_BF16, [256, 4, 96]),
@@ -143,10 +182,12 @@ def _call(L, **over):
     (dict(mod=fa.ScoreMod(kind=2, softcap=0.0)), fa.FA_ERR_INVALID_ARG, "softcap"),
     (dict(mod=fa.ScoreMod(kind=7)), fa.FA_ERR_INVALID_ARG, "kind"),
     (dict(bm=fa.BlockMask(data=FAKE * 9, n_qblk=1, n_kblk=1, blk_q=64, blk_k=64)), fa.FA_ERR_UNSUPPORTED, "128x128"),
-    (dict(pro=fa.Prologue(q_mul=1, q_add=0.5, k_mul=1, v_mul=1)), fa.FA_ERR_UNSUPPORTED, "q_add"),
-    (dict(pro=fa.Prologue(q_mul=1, k_mul=1, k_add=0.5, v_mul=1), mod=fa.ScoreMod(kind=2, softcap=5.0)),
-     fa.FA_ERR_UNSUPPORTED, "soft-cap"),
-    (dict(pro=fa.Prologue(q_mul=float("nan"), k_mul=1, v_mul=1)), fa.FA_ERR_INVALID_ARG, "finite"),
+    (dict(pro=fa.make_prologue({"q": [("mul", float("nan"))]})), fa.FA_ERR_INVALID_ARG, "finite"),
+    (dict(pro=fa.make_prologue({"k": [("div", 0.0)]})), fa.FA_ERR_INVALID_ARG, "divides by 0"),
+    (dict(pro=_raw_prologue(n_v=9)), fa.FA_ERR_INVALID_ARG, "ops"),
+    (dict(pro=_raw_prologue(n_q=1, q_op=7)), fa.FA_ERR_INVALID_ARG, "FA_OP_MUL"),
+    (dict(pro=fa.make_prologue({"q": [("mul", 3e38)], "k": [("mul", 3e38)]})), fa.FA_ERR_INVALID_ARG, "overflow"),
+    (dict(pro=fa.make_prologue({"q": [("add", 0.5)]})), fa.FA_ERR_INVALID_ARG, "workspace"),
     (dict(bm=fa.BlockMask(data=FAKE * 9, n_qblk=0, n_kblk=1, blk_q=128, blk_k=128)), fa.FA_ERR_INVALID_ARG, "cover"),
     (dict(launch=None), fa.FA_ERR_INVALID_ARG, "launch"),
 ])

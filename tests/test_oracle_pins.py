@@ -64,10 +64,18 @@ def brute_mask(p, b, h, sq, sk):
     return m
 
 
+def apply_ops(x, ops):
+    """A prologue op chain applied to a widened numpy array, op after op."""
+    for name, c in ops or ():
+        x = {"mul": lambda a: a * c, "add": lambda a: a + c, "sub": lambda a: a - c,
+             "div": lambda a: a / c}[name](x)
+    return x
+
+
 def sdpa_reference(p, bias_fn=None, maps=None):
     """torch fp64 SDPA per sequence (GQA by repeat_interleave) and logsumexp.
-    ``maps``: (q_mul, q_add, k_mul, k_add, v_mul, v_add) applied to the
-    widened tensors first."""
+    ``maps``: prologue op chains {"q": [...], "k": [...], "v": [...]}
+    applied to the widened tensors first."""
     if p.q_dtype == "e4m3":
         q = torch.from_numpy(p.q.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
     else:
@@ -75,7 +83,7 @@ def sdpa_reference(p, bias_fn=None, maps=None):
     k = kv_tokens_f64(p, "k")
     v = kv_tokens_f64(p, "v")
     if maps is not None:
-        q, k, v = maps[0] * q + maps[1], maps[2] * k + maps[3], maps[4] * v + maps[5]
+        q, k, v = apply_ops(q, maps.get("q")), apply_ops(k, maps.get("k")), apply_ops(v, maps.get("v"))
     g = p.hq // p.hkv
     outs = np.zeros((p.total_q, p.hq, p.dv))
     lses = np.zeros((p.hq, p.total_q))
@@ -566,10 +574,11 @@ def test_e4m3_q_scale_is_folded_into_softmax_scale():
 
 
 # ---------------------------------------------------------------- prologue ----
-# Element maps x -> mul * x + add on Q, K, V as read (fkl_python PR #7,
-# prologue-fusion commit).
+# Op chains (Mul, Add, Sub, Div by scalars) applied in order to every element
+# of Q, K and V as read (fkl_python PR #7, prologue-fusion commit).
 
-PRO = (0.75, 0.2, -1.5, 0.3, 2.0, -0.25)
+PRO = {"q": [("mul", 0.75), ("add", 0.2)], "k": [("sub", 0.3), ("mul", -1.5), ("div", 1.25)],
+       "v": [("add", -0.25), ("mul", 2.0)]}
 
 
 @pytest.mark.parametrize("causal,paged", [(False, False), (True, False), (True, True)])
@@ -582,13 +591,49 @@ def test_prologue_matches_sdpa_on_transformed_inputs(causal, paged):
     assert_close(lse, rl, 1e-12)
 
 
+def test_prologue_ops_apply_in_order():
+    """(x + 1) * 2 and x * 2 + 1 differ; x * 2 + 2 equals (x + 1) * 2."""
+    base = fi.make_problem([40, 7], [50, 30], hq=2, dk=16, seed=25, causal=True)
+    add_mul = oracle.forward(base.replace(prologue={"k": [("add", 1.0), ("mul", 2.0)]}))
+    mul_add = oracle.forward(base.replace(prologue={"k": [("mul", 2.0), ("add", 1.0)]}))
+    same = oracle.forward(base.replace(prologue={"k": [("mul", 2.0), ("add", 2.0)]}))
+    assert np.max(np.abs(add_mul[1] - mul_add[1])[np.isfinite(add_mul[1])]) > 0.1
+    assert_close(add_mul[0], same[0], 1e-12)
+    assert_close(add_mul[1], same[1], 1e-12)
+    sub_div = oracle.forward(base.replace(prologue={"v": [("sub", 0.5), ("div", 4.0)]}))
+    mul_add_v = oracle.forward(base.replace(prologue={"v": [("mul", 0.25), ("add", -0.125)]}))
+    assert_close(sub_div[0], mul_add_v[0], 1e-12)
+
+
+def test_prologue_q_shift_adds_a_per_key_term():
+    """Adding c to every element of q adds scale * c * sum_d k_j[d] to score
+    j; with one visible key per row (causal, window 1) the output is that
+    key's v exactly and the LSE is the shifted score."""
+    base = fi.make_problem([20, 9], [20, 30], hq=2, dk=16, seed=26, causal=True, window=1)
+    c = 0.6
+    out0, lse0 = oracle.forward(base)
+    out1, lse1 = oracle.forward(base.replace(prologue={"q": [("add", c)]}))
+    assert_close(out1, out0, 0.0)
+    k = kv_tokens_f64(base, "k")                                    # [T_k, Hkv, D]
+    shift = np.zeros_like(lse0)
+    for b in range(base.num_seqs):
+        q0, q1 = int(base.cu_seqlens_q[b]), int(base.cu_seqlens_q[b + 1])
+        k0, sk = int(base.cu_seqlens_k[b]), int(base.seqlens_k[b])
+        sq = q1 - q0
+        for i in range(sq):
+            j = i + sk - sq                                         # the diagonal key
+            for h in range(base.hq):
+                shift[h, q0 + i] = base.softmax_scale * c * k[k0 + j, h // (base.hq // base.hkv)].sum()
+    assert_close(lse1, lse0 + shift, 1e-11)
+
+
 def test_prologue_k_shift_moves_only_the_lse():
     """Adding c to every key element adds scale * c * sum_d q_i[d] to every
     score of row i: the softmax is unchanged and the LSE moves by that much."""
     base = fi.make_problem([50, 9], [64, 30], hq=2, dk=16, seed=22, causal=True, mod="alibi", alibi_slope=0.1)
     c = 0.7
     out0, lse0 = oracle.forward(base)
-    out1, lse1 = oracle.forward(base.replace(prologue=(1.0, 0.0, 1.0, c, 1.0, 0.0)))
+    out1, lse1 = oracle.forward(base.replace(prologue={"k": [("add", c)]}))
     q = fi.bf16_to_f32(base.q).astype(np.float64)                  # [T, H, D]
     shift = base.softmax_scale * c * q.sum(-1).T                   # [H, T]
     assert_close(out1, out0, 1e-12)
@@ -598,7 +643,7 @@ def test_prologue_k_shift_moves_only_the_lse():
 def test_prologue_v_map_acts_on_the_output():
     base = fi.make_problem([40, 5], [40, 0], hq=2, dk=16, seed=23, window=6)
     out0, lse0 = oracle.forward(base)
-    out1, lse1 = oracle.forward(base.replace(prologue=(1.0, 0.0, 1.0, 0.0, -3.0, 0.5)))
+    out1, lse1 = oracle.forward(base.replace(prologue={"v": [("mul", -3.0), ("add", 0.5)]}))
     empty = np.isneginf(lse0).T[..., None]                         # [T, H, 1]
     assert_close(out1, np.where(empty, 0.0, -3.0 * out0 + 0.5), 1e-12)
     assert_close(lse1, lse0, 0.0)
@@ -607,18 +652,29 @@ def test_prologue_v_map_acts_on_the_output():
 def test_prologue_scales_equal_a_softmax_scale():
     base = fi.make_problem([30], [45], hq=2, dk=16, seed=24, mod="softcap", softcap=3.0)
     out0, lse0 = oracle.forward(base.replace(softmax_scale=base.softmax_scale * 0.5 * 3.0))
-    out1, lse1 = oracle.forward(base.replace(prologue=(0.5, 0.0, 3.0, 0.0, 1.0, 0.0)))
+    out1, lse1 = oracle.forward(base.replace(prologue={"q": [("mul", 0.5)], "k": [("div", 1 / 3.0)]}))
     assert_close(out1, out0, 1e-12)
     assert_close(lse1, lse0, 1e-12)
 
 
-def test_make_prologue_composes_op_chains():
-    import flashattention_forward_gb300 as fa
-    pro = fa.make_prologue({"q": [("mul", 2.0), ("add", 1.0)], "k": [("add", 1.0), ("mul", 2.0)],
-                            "v": [("sub", 0.5), ("div", 4.0)]})
-    got = (pro.q_mul, pro.q_add, pro.k_mul, pro.k_add, pro.v_mul, pro.v_add)
-    assert got == (2.0, 1.0, 2.0, 2.0, 0.25, -0.125)
-    ident = fa.make_prologue({})
-    assert (ident.q_mul, ident.q_add, ident.k_mul, ident.k_add, ident.v_mul, ident.v_add) == (1, 0, 1, 0, 1, 0)
+def test_oracle_rejects_unknown_prologue_ops():
+    base = fi.make_problem([3], [3], hq=1, dk=16, seed=27)
     with pytest.raises(ValueError):
-        fa.make_prologue({"q": [("pow", 2.0)]})
+        oracle.forward(base.replace(prologue={"q": [("pow", 2.0)]}))
+    with pytest.raises(ValueError):
+        oracle.forward(base.replace(prologue={"k": [("mul", 1.0)] * 9}))
+
+
+def test_config5_runs_share_inputs_and_equal_config5():
+    """The benchmark's shared-input config-5 runs are the config5(run)
+    problems, field by field (checked at a small sequence length)."""
+    import dataclasses
+    runs = fi.config5_runs(seq=256, batch=2)
+    for run, p in zip(fi.CONFIG5_RUNS, runs):
+        ref = fi.config5(run, seq=256, batch=2)
+        for f in dataclasses.fields(fi.Problem):
+            a, b = getattr(p, f.name), getattr(ref, f.name)
+            if isinstance(a, np.ndarray) or isinstance(b, np.ndarray):
+                assert (a is None and b is None) or np.array_equal(a, b), (run, f.name)
+            else:
+                assert a == b, (run, f.name, a, b)
