@@ -853,13 +853,17 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   L.variant = prefill_variant();
   // The plain-softmax kernels fold a positive scale into the exponent and
   // have no per-key term; any other scale, and a Q add, take the general
-  // score path (ALiBi with slope 0).
+  // score path (ALiBi with slope 0).  The prologue's score terms select the
+  // kernels that carry them (mod 3: general score, 4: soft-cap).
+  // The row term enters the kernels only under the soft-cap (as pro_row_*),
+  // where it selects them too.
+  const bool terms = col_bias_ptr || pro_row_k != 0.f || pro_row_c != 0.f;
+  int kmod = mod;
   if (mod == 0 && (!(softmax_scale > 0.f) || col_bias_ptr)) {
-    L.mod = 1;
+    kmod = 1;
     p.alibi_log2 = 0.f;
-  } else {
-    L.mod = mod;
   }
+  L.mod = terms ? kmod + 2 : kmod;
   p.head_group = (int)head_group;
   p.n_hgroups = (int)n_hgroups;
   p.n_items = (int)n_blocks;

@@ -14,7 +14,8 @@ namespace fa {
 struct PrefillLaunch {
   CUtensorMap tm_q, tm_k, tm_v;
   PrefillParams p;
-  int paged, fp8, mod;
+  int paged, fp8;
+  int mod;       // 0 plain, 1 ALiBi, 2 soft-cap; 3, 4: 1, 2 with a Q add's per-key term
   int int8;      // with fp8: the byte cache holds int8 values (else e4m3)
   int q8;        // with fp8 (e4m3): Q is e4m3 and QK runs on the bytes
   int variant;   // 0: fastest available, 1: force the 10-warp two-pass softmax
@@ -69,6 +70,12 @@ cudaError_t launch_prefill_64_64_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_192_128_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128_q8(const PrefillLaunch &L);
+// Kernels with a prologue's per-key score term (PrefillLaunch::mod 3 or 4), in
+// translation units of their own: the ping-pong kernel (bf16 K/V, Dk = Dv in
+// {64, 128}) and the chunked-ring kernel (bf16 Dk 192, e4m3 and int8 caches).
+cudaError_t launch_prefill2_kt(int d, const PrefillLaunch &L);
+cudaError_t launch_prefill3_kt(int dk, bool fp8, const PrefillLaunch &L);
+cudaError_t launch_prefill3_kt_i8(int dk, const PrefillLaunch &L);
 cudaError_t launch_decode(int d, const DecodeLaunch &L);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
                            int dv, void *out, float *lse, cudaStream_t stream);

@@ -99,6 +99,11 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     fa_prefill2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using Cfg = Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>;
+  // MOD: 0 plain scores, 1 ALiBi, 2 soft-cap; 3 and 4 are 1 and 2 with the
+  // prologue's score terms (KT): a Q add's per-key term and, under the
+  // soft-cap, the row term of a K add
+  constexpr int MK = MOD >= 3 ? MOD - 2 : MOD;
+  constexpr bool KT = MOD >= 3;
   constexpr int NSK = Cfg::NSK, NSV = Cfg::NSV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -434,18 +439,19 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     const uint32_t colS = X ? 128u : 0u, colO = 256u + (X ? 128u : 0u);
     const int i = hx.q0 + r;
     const int ip = i + pi.sk - pi.sq;
-    // Prologue terms (see PrefillParams): the row term enters the scores
-    // under the soft-cap only; the per-key term of a Q add, when present, is
-    // read per 32-key chunk (all lanes read the same addresses; the address
-    // is formed from the parameter block there, so nothing stays live).
+    // Prologue terms (see PrefillParams; kernels with KT only): the row term
+    // enters the scores under the soft-cap; the per-key term of a Q add, when
+    // present, is read per 32-key chunk (all lanes read the same addresses;
+    // the address is formed from the parameter block there, so nothing stays
+    // live).
     const float row_term =
-        (MOD == 2 && i < pi.sq) ? softcap_row_term<DK>(p, (int64_t)pi.q_row0 + X * kBlockM + r, pi.h) : 0.f;
+        (KT && MK == 2 && i < pi.sq) ? softcap_row_term<DK>(p, (int64_t)pi.q_row0 + X * kBlockM + r, pi.h) : 0.f;
     float m_ref = -INFINITY, l = 0.f;
     int cnt = 0;
     bool ok = true;
     // MOD 0 runs with a positive scale only (the host routes other scales to
     // the general path), so raw scores can be maxed before scaling.
-    constexpr bool fast = (MOD == 0);
+    constexpr bool fast = (MK == 0);
     // Exponentials 2^(c*v - m) of a 32-column chunk with packed fp32 math,
     // their row sums and the bf16 packing of P.
     auto chunk_exp = [&](const float (&v)[32], float c, float m, uint32_t (&pk)[16], float (&acc)[4]) {
@@ -462,8 +468,15 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     const float cexp = fast ? p.scale_log2 : 1.f;
     // The deferred max (below) shortens the softmax; it pays where the
     // softmax is the critical path, i.e. with a score mod.  Plain scores keep
-    // the max-first order.
-    constexpr bool kDeferredMax = (MOD != 0);
+    // the max-first order, and so does ALiBi, for accuracy: its bias puts a
+    // row's mass on the nearest keys, and each tile toward them raises the
+    // row max past the rescale threshold, so with the max taken first the
+    // reference lands on the dominant key and its P is exactly 1.  Against a
+    // deferred reference that P can be anything up to 2^64, and its bf16
+    // rounding (up to 2^-9 relative, not mirrored in the fp32 row sum) moved
+    // outputs of magnitude 2 by a whole bf16 step.  Soft-capped scores are
+    // bounded, so no single key takes over a row and the deferred max stays.
+    constexpr bool kDeferredMax = (MK == 2);
     int j = -1;   // index of the tile in the pair's list (K/V ring position)
     for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
       ++j;
@@ -485,32 +498,38 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         if (!fast) {
           const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
           const float c2u = 2.f * kLog2e * p.softcap_arg;   // soft-cap: raw score -> 2u log2(e)
-          // Scaled score (log2 units; soft-cap: its argument 2u log2(e)) plus
-          // the prologue's row term (soft-cap only) and per-key term.
-          const float lin = MOD == 2 ? c2u : p.scale_log2;
-          if (p.col_bias && jc + 32 <= p.cb_ld) {   // no term is read past cb_ld (the pre-pass flags such keys)
+          if constexpr (KT) {
+            // scaled score (log2 units; soft-cap: its argument 2u log2(e))
+            // plus the row term (soft-cap) and the key's term; no term is
+            // read past cb_ld (the pre-pass flags such keys)
+            const float lin = MK == 2 ? c2u : p.scale_log2;
+            const bool in_ld = p.col_bias != nullptr && jc + 32 <= p.cb_ld;
             const float4 *c4 =
                 reinterpret_cast<const float4 *>(p.col_bias + ((int64_t)pi.b * p.hkv + pi.hk) * p.cb_ld + jc);
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-              const float4 c = c4[e >> 2];
+              const float4 c = in_ld ? c4[e >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
               v[e] = fmaf(v[e], lin, c.x + row_term);
               v[e + 1] = fmaf(v[e + 1], lin, c.y + row_term);
               v[e + 2] = fmaf(v[e + 2], lin, c.z + row_term);
               v[e + 3] = fmaf(v[e + 3], lin, c.w + row_term);
             }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = fmaf(v[e], lin, row_term);
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            float x = v[e];
-            if constexpr (MOD == 2) {
+            float x;
+            if constexpr (KT) {
+              x = v[e];
+            } else if constexpr (MK == 2) {
+              x = v[e] * c2u;
+            } else {
+              x = v[e] * p.scale_log2;
+            }
+            if constexpr (MK == 2) {
               float r;
               x = softcap_log2_score(ex2(x), p.softcap_log2, r);
             }
-            if constexpr (MOD == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
+            if constexpr (MK == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
             v[e] = x;
           }
         }

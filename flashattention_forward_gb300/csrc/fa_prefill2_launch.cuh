@@ -1,0 +1,56 @@
+// Launcher of the two-query-tile ping-pong kernel (fa_prefill2.cuh), shared
+// by the translation units that instantiate it for one head dim each.
+#pragma once
+#include "fa_internal.h"
+#include "fa_prefill2.cuh"
+
+namespace fa {
+
+// The 12-warp variant raises the softmax warps to Cfg::kRegsSoftmax registers
+// with setmaxnreg.inc, which waits until other warps of the CTA release
+// registers.  It is launched only when the compiled launch register count
+// makes the whole split fit the CTA's pool; otherwise the 10-warp variant runs.
+template <int D, bool PAGED, int MOD>
+bool prefill2_bigreg_fits() {
+  using Big = Prefill2Cfg<D, D, PAGED, MOD, true>;
+  static int verdict = -1;   // per process: all devices run the same binary
+  if (verdict < 0) {
+    cudaFuncAttributes a;
+    const bool ok = cudaFuncGetAttributes(&a, fa_prefill2_kernel<D, D, PAGED, MOD, true>) == cudaSuccess &&
+                    a.numRegs >= Big::kMinLaunchRegs && a.numRegs * Big::kThreads >=
+                    8 * 32 * Big::kRegsSoftmax + 4 * 32 * Big::kRegsOther;
+    verdict = ok ? 1 : 0;
+  }
+  return verdict == 1;
+}
+
+template <int D, bool PAGED, int MOD, bool BIG>
+cudaError_t prefill2_launch_one(const PrefillLaunch &L) {
+  using Cfg = Prefill2Cfg<D, D, PAGED, MOD, BIG>;
+  static unsigned long long done = 0;
+  auto kern = fa_prefill2_kernel<D, D, PAGED, MOD, BIG>;
+  cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
+  if (e != cudaSuccess) return e;
+  kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+  return cudaGetLastError();
+}
+
+template <int D, bool PAGED, int MOD>
+cudaError_t prefill2_pick(const PrefillLaunch &L) {
+  if (L.variant != 1 && prefill2_bigreg_fits<D, PAGED, MOD>()) return prefill2_launch_one<D, PAGED, MOD, true>(L);
+  return prefill2_launch_one<D, PAGED, MOD, false>(L);
+}
+
+// MOD 0 plain, 1 ALiBi, 2 soft-cap; 3 and 4 (a prologue's per-key score
+// term) are instantiated in fa_prefill_kt.cu.
+template <int D, bool PAGED>
+cudaError_t prefill2_by_mod(const PrefillLaunch &L) {
+  switch (L.mod) {
+    case 0: return prefill2_pick<D, PAGED, 0>(L);
+    case 1: return prefill2_pick<D, PAGED, 1>(L);
+    case 2: return prefill2_pick<D, PAGED, 2>(L);
+    default: return launch_prefill2_kt(D, L);
+  }
+}
+
+}  // namespace fa

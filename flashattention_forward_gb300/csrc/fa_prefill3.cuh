@@ -182,6 +182,11 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     fa_prefill3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
+  // MOD: 0 plain scores, 1 ALiBi, 2 soft-cap; 3 and 4 are 1 and 2 with the
+  // prologue's score terms (KT): a Q add's per-key term and, under the
+  // soft-cap, the row term of a K add
+  constexpr int MK = MOD >= 3 ? MOD - 2 : MOD;
+  constexpr bool KT = MOD >= 3;
   static_assert(!(Q8 && I8), "int8 keys have no e4m3 QK");
   constexpr int KC = Cfg::KC, VC = Cfg::VC, NCK = Cfg::NCK, NSV = Cfg::NSV;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -697,12 +702,13 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     const uint32_t colS = X ? 128u : 0u, colO = 256u + (X ? 128u : 0u);
     const int i = hx.q0 + r;
     const int ip = i + pi.sk - pi.sq;
-    // Prologue terms (see PrefillParams): the row term enters the scores
-    // under the soft-cap only; the per-key term of a Q add, when present, is
-    // read per 32-key chunk (all lanes read the same addresses; the address
-    // is formed from the parameter block there, so nothing stays live).
+    // Prologue terms (see PrefillParams; kernels with KT only): the row term
+    // enters the scores under the soft-cap; the per-key term of a Q add, when
+    // present, is read per 32-key chunk (all lanes read the same addresses;
+    // the address is formed from the parameter block there, so nothing stays
+    // live).
     const float row_term =
-        (MOD == 2 && i < pi.sq) ? softcap_row_term<DK>(p, (int64_t)pi.q_row0 + X * kBlockM + r, pi.h) : 0.f;
+        (KT && MK == 2 && i < pi.sq) ? softcap_row_term<DK>(p, (int64_t)pi.q_row0 + X * kBlockM + r, pi.h) : 0.f;
     float m_ref = -INFINITY, l = 0.f;
     int cnt = 0;
     bool ok = true;
@@ -751,13 +757,21 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     }
     // MOD 0 runs with a positive scale only (the host routes other scales to
     // the general path), so raw scores can be maxed before scaling.
-    constexpr bool fast = (MOD == 0);
+    constexpr bool fast = (MK == 0);
     // Deferred-max guard on a tile's row sum: P must stay finite in its
     // packed type (f16 for e4m3 caches: below 65504; bf16: any fp32 value).
     constexpr float kGuard = FP8 ? 0x1p15f : kGuardSum;
     const float sl2 = p.scale_log2 * rowf;
     const float c2u = 2.f * kLog2e * p.softcap_arg * rowf;   // soft-cap: raw score -> 2u log2(e)
     auto pack_p = [](float a, float b) -> uint32_t { return FP8 ? pack_f16x2(a, b) : pack_bf16x2(a, b); };
+    auto unpack_p = [](uint32_t w, float &a, float &b) {
+      if constexpr (FP8) {
+        unpack_f16x2(w, a, b);
+      } else {
+        a = __uint_as_float(w << 16);
+        b = __uint_as_float(w & 0xFFFF0000u);
+      }
+    };
     auto chunk_exp = [&](const float (&v)[32], float c, float m, uint32_t (&pk)[16], float (&acc)[4]) {
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
@@ -770,7 +784,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       }
     };
     const float cexp = fast ? sl2 : 1.f;
-    constexpr bool kDeferredMax = (MOD != 0);   // as in fa_prefill2.cuh
+    constexpr bool kDeferredMax = (MK == 2);   // soft-cap only, as in fa_prefill2.cuh
     int j = -1;   // index of the tile in the pair's list (ring position)
     for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
       ++j;
@@ -805,32 +819,38 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         }
         if (!fast) {
           const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
-          // Scaled score (log2 units; soft-cap: its argument 2u log2(e)) plus
-          // the prologue's row term (soft-cap only) and per-key term.
-          const float lin = MOD == 2 ? c2u : sl2;
-          if (p.col_bias && jc + 32 <= p.cb_ld) {   // no term is read past cb_ld (the pre-pass flags such keys)
+          if constexpr (KT) {
+            // scaled score (log2 units; soft-cap: its argument 2u log2(e))
+            // plus the row term (soft-cap) and the key's term; no term is
+            // read past cb_ld (the pre-pass flags such keys)
+            const float lin = MK == 2 ? c2u : sl2;
+            const bool in_ld = p.col_bias != nullptr && jc + 32 <= p.cb_ld;
             const float4 *c4 =
                 reinterpret_cast<const float4 *>(p.col_bias + ((int64_t)pi.b * p.hkv + pi.hk) * p.cb_ld + jc);
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-              const float4 c = c4[e >> 2];
+              const float4 c = in_ld ? c4[e >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
               v[e] = fmaf(v[e], lin, c.x + row_term);
               v[e + 1] = fmaf(v[e + 1], lin, c.y + row_term);
               v[e + 2] = fmaf(v[e + 2], lin, c.z + row_term);
               v[e + 3] = fmaf(v[e + 3], lin, c.w + row_term);
             }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = fmaf(v[e], lin, row_term);
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            float x = v[e];
-            if constexpr (MOD == 2) {
+            float x;
+            if constexpr (KT) {
+              x = v[e];
+            } else if constexpr (MK == 2) {
+              x = v[e] * c2u;
+            } else {
+              x = v[e] * sl2;
+            }
+            if constexpr (MK == 2) {
               float r;
               x = softcap_log2_score(ex2(x), p.softcap_log2, r);
             }
-            if constexpr (MOD == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
+            if constexpr (MK == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
             v[e] = x;
           }
         }
@@ -973,12 +993,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
                 for (int e = 0; e < 32; ++e) {
                   const uint32_t u = __float_as_uint(pw[e]);
                   float lo, hi;
-                  if constexpr (FP8) {
-                    unpack_f16x2(u, lo, hi);
-                  } else {
-                    lo = __uint_as_float(u << 16);
-                    hi = __uint_as_float(u & 0xFFFF0000u);
-                  }
+                  unpack_p(u, lo, hi);
                   w[e] = pack_p(lo * alpha, hi * alpha);
                 }
                 tmem_st32(sa, w);

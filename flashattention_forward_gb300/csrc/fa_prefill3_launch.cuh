@@ -51,9 +51,15 @@ cudaError_t launch_prefill3_pick(const PrefillLaunch &L) {
 }
 
 // FP8: byte caches with per-token scales; I8 selects int8 values over e4m3;
-// Q8 (e4m3 caches) takes e4m3 Q and runs QK on the bytes.
+// Q8 (e4m3 caches) takes e4m3 Q and runs QK on the bytes.  MOD 0 plain, 1
+// ALiBi, 2 soft-cap; 3 and 4 (a prologue's per-key score term, never with
+// Q8) are instantiated in translation units of their own.
 template <int DK, int DV, bool FP8, bool I8 = false, bool Q8 = false>
 cudaError_t launch_prefill3(const PrefillLaunch &L) {
+  if (L.mod >= 3) {
+    if (Q8) return cudaErrorInvalidValue;
+    return I8 ? launch_prefill3_kt_i8(DK, L) : launch_prefill3_kt(DK, FP8, L);
+  }
   auto by_mod = [&](auto paged_tag) -> cudaError_t {
     constexpr bool PG = decltype(paged_tag)::value;
     switch (L.mod) {
@@ -63,6 +69,16 @@ cudaError_t launch_prefill3(const PrefillLaunch &L) {
     }
   };
   return L.paged ? by_mod(std::true_type{}) : by_mod(std::false_type{});
+}
+
+// The MOD 3 and 4 kernels of one (Dk, Dv, cache) combination.
+template <int DK, int DV, bool FP8, bool I8>
+cudaError_t launch_prefill3_kt_one(const PrefillLaunch &L) {
+  if (L.paged)
+    return L.mod == 3 ? launch_prefill3_pick<DK, DV, true, FP8, 3, I8, false>(L)
+                      : launch_prefill3_pick<DK, DV, true, FP8, 4, I8, false>(L);
+  return L.mod == 3 ? launch_prefill3_pick<DK, DV, false, FP8, 3, I8, false>(L)
+                    : launch_prefill3_pick<DK, DV, false, FP8, 4, I8, false>(L);
 }
 
 }  // namespace fa
