@@ -392,6 +392,29 @@ def cpu_oracle_sample(p, seconds_target=2.0, seed=0, n0=256):
     return flops / dt, len(units), threads, dt, flops
 
 
+def measure_fp8_peak(dev, n=8192, reps=10):
+    """Dense e4m3 x e4m3 -> bf16 GEMM throughput (torch._scaled_mm, cuBLASLt),
+    best of `reps`, TFLOP/s: the denominator for contractions that run at the
+    e4m3 rate.  None if this torch has no _scaled_mm."""
+    if not hasattr(torch, "_scaled_mm"):
+        return None
+    a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device=dev)
+    for _ in range(3):
+        torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    best = float("inf")
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    del a, b
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
 def max_over_ranks(ms, dist=None, device="cpu"):
     """The slowest rank's step time: every replica's work counts only once all
     ranks have finished it."""
@@ -692,6 +715,7 @@ def compact_summary(runs, extra, pk):
            "paged_decode_64seq_hq32_hkv8_p16": "c3", "paged_decode_e4m3_64seq_hq32_hkv8_p16": "c3_e4m3",
            "paged_decode_int8_64seq_hq32_hkv8_p16": "c3_int8", "paged_fp8_d192_v128_16seq_h16_p64_causal": "c4",
            "paged_fp8kv_qe4m3_d128_16seq_h16_p64_causal": "c4_q8_d128",
+           "paged_fp8kv_qe4m3_d192_v128_16seq_h16_p64_causal": "c4_q8",
            "bwd_4x4096_h16_d128_noncausal": "bwd_4x4096"}
     for name, short in key.items():
         v = extra.get(name)
@@ -822,6 +846,24 @@ def other_workloads(dev, warmup, steps, flush, pk):
                                                         "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
                                                         "gflop": fl / 1e9}
     del t
+    # config 4 with e4m3 Q (QK on the e4m3 bytes by kind::f8f6f4, PV kind::f16):
+    # besides the bf16 peak, the fraction of the peak of the mix the kernel
+    # runs -- QK's 2 Dk flops per pair at the e4m3 rate, PV's 2 Dv at the
+    # 16-bit rate
+    fp8_peak = measure_fp8_peak(dev)
+    lens4 = [int(x) for x in np.diff(fi.config4().cu_seqlens_q)]
+    p = fi.make_problem(lens4, hq=16, hkv=16, dk=192, dv=128, seed=1, page_size=64, kv_dtype="e4m3",
+                        q_dtype="e4m3", spare_pages=16, causal=True, name="config4_e4m3q")
+    t = dev_tensors(p, dev)
+    call, _, _, _ = make_call(p, t, num_splits=0)
+    ms = statistics.mean(time_calls([call], warmup, steps, flush))
+    fl = fi.prefill_flops(p)
+    pairs = fl / (2 * p.dk + 2 * p.dv)
+    t_peak = pairs * 2 * p.dk / (fp8_peak * 1e12) + pairs * 2 * p.dv / (pk["bf16"] * 1e12)
+    res["paged_fp8kv_qe4m3_d192_v128_16seq_h16_p64_causal"] = {
+        "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+        "frac_of_mixed_peak": t_peak / (ms * 1e-3), "fp8_peak_tflops": fp8_peak, "gflop": fl / 1e9}
+    del t
     # the same lengths at Dk = Dv = 128 with e4m3 K/V: bf16 Q (f16 QK) and
     # e4m3 Q (QK on the e4m3 bytes)
     for qd in ("bf16", "e4m3"):
@@ -871,6 +913,11 @@ def profile_only(name, warmup, steps):
         p, splits = fi.make_problem([8192] * 4, hq=16, dk=128, name="long_noncausal"), 0
     elif name == "fp8":
         p, splits = fi.config4(), 0
+    elif name == "e4m3q_d192":
+        lens = [int(x) for x in np.diff(fi.config4().cu_seqlens_q)]
+        p = fi.make_problem(lens, hq=16, hkv=16, dk=192, dv=128, seed=1, page_size=64, kv_dtype="e4m3",
+                            q_dtype="e4m3", spare_pages=16, causal=True, name=name)
+        splits = 0
     elif name in ("fp8kv_d128", "e4m3q_d128"):
         lens = [int(x) for x in np.diff(fi.config4().cu_seqlens_q)]
         p = fi.make_problem(lens, hq=16, hkv=16, dk=128, dv=128, seed=1, page_size=64, kv_dtype="e4m3",

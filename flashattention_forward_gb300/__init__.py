@@ -218,8 +218,8 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None, prologue=None):
     """Attention forward over packed varlen Q and packed or paged K/V.
 
-    q [T_q, Hq, Dk] bf16, or float8_e4m3fn with e4m3 caches at Dk = Dv = 128
-    (QK then runs on the e4m3 bytes; fold a per-tensor Q scale into
+    q [T_q, Hq, Dk] bf16, or float8_e4m3fn with e4m3 caches at Dk 128 or 192
+    and Dv 128 (QK then runs on the e4m3 bytes; fold a per-tensor Q scale into
     ``softmax_scale``); k_cache/v_cache packed [T_k, Hkv, D] or paged
     [N_pg, P_s, Hkv, D] (bf16, or e4m3 as float8_e4m3fn/uint8, or int8, with
     k_scale/v_scale); cu_seqlens int32 [B+1].  ``max_seqlen_q/k`` are host ints (no

@@ -462,7 +462,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   // e4m3 Q: QK on the e4m3 bytes, which needs e4m3 keys; one head-dim pair.
   const bool q8 = q_dt == FA_E4M3;
   if (q8 && kv_dt != FA_E4M3) return fail(FA_ERR_UNSUPPORTED, "e4m3 q needs e4m3 k_cache/v_cache");
-  if (q8 && (Dk != 128 || Dv != 128)) return fail(FA_ERR_UNSUPPORTED, "e4m3 q is compiled for Dk = Dv = 128 only");
+  if (q8 && !((Dk == 128 || Dk == 192) && Dv == 128))
+    return fail(FA_ERR_UNSUPPORTED, "e4m3 q is compiled for (Dk, Dv) = (128, 128) and (192, 128)");
   if (q8 && launch->num_splits > 0) return fail(FA_ERR_UNSUPPORTED, "split-KV takes bf16 q; use num_splits = 0 with e4m3 q");
   const int esz = dtype_size(kv_dt);
   for (const fa_tensor_t *t : {k_cache, v_cache}) {

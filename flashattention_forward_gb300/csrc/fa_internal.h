@@ -70,6 +70,7 @@ cudaError_t launch_prefill_64_64_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_192_128_i8(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128_q8(const PrefillLaunch &L);
+cudaError_t launch_prefill_192_128_q8(const PrefillLaunch &L);
 // Kernels with a prologue's per-key score term (PrefillLaunch::mod 3 or 4), in
 // translation units of their own: the ping-pong kernel (bf16 K/V, Dk = Dv in
 // {64, 128}) and the chunked-ring kernel (bf16 Dk 192, e4m3 and int8 caches).

@@ -34,15 +34,16 @@
 // issue; e4m3: 10-15 converters (16 warps); bf16: 10-11 idle in the 12-warp
 // variant (warpgroup 2 hands its registers to the softmax warpgroups).
 //
-// Q8 (e4m3 Q with e4m3 K/V, Dk = Dv = 128; FlyDSL PR #1066 description: OCP
-// E4M3 Q/K/V with scalar descales): Q and K are the operands of a
-// kind::f8f6f4 QK as stored -- TMA drops them 128-byte swizzled, no
-// conversion -- so S' = sum_d q8 k8 and the score is S'_ij * k_scale_j (the
-// per-tensor Q scale is part of softmax_scale).  The producer lanes copy the
-// 128 K scales of a tile into a small array beside its ring chunk with
-// cp.async, tracked by the chunk's barrier; the softmax multiplies each S
-// column by its scale before the max.  V is still converted to f16 and PV
-// runs kind::f16 with P in f16.
+// Q8 (e4m3 Q with e4m3 K/V, Dk 128 or 192, Dv 128; FlyDSL PR #1066
+// description: OCP E4M3 Q/K/V with scalar descales): Q and K are the operands
+// of a kind::f8f6f4 QK as stored -- TMA drops them 128-byte swizzled in
+// chunks of 128 columns, no conversion -- so S' = sum_d q8 k8 and the score
+// is S'_ij * k_scale_j (the per-tensor Q scale is part of softmax_scale).
+// At Dk 192 a row spans two chunks; TMA fills columns 192..255 of the second
+// with zeros and the QK skips them.  The producer lanes copy the 128 K
+// scales of a tile with cp.async into a ring of their own (one slot per
+// tile); the softmax multiplies each S column by its scale before the max.
+// V is still converted to f16 and PV runs kind::f16 with P in f16.
 #pragma once
 #include "fa_prefill2.cuh"
 
@@ -51,24 +52,27 @@ namespace fa {
 template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool Q8 = false>
 struct Prefill3Cfg {
   // 16 KB chunks per K tile: 64 bf16/f16 columns, or (Q8) 128 e4m3 columns
-  static constexpr int KC = Q8 ? DK / 128 : DK / 64;
+  // (Dk 192: two chunks, the second half zero-filled by TMA)
+  static constexpr int KC = Q8 ? (DK + 127) / 128 : DK / 64;
   static constexpr int VC = DV / 64;              // 64-column blocks per V tile
   static constexpr int kChunkBytes = kBlockN * 128;
-  static constexpr int kQTileBytes = kBlockM * DK * (Q8 ? 1 : 2);
+  static constexpr int kQTileBytes = Q8 ? KC * kBlockM * 128 : kBlockM * DK * 2;
   static constexpr int kVBytes = VC * kChunkBytes;
-  static constexpr int kKsBytes = Q8 ? kBlockN * 4 : 0;    // per chunk: the K scales of its keys
+  // Q8: a ring of NSS tiles' K scales (NSS >= NSV + 1: see the producer)
+  static constexpr int NSS = Q8 ? 4 : 1;
+  static constexpr int kKsBytes = Q8 ? NSS * kBlockN * 4 : 0;
   static constexpr int kRing = 229376 - 2 * kQTileBytes;   // 224 KB minus the Q tiles
   static constexpr int NSV = (DV <= 64) ? 6 : 2;
-  static constexpr int NCK_raw = (kRing - NSV * kVBytes) / (kChunkBytes + kKsBytes);
+  static constexpr int NCK_raw = (kRing - NSV * kVBytes - kKsBytes) / kChunkBytes;
   static constexpr int NCK = NCK_raw > 8 ? 8 : NCK_raw;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + NCK * kChunkBytes;
   static constexpr int kOffKs = kOffV + NSV * kVBytes;
-  static constexpr int kOffBar = kOffKs + NCK * kKsBytes;
+  static constexpr int kOffBar = kOffKs + kKsBytes;
   // q_full, q_conv[2], kc_full/kc_empty/kc_stage[NCK], v_full/v_empty/v_stage[NSV],
-  // s_full[2], p_full[2], o_done[2]
-  static constexpr int kNumBars = 3 + 3 * NCK + 3 * NSV + 6;
+  // s_full[2], p_full[2], o_done[2], Q8: ks_full[NSS]
+  static constexpr int kNumBars = 3 + 3 * NCK + 3 * NSV + 6 + (Q8 ? NSS : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64;
   // e4m3: 16 warps, always with the register split; bf16: BIGREG selects the
@@ -91,11 +95,9 @@ struct Prefill3Cfg {
   static_assert(NCK >= KC, "the K ring holds at least one tile");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(!kSplitRegs || kPoolNeeded <= 65536, "register split exceeds the register file");
-  static_assert(!Q8 || (FP8 && DK == 128 && DV == 128), "e4m3 Q runs with e4m3 K/V at Dk = Dv = 128");
-  // Q8: the scales of a chunk are read by the softmax after its QK; the chunk
-  // is refilled only after the producer has passed the V stage of a later
-  // tile, whose release follows that softmax.
-  static_assert(!Q8 || NCK >= NSV + 1, "K scales outlive their readers");
+  static_assert(!Q8 || (FP8 && (DK == 128 || DK == 192) && DV == 128),
+                "e4m3 Q runs with e4m3 K/V at Dk 128 or 192, Dv 128");
+  static_assert(!Q8 || NSS >= NSV + 1, "K scales outlive their readers");
 };
 
 // tcgen05 MMA with A and B from shared memory, e4m3 x e4m3 -> fp32 (K = 32 per
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
   uint8_t *sQ = smem + Cfg::kOffQ;
   uint8_t *sK = smem + Cfg::kOffK;
   uint8_t *sV = smem + Cfg::kOffV;
-  float *sKs = reinterpret_cast<float *>(smem + Cfg::kOffKs);   // Q8: [NCK][kBlockN]
+  float *sKs = reinterpret_cast<float *>(smem + Cfg::kOffKs);   // Q8: [NSS][kBlockN]
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
   uint64_t *q_full = bars;
   uint64_t *q_conv = bars + 1;          // [2] Q tile in f16 (e4m3 caches)
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
   uint64_t *s_full = v_stage + NSV;     // [2]
   uint64_t *p_full = s_full + 2;        // [2]
   uint64_t *o_done = p_full + 2;        // [2]
+  uint64_t *ks_full = o_done + 2;       // Q8: [NSS] a tile's K scales landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 8);
 
@@ -284,8 +287,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     // producer lane for gathered rows (pages of < 16 keys, never with Q8)
     const uint32_t n_fill = (PAGED && !Q8 && p.gather) ? 32u : 1u;
     for (int s = 0; s < NCK; ++s) {
-      // converted K: one arrive per slice; Q8: the TMA arrive + one per producer lane (scales)
-      mbar_init(smem_u32(kc_full + s), Q8 ? 1 + 32 : (FP8 ? 4 : n_fill));
+      // converted K: one arrive per slice; Q8: the TMA arrive
+      mbar_init(smem_u32(kc_full + s), Q8 ? 1 : (FP8 ? 4 : n_fill));
       mbar_init(smem_u32(kc_empty + s), 1);
       mbar_init(smem_u32(kc_stage + s), n_fill);
     }
@@ -299,6 +302,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       mbar_init(smem_u32(p_full + x), kBlockM);
       mbar_init(smem_u32(o_done + x), 1);
     }
+    if constexpr (Q8)
+      for (int s = 0; s < Cfg::NSS; ++s) mbar_init(smem_u32(ks_full + s), 32);   // one per producer lane
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -363,7 +368,11 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     constexpr uint32_t kKBlockBytes = kStageK ? kBlockN * 64 : kBlockN * 128;
     constexpr uint32_t kVBlockBytes = FP8 ? kBlockN * 64 : kBlockN * 128;
     // Q8: lane l copies the scales of keys 4l .. 4l+3 of a tile (one page:
-    // pages hold >= 16 keys), looked up one tile ahead like the box pages.
+    // pages hold >= 16 keys), looked up one tile ahead like the box pages,
+    // into slot j mod NSS of the scale ring.  The slot's previous tile,
+    // j - NSS <= j - 1 - NSV, is done with it: before the loads of tile j the
+    // producer waited for the release of V stage j - 1 - NSV, which follows
+    // the PV of that tile, which follows its softmax's reads of the scales.
     auto ks_page_at = [&](int kt) -> int {
       if constexpr (Q8 && PAGED) {
         const int key0 = kt * kBlockN + 4 * lane;
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       }
     };
     auto load_scales = [&](int slot, int kt, int kpage) {
-      const uint32_t dst = smem_u32(sKs + slot * kBlockN + 4 * lane);
+      const uint32_t dst = smem_u32(sKs + slot * kBlockN + 4 * lane);   // slot = tile j mod NSS
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int key = kt * kBlockN + 4 * lane + u;
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         else tok = (int64_t)pi.k_row0 + key;
         cp_async_4(dst + 4 * u, live ? p.k_scale + tok * p.hkv + pi.hk : p.k_scale, live ? 4u : 0u);
       }
-      cp_async_arrive_noinc(smem_u32(kc_full + slot));
+      cp_async_arrive_noinc(smem_u32(ks_full + slot));
     };
     bool gathered = false;
     if constexpr (PAGED && !Q8) {
@@ -465,7 +474,9 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c * (Q8 ? 128 : 64), kt, page, kStageK);
-        if constexpr (Q8) load_scales(slot, kt, kpage);
+        if constexpr (Q8) {
+          if (c == 0) load_scales(j % Cfg::NSS, kt, kpage);
+        }
       }
       if (!ok) break;
       const int sv = j % NSV;
@@ -524,8 +535,11 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         }
         const uint32_t a = a0 + (uint32_t)(c * ((kBlockM * 128) >> 4));
         const uint32_t b = k_lo + (uint32_t)(slot * (Cfg::kChunkBytes >> 4));
+        // Q8 at Dk 192: the second chunk's columns 192..255 are zeros
+        const int n_ks = Q8 ? min(4, (DK - 128 * c) / 32) : 4;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
+          if (ks >= n_ks) break;
           if constexpr (Q8) {
             if (c == 0 && ks == 0) mma_ss_f8_w<0>(d, a, qk_hi, b, qk_hi, idesc_qk);
             else mma_ss_f8_w<1>(d, a + 2 * ks, qk_hi, b + 2 * ks, qk_hi, idesc_qk);
@@ -793,11 +807,10 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const uint32_t sa = tmem + lane_base + colS;
-      // Q8: the tile's K scales (their cp.async copies completed on the
-      // chunk's barrier, which the QK waited for too).
-      const float *ks_tile = sKs + (j % NCK) * kBlockN;
+      // Q8: the tile's K scales, slot j mod NSS of their ring.
+      const float *ks_tile = sKs + (j % Cfg::NSS) * kBlockN;
       if constexpr (Q8) {
-        ok = mbar_wait(smem_u32(kc_full + j % NCK), (j / NCK) & 1, abort_flag, p.err);
+        ok = mbar_wait(smem_u32(ks_full + j % Cfg::NSS), (j / Cfg::NSS) & 1, abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
       const int j0 = kt * kBlockN;

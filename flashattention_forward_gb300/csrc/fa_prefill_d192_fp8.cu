@@ -5,6 +5,7 @@
 
 namespace fa {
 cudaError_t launch_prefill_192_128_fp8(const PrefillLaunch &L) {
+  if (L.q8) return launch_prefill_192_128_q8(L);
   return L.int8 ? launch_prefill_192_128_i8(L) : launch_prefill3<192, 128, true>(L);
 }
 }  // namespace fa

@@ -154,11 +154,11 @@ typedef struct {
 /*
  * fa_fwd_varlen -- the attention forward pass.
  *
- *  q            bf16 [T_q, Hq, Dk], or e4m3 [T_q, Hq, 128] with e4m3 caches
- *               and Dv = 128 (FlyDSL PR #1066 description: E4M3 Q/K/V with
- *               scalar descales; the caller folds the Q descale into
- *               softmax_scale, and QK runs on the e4m3 bytes with the per-key
- *               scale applied to each score).  Last dim contiguous, the other
+ *  q            bf16 [T_q, Hq, Dk], or e4m3 [T_q, Hq, Dk] with e4m3 caches,
+ *               Dk 128 or 192 and Dv 128 (FlyDSL PR #1066 description: E4M3
+ *               Q/K/V with scalar descales; the caller folds the Q descale
+ *               into softmax_scale, and QK runs on the e4m3 bytes with the
+ *               per-key scale applied to each score).  Last dim contiguous, the other
  *               strides multiples of 16 bytes.  Split-KV takes bf16 q only
  *               (Dk = Dv in {64, 128}); score mods, block masks and
  *               prologues apply to it as to the single pass.

@@ -226,7 +226,8 @@ def test_byte_caches_need_scales(L, dt):
 
 
 def test_e4m3_q_limits(L):
-    """e4m3 Q runs only with e4m3 K/V at Dk = Dv = 128 and without split-KV."""
+    """e4m3 Q runs only with e4m3 K/V at (Dk, Dv) = (128, 128) or (192, 128) and
+    without split-KV."""
     T, H = 256, 4
     q8 = _t(FAKE, fa.FA_E4M3, [T, H, 128])
     k8 = _t(FAKE * 2, fa.FA_E4M3, [T, H, 128])
@@ -239,7 +240,7 @@ def test_e4m3_q_limits(L):
     assert st == fa.FA_ERR_UNSUPPORTED and "e4m3 k_cache" in msg
     st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 64]), k=_t(FAKE * 2, fa.FA_E4M3, [T, H, 64]),
                     v=_t(FAKE * 3, fa.FA_E4M3, [T, H, 64]), ks=ks, vs=vs)
-    assert st == fa.FA_ERR_UNSUPPORTED and "Dk = Dv = 128" in msg
+    assert st == fa.FA_ERR_UNSUPPORTED and "(192, 128)" in msg
     st, msg = _call(L, q=q8, k=k8, v=v8, ks=ks, vs=vs, out=out,
                     launch=fa.Launch(num_seqs=2, max_seqlen_q=1, max_seqlen_k=128, num_splits=4,
                                      total_q=T, total_k=T))

@@ -536,14 +536,16 @@ def test_int8_with_scales_matches_torch_sdpa_on_dequantised_values():
     assert np.max(np.abs(o3 - o1)) > 1e-3
 
 
+@pytest.mark.parametrize("dk,dv", [(32, 16), (192, 128)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_e4m3_q_matches_torch_sdpa(causal):
+def test_e4m3_q_matches_torch_sdpa(causal, dk, dv):
     """e4m3 Q bytes (decoded by torch) with paged e4m3 K/V against torch's
-    fp64 SDPA: pins the Q decode and the Q byte layout."""
-    p = fi.make_problem([37, 0, 64], [45, 3, 64], hq=4, hkv=2, dk=32, dv=16, seed=23,
+    fp64 SDPA: pins the Q decode and the Q byte layout, also at the Q/K 192,
+    V/O 128 geometry."""
+    p = fi.make_problem([37, 0, 64], [45, 3, 64], hq=4, hkv=2, dk=dk, dv=dv, seed=23,
                         page_size=16, kv_dtype="e4m3", spare_pages=2, causal=causal,
                         q_dtype="e4m3")
-    assert p.q.dtype == np.uint8 and p.q.shape == (101, 4, 32)
+    assert p.q.dtype == np.uint8 and p.q.shape == (101, 4, dk)
     out, lse = oracle.forward(p)
     ro, rl = sdpa_reference(p)
     assert_close(out, ro, 1e-12)

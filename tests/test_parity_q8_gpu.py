@@ -51,6 +51,37 @@ def test_q8_cases(case):
     check(fi.make_problem(lens_q, lens_k, seed=500 + case, dk=128, dv=128, kv_dtype="e4m3", q_dtype="e4m3", **kw))
 
 
+Q8_D192_CASES = [
+    dict(lens_q=[300, 129, 1], lens_k=[300, 400, 77], hq=4, hkv=2),                                # packed
+    dict(lens_q=[300, 129], lens_k=[300, 400], hq=4, hkv=2, page_size=16, spare_pages=4, causal=True),
+    dict(lens_q=[200, 64, 3], lens_k=[260, 64, 500], hq=8, hkv=1, page_size=64, causal=True, window=90),
+    dict(lens_q=[130, 260], lens_k=[130, 260], hq=4, page_size=128, mod="alibi"),
+    dict(lens_q=[130, 70], lens_k=[300, 70], hq=4, page_size=64, mod="softcap", softcap=5.0, causal=True),
+    dict(lens_q=[0, 5, 0], lens_k=[7, 0, 0], hq=2, page_size=16),                                     # empty rows
+    dict(lens_q=[200, 330], lens_k=[200, 330], hq=4, page_size=1024, block_mask_density=0.5),
+    dict(lens_q=[300, 40], lens_k=[100, 40], hq=2, page_size=64, causal=True),                        # Sk < Sq
+]
+
+
+@pytest.mark.parametrize("case", range(len(Q8_D192_CASES)))
+def test_q8_d192_cases(case):
+    """e4m3 Q at Q/K 192, V/O 128: a key row spans two 128-column chunks,
+    the second half-empty (TMA zero-fills columns 192..255)."""
+    kw = dict(Q8_D192_CASES[case])
+    lens_q = kw.pop("lens_q")
+    lens_k = kw.pop("lens_k", None)
+    check(fi.make_problem(lens_q, lens_k, seed=520 + case, dk=192, dv=128, kv_dtype="e4m3", q_dtype="e4m3", **kw))
+
+
+def test_q8_config4_geometry_every_row():
+    """Config 4 (16 sequences of U{1..4096} tokens, H 16, Q/K 192, V/O 128,
+    page 64, causal) with e4m3 Q: every (token, head) row against the oracle."""
+    base = fi.config4()
+    p = fi.make_problem(list(np.diff(base.cu_seqlens_q)), hq=16, hkv=16, dk=192, dv=128, seed=1, page_size=64,
+                        kv_dtype="e4m3", q_dtype="e4m3", spare_pages=16, causal=True, name="config4_e4m3q")
+    check(p)
+
+
 def test_q8_key_scales_spread():
     """Key scales spread over 2^-4 .. 2^4 of their quantiser's value (scores
     then span a wide range): each score column must carry its own key's
