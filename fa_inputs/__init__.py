@@ -204,6 +204,19 @@ def scatter_pages(tokens: np.ndarray, cu_k: np.ndarray, block_table: np.ndarray,
     return pool
 
 
+def vectorize_pages(k: np.ndarray, v: np.ndarray, x: int = 16):
+    """The vectorized 5-D page layouts of a paged byte cache: K [N_pg, P_s,
+    Hkv, Dk] -> [N_pg, Hkv, Dk/x, P_s, x] and V [N_pg, P_s, Hkv, Dv] ->
+    [N_pg, Hkv, P_s/x, Dv, x] (x = 16 one-byte elements, 16 bytes).  The
+    permutes (0, 3, 1, 2, 4) of K and (0, 2, 4, 1, 3) of V undo them (FlyDSL
+    PR #1066, review).  A layout only: the same bytes, moved."""
+    n, ps, hkv, dk = k.shape
+    dv = v.shape[3]
+    k5 = np.ascontiguousarray(k.reshape(n, ps, hkv, dk // x, x).transpose(0, 2, 3, 1, 4))
+    v5 = np.ascontiguousarray(v.reshape(n, ps // x, x, hkv, dv).transpose(0, 3, 1, 4, 2))
+    return k5, v5
+
+
 def make_problem(seqlens_q: Sequence[int], seqlens_k: Optional[Sequence[int]] = None, *,
                  hq: int = 4, hkv: Optional[int] = None, dk: int = 64, dv: Optional[int] = None,
                  seed: int = 0, page_size: int = 0, kv_dtype: str = "bf16",

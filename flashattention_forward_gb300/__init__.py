@@ -166,6 +166,15 @@ def _kv_dtype(k_cache: torch.Tensor) -> int:
     return FA_E4M3
 
 
+def _cache_dims(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    """(Hkv, Dv) of packed [T_k, Hkv, D] or paged [N_pg, P_s, Hkv, D] caches,
+    or of the vectorized 5-D pages K [N_pg, Hkv, Dk/16, P_s, 16] and
+    V [N_pg, Hkv, P_s/16, Dv, 16]."""
+    if k_cache.dim() == 5:
+        return k_cache.shape[1], v_cache.shape[3]
+    return k_cache.shape[-2], v_cache.shape[-1]
+
+
 def as_tensor(t: Optional[torch.Tensor], fa_dtype: Optional[int] = None) -> Optional[Tensor]:
     """Describe a torch tensor (device pointer, shape, element strides)."""
     if t is None:
@@ -222,7 +231,9 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     and Dv 128 (QK then runs on the e4m3 bytes; fold a per-tensor Q scale into
     ``softmax_scale``); k_cache/v_cache packed [T_k, Hkv, D] or paged
     [N_pg, P_s, Hkv, D] (bf16, or e4m3 as float8_e4m3fn/uint8, or int8, with
-    k_scale/v_scale); cu_seqlens int32 [B+1].  ``max_seqlen_q/k`` are host ints (no
+    k_scale/v_scale), or -- e4m3 and int8 pages of >= 16 keys -- the
+    vectorized 5-D pages K [N_pg, Hkv, Dk/16, P_s, 16], V [N_pg, Hkv, P_s/16,
+    Dv, 16] (scales stay [N_pg, P_s, Hkv]); cu_seqlens int32 [B+1].  ``max_seqlen_q/k`` are host ints (no
     device read-back).  Returns ``(out [T_q, Hq, Dv] bf16, lse [Hq, T_q] fp32
     or None)``.  ``num_splits=None`` picks the library's default (split-KV for
     decode shapes); 0 forces the single-pass kernel.  ``prologue``: op chains
@@ -232,8 +243,7 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     L = lib()
     B = cu_seqlens_q.shape[0] - 1
     Tq, Hq, Dk = q.shape
-    Dv = v_cache.shape[-1]
-    Hkv = k_cache.shape[-2]
+    Hkv, Dv = _cache_dims(k_cache, v_cache)
     kv_dt = _kv_dtype(k_cache)
     if out is None:
         out = torch.empty((Tq, Hq, Dv), dtype=torch.bfloat16, device=q.device)
@@ -320,8 +330,7 @@ class FwdPlan:
                                                                            if isinstance(v, torch.Tensor)]
         B = cu_seqlens_q.shape[0] - 1
         Tq, Hq, Dk = q.shape
-        Dv = v_cache.shape[-1]
-        Hkv = k_cache.shape[-2]
+        Hkv, Dv = _cache_dims(k_cache, v_cache)
         kv_dt = _kv_dtype(k_cache)
         self.out = kw.get("out")
         if self.out is None:

@@ -180,6 +180,24 @@ fa::KvGather kv_gather(const fa_tensor_t *t, int esz) {
   return g;
 }
 
+// Tensor maps over byte caches in the vectorized 5-D page layouts:
+// K [N_pg, Hkv, Dk/16, P_s, 16] in boxes of {16 bytes, k_rows tokens,
+// k_groups column groups}, V [N_pg, Hkv, P_s/16, Dv, 16] in boxes of
+// {16 tokens, v_dims dims, v_groups token groups}; unswizzled uint8.
+fa_status_t make_vec5_maps(CUtensorMap *tk, CUtensorMap *tv, const fa_tensor_t *k, const fa_tensor_t *v, int64_t dk,
+                           int64_t dv, int64_t hkv, int64_t ps, int64_t n_pages, uint32_t k_rows, uint32_t k_groups,
+                           uint32_t v_dims, uint32_t v_groups) {
+  const uint64_t kd[5] = {16, (uint64_t)ps, (uint64_t)(dk / 16), (uint64_t)hkv, (uint64_t)n_pages};
+  const uint64_t ks[4] = {(uint64_t)k->stride[3], (uint64_t)k->stride[2], (uint64_t)k->stride[1], (uint64_t)k->stride[0]};
+  const uint32_t kb[5] = {16, k_rows, k_groups, 1, 1};
+  const uint64_t vd[5] = {16, (uint64_t)dv, (uint64_t)(ps / 16), (uint64_t)hkv, (uint64_t)n_pages};
+  const uint64_t vs[4] = {(uint64_t)v->stride[3], (uint64_t)v->stride[2], (uint64_t)v->stride[1], (uint64_t)v->stride[0]};
+  const uint32_t vb[5] = {16, v_dims, v_groups, 1, 1};
+  fa_status_t st = make_map(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, k->data, kd, ks, kb, "k (5-D)", CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st) return st;
+  return make_map(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, v->data, vd, vs, vb, "v (5-D)", CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 bool supported_dims(int64_t dk, int64_t dv) {
   return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
 }
@@ -442,21 +460,39 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   if (Tq != launch->total_q) return fail(FA_ERR_INVALID_ARG, "q.shape[0]=%lld != launch.total_q=%lld", (long long)Tq, (long long)launch->total_q);
   if (q->stride[2] != 1 || (q->stride[1] * qsz) % 16 || (q->stride[0] * qsz) % 16)
     return fail(FA_ERR_INVALID_ARG, "q needs a contiguous last dim and strides that are multiples of 16 bytes");
-  // ---- k/v
+  // ---- k/v: packed [T_k, Hkv, D], paged [N_pg, P_s, Hkv, D], or (byte
+  // caches) the vectorized 5-D pages K [N_pg, Hkv, Dk/16, P_s, 16] and
+  // V [N_pg, Hkv, P_s/16, Dv, 16]
   const bool paged = block_table != nullptr;
-  const int kvnd = paged ? 4 : 3;
   if (!k_cache || !v_cache) return fail(FA_ERR_INVALID_ARG, "k_cache/v_cache is NULL");
+  const bool vec5 = paged && k_cache->ndim == 5;
+  const int kvnd = vec5 ? 5 : (paged ? 4 : 3);
   const int kv_dt = k_cache->dtype;
   if (kv_dt != FA_BF16 && kv_dt != FA_E4M3 && kv_dt != FA_I8)
     return fail(FA_ERR_INVALID_ARG, "k_cache dtype must be bf16, e4m3 or int8");
   if ((st = check_tensor(k_cache, "k_cache", kv_dt, kvnd))) return st;
   if ((st = check_tensor(v_cache, "v_cache", kv_dt, kvnd))) return st;
-  const int64_t Hkv = k_cache->shape[kvnd - 2];
-  const int64_t Dk2 = k_cache->shape[kvnd - 1], Dv = v_cache->shape[kvnd - 1];
+  int64_t Hkv, Dk2, Dv, cache_ps = 0;
+  if (vec5) {
+    if (kv_dt == FA_BF16) return fail(FA_ERR_UNSUPPORTED, "the vectorized 5-D layout is accepted for e4m3 and int8 caches");
+    if (k_cache->shape[4] != 16 || v_cache->shape[4] != 16)
+      return fail(FA_ERR_INVALID_ARG, "5-D k/v caches: the last dim holds 16 one-byte elements");
+    Hkv = k_cache->shape[1];
+    Dk2 = k_cache->shape[2] * 16;
+    cache_ps = k_cache->shape[3];
+    Dv = v_cache->shape[3];
+    if (v_cache->shape[1] != Hkv || v_cache->shape[0] != k_cache->shape[0] || v_cache->shape[2] * 16 != cache_ps)
+      return fail(FA_ERR_INVALID_ARG, "5-D k_cache [N_pg, Hkv, Dk/16, P_s, 16] and v_cache [N_pg, Hkv, P_s/16, Dv, 16] disagree");
+  } else {
+    Hkv = k_cache->shape[kvnd - 2];
+    Dk2 = k_cache->shape[kvnd - 1];
+    Dv = v_cache->shape[kvnd - 1];
+    if (paged) cache_ps = k_cache->shape[1];
+    if (v_cache->shape[kvnd - 2] != Hkv) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache disagree on Hkv");
+    for (int i = 0; i < kvnd - 2; ++i)
+      if (v_cache->shape[i] != k_cache->shape[i]) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache shapes disagree");
+  }
   if (Dk2 != Dk) return fail(FA_ERR_INVALID_ARG, "k_cache head dim %lld != q head dim %lld", (long long)Dk2, (long long)Dk);
-  if (v_cache->shape[kvnd - 2] != Hkv) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache disagree on Hkv");
-  for (int i = 0; i < kvnd - 2; ++i)
-    if (v_cache->shape[i] != k_cache->shape[i]) return fail(FA_ERR_INVALID_ARG, "k_cache and v_cache shapes disagree");
   if (Hkv <= 0 || Hq <= 0 || Hq % Hkv) return fail(FA_ERR_INVALID_ARG, "Hq=%lld must be a positive multiple of Hkv=%lld", (long long)Hq, (long long)Hkv);
   if (!supported_dims(Dk, Dv)) return fail(FA_ERR_UNSUPPORTED, "(Dk, Dv) = (%lld, %lld) is not compiled", (long long)Dk, (long long)Dv);
   // e4m3 Q: QK on the e4m3 bytes, which needs e4m3 keys; one head-dim pair.
@@ -487,7 +523,9 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     if (!is_pow2(page_size) || page_size < 1 || page_size > 1024)
       return fail(FA_ERR_UNSUPPORTED, "page_size %d: supported sizes are powers of two from 1 to 1024", page_size);
     if (q8 && page_size < 16) return fail(FA_ERR_UNSUPPORTED, "e4m3 q needs pages of at least 16 keys");
-    if (k_cache->shape[1] != page_size) return fail(FA_ERR_INVALID_ARG, "k_cache.shape[1]=%lld != page_size=%d", (long long)k_cache->shape[1], page_size);
+    if (cache_ps != page_size) return fail(FA_ERR_INVALID_ARG, "the k_cache page holds %lld keys, page_size=%d", (long long)cache_ps, page_size);
+    if (vec5 && page_size < 16) return fail(FA_ERR_UNSUPPORTED, "the vectorized 5-D layout needs pages of at least 16 keys");
+    if (vec5 && q8) return fail(FA_ERR_UNSUPPORTED, "e4m3 q reads keys in the token-major page layout only");
     if ((int64_t)launch->max_seqlen_k > max_pages * page_size) return fail(FA_ERR_INVALID_ARG, "max_seqlen_k exceeds block_table capacity");
     if (n_pages >= (int64_t(1) << 31)) return fail(FA_ERR_OVERFLOW, "num_pages must fit int32");
   }
@@ -507,10 +545,13 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const bool fp8 = kv_dt == FA_E4M3 || kv_dt == FA_I8;
   if (fp8) {
     if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "e4m3 and int8 caches need k_scale and v_scale");
+    // per token and kv head: [N_pg, P_s, Hkv] (paged, either page layout) or [T_k, Hkv]
+    const int snd = paged ? 3 : 2;
+    const int64_t want[3] = {k_cache->shape[0], paged ? cache_ps : Hkv, Hkv};
     for (const fa_tensor_t *s : {k_scale, v_scale}) {
-      if ((st = check_tensor(s, "kv scale", FA_F32, kvnd - 1))) return st;
-      for (int i = 0; i < kvnd - 1; ++i)
-        if (s->shape[i] != k_cache->shape[i]) return fail(FA_ERR_INVALID_ARG, "kv scale shape must be the cache shape without the head dim");
+      if ((st = check_tensor(s, "kv scale", FA_F32, snd))) return st;
+      for (int i = 0; i < snd; ++i)
+        if (s->shape[i] != want[i]) return fail(FA_ERR_INVALID_ARG, "kv scales must be [N_pg, P_s, Hkv] (paged) or [T_k, Hkv]");
       if (!contiguous(s)) return fail(FA_ERR_INVALID_ARG, "kv scales must be contiguous");
     }
   } else if (k_scale || v_scale) {
@@ -543,6 +584,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const bool col_bias = needs_col_bias(fo);
   if (q8 && (fo.bq != 0.0 || fo.bk != 0.0))
     return fail(FA_ERR_UNSUPPORTED, "prologue adds on q or k with e4m3 q");
+  if (vec5 && col_bias) return fail(FA_ERR_UNSUPPORTED, "a prologue q add reads keys in the token-major page layout only");
   float pro_vmul = (float)fo.av, pro_vadd = (float)fo.bv;
   float pro_lse_k = 0.f, pro_lse_c = 0.f, pro_row_k = 0.f, pro_row_c = 0.f, cb_factor = 0.f;
   {
@@ -627,7 +669,11 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     const int rows_box = paged ? (page_size < fa::kDecStageKeys ? page_size : fa::kDecStageKeys) : fa::kDecStageKeys;
     if (have_keys && fp8) {
       // byte caches: one box per page piece, all D bytes of a key, unswizzled
-      if (paged) {
+      if (vec5) {
+        if ((st = make_vec5_maps(&L.tm_k, &L.tm_v, k_cache, v_cache, Dk, Dv, Hkv, page_size, n_pages,
+                                 (uint32_t)rows_box, (uint32_t)(Dk / 16), (uint32_t)Dv, (uint32_t)(rows_box / 16))))
+          return st;
+      } else if (paged) {
         const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
         const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
         const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2]), (uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
@@ -684,6 +730,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.pro_row_c = pro_row_c;
     p.col_bias = col_bias_ptr;
     p.cb_ld = cb_ld;
+    p.vec5 = vec5;
     // the plain score loop has no per-key term: a Q add takes the general
     // path (ALiBi with slope 0)
     p.mod = (mod == 0 && col_bias_ptr) ? 1 : mod;
@@ -762,7 +809,13 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const uint32_t k8_cols = q8 ? 128u : 64u;
   const CUtensorMapSwizzle k8_swz = q8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   if (have_keys && fp8) {
-    if (paged) {
+    if (vec5) {
+      // staged byte rows for the converters: K boxes of 64 columns (4 groups
+      // of 16), V boxes of 64 dims
+      if ((st = make_vec5_maps(&L.tm_k, &L.tm_v, k_cache, v_cache, Dk, Dv, Hkv, page_size, n_pages,
+                               (uint32_t)rows_box8, 4, 64, (uint32_t)(rows_box8 / 16))))
+        return st;
+    } else if (paged) {
       const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)page_size, (uint64_t)n_pages};
       const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
@@ -835,6 +888,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   p.pro_row_c = pro_row_c;
   p.col_bias = col_bias_ptr;
   p.cb_ld = cb_ld;
+  p.vec5 = vec5;
   p.q = (const __nv_bfloat16 *)q->data;
   p.q_stride_t = q->stride[0];
   p.q_stride_h = q->stride[1];

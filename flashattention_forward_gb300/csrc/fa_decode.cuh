@@ -70,6 +70,9 @@ struct DecodeParams {
   float pro_vmul, pro_vadd, pro_lse_k, pro_lse_c, pro_row_k, pro_row_c;
   const float *col_bias;
   int64_t cb_ld;
+  // byte caches in the vectorized 5-D layouts (paged, pages of >= 16 keys):
+  // K [N_pg, Hkv, D/16, P_s, 16], V [N_pg, Hkv, P_s/16, D, 16]
+  int32_t vec5;
   // score mods (0 none, 1 ALiBi, 2 soft-cap) and 128 x 128 block masks, as
   // in the prefill kernels
   int32_t mod;
@@ -385,8 +388,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const int slot = key0 & (p.page_size - 1);
         if constexpr (KV) {
           // one box per page piece: rows_per_box keys x D bytes, unswizzled
+          // (5-D: K as [D/16][rows][16], V as [rows/16][D][16 tokens])
           const uint32_t off = bx * p.rows_per_box * D;
-          if (bt) {
+          if (bt && p.vec5) {
+            tma_load_5d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, slot, 0, hk, pg);
+            tma_load_5d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, 0, slot >> 4, hk, pg);
+          } else if (bt) {
             tma_load_4d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, hk, slot, pg);
             tma_load_4d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, hk, slot, pg);
           } else {
@@ -487,13 +494,18 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       // swizzled buffer, K first and V after the QK product.  Each pass, the
       // 32 lanes read 512 consecutive bytes (16 per lane, no bank conflicts);
       // keys at or past key_hi become zeros (their bytes may be anything).
+      // 5-D K: key kk's 16 bytes from column c0 sit at (kk / R) R D +
+      // (c0 / 16) 16 R + (kk % R) 16 of the stage, R = rows_per_box.
+      const int R = p.rows_per_box;
       auto convert = [&](const uint8_t *src) {
 #pragma unroll
         for (int ps_ = 0; ps_ < D / 32; ++ps_) {
           const int off = ps_ * 512 + lane * 16;
           const int lr = off / D, c0 = off % D;             // key within the 16, first element
           const bool live = key_base + lr < key_hi;
-          const uint4 raw = live ? *reinterpret_cast<const uint4 *>(src + kw0 * D + off) : make_uint4(0, 0, 0, 0);
+          const int kk = kw0 + lr;
+          const uint8_t *at = p.vec5 ? src + (kk / R) * R * D + (c0 >> 4) * 16 * R + (kk % R) * 16 : src + kw0 * D + off;
+          const uint4 raw = live ? *reinterpret_cast<const uint4 *>(at) : make_uint4(0, 0, 0, 0);
           uint32_t h[8];
           dec_bytes4_to_f16<KV>(raw.x, h[0], h[1]);
           dec_bytes4_to_f16<KV>(raw.y, h[2], h[3]);
@@ -622,7 +634,32 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       if constexpr (KV) {
         __syncwarp();                 // the QK product has read K from the buffer
-        convert(vd);
+        if (p.vec5) {
+          // 5-D V: the warp's 16 keys are one token group, [D][16 bytes] at
+          // (kw0 / R) R D + ((kw0 % R) / 16) 16 D of the stage.  Lane (octet
+          // oc, half th) transposes 8 tokens x 8 dims and writes 8 key rows.
+          const uint8_t *gsrc = vd + (kw0 / R) * R * D + ((kw0 % R) >> 4) * 16 * D;
+          const int oc = lane >> 1, th = lane & 1;
+          if (oc < D / 8) {
+            uint2 in[8], tr[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) in[k] = *reinterpret_cast<const uint2 *>(gsrc + (8 * oc + k) * 16 + 8 * th);
+            transpose_8x8_bytes(in, tr);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int lr = 8 * th + t;
+              uint32_t h[4];
+              dec_bytes4_to_f16<KV>(tr[t].x, h[0], h[1]);
+              dec_bytes4_to_f16<KV>(tr[t].y, h[2], h[3]);
+              if (key_base + lr >= key_hi) h[0] = h[1] = h[2] = h[3] = 0u;
+              const int c = 8 * oc, cb = c >> 6, ch = (c & 63) >> 3;
+              *reinterpret_cast<uint4 *>(conv + cb * 16 * 128 + sw128(lr, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+          }
+          __syncwarp();
+        } else {
+          convert(vd);
+        }
         // the stage's bytes and scales are no longer needed by this warp
         if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
       }

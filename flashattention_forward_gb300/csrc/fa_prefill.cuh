@@ -62,6 +62,9 @@ struct PrefillParams {
   // null when there is none
   const float *col_bias;
   int64_t cb_ld;
+  // byte caches in the vectorized 5-D layouts (paged, pages of >= 16 keys):
+  // K [N_pg, Hkv, Dk/16, P_s, 16], V [N_pg, Hkv, P_s/16, Dv, 16]
+  int32_t vec5;
 };
 
 

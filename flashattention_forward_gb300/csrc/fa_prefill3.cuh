@@ -355,11 +355,22 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     // (64 columns) and Q8 key rows (128 e4m3 columns) land swizzled, the MMA
     // operand; staged byte rows (64 columns) land raw in the upper half of
     // their 32-row slice, for the converters.
-    auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int x, int kt, int page, bool staged) {
+    // Vectorized 5-D byte caches (p.vec5): a box of a page piece lands as
+    // [4 column groups][rows][16 bytes] for K and [rows / 16][64 dims][16
+    // tokens] for V, in the same bytes the token-major box fills; the
+    // converters read either form.
+    auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int x, int kt, int page, bool staged,
+                          bool isv) {
       if (!boxer) return;
       const uint32_t at = staged ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64) : smem_u32(dst + r0 * 128);
       if constexpr (PAGED) {
-        tma_load_4d(at, tm, smem_u32(bar), x, pi.hk, (kt * kBlockN + r0) & (p.page_size - 1), page);
+        const int slot = (kt * kBlockN + r0) & (p.page_size - 1);
+        if (FP8 && p.vec5) {
+          if (isv) tma_load_5d(at, tm, smem_u32(bar), 0, x, slot >> 4, pi.hk, page);
+          else tma_load_5d(at, tm, smem_u32(bar), 0, slot, x >> 4, pi.hk, page);
+        } else {
+          tma_load_4d(at, tm, smem_u32(bar), x, pi.hk, slot, page);
+        }
       } else {
         tma_load_3d(at, tm, smem_u32(bar), x, pi.hk, pi.k_row0 + kt * kBlockN + r0);
       }
@@ -473,7 +484,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c * (Q8 ? 128 : 64), kt, page, kStageK);
+        load_block(&tm_k, sK + slot * Cfg::kChunkBytes, bar, c * (Q8 ? 128 : 64), kt, page, kStageK, false);
         if constexpr (Q8) {
           if (c == 0) load_scales(j % Cfg::NSS, kt, kpage);
         }
@@ -489,7 +500,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       if (!ok) break;
 #pragma unroll
       for (int c = 0; c < VC; ++c)
-        load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c * 64, kt, page, FP8);
+        load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c * 64, kt, page, FP8, true);
       kt = kn;
       page = page_next;
       kpage = kpage_next;
@@ -668,33 +679,65 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         ok = mbar_wait(smem_u32(stage_bar), par, abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const uint8_t *stg = base + q * 4096 + 2048;
-        const int part = lane & 3;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int rr = 8 * t + (lane >> 2);              // row within the slice
-          const uint4 raw = *reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16);
-          const float s_row = __shfl_sync(0xffffffffu, sa, rr);
-          const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
-          uint32_t o[8];
+        // e4m3 or int8 bytes times the row's scale -> one 16-byte f16 chunk
+        auto conv16 = [&](uint32_t w0, uint32_t w1, float s, uint32_t (&o)[4]) {
           if constexpr (I8) {
-            i8x4_scaled_f16(raw.x, s_row, o[0], o[1]);
-            i8x4_scaled_f16(raw.y, s_row, o[2], o[3]);
-            i8x4_scaled_f16(raw.z, s_row, o[4], o[5]);
-            i8x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+            i8x4_scaled_f16(w0, s, o[0], o[1]);
+            i8x4_scaled_f16(w1, s, o[2], o[3]);
           } else {
-            e4m3x4_scaled_f16(raw.x, s_row, o[0], o[1]);
-            e4m3x4_scaled_f16(raw.y, s_row, o[2], o[3]);
-            e4m3x4_scaled_f16(raw.z, s_row, o[4], o[5]);
-            e4m3x4_scaled_f16(raw.w, s_row, o[6], o[7]);
+            e4m3x4_scaled_f16(w0, s, o[0], o[1]);
+            e4m3x4_scaled_f16(w1, s, o[2], o[3]);
           }
-          if (!live) {
+        };
+        if (isv && p.vec5) {
+          // 5-D V: the slice's staging is [2 groups of 16 tokens][64 dims]
+          // [16 bytes].  Lane (g, octet oc, half th) takes tokens 16g + 8th
+          // .. +7 of dims 8oc .. 8oc+7, transposes the 8 x 8 bytes and writes
+          // 8 row chunks; every lane reads before any lane writes (the
+          // staging lies in the upper half of the output).
+          const int g = lane >> 4, oc = (lane >> 1) & 7, th = lane & 1;
+          uint2 in[8], tr[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] = 0u;
+          for (int k = 0; k < 8; ++k)
+            in[k] = *reinterpret_cast<const uint2 *>(stg + g * 1024 + (8 * oc + k) * 16 + 8 * th);
+          __syncwarp();
+          transpose_8x8_bytes(in, tr);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int rr = 16 * g + 8 * th + t;            // row within the slice
+            const float s_row = __shfl_sync(0xffffffffu, sa, rr);
+            const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
+            uint32_t o[4];
+            conv16(tr[t].x, tr[t].y, s_row, o);
+            if (!live) o[0] = o[1] = o[2] = o[3] = 0u;
+            const int r = q * 32 + rr;
+            *reinterpret_cast<uint4 *>(base + r * 128 + ((oc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
-          const int r = q * 32 + rr;
-          uint8_t *row = base + r * 128;
-          *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+          const int part = lane & 3;
+          // K staging: token rows of 64 bytes, or with 5-D K per box
+          // [4 groups of 16 columns][rows_per_box][16 bytes]
+          const int R = p.rows_per_box;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int rr = 8 * t + (lane >> 2);              // row within the slice
+            const uint8_t *src = (!isv && p.vec5) ? stg + (rr / R) * 64 * R + part * 16 * R + (rr % R) * 16
+                                                  : stg + rr * 64 + part * 16;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+            const float s_row = __shfl_sync(0xffffffffu, sa, rr);
+            const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
+            uint32_t o[8];
+            conv16(raw.x, raw.y, s_row, *reinterpret_cast<uint32_t(*)[4]>(o));
+            conv16(raw.z, raw.w, s_row, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
+            if (!live) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) o[k] = 0u;
+            }
+            const int r = q * 32 + rr;
+            uint8_t *row = base + r * 128;
+            *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();

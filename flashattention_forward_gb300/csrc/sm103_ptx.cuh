@@ -85,6 +85,38 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+      : "memory");
+}
+
+// 8 x 8 byte transpose: in[k] holds bytes (t = 0..7) of row k; out[t] gets
+// bytes (k = 0..7) of column t.  Four 4 x 4 transposes of byte_perm pairs.
+__device__ __forceinline__ void transpose_8x8_bytes(const uint2 (&in)[8], uint2 (&out)[8]) {
+#pragma unroll
+  for (int hk = 0; hk < 2; ++hk) {         // rows 4hk .. 4hk+3 -> bytes 4hk .. 4hk+3 of every out[t]
+#pragma unroll
+    for (int ht = 0; ht < 2; ++ht) {       // columns 4ht .. 4ht+3
+      const uint32_t p0 = ht ? in[4 * hk + 0].y : in[4 * hk + 0].x;
+      const uint32_t p1 = ht ? in[4 * hk + 1].y : in[4 * hk + 1].x;
+      const uint32_t p2 = ht ? in[4 * hk + 2].y : in[4 * hk + 2].x;
+      const uint32_t p3 = ht ? in[4 * hk + 3].y : in[4 * hk + 3].x;
+      const uint32_t a = __byte_perm(p0, p1, 0x5140), b = __byte_perm(p0, p1, 0x7362);
+      const uint32_t c = __byte_perm(p2, p3, 0x5140), d = __byte_perm(p2, p3, 0x7362);
+      const uint32_t t0 = __byte_perm(a, c, 0x5410), t1 = __byte_perm(a, c, 0x7632);
+      const uint32_t t2 = __byte_perm(b, d, 0x5410), t3 = __byte_perm(b, d, 0x7632);
+      if (hk) {
+        out[4 * ht + 0].y = t0; out[4 * ht + 1].y = t1; out[4 * ht + 2].y = t2; out[4 * ht + 3].y = t3;
+      } else {
+        out[4 * ht + 0].x = t0; out[4 * ht + 1].x = t1; out[4 * ht + 2].x = t2; out[4 * ht + 3].x = t3;
+      }
+    }
+  }
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

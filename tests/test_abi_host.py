@@ -361,3 +361,46 @@ def test_bwd_validation_rejects_before_launch(L, over, status, words):
     st, msg = _bcall(L, **over)
     assert st == status, msg
     assert words in msg, msg
+
+
+def test_vec5_limits(L):
+    """The vectorized 5-D pages are accepted for e4m3 and int8 caches with
+    pages of >= 16 keys and bf16 q; other combinations fail before launch."""
+    T, H = 256, 4
+    q = _t(FAKE, fa.FA_BF16, [T, H, 128])
+    out = _t(FAKE * 6, fa.FA_BF16, [T, H, 128])
+    bt = _t(FAKE * 10, fa.FA_I32, [2, 8])
+    ks = _t(FAKE * 8, fa.FA_F32, [32, 16, H])
+    vs = _t(FAKE * 9, fa.FA_F32, [32, 16, H])
+    k5 = _t(FAKE * 2, fa.FA_E4M3, [32, H, 8, 16, 16])
+    v5 = _t(FAKE * 3, fa.FA_E4M3, [32, H, 1, 128, 16])
+    lau = fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=T, total_k=0)
+    st, msg = _call(L, q=q, k=_t(FAKE * 2, fa.FA_BF16, [32, H, 16, 16, 8]), v=_t(FAKE * 3, fa.FA_BF16, [32, H, 2, 128, 8]),
+                    bt=bt, page=16, out=out, launch=lau)
+    assert st == fa.FA_ERR_UNSUPPORTED and "5-D" in msg
+    st, msg = _call(L, q=q, k=k5, v=_t(FAKE * 3, fa.FA_E4M3, [32, H, 2, 128, 16]), ks=ks, vs=vs, bt=bt, page=16,
+                    out=out, launch=lau)
+    assert st == fa.FA_ERR_INVALID_ARG and "disagree" in msg
+    st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 128]), k=k5, v=v5, ks=ks, vs=vs, bt=bt, page=16, out=out,
+                    launch=lau)
+    assert st == fa.FA_ERR_UNSUPPORTED and "token-major" in msg
+    st, msg = _call(L, q=q, k=k5, v=v5, ks=_t(FAKE * 8, fa.FA_F32, [32, H, 16]), vs=vs, bt=bt, page=16, out=out,
+                    launch=lau)
+    assert st == fa.FA_ERR_INVALID_ARG and "[N_pg, P_s, Hkv]" in msg
+
+
+def test_vectorize_pages_inverts_with_the_pages_permutes():
+    """fa_inputs.vectorize_pages builds the 5-D K [N_pg, Hkv, Dk/16, P_s, 16]
+    and V [N_pg, Hkv, P_s/16, Dv, 16]; the permutes (0, 3, 1, 2, 4) and
+    (0, 2, 4, 1, 3) (FlyDSL PR #1066, review) give the token-major pages back."""
+    import numpy as np
+    import fa_inputs as fi
+    p = fi.make_problem([40, 70], [100, 70], hq=4, hkv=2, dk=192, dv=128, seed=3, page_size=32, kv_dtype="e4m3",
+                        spare_pages=2)
+    k5, v5 = fi.vectorize_pages(p.k, p.v)
+    assert k5.shape == (p.k.shape[0], 2, 12, 32, 16) and v5.shape == (p.v.shape[0], 2, 2, 128, 16)
+    assert np.array_equal(k5.transpose(0, 3, 1, 2, 4).reshape(p.k.shape), p.k)
+    assert np.array_equal(v5.transpose(0, 2, 4, 1, 3).reshape(p.v.shape), p.v)
+    # element (page, slot, head, d) of K sits at [page, head, d // 16, slot, d % 16]
+    assert k5[3, 1, 5, 7, 9] == p.k[3, 7, 1, 5 * 16 + 9]
+    assert v5[2, 0, 1, 100, 3] == p.v[2, 16 + 3, 0, 100]
