@@ -716,14 +716,26 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         } else {
           const int part = lane & 3;
           // K staging: token rows of 64 bytes, or with 5-D K per box
-          // [4 groups of 16 columns][rows_per_box][16 bytes]
+          // [4 groups of 16 columns][rows_per_box][16 bytes].  Token rows
+          // are read and written step by step: the staging rows a step
+          // overwrites were read in earlier steps.  The 5-D order spreads a
+          // row's bytes over the whole staging half, so there every lane
+          // reads all four of its pieces before the warp writes any.
           const int R = p.rows_per_box;
+          const bool k5 = !isv && p.vec5;
+          uint4 pre[4];
+          if (k5) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int rr = 8 * t + (lane >> 2);
+              pre[t] = *reinterpret_cast<const uint4 *>(stg + (rr / R) * 64 * R + part * 16 * R + (rr % R) * 16);
+            }
+            __syncwarp();
+          }
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int rr = 8 * t + (lane >> 2);              // row within the slice
-            const uint8_t *src = (!isv && p.vec5) ? stg + (rr / R) * 64 * R + part * 16 * R + (rr % R) * 16
-                                                  : stg + rr * 64 + part * 16;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+            const uint4 raw = k5 ? pre[t] : *reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16);
             const float s_row = __shfl_sync(0xffffffffu, sa, rr);
             const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
             uint32_t o[8];
