@@ -716,6 +716,8 @@ def compact_summary(runs, extra, pk):
            "paged_decode_int8_64seq_hq32_hkv8_p16": "c3_int8", "paged_fp8_d192_v128_16seq_h16_p64_causal": "c4",
            "paged_fp8kv_qe4m3_d128_16seq_h16_p64_causal": "c4_q8_d128",
            "paged_fp8kv_qe4m3_d192_v128_16seq_h16_p64_causal": "c4_q8",
+           "paged_fp8_d192_v128_16seq_h16_p64_causal_vec5": "c4_vec5",
+           "paged_decode_e4m3_64seq_hq32_hkv8_p16_vec5": "c3_e4m3_vec5",
            "bwd_4x4096_h16_d128_noncausal": "bwd_4x4096"}
     for name, short in key.items():
         v = extra.get(name)
@@ -812,6 +814,16 @@ def other_workloads(dev, warmup, steps, flush, pk):
         res[f"paged_decode_{kvd}_64seq_hq32_hkv8_p16"] = {
             "ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"], "bytes": fi.decode_bytes(p),
             "num_splits": fa.default_splits(p.num_seqs, 1, p.max_seqlen_k, 32, 8, 16, p.total_k)}
+        # the same cache in the vectorized 5-D pages
+        k5, v5 = fi.vectorize_pages(p.k.view(np.uint8), p.v.view(np.uint8))
+        kvt = torch.int8 if kvd == "int8" else torch.float8_e4m3fn
+        t["k"] = torch.from_numpy(k5).view(kvt).to(dev)
+        t["v"] = torch.from_numpy(v5).view(kvt).to(dev)
+        call, n, _, _ = make_call(p, t, num_splits=None)
+        ms = statistics.mean(time_calls([call], warmup, steps, flush))
+        gbs = fi.decode_bytes(p) / (ms * 1e-3) / 1e9
+        res[f"paged_decode_{kvd}_64seq_hq32_hkv8_p16_vec5"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm"],
+                                                               "bytes": fi.decode_bytes(p)}
         del t
     # paged e4m3 KV, Q/K 192, V/O 128, page 64, 16 seqs U{1..4096}, causal
     p = fi.config4()
@@ -824,6 +836,18 @@ def other_workloads(dev, warmup, steps, flush, pk):
                                                         "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
                                                         "gflop": fl / 1e9}
     del t
+    # the same tokens in the vectorized 5-D pages (K [N_pg, Hkv, Dk/16, P_s,
+    # 16], V [N_pg, Hkv, P_s/16, Dv, 16]; bit-identical results)
+    k5, v5 = fi.vectorize_pages(p.k.view(np.uint8), p.v.view(np.uint8))
+    t5 = dev_tensors(p, dev)
+    t5["k"] = torch.from_numpy(k5).view(torch.float8_e4m3fn).to(dev)
+    t5["v"] = torch.from_numpy(v5).view(torch.float8_e4m3fn).to(dev)
+    call, _, _, _ = make_call(p, t5, num_splits=0)
+    ms = statistics.mean(time_calls([call], warmup, steps, flush))
+    res["paged_fp8_d192_v128_16seq_h16_p64_causal_vec5"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                                            "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+                                                            "gflop": fl / 1e9}
+    del t5
     # the same tokens one key per page (rows gathered by cp.async, no TMA boxes)
     lens4 = [int(x) for x in np.diff(p.cu_seqlens_q)]
     p1 = fi.make_problem(lens4, hq=16, hkv=16, dk=192, dv=128, seed=1, page_size=1, spare_pages=16,
