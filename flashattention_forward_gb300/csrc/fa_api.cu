@@ -585,6 +585,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   if (q8 && (fo.bq != 0.0 || fo.bk != 0.0))
     return fail(FA_ERR_UNSUPPORTED, "prologue adds on q or k with e4m3 q");
   if (vec5 && col_bias) return fail(FA_ERR_UNSUPPORTED, "a prologue q add reads keys in the token-major page layout only");
+  if (vec5 && mod == 2 && fo.bk != 0.0)
+    return fail(FA_ERR_UNSUPPORTED, "a prologue k add under the soft-cap is not taken with the vectorized 5-D pages");
   float pro_vmul = (float)fo.av, pro_vadd = (float)fo.bv;
   float pro_lse_k = 0.f, pro_lse_c = 0.f, pro_row_k = 0.f, pro_row_c = 0.f, cb_factor = 0.f;
   {

@@ -3,10 +3,10 @@
 
 namespace fa {
 
-template <int D, int KV>
+template <int D, int KV, bool V5>
 static cudaError_t launch_decode_d(const DecodeLaunch &L) {
   static unsigned long long done = 0;
-  auto kern = fa_decode_kernel<D, KV>;
+  auto kern = fa_decode_kernel<D, KV, V5>;
   cudaError_t e = ensure_smem_attr(kern, DecodeCfg<D, KV>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, kDecThreads, DecodeCfg<D, KV>::kSmemBytes, L.stream>>>(L.tm_k, L.tm_v, L.p);
@@ -15,8 +15,15 @@ static cudaError_t launch_decode_d(const DecodeLaunch &L) {
 
 template <int KV>
 static cudaError_t launch_decode_kv(int d, const DecodeLaunch &L) {
-  if (d == 64) return launch_decode_d<64, KV>(L);
-  if (d == 128) return launch_decode_d<128, KV>(L);
+  if constexpr (KV != 0) {
+    if (L.p.vec5) {
+      if (d == 64) return launch_decode_d<64, KV, true>(L);
+      if (d == 128) return launch_decode_d<128, KV, true>(L);
+      return cudaErrorNotSupported;
+    }
+  }
+  if (d == 64) return launch_decode_d<64, KV, false>(L);
+  if (d == 128) return launch_decode_d<128, KV, false>(L);
   return cudaErrorNotSupported;
 }
 

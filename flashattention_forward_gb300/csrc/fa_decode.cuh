@@ -166,7 +166,9 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D, int KV = 0>
+// V5: byte caches in the vectorized 5-D pages (a kernel of its own, so that
+// the token-major kernels keep their register allocation).
+template <int D, int KV = 0, bool V5 = false>
 __global__ void __launch_bounds__(kDecThreads, 2)
     fa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p) {
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           // one box per page piece: rows_per_box keys x D bytes, unswizzled
           // (5-D: K as [D/16][rows][16], V as [rows/16][D][16 tokens])
           const uint32_t off = bx * p.rows_per_box * D;
-          if (bt && p.vec5) {
+          if (V5) {
             tma_load_5d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, slot, 0, hk, pg);
             tma_load_5d(smem_u32(vd + off), &tm_v, smem_u32(full + slot_i), 0, 0, slot >> 4, hk, pg);
           } else if (bt) {
@@ -479,6 +481,24 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
+    // Byte caches: stage offsets of the lane's 16-byte pieces, one per pass
+    // (see convert below) -- token rows of D bytes, and K in the vectorized
+    // 5-D pages, where key kk's bytes from column c0 sit at (kk / R) R D +
+    // (c0 / 16) 16 R + (kk % R) 16, R = rows_per_box (a power of two).
+    // 5-D V: the warp's 16 keys are one token group, [D][16 bytes] at
+    // (kw / R) R D + ((kw % R) / 16) 16 D of the stage (kw = the warp's first key).
+    int koff[D / 32], voff[D / 32], v5off;
+    {
+      const int R = p.rows_per_box, lg = __ffs(R) - 1, kw = warp * 16;
+      v5off = ((kw >> lg) << lg) * D + ((kw & (R - 1)) >> 4) * 16 * D;
+#pragma unroll
+      for (int ps_ = 0; ps_ < D / 32; ++ps_) {
+        const int off = ps_ * 512 + lane * 16;
+        const int kk = kw + off / D, c0 = off % D;
+        voff[ps_] = kw * D + off;
+        koff[ps_] = V5 ? ((kk >> lg) << lg) * D + ((c0 >> 4) << (4 + lg)) + ((kk & (R - 1)) << 4) : voff[ps_];
+      }
+    }
     bool ok = true;
     for (int st = first_stage; st < n_stages; ++st) {
       const int it = st - first_stage;
@@ -494,18 +514,13 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       // swizzled buffer, K first and V after the QK product.  Each pass, the
       // 32 lanes read 512 consecutive bytes (16 per lane, no bank conflicts);
       // keys at or past key_hi become zeros (their bytes may be anything).
-      // 5-D K: key kk's 16 bytes from column c0 sit at (kk / R) R D +
-      // (c0 / 16) 16 R + (kk % R) 16 of the stage, R = rows_per_box.
-      const int R = p.rows_per_box;
-      auto convert = [&](const uint8_t *src) {
+      auto convert = [&](const uint8_t *src, const int (&offs)[D / 32]) {
 #pragma unroll
         for (int ps_ = 0; ps_ < D / 32; ++ps_) {
           const int off = ps_ * 512 + lane * 16;
           const int lr = off / D, c0 = off % D;             // key within the 16, first element
           const bool live = key_base + lr < key_hi;
-          const int kk = kw0 + lr;
-          const uint8_t *at = p.vec5 ? src + (kk / R) * R * D + (c0 >> 4) * 16 * R + (kk % R) * 16 : src + kw0 * D + off;
-          const uint4 raw = live ? *reinterpret_cast<const uint4 *>(at) : make_uint4(0, 0, 0, 0);
+          const uint4 raw = live ? *reinterpret_cast<const uint4 *>(src + offs[ps_]) : make_uint4(0, 0, 0, 0);
           uint32_t h[8];
           dec_bytes4_to_f16<KV>(raw.x, h[0], h[1]);
           dec_bytes4_to_f16<KV>(raw.y, h[2], h[3]);
@@ -522,7 +537,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         __syncwarp();
       };
       if constexpr (KV) {
-        convert(kd);
+        convert(kd, koff);
         const float *sct = reinterpret_cast<const float *>(vd + Cfg::kVBytes);
 #pragma unroll
         for (int n = 0; n < 2; ++n)
@@ -634,11 +649,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       if constexpr (KV) {
         __syncwarp();                 // the QK product has read K from the buffer
-        if (p.vec5) {
-          // 5-D V: the warp's 16 keys are one token group, [D][16 bytes] at
-          // (kw0 / R) R D + ((kw0 % R) / 16) 16 D of the stage.  Lane (octet
-          // oc, half th) transposes 8 tokens x 8 dims and writes 8 key rows.
-          const uint8_t *gsrc = vd + (kw0 / R) * R * D + ((kw0 % R) >> 4) * 16 * D;
+        if constexpr (V5) {
+          // 5-D V (the token group at v5off): lane (octet oc, half th)
+          // transposes 8 tokens x 8 dims and writes 8 key rows.
+          const uint8_t *gsrc = vd + v5off;
           const int oc = lane >> 1, th = lane & 1;
           if (oc < D / 8) {
             uint2 in[8], tr[8];
@@ -658,7 +672,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           }
           __syncwarp();
         } else {
-          convert(vd);
+          convert(vd, voff);
         }
         // the stage's bytes and scales are no longer needed by this warp
         if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));

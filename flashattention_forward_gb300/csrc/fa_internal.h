@@ -77,6 +77,10 @@ cudaError_t launch_prefill_192_128_q8(const PrefillLaunch &L);
 cudaError_t launch_prefill2_kt(int d, const PrefillLaunch &L);
 cudaError_t launch_prefill3_kt(int dk, bool fp8, const PrefillLaunch &L);
 cudaError_t launch_prefill3_kt_i8(int dk, const PrefillLaunch &L);
+// Chunked-ring kernels for byte caches in the vectorized 5-D page layouts
+// (MOD 0-2), in translation units of their own.
+cudaError_t launch_prefill3_vec5(int dk, bool i8, const PrefillLaunch &L);
+cudaError_t launch_prefill3_vec5_i8(int dk, const PrefillLaunch &L);
 cudaError_t launch_decode(int d, const DecodeLaunch &L);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
                            int dv, void *out, float *lse, cudaStream_t stream);

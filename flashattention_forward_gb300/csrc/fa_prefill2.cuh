@@ -495,24 +495,52 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
       // Scores of 32 keys starting at key jc, in scaled log2 units (the fast
       // path keeps raw scores and folds the scale into the exponent's FMA).
       auto scores = [&](float (&v)[32], int jc) {
-        if (!fast) {
-          const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
-          const float c2u = 2.f * kLog2e * p.softcap_arg;   // soft-cap: raw score -> 2u log2(e)
+        if constexpr (MK == 2) {
+          // Soft-cap: each step runs over the whole chunk before the next,
+          // with packed pairs, so that the 32 independent chains of its two
+          // transcendental steps interleave.
+          const float c2u = 2.f * kLog2e * p.softcap_arg;   // raw score -> 2u log2(e)
           if constexpr (KT) {
-            // scaled score (log2 units; soft-cap: its argument 2u log2(e))
-            // plus the row term (soft-cap) and the key's term; no term is
-            // read past cb_ld (the pre-pass flags such keys)
-            const float lin = MK == 2 ? c2u : p.scale_log2;
+            // plus the row term and the key's term (in the same units); no
+            // term is read past cb_ld (the pre-pass flags such keys)
             const bool in_ld = p.col_bias != nullptr && jc + 32 <= p.cb_ld;
             const float4 *c4 =
                 reinterpret_cast<const float4 *>(p.col_bias + ((int64_t)pi.b * p.hkv + pi.hk) * p.cb_ld + jc);
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
               const float4 c = in_ld ? c4[e >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
-              v[e] = fmaf(v[e], lin, c.x + row_term);
-              v[e + 1] = fmaf(v[e + 1], lin, c.y + row_term);
-              v[e + 2] = fmaf(v[e + 2], lin, c.z + row_term);
-              v[e + 3] = fmaf(v[e + 3], lin, c.w + row_term);
+              fma2v(v[e], v[e + 1], c2u, c.x + row_term, c.y + row_term);
+              fma2v(v[e + 2], v[e + 3], c2u, c.z + row_term, c.w + row_term);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) mul2(v[e], v[e + 1], c2u);
+          }
+          // cl tanh(u) = cl - 2 cl / (1 + e^{2u})  (see softcap_log2_score)
+          const float cl = p.softcap_log2;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = ex2(v[e]);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) add2(v[e], v[e + 1], 1.f, 1.f);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = rcp_approx(v[e]);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) fma2(v[e], v[e + 1], v[e], v[e + 1], -2.f * cl, cl);
+        } else if constexpr (!fast) {
+          const float dbase = (float)(ip - jc);   // ALiBi: |i' - j| = |dbase - e|, exact in fp32
+          if constexpr (KT) {
+            // scaled score (log2 units) plus the key's term; no term is read
+            // past cb_ld (the pre-pass flags such keys)
+            const bool in_ld = p.col_bias != nullptr && jc + 32 <= p.cb_ld;
+            const float4 *c4 =
+                reinterpret_cast<const float4 *>(p.col_bias + ((int64_t)pi.b * p.hkv + pi.hk) * p.cb_ld + jc);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 c = in_ld ? c4[e >> 2] : make_float4(0.f, 0.f, 0.f, 0.f);
+              v[e] = fmaf(v[e], p.scale_log2, c.x + row_term);
+              v[e + 1] = fmaf(v[e + 1], p.scale_log2, c.y + row_term);
+              v[e + 2] = fmaf(v[e + 2], p.scale_log2, c.z + row_term);
+              v[e + 3] = fmaf(v[e + 3], p.scale_log2, c.w + row_term);
             }
           }
 #pragma unroll
@@ -520,16 +548,10 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
             float x;
             if constexpr (KT) {
               x = v[e];
-            } else if constexpr (MK == 2) {
-              x = v[e] * c2u;
             } else {
               x = v[e] * p.scale_log2;
             }
-            if constexpr (MK == 2) {
-              float r;
-              x = softcap_log2_score(ex2(x), p.softcap_log2, r);
-            }
-            if constexpr (MK == 1) x -= p.alibi_log2 * fabsf(dbase - (float)e);
+            x -= p.alibi_log2 * fabsf(dbase - (float)e);
             v[e] = x;
           }
         }

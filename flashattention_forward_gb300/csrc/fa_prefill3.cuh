@@ -179,11 +179,15 @@ __device__ __forceinline__ void i8x4_scaled_f16(uint32_t w, float s, uint32_t &o
 
 // I8 (with FP8): the byte cache holds int8 values instead of e4m3.
 // Q8 (with FP8, not I8): Q is e4m3 too and QK runs on the e4m3 bytes.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8 = false>
+// V5 (with FP8 and PAGED, not Q8): the pages are in the vectorized 5-D
+// layouts; kernels of their own, so that the token-major kernels carry none
+// of the 5-D code.
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8 = false, bool V5 = false>
 __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>::kThreads, 1)
     fa_prefill3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
+  static_assert(!V5 || (FP8 && PAGED && !Q8), "5-D pages: paged byte caches with bf16 Q");
   // MOD: 0 plain scores, 1 ALiBi, 2 soft-cap; 3 and 4 are 1 and 2 with the
   // prologue's score terms (KT): a Q add's per-key term and, under the
   // soft-cap, the row term of a K add
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     // (64 columns) and Q8 key rows (128 e4m3 columns) land swizzled, the MMA
     // operand; staged byte rows (64 columns) land raw in the upper half of
     // their 32-row slice, for the converters.
-    // Vectorized 5-D byte caches (p.vec5): a box of a page piece lands as
+    // Vectorized 5-D byte caches (V5): a box of a page piece lands as
     // [4 column groups][rows][16 bytes] for K and [rows / 16][64 dims][16
     // tokens] for V, in the same bytes the token-major box fills; the
     // converters read either form.
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       const uint32_t at = staged ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64) : smem_u32(dst + r0 * 128);
       if constexpr (PAGED) {
         const int slot = (kt * kBlockN + r0) & (p.page_size - 1);
-        if (FP8 && p.vec5) {
+        if constexpr (V5) {
           if (isv) tma_load_5d(at, tm, smem_u32(bar), 0, x, slot >> 4, pi.hk, page);
           else tma_load_5d(at, tm, smem_u32(bar), 0, slot, x >> 4, pi.hk, page);
         } else {
@@ -689,7 +693,33 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
             e4m3x4_scaled_f16(w1, s, o[2], o[3]);
           }
         };
-        if (isv && p.vec5) {
+        const int part = lane & 3;
+        // one staged row piece (16 bytes, row rr of the slice) -> 16 f16
+        // values of row q * 32 + rr, zeros past the sequence end
+        auto put_row = [&](const uint4 raw, int rr) {
+          const float s_row = __shfl_sync(0xffffffffu, sa, rr);
+          const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
+          uint32_t o[8];
+          conv16(raw.x, raw.y, s_row, *reinterpret_cast<uint32_t(*)[4]>(o));
+          conv16(raw.z, raw.w, s_row, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
+          if (!live) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = 0u;
+          }
+          const int r = q * 32 + rr;
+          uint8_t *row = base + r * 128;
+          *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        };
+        if constexpr (!V5) {
+          // Token rows of 64 bytes, read and written step by step: the
+          // staging rows a step overwrites were read in earlier steps.
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int rr = 8 * t + (lane >> 2);              // row within the slice
+            put_row(*reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16), rr);
+          }
+        } else if (isv) {
           // 5-D V: the slice's staging is [2 groups of 16 tokens][64 dims]
           // [16 bytes].  Lane (g, octet oc, half th) takes tokens 16g + 8th
           // .. +7 of dims 8oc .. 8oc+7, transposes the 8 x 8 bytes and writes
@@ -714,42 +744,21 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
             *reinterpret_cast<uint4 *>(base + r * 128 + ((oc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         } else {
-          const int part = lane & 3;
-          // K staging: token rows of 64 bytes, or with 5-D K per box
-          // [4 groups of 16 columns][rows_per_box][16 bytes].  Token rows
-          // are read and written step by step: the staging rows a step
-          // overwrites were read in earlier steps.  The 5-D order spreads a
-          // row's bytes over the whole staging half, so there every lane
-          // reads all four of its pieces before the warp writes any.
-          const int R = p.rows_per_box;
-          const bool k5 = !isv && p.vec5;
-          uint4 pre[4];
-          if (k5) {
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int rr = 8 * t + (lane >> 2);
-              pre[t] = *reinterpret_cast<const uint4 *>(stg + (rr / R) * 64 * R + part * 16 * R + (rr % R) * 16);
-            }
-            __syncwarp();
-          }
+          // 5-D K: a box of R = rows_per_box rows (a power of two) lands as
+          // [4 column groups][R rows][16 bytes], which spreads a row's bytes
+          // over the whole staging half, so every lane reads its four pieces
+          // before the warp writes any.
+          const int R = p.rows_per_box, lg = __ffs(R) - 1;
+          uint4 raw[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const int rr = 8 * t + (lane >> 2);              // row within the slice
-            const uint4 raw = k5 ? pre[t] : *reinterpret_cast<const uint4 *>(stg + rr * 64 + part * 16);
-            const float s_row = __shfl_sync(0xffffffffu, sa, rr);
-            const bool live = kt * kBlockN + q * 32 + rr < pi.sk;
-            uint32_t o[8];
-            conv16(raw.x, raw.y, s_row, *reinterpret_cast<uint32_t(*)[4]>(o));
-            conv16(raw.z, raw.w, s_row, *reinterpret_cast<uint32_t(*)[4]>(o + 4));
-            if (!live) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) o[k] = 0u;
-            }
-            const int r = q * 32 + rr;
-            uint8_t *row = base + r * 128;
-            *reinterpret_cast<uint4 *>(row + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4 *>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            const int rr = 8 * t + (lane >> 2);
+            raw[t] = *reinterpret_cast<const uint4 *>(stg + ((rr >> lg) << (6 + lg)) + (part << (4 + lg)) +
+                                                      ((rr & (R - 1)) << 4));
           }
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < 4; ++t) put_row(raw[t], 8 * t + (lane >> 2));
         }
         fence_proxy_async_smem();
         __syncwarp();

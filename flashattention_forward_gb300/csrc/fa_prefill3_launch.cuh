@@ -10,14 +10,14 @@ namespace fa {
 // A register-split variant raises the softmax warps with setmaxnreg.inc,
 // which waits until other warps of the CTA release registers: it may run only
 // when the compiled launch register count covers the whole split.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false>
 bool prefill3_split_fits() {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
   if constexpr (!Cfg::kSplitRegs) return true;
   static int verdict = -1;   // per process: all devices run the same binary
   if (verdict < 0) {
     cudaFuncAttributes a;
-    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8>) == cudaSuccess &&
+    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5>) == cudaSuccess &&
                a.numRegs * Cfg::kThreads >= Cfg::kPoolNeeded)
                   ? 1
                   : 0;
@@ -25,12 +25,12 @@ bool prefill3_split_fits() {
   return verdict == 1;
 }
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false>
 cudaError_t launch_prefill3_one(const PrefillLaunch &L) {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
-  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8>()) return cudaErrorNotSupported;
+  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5>()) return cudaErrorNotSupported;
   static unsigned long long done = 0;
-  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8>;
+  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
@@ -56,6 +56,9 @@ cudaError_t launch_prefill3_pick(const PrefillLaunch &L) {
 // Q8) are instantiated in translation units of their own.
 template <int DK, int DV, bool FP8, bool I8 = false, bool Q8 = false>
 cudaError_t launch_prefill3(const PrefillLaunch &L) {
+  if constexpr (FP8 && !Q8) {
+    if (L.p.vec5) return launch_prefill3_vec5(DK, I8, L);
+  }
   if (L.mod >= 3) {
     if (Q8) return cudaErrorInvalidValue;
     return I8 ? launch_prefill3_kt_i8(DK, L) : launch_prefill3_kt(DK, FP8, L);
@@ -69,6 +72,18 @@ cudaError_t launch_prefill3(const PrefillLaunch &L) {
     }
   };
   return L.paged ? by_mod(std::true_type{}) : by_mod(std::false_type{});
+}
+
+// The 5-D page kernels of one (Dk, Dv, cache) combination (MOD 0-2; the
+// host takes no prologue score terms with 5-D pages).
+template <int DK, int DV, bool I8>
+cudaError_t launch_prefill3_vec5_one(const PrefillLaunch &L) {
+  switch (L.mod) {
+    case 0: return launch_prefill3_one<DK, DV, true, true, 0, false, I8, false, true>(L);
+    case 1: return launch_prefill3_one<DK, DV, true, true, 1, false, I8, false, true>(L);
+    case 2: return launch_prefill3_one<DK, DV, true, true, 2, false, I8, false, true>(L);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // The MOD 3 and 4 kernels of one (Dk, Dv, cache) combination.

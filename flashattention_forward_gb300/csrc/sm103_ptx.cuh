@@ -298,6 +298,21 @@ __device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
       : "+f"(a0), "+f"(a1)
       : "f"(b0), "f"(b1));
 }
+// d = a * b on two lanes, and d = a * b + c with a separate addend per lane.
+__device__ __forceinline__ void mul2(float &a0, float &a1, float b) {
+  asm("{\n\t.reg .b64 x, y, r;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %2};\n\t"
+      "mul.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b));
+}
+__device__ __forceinline__ void fma2v(float &a0, float &a1, float b, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z, r;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %2};\n\tmov.b64 z, {%3, %4};\n\t"
+      "fma.rn.f32x2 r, x, y, z;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b), "f"(c0), "f"(c1));
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -165,6 +165,14 @@ typedef struct {
  *  k_cache      paged: [N_pg, P_s, Hkv, Dk]; packed (block_table NULL):
  *               [T_k, Hkv, Dk].  bf16, e4m3 or int8.  Last three dims contiguous.
  *  v_cache      same layout and dtype with Dv (Dv may differ from Dk).
+ *               Paged e4m3 and int8 caches may instead come in the
+ *               vectorized 5-D layouts (FlyDSL PR #1066, Technical Details
+ *               and review): K [N_pg, Hkv, Dk/16, P_s, 16] and V [N_pg, Hkv,
+ *               P_s/16, Dv, 16], contiguous, 16 one-byte elements in the last
+ *               dim, with pages of >= 16 keys and k_scale/v_scale
+ *               [N_pg, P_s, Hkv]; results are bit-identical to the
+ *               token-major pages.  Not with e4m3 q, a prologue add on q, or
+ *               an add on k under the soft-cap (FA_ERR_UNSUPPORTED).
  *  block_table  int32 [num_seqs, max_pages], or NULL for packed K/V.  Entries
  *               for pages past a sequence's length are never read.
  *  cu_seqlens_q int32 [num_seqs + 1], prefix sums of query lengths.

@@ -387,6 +387,14 @@ def test_vec5_limits(L):
     st, msg = _call(L, q=q, k=k5, v=v5, ks=_t(FAKE * 8, fa.FA_F32, [32, H, 16]), vs=vs, bt=bt, page=16, out=out,
                     launch=lau)
     assert st == fa.FA_ERR_INVALID_ARG and "[N_pg, P_s, Hkv]" in msg
+    # prologue adds that need key sums or the row term under the cap
+    st, msg = _call(L, q=q, k=k5, v=v5, ks=ks, vs=vs, bt=bt, page=16, out=out, launch=lau,
+                    pro=fa.make_prologue({"q": [("add", 0.5)]}))
+    assert st == fa.FA_ERR_UNSUPPORTED and "token-major" in msg
+    cap = fa.ScoreMod(kind=fa.MOD_SOFTCAP, alibi_slope=0.0, softcap=20.0)
+    st, msg = _call(L, q=q, k=k5, v=v5, ks=ks, vs=vs, bt=bt, page=16, out=out, launch=lau, mod=cap,
+                    pro=fa.make_prologue({"k": [("add", 0.5)]}))
+    assert st == fa.FA_ERR_UNSUPPORTED and "5-D" in msg
 
 
 def test_vectorize_pages_inverts_with_the_pages_permutes():
