@@ -1,6 +1,7 @@
 // fa_api.cu -- the C ABI declared in include/fa_gb300.h: host-side validation,
 // TMA descriptor encoding and variant dispatch.  Every check runs on the host
 // before anything is enqueued; no device memory is read back or allocated.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -159,15 +160,40 @@ fa_status_t check_mods(const fa_score_mod_t *score_mod, const fa_block_mask_t *b
 }
 
 // The bf16 prefill runs its register-rebalanced one-pass softmax when the
-// build's launch registers allow it; FA_GB300_PREFILL_VARIANT=1 in the
-// environment at the first forward call of the process selects the 10-warp
-// two-pass form instead (a diagnosis switch; results agree to rounding).
+// build's launch registers allow it, with two query tiles per CTA or one
+// (two CTAs per SM) as tiles_per_cta() picks.  FA_GB300_PREFILL_VARIANT in
+// the environment at the first forward call of the process overrides that
+// (a diagnosis switch; results agree to rounding): 1 selects the 10-warp
+// two-pass form, 2 one tile per CTA wherever it exists, 3 two tiles.
 int prefill_variant() {
   static const int v = [] {
     const char *e = getenv("FA_GB300_PREFILL_VARIANT");
-    return (e && e[0] == '1') ? 1 : 0;
+    return (e && e[0] >= '1' && e[0] <= '3') ? e[0] - '0' : 0;
   }();
   return v;
+}
+
+// Query tiles per CTA of the bf16 ping-pong prefill.  One tile per CTA lets
+// two CTAs share an SM, so that each CTA's set-up, pipeline fill and
+// epilogue overlap the other's main loop, and each CTA walks only its own
+// tile's key tiles (a two-tile CTA walks the union of both tiles' lists).
+// Measured on one GB300 (one tile against two): config-5 window run +25%,
+// 50% block mask +26%, soft-cap +3-4%, ALiBi causal +2%, config-2 lengths
+// +4% (+10% causal); long dense plain runs -3% and ALiBi non-causal -4%
+// (one-tile CTAs reload K/V twice as often); a grid of a few CTAs is
+// faster with two tiles.
+struct TileHints {
+  double avg_key_tiles;   // key tiles a query tile visits, on average
+  double n_tiles;         // query tiles x heads, about
+  bool block_mask, causal, window;
+  int mod;                // 0 plain, 1 ALiBi, 2 soft-cap
+};
+int tiles_per_cta(bool eligible, int variant, const TileHints &h) {
+  if (!eligible || variant == 1 || variant == 3) return 2;
+  if (variant == 2) return 1;
+  if (h.n_tiles <= 64) return 2;
+  if (h.block_mask || h.window || h.mod == 2 || h.avg_key_tiles <= 8.0 || (h.mod == 1 && h.causal)) return 1;
+  return 2;
 }
 
 // Byte geometry of a paged cache [N_pg, P_s, Hkv, D] for the row gather.
@@ -782,8 +808,29 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   }
 
   // ------------------------------------------------------------ prefill --
-  // Every prefill kernel computes two 128-row query tiles per CTA.
-  const int64_t rows_per_cta = 2 * fa::kBlockM;
+  // Prefill kernels compute two 128-row query tiles per CTA, except the bf16
+  // ping-pong kernel's one-tile form (tiles_per_cta): Dk = Dv in {64, 128},
+  // no prologue score terms, pages of >= 16 keys.
+  const bool terms = col_bias_ptr || pro_row_k != 0.f || pro_row_c != 0.f;
+  int ntiles;
+  {
+    const bool eligible = !fp8 && !q8 && Dk == Dv && (Dk == 64 || Dk == 128) && !(paged && page_size < 16) && !terms;
+    // average key tiles a query tile visits: keys per sequence, halved by a
+    // causal mask, bounded by a window
+    TileHints h;
+    h.avg_key_tiles = (double)launch->total_k / (double)B / (double)fa::kBlockN;
+    if (paged) h.avg_key_tiles = (double)launch->max_seqlen_k / (double)fa::kBlockN;
+    if (causal) h.avg_key_tiles *= 0.5;
+    if (window > 0)
+      h.avg_key_tiles = std::min(h.avg_key_tiles, (double)(causal ? window : 2 * window) / fa::kBlockN + 1.0);
+    h.n_tiles = ((double)Tq / (double)fa::kBlockM + (double)B) * (double)Hq;
+    h.block_mask = block_mask != nullptr;
+    h.causal = causal != 0;
+    h.window = window > 0;
+    h.mod = mod;
+    ntiles = tiles_per_cta(eligible, prefill_variant(), h);
+  }
+  const int64_t rows_per_cta = ntiles * fa::kBlockM;
   const int64_t n_qtiles = (launch->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   const int64_t head_group = Hq < 8 ? Hq : 8;
   const int64_t n_hgroups = (Hq + head_group - 1) / head_group;
@@ -908,13 +955,13 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   L.int8 = kv_dt == FA_I8;
   L.q8 = q8;
   L.variant = prefill_variant();
+  L.tiles_per_cta = ntiles;
   // The plain-softmax kernels fold a positive scale into the exponent and
   // have no per-key term; any other scale, and a Q add, take the general
   // score path (ALiBi with slope 0).  The prologue's score terms select the
   // kernels that carry them (mod 3: general score, 4: soft-cap).
   // The row term enters the kernels only under the soft-cap (as pro_row_*),
   // where it selects them too.
-  const bool terms = col_bias_ptr || pro_row_k != 0.f || pro_row_c != 0.f;
   int kmod = mod;
   if (mod == 0 && (!(softmax_scale > 0.f) || col_bias_ptr)) {
     kmod = 1;

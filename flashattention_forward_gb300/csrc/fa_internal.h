@@ -19,6 +19,7 @@ struct PrefillLaunch {
   int int8;      // with fp8: the byte cache holds int8 values (else e4m3)
   int q8;        // with fp8 (e4m3): Q is e4m3 and QK runs on the bytes
   int variant;   // 0: fastest available, 1: force the 10-warp two-pass softmax
+  int tiles_per_cta;   // 128-row query tiles per CTA: 2 (ping-pong), or 1 (two CTAs per SM)
   dim3 grid;
   cudaStream_t stream;
 };
@@ -75,6 +76,9 @@ cudaError_t launch_prefill_192_128_q8(const PrefillLaunch &L);
 // translation units of their own: the ping-pong kernel (bf16 K/V, Dk = Dv in
 // {64, 128}) and the chunked-ring kernel (bf16 Dk 192, e4m3 and int8 caches).
 cudaError_t launch_prefill2_kt(int d, const PrefillLaunch &L);
+// The ping-pong kernel with one query tile per CTA (two CTAs per SM; bf16
+// K/V, Dk = Dv in {64, 128}, MOD 0-2), in a translation unit of its own.
+cudaError_t launch_prefill2_t1(int d, const PrefillLaunch &L);
 cudaError_t launch_prefill3_kt(int dk, bool fp8, const PrefillLaunch &L);
 cudaError_t launch_prefill3_kt_i8(int dk, const PrefillLaunch &L);
 // Chunked-ring kernels for byte caches in the vectorized 5-D page layouts
@@ -97,6 +101,10 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long *done_mask)
   const unsigned long long bit = 1ull << (dev & 63);
   if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // all shared memory, none as L1, so that kernels sized for two CTAs per
+  // SM get them
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
   return e;
 }

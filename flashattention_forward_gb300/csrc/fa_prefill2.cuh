@@ -20,20 +20,29 @@
 // Warps: 0-3 softmax A, 4-7 softmax B, 8 TMA producer (Q, K, V), 9 TMEM
 // allocation + MMA issue; the 12-warp variant adds two idle warps so that
 // warpgroup 2 can hand its registers to the softmax warpgroups (setmaxnreg).
+//
+// NT = 1: one query tile per CTA (warps 0-3 softmax, 4 producer, 5 MMA, and
+// 6-7 idle: setmaxnreg is executed by whole warpgroups), 256 TMEM columns (S [0,128), O [128,256)) and about 96 KB of shared memory,
+// so that two CTAs share an SM: the tensor core alternates between the two
+// CTAs' tiles as it does between A and B, and one CTA's set-up, pipeline
+// fill and epilogue run under the other's main loop.  For short or ragged
+// sequences, where those fixed costs weigh most.
 #pragma once
 #include "fa_prefill.cuh"
 
 namespace fa {
 
-template <int DK, int DV, bool PAGED, int MOD, bool BIGREG>
+template <int DK, int DV, bool PAGED, int MOD, bool BIGREG, int NT = 2>
 struct Prefill2Cfg {
-  static constexpr int NSK = (DK <= 64) ? 4 : 3;
-  static constexpr int NSV = (DK <= 64) ? 4 : 2;
+  static_assert(NT == 2 || (NT == 1 && BIGREG), "one query tile per CTA: register-split variant only");
+  // K/V ring depths; one tile per CTA keeps two CTAs' rings within an SM
+  static constexpr int NSK = NT == 2 ? ((DK <= 64) ? 4 : 3) : ((DK <= 64) ? 3 : 1);
+  static constexpr int NSV = NT == 2 ? ((DK <= 64) ? 4 : 2) : ((DK <= 64) ? 2 : 1);
   static constexpr int kQTileBytes = kBlockM * DK * 2;
   static constexpr int kKBytes = kBlockN * DK * 2;
   static constexpr int kVBytes = kBlockN * DV * 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = 2 * kQTileBytes;
+  static constexpr int kOffK = NT * kQTileBytes;
   static constexpr int kOffV = kOffK + NSK * kKBytes;
   static constexpr int kOffBar = kOffV + NSV * kVBytes;
   static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 6;
@@ -41,13 +50,23 @@ struct Prefill2Cfg {
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;
   // BIGREG: 12 warps; the producer/MMA warpgroup gives registers to the two
   // softmax warpgroups (setmaxnreg), so a whole S row fits in registers.
-  static constexpr int kThreads = (BIGREG ? 12 : 10) * 32;
-  static constexpr int kRegsSoftmax = 208, kRegsOther = 80;
-  // launch registers per thread needed for that split to fit the CTA's pool
-  static constexpr int kMinLaunchRegs = (8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther + kThreads - 1) / kThreads;
-  static constexpr uint32_t kTmemCols = 512;
+  // setmaxnreg acts on whole warpgroups, so the register-split variants fill
+  // the last warpgroup with idle warps
+  static constexpr int kThreads = NT == 2 ? (BIGREG ? 12 : 10) * 32 : 8 * 32;
+  static constexpr int kSoftmaxWarps = 4 * NT;
+  static constexpr int kProducerWarp = 4 * NT, kMmaWarp = 4 * NT + 1;
+  static constexpr int kCtasPerSm = NT == 2 ? 1 : 2;
+  static constexpr int kRegsSoftmax = NT == 2 ? 208 : 200, kRegsOther = NT == 2 ? 80 : 56;
+  // registers the split needs from the CTA's pool, and the launch registers
+  // per thread that provide them
+  static constexpr int kPoolNeeded = kSoftmaxWarps * 32 * kRegsSoftmax + (kThreads - kSoftmaxWarps * 32) * kRegsOther;
+  static constexpr int kMinLaunchRegs = (kPoolNeeded + kThreads - 1) / kThreads;
+  static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
   static_assert(DV <= 128, "O_A/O_B hold 128 columns each");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(NT == 2 || 2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+  static_assert(NT == 2 || kMinLaunchRegs * kThreads * 2 <= 65536, "two CTAs' register pools per SM");
+  static_assert(kThreads % 128 == 0 || !BIGREG, "setmaxnreg needs whole warpgroups");
 };
 
 struct Half {
@@ -94,11 +113,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 
-template <int DK, int DV, bool PAGED, int MOD, bool BIGREG>
-__global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThreads, 1)
+template <int DK, int DV, bool PAGED, int MOD, bool BIGREG, int NT = 2>
+__global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::kThreads,
+                                  Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::kCtasPerSm)
     fa_prefill2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using Cfg = Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>;
+  using Cfg = Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>;
+  constexpr int kProducerWarp = Cfg::kProducerWarp, kMmaWarp = Cfg::kMmaWarp;
   // MOD: 0 plain scores, 1 ALiBi, 2 soft-cap; 3 and 4 are 1 and 2 with the
   // prologue's score terms (KT): a Q add's per-key term and, under the
   // soft-cap, the row term of a K add
@@ -119,18 +140,18 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     const int ka = __ldg(p.cu_k + pi.b), kb = __ldg(p.cu_k + pi.b + 1);
     pi.sq = qb - qa;
     pi.sk = kb - ka;
-    pi.q_row0 = qa + pt * 2 * kBlockM;
+    pi.q_row0 = qa + pt * NT * kBlockM;
     pi.k_row0 = ka;
   }
-  if (pt * 2 * kBlockM >= pi.sq) return;
+  if (pt * NT * kBlockM >= pi.sq) return;
   pi.kt_lo = 1 << 30;
   pi.kt_hi = 0;
 #pragma unroll
   for (int X = 0; X < 2; ++X) {
     Half &hx = pi.x[X];
-    hx.qt = pt * 2 + X;
+    hx.qt = pt * NT + X;
     hx.q0 = hx.qt * kBlockM;
-    hx.valid = hx.q0 < pi.sq;
+    hx.valid = X < NT && hx.q0 < pi.sq;
     hx.klo = hx.khi = 0;
     if (!hx.valid) continue;
     const int last = min(hx.q0 + kBlockM, pi.sq) - 1;
@@ -157,8 +178,8 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
   for (int kt = first_kt; kt < pi.kt_hi; kt = pair_next(p, pi, kt)) ++n_tiles;
 
   if (n_tiles == 0) {
-    for (int e = threadIdx.x; e < 2 * kBlockM; e += blockDim.x) {
-      const int i = pt * 2 * kBlockM + e;
+    for (int e = threadIdx.x; e < NT * kBlockM; e += blockDim.x) {
+      const int i = pt * NT * kBlockM + e;
       if (i >= pi.sq) break;
       const int64_t t = (int64_t)pi.q_row0 + e;
       __nv_bfloat16 *o = p.out + t * p.out_stride_t + (int64_t)pi.h * p.out_stride_h;
@@ -205,7 +226,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -213,21 +234,21 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // BIGREG: warpgroups 0-1 (softmax) take the registers warpgroup 2 releases
+  // BIGREG: the softmax warps take the registers the other warps release
   // (setmaxnreg at the head of each role's branch).  The host launches this
-  // variant only when the kernel's launch register count makes
-  // 8*32*224 + 4*32*56 fit the CTA's register pool.
-  if (BIGREG && warp >= 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsOther));
+  // variant only when the kernel's launch register count makes the split
+  // (Cfg::kPoolNeeded) fit the CTA's register pool.
+  if (BIGREG && warp >= kProducerWarp) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsOther));
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------ producer: Q, K, V --
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_expect_tx(smem_u32(q_full), 2 * Cfg::kQTileBytes);
+      mbar_expect_tx(smem_u32(q_full), NT * Cfg::kQTileBytes);
 #pragma unroll
-      for (int X = 0; X < 2; ++X)
+      for (int X = 0; X < NT; ++X)
 #pragma unroll
         for (int cb = 0; cb < DK / 64; ++cb)
           tma_load_3d(smem_u32(sQ + X * Cfg::kQTileBytes + cb * kBlockM * 128), &tm_q, smem_u32(q_full), cb * 64,
@@ -336,7 +357,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer --
     constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, DV, 0, 1);
@@ -368,7 +389,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
     };
     auto pv = [&](int X, int sv) {
       const uint32_t a = tmem + (X ? 128u : 0u);                 // P_X aliases S_X
-      const uint32_t d = tmem + 256u + (X ? 128u : 0u);
+      const uint32_t d = tmem + NT * 128u + (X ? 128u : 0u);
       uint32_t b = v_lo + (uint32_t)(sv * (Cfg::kVBytes >> 4));
       const uint32_t acc0 = n_pv[X] > 0 ? 1u : 0u;
 #pragma unroll
@@ -429,14 +450,14 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
         kt = kn;
       }
     }
-  } else if (warp < 8) {
+  } else if (warp < Cfg::kSoftmaxWarps) {
     // ---------------------------------------------------------- softmax --
     if constexpr (BIGREG) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kRegsSoftmax));
     const int X = warp >> 2;                  // 0: tile A, 1: tile B
     const int r = threadIdx.x & 127;          // row in the tile == TMEM lane
     const Half hx = X ? pi.x[1] : pi.x[0];
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t colS = X ? 128u : 0u, colO = 256u + (X ? 128u : 0u);
+    const uint32_t colS = X ? 128u : 0u, colO = NT * 128u + (X ? 128u : 0u);
     const int i = hx.q0 + r;
     const int ip = i + pi.sk - pi.sq;
     // Prologue terms (see PrefillParams; kernels with KT only): the row term
@@ -806,7 +827,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG>::kThre
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }

@@ -10,25 +10,24 @@ namespace fa {
 // with setmaxnreg.inc, which waits until other warps of the CTA release
 // registers.  It is launched only when the compiled launch register count
 // makes the whole split fit the CTA's pool; otherwise the 10-warp variant runs.
-template <int D, bool PAGED, int MOD>
+template <int D, bool PAGED, int MOD, int NT = 2>
 bool prefill2_bigreg_fits() {
-  using Big = Prefill2Cfg<D, D, PAGED, MOD, true>;
+  using Big = Prefill2Cfg<D, D, PAGED, MOD, true, NT>;
   static int verdict = -1;   // per process: all devices run the same binary
   if (verdict < 0) {
     cudaFuncAttributes a;
-    const bool ok = cudaFuncGetAttributes(&a, fa_prefill2_kernel<D, D, PAGED, MOD, true>) == cudaSuccess &&
-                    a.numRegs >= Big::kMinLaunchRegs && a.numRegs * Big::kThreads >=
-                    8 * 32 * Big::kRegsSoftmax + 4 * 32 * Big::kRegsOther;
+    const bool ok = cudaFuncGetAttributes(&a, fa_prefill2_kernel<D, D, PAGED, MOD, true, NT>) == cudaSuccess &&
+                    a.numRegs >= Big::kMinLaunchRegs && a.numRegs * Big::kThreads >= Big::kPoolNeeded;
     verdict = ok ? 1 : 0;
   }
   return verdict == 1;
 }
 
-template <int D, bool PAGED, int MOD, bool BIG>
+template <int D, bool PAGED, int MOD, bool BIG, int NT = 2>
 cudaError_t prefill2_launch_one(const PrefillLaunch &L) {
-  using Cfg = Prefill2Cfg<D, D, PAGED, MOD, BIG>;
+  using Cfg = Prefill2Cfg<D, D, PAGED, MOD, BIG, NT>;
   static unsigned long long done = 0;
-  auto kern = fa_prefill2_kernel<D, D, PAGED, MOD, BIG>;
+  auto kern = fa_prefill2_kernel<D, D, PAGED, MOD, BIG, NT>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
@@ -43,8 +42,17 @@ cudaError_t prefill2_pick(const PrefillLaunch &L) {
 
 // MOD 0 plain, 1 ALiBi, 2 soft-cap; 3 and 4 (a prologue's per-key score
 // term) are instantiated in fa_prefill_kt.cu.
+// One query tile per CTA, two CTAs per SM (L.tiles_per_cta == 1; MOD 0-2):
+// instantiated in fa_prefill_t1.cu.
+template <int D, bool PAGED, int MOD>
+cudaError_t prefill2_launch_t1(const PrefillLaunch &L) {
+  if (!prefill2_bigreg_fits<D, PAGED, MOD, 1>()) return cudaErrorNotSupported;
+  return prefill2_launch_one<D, PAGED, MOD, true, 1>(L);
+}
+
 template <int D, bool PAGED>
 cudaError_t prefill2_by_mod(const PrefillLaunch &L) {
+  if (L.tiles_per_cta == 1) return launch_prefill2_t1(D, L);
   switch (L.mod) {
     case 0: return prefill2_pick<D, PAGED, 0>(L);
     case 1: return prefill2_pick<D, PAGED, 1>(L);
