@@ -666,7 +666,8 @@ def main():
     mod_name = {0: "none", 1: "alibi", 2: "softcap"}[pd.mod_kind]
     roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": ach / pk["bf16"], "traffic": traffic, "algorithmic_bytes": prefill_bytes(pd),
-                "kernel": f"fa_prefill2_kernel<128,128,packed,{mod_name}>, config-5 run '{run_d}'",
+                "kernel": f"fa_prefill2_kernel<128,128,packed,{mod_name}>, config-5 run '{run_d}' "
+                          f"({'one query tile per CTA, two CTAs per SM' if pd.mod_kind == 2 or pd.window > 0 or (pd.mod_kind == 1 and pd.causal) or pd.block_mask is not None else 'two query tiles per CTA'}, as the library picks)",
                 "share_of_step": ms_d / statistics.mean(step_ms),
                 "peak_source": f"{pk['src']} bf16 burst (cuBLAS 8192^3)"}
     extra, summary, e2e, cpu = {}, {}, None, None
