@@ -144,20 +144,21 @@ __device__ __forceinline__ void dec_cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 // Four cache bytes -> four f16 values (two packed pairs), exactly: e4m3 by the
-// hardware conversion, int8 through the fp32 2^23 + (x + 128) - (2^23 + 128).
+// hardware conversion of each 16-bit half; int8 byte x as the f16 whose bits
+// are 0x6400 | (x + 128), i.e. 1024 + (x + 128) (f16 spacing is 1 on
+// [1024, 2048)), minus 1152 in f16 (exact; checked for all 256 bytes).
 template <int KV>
 __device__ __forceinline__ void dec_bytes4_to_f16(uint32_t w, uint32_t &o0, uint32_t &o1) {
   if constexpr (KV == 1) {
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(o0) : "r"(w & 0xFFFFu));
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(o1) : "r"(w >> 16));
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(o0), "=r"(o1)
+        : "r"(w));
   } else {
     const uint32_t u = w ^ 0x80808080u;
-    const float a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.f;
-    const float b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.f;
-    const float c = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.f;
-    const float d = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.f;
-    o0 = pack_f16x2(a, b);
-    o1 = pack_f16x2(c, d);
+    const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140), hi = __byte_perm(u, 0x64646464u, 0x4342);
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(o0) : "r"(lo), "r"(0x64806480u));   // 0x6480 = 1152 in f16
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(o1) : "r"(hi), "r"(0x64806480u));
   }
 }
 
@@ -627,12 +628,17 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       l0 = l0 * a0 + sum0;   // per-thread partial sums; reduced across the quad at the end
       l1 = l1 * a1 + sum1;
+      // O is rescaled only when a row maximum moved somewhere in the warp
+      // (after the first stages it rarely does); the factors are exactly 1
+      // otherwise, so skipping changes nothing.
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= a0;
-        o[n][1] *= a0;
-        o[n][2] *= a1;
-        o[n][3] *= a1;
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][0] *= a0;
+          o[n][1] *= a0;
+          o[n][2] *= a1;
+          o[n][3] *= a1;
+        }
       }
       uint32_t pa[4];
       if constexpr (KV) {
