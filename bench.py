@@ -157,7 +157,7 @@ def prefill_bytes(p):
     return qo + kv
 
 
-def make_call(p, t, num_splits=0):
+def make_call(p, t, num_splits=0, pv_e4m3=False):
     import flashattention_forward_gb300 as fa
     dev = t["q"].device
     out = torch.empty((p.total_q, p.hq, p.dv), dtype=torch.bfloat16, device=dev)
@@ -167,7 +167,8 @@ def make_call(p, t, num_splits=0):
         num_splits = fa.default_splits(p.num_seqs, p.max_seqlen_q, p.max_seqlen_k, p.hq, p.hkv, p.page_size,
                                        p.total_k)
     launch = fa.Launch(num_seqs=p.num_seqs, max_seqlen_q=p.max_seqlen_q, max_seqlen_k=p.max_seqlen_k,
-                       num_splits=num_splits, total_q=p.total_q, total_k=p.total_k)
+                       num_splits=num_splits, total_q=p.total_q, total_k=p.total_k,
+                       flags=fa.FLAG_PV_E4M3 if pv_e4m3 else 0)
     need = fa.workspace_bytes(launch, p.hq, p.hkv, p.dv, p.prologue)
     if need:
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -177,7 +178,7 @@ def make_call(p, t, num_splits=0):
                       page_size=p.page_size, k_scale=t.get("k_scale"), v_scale=t.get("v_scale"),
                       softmax_scale=p.softmax_scale, causal=p.causal, window=p.window, score_mod=p.mod_kind,
                       alibi_slope=p.alibi_slope, softcap=p.softcap, block_mask=t.get("bm"),
-                      num_splits=num_splits, out=out, lse=lse, workspace=ws)
+                      num_splits=num_splits, out=out, lse=lse, workspace=ws, pv_e4m3=pv_e4m3)
 
     def call():
         return plan.run()
@@ -719,6 +720,7 @@ def compact_summary(runs, extra, pk):
            "paged_decode_int8_64seq_hq32_hkv8_p16": "c3_int8", "paged_fp8_d192_v128_16seq_h16_p64_causal": "c4",
            "paged_fp8kv_qe4m3_d128_16seq_h16_p64_causal": "c4_q8_d128",
            "paged_fp8kv_qe4m3_d192_v128_16seq_h16_p64_causal": "c4_q8",
+           "paged_fp8kv_qe4m3_pv8_d192_v128_16seq_h16_p64_causal": "c4_q8_pv8",
            "paged_fp8_d192_v128_16seq_h16_p64_causal_vec5": "c4_vec5",
            "paged_decode_e4m3_64seq_hq32_hkv8_p16_vec5": "c3_e4m3_vec5",
            "bwd_4x4096_h16_d128_noncausal": "bwd_4x4096"}
@@ -729,11 +731,12 @@ def compact_summary(runs, extra, pk):
         if "GB/s" in v:
             out[short] = [r3(v["ms"]), r3(v["GB/s"]), r3(v["frac_hbm"])]
         else:
-            out[short] = [r3(v["ms"]), r3(v["tflops"]), r3(v["frac_bf16"])]
+            out[short] = [r3(v["ms"]), r3(v["tflops"]), r3(v.get("frac_bf16", v.get("frac_fp8", 0.0)))]
     d = extra.get("dense_causal_b2_h4_s128_d64")
     if d:
         out["c1_us"] = [r3(d["device_us_per_launch"]), r3(d["wall_us_per_call"])]
-    out["fields"] = "c5 and prefill: [ms, TFLOP/s, frac of bf16 peak]; decode and window: [ms, GB/s, frac of HBM]"
+    out["fields"] = ("c5 and prefill: [ms, TFLOP/s, frac of bf16 peak (c4_q8_pv8: of the e4m3 peak)]; "
+                     "decode and window: [ms, GB/s, frac of HBM]")
     return out
 
 
@@ -890,6 +893,13 @@ def other_workloads(dev, warmup, steps, flush, pk):
     res["paged_fp8kv_qe4m3_d192_v128_16seq_h16_p64_causal"] = {
         "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
         "frac_of_mixed_peak": t_peak / (ms * 1e-3), "fp8_peak_tflops": fp8_peak, "gflop": fl / 1e9}
+    # the same with the opt-in e4m3 P * V (both contractions kind::f8f6f4):
+    # against the measured e4m3 peak
+    call, _, _, _ = make_call(p, t, num_splits=0, pv_e4m3=True)
+    ms = statistics.mean(time_calls([call], warmup, steps, flush))
+    res["paged_fp8kv_qe4m3_pv8_d192_v128_16seq_h16_p64_causal"] = {
+        "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "frac_fp8": fl / (ms * 1e-3) / 1e12 / fp8_peak,
+        "fp8_peak_tflops": fp8_peak, "gflop": fl / 1e9, "mode": "FA_FLAG_PV_E4M3 (opt-in precision)"}
     del t
     # the same lengths at Dk = Dv = 128 with e4m3 K/V: bf16 Q (f16 QK) and
     # e4m3 Q (QK on the e4m3 bytes)
@@ -940,7 +950,7 @@ def profile_only(name, warmup, steps):
         p, splits = fi.make_problem([8192] * 4, hq=16, dk=128, name="long_noncausal"), 0
     elif name == "fp8":
         p, splits = fi.config4(), 0
-    elif name == "e4m3q_d192":
+    elif name in ("e4m3q_d192", "e4m3q_pv8_d192"):
         lens = [int(x) for x in np.diff(fi.config4().cu_seqlens_q)]
         p = fi.make_problem(lens, hq=16, hkv=16, dk=192, dv=128, seed=1, page_size=64, kv_dtype="e4m3",
                             q_dtype="e4m3", spare_pages=16, causal=True, name=name)
@@ -980,7 +990,7 @@ def profile_only(name, warmup, steps):
     if splits == "bwd":
         call = make_bwd_call(p, t)
     else:
-        call, _, _, _ = make_call(p, t, num_splits=splits)
+        call, _, _, _ = make_call(p, t, num_splits=splits, pv_e4m3=(name == "e4m3q_pv8_d192"))
     for _ in range(warmup + steps):
         call()
     torch.cuda.synchronize()

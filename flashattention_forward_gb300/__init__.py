@@ -92,7 +92,13 @@ class Launch(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
                 ("max_seqlen_k", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("total_q", ctypes.c_int64), ("total_k", ctypes.c_int64),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("flags", ctypes.c_int32)]
+
+
+# fa_launch_t.flags: P * V on e4m3 operands (opt-in precision mode, e4m3 q
+# with e4m3 caches; see FA_FLAG_PV_E4M3 in fa_gb300.h)
+FLAG_PV_E4M3 = 1
 
 
 _lib = None
@@ -211,7 +217,8 @@ def default_splits(num_seqs, max_seqlen_q, max_seqlen_k, hq, hkv, page_size=0, t
 
 
 def workspace_bytes(launch: "Launch", hq: int, hkv: int, dv: int, prologue=None) -> int:
-    """Workspace bytes of a forward call (split-KV partials, a Q add's per-key terms)."""
+    """Workspace bytes of a forward call (split-KV partials, a Q add's per-key
+    terms, the V-scale maxima of the e4m3 P * V mode)."""
     return int(lib().fa_fwd_workspace_bytes(ctypes.byref(launch), hq, hkv, dv, _ref(make_prologue(prologue))))
 
 
@@ -224,7 +231,8 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                score_mod: int = MOD_NONE, alibi_slope: float = 0.0, softcap: float = 0.0,
                block_mask: Optional[torch.Tensor] = None, num_splits: Optional[int] = None,
                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-               return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None, prologue=None):
+               return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None, prologue=None,
+               pv_e4m3: bool = False):
     """Attention forward over packed varlen Q and packed or paged K/V.
 
     q [T_q, Hq, Dk] bf16, or float8_e4m3fn with e4m3 caches at Dk 128 or 192
@@ -238,7 +246,8 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     or None)``.  ``num_splits=None`` picks the library's default (split-KV for
     decode shapes); 0 forces the single-pass kernel.  ``prologue``: op chains
     on the Q/K/V reads, {"q": [("mul", c), ("add", d), ...], "k": ..., "v": ...}
-    (see make_prologue and fa_prologue_t).
+    (see make_prologue and fa_prologue_t).  ``pv_e4m3``: the opt-in precision
+    mode FA_FLAG_PV_E4M3 (P * V on e4m3 operands; e4m3 q with e4m3 caches).
     """
     L = lib()
     B = cu_seqlens_q.shape[0] - 1
@@ -258,7 +267,8 @@ def fwd_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         if q.dtype != torch.bfloat16 or Dk != Dv:
             num_splits = 0
     launch = Launch(num_seqs=B, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
-                    num_splits=num_splits, total_q=Tq, total_k=total_k)
+                    num_splits=num_splits, total_q=Tq, total_k=total_k,
+                    flags=FLAG_PV_E4M3 if pv_e4m3 else 0)
     pro = make_prologue(prologue)
     need = workspace_bytes(launch, Hq, Hkv, Dv, pro)
     if need:
@@ -354,7 +364,8 @@ class FwdPlan:
             if q.dtype != torch.bfloat16 or Dk != Dv:
                 num_splits = 0
         self.launch = Launch(num_seqs=B, max_seqlen_q=kw["max_seqlen_q"], max_seqlen_k=kw["max_seqlen_k"],
-                             num_splits=num_splits, total_q=Tq, total_k=total_k)
+                             num_splits=num_splits, total_q=Tq, total_k=total_k,
+                             flags=FLAG_PV_E4M3 if kw.get("pv_e4m3") else 0)
         ws = kw.get("workspace")
         pro = make_prologue(kw.get("prologue"))
         need = workspace_bytes(self.launch, Hq, Hkv, Dv, pro)

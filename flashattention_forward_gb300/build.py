@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfa_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fa_api.cu", "fa_noalloc.cu", "fa_prologue.cu", "fa_prefill_kt.cu", "fa_prefill3_kt.cu", "fa_prefill3_kt_i8.cu", "fa_prefill3_vec5.cu", "fa_prefill_t1.cu", "fa_prefill3_vec5_i8.cu", "fa_decode.cu", "fa_prefill_d64.cu", "fa_prefill_d128.cu", "fa_prefill_d192.cu",
+SOURCES = ["fa_api.cu", "fa_noalloc.cu", "fa_prologue.cu", "fa_prefill_kt.cu", "fa_prefill3_kt.cu", "fa_prefill3_kt_i8.cu", "fa_prefill3_vec5.cu", "fa_prefill_t1.cu", "fa_prefill_pv8.cu", "fa_prefill3_vec5_i8.cu", "fa_decode.cu", "fa_prefill_d64.cu", "fa_prefill_d128.cu", "fa_prefill_d192.cu",
            "fa_prefill_d192_fp8.cu",
            "fa_prefill_i8.cu", "fa_prefill_q8.cu", "fa_bwd.cu"]
 

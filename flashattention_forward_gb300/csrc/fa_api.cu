@@ -283,6 +283,12 @@ size_t col_part_bytes(const fa_launch_t *L, int32_t hkv, const Folded &f) {
   return align256((size_t)L->num_seqs * hkv * col_bias_ld(L->max_seqlen_k) * sizeof(float));
 }
 
+// e4m3 P * V: one fp32 per (sequence, kv head), the largest V scale.
+size_t vmax_part_bytes(const fa_launch_t *L, int32_t hkv) {
+  if (!(L->flags & FA_FLAG_PV_E4M3) || L->num_seqs <= 0 || hkv <= 0) return 0;
+  return align256((size_t)L->num_seqs * hkv * sizeof(float));
+}
+
 }  // namespace
 
 namespace fa {
@@ -296,6 +302,8 @@ struct fa_fwd_plan_s {
   int dk = 0, fp8 = 0;
   int has_cb = 0;            // the prologue's per-key term is computed first
   fa::ColBiasParams cb;
+  int has_vm = 0;            // e4m3 P * V: the V-scale maxima are computed first
+  fa::VmaxParams vm;
   fa::DecodeLaunch dl;
   int splits = 0, hq = 0, dv = 0;
   int64_t rows = 0;
@@ -306,6 +314,10 @@ struct fa_fwd_plan_s {
 namespace {
 
 fa_status_t run_col_bias(const fa_fwd_plan_s &P, cudaStream_t s) {
+  if (P.has_vm) {
+    cudaError_t e = fa::launch_vscale_max(P.vm, s);
+    if (e != cudaSuccess) return cuda_fail(e, "V-scale pre-pass launch");
+  }
   if (!P.has_cb) return FA_OK;
   cudaError_t e = fa::launch_col_bias(P.cb, s);
   if (e != cudaSuccess) return cuda_fail(e, "prologue key-term launch");
@@ -365,7 +377,7 @@ size_t fa_fwd_workspace_bytes(const fa_launch_t *launch, int32_t hq, int32_t hkv
   memcpy(saved, g_msg, sizeof g_msg);
   if (fold_prologue(prologue, &f) != FA_OK) f = Folded();   // the call itself reports a malformed prologue
   memcpy(g_msg, saved, sizeof g_msg);
-  return split_part_bytes(launch, hq, dv) + col_part_bytes(launch, hkv, f);
+  return split_part_bytes(launch, hq, dv) + col_part_bytes(launch, hkv, f) + vmax_part_bytes(launch, hkv);
 }
 
 int32_t fa_fwd_default_splits(int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k, int64_t total_k,
@@ -610,6 +622,10 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const bool col_bias = needs_col_bias(fo);
   if (q8 && (fo.bq != 0.0 || fo.bk != 0.0))
     return fail(FA_ERR_UNSUPPORTED, "prologue adds on q or k with e4m3 q");
+  // ---- opt-in precision mode: P * V on e4m3 operands
+  if (launch->flags & ~FA_FLAG_PV_E4M3) return fail(FA_ERR_INVALID_ARG, "unknown launch flags 0x%x", launch->flags);
+  const bool pv8 = (launch->flags & FA_FLAG_PV_E4M3) != 0;
+  if (pv8 && !q8) return fail(FA_ERR_UNSUPPORTED, "FA_FLAG_PV_E4M3 takes e4m3 q with e4m3 k/v caches");
   if (vec5 && col_bias) return fail(FA_ERR_UNSUPPORTED, "a prologue q add reads keys in the token-major page layout only");
   if (vec5 && mod == 2 && fo.bk != 0.0)
     return fail(FA_ERR_UNSUPPORTED, "a prologue k add under the soft-cap is not taken with the vectorized 5-D pages");
@@ -643,9 +659,10 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   const CUtensorMapDataType kv_tmdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int group = (int)(Hq / Hkv);
   const bool have_keys = launch->total_k > 0 || (paged && n_pages > 0);
-  // ---- workspace: [split-KV partials][prologue key terms]
+  // ---- workspace: [split-KV partials][prologue key terms][V-scale maxima]
   const size_t ws_split = split_part_bytes(launch, (int32_t)Hq, (int32_t)Dv);
-  const size_t ws_need = ws_split + col_part_bytes(launch, (int32_t)Hkv, fo);
+  const size_t ws_cb = col_part_bytes(launch, (int32_t)Hkv, fo);
+  const size_t ws_need = ws_split + ws_cb + vmax_part_bytes(launch, (int32_t)Hkv);
   // checked by each path after its own limits
   auto check_workspace = [&]() -> fa_status_t {
     if (ws_need == 0) return FA_OK;
@@ -938,6 +955,26 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   p.col_bias = col_bias_ptr;
   p.cb_ld = cb_ld;
   p.vec5 = vec5;
+  // e4m3 P * V: the V-scale maxima, written by a pre-pass into the workspace
+  fa::VmaxParams vmp;
+  memset(&vmp, 0, sizeof vmp);
+  if (pv8) {
+    float *vmax_ptr = (float *)((char *)launch->workspace + ws_split + ws_cb);
+    vmp.v_scale = (const float *)v_scale->data;
+    vmp.block_table = paged ? (const int32_t *)block_table->data : nullptr;
+    vmp.bt_stride = paged ? block_table->stride[0] : 0;
+    vmp.max_pages = max_pages;
+    vmp.page_size = paged ? page_size : 1;
+    vmp.page_shift = paged ? ilog2(page_size) : 0;
+    vmp.n_pages = paged ? n_pages : v_cache->shape[0];
+    vmp.cu_k = (const int32_t *)cu_seqlens_k->data;
+    vmp.hkv = (int32_t)Hkv;
+    vmp.num_seqs = (int32_t)B;
+    vmp.out = vmax_ptr;
+    vmp.err = error_word();
+    p.pv_vmax = vmax_ptr;
+  }
+  L.pv8 = pv8;
   p.q = (const __nv_bfloat16 *)q->data;
   p.q_stride_t = q->stride[0];
   p.q_stride_h = q->stride[1];
@@ -981,6 +1018,8 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   P.fp8 = fp8;
   P.has_cb = col_bias_ptr != nullptr;
   P.cb = cbp;
+  P.has_vm = pv8 && B > 0;
+  P.vm = vmp;
   P.pl = L;
   return plan ? FA_OK : run_prefill(L, P, s);
 }

@@ -20,6 +20,7 @@ struct PrefillLaunch {
   int q8;        // with fp8 (e4m3): Q is e4m3 and QK runs on the bytes
   int variant;   // 0: fastest available, 1: force the 10-warp two-pass softmax
   int tiles_per_cta;   // 128-row query tiles per CTA: 2 (ping-pong), or 1 (two CTAs per SM)
+  int pv8;             // with q8: P * V on e4m3 P and V (opt-in precision mode)
   dim3 grid;
   cudaStream_t stream;
 };
@@ -62,6 +63,20 @@ struct ColBiasParams {
 };
 cudaError_t launch_col_bias(const ColBiasParams &p, cudaStream_t stream);
 
+// The largest |v_scale| of each (sequence, kv head), for the e4m3 P * V mode.
+struct VmaxParams {
+  const float *v_scale;         // [N_pg, P_s, Hkv] (paged) or [T_k, Hkv]
+  const int32_t *block_table;   // [B, bt_stride] or null (packed)
+  int64_t bt_stride, max_pages;
+  int32_t page_size, page_shift;
+  int64_t n_pages;              // pages in the pool (packed: tokens of the cache)
+  const int32_t *cu_k;
+  int32_t hkv, num_seqs;
+  float *out;                   // [B][Hkv]
+  int *err;
+};
+cudaError_t launch_vscale_max(const VmaxParams &p, cudaStream_t stream);
+
 cudaError_t launch_bwd(int d, const BwdLaunch &L);
 cudaError_t launch_prefill_64_64(const PrefillLaunch &L);
 cudaError_t launch_prefill_128_128(const PrefillLaunch &L);
@@ -85,6 +100,9 @@ cudaError_t launch_prefill3_kt_i8(int dk, const PrefillLaunch &L);
 // (MOD 0-2), in translation units of their own.
 cudaError_t launch_prefill3_vec5(int dk, bool i8, const PrefillLaunch &L);
 cudaError_t launch_prefill3_vec5_i8(int dk, const PrefillLaunch &L);
+// Chunked-ring kernels with e4m3 Q and P * V on e4m3 P and V (Dk 128 or 192,
+// Dv 128, MOD 0-2), in a translation unit of their own.
+cudaError_t launch_prefill3_pv8(int dk, const PrefillLaunch &L);
 cudaError_t launch_decode(int d, const DecodeLaunch &L);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int64_t n_rows, int hq,
                            int dv, void *out, float *lse, cudaStream_t stream);

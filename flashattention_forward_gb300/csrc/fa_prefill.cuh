@@ -65,6 +65,9 @@ struct PrefillParams {
   // byte caches in the vectorized 5-D layouts (paged, pages of >= 16 keys):
   // K [N_pg, Hkv, Dk/16, P_s, 16], V [N_pg, Hkv, P_s/16, Dv, 16]
   int32_t vec5;
+  // e4m3 P * V (opt-in): the largest |v_scale| of each (sequence, kv head),
+  // [B][Hkv] fp32 written by a pre-pass; null otherwise
+  const float *pv_vmax;
 };
 
 

@@ -49,7 +49,10 @@
 
 namespace fa {
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool Q8 = false>
+// PV8 (with Q8): P * V on the e4m3 bytes as well -- P in e4m3 in shared
+// memory, V transposed by the converters into a K-major e4m3 operand,
+// kind::f8f6f4 -- an opt-in precision mode (see the P8 notes in the kernel).
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool Q8 = false, bool PV8 = false>
 struct Prefill3Cfg {
   // 16 KB chunks per K tile: 64 bf16/f16 columns, or (Q8) 128 e4m3 columns
   // (Dk 192: two chunks, the second half zero-filled by TMA)
@@ -58,17 +61,20 @@ struct Prefill3Cfg {
   static constexpr int kChunkBytes = kBlockN * 128;
   static constexpr int kQTileBytes = Q8 ? KC * kBlockM * 128 : kBlockM * DK * 2;
   static constexpr int kVBytes = VC * kChunkBytes;
-  // Q8: a ring of NSS tiles' K scales (NSS >= NSV + 1: see the producer)
+  // Q8: a ring of NSS tiles' K scales (NSS >= NSV + 1: see the producer);
+  // PV8 adds the V scales beside them and two e4m3 P tiles
   static constexpr int NSS = Q8 ? 4 : 1;
-  static constexpr int kKsBytes = Q8 ? NSS * kBlockN * 4 : 0;
-  static constexpr int kRing = 229376 - 2 * kQTileBytes;   // 224 KB minus the Q tiles
+  static constexpr int kKsBytes = Q8 ? (PV8 ? 2 : 1) * NSS * kBlockN * 4 : 0;
+  static constexpr int kPBytes = PV8 ? 2 * kBlockM * 128 : 0;
+  static constexpr int kRing = 229376 - 2 * kQTileBytes - kPBytes;   // 224 KB minus the Q (and P) tiles
   static constexpr int NSV = (DV <= 64) ? 6 : 2;
   static constexpr int NCK_raw = (kRing - NSV * kVBytes - kKsBytes) / kChunkBytes;
   static constexpr int NCK = NCK_raw > 8 ? 8 : NCK_raw;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + NCK * kChunkBytes;
-  static constexpr int kOffKs = kOffV + NSV * kVBytes;
+  static constexpr int kOffP = kOffV + NSV * kVBytes;
+  static constexpr int kOffKs = kOffP + kPBytes;
   static constexpr int kOffBar = kOffKs + kKsBytes;
   // q_full, q_conv[2], kc_full/kc_empty/kc_stage[NCK], v_full/v_empty/v_stage[NSV],
   // s_full[2], p_full[2], o_done[2], Q8: ks_full[NSS]
@@ -98,6 +104,7 @@ struct Prefill3Cfg {
   static_assert(!Q8 || (FP8 && (DK == 128 || DK == 192) && DV == 128),
                 "e4m3 Q runs with e4m3 K/V at Dk 128 or 192, Dv 128");
   static_assert(!Q8 || NSS >= NSV + 1, "K scales outlive their readers");
+  static_assert(!PV8 || (Q8 && DV == 128), "e4m3 P * V: with e4m3 Q, Dv 128");
 };
 
 // tcgen05 MMA with A and B from shared memory, e4m3 x e4m3 -> fp32 (K = 32 per
@@ -141,6 +148,28 @@ __device__ __forceinline__ void unpack_f16x2(uint32_t h, float &lo, float &hi) {
       : "r"(h));
 }
 
+// Four floats -> four e4m3 bytes (a in the low byte), round to nearest,
+// saturating at +-448; and back (exact).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+__device__ __forceinline__ void unpack_e4m3x4(uint32_t w, float &a, float &b, float &c, float &d) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+  unpack_f16x2(lo, a, b);
+  unpack_f16x2(hi, c, d);
+}
+
+
 // Two e4m3 bytes (low 16 bits of `two`) -> f16 pair, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   uint32_t h;
@@ -182,11 +211,12 @@ __device__ __forceinline__ void i8x4_scaled_f16(uint32_t w, float s, uint32_t &o
 // V5 (with FP8 and PAGED, not Q8): the pages are in the vectorized 5-D
 // layouts; kernels of their own, so that the token-major kernels carry none
 // of the 5-D code.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8 = false, bool V5 = false>
-__global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>::kThreads, 1)
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8 = false, bool V5 = false,
+          bool PV8 = false>
+__global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8, PV8>::kThreads, 1)
     fa_prefill3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8, PV8>;
   static_assert(!V5 || (FP8 && PAGED && !Q8), "5-D pages: paged byte caches with bf16 Q");
   // MOD: 0 plain scores, 1 ALiBi, 2 soft-cap; 3 and 4 are 1 and 2 with the
   // prologue's score terms (KT): a Q add's per-key term and, under the
@@ -267,6 +297,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
   uint8_t *sK = smem + Cfg::kOffK;
   uint8_t *sV = smem + Cfg::kOffV;
   float *sKs = reinterpret_cast<float *>(smem + Cfg::kOffKs);   // Q8: [NSS][kBlockN]
+  float *sVs = sKs + Cfg::NSS * kBlockN;                         // PV8: [NSS][kBlockN] V scales
+  uint8_t *sP = smem + Cfg::kOffP;                               // PV8: [2][128 rows][128 keys] e4m3
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
   uint64_t *q_full = bars;
   uint64_t *q_conv = bars + 1;          // [2] Q tile in f16 (e4m3 caches)
@@ -362,11 +394,15 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
     // Vectorized 5-D byte caches (V5): a box of a page piece lands as
     // [4 column groups][rows][16 bytes] for K and [rows / 16][64 dims][16
     // tokens] for V, in the same bytes the token-major box fills; the
-    // converters read either form.
+    // converters read either form.  PV8: a V block's byte rows (64 columns)
+    // land raw and contiguous ([128 keys][64 bytes]) in the upper half of the
+    // V stage, and the converters transpose them into its lower half.
     auto load_block = [&](const CUtensorMap *tm, uint8_t *dst, uint64_t *bar, int x, int kt, int page, bool staged,
                           bool isv) {
       if (!boxer) return;
-      const uint32_t at = staged ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64) : smem_u32(dst + r0 * 128);
+      const uint32_t at = (PV8 && isv) ? smem_u32(dst + r0 * 64)
+                          : staged     ? smem_u32(dst + (r0 >> 5) * 4096 + 2048 + (r0 & 31) * 64)
+                                       : smem_u32(dst + r0 * 128);
       if constexpr (PAGED) {
         const int slot = (kt * kBlockN + r0) & (p.page_size - 1);
         if constexpr (V5) {
@@ -406,6 +442,9 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         if constexpr (PAGED) tok = (int64_t)kpage * p.page_size + (key & (p.page_size - 1));
         else tok = (int64_t)pi.k_row0 + key;
         cp_async_4(dst + 4 * u, live ? p.k_scale + tok * p.hkv + pi.hk : p.k_scale, live ? 4u : 0u);
+        if constexpr (PV8)
+          cp_async_4(dst + 4 * u + Cfg::NSS * kBlockN * 4, live ? p.v_scale + tok * p.hkv + pi.hk : p.v_scale,
+                     live ? 4u : 0u);
       }
       cp_async_arrive_noinc(smem_u32(ks_full + slot));
     };
@@ -504,7 +543,8 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       if (!ok) break;
 #pragma unroll
       for (int c = 0; c < VC; ++c)
-        load_block(&tm_v, sV + sv * Cfg::kVBytes + c * Cfg::kChunkBytes, vbar, c * 64, kt, page, FP8, true);
+        load_block(&tm_v, sV + sv * Cfg::kVBytes + (PV8 ? Cfg::kChunkBytes + c * kBlockN * 64 : c * Cfg::kChunkBytes),
+                   vbar, c * 64, kt, page, FP8, true);
       kt = kn;
       page = page_next;
       kpage = kpage_next;
@@ -568,15 +608,31 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       tc_commit(smem_u32(s_full + X));
       return true;
     };
+    // PV8: A = the e4m3 P tile X, B = the transposed e4m3 V tile, both
+    // K-major and 128-byte swizzled like the Q8 QK's operands (the same
+    // descriptor high word), kind::f8f6f4 with K = 32 keys per instruction.
+    constexpr uint32_t idesc_pv8 = idesc_f16_f32(kBlockM, DV, 0, 0);
+    const uint32_t p8_lo = (uint32_t)smem_desc_sw128(smem_u32(sP), 16, 1024);
+    const uint32_t vt_lo = (uint32_t)smem_desc_sw128(sVa, 16, 1024);
     auto pv = [&](int X, int sv) {
-      const uint32_t a = tmem + (X ? 128u : 0u);                 // P_X aliases S_X
       const uint32_t d = tmem + 256u + (X ? 128u : 0u);
-      uint32_t b = v_lo + (uint32_t)(sv * (Cfg::kVBytes >> 4));
-      const uint32_t acc0 = n_pv[X] > 0 ? 1u : 0u;
+      if constexpr (PV8) {
+        const uint32_t a = p8_lo + (uint32_t)(X * ((kBlockM * 128) >> 4));
+        const uint32_t b = vt_lo + (uint32_t)(sv * (Cfg::kVBytes >> 4));
 #pragma unroll
-      for (int ks = 0; ks < kBlockN / 16; ++ks) {
-        mma_ts_w(d, a + ks * 8, b, v_hi, idesc_pv, ks > 0 ? 1u : acc0);
-        b += (16 * 128) >> 4;
+        for (int ks = 0; ks < kBlockN / 32; ++ks) {
+          if (ks == 0 && n_pv[X] == 0) mma_ss_f8_w<0>(d, a, qk_hi, b, qk_hi, idesc_pv8);
+          else mma_ss_f8_w<1>(d, a + 2 * ks, qk_hi, b + 2 * ks, qk_hi, idesc_pv8);
+        }
+      } else {
+        const uint32_t a = tmem + (X ? 128u : 0u);                 // P_X aliases S_X
+        uint32_t b = v_lo + (uint32_t)(sv * (Cfg::kVBytes >> 4));
+        const uint32_t acc0 = n_pv[X] > 0 ? 1u : 0u;
+#pragma unroll
+        for (int ks = 0; ks < kBlockN / 16; ++ks) {
+          mma_ts_w(d, a + ks * 8, b, v_hi, idesc_pv, ks > 0 ? 1u : acc0);
+          b += (16 * 128) >> 4;
+        }
       }
       tc_commit(smem_u32(o_done + X));
     };
@@ -634,7 +690,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       };
       auto key_of = [&](const It &it) { return it.kt * kBlockN + ((it.g % S) & 3) * 32 + lane; };
       auto page_of = [&](const It &it) -> int {
-        if constexpr (PAGED) {
+        if constexpr (PAGED && !PV8) {
           const int key = key_of(it);
           return (it.kt < pi.kt_hi && key < pi.sk) ? __ldg(bt + (key >> p.page_shift)) : 0;
         } else {
@@ -642,6 +698,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
         }
       };
       auto scale_of = [&](const It &it, int page) -> float {
+        if constexpr (PV8) return 0.f;   // the V scales go into P
         const int key = key_of(it);
         if (!(it.kt < pi.kt_hi && key < pi.sk)) return 0.f;
         int64_t tok;
@@ -693,6 +750,33 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
             e4m3x4_scaled_f16(w1, s, o[2], o[3]);
           }
         };
+        if constexpr (PV8) {
+          // e4m3 P * V: V becomes the K-major operand V^T [128 dims][128 keys]
+          // (128-byte swizzled, like a Q8 key tile) in the stage's lower half,
+          // its bytes unscaled (the V scales go into P).  The slice -- keys
+          // q*32 .. +31 of dims cb*64 .. +63, staged [key][64 bytes] in the
+          // upper half -- is 4 x 8 blocks of 8 x 8 bytes: lane (key group kg,
+          // dim group dg) transposes one and writes 8 dims' rows of 8 keys.
+          // Keys past the sequence end become zeros (their bytes may be
+          // anything, and 0 * NaN would be NaN).
+          uint8_t *vt = sV + (j % NSV) * Cfg::kVBytes;
+          const uint8_t *src = vt + Cfg::kChunkBytes + cb * (kBlockN * 64) + q * 32 * 64;
+          const int kg = lane >> 3, dg = lane & 7;
+          uint2 in[8], tr[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) in[k] = *reinterpret_cast<const uint2 *>(src + (kg * 8 + k) * 64 + dg * 8);
+          transpose_8x8_bytes(in, tr);
+          const int nlive = min(max(pi.sk - (kt * kBlockN + q * 32 + kg * 8), 0), 8);
+          const uint32_t mlo = nlive >= 4 ? 0xFFFFFFFFu : (uint32_t)((1ull << (8 * nlive)) - 1);
+          const uint32_t mhi = nlive >= 8 ? 0xFFFFFFFFu : (nlive <= 4 ? 0u : (uint32_t)((1ull << (8 * (nlive - 4))) - 1));
+          const int kb = q * 32 + kg * 8;   // the 8 keys' first byte in a 128-byte row
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int d = cb * 64 + dg * 8 + t;
+            *reinterpret_cast<uint2 *>(vt + d * 128 + ((((kb >> 4) ^ (d & 7))) << 4) + (kb & 15)) =
+                make_uint2(tr[t].x & mlo, tr[t].y & mhi);
+          }
+        } else {
         const int part = lane & 3;
         // one staged row piece (16 bytes, row rr of the slice) -> 16 f16
         // values of row q * 32 + rr, zeros past the sequence end
@@ -759,6 +843,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
           __syncwarp();
 #pragma unroll
           for (int t = 0; t < 4; ++t) put_row(raw[t], 8 * t + (lane >> 2));
+        }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -833,12 +918,26 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       }
       mbar_arrive(smem_u32(q_conv + X));
     }
+    // PV8 (P8 below): the weights go to e4m3 as p * v_scale * 2^-pexp, with
+    // 2^pexp above the largest V scale of the sequence (a pre-pass writes
+    // that maximum), so that with the max taken first (p <= 2^8) every
+    // weight stays below 2^8, inside the e4m3 range (448).  The factor is
+    // folded into the exponent's reference (p' = 2^(x - m - pexp)): the row
+    // sum then carries it too, O / l needs no correction, and the LSE adds
+    // pexp back.
+    int pexp = 0;
+    if constexpr (PV8) {
+      const float vmax = __ldg(p.pv_vmax + (int64_t)pi.b * p.hkv + pi.hk);
+      if (vmax > 0.f && vmax <= 3.0e38f) pexp = (int)((__float_as_uint(vmax) >> 23) & 0xFF) - 126;
+    }
+    const float mshift = (float)pexp;
     // MOD 0 runs with a positive scale only (the host routes other scales to
     // the general path), so raw scores can be maxed before scaling.
     constexpr bool fast = (MK == 0);
     // Deferred-max guard on a tile's row sum: P must stay finite in its
     // packed type (f16 for e4m3 caches: below 65504; bf16: any fp32 value).
     constexpr float kGuard = FP8 ? 0x1p15f : kGuardSum;
+    static_assert(!PV8 || !Cfg::kOnePass, "e4m3 P: the two-half softmax");
     const float sl2 = p.scale_log2 * rowf;
     const float c2u = 2.f * kLog2e * p.softcap_arg * rowf;   // soft-cap: raw score -> 2u log2(e)
     auto pack_p = [](float a, float b) -> uint32_t { return FP8 ? pack_f16x2(a, b) : pack_bf16x2(a, b); };
@@ -862,7 +961,23 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
       }
     };
     const float cexp = fast ? sl2 : 1.f;
-    constexpr bool kDeferredMax = (MK == 2);   // soft-cap only, as in fa_prefill2.cuh
+    constexpr bool kDeferredMax = (MK == 2) && !PV8;   // soft-cap only, as in fa_prefill2.cuh
+    // PV8: row r of the e4m3 P tile, 128 keys in eight 16-byte chunks,
+    // 128-byte swizzled (the K-major A operand of the e4m3 PV)
+    uint8_t *prow = sP + X * (kBlockM * 128) + r * 128;
+    // 32 weights of keys jc .. jc+31 (relative to the tile start: kr) times
+    // their V scales, to e4m3, into P row r
+    auto store_p8 = [&](const float (&w)[32], int kr, const float *vs) {
+      uint32_t b[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(vs + kr + 4 * k);
+        b[k] = pack_e4m3x4(w[4 * k] * s4.x, w[4 * k + 1] * s4.y, w[4 * k + 2] * s4.z, w[4 * k + 3] * s4.w);
+      }
+      const int c0 = kr >> 4;
+      *reinterpret_cast<uint4 *>(prow + (((c0) ^ (r & 7)) << 4)) = make_uint4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(b[4], b[5], b[6], b[7]);
+    };
     int j = -1;   // index of the tile in the pair's list (ring position)
     for (int kt = first_kt; ok && kt < pi.kt_hi; kt = pair_next(p, pi, kt)) {
       ++j;
@@ -1016,9 +1131,23 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
           auto exp_store = [&](float m_use) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              uint32_t pk[16];
-              chunk_exp(sv[c], cexp, m_use, pk, hsum);
-              tmem_st16(sa + hf * 32 + c * 16, pk);
+              if constexpr (PV8) {
+                float w[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  float t0, t1;
+                  fma2(t0, t1, sv[c][e], sv[c][e + 1], cexp, -(m_use + mshift));
+                  w[e] = ex2(t0);
+                  w[e + 1] = ex2(t1);
+                  const int qq = ((e >> 1) & 1) * 2;
+                  add2(hsum[qq], hsum[qq + 1], w[e], w[e + 1]);
+                }
+                store_p8(w, hf * 64 + c * 32, sVs + (j % Cfg::NSS) * kBlockN);
+              } else {
+                uint32_t pk[16];
+                chunk_exp(sv[c], cexp, m_use, pk, hsum);
+                tmem_st16(sa + hf * 32 + c * 16, pk);
+              }
             }
           };
           bool slow = !kDeferredMax || __any_sync(0xffffffffu, m_ref == -INFINITY);
@@ -1061,6 +1190,25 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
               alpha_tile *= alpha;
               warp_need = true;
               if (hf == 1) {
+                if constexpr (PV8) {
+                  // the first half's e4m3 weights, rescaled in place (a
+                  // second rounding, on a rare event that shrinks them by
+                  // at least 2^-8)
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) {
+                    uint4 *ptr = reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4));
+                    const uint4 u = *ptr;
+                    const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                      float f0, f1, f2, f3;
+                      unpack_e4m3x4(uu[k], f0, f1, f2, f3);
+                      o[k] = pack_e4m3x4(f0 * alpha, f1 * alpha, f2 * alpha, f3 * alpha);
+                    }
+                    *ptr = make_uint4(o[0], o[1], o[2], o[3]);
+                  }
+                } else {
                 tmem_wait_st();
                 float pw[32];
                 tmem_ld32(sa, pw);
@@ -1074,6 +1222,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
                   w[e] = pack_p(lo * alpha, hi * alpha);
                 }
                 tmem_st32(sa, w);
+                }
               }
             }
             exp_store((m_ref == -INFINITY) ? 0.f : m_ref);
@@ -1119,6 +1268,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
           fence_proxy_async_smem();
         }
       }
+      if constexpr (PV8) fence_proxy_async_smem();   // P8 for the tensor core
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(p_full + X));
@@ -1159,7 +1309,7 @@ __global__ void __launch_bounds__(Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q
             }
           }
           if (row_ok && p.lse) {
-            float lv = has ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+            float lv = has ? ((PV8 ? m_ref + mshift : m_ref) + __log2f(l)) * kLn2 : -INFINITY;
             // the prologue's row term: the softmax cancels it, the LSE carries it
             if (has) lv += p.pro_lse_c;
             if (has && p.pro_lse_k != 0.f)

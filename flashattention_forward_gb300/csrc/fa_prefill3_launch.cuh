@@ -10,14 +10,15 @@ namespace fa {
 // A register-split variant raises the softmax warps with setmaxnreg.inc,
 // which waits until other warps of the CTA release registers: it may run only
 // when the compiled launch register count covers the whole split.
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false,
+          bool PV8 = false>
 bool prefill3_split_fits() {
-  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8, PV8>;
   if constexpr (!Cfg::kSplitRegs) return true;
   static int verdict = -1;   // per process: all devices run the same binary
   if (verdict < 0) {
     cudaFuncAttributes a;
-    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5>) == cudaSuccess &&
+    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5, PV8>) == cudaSuccess &&
                a.numRegs * Cfg::kThreads >= Cfg::kPoolNeeded)
                   ? 1
                   : 0;
@@ -25,12 +26,13 @@ bool prefill3_split_fits() {
   return verdict == 1;
 }
 
-template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false>
+template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false,
+          bool PV8 = false>
 cudaError_t launch_prefill3_one(const PrefillLaunch &L) {
-  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8>;
-  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5>()) return cudaErrorNotSupported;
+  using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8, PV8>;
+  if (!prefill3_split_fits<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5, PV8>()) return cudaErrorNotSupported;
   static unsigned long long done = 0;
-  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5>;
+  auto kern = fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5, PV8>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
@@ -59,6 +61,9 @@ cudaError_t launch_prefill3(const PrefillLaunch &L) {
   if constexpr (FP8 && !Q8) {
     if (L.p.vec5) return launch_prefill3_vec5(DK, I8, L);
   }
+  if constexpr (Q8) {
+    if (L.pv8) return launch_prefill3_pv8(DK, L);
+  }
   if (L.mod >= 3) {
     if (Q8) return cudaErrorInvalidValue;
     return I8 ? launch_prefill3_kt_i8(DK, L) : launch_prefill3_kt(DK, FP8, L);
@@ -84,6 +89,21 @@ cudaError_t launch_prefill3_vec5_one(const PrefillLaunch &L) {
     case 2: return launch_prefill3_one<DK, DV, true, true, 2, false, I8, false, true>(L);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// The e4m3 P * V kernels (with e4m3 Q) of one Dk (MOD 0-2).
+template <int DK>
+cudaError_t launch_prefill3_pv8_one(const PrefillLaunch &L) {
+  auto by_mod = [&](auto paged_tag) -> cudaError_t {
+    constexpr bool PG = decltype(paged_tag)::value;
+    switch (L.mod) {
+      case 0: return launch_prefill3_one<DK, 128, PG, true, 0, false, false, true, false, true>(L);
+      case 1: return launch_prefill3_one<DK, 128, PG, true, 1, false, false, true, false, true>(L);
+      case 2: return launch_prefill3_one<DK, 128, PG, true, 2, false, false, true, false, true>(L);
+      default: return cudaErrorInvalidValue;
+    }
+  };
+  return L.paged ? by_mod(std::true_type{}) : by_mod(std::false_type{});
 }
 
 // The MOD 3 and 4 kernels of one (Dk, Dv, cache) combination.

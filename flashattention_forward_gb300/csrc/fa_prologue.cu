@@ -1,6 +1,7 @@
-// fa_prologue.cu -- the per-key score term of a prologue that adds a
-// constant to Q (fkl_python PR #7, prologue-fusion commit: op chains fused
-// onto the Q/K/V reads).
+// fa_prologue.cu -- pre-passes over the keys: the per-key score term of a
+// prologue that adds a constant to Q (fkl_python PR #7, prologue-fusion
+// commit: op chains fused onto the Q/K/V reads), and the largest V scale of
+// each sequence for the e4m3 P * V mode.
 //
 // With q' = a_q q + b_q and k' = a_k k + b_k, the score scale * <q'_i, k'_j>
 // holds the term scale * b_q * a_k * sum_d k_j[d], which depends on the key
@@ -104,7 +105,52 @@ __global__ void __launch_bounds__(128) fa_col_bias_kernel(const ColBiasParams p)
   *dst = p.factor * sum;
 }
 
+// The largest |v_scale| over the keys of one (sequence, kv head): 256
+// threads stride over the keys (page-table lookups for paged caches) and
+// reduce through shared memory.  Page ids outside the pool are flagged
+// (FA_ERR_DEVICE_BOUNDS) and skipped.
+__global__ void __launch_bounds__(256) fa_vscale_max_kernel(const VmaxParams p) {
+  const int hk = blockIdx.x, b = blockIdx.y;
+  const int k0 = __ldg(p.cu_k + b), sk = __ldg(p.cu_k + b + 1) - k0;
+  float m = 0.f;
+  for (int j = threadIdx.x; j < sk; j += 256) {
+    int64_t tok;
+    if (p.block_table) {
+      const int64_t pi = j >> p.page_shift;
+      const int page = pi < p.max_pages ? __ldg(p.block_table + (int64_t)b * p.bt_stride + pi) : -1;
+      if (page < 0 || page >= p.n_pages) {
+        atomicCAS(p.err, 0, (int)FA_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      tok = (int64_t)page * p.page_size + (j & (p.page_size - 1));
+    } else {
+      tok = (int64_t)k0 + j;
+      if (tok >= p.n_pages) {
+        atomicCAS(p.err, 0, (int)FA_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+    }
+    m = fmaxf(m, fabsf(__ldg(p.v_scale + tok * p.hkv + hk)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
+    p.out[(int64_t)b * p.hkv + hk] = r;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_vscale_max(const VmaxParams &p, cudaStream_t stream) {
+  fa_vscale_max_kernel<<<dim3((unsigned)p.hkv, (unsigned)p.num_seqs), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_col_bias(const ColBiasParams &p, cudaStream_t stream) {
   const dim3 grid((unsigned)((p.ld + 127) / 128), (unsigned)p.hkv, (unsigned)p.num_seqs);

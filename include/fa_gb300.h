@@ -136,10 +136,25 @@ typedef struct {
     int32_t n_qblk, n_kblk, blk_q, blk_k;
 } fa_block_mask_t;
 
+/* Opt-in precision mode (fa_launch_t.flags): P * V on e4m3 operands
+ * (FlyDSL PR #1066, Technical Details and Test Result: direct FP8 P x V at V
+ * head dim 128, with its larger error).  Taken with e4m3 q and e4m3 K/V,
+ * (Dk, Dv) in {(128, 128), (192, 128)}, token-major pages or packed K/V, no
+ * prologue and a single pass (num_splits 0); FA_ERR_UNSUPPORTED otherwise.
+ * The attention weights go to e4m3 as p * v_scale / 2^e, with 2^e above the
+ * largest V scale of the sequence (a pre-pass over the V scales, writing one
+ * fp32 per (sequence, kv head) into the workspace), and P * V runs on the
+ * tensor core's e4m3 path with fp32 accumulation; the row sums and the LSE
+ * stay fp32.  Each weight carries up to 2^-4 relative rounding, so outputs
+ * differ from the exact attention by more than in the default mode (the
+ * tests hold them to 4e-2; the LSE keeps its 1e-3). */
+#define FA_FLAG_PV_E4M3 1
+
 /* Host-side scalars, so that no length is read back from the device.
  * num_splits: 0 = single pass; > 0 = split-KV over that many key ranges
  * followed by the combine.  workspace: fa_fwd_workspace_bytes() bytes, needed
- * by split-KV with 2 or more splits and by a prologue with a Q add. */
+ * by split-KV with 2 or more splits, by a prologue with a Q add and by
+ * FA_FLAG_PV_E4M3.  flags: 0, or FA_FLAG_PV_E4M3. */
 typedef struct {
     int32_t num_seqs;
     int32_t max_seqlen_q;
@@ -149,6 +164,7 @@ typedef struct {
     int64_t total_k;
     void *workspace;         /* device, 256-byte aligned, caller-owned */
     size_t workspace_bytes;
+    int32_t flags;
 } fa_launch_t;
 
 /*

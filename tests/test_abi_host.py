@@ -412,3 +412,29 @@ def test_vectorize_pages_inverts_with_the_pages_permutes():
     # element (page, slot, head, d) of K sits at [page, head, d // 16, slot, d % 16]
     assert k5[3, 1, 5, 7, 9] == p.k[3, 7, 1, 5 * 16 + 9]
     assert v5[2, 0, 1, 100, 3] == p.v[2, 16 + 3, 0, 100]
+
+
+def test_pv_e4m3_flag_limits(L):
+    """FA_FLAG_PV_E4M3 takes e4m3 q with e4m3 caches; other flag bits are
+    rejected; the workspace gains one fp32 per (sequence, kv head)."""
+    T, H = 256, 4
+    bt = _t(FAKE * 10, fa.FA_I32, [2, 8])
+    ks = _t(FAKE * 8, fa.FA_F32, [32, 16, H])
+    vs = _t(FAKE * 9, fa.FA_F32, [32, 16, H])
+    k8 = _t(FAKE * 2, fa.FA_E4M3, [32, 16, H, 128])
+    v8 = _t(FAKE * 3, fa.FA_E4M3, [32, 16, H, 128])
+    out = _t(FAKE * 6, fa.FA_BF16, [T, H, 128])
+    lau = fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=T, total_k=0, flags=fa.FLAG_PV_E4M3)
+    st, msg = _call(L, q=_t(FAKE, fa.FA_BF16, [T, H, 128]), k=k8, v=v8, ks=ks, vs=vs, bt=bt, page=16, out=out,
+                    launch=lau)
+    assert st == fa.FA_ERR_UNSUPPORTED and "FA_FLAG_PV_E4M3" in msg
+    bad = fa.Launch(num_seqs=2, max_seqlen_q=128, max_seqlen_k=128, total_q=T, total_k=0, flags=6)
+    st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 128]), k=k8, v=v8, ks=ks, vs=vs, bt=bt, page=16, out=out,
+                    launch=bad)
+    assert st == fa.FA_ERR_INVALID_ARG and "flags" in msg
+    plain = fa.Launch(num_seqs=3, max_seqlen_q=10, max_seqlen_k=300, total_q=10, total_k=0)
+    flagged = fa.Launch(num_seqs=3, max_seqlen_q=10, max_seqlen_k=300, total_q=10, total_k=0, flags=fa.FLAG_PV_E4M3)
+    assert fa.workspace_bytes(flagged, 8, 2, 128) - fa.workspace_bytes(plain, 8, 2, 128) == 256
+    st, msg = _call(L, q=_t(FAKE, fa.FA_E4M3, [T, H, 128]), k=k8, v=v8, ks=ks, vs=vs, bt=bt, page=16, out=out,
+                    launch=lau)
+    assert st == fa.FA_ERR_INVALID_ARG and "workspace" in msg
