@@ -35,6 +35,7 @@ namespace fa {
 template <int DK, int DV, bool PAGED, int MOD, bool BIGREG, int NT = 2>
 struct Prefill2Cfg {
   static_assert(NT == 2 || (NT == 1 && BIGREG), "one query tile per CTA: register-split variant only");
+  static_assert(MOD != 5 || NT == 1, "ALiBi in the contraction: one tile per CTA");
   // K/V ring depths; one tile per CTA keeps two CTAs' rings within an SM
   static constexpr int NSK = NT == 2 ? ((DK <= 64) ? 4 : 3) : ((DK <= 64) ? 3 : 1);
   static constexpr int NSV = NT == 2 ? ((DK <= 64) ? 4 : 2) : ((DK <= 64) ? 2 : 1);
@@ -42,7 +43,12 @@ struct Prefill2Cfg {
   static constexpr int kKBytes = kBlockN * DK * 2;
   static constexpr int kVBytes = kBlockN * DV * 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = NT * kQTileBytes;
+  // MOD 5 (ALiBi with the bias in the contraction, one tile per CTA): three
+  // 4 KB operands of one K=16 step, 32-byte swizzled -- Q rows (+a_hi, +a_lo),
+  // (-a_hi, -a_lo) and key rows (n, n) -- after the Q tile
+  static constexpr int kAugBytes = MOD == 5 ? 3 * 4096 : 0;
+  static constexpr int kOffAug = NT * kQTileBytes;
+  static constexpr int kOffK = kOffAug + kAugBytes;
   static constexpr int kOffV = kOffK + NSK * kKBytes;
   static constexpr int kOffBar = kOffV + NSV * kVBytes;
   static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 6;
@@ -98,6 +104,30 @@ __device__ __forceinline__ bool half_active(const PrefillParams &p, const PairIn
   return X ? half_active_h(p, pi, pi.x[1], kt) : half_active_h(p, pi, pi.x[0], kt);
 }
 
+// ALiBi with the bias in the contraction (MOD 5): which linear form the key
+// tile starting at kt * 128 takes for every row of the query tile -- +1 when
+// all its keys are at or left of every row's diagonal i' (or under a causal
+// mask, which hides the others), -1 when all are right of it, 0 when it
+// straddles (the softmax then takes |i' - j| per element).
+__device__ __forceinline__ int alibi_side(const PrefillParams &p, const Half &hx, int kt) {
+  const int j0 = kt * kBlockN;
+  if (p.causal || j0 + kBlockN - 1 <= hx.ip_min) return 1;
+  if (j0 > hx.ip_max) return -1;
+  return 0;
+}
+
+// Shared-memory descriptor of a K-major operand with 32-byte rows (K = 16
+// bf16), 32-byte swizzle (mode 6), 8-row groups 256 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(16 >> 4) << 16;
+  d |= (uint64_t)(256 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)6 << 61;
+  return d;
+}
+
 __device__ __forceinline__ int pair_next(const PrefillParams &p, const PairInfo &pi, int kt) {
   ++kt;
   while (kt < pi.kt_hi && !half_active(p, pi, 0, kt) && !half_active(p, pi, 1, kt)) ++kt;
@@ -123,8 +153,12 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
   // MOD: 0 plain scores, 1 ALiBi, 2 soft-cap; 3 and 4 are 1 and 2 with the
   // prologue's score terms (KT): a Q add's per-key term and, under the
   // soft-cap, the row term of a K add
-  constexpr int MK = MOD >= 3 ? MOD - 2 : MOD;
-  constexpr bool KT = MOD >= 3;
+  // MOD 5: ALiBi whose linear part rides in the QK contraction (one extra
+  // K=16 step against constant operands), so the softmax is the plain one
+  // plus a per-tile row constant; see the notes at the MMA issuer
+  constexpr bool AMMA = MOD == 5;
+  constexpr int MK = AMMA ? 0 : (MOD >= 3 ? MOD - 2 : MOD);
+  constexpr bool KT = MOD == 3 || MOD == 4;
   constexpr int NSK = Cfg::NSK, NSV = Cfg::NSV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -229,6 +263,30 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
     tmem_relinquish();
+  }
+  if constexpr (AMMA) {
+    // The slope in raw-score units, a = alibi_log2 / scale_log2 (scale > 0),
+    // as a bf16 pair a_hi + a_lo (products with key offsets n <= 127, exact
+    // in bf16, then carry a to about 2^-17).  32-byte swizzle: a row's
+    // 16-byte chunk c sits at chunk c ^ ((row >> 2) & 1).
+    const float a = p.alibi_log2 / p.scale_log2;
+    const __nv_bfloat16 ah = __float2bfloat16_rn(a);
+    const __nv_bfloat16 al = __float2bfloat16_rn(a - __bfloat162float(ah));
+    const uint32_t qpos = pack_bf16x2(__bfloat162float(ah), __bfloat162float(al));
+    const uint32_t qneg = pack_bf16x2(-__bfloat162float(ah), -__bfloat162float(al));
+    uint8_t *aug = smem + Cfg::kOffAug;
+    for (int row = threadIdx.x; row < 128; row += blockDim.x) {
+      const uint32_t kn = pack_bf16x2((float)row, (float)row);
+      const int sw = (row >> 2) & 1;
+      const uint32_t vals[3] = {qpos, qneg, kn};
+#pragma unroll
+      for (int b = 0; b < 3; ++b) {
+        uint8_t *base = aug + b * 4096 + row * 32;
+        *reinterpret_cast<uint4 *>(base + (sw << 4)) = make_uint4(vals[b], 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(base + ((1 ^ sw) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -373,7 +431,13 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
     const uint64_t dv0 = smem_desc_sw128(sVa, kBlockN * 128, 1024);
     const uint32_t q_lo = (uint32_t)dq0, k_lo = (uint32_t)dk0, qk_hi = (uint32_t)(dq0 >> 32);
     const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
-    auto qk = [&](int X, int st) {
+    // MOD 5: one more K=16 step adds a * (j - j0) (left of every row's
+    // diagonal, or under a causal mask) or -a * (j - j0) (right of it) to
+    // each score of the key tile starting at j0; tiles that straddle the
+    // diagonal get no extra step (the softmax takes |i' - j| per element).
+    const uint64_t aug_q0 = smem_desc_sw32(smem_u32(smem + Cfg::kOffAug));
+    const uint32_t aug_lo = (uint32_t)aug_q0, aug_hi = (uint32_t)(aug_q0 >> 32);
+    auto qk = [&](int X, int st, int kt) {
       const uint32_t d = tmem + (X ? 128u : 0u);
       uint32_t a = q_lo + (uint32_t)(X * (Cfg::kQTileBytes >> 4));
       uint32_t b = k_lo + (uint32_t)(st * (Cfg::kKBytes >> 4));
@@ -384,6 +448,12 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
         const uint32_t step = ((ks + 1) & 3) ? 2u : (uint32_t)((kBlockM * 128 - 96) >> 4);
         a += step;
         b += step;
+      }
+      if constexpr (AMMA) {
+        const int side = alibi_side(p, pi.x[0], kt);
+        if (side != 0)
+          mma_ss_w<1>(d, aug_lo + (side > 0 ? 0u : (4096u >> 4)), aug_hi, aug_lo + (2u * 4096u >> 4), aug_hi,
+                      idesc_qk);
       }
       tc_commit(smem_u32(s_full + X));
     };
@@ -408,8 +478,8 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
       ok = mbar_wait(smem_u32(k_full + 0), 0, abort_flag, p.err);
       if (ok) {
         tc_fence_after();
-        if (a0) qk(0, 0);
-        if (a1) qk(1, 0);
+        if (a0) qk(0, 0, first_kt);
+        if (a1) qk(1, 0, first_kt);
         tc_commit(smem_u32(k_empty + 0));
       }
       int j = 0;
@@ -432,7 +502,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
         if (more) {
           if (!(ok = mbar_wait(smem_u32(k_full + st), ((j + 1) / NSK) & 1, abort_flag, p.err))) break;
           tc_fence_after();
-          if (n0) qk(0, st);
+          if (n0) qk(0, st, kn);
         }
         if (a1) {
           if (!(ok = mbar_wait(smem_u32(p_full + 1), n_pv[1] & 1, abort_flag, p.err))) break;
@@ -442,7 +512,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
         }
         tc_commit(smem_u32(v_empty + sv));
         if (more) {
-          if (n1) qk(1, st);
+          if (n1) qk(1, st, kn);
           tc_commit(smem_u32(k_empty + st));
         }
         a0 = n0;
@@ -513,6 +583,20 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
         if (j0 < hx.ip_max - p.window + 1) need_mask = true;
         if (!p.causal && j0 + kBlockN - 1 > hx.ip_min + p.window - 1) need_mask = true;
       }
+      // MOD 5: S already holds -+slope (j - j0) in raw units for a tile on
+      // one side of the diagonal; the rest of the bias, -+slope (i' - j0),
+      // is a row constant (ct, log2 units) that joins the max and the
+      // exponent's reference.  A straddling tile (lin false) takes the
+      // per-element form instead.
+      bool lin = true;
+      float ct = 0.f;
+      if constexpr (AMMA) {
+        const int side = alibi_side(p, hx, kt);
+        lin = side != 0;
+        ct = side > 0 ? p.alibi_log2 * (float)(j0 - ip) : p.alibi_log2 * (float)(ip - j0);
+      }
+      const float cexp_t = AMMA ? (lin ? p.scale_log2 : 1.f) : cexp;
+      const float mshift_t = (AMMA && lin) ? ct : 0.f;
       // Scores of 32 keys starting at key jc, in scaled log2 units (the fast
       // path keeps raw scores and folds the scale into the exponent's FMA).
       auto scores = [&](float (&v)[32], int jc) {
@@ -576,6 +660,13 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
             v[e] = x;
           }
         }
+        if constexpr (AMMA) {
+          if (!lin) {
+            const float dbase = (float)(ip - jc);   // |i' - j| = |dbase - e|, exact in fp32
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = fmaf(-p.alibi_log2, fabsf(dbase - (float)e), v[e] * p.scale_log2);
+          }
+        }
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -604,7 +695,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
-            chunk_exp(sv[c], cexp, m_use, pk, acc);
+            chunk_exp(sv[c], cexp_t, AMMA ? m_use - mshift_t : m_use, pk, acc);
             tmem_st16(sa + c * 16, pk);
           }
         };
@@ -641,7 +732,11 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
 #pragma unroll
           for (int k = 0; k < 5; ++k) t3[k] = max3(t2[3 * k], t2[3 * k + 1], t2[3 * k + 2]);
           float tmax = fmaxf(max3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
-          if (fast && tmax != -INFINITY) tmax *= p.scale_log2;
+          if constexpr (AMMA) {
+            if (lin && tmax != -INFINITY) tmax = fmaf(tmax, p.scale_log2, ct);
+          } else {
+            if (fast && tmax != -INFINITY) tmax *= p.scale_log2;
+          }
           const float m_new = fmaxf(m_ref, tmax);
           const bool need = m_new > m_ref + kRescaleThreshold;
           warp_need = __any_sync(0xffffffffu, need);

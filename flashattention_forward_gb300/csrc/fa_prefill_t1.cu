@@ -1,6 +1,7 @@
 // Ping-pong prefill kernels with one 128-row query tile per CTA, so that two
-// CTAs share an SM (bf16 K/V, Dk = Dv in {64, 128}, plain, ALiBi and
-// soft-cap scores, packed or paged K/V with pages of >= 16 keys).
+// CTAs share an SM (bf16 K/V, Dk = Dv in {64, 128}, plain, ALiBi, soft-cap
+// and ALiBi with its bias in the contraction (MOD 5), packed or paged K/V
+// with pages of >= 16 keys).
 #include "fa_prefill2_launch.cuh"
 
 namespace fa {
@@ -10,6 +11,7 @@ static cudaError_t t1_by_mod(const PrefillLaunch &L) {
     case 0: return prefill2_launch_t1<D, PAGED, 0>(L);
     case 1: return prefill2_launch_t1<D, PAGED, 1>(L);
     case 2: return prefill2_launch_t1<D, PAGED, 2>(L);
+    case 5: return prefill2_launch_t1<D, PAGED, 5>(L);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -3,7 +3,9 @@ per SM) and with two: each form forced for a whole process through
 FA_GB300_PREFILL_VARIANT (read once per process), on ragged, causal,
 windowed, masked and score-modded cases.  A query tile walks the same key
 tiles in the same order either way, so the two forms must agree bit for bit,
-and both with the fp64 oracle."""
+and both with the fp64 oracle -- except under ALiBi, where the one-tile form
+adds the bias's linear part inside the QK contraction (other roundings):
+there both forms are held to the oracle."""
 import os
 import subprocess
 import sys
@@ -27,6 +29,7 @@ CASES = [
     dict(lens_q=[200, 64], lens_k=[100, 10], hq=2, dk=128, causal=True),
     dict(lens_q=[130, 900], lens_k=[400, 900], hq=8, hkv=1, dk=128, causal=True, window=100),
     dict(lens_q=[300, 513], lens_k=[300, 600], hq=4, dk=128, mod="alibi", alibi_slope=0.0625, causal=True),
+    dict(lens_q=[300, 700], lens_k=[500, 700], hq=4, dk=64, mod="alibi", alibi_slope=0.0625),    # straddling tiles
     dict(lens_q=[300, 640], lens_k=[300, 700], hq=4, dk=128, mod="softcap", softcap=5.0),
     dict(lens_q=[300, 650], lens_k=[330, 650], hq=4, hkv=2, dk=128, block_mask_density=0.5),
     dict(lens_q=[70, 300, 1, 400], lens_k=[200, 300, 1000, 400], hq=8, hkv=2, dk=128, page_size=64,
@@ -71,11 +74,13 @@ def test_one_and_two_tiles_per_cta_agree_bit_for_bit_and_with_the_oracle(tmp_pat
     one = _run(2, str(tmp_path / "one.npz"))
     two = _run(3, str(tmp_path / "two.npz"))
     for i, kw in enumerate(CASES):
-        assert np.array_equal(one["o%d" % i], two["o%d" % i]), i
-        assert np.array_equal(one["l%d" % i], two["l%d" % i]), i
+        if kw.get("mod") != "alibi":
+            assert np.array_equal(one["o%d" % i], two["o%d" % i]), i
+            assert np.array_equal(one["l%d" % i], two["l%d" % i]), i
         kw = dict(kw)
         lq = kw.pop("lens_q")
         lk = kw.pop("lens_k", None)
         p = fi.make_problem(lq, lk, seed=700 + i, **kw)
         ro, rl = oracle.forward(p)
         compare(one["o%d" % i], one["l%d" % i], ro, rl)
+        compare(two["o%d" % i], two["l%d" % i], ro, rl)
