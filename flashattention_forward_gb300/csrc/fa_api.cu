@@ -181,9 +181,10 @@ int prefill_variant() {
 // 50% block mask +26%, soft-cap +3-4%, ALiBi causal +2%, config-2 lengths
 // +4% (+10% causal); long dense plain runs -3% and ALiBi non-causal -4%
 // (one-tile CTAs reload K/V twice as often); a grid of a few CTAs is
-// faster with two tiles.  ALiBi runs one tile per CTA so that its bias can
-// ride in the contraction (MOD 5; fa_prefill2.cuh): config 5's ALiBi runs
-// measured +7.9% causal, +2.3% non-causal against the best earlier form.
+// faster with two tiles.  With ALiBi's bias in the contraction (MOD 5,
+// either form; fa_prefill2.cuh) config 5's causal run is faster with one
+// tile (944 against 932 TFLOP/s) and the non-causal one with two (1070
+// against 1034).
 struct TileHints {
   double avg_key_tiles;   // key tiles a query tile visits, on average
   double n_tiles;         // query tiles x heads, about
@@ -194,7 +195,7 @@ int tiles_per_cta(bool eligible, int variant, const TileHints &h) {
   if (!eligible || variant == 1 || variant == 3) return 2;
   if (variant == 2) return 1;
   if (h.n_tiles <= 64) return 2;
-  if (h.block_mask || h.window || h.mod == 2 || h.avg_key_tiles <= 8.0 || h.mod == 1) return 1;
+  if (h.block_mask || h.window || h.mod == 2 || h.avg_key_tiles <= 8.0 || (h.mod == 1 && h.causal)) return 1;
   return 2;
 }
 
@@ -1007,9 +1008,10 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     p.alibi_log2 = 0.f;
   }
   L.mod = terms ? kmod + 2 : kmod;
-  // ALiBi with a positive scale on the one-tile ping-pong kernel: the bias's
-  // linear part goes into the QK contraction (MOD 5)
-  if (L.mod == 1 && mod == 1 && ntiles == 1 && softmax_scale > 0.f) L.mod = 5;
+  // ALiBi with a positive scale on the ping-pong kernel (register-split
+  // variants): the bias's linear part goes into the QK contraction (MOD 5)
+  const bool alibi_mma_ok = !fp8 && !q8 && Dk == Dv && (Dk == 64 || Dk == 128) && !(paged && page_size < 16);
+  if (L.mod == 1 && mod == 1 && alibi_mma_ok && softmax_scale > 0.f && prefill_variant() != 1) L.mod = 5;
   p.head_group = (int)head_group;
   p.n_hgroups = (int)n_hgroups;
   p.n_items = (int)n_blocks;

@@ -35,9 +35,11 @@ namespace fa {
 template <int DK, int DV, bool PAGED, int MOD, bool BIGREG, int NT = 2>
 struct Prefill2Cfg {
   static_assert(NT == 2 || (NT == 1 && BIGREG), "one query tile per CTA: register-split variant only");
-  static_assert(MOD != 5 || NT == 1, "ALiBi in the contraction: one tile per CTA");
+  static_assert(MOD != 5 || BIGREG, "ALiBi in the contraction: register-split variants only");
   // K/V ring depths; one tile per CTA keeps two CTAs' rings within an SM
-  static constexpr int NSK = NT == 2 ? ((DK <= 64) ? 4 : 3) : ((DK <= 64) ? 3 : 1);
+  // (MOD 5 at Dk 128 with two tiles: one K stage fewer, for its 12 KB of
+  // constant operands)
+  static constexpr int NSK = NT == 2 ? ((DK <= 64) ? 4 : (MOD == 5 ? 2 : 3)) : ((DK <= 64) ? 3 : 1);
   static constexpr int NSV = NT == 2 ? ((DK <= 64) ? 4 : 2) : ((DK <= 64) ? 2 : 1);
   static constexpr int kQTileBytes = kBlockM * DK * 2;
   static constexpr int kKBytes = kBlockN * DK * 2;
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(Prefill2Cfg<DK, DV, PAGED, MOD, BIGREG, NT>::k
         b += step;
       }
       if constexpr (AMMA) {
-        const int side = alibi_side(p, pi.x[0], kt);
+        const int side = alibi_side(p, X ? pi.x[1] : pi.x[0], kt);
         if (side != 0)
           mma_ss_w<1>(d, aug_lo + (side > 0 ? 0u : (4096u >> 4)), aug_hi, aug_lo + (2u * 4096u >> 4), aug_hi,
                       idesc_qk);

@@ -36,8 +36,13 @@ cudaError_t prefill2_launch_one(const PrefillLaunch &L) {
 
 template <int D, bool PAGED, int MOD>
 cudaError_t prefill2_pick(const PrefillLaunch &L) {
-  if (L.variant != 1 && prefill2_bigreg_fits<D, PAGED, MOD>()) return prefill2_launch_one<D, PAGED, MOD, true>(L);
-  return prefill2_launch_one<D, PAGED, MOD, false>(L);
+  if constexpr (MOD == 5) {   // the one-pass softmax only
+    if (!prefill2_bigreg_fits<D, PAGED, MOD>()) return cudaErrorNotSupported;
+    return prefill2_launch_one<D, PAGED, MOD, true>(L);
+  } else {
+    if (L.variant != 1 && prefill2_bigreg_fits<D, PAGED, MOD>()) return prefill2_launch_one<D, PAGED, MOD, true>(L);
+    return prefill2_launch_one<D, PAGED, MOD, false>(L);
+  }
 }
 
 // MOD 0 plain, 1 ALiBi, 2 soft-cap; 3 and 4 (a prologue's per-key score
@@ -57,6 +62,7 @@ cudaError_t prefill2_by_mod(const PrefillLaunch &L) {
     case 0: return prefill2_pick<D, PAGED, 0>(L);
     case 1: return prefill2_pick<D, PAGED, 1>(L);
     case 2: return prefill2_pick<D, PAGED, 2>(L);
+    case 5: return prefill2_pick<D, PAGED, 5>(L);
     default: return launch_prefill2_kt(D, L);
   }
 }
