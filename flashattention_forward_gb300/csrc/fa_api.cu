@@ -1010,7 +1010,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
   L.mod = terms ? kmod + 2 : kmod;
   // ALiBi with a positive scale on the ping-pong kernel (register-split
   // variants): the bias's linear part goes into the QK contraction (MOD 5)
-  const bool alibi_mma_ok = !fp8 && !q8 && Dk == Dv && (Dk == 64 || Dk == 128) && !(paged && page_size < 16);
+  const bool alibi_mma_ok = !fp8 && !q8 && Dk == Dv && (Dk == 64 || Dk == 128);
   if (L.mod == 1 && mod == 1 && alibi_mma_ok && softmax_scale > 0.f && prefill_variant() != 1) L.mod = 5;
   p.head_group = (int)head_group;
   p.n_hgroups = (int)n_hgroups;
