@@ -716,7 +716,9 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     L.kv = kv_dt == FA_E4M3 ? 1 : (kv_dt == FA_I8 ? 2 : 0);
     const int rows_box = paged ? (page_size < fa::kDecStageKeys ? page_size : fa::kDecStageKeys) : fa::kDecStageKeys;
     if (have_keys && fp8) {
-      // byte caches: one box per page piece, all D bytes of a key, unswizzled
+      // byte caches: one box per page piece, all D bytes of a key; at D = 128
+      // 128-byte swizzled (the kernel reads the bytes into MMA fragments)
+      const CUtensorMapSwizzle kv8_swz = Dk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
       if (vec5) {
         if ((st = make_vec5_maps(&L.tm_k, &L.tm_v, k_cache, v_cache, Dk, Dv, Hkv, page_size, n_pages,
                                  (uint32_t)rows_box, (uint32_t)(Dk / 16), (uint32_t)Dv, (uint32_t)(rows_box / 16))))
@@ -726,15 +728,15 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
         const uint64_t sk[3] = {(uint64_t)(k_cache->stride[2]), (uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
         const uint64_t sv[3] = {(uint64_t)(v_cache->stride[2]), (uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
         const uint32_t box[4] = {(uint32_t)Dk, 1, (uint32_t)rows_box, 1};
-        if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, box, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
-        if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dk, sv, box, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+        if ((st = make_map(&L.tm_k, kv_tmdt, 4, k_cache->data, dk, sk, box, "k8", kv8_swz))) return st;
+        if ((st = make_map(&L.tm_v, kv_tmdt, 4, v_cache->data, dk, sv, box, "v8", kv8_swz))) return st;
       } else {
         const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)k_cache->shape[0]};
         const uint64_t sk[2] = {(uint64_t)(k_cache->stride[1]), (uint64_t)(k_cache->stride[0])};
         const uint64_t sv[2] = {(uint64_t)(v_cache->stride[1]), (uint64_t)(v_cache->stride[0])};
         const uint32_t box[3] = {(uint32_t)Dk, 1, (uint32_t)rows_box};
-        if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, box, "k8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
-        if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dk, sv, box, "v8", CU_TENSOR_MAP_SWIZZLE_NONE))) return st;
+        if ((st = make_map(&L.tm_k, kv_tmdt, 3, k_cache->data, dk, sk, box, "k8", kv8_swz))) return st;
+        if ((st = make_map(&L.tm_v, kv_tmdt, 3, v_cache->data, dk, sv, box, "v8", kv8_swz))) return st;
       }
     } else if (have_keys) {
       if (paged) {

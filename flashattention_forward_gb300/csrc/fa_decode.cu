@@ -7,9 +7,10 @@ template <int D, int KV, bool V5>
 static cudaError_t launch_decode_d(const DecodeLaunch &L) {
   static unsigned long long done = 0;
   auto kern = fa_decode_kernel<D, KV, V5>;
-  cudaError_t e = ensure_smem_attr(kern, DecodeCfg<D, KV>::kSmemBytes, &done);
+  constexpr int kSmem = DecodeCfg<D, KV, dec_direct<D, KV, V5>()>::kSmemBytes;
+  cudaError_t e = ensure_smem_attr(kern, kSmem, &done);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, kDecThreads, DecodeCfg<D, KV>::kSmemBytes, L.stream>>>(L.tm_k, L.tm_v, L.p);
+  kern<<<L.grid, kDecThreads, kSmem, L.stream>>>(L.tm_k, L.tm_v, L.p);
   return cudaGetLastError();
 }
 

@@ -82,19 +82,26 @@ struct DecodeParams {
   int32_t n_qblk, n_kblk;
 };
 
-template <int D, int KV = 0>
+// DIRECT (byte caches at D = 128, token-major pages): the stage's K and V
+// bytes land 128-byte swizzled and go from shared memory straight into the
+// MMA fragments (see the consumer), with no f16 copy in between.
+template <int D, int KV = 0, bool DIRECT = false>
 struct DecodeCfg {
+  static_assert(!DIRECT || (KV && D == 128), "fragment-direct bytes: byte caches at D = 128");
   static constexpr int kElt = KV ? 1 : 2;                  // cache bytes per element
   static constexpr int kKBytes = kDecStageKeys * D * kElt;   // per stage
   static constexpr int kVBytes = kDecStageKeys * D * kElt;
   static constexpr int kScaleBytes = KV ? 2 * kDecStageKeys * 4 : 0;   // k then v scales of the stage
-  static constexpr int kStageBytes = kKBytes + kVBytes + kScaleBytes;
+  // DIRECT: stages start on 1024-byte boundaries (the swizzle pattern's period)
+  static constexpr int kStageBytes = DIRECT ? (kKBytes + kVBytes + kScaleBytes + 1023) / 1024 * 1024
+                                            : kKBytes + kVBytes + kScaleBytes;
   // byte caches: a deeper ring of half-size stages keeps as many bytes in
-  // flight as the bf16 ring does
-  static constexpr int NST = KV ? 5 : kDecStages;
+  // flight as the bf16 ring does (DIRECT: one more, in the conversion
+  // buffers' room)
+  static constexpr int NST = KV ? (DIRECT ? 6 : 5) : kDecStages;
   static constexpr int kOffStages = 0;
   // byte caches: per consumer warp, its 16 keys of K, then of V, as swizzled f16
-  static constexpr int kConvWarpBytes = KV ? 16 * D * 2 : 0;
+  static constexpr int kConvWarpBytes = (KV && !DIRECT) ? 16 * D * 2 : 0;
   static constexpr int kOffConv = ((NST * kStageBytes + 1023) / 1024) * 1024;
   static constexpr int kOffQ = kOffConv + kDecWarps * kConvWarpBytes;   // 16 x D bf16 (f16 for byte caches)
   static constexpr int kOffQInv = kOffQ + kDecRows * D * 2;            // byte caches: 2^-e per Q row
@@ -169,11 +176,15 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 
 // V5: byte caches in the vectorized 5-D pages (a kernel of its own, so that
 // the token-major kernels keep their register allocation).
+template <int D, int KV, bool V5>
+constexpr bool dec_direct() { return KV != 0 && D == 128 && !V5; }
+
 template <int D, int KV = 0, bool V5 = false>
 __global__ void __launch_bounds__(kDecThreads, 2)
     fa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p) {
-  using Cfg = DecodeCfg<D, KV>;
+  constexpr bool DIRECT = dec_direct<D, KV, V5>();
+  using Cfg = DecodeCfg<D, KV, DIRECT>;
   constexpr int NCB = D / 64;          // 64-dim column blocks
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -338,8 +349,13 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             dec_cp_async_4(sdst + 4 * (kDecStageKeys + kk), live ? p.v_scale + at : p.v_scale, live ? 4u : 0u);
           }
           dec_cp_async_arrive_noinc(smem_u32(full + slot_i));
-          gather_block<kDecStageKeys, D, kGatherPlain, 4>(kd, p.gk, hk, key0, p.page_size - 1, 0, pg, lane);
-          gather_block<kDecStageKeys, D, kGatherPlain, 4>(vd, p.gv, hk, key0, p.page_size - 1, 0, pg, lane);
+          if constexpr (DIRECT) {
+            gather_block<kDecStageKeys, 128, kGatherSw128, 4>(kd, p.gk, hk, key0, p.page_size - 1, 0, pg, lane);
+            gather_block<kDecStageKeys, 128, kGatherSw128, 4>(vd, p.gv, hk, key0, p.page_size - 1, 0, pg, lane);
+          } else {
+            gather_block<kDecStageKeys, D, kGatherPlain, 4>(kd, p.gk, hk, key0, p.page_size - 1, 0, pg, lane);
+            gather_block<kDecStageKeys, D, kGatherPlain, 4>(vd, p.gv, hk, key0, p.page_size - 1, 0, pg, lane);
+          }
         } else {
 #pragma unroll
           for (int cb = 0; cb < NCB; ++cb) {
@@ -391,7 +407,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const int slot = key0 & (p.page_size - 1);
         if constexpr (KV) {
           // one box per page piece: rows_per_box keys x D bytes, unswizzled
-          // (5-D: K as [D/16][rows][16], V as [rows/16][D][16 tokens])
+          // (DIRECT: 128-byte swizzled; 5-D: K as [D/16][rows][16], V as
+          // [rows/16][D][16 tokens])
           const uint32_t off = bx * p.rows_per_box * D;
           if (V5) {
             tma_load_5d(smem_u32(kd + off), &tm_k, smem_u32(full + slot_i), 0, slot, 0, hk, pg);
@@ -422,7 +439,24 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     // ------------------------------------------------------- consumers --
     // Q fragments (A operand, 16 rows x D) for all D/16 k-steps.
     uint32_t qf[D / 16][4];
-    {
+    if constexpr (DIRECT) {
+      // The contraction index is permuted so that a lane's K bytes are
+      // contiguous: in k-step ks, lane (g, t) holds the MMA's k positions
+      // 2t, 2t+1, 2t+8, 2t+9, which stand for the dims 32t + 4ks + 0..3 --
+      // four consecutive bytes of a key row.  Q takes the same order: a0/a2
+      // of row r are its f16 pairs at dims 32t + 4ks and 32t + 4ks + 2.
+      const int g = lane >> 2, t = lane & 3;
+      const __half *q16 = reinterpret_cast<const __half *>(sQ);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint2 lo = *reinterpret_cast<const uint2 *>(q16 + g * D + 32 * t + 4 * ks);
+        const uint2 hi = *reinterpret_cast<const uint2 *>(q16 + (g + 8) * D + 32 * t + 4 * ks);
+        qf[ks][0] = lo.x;
+        qf[ks][1] = hi.x;
+        qf[ks][2] = lo.y;
+        qf[ks][3] = hi.y;
+      }
+    } else {
       const uint32_t qbase = smem_u32(sQ);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -538,7 +572,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         __syncwarp();
       };
       if constexpr (KV) {
-        convert(kd, koff);
+        if constexpr (!DIRECT) convert(kd, koff);
         const float *sct = reinterpret_cast<const float *>(vd + Cfg::kVBytes);
 #pragma unroll
         for (int n = 0; n < 2; ++n)
@@ -564,8 +598,30 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       float s[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      if constexpr (DIRECT) {
+        // Lane (g, t) reads 32 bytes (dims 32t .. 32t+31) of keys g and 8+g
+        // of the warp's 16: chunks 2t and 2t+1, swizzled by the row (kw0 is a
+        // multiple of 16, so both rows swizzle by g).  A quarter warp covers
+        // all eight chunk positions: no bank conflicts.
+        const int g = lane >> 2, t = lane & 3;
+        const uint8_t *k0 = kd + (kw0 + g) * 128, *k1 = kd + (kw0 + 8 + g) * 128;
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(k0 + (((2 * t) ^ g) << 4));
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(k0 + (((2 * t + 1) ^ g) << 4));
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(k1 + (((2 * t) ^ g) << 4));
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(k1 + (((2 * t + 1) ^ g) << 4));
+        const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t w1[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b0, b1;
+          dec_bytes4_to_f16<KV>(w0[ks], b0, b1);
+          dec_mma<KV>(s[0], qf[ks], b0, b1);
+          dec_bytes4_to_f16<KV>(w1[ks], b0, b1);
+          dec_mma<KV>(s[1], qf[ks], b0, b1);
+        }
+      }
+#pragma unroll
+      for (int ks = 0; ks < (DIRECT ? 0 : D / 16); ++ks) {
         // matrices: (keys 0-7, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 0-7), (keys 8-15, dims 8-15)
         const int krow = (lane & 7) + (lane >> 4) * 8;   // key within the warp's 16
         const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
@@ -653,7 +709,39 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
         pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
       }
-      if constexpr (KV) {
+      if constexpr (DIRECT) {
+        // O += P V with the bytes in registers.  Lane (g, t) reads the 16
+        // bytes of dims 16g .. 16g+15 of keys 2t, 2t+1, 2t+8 and 2t+9 (the
+        // k positions its B fragments hold; chunk g swizzled by the row:
+        // conflict-free per quarter warp), zeroes keys past key_hi (their
+        // bytes may be anything, and 0 * NaN would be NaN), and pairs the
+        // keys' bytes per dim with byte permutes.  The output dims are
+        // permuted too: n-tile j, column n stands for dim 16n + j.
+        const int g = lane >> 2, t = lane & 3;
+        const int rk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+        uint4 vr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = kw0 + rk[i];
+          vr[i] = *reinterpret_cast<const uint4 *>(vd + row * 128 + ((g ^ (row & 7)) << 4));
+          if (key_base + rk[i] >= key_hi) vr[i] = make_uint4(0, 0, 0, 0);
+        }
+        const uint32_t r0w[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w}, r1w[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+        const uint32_t r2w[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w}, r3w[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t b0[4], b1[4];   // per dim 16g + 4w + i: keys (2t, 2t+1) and (2t+8, 2t+9)
+          dec_bytes4_to_f16<KV>(__byte_perm(r0w[w], r1w[w], 0x5140), b0[0], b0[1]);
+          dec_bytes4_to_f16<KV>(__byte_perm(r0w[w], r1w[w], 0x7362), b0[2], b0[3]);
+          dec_bytes4_to_f16<KV>(__byte_perm(r2w[w], r3w[w], 0x5140), b1[0], b1[1]);
+          dec_bytes4_to_f16<KV>(__byte_perm(r2w[w], r3w[w], 0x7362), b1[2], b1[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dec_mma<KV>(o[4 * w + i], pa, b0[i], b1[i]);
+        }
+        // every lane has used its K and V bytes and the stage's scales
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + slot_i));
+      } else if constexpr (KV) {
         __syncwarp();                 // the QK product has read K from the buffer
         if constexpr (V5) {
           // 5-D V (the token group at v5off): lane (octet oc, half th)
@@ -685,7 +773,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       // O += P V : D/8 n-tiles of 8 dims, one k-step of 16 keys.
 #pragma unroll
-      for (int nd = 0; nd < D / 16; ++nd) {
+      for (int nd = 0; nd < (DIRECT ? 0 : D / 16); ++nd) {
         // matrices: (keys 0-7, dims 0-7), (keys 8-15, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 8-15)
         const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // key within the warp's 16
         const int dim = nd * 16 + (lane >> 4) * 8;
@@ -715,11 +803,13 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     if (ok) {
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
-        const int c = n * 8 + (lane & 3) * 2;
+        // DIRECT: n-tile n, column 2t + e is dim 16 (2t + e) + n
+        const int c = DIRECT ? 32 * (lane & 3) + n : n * 8 + (lane & 3) * 2;
+        const int c1 = DIRECT ? c + 16 : c + 1;
         red_o[(warp * kDecRows + r0) * D + c] = o[n][0];
-        red_o[(warp * kDecRows + r0) * D + c + 1] = o[n][1];
+        red_o[(warp * kDecRows + r0) * D + c1] = o[n][1];
         red_o[(warp * kDecRows + r1) * D + c] = o[n][2];
-        red_o[(warp * kDecRows + r1) * D + c + 1] = o[n][3];
+        red_o[(warp * kDecRows + r1) * D + c1] = o[n][3];
       }
       if ((lane & 3) == 0) {
         red_ml[(warp * kDecRows + r0) * 2] = m0;
