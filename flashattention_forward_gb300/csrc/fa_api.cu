@@ -714,6 +714,7 @@ fa_status_t fwd_build(const fa_tensor_t *q, const fa_tensor_t *k_cache, const fa
     fa::DecodeLaunch L;
     memset(&L, 0, sizeof L);
     L.kv = kv_dt == FA_E4M3 ? 1 : (kv_dt == FA_I8 ? 2 : 0);
+    L.rows8 = (int64_t)launch->max_seqlen_q * group <= 8;
     const int rows_box = paged ? (page_size < fa::kDecStageKeys ? page_size : fa::kDecStageKeys) : fa::kDecStageKeys;
     if (have_keys && fp8) {
       // byte caches: one box per page piece, all D bytes of a key; at D = 128

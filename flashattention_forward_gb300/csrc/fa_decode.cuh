@@ -84,10 +84,13 @@ struct DecodeParams {
 
 // DIRECT (byte caches at D = 128, token-major pages): the stage's K and V
 // bytes land 128-byte swizzled and go from shared memory straight into the
-// MMA fragments (see the consumer), with no f16 copy in between.
-template <int D, int KV = 0, bool DIRECT = false>
+// MMA fragments (see the consumer), with no f16 copy in between.  OT (with
+// DIRECT, at most 8 query rows): P V is computed transposed, half the MMAs
+// and accumulators, which lets three CTAs share an SM.
+template <int D, int KV = 0, bool DIRECT = false, bool OT = false>
 struct DecodeCfg {
   static_assert(!DIRECT || (KV && D == 128), "fragment-direct bytes: byte caches at D = 128");
+  static_assert(!OT || DIRECT, "the transposed P V runs on the fragment-direct path");
   static constexpr int kElt = KV ? 1 : 2;                  // cache bytes per element
   static constexpr int kKBytes = kDecStageKeys * D * kElt;   // per stage
   static constexpr int kVBytes = kDecStageKeys * D * kElt;
@@ -98,7 +101,7 @@ struct DecodeCfg {
   // byte caches: a deeper ring of half-size stages keeps as many bytes in
   // flight as the bf16 ring does (DIRECT: one more, in the conversion
   // buffers' room)
-  static constexpr int NST = KV ? (DIRECT ? 6 : 5) : kDecStages;
+  static constexpr int NST = KV ? (DIRECT ? (OT ? 4 : 6) : 5) : kDecStages;
   static constexpr int kOffStages = 0;
   // byte caches: per consumer warp, its 16 keys of K, then of V, as swizzled f16
   static constexpr int kConvWarpBytes = (KV && !DIRECT) ? 16 * D * 2 : 0;
@@ -179,12 +182,19 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 template <int D, int KV, bool V5>
 constexpr bool dec_direct() { return KV != 0 && D == 128 && !V5; }
 
-template <int D, int KV = 0, bool V5 = false>
-__global__ void __launch_bounds__(kDecThreads, 2)
+// R8: every CTA has at most 8 query rows (max_seqlen_q * Hq/Hkv <= 8).
+template <int D, int KV = 0, bool V5 = false, bool R8 = false>
+__global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ? 3 : 2)
     fa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p) {
   constexpr bool DIRECT = dec_direct<D, KV, V5>();
-  using Cfg = DecodeCfg<D, KV, DIRECT>;
+  static_assert(!R8 || DIRECT, "the 8-row form exists on the fragment-direct path only");
+  constexpr bool OT = R8;
+  // KDIR (byte caches at D = 128, token-major or 5-D pages): the QK product
+  // reads the raw K bytes into its fragments, with the permuted contraction
+  // order below, so that both page layouts sum the scores alike
+  constexpr bool KDIR = KV != 0 && D == 128;
+  using Cfg = DecodeCfg<D, KV, DIRECT, OT>;
   constexpr int NCB = D / 64;          // 64-dim column blocks
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     // ------------------------------------------------------- consumers --
     // Q fragments (A operand, 16 rows x D) for all D/16 k-steps.
     uint32_t qf[D / 16][4];
-    if constexpr (DIRECT) {
+    if constexpr (KDIR) {
       // The contraction index is permuted so that a lane's K bytes are
       // contiguous: in k-step ks, lane (g, t) holds the MMA's k positions
       // 2t, 2t+1, 2t+8, 2t+9, which stand for the dims 32t + 4ks + 0..3 --
@@ -512,9 +522,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     };
     uint8_t *conv = smem + Cfg::kOffConv + warp * Cfg::kConvWarpBytes;   // byte caches only
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[D / 8][4];
+    // O accumulators: D/8 n-tiles of 8 dims (rows r0, r1), or (OT) O^T as
+    // D/16 m-tiles of 16 dims for the rows 2t, 2t+1 (see the P V product)
+    constexpr int NO = OT ? D / 16 : D / 8;
+    float o[NO][4];
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     // Byte caches: stage offsets of the lane's 16-byte pieces, one per pass
     // (see convert below) -- token rows of D bytes, and K in the vectorized
@@ -532,6 +545,21 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const int kk = kw + off / D, c0 = off % D;
         voff[ps_] = kw * D + off;
         koff[ps_] = V5 ? ((kk >> lg) << lg) * D + ((c0 >> 4) << (4 + lg)) + ((kk & (R - 1)) << 4) : voff[ps_];
+      }
+    }
+    // KDIR: stage offsets of the 16-byte pieces (keys kw + g and kw + 8 + g,
+    // dims 32t .. +15 and 32t+16 .. +31) the lane's QK fragments come from:
+    // token-major rows 128-byte swizzled (kw is a multiple of 16, so both rows
+    // swizzle by g, and a quarter warp covers all eight chunk positions: no
+    // bank conflicts), or the 5-D pieces at (kk / R) R D + (c / 16) 16 R + (kk % R) 16
+    int kdo[4];
+    {
+      const int g = lane >> 2, t = lane & 3, kw = warp * 16;
+      const int R = p.rows_per_box, lg = __ffs(R) - 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kk = kw + g + 8 * (i >> 1), cg = 2 * t + (i & 1);
+        kdo[i] = V5 ? ((kk >> lg) << lg) * D + (cg << (4 + lg)) + ((kk & (R - 1)) << 4) : kk * 128 + ((cg ^ g) << 4);
       }
     }
     bool ok = true;
@@ -572,7 +600,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         __syncwarp();
       };
       if constexpr (KV) {
-        if constexpr (!DIRECT) convert(kd, koff);
+        if constexpr (!KDIR) convert(kd, koff);
         const float *sct = reinterpret_cast<const float *>(vd + Cfg::kVBytes);
 #pragma unroll
         for (int n = 0; n < 2; ++n)
@@ -598,17 +626,13 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       float s[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-      if constexpr (DIRECT) {
+      if constexpr (KDIR) {
         // Lane (g, t) reads 32 bytes (dims 32t .. 32t+31) of keys g and 8+g
-        // of the warp's 16: chunks 2t and 2t+1, swizzled by the row (kw0 is a
-        // multiple of 16, so both rows swizzle by g).  A quarter warp covers
-        // all eight chunk positions: no bank conflicts.
-        const int g = lane >> 2, t = lane & 3;
-        const uint8_t *k0 = kd + (kw0 + g) * 128, *k1 = kd + (kw0 + 8 + g) * 128;
-        const uint4 a0 = *reinterpret_cast<const uint4 *>(k0 + (((2 * t) ^ g) << 4));
-        const uint4 a1 = *reinterpret_cast<const uint4 *>(k0 + (((2 * t + 1) ^ g) << 4));
-        const uint4 c0 = *reinterpret_cast<const uint4 *>(k1 + (((2 * t) ^ g) << 4));
-        const uint4 c1 = *reinterpret_cast<const uint4 *>(k1 + (((2 * t + 1) ^ g) << 4));
+        // of the warp's 16 (offsets kdo, fixed per lane).
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(kd + kdo[0]);
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(kd + kdo[1]);
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(kd + kdo[2]);
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(kd + kdo[3]);
         const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         const uint32_t w1[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
@@ -621,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         }
       }
 #pragma unroll
-      for (int ks = 0; ks < (DIRECT ? 0 : D / 16); ++ks) {
+      for (int ks = 0; ks < (KDIR ? 0 : D / 16); ++ks) {
         // matrices: (keys 0-7, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 0-7), (keys 8-15, dims 8-15)
         const int krow = (lane & 7) + (lane >> 4) * 8;   // key within the warp's 16
         const int dim = ks * 16 + ((lane >> 3) & 1) * 8;
@@ -643,7 +667,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         for (int e = 0; e < 2; ++e) {
           const int j = key_base + n * 8 + (lane & 3) * 2 + e;
           const bool in = j < key_hi;
-          bool ok0 = in && r0 < rows && blk0, ok1 = in && r1 < rows && blk1;
+          bool ok0 = in && r0 < rows && blk0, ok1 = !OT && in && r1 < rows && blk1;
           if (p.causal) { ok0 = ok0 && j <= ip0; ok1 = ok1 && j <= ip1; }
           if (p.window > 0) {
             if (p.causal) { ok0 = ok0 && ip0 - j < p.window; ok1 = ok1 && ip1 - j < p.window; }
@@ -688,12 +712,25 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       // (after the first stages it rarely does); the factors are exactly 1
       // otherwise, so skipping changes nothing.
       if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+        if constexpr (OT) {
+          // rows 2t and 2t+1: their factors from lanes 8t and 8t + 4 (g = row)
+          const int t = lane & 3;
+          const float at0 = __shfl_sync(0xffffffffu, a0, 8 * t), at1 = __shfl_sync(0xffffffffu, a0, 8 * t + 4);
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          o[n][0] *= a0;
-          o[n][1] *= a0;
-          o[n][2] *= a1;
-          o[n][3] *= a1;
+          for (int n = 0; n < NO; ++n) {
+            o[n][0] *= at0;
+            o[n][1] *= at1;
+            o[n][2] *= at0;
+            o[n][3] *= at1;
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NO; ++n) {
+            o[n][0] *= a0;
+            o[n][1] *= a0;
+            o[n][2] *= a1;
+            o[n][3] *= a1;
+          }
         }
       }
       uint32_t pa[4];
@@ -735,8 +772,18 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           dec_bytes4_to_f16<KV>(__byte_perm(r0w[w], r1w[w], 0x7362), b0[2], b0[3]);
           dec_bytes4_to_f16<KV>(__byte_perm(r2w[w], r3w[w], 0x5140), b1[0], b1[1]);
           dec_bytes4_to_f16<KV>(__byte_perm(r2w[w], r3w[w], 0x7362), b1[2], b1[3]);
+          if constexpr (OT) {
+            // O^T += V^T P^T: m-tile j's rows g and g+8 stand for the dims
+            // 16g + 2j and 16g + 2j + 1, so the pairs above are its A
+            // fragments as they come; B = P^T is pa[0] / pa[2] (row g of P,
+            // keys 2t, 2t+1 and 2t+8, 2t+9).  C: rows 2t, 2t+1 of O.
+            const uint32_t e0[4] = {b0[0], b0[1], b1[0], b1[1]}, e1[4] = {b0[2], b0[3], b1[2], b1[3]};
+            dec_mma<KV>(o[2 * w], e0, pa[0], pa[2]);
+            dec_mma<KV>(o[2 * w + 1], e1, pa[0], pa[2]);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dec_mma<KV>(o[4 * w + i], pa, b0[i], b1[i]);
+            for (int i = 0; i < 4; ++i) dec_mma<KV>(o[4 * w + i], pa, b0[i], b1[i]);
+          }
         }
         // every lane has used its K and V bytes and the stage's scales
         __syncwarp();
@@ -800,9 +847,18 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     float *red_o = reinterpret_cast<float *>(stages);                     // [4][16][D]
     float *red_ml = reinterpret_cast<float *>(stages + kDecWarps * kDecRows * D * 4);  // [4][16][2]
     asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
-    if (ok) {
+    if (ok && OT) {
+      // O^T m-tile j of lane (g, t): rows 2t, 2t+1 at the dims 16g + 2j, +1
+      const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
+      for (int j = 0; j < NO; ++j) {
+        const int c = 16 * g + 2 * j;
+        *reinterpret_cast<float2 *>(red_o + (warp * kDecRows + 2 * t) * D + c) = make_float2(o[j][0], o[j][2]);
+        *reinterpret_cast<float2 *>(red_o + (warp * kDecRows + 2 * t + 1) * D + c) = make_float2(o[j][1], o[j][3]);
+      }
+    } else if (ok) {
+#pragma unroll
+      for (int n = 0; n < NO; ++n) {
         // DIRECT: n-tile n, column 2t + e is dim 16 (2t + e) + n
         const int c = DIRECT ? 32 * (lane & 3) + n : n * 8 + (lane & 3) * 2;
         const int c1 = DIRECT ? c + 16 : c + 1;
@@ -811,12 +867,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         red_o[(warp * kDecRows + r1) * D + c] = o[n][2];
         red_o[(warp * kDecRows + r1) * D + c1] = o[n][3];
       }
-      if ((lane & 3) == 0) {
-        red_ml[(warp * kDecRows + r0) * 2] = m0;
-        red_ml[(warp * kDecRows + r0) * 2 + 1] = l0;
-        red_ml[(warp * kDecRows + r1) * 2] = m1;
-        red_ml[(warp * kDecRows + r1) * 2 + 1] = l1;
-      }
+    }
+    if (ok && (lane & 3) == 0) {
+      red_ml[(warp * kDecRows + r0) * 2] = m0;
+      red_ml[(warp * kDecRows + r0) * 2 + 1] = l0;
+      red_ml[(warp * kDecRows + r1) * 2] = m1;
+      red_ml[(warp * kDecRows + r1) * 2 + 1] = l1;
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
     if (ok) {

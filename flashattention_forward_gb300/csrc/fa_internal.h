@@ -29,6 +29,7 @@ struct DecodeLaunch {
   CUtensorMap tm_k, tm_v;
   DecodeParams p;
   int kv;        // cache: 0 bf16, 1 e4m3, 2 int8 (the last two with per-token scales)
+  int rows8;     // every CTA has at most 8 query rows (max_seqlen_q * Hq/Hkv <= 8)
   dim3 grid;
   cudaStream_t stream;
 };

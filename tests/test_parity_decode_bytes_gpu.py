@@ -58,6 +58,11 @@ CASES = {
                                     page_size=32, spare_pages=2, causal=True),
     "paged_e4m3_p1024": dict(lens_q=[1, 1], lens_k=[2500, 100], hq=8, hkv=8, dk=128, kv_dtype="e4m3",
                              page_size=1024, spare_pages=1),
+    # exactly 8 query rows per kv head (2 tokens x 4 heads) and fewer: the transposed P V form
+    "paged_e4m3_rows8_causal": dict(lens_q=[2, 1, 2], lens_k=[500, 77, 1300], hq=8, hkv=2, dk=128,
+                                    kv_dtype="e4m3", page_size=16, spare_pages=4, causal=True),
+    "paged_int8_rows8_alibi": dict(lens_q=[2, 2], lens_k=[640, 129], hq=16, hkv=4, dk=128, kv_dtype="int8",
+                                   page_size=64, spare_pages=2, causal=True, mod="alibi"),
 }
 
 
