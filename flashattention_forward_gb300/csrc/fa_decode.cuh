@@ -20,8 +20,10 @@
 // fp8 KV decode from the raw quantised bytes, half the traffic of bf16).  TMA
 // lands the bytes, the producer lanes copy the stage's per-token k/v scales
 // with cp.async beside them, and each consumer warp turns its own 16 keys into
-// f16 exactly (e4m3 and int8 values are f16 numbers) in a private swizzled
-// buffer.  Q is brought to f16 with a per-row power-of-two factor.  The scales
+// f16 exactly (e4m3 and int8 values are f16 numbers): at D = 128 in registers,
+// straight from the 128-byte-swizzled stage into its MMA fragments (DIRECT
+// below), at D = 64 through a private swizzled f16 buffer.  Q is brought to
+// f16 with a per-row power-of-two factor.  The scales
 // stay in fp32: k_scale multiplies each score column, v_scale each P column
 // before the f16 P V product, so the cached values are never rounded.
 #pragma once
