@@ -7,7 +7,7 @@ template <int D, int KV, bool V5, bool R8 = false>
 static cudaError_t launch_decode_d(const DecodeLaunch &L) {
   static unsigned long long done = 0;
   auto kern = fa_decode_kernel<D, KV, V5, R8>;
-  constexpr int kSmem = DecodeCfg<D, KV, dec_direct<D, KV, V5>(), R8>::kSmemBytes;
+  constexpr int kSmem = DecodeCfg<D, KV, dec_direct<D, KV, V5>(), dec_direct<D, KV, V5>() && R8>::kSmemBytes;
   cudaError_t e = ensure_smem_attr(kern, kSmem, &done);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, kDecThreads, kSmem, L.stream>>>(L.tm_k, L.tm_v, L.p);
@@ -19,6 +19,7 @@ static cudaError_t launch_decode_kv(int d, const DecodeLaunch &L) {
   if constexpr (KV != 0) {
     if (L.p.vec5) {
       if (d == 64) return launch_decode_d<64, KV, true>(L);
+      if (d == 128 && L.rows8) return launch_decode_d<128, KV, true, true>(L);
       if (d == 128) return launch_decode_d<128, KV, true>(L);
       return cudaErrorNotSupported;
     }

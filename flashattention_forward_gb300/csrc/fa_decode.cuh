@@ -190,12 +190,16 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
     fa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p) {
   constexpr bool DIRECT = dec_direct<D, KV, V5>();
-  static_assert(!R8 || DIRECT, "the 8-row form exists on the fragment-direct path only");
-  constexpr bool OT = R8;
+  constexpr bool OT = R8 && DIRECT;
   // KDIR (byte caches at D = 128, token-major or 5-D pages): the QK product
   // reads the raw K bytes into its fragments, with the permuted contraction
   // order below, so that both page layouts sum the scores alike
   constexpr bool KDIR = KV != 0 && D == 128;
+  // QT (with KDIR, at most 8 query rows): QK computed transposed as well,
+  // S^T = K Q^T with N = 8 rows (half the QK MMAs); the thread then owns rows
+  // 2t and 2t+1, and P reaches the P V operand layout by shuffles
+  static_assert(!R8 || KDIR, "the 8-row forms read the key bytes directly");
+  constexpr bool QT = R8;
   using Cfg = DecodeCfg<D, KV, DIRECT, OT>;
   constexpr int NCB = D / 64;          // 64-dim column blocks
   extern __shared__ uint8_t smem_raw[];
@@ -479,7 +483,8 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
       }
     }
     // Rows this thread holds in the C fragments: g0 = lane/4, g1 = lane/4 + 8.
-    const int r0 = lane >> 2, r1 = r0 + 8;
+    // (QT: rows 2t and 2t+1, the columns of the S^T fragment)
+    const int r0 = QT ? 2 * (lane & 3) : lane >> 2, r1 = QT ? r0 + 1 : r0 + 8;
     const int ip0 = (r0 / p.group) + sk - sq;   // bottom-right aligned positions
     const int ip1 = (r1 / p.group) + sk - sq;
     // byte caches: Q rows carry a factor 2^e that the score scale removes
@@ -624,6 +629,95 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
         }
         __syncwarp();
       }
+      float a0, a1;     // the rows' rescale factors (rows r0, r1)
+      uint32_t pa[4];   // P as the A fragment of O = P V (rows g, g+8; keys 2t, 2t+1 / 2t+8, 2t+9)
+      if constexpr (QT) {
+        // S^T = K Q^T for the warp's 16 keys: M = 16 keys (g, g+8), N = 8
+        // rows, the contraction order of the KDIR fragments.  C: keys g and
+        // g+8 (c0/c1 and c2/c3) of rows 2t and 2t+1.  Two partial
+        // accumulators (even and odd k-steps) halve the dependent chain.
+        const uint4 ka0 = *reinterpret_cast<const uint4 *>(kd + kdo[0]);
+        const uint4 ka1 = *reinterpret_cast<const uint4 *>(kd + kdo[1]);
+        const uint4 kc0 = *reinterpret_cast<const uint4 *>(kd + kdo[2]);
+        const uint4 kc1 = *reinterpret_cast<const uint4 *>(kd + kdo[3]);
+        const uint32_t w0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+        const uint32_t w1[8] = {kc0.x, kc0.y, kc0.z, kc0.w, kc1.x, kc1.y, kc1.z, kc1.w};
+        float st[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t ak[4];
+          dec_bytes4_to_f16<KV>(w0[ks], ak[0], ak[2]);
+          dec_bytes4_to_f16<KV>(w1[ks], ak[1], ak[3]);
+          dec_mma<KV>(st[ks & 1], ak, qf[ks][0], qf[ks][2]);
+        }
+        float sv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sv[e] = st[0][e] + st[1][e];
+        const float *sct = reinterpret_cast<const float *>(vd + Cfg::kVBytes);
+        const int g = lane >> 2, t = lane & 3;
+        const bool blk0 = block_live(h0, qb0, key_base / 128), blk1 = block_live(h1, qb1, key_base / 128);
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+        float vk[2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const int jj = kw0 + g + 8 * n;   // key within the stage
+          const int j = key_base + g + 8 * n;
+          const bool in = j < key_hi;
+          bool ok0 = in && r0 < rows && blk0, ok1 = in && r1 < rows && blk1;
+          if (p.causal) { ok0 = ok0 && j <= ip0; ok1 = ok1 && j <= ip1; }
+          if (p.window > 0) {
+            if (p.causal) { ok0 = ok0 && ip0 - j < p.window; ok1 = ok1 && ip1 - j < p.window; }
+            else { ok0 = ok0 && abs(ip0 - j) < p.window; ok1 = ok1 && abs(ip1 - j) < p.window; }
+          }
+          const float kf = sct[jj];
+          vk[n] = sct[kDecStageKeys + jj];
+          float x0 = sv[2 * n], x1 = sv[2 * n + 1];
+          if (p.mod == 0) {
+            x0 = ok0 ? x0 * kf * sc0 : -INFINITY;
+            x1 = ok1 ? x1 * kf * sc1 : -INFINITY;
+          } else {
+            const float cb = (cb_row && in && j < p.cb_ld) ? cb_row[j] : 0.f;
+            x0 = ok0 ? mod_score(x0 * kf * qf0, ip0, j, rt0, cb) : -INFINITY;
+            x1 = ok1 ? mod_score(x1 * kf * qf1, ip1, j, rt1, cb) : -INFINITY;
+          }
+          sv[2 * n] = x0;
+          sv[2 * n + 1] = x1;
+          mx0 = fmaxf(mx0, x0);
+          mx1 = fmaxf(mx1, x1);
+        }
+        // the rows' maxima over the 16 keys: the 8 lanes of each t
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        a0 = ex2(m0 - mu0);
+        a1 = ex2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        float pp[4];
+        pp[0] = ex2(sv[0] - mu0);
+        pp[1] = ex2(sv[1] - mu1);
+        pp[2] = ex2(sv[2] - mu0);
+        pp[3] = ex2(sv[3] - mu1);
+        l0 = l0 * a0 + (pp[0] + pp[2]);   // per-thread partial sums; reduced over g at the end
+        l1 = l1 * a1 + (pp[1] + pp[3]);
+        // P (times the keys' v scales) to the A layout: lane (g, t) needs
+        // row g at keys 2t, 2t+1 (and + 8), held by lanes (2t, g/2) and
+        // (2t+1, g/2) as the half g mod 2 of their (row 2t', 2t'+1) pairs.
+        const uint32_t pk0 = pack_f16x2(pp[0] * vk[0], pp[1] * vk[0]);
+        const uint32_t pk1 = pack_f16x2(pp[2] * vk[1], pp[3] * vk[1]);
+        const int src0 = ((2 * t) << 2) | (g >> 1), src1 = ((2 * t + 1) << 2) | (g >> 1);
+        const uint32_t u0 = __shfl_sync(0xffffffffu, pk0, src0), u1 = __shfl_sync(0xffffffffu, pk0, src1);
+        const uint32_t v0 = __shfl_sync(0xffffffffu, pk1, src0), v1 = __shfl_sync(0xffffffffu, pk1, src1);
+        const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+        pa[0] = __byte_perm(u0, u1, sel);
+        pa[1] = 0u;
+        pa[2] = __byte_perm(v0, v1, sel);
+        pa[3] = 0u;
+      } else {
       // S = Q K^T for 16 keys: two n-tiles of 8 keys.
       float s[2][4];
 #pragma unroll
@@ -694,7 +788,8 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float a0 = ex2(m0 - mu0), a1 = ex2(m1 - mu1);   // 0 when the old max is -inf
+      a0 = ex2(m0 - mu0);   // 0 when the old max is -inf
+      a1 = ex2(m1 - mu1);
       m0 = mn0;
       m1 = mn1;
       float ps[2][4];
@@ -710,32 +805,6 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
       }
       l0 = l0 * a0 + sum0;   // per-thread partial sums; reduced across the quad at the end
       l1 = l1 * a1 + sum1;
-      // O is rescaled only when a row maximum moved somewhere in the warp
-      // (after the first stages it rarely does); the factors are exactly 1
-      // otherwise, so skipping changes nothing.
-      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
-        if constexpr (OT) {
-          // rows 2t and 2t+1: their factors from lanes 8t and 8t + 4 (g = row)
-          const int t = lane & 3;
-          const float at0 = __shfl_sync(0xffffffffu, a0, 8 * t), at1 = __shfl_sync(0xffffffffu, a0, 8 * t + 4);
-#pragma unroll
-          for (int n = 0; n < NO; ++n) {
-            o[n][0] *= at0;
-            o[n][1] *= at1;
-            o[n][2] *= at0;
-            o[n][3] *= at1;
-          }
-        } else {
-#pragma unroll
-          for (int n = 0; n < NO; ++n) {
-            o[n][0] *= a0;
-            o[n][1] *= a0;
-            o[n][2] *= a1;
-            o[n][3] *= a1;
-          }
-        }
-      }
-      uint32_t pa[4];
       if constexpr (KV) {
         // P times the keys' v scales (f16; the row sums above use P itself)
         pa[0] = pack_f16x2(ps[0][0] * vsc[0][0], ps[0][1] * vsc[0][1]);
@@ -747,6 +816,44 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
         pa[1] = pack_bf16x2(ps[0][2], ps[0][3]);
         pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
         pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
+      }
+      }
+      // O is rescaled only when a row maximum moved somewhere in the warp
+      // (after the first stages it rarely does); the factors are exactly 1
+      // otherwise, so skipping changes nothing.
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+        if constexpr (OT) {
+          // rows 2t and 2t+1: the thread's own (QT), or from lanes 8t and
+          // 8t + 4 (g = row)
+          const int t = lane & 3;
+          const float at0 = QT ? a0 : __shfl_sync(0xffffffffu, a0, 8 * t);
+          const float at1 = QT ? a1 : __shfl_sync(0xffffffffu, a0, 8 * t + 4);
+#pragma unroll
+          for (int n = 0; n < NO; ++n) {
+            o[n][0] *= at0;
+            o[n][1] *= at1;
+            o[n][2] *= at0;
+            o[n][3] *= at1;
+          }
+        } else if constexpr (QT) {
+          // O rows g (and g+8, all zero): row g's factor from lane g/2 (t = g/2)
+          const int g = lane >> 2;
+          const float x0 = __shfl_sync(0xffffffffu, a0, g >> 1), x1 = __shfl_sync(0xffffffffu, a1, g >> 1);
+          const float ag = (g & 1) ? x1 : x0;
+#pragma unroll
+          for (int n = 0; n < NO; ++n) {
+            o[n][0] *= ag;
+            o[n][1] *= ag;
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NO; ++n) {
+            o[n][0] *= a0;
+            o[n][1] *= a0;
+            o[n][2] *= a1;
+            o[n][3] *= a1;
+          }
+        }
       }
       if constexpr (DIRECT) {
         // O += P V with the bytes in registers.  Lane (g, t) reads the 16
@@ -838,11 +945,12 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
       if (KV == 0 && lane == 0) mbar_arrive(smem_u32(empty + slot_i));
     }
 
-    // Reduce l over the quad (the 4 lanes sharing a row).
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    // Reduce l over the lanes sharing a row: the quad, or (QT) the 8 lanes of a t.
+#pragma unroll
+    for (int o_ = QT ? 4 : 1; o_ < (QT ? 32 : 4); o_ <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+    }
 
     // Merge the four warps' (m, l, O) through shared memory (stage buffers are
     // free once every warp has passed its last stage).
@@ -861,16 +969,18 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
     } else if (ok) {
 #pragma unroll
       for (int n = 0; n < NO; ++n) {
-        // DIRECT: n-tile n, column 2t + e is dim 16 (2t + e) + n
+        // O rows g and g+8; DIRECT: n-tile n, column 2t + e is dim 16 (2t + e) + n
+        const int og = lane >> 2;
         const int c = DIRECT ? 32 * (lane & 3) + n : n * 8 + (lane & 3) * 2;
         const int c1 = DIRECT ? c + 16 : c + 1;
-        red_o[(warp * kDecRows + r0) * D + c] = o[n][0];
-        red_o[(warp * kDecRows + r0) * D + c1] = o[n][1];
-        red_o[(warp * kDecRows + r1) * D + c] = o[n][2];
-        red_o[(warp * kDecRows + r1) * D + c1] = o[n][3];
+        red_o[(warp * kDecRows + og) * D + c] = o[n][0];
+        red_o[(warp * kDecRows + og) * D + c1] = o[n][1];
+        red_o[(warp * kDecRows + og + 8) * D + c] = o[n][2];
+        red_o[(warp * kDecRows + og + 8) * D + c1] = o[n][3];
       }
     }
-    if (ok && (lane & 3) == 0) {
+    // m and l of rows r0, r1: one lane per row pair (QT: the lanes with g = 0)
+    if (ok && (QT ? (lane >> 2) == 0 : (lane & 3) == 0)) {
       red_ml[(warp * kDecRows + r0) * 2] = m0;
       red_ml[(warp * kDecRows + r0) * 2 + 1] = l0;
       red_ml[(warp * kDecRows + r1) * 2] = m1;
