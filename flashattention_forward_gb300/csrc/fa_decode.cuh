@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(kDecThreads, (dec_direct<D, KV, V5>() && R8) ?
         for (int e = 0; e < 2; ++e) {
           const int j = key_base + n * 8 + (lane & 3) * 2 + e;
           const bool in = j < key_hi;
-          bool ok0 = in && r0 < rows && blk0, ok1 = !OT && in && r1 < rows && blk1;
+          bool ok0 = in && r0 < rows && blk0, ok1 = in && r1 < rows && blk1;
           if (p.causal) { ok0 = ok0 && j <= ip0; ok1 = ok1 && j <= ip1; }
           if (p.window > 0) {
             if (p.causal) { ok0 = ok0 && ip0 - j < p.window; ok1 = ok1 && ip1 - j < p.window; }
