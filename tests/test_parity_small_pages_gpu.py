@@ -69,6 +69,8 @@ DECODE = {
     "bf16_d128": dict(hq=8, hkv=2, dk=128),
     "bf16_d64_rows2": dict(hq=8, hkv=2, dk=64, sq=2),
     "e4m3_d128": dict(hq=8, hkv=2, dk=128, kv_dtype="e4m3"),
+    "e4m3_d128_rows8": dict(hq=8, hkv=2, dk=128, kv_dtype="e4m3", sq=2),
+    "int8_d128_rows16": dict(hq=8, hkv=2, dk=128, kv_dtype="int8", sq=4),
     "int8_d64": dict(hq=4, hkv=4, dk=64, kv_dtype="int8"),
 }
 
