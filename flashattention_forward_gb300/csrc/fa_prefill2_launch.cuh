@@ -13,14 +13,14 @@ namespace fa {
 template <int D, bool PAGED, int MOD, int NT = 2>
 bool prefill2_bigreg_fits() {
   using Big = Prefill2Cfg<D, D, PAGED, MOD, true, NT>;
-  static int verdict = -1;   // per process: all devices run the same binary
-  if (verdict < 0) {
+  static int fits = -1;   // per process: all devices run the same binary
+  if (fits < 0) {
     cudaFuncAttributes a;
     const bool ok = cudaFuncGetAttributes(&a, fa_prefill2_kernel<D, D, PAGED, MOD, true, NT>) == cudaSuccess &&
                     a.numRegs >= Big::kMinLaunchRegs && a.numRegs * Big::kThreads >= Big::kPoolNeeded;
-    verdict = ok ? 1 : 0;
+    fits = ok ? 1 : 0;
   }
-  return verdict == 1;
+  return fits == 1;
 }
 
 template <int D, bool PAGED, int MOD, bool BIG, int NT = 2>

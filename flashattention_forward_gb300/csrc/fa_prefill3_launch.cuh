@@ -15,15 +15,15 @@ template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, b
 bool prefill3_split_fits() {
   using Cfg = Prefill3Cfg<DK, DV, PAGED, FP8, MOD, BIGREG, Q8, PV8>;
   if constexpr (!Cfg::kSplitRegs) return true;
-  static int verdict = -1;   // per process: all devices run the same binary
-  if (verdict < 0) {
+  static int fits = -1;   // per process: all devices run the same binary
+  if (fits < 0) {
     cudaFuncAttributes a;
-    verdict = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5, PV8>) == cudaSuccess &&
+    fits = (cudaFuncGetAttributes(&a, fa_prefill3_kernel<DK, DV, PAGED, FP8, MOD, BIGREG, I8, Q8, V5, PV8>) == cudaSuccess &&
                a.numRegs * Cfg::kThreads >= Cfg::kPoolNeeded)
                   ? 1
                   : 0;
   }
-  return verdict == 1;
+  return fits == 1;
 }
 
 template <int DK, int DV, bool PAGED, bool FP8, int MOD, bool BIGREG, bool I8, bool Q8, bool V5 = false,
